@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""KDA benchmark on GB300: prefill tokens/s (headline), decode tokens/s, roofline fractions.
+
+One step of the headline is one chunked prefill of the workload B=4, T=8192, H=32,
+d_k=d_v=128 (bf16 q/k/v/g/beta, fp32 state, zero initial state) through the C ABI. The
+decode sub-benchmark runs 1000 consecutive decode steps for 256 sequences x 32 heads x
+d=128 from fp32 states ~ N(0, 0.02), with 1000 pre-generated input sets resident on the
+device. Inputs are synthetic and seeded (kda_inputs), drawn on the device.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With N > 1 the script runs under torchrun, one rank per GPU; every rank processes its own
+copy of the workload (weak scaling: (sequence, head) pairs are independent, so ranks need
+no collective on the data path) and rank 0 prints the line with the max time over ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the
+same workload (there is no other reference implementation of the method).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "KDA prefill tokens/s and decode tokens/s on 1 GB300; % of roofline"
+PF = dict(B=4, T=8192, H=32, d=128, chunk=64)
+DEC = dict(N=256, H=32, d=128, steps=1000)
+NAMES = ("q", "k", "v", "g", "beta")
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--decode-steps", type=int, default=DEC["steps"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return args
+
+
+# ------------------------------------------------------------------------ ranks ---------
+
+class Ranks:
+    def __init__(self, gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        if self.world != gpus:
+            raise SystemExit(f"--gpus {gpus} but WORLD_SIZE={self.world}")
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            self.dist = dist
+        torch.cuda.set_device(self.local)
+        self.device = torch.device("cuda", self.local)
+
+    def barrier(self):
+        if self.dist:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.dist:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist:
+            self.dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------- clocks ----------
+
+class ClockSampler:
+    """nvidia-smi samples (100 ms) of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.ident = None
+        try:
+            u = str(torch.cuda.get_device_properties(device).uuid)
+            self.ident = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            self.ident = str(device.index)
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.ident, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[2], parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i, f in enumerate(r[3]) if f.lower() == "active"})
+        top = max(r[0] for r in rows)
+        loaded = [r[0] for r in rows if r[0] >= 0.5 * top] or [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# -------------------------------------------------------------------- roofline ----------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(key, files):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source it was
+    taken on is the current one; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(key)
+    if not rec or rec.get("source_sha") != source_digest(files):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+PREFILL_SOURCES = ["gated_delta_rule_56_gb300/csrc/kda_prefill_tc.cu", "gated_delta_rule_56_gb300/csrc/kda_tc.cuh"]
+DECODE_SOURCES = ["gated_delta_rule_56_gb300/csrc/kda_recurrent.cu"]
+
+
+def prefill_bytes(B, T, H, d):
+    """Algorithmic HBM bytes of one prefill launch: read q, k, v, g (bf16) and beta, write o
+    (bf16) -- 1282 B per token-head at d=128 -- plus the fp32 final state per (seq, head)."""
+    per_token_head = 4 * d * 2 + 2 + 2 * d
+    return B * T * H * per_token_head + B * H * d * d * 4
+
+
+def decode_bytes(N, H, d):
+    """Algorithmic HBM bytes of one decode step: fp32 state read + write per head, bf16
+    q, k, g, v and beta read, bf16 o written."""
+    return N * H * (2 * d * d * 4 + 4 * d * 2 + 2 + 2 * d)
+
+
+def existing_files(files):
+    return [f for f in files if os.path.exists(os.path.join(ROOT, f))]
+
+
+# ----------------------------------------------------------------- timing helpers -------
+
+def time_steps(fn, steps, warmup, ranks):
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        fn(i)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    total_ms = ev[0].elapsed_time(ev[steps])
+    return total_ms, per
+
+
+# --------------------------------------------------------------------- our arm ----------
+
+def run_ours(args):
+    import gated_delta_rule_56_gb300 as kda
+    import kda_inputs as ki
+    from gated_delta_rule_56_gb300.build import build
+
+    ranks = Ranks(args.gpus)
+    if ranks.local == 0:
+        build()
+    ranks.barrier()
+    kda.load()
+    dev = ranks.device
+    B, T, H, d = PF["B"], PF["T"], PF["H"], PF["d"]
+    x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=ranks.rank)
+    o = torch.empty(B, T, H, d, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty(B, H, d, d, dtype=torch.float32, device=dev)
+    args_in = [x[n] for n in NAMES]
+
+    def step(_i):
+        kda.prefill(*args_in, o=o, final_state=fin)
+
+    step(0)
+    kda.check_status()
+    peak_bw, peak_tc, peak_kind = measured_peaks()
+    with ClockSampler(dev) as clk:
+        total_ms, per = time_steps(step, args.steps, args.warmup, ranks)
+    kda.check_status()
+    total_ms = ranks.max(total_ms)
+    ms = total_ms / args.steps
+    tokens = B * T
+    value = args.gpus * tokens * args.steps / (total_ms / 1e3)
+    kernel_ms = statistics.mean(per)
+    alg = prefill_bytes(B, T, H, d)
+    achieved = alg / (kernel_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"KDA chunked prefill B={B} T={T} H={H} dk=dv={d} bf16 in, fp32 state, zero init",
+                   "global_batch": B * args.gpus, "seq_len": T, "heads": H, "head_dim": d, "chunk": PF["chunk"],
+                   "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single",
+                   "l2": f"no flush: each step reads {alg / 1e9:.2f} GB > {L2_BYTES / 2**20:.0f} MiB L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s",
+                     "frac": achieved / peak_bw, "peak_source": peak_kind,
+                     "traffic": recorded_traffic("prefill", existing_files(PREFILL_SOURCES)),
+                     "alg_bytes_per_launch": alg, "kernel_ms": kernel_ms,
+                     "tensor_flop_per_launch": B * T * H * 2 * (1.5 * 64 * d + 64 * d + 3 * d * d),
+                     "tensor_frac_of_peak": B * T * H * 2 * (1.5 * 64 * d + 64 * d + 3 * d * d)
+                     / (kernel_ms / 1e3) / (peak_tc * 1e12)},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(args, kda, x, ranks, tokens)
+    if not args.no_decode:
+        del x, args_in, o, fin
+        torch.cuda.empty_cache()
+        line["decode"] = run_decode(args, kda, ki, ranks, peak_bw, peak_kind)
+    if ranks.rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(ki, dev)
+    ranks.close()
+    if ranks.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, kda, x, ranks, tokens):
+    """Same metric through the public call with host buffers: every step copies that
+    step's inputs from pinned host memory and reads o and the final state back."""
+    dev = ranks.device
+    host = {n: x[n].cpu().pin_memory() for n in NAMES}
+    dev_in = {n: torch.empty_like(x[n]) for n in NAMES}
+    B, T, H, d = PF["B"], PF["T"], PF["H"], PF["d"]
+    o = torch.empty(B, T, H, d, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty(B, H, d, d, dtype=torch.float32, device=dev)
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    fin_h = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+
+    def step(_i):
+        for n in NAMES:
+            dev_in[n].copy_(host[n], non_blocking=True)
+        kda.prefill(*(dev_in[n] for n in NAMES), o=o, final_state=fin)
+        o_h.copy_(o, non_blocking=True)
+        fin_h.copy_(fin, non_blocking=True)
+
+    steps = max(3, min(args.e2e_steps, args.steps))
+    total_ms, _ = time_steps(step, steps, 3, ranks)
+    kda.check_status()
+    total_ms = ranks.max(total_ms)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in NAMES)
+    d2h = o_h.numel() * o_h.element_size() + fin_h.numel() * fin_h.element_size()
+    return {"value": args.gpus * tokens * steps / (total_ms / 1e3), "unit": "tokens/s", "steps": steps,
+            "ms_per_step": total_ms / steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "gpu_launches": steps}
+
+
+def run_decode(args, kda, ki, ranks, peak_bw, peak_kind):
+    dev = ranks.device
+    N, H, d = DEC["N"], DEC["H"], DEC["d"]
+    steps = args.decode_steps
+    x = ki.decode_inputs(steps, N, H, d, d, device=dev, seed=100 + ranks.rank)
+    state = x["state"]
+    o = torch.empty(N, H, d, dtype=torch.bfloat16, device=dev)
+
+    def step(i):
+        j = i % steps
+        kda.decode_step(x["q"][j], x["k"][j], x["v"][j], x["g"][j], x["beta"][j], state, o=o)
+
+    total_ms, per = time_steps(step, steps, 10, ranks)
+    kda.check_status()
+    total_ms = ranks.max(total_ms)
+    ms = total_ms / steps
+    alg = decode_bytes(N, H, d)
+    kernel_ms = statistics.mean(per)
+    achieved = alg / (kernel_ms / 1e3) / 1e9
+    return {"metric": "KDA decode tokens/s (one token for each of N=256 sequences per step, H=32, "
+                      "dk=dv=128, bf16 in, fp32 state)",
+            "value": args.gpus * N * steps / (total_ms / 1e3), "unit": "tokens/s", "steps": steps,
+            "ms_per_step": ms, "gpu_launches": steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s",
+                         "frac": achieved / peak_bw, "peak_source": peak_kind,
+                         "traffic": recorded_traffic("decode", existing_files(DECODE_SOURCES)),
+                         "alg_bytes_per_launch": alg, "kernel_ms": kernel_ms}}
+
+
+# ----------------------------------------------------------------- CPU baseline ---------
+
+def _oracle_pairs(ki, dev, pairs, tokens):
+    """Inputs of `pairs` (batch row, head) problems of `tokens` tokens from the workload's
+    seeded inputs, on the host."""
+    B, T, H, d = PF["B"], PF["T"], PF["H"], PF["d"]
+    x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)
+    sel = [(i % B, (i * 7) % H) for i in range(pairs)]
+    out = []
+    for b, h in sel:
+        out.append({n: x[n][b:b + 1, :tokens, h:h + 1].cpu() for n in NAMES})
+    del x
+    return out
+
+
+def cpu_baseline(ki, dev, pairs=None, tokens=None):
+    import oracle
+    cores = oracle.max_threads()
+    pairs = pairs or max(cores, 32)
+    tokens = tokens or PF["T"]
+    probs = _oracle_pairs(ki, dev, pairs, tokens)
+    # One call over all sampled pairs so OpenMP spreads them over the cores.
+    cat = {n: torch.cat([p[n] for p in probs], dim=2) for n in NAMES}
+    t0 = time.perf_counter()
+    oracle.recurrent(*(cat[n] for n in NAMES), n_threads=cores)
+    dt = time.perf_counter() - t0
+    token_heads = pairs * tokens
+    return {"value": token_heads / PF["H"] / dt, "unit": "tokens/s", "cores": min(cores, pairs),
+            "kind": "oracle",
+            "sample": f"fp64 recurrence over {pairs} (batch row, head) pairs x {tokens} tokens of the "
+                      f"B=4 T=8192 H=32 d=128 workload ({token_heads} token-heads, {dt:.2f} s wall); "
+                      f"tokens/s = token-heads/s / 32 heads"}
+
+
+# ------------------------------------------------------------------ reference arm -------
+
+def run_reference(args):
+    """The fp64 oracle as the reference arm, on host cores, rank 0 only."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import kda_inputs as ki
+    import oracle
+    cores = oracle.max_threads()
+    pairs, tokens = cores, 256
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))) if torch.cuda.is_available() else "cpu"
+    probs = _oracle_pairs(ki, dev, pairs, tokens)
+    cat = {n: torch.cat([p[n] for p in probs], dim=2) for n in NAMES}
+    for _ in range(args.warmup):
+        oracle.recurrent(*(cat[n] for n in NAMES), n_threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.recurrent(*(cat[n] for n in NAMES), n_threads=cores)
+    dt = time.perf_counter() - t0
+    value = pairs * tokens / PF["H"] * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"KDA chunked prefill B={PF['B']} T={PF['T']} H={PF['H']} dk=dv={PF['d']} "
+                                   "bf16 in, fp32 state, zero init"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step: fp64 recurrence over {pairs} (batch row, head) pairs x "
+                                       f"{tokens} tokens of the workload"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+"""ctypes binding of libkda.so: argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels. This module checks the
+torch tensors it is handed (device, dtype, shape, contiguity), allocates the outputs the
+caller did not pass, and forwards raw device pointers and the current CUDA stream to the
+C ABI declared in include/kda.h. There is no fallback: without the built library the
+functions raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from .build import LIB_PATH, INCLUDE
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(5)
+KDA_BF16, KDA_F32 = 0, 1
+_DTYPES = {torch.bfloat16: KDA_BF16, torch.float32: KDA_F32}
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_string(status)}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def declared_symbols() -> list[str]:
+    """Names of the functions include/kda.h declares."""
+    text = open(os.path.join(INCLUDE, "kda.h")).read()
+    return re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", text)
+
+
+def load():
+    """Load libkda.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it first with "
+                               "gated_delta_rule_56_gb300.build.build() (nvcc, sm_103a)")
+        lib = ctypes.CDLL(LIB_PATH)
+        lib.kda_prefill.argtypes = [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp,
+                                    _vp, _vp, ctypes.c_size_t, _vp]
+        lib.kda_prefill.restype = _i
+        lib.kda_prefill_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+        lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+        lib.kda_decode_step.argtypes = [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        lib.kda_decode_step.restype = _i
+        lib.kda_check_status.argtypes = [_vp]
+        lib.kda_check_status.restype = _i
+        lib.kda_status_string.argtypes = [_i]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_last_error.argtypes = []
+        lib.kda_last_error.restype = ctypes.c_char_p
+        lib.kda_version.argtypes = []
+        lib.kda_version.restype = _i
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def last_error() -> str:
+    return load().kda_last_error().decode()
+
+
+def version() -> int:
+    return int(load().kda_version())
+
+
+def _raise_if(status: int):
+    if status != KDA_OK:
+        raise KDAError(status, last_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(name, t, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def prefill(q, k, v, g, beta, cu_seqlens=None, initial_state=None, output_final_state=True,
+            o=None, final_state=None):
+    """Chunked KDA prefill on the GPU.
+
+    q, k, g [B, T, H, dk]; v [B, T, H, dv]; beta [B, T, H]; all bf16 or all fp32, on one CUDA
+    device. With ``cu_seqlens`` (int32 [N+1] on the device) B must be 1 and the rows are
+    packed sequences. ``initial_state``: fp32 [N, H, dk, dv] or None (zeros).
+    Returns (o [B, T, H, dv], final_state [N, H, dk, dv] fp32 or None).
+    """
+    lib = load()
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t, shp in (("q", q, (B, T, H, dk)), ("k", k, (B, T, H, dk)), ("g", g, (B, T, H, dk)),
+                         ("v", v, (B, T, H, dv)), ("beta", beta, (B, T, H))):
+        _check(name, t, q.dtype, shp, dev)
+    if cu_seqlens is not None:
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+            raise ValueError("cu_seqlens must be a 1-D int32 tensor [N+1]")
+        _check("cu_seqlens", cu_seqlens, torch.int32, (cu_seqlens.numel(),), dev)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if initial_state is not None:
+        _check("initial_state", initial_state, torch.float32, (N, H, dk, dv), dev)
+    if o is None:
+        o = torch.empty(B, T, H, dv, dtype=q.dtype, device=dev)
+    else:
+        _check("o", o, q.dtype, (B, T, H, dv), dev)
+    if final_state is None and output_final_state:
+        final_state = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+    elif final_state is not None:
+        _check("final_state", final_state, torch.float32, (N, H, dk, dv), dev)
+    dt = _DTYPES[q.dtype]
+    ws_bytes = int(lib.kda_prefill_workspace_size(dt, B, T, H, dk, dv, N))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    with torch.cuda.device(dev):
+        st = lib.kda_prefill(dt, B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                             _ptr(cu_seqlens), N, _ptr(initial_state), _ptr(o), _ptr(final_state),
+                             _ptr(ws), ws_bytes, _stream(dev))
+    _raise_if(st)
+    return o, final_state
+
+
+def decode_step(q, k, v, g, beta, state, o=None):
+    """One KDA decode token for N sequences; ``state`` (fp32 [N, H, dk, dv]) is updated in
+    place. q, k, g [N, H, dk]; v [N, H, dv]; beta [N, H]. Returns o [N, H, dv]."""
+    lib = load()
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("g", g, (N, H, dk)),
+                         ("v", v, (N, H, dv)), ("beta", beta, (N, H))):
+        _check(name, t, q.dtype, shp, dev)
+    _check("state", state, torch.float32, (N, H, dk, dv), dev)
+    if o is None:
+        o = torch.empty(N, H, dv, dtype=q.dtype, device=dev)
+    else:
+        _check("o", o, q.dtype, (N, H, dv), dev)
+    with torch.cuda.device(dev):
+        st = lib.kda_decode_step(_DTYPES[q.dtype], N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                 _ptr(beta), _ptr(state), _ptr(o), _stream(dev))
+    _raise_if(st)
+    return o
+
+
+def check_status(device=None):
+    """Synchronise the current stream and raise KDAError if a kernel flagged an error."""
+    lib = load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _raise_if(lib.kda_check_status(_stream(dev)))

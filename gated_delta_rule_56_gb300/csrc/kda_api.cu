@@ -1,0 +1,199 @@
+// kda_api.cu -- the C ABI of libkda.so: host-side validation and kernel dispatch.
+//
+// Entry points and their contracts are declared in include/kda.h. Every check that can be
+// made on the host is made here before anything is queued; the kernels only see arguments
+// that passed. Conditions only the device can see are OR-ed into a per-device error word.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+__device__ unsigned g_error_word;  // one per device: bits kErrBadSeqlens | kErrTimeout
+
+thread_local char g_last_error[512];
+
+kda_status fail(kda_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+kda_status ok() {
+    g_last_error[0] = '\0';
+    return KDA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_head(int dk, int dv) { return dk == dv && (dk == 32 || dk == 64 || dk == 128); }
+
+kda_status check_head(int dk, int dv) {
+    if (dk <= 0 || dv <= 0) return fail(KDA_ERR_INVALID_ARG, "dk=%d dv=%d must be positive", dk, dv);
+    if (!supported_head(dk, dv))
+        return fail(KDA_ERR_UNSUPPORTED, "head sizes dk=%d dv=%d: supported dk == dv in {32, 64, 128}",
+                    dk, dv);
+    return KDA_OK;
+}
+
+kda_status check_dtype(kda_dtype dt) {
+    if (dt != KDA_BF16 && dt != KDA_F32) return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+    return KDA_OK;
+}
+
+kda_status check_ptr(const void *p, const char *name, bool need_align) {
+    if (!p) return fail(KDA_ERR_INVALID_ARG, "%s is NULL", name);
+    if (need_align && !aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+    return KDA_OK;
+}
+
+kda_status launched(cudaError_t e, const char *what) {
+    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+}  // namespace
+
+unsigned *device_error_word() {
+    static std::mutex mu;
+    static unsigned *words[256] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!words[dev]) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_error_word) != cudaSuccess) return nullptr;
+        words[dev] = static_cast<unsigned *>(addr);
+    }
+    return words[dev];
+}
+
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+int kda_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char *kda_status_string(kda_status status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+const char *kda_last_error(void) { return g_last_error; }
+
+size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv, int n_seqs) {
+    (void)dtype; (void)B; (void)T; (void)H; (void)dk; (void)dv; (void)n_seqs;
+    return 0;
+}
+
+kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,
+                       const void *k, const void *v, const void *g, const void *beta,
+                       const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,
+                       float *final_state, void *workspace, size_t workspace_bytes,
+                       kda_stream_t stream) {
+    kda_status st;
+    if ((st = check_dtype(dtype)) != KDA_OK) return st;
+    if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "negative size B=%d T=%d H=%d", B, T, H);
+    if ((st = check_head(dk, dv)) != KDA_OK) return st;
+    if (cu_seqlens) {
+        if (B != 1) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens requires B == 1 (got B=%d)", B);
+        if (n_seqs < 0) return fail(KDA_ERR_INVALID_ARG, "n_seqs=%d is negative", n_seqs);
+        if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is not 4-byte aligned");
+    } else {
+        n_seqs = B;
+    }
+    (void)workspace;
+    (void)workspace_bytes;
+    const long long rows = (long long)B * T;
+    if ((long long)n_seqs * H > 0x7fffffffLL) return fail(KDA_ERR_INVALID_ARG, "too many (sequence, head) pairs");
+    if (rows * H * (long long)(dk > dv ? dk : dv) > (1LL << 46))
+        return fail(KDA_ERR_INVALID_ARG, "tensor too large");
+    if (rows > 0) {
+        if ((st = check_ptr(q, "q", true)) || (st = check_ptr(k, "k", true)) ||
+            (st = check_ptr(v, "v", true)) || (st = check_ptr(g, "g", true)) ||
+            (st = check_ptr(o, "o", true)) || (st = check_ptr(beta, "beta", false)))
+            return st;
+        if ((reinterpret_cast<uintptr_t>(beta) & (dtype == KDA_BF16 ? 1u : 3u)) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "beta is not aligned to its element size");
+    }
+    if (initial_state && !aligned16(initial_state))
+        return fail(KDA_ERR_INVALID_ARG, "initial_state is not 16-byte aligned");
+    if (final_state && !aligned16(final_state))
+        return fail(KDA_ERR_INVALID_ARG, "final_state is not 16-byte aligned");
+    if ((long long)n_seqs * H == 0) return ok();
+
+    RunParams p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    p.cu_seqlens = cu_seqlens;
+    p.init = initial_state;
+    p.fin = final_state;
+    p.o = o;
+    p.T = T;
+    p.H = H;
+    p.n_seqs = n_seqs;
+    p.err = device_error_word();
+    if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word: %s",
+                            cudaGetErrorString(cudaGetLastError()));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (tc_prefill_supported(dtype, dk, dv, p)) return launched(launch_tc_prefill(p, s), "tensor-core prefill");
+    return launched(launch_recurrent(dtype, dk, dv, p, s), "recurrent prefill");
+}
+
+kda_status kda_decode_step(kda_dtype dtype, int N, int H, int dk, int dv, const void *q, const void *k,
+                           const void *v, const void *g, const void *beta, float *state, void *o,
+                           kda_stream_t stream) {
+    kda_status st;
+    if ((st = check_dtype(dtype)) != KDA_OK) return st;
+    if (N < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "negative size N=%d H=%d", N, H);
+    if ((st = check_head(dk, dv)) != KDA_OK) return st;
+    if ((long long)N * H == 0) return ok();
+    if ((long long)N * H > 0x7fffffffLL) return fail(KDA_ERR_INVALID_ARG, "too many (sequence, head) pairs");
+    if ((st = check_ptr(q, "q", true)) || (st = check_ptr(k, "k", true)) || (st = check_ptr(v, "v", true)) ||
+        (st = check_ptr(g, "g", true)) || (st = check_ptr(o, "o", true)) ||
+        (st = check_ptr(state, "state", true)) || (st = check_ptr(beta, "beta", false)))
+        return st;
+    if ((reinterpret_cast<uintptr_t>(beta) & (dtype == KDA_BF16 ? 1u : 3u)) != 0)
+        return fail(KDA_ERR_INVALID_ARG, "beta is not aligned to its element size");
+
+    RunParams p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    p.cu_seqlens = nullptr;
+    p.init = state;
+    p.fin = state;
+    p.o = o;
+    p.T = 1;
+    p.H = H;
+    p.n_seqs = N;
+    p.err = device_error_word();
+    if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word");
+    return launched(launch_recurrent(dtype, dk, dv, p, reinterpret_cast<cudaStream_t>(stream)), "decode step");
+}
+
+kda_status kda_check_status(kda_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+    unsigned word = 0, zero = 0;
+    e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word));
+    if (e == cudaSuccess && word) e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "error word: %s", cudaGetErrorString(e));
+    if (word & kErrTimeout) return fail(KDA_ERR_TIMEOUT, "a device-side wait gave up (error word 0x%x)", word);
+    if (word & kErrBadSeqlens)
+        return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is not a non-decreasing list ending at T (error word 0x%x)", word);
+    return ok();
+}
+
+}  // extern "C"

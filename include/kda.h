@@ -1,0 +1,127 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention library, libkda.so.
+ *
+ * The operation. Kimi Delta Attention (KDA) is linear attention with a fixed-size state per
+ * (sequence, head): "Inside Kimi K3's Architecture" (maidul-haque blog), section "Kimi Delta
+ * Attention: the linear core" -- the delta rule subtracts the value a key currently reads
+ * before writing the fresh one, and the forget gate decays each channel separately; "Kimi K3
+ * Explained" (researchpapers.dev), "Architecture at a glance" and FAQ "What is Kimi Delta
+ * Attention?" -- channel-wise forget gate with a log-decay bounded below through a scaled
+ * sigmoid, computed chunkwise on dense tensor-core tiles. Per (sequence, head), with the
+ * state S (d_k x d_v, fp32) and natural-log decay g_t (one value per key channel):
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t                                      (no scale is applied to q)
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers are device pointers to caller-owned memory. The library never allocates,
+ *    frees or keeps a pointer after the call returns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *    Argument errors are found on the host and returned before anything is launched.
+ *    A launch failure returns KDA_ERR_CUDA. Conditions only the device can see (a
+ *    cu_seqlens array that is not monotonic, a pipeline wait that ran out) are recorded in a
+ *    per-device error word that kda_check_status() returns.
+ *  - Layouts are row-major and dense: q, k, g [B, T, H, d_k]; v, o [B, T, H, d_v];
+ *    beta [B, T, H]; states [N, H, d_k, d_v] (fp32, row index = key channel).
+ *  - Accuracy is stated for g in [-5, 0] (the scaled-sigmoid bound with constant 5): inputs
+ *    outside it are computed, but the bf16 tensor-core path may lose accuracy there.
+ *  - Not thread-safe per device error word only: concurrent calls are fine, but
+ *    kda_check_status() reports (and clears) errors of every call on that device.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kda_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, bad cu_seqlens */
+    KDA_ERR_UNSUPPORTED = 2, /* well-formed request this build has no kernel for */
+    KDA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    KDA_ERR_TIMEOUT = 4      /* a device-side pipeline wait gave up (kda_check_status) */
+} kda_status;
+
+typedef enum {
+    KDA_BF16 = 0, /* q, k, v, g, beta and o are bfloat16 */
+    KDA_F32 = 1   /* q, k, v, g, beta and o are float32 */
+} kda_dtype;
+
+/*
+ * kda_prefill -- run the recurrence over whole sequences (chunked prefill).
+ *
+ * dtype        element type of q, k, v, g, beta and o.
+ * B, T, H      batch, tokens per batch row, heads. With cu_seqlens == NULL the call covers
+ *              B sequences of T tokens each. With cu_seqlens != NULL, B must be 1 and T is
+ *              the total packed token count.
+ * dk, dv       key and value head sizes. Supported: dk == dv in {32, 64, 128}.
+ * q, k, g      [B, T, H, dk]; v [B, T, H, dv]; beta [B, T, H]. g is log(alpha) <= 0.
+ * cu_seqlens   NULL, or int32 [n_seqs + 1] on the device: sequence n covers packed rows
+ *              cu_seqlens[n] .. cu_seqlens[n+1]-1; must start at 0, be non-decreasing and
+ *              end at T (checked on the device; a violation skips the bad sequence and sets
+ *              KDA_ERR_INVALID_ARG in the error word). Chunks restart at every sequence start.
+ * n_seqs       number of sequences when cu_seqlens != NULL (ignored otherwise; N = B).
+ * initial_state  fp32 [N, H, dk, dv] or NULL (zero state).
+ * o            output [B, T, H, dv], same dtype as the inputs. Every row is written.
+ * final_state  fp32 [N, H, dk, dv] or NULL (not written). May alias initial_state.
+ * workspace, workspace_bytes  device scratch of at least kda_prefill_workspace_size() bytes
+ *              (NULL / 0 when that size is 0).
+ * Alignment: all pointers 16-byte aligned. Rows of q, k, v, g, o are contiguous.
+ * Returns KDA_OK once the work is queued on `stream`.
+ */
+KDA_API kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int dv,
+                       const void *q, const void *k, const void *v, const void *g,
+                       const void *beta, const int32_t *cu_seqlens, int n_seqs,
+                       const float *initial_state, void *o, float *final_state,
+                       void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/* Bytes of device workspace kda_prefill needs for these sizes (0 when none). */
+KDA_API size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv,
+                                  int n_seqs);
+
+/*
+ * kda_decode_step -- one token of the recurrence for N independent sequences.
+ *
+ * q, k, g  [N, H, dk]; v [N, H, dv]; beta [N, H]; o [N, H, dv]; all `dtype`.
+ * state    fp32 [N, H, dk, dv], read and updated in place (S_{t-1} -> S_t).
+ * o        receives o_t = S_t^T q_t.
+ * Supported: dk == dv in {32, 64, 128}; pointers 16-byte aligned.
+ */
+KDA_API kda_status kda_decode_step(kda_dtype dtype, int N, int H, int dk, int dv,
+                           const void *q, const void *k, const void *v, const void *g,
+                           const void *beta, float *state, void *o, kda_stream_t stream);
+
+/*
+ * kda_check_status -- synchronise `stream`, then read and clear the device error word of the
+ * current device. Returns KDA_OK, KDA_ERR_INVALID_ARG (bad cu_seqlens seen by a kernel),
+ * KDA_ERR_TIMEOUT (a bounded pipeline wait gave up; that (sequence, head) is left
+ * unfinished) or KDA_ERR_CUDA (the synchronisation itself failed).
+ */
+KDA_API kda_status kda_check_status(kda_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+KDA_API const char *kda_status_string(kda_status status);
+
+/* Detail of the most recent failure in the calling host thread ("" if none). */
+KDA_API const char *kda_last_error(void);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+KDA_API int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,105 @@
+"""The C ABI without a GPU: the library builds, loads, exports what include/kda.h declares,
+and rejects malformed arguments on the host before touching the device."""
+
+import ctypes
+import subprocess
+
+import pytest
+
+import gated_delta_rule_56_gb300 as kda
+from gated_delta_rule_56_gb300 import _lib
+from gated_delta_rule_56_gb300.build import build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return kda.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = kda.declared_symbols()
+    assert {"kda_prefill", "kda_decode_step", "kda_check_status", "kda_status_string",
+            "kda_prefill_workspace_size", "kda_last_error", "kda_version"} <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", kda.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for n in names:
+        assert n in exported, f"{n} declared in include/kda.h but not exported"
+        assert getattr(lib, n) is not None
+
+
+def test_status_strings_and_version(lib):
+    assert kda.status_string(0) == "KDA_OK"
+    assert kda.status_string(1) == "KDA_ERR_INVALID_ARG"
+    assert kda.status_string(2) == "KDA_ERR_UNSUPPORTED"
+    assert kda.status_string(3) == "KDA_ERR_CUDA"
+    assert kda.status_string(4) == "KDA_ERR_TIMEOUT"
+    assert kda.status_string(99) == "KDA_ERR_UNKNOWN"
+    assert kda.version() >= 10000
+
+
+def test_workspace_size_is_zero(lib):
+    assert lib.kda_prefill_workspace_size(0, 4, 8192, 32, 128, 128, 4) == 0
+
+
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: validation fails first
+
+
+def _prefill(lib, dtype=0, B=1, T=64, H=2, dk=128, dv=128, ptrs=None, cu=None, n=0, init=None,
+             fin=None):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, o=FAKE)
+    p.update(ptrs or {})
+    return lib.kda_prefill(dtype, B, T, H, dk, dv, p["q"], p["k"], p["v"], p["g"], p["beta"], cu, n,
+                           init, p["o"], fin, None, 0, None)
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(dtype=7), _lib.KDA_ERR_INVALID_ARG),
+    (dict(B=-1), _lib.KDA_ERR_INVALID_ARG),
+    (dict(dk=0), _lib.KDA_ERR_INVALID_ARG),
+    (dict(dk=48, dv=48), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(dk=128, dv=64), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(ptrs=dict(q=None)), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ptrs=dict(o=None)), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ptrs=dict(k=FAKE + 8)), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ptrs=dict(beta=FAKE + 1)), _lib.KDA_ERR_INVALID_ARG),
+    (dict(B=2, cu=FAKE, n=2), _lib.KDA_ERR_INVALID_ARG),
+    (dict(cu=FAKE + 2, n=1), _lib.KDA_ERR_INVALID_ARG),
+    (dict(cu=FAKE, n=-1), _lib.KDA_ERR_INVALID_ARG),
+    (dict(init=FAKE + 4), _lib.KDA_ERR_INVALID_ARG),
+    (dict(fin=FAKE + 4), _lib.KDA_ERR_INVALID_ARG),
+])
+def test_prefill_rejects_bad_arguments_on_host(lib, case, expect):
+    st = _prefill(lib, **case)
+    assert st == expect, (case, kda.status_string(st), kda.last_error())
+    assert kda.last_error() != ""
+
+
+def test_empty_prefill_is_a_no_op(lib):
+    # No (sequence, head) pair: nothing is queued and no device is needed.
+    assert _prefill(lib, B=0, ptrs=dict(q=None, k=None, v=None, g=None, beta=None, o=None)) == 0
+    assert _prefill(lib, H=0, T=0, ptrs=dict(q=None, k=None, v=None, g=None, beta=None, o=None)) == 0
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(dtype=5), _lib.KDA_ERR_INVALID_ARG),
+    (dict(N=-3), _lib.KDA_ERR_INVALID_ARG),
+    (dict(dk=96, dv=96), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(state=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(state=FAKE + 4), _lib.KDA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 2), _lib.KDA_ERR_INVALID_ARG),
+])
+def test_decode_rejects_bad_arguments_on_host(lib, case, expect):
+    a = dict(dtype=0, N=4, H=2, dk=64, dv=64, q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state=FAKE, o=FAKE)
+    a.update(case)
+    st = lib.kda_decode_step(a["dtype"], a["N"], a["H"], a["dk"], a["dv"], a["q"], a["k"], a["v"], a["g"],
+                             a["beta"], a["state"], a["o"], None)
+    assert st == expect, (case, kda.status_string(st), kda.last_error())
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 4, 1, 32, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kda.prefill(x, x, x, x, torch.zeros(1, 4, 1, dtype=torch.bfloat16))
