@@ -1,5 +1,8 @@
 """Helpers shared by the GPU parity tests: tolerances and comparison against the oracle."""
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -26,8 +29,18 @@ def errors(got, ref):
     return max_abs, rel
 
 
+def _log(name, ma, rf):
+    """Append the measured errors to $KDA_PARITY_LOG (JSON lines) when it is set."""
+    path = os.environ.get("KDA_PARITY_LOG")
+    if path:
+        test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+        with open(path, "a") as f:
+            f.write(json.dumps({"test": test, "tensor": name, "max_abs": ma, "rel_frob": rf}) + "\n")
+
+
 def assert_close(got, ref, name, max_abs=MAX_ABS, rel_frob=REL_FROB):
     ma, rf = errors(got, ref)
+    _log(name, ma, rf)
     assert ma <= max_abs and rf <= rel_frob, f"{name}: max-abs {ma:.3e} (<= {max_abs}), rel-Frob {rf:.3e} (<= {rel_frob})"
     return ma, rf
 

@@ -106,19 +106,20 @@ def test_final_state_aliases_initial_state():
     assert_close(st, rs, "final_state")
 
 
-def test_split_prefill_equals_unsplit_on_gpu():
-    """Prefill-cache property on the GPU: 300 tokens in one call, or 100 then 200 with the
-    final state handed over, give the same outputs and state."""
+def test_split_prefill_matches_oracle_on_gpu():
+    """Prefill-cache property on the GPU: 300 tokens run as 100 then 200 with the final
+    state handed over meets the parity bar against the oracle of the unsplit run (chunk
+    boundaries move, so the two GPU runs round differently)."""
     x = ki.prefill_inputs(2, 300, 2, 128, 128, device=DEV, seed=6, state_std=0.02)
-    o, s = run(x)
+    ro, rs = ref(x)
     a = {n: x[n][:, :100].contiguous() for n in NAMES}
     b = {n: x[n][:, 100:].contiguous() for n in NAMES}
     a["initial_state"] = x["initial_state"]
     oa, sa = run(a)
     b["initial_state"] = sa
     ob, sb = run(b)
-    assert_close(torch.cat([oa, ob], 1), o.double(), "o (split vs unsplit)", max_abs=1e-2, rel_frob=2e-3)
-    assert_close(sb, s.double(), "state (split vs unsplit)", max_abs=1e-2, rel_frob=2e-3)
+    assert_close(torch.cat([oa, ob], 1), ro, "o (split run)")
+    assert_close(sb, rs, "final_state (split run)")
 
 
 def test_bad_cu_seqlens_is_reported():
