@@ -23,7 +23,8 @@
 //
 // Layout of the work: one CTA of 256 threads per (sequence, head); chunks run in order.
 //   TMA: q, k, g tiles (64 rows x 128 channels, 128-byte swizzle) for the next chunk are in
-//        flight while the current one computes; v and beta use plain coalesced loads.
+//        flight while the current one computes; the v tile is fetched once the intra-chunk
+//        tiles have retired (into their operand region); beta uses plain loads.
 //   TMEM (512 columns): [0,64) diagonal A|P tile, [64,96) off-diagonal tile,
 //        [128,256) (K+ S | Q+ S -> O), [256,320) U, [320,448) the fp32 state S^T (lanes = d_v).
 //   MMAs (kind::f16, bf16 operands, fp32 accumulate, M = 128):
@@ -71,6 +72,7 @@ constexpr uint32_t SM_P = SM_X + 64 * SA * 4;             //   then P bf16 opera
 constexpr uint32_t SM_OFF = SM_AP + 49152;                // off tile operands (32 KB), see below
 constexpr uint32_t SM_Y = SM_OFF;                         //   then solve scratch fp32 [32 x 68]
 constexpr uint32_t SM_OST = SM_OFF;                       //   then O staging bf16 [64 x 128]
+constexpr uint32_t SM_VT = SM_OFF + 16384;                //   then the v tile (TMA, like q/k/g)
 constexpr uint32_t SM_MISC = SM_OFF + 32768;
 constexpr uint32_t SM_REF = SM_MISC;                      // fp32 [4][128]: Gam_15, Gam_31, Gam_47, Gam_63
 constexpr uint32_t SM_CST = SM_REF + 2048;                // fp32 [9][128] per-channel factors
@@ -92,7 +94,7 @@ enum { CST_M0 = 0, CST_M1, CST_C0, CST_C1, CST_EM0, CST_EG31, CST_E63M1, CST_E63
 constexpr uint32_t TM_AP = 0, TM_OFF = 64, TM_D1 = 128, TM_U = 256, TM_S = 320, TM_COLS = 512;
 
 // Barriers.
-enum { BAR_TMA = 0, BAR_AP, BAR_M1, BAR_M2, BAR_M34, BAR_N };
+enum { BAR_TMA = 0, BAR_AP, BAR_M1, BAR_M2, BAR_M34, BAR_V, BAR_N };
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -185,7 +187,7 @@ __device__ __forceinline__ void issue_mma(uint32_t d_tmem, uint32_t a_smem, uint
 }
 
 struct Maps {
-    CUtensorMap q, k, g;
+    CUtensorMap q, k, g, v;
 };
 
 __global__ void __launch_bounds__(NT, 1)
@@ -232,6 +234,7 @@ __global__ void __launch_bounds__(NT, 1)
         prefetch_tensormap(&maps.q);
         prefetch_tensormap(&maps.k);
         prefetch_tensormap(&maps.g);
+        prefetch_tensormap(&maps.v);
     }
     tc_fence_before();
     __syncthreads();
@@ -242,7 +245,6 @@ __global__ void __launch_bounds__(NT, 1)
     // Epilogue mapping: TMEM lane ev (= d_v index), column half eh.
     const int ev = tid & 127, eh = tid >> 7;
     const size_t state_off = ((size_t)n * H + h) * (size_t)D * D;
-    const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(p.v);
     const __nv_bfloat16 *bg = static_cast<const __nv_bfloat16 *>(p.beta);
     __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o);
 
@@ -287,14 +289,6 @@ __global__ void __launch_bounds__(NT, 1)
         const long long row0 = bos + (long long)c * C;
         const int len = (int)min((long long)C, eos - row0);
 
-        // v (rows 32*eh .. +31 of column ev) and beta: issued now, first used much later.
-        uint16_t vr[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int r = 32 * eh + i;
-            vr[i] = r < len ? __ldg(reinterpret_cast<const unsigned short *>(vg) + ((size_t)(row0 + r) * H + h) * D + ev)
-                            : (uint16_t)0;
-        }
         float bet = 0.f;
         if (tid < C && tid < len) bet = __bfloat162float(bg[(size_t)(row0 + tid) * H + h]);
 
@@ -475,6 +469,13 @@ __global__ void __launch_bounds__(NT, 1)
         if (!(ok = wait_all(&bars[BAR_AP], par))) break;
         pending &= ~(1u << BAR_AP);
         tc_fence_after();
+        // The off-tile operands are consumed: the v tile of this chunk can land in their region.
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bars[BAR_V], 16384);
+            tma_load_3d(sm + SM_VT, &maps.v, &bars[BAR_V], 0, h, (int)row0);
+            tma_load_3d(sm + SM_VT + 8192, &maps.v, &bars[BAR_V], 64, h, (int)row0);
+        }
+        pending |= 1u << BAR_V;
         {
             const int L = 32 * (warp & 3) + lane;
             const int i = L & 63;
@@ -584,13 +585,21 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_after();
 
         // ---- 6. R = V - K+ S  (thread: d_v lane ev, rows 32*eh..+31) ------------------------
+        if (!(ok = wait_all(&bars[BAR_V], par))) break;
+        pending &= ~(1u << BAR_V);
         {
             float ks[32];
             tmem_ld32(tmem + tq + TM_D1 + 32 * eh, ks);
             tmem_ld_wait();
+            const uint32_t vcol = (uint32_t)((ev >> 6) * 8192 + ((ev & 7) << 1));
+            const int vchunk = (ev & 63) >> 3;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                ks[i] = (32 * eh + i < len) ? __uint_as_float((uint32_t)vr[i] << 16) - ks[i] : 0.f;
+            for (int i = 0; i < 32; ++i) {
+                const int r = 32 * eh + i;
+                const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                    sm + SM_VT + vcol + r * 128 + ((vchunk ^ (r & 7)) << 4)));
+                ks[i] = (r < len) ? vv - ks[i] : 0.f;
+            }
             st_row32(sm + SM_RT, ev, 32 * eh, C, ks);
         }
         fence_async_smem();
@@ -749,7 +758,7 @@ cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
     const long long rows = p.cu_seqlens ? (long long)p.T : (long long)p.n_seqs * p.T;
     Maps maps;
     if (!encode_map(&maps.q, p.q, rows, p.H) || !encode_map(&maps.k, p.k, rows, p.H) ||
-        !encode_map(&maps.g, p.g, rows, p.H))
+        !encode_map(&maps.g, p.g, rows, p.H) || !encode_map(&maps.v, p.v, rows, p.H))
         return cudaErrorInvalidValue;
     kda_prefill_tc_kernel<<<(unsigned)(p.n_seqs * p.H), NT, SMEM_BYTES, s>>>(maps, p);
     return cudaGetLastError();
