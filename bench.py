@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", choices=("prefill", "decode"),
+                    help="run two launches of the small profiling case (for ncu) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -420,8 +422,32 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def ncu_case(kind):
+    """Small cases sized for an ncu capture: inputs larger than L2, a few hundred MB on the
+    device. prefill: B=4 T=2048 H=32 d=128 (128 CTAs); decode: N=64 H=32 d=128 (2048 CTAs)."""
+    import gated_delta_rule_56_gb300 as kda
+    import kda_inputs as ki
+    from gated_delta_rule_56_gb300.build import build
+    build()
+    dev = torch.device("cuda", 0)
+    if kind == "prefill":
+        x = ki.prefill_inputs(4, 2048, 32, 128, 128, device=dev, seed=0)
+        for _ in range(2):
+            o, _s = kda.prefill(*(x[n] for n in NAMES))
+    else:
+        x = ki.decode_inputs(2, 64, 32, 128, 128, device=dev, seed=0)
+        st = x["state"].clone()
+        for t in range(2):
+            o = kda.decode_step(*(x[n][t] for n in NAMES), st)
+    kda.check_status()
+    print(json.dumps({"ncu_case": kind, "checksum": float(o.float().abs().mean())}))
+
+
 def main():
     args = parse()
+    if args.ncu_case:
+        ncu_case(args.ncu_case)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
