@@ -25,15 +25,16 @@
 //   TMA: q, k, g tiles (64 rows x 128 channels, 128-byte swizzle) for the next chunk are in
 //        flight while the current one computes; the v tile is fetched once the intra-chunk
 //        tiles have retired (into their operand region); beta uses plain loads.
-//   TMEM (512 columns): [0,64) diagonal A|P tile, [64,96) off-diagonal tile,
-//        [128,256) (K+ S | Q+ S -> O), [256,320) U, [320,448) the fp32 state S^T (lanes = d_v).
-//   MMAs (kind::f16, bf16 operands, fp32 accumulate, M = 128):
+//   TMEM (512 columns): [0,64) diagonal A|P tile, [64,96) off-diagonal tile, [96,128) the
+//        bf16 A operand -(K+ S)^T then U^T, [128,256) (K+ S | Q+ S -> O), [256,320) U,
+//        [320,448) the fp32 state S^T (lanes = d_v), [448,512) its bf16 copy (MMA1's A).
+//   MMAs (kind::f16, bf16 operands, fp32 accumulate, M = 128; "tmem" = A read from TMEM):
 //        diag  [K*f ; Q*f] x [K/f]^T              N = 64, K = 128
 //        off   [K*e ; Q*e] x [K*e']^T             N = 32, K = 128
-//        MMA1  S^T x [K+ ; Q+]^T                  N = 128, K = 128   -> (K+ S)^T, (Q+ S)^T
-//        MMA2  (V - K+ S)^T x T^T                 N = 64,  K = 64    -> U^T
-//        MMA3  U^T x P^T  (onto (Q+ S)^T)         N = 64,  K = 64    -> O^T
-//        MMA4  U^T x Khat^T  (onto the state)     N = 128, K = 64    -> S^T
+//        MMA1  S^T (tmem) x [K+ ; Q+]^T           N = 128, K = 128   -> (K+ S)^T, (Q+ S)^T
+//        MMA2  V^T x T^T  (V tile, MN-major)      N = 64,  K = 64    -> then += -(K+ S)^T (tmem) x T^T = U^T
+//        MMA3  U^T (tmem) x P^T  (onto (Q+ S)^T)  N = 64,  K = 64    -> O^T
+//        MMA4  U^T (tmem) x Khat  (MN-major B)    N = 128, K = 64    -> S^T
 //   The 64 x 64 triangular inverse: 16 x 16 diagonal blocks by forward substitution on CUDA
 //   cores, then the 16->32 and 32->64 block merges as tf32 warp-level MMAs.
 // Every mbarrier wait is bounded; on time-out the CTA records kErrTimeout, drains what it
@@ -58,12 +59,10 @@ constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
 
 // Shared memory map (bytes from a 1024-byte aligned base).
 constexpr uint32_t SM_Q = 0, SM_K = 16384, SM_G = 32768;  // TMA tiles, 2 boxes x (64 rows x 128 B)
-constexpr uint32_t SM_S = 49152;                          // S^T bf16 operand   [128 x 128]
-constexpr uint32_t SM_KH = SM_S + 32768;                  // Khat^T operand     [128 x 64]
+constexpr uint32_t SM_KH = 49152;                         // Khat [64 rows x 128 ch], same swizzled layout
 constexpr uint32_t SM_KQ = SM_KH + 16384;                 // [K+ ; Q+] operand  [128 x 128]
-constexpr uint32_t SM_T = SM_KQ;                          //   then T           [64 x 64]
-constexpr uint32_t SM_RT = SM_KQ + 8192;                  //   then R^T / U^T   [128 x 64]
-constexpr uint32_t SM_AP = SM_KQ + 32768;                 // [K*f ; Q*f]        [128 x 128]
+constexpr uint32_t SM_T = SM_KQ + 32768;                  // T operand          [64 x 64]
+constexpr uint32_t SM_AP = SM_T + 8192;                   // [K*f ; Q*f]        [128 x 128]
 constexpr uint32_t SM_APB = SM_AP + 32768;                // K/f                [64 x 128]
 constexpr uint32_t SA = 68;                               // row stride (floats) of A and X
 constexpr uint32_t SM_AS = SM_AP;                         //   then A  fp32 [64 x 68]
@@ -82,6 +81,7 @@ constexpr uint32_t SM_TPTR = SM_BAR + 64;                 // TMEM base address
 constexpr uint32_t SM_USED = SM_TPTR + 16;
 constexpr uint32_t SMEM_BYTES = SM_USED + 1024;           // + alignment slack
 static_assert(SM_P + 8192 <= SM_OFF, "solve buffers overflow their region");
+static_assert(SM_KH % 1024 == 0 && SM_VT % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 // The off-diagonal tile's A operand spans the whole 32 KB region as 128 rows: rows 32..63
 // (K side) and 96..127 (Q side) hold data; its B operand (32 rows) sits in rows 0..31, and
@@ -91,7 +91,8 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 enum { CST_M0 = 0, CST_M1, CST_C0, CST_C1, CST_EM0, CST_EG31, CST_E63M1, CST_E63G31, CST_GC, CST_N };
 
 // TMEM column offsets.
-constexpr uint32_t TM_AP = 0, TM_OFF = 64, TM_D1 = 128, TM_U = 256, TM_S = 320, TM_COLS = 512;
+constexpr uint32_t TM_AP = 0, TM_OFF = 64, TM_RA = 96, TM_D1 = 128, TM_U = 256, TM_S = 320, TM_SA = 448;
+constexpr uint32_t TM_COLS = 512;
 
 // Barriers.
 enum { BAR_TMA = 0, BAR_AP, BAR_M1, BAR_M2, BAR_M34, BAR_V, BAR_N };
@@ -133,6 +134,12 @@ __device__ __forceinline__ void st_row32(uint8_t *base, int row, int k0, int K, 
     }
 }
 
+// 32 floats -> 16 bf16 pairs (element 2i in the low half), optionally negated.
+__device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&w)[16], float sign) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16(sign * v[2 * i], sign * v[2 * i + 1]);
+}
+
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -166,6 +173,17 @@ __device__ __forceinline__ void warp_store_16x8(float *Out, int os, const float 
     const int g = lane >> 2, t = lane & 3;
     *reinterpret_cast<float2 *>(Out + g * os + 2 * t) = make_float2(scale * acc[0], scale * acc[1]);
     *reinterpret_cast<float2 *>(Out + (g + 8) * os + 2 * t) = make_float2(scale * acc[2], scale * acc[3]);
+}
+
+// T entries of a 16 x 8 accumulator holding -X (rows r0.., columns c0..): T = X Diag(beta),
+// written as bf16 pairs into the K-major T operand (64 x 64).
+__device__ __forceinline__ void store_t_16x8(uint8_t *Tbase, int r0, int c0, const float (&acc)[4], const float *beta,
+                                             int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const int cc = c0 + 2 * t;
+    const float b0 = -beta[cc], b1 = -beta[cc + 1];
+    *reinterpret_cast<uint32_t *>(Tbase + kmajor_offset(r0 + g, cc, 64)) = pack_bf16(acc[0] * b0, acc[1] * b1);
+    *reinterpret_cast<uint32_t *>(Tbase + kmajor_offset(r0 + g + 8, cc, 64)) = pack_bf16(acc[2] * b0, acc[3] * b1);
 }
 
 // All threads wait on `bar`; true only if every thread saw the phase complete.
@@ -257,7 +275,9 @@ __global__ void __launch_bounds__(NT, 1)
         for (int i = 0; i < 32; ++i)
             buf[i] = p.init ? __ldcs(p.init + state_off + (size_t)(k0 + i) * D + ev) : 0.f;
         tmem_st32(tmem + tq + TM_S + k0, buf);
-        st_row32(sm + SM_S, ev, k0, D, buf);
+        uint32_t w[16];
+        pack32(buf, w, 1.f);
+        tmem_st16(tmem + tq + TM_SA + k0 / 2, w);
     }
     tmem_st_wait();
 
@@ -282,31 +302,29 @@ __global__ void __launch_bounds__(NT, 1)
     const int rlo = lane & 7;
     const int j = 4 * (warp & 3) + (lane >> 3);
     const int mh = warp >> 2;
-    int c = 0;
-#pragma unroll 1
-    for (; c < nchunks; ++c) {
-        const uint32_t par = (uint32_t)(c & 1);
-        const long long row0 = bos + (long long)c * C;
-        const int len = (int)min((long long)C, eos - row0);
-
+    float gm[4][8];  // Gam of the operand mapping's 4 rows x 8 channels (current chunk)
+    // Step 1 of chunk cc: wait for its q/k/g tiles, Gam = cumsum of g into gm, the reference
+    // rows and per-channel factors into shared memory, beta into sbeta. Runs for chunk c + 1
+    // while the last MMAs of chunk c are in flight. False if the TMA wait ran out.
+    auto step1 = [&](int cc) -> bool {
+        const long long r0 = bos + (long long)cc * C;
+        const int ln = (int)min((long long)C, eos - r0);
         float bet = 0.f;
-        if (tid < C && tid < len) bet = __bfloat162float(bg[(size_t)(row0 + tid) * H + h]);
-
-        if (!(ok = wait_all(&bars[BAR_TMA], par))) break;
+        if (tid < C && tid < ln) bet = __bfloat162float(bg[(size_t)(r0 + tid) * H + h]);
+        if (!wait_all(&bars[BAR_TMA], (uint32_t)(cc & 1))) return false;
         pending &= ~(1u << BAR_TMA);
 
         // ---- 1. Gam = cumsum_r g within the chunk, per key channel --------------------------
         // A warp holds 32 consecutive rows of 32 channels: scan over the 8 lanes of a row
         // group with shuffles, then over the 4 row groups in registers; the second row half
         // then adds Gam_31.
-        float gm[4][8];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             const int r = rlo + 8 * (4 * mh + m);
             const uint4 w = *reinterpret_cast<const uint4 *>(sm + SM_G + tile_chunk(r, j));
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) gm[m][i] = r < len ? ((i & 1) ? bf_hi(ww[i >> 1]) : bf_lo(ww[i >> 1])) : 0.f;
+            for (int i = 0; i < 8; ++i) gm[m][i] = r < ln ? ((i & 1) ? bf_hi(ww[i >> 1]) : bf_lo(ww[i >> 1])) : 0.f;
         }
 #pragma unroll
         for (int d = 1; d < 8; d <<= 1) {
@@ -366,6 +384,17 @@ __global__ void __launch_bounds__(NT, 1)
         }
         __syncthreads();
 
+        return true;
+    };
+
+    int c = 0;
+    if (nchunks > 0) ok = step1(0);
+#pragma unroll 1
+    for (; ok && c < nchunks; ++c) {
+        const uint32_t par = (uint32_t)(c & 1);
+        const long long row0 = bos + (long long)c * C;
+        const int len = (int)min((long long)C, eos - row0);
+
         // ---- 2. decay-scaled operands -----------------------------------------------------
         {
             // Per-channel factors of this row half (see the exponent-range note at the top):
@@ -380,7 +409,6 @@ __global__ void __launch_bounds__(NT, 1)
                 pe[i] = cst[(mh ? CST_EG31 : CST_EM0) * 128 + ch];
                 khe[i] = cst[(mh ? CST_E63M1 : CST_E63G31) * 128 + ch];
             }
-            uint32_t khp[4][4];  // Khat as bf16 pairs: [m][channel pair]
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int r = rlo + 8 * (4 * mh + m);
@@ -423,18 +451,7 @@ __global__ void __launch_bounds__(NT, 1)
                 if (mh) st_chunk(sm, SM_OFF + kmajor_offset(64 + r, 8 * j, D), ofr_q);
                 st_chunk(sm, SM_KQ + kmajor_offset(r, 8 * j, D), kp);
                 st_chunk(sm, SM_KQ + kmajor_offset(64 + r, 8 * j, D), qp);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) khp[m][i] = pack_bf16(kh[2 * i], kh[2 * i + 1]);
-            }
-            // Khat^T [128 channels x 64 rows]: element (8j+i, r) -- scalar bf16 stores.
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int r = rlo + 8 * (4 * mh + m);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint16_t hv = (uint16_t)((i & 1) ? (khp[m][i >> 1] >> 16) : (khp[m][i >> 1] & 0xffffu));
-                    *reinterpret_cast<uint16_t *>(sm + SM_KH + kmajor_offset(8 * j + i, r, C)) = hv;
-                }
+                st_chunk(sm, SM_KH + tile_chunk(r, j), kh);  // row-major: MMA4 reads it MN-major
             }
         }
         fence_async_smem();
@@ -442,12 +459,37 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         tc_fence_after();
 
-        // ---- 3. issue the intra-chunk tiles, MMA1 and the next chunk's TMA -----------------
+        // ---- 3. intra-chunk tiles; the state decay runs in their shadow ------------------------
         if (tid == 0) {
             issue_mma(tmem + TM_AP, sb + SM_AP, sb + SM_APB, D, D / 16, idesc_bf16(128, 64), false);
             issue_mma(tmem + TM_OFF, sb + SM_OFF, sb + SM_OFF, D, D / 16, idesc_bf16(128, 32), false);
             mma_commit(&bars[BAR_AP]);
-            issue_mma(tmem + TM_D1, sb + SM_S, sb + SM_KQ, D, D / 16, idesc_bf16(128, 128), false);
+        }
+        pending |= 1u << BAR_AP;
+        // S <- S Diag(gam_last): the state in TMEM is next read by MMA4 of this chunk.
+#pragma unroll 1
+        for (int cb = 0; cb < 2; ++cb) {
+            const int k0 = 64 * eh + 32 * cb;
+            float sv[32];
+            tmem_ld32(tmem + tq + TM_S + k0, sv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sv[i] *= cst[CST_GC * 128 + k0 + i];
+            tmem_st32(tmem + tq + TM_S + k0, sv);
+        }
+        tmem_st_wait();
+
+        // ---- 4. A (fp32, for the solve) and P (bf16 operand) out of TMEM -------------------
+        if (!(ok = wait_all(&bars[BAR_AP], par))) break;
+        pending &= ~(1u << BAR_AP);
+        tc_fence_after();
+        // MMA1 and the next chunk's tiles are issued from warp 4, whose share of the epilogue
+        // below is zero-filling (its rows sit above the diagonal), so the issue wait is hidden.
+        if (tid == 128) {
+#pragma unroll 1
+            for (int st = 0; st < D / 16; ++st)
+                mma_bf16_tmem_a(tmem + TM_D1, tmem + TM_SA + 8 * st, sdesc(sb + SM_KQ + 256u * st, 128u, 2048u),
+                                idesc_bf16(128, 128), st > 0);
             mma_commit(&bars[BAR_M1]);
             if (c + 1 < nchunks) {
                 const int nr = (int)(row0 + C);
@@ -459,16 +501,11 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
         }
-        pending |= (1u << BAR_AP) | (1u << BAR_M1);
+        pending |= 1u << BAR_M1;
         if (c + 1 < nchunks) {
             pending |= 1u << BAR_TMA;
             tma_par = (uint32_t)((c + 1) & 1);
         }
-
-        // ---- 4. A (fp32, for the solve) and P (bf16 operand) out of TMEM -------------------
-        if (!(ok = wait_all(&bars[BAR_AP], par))) break;
-        pending &= ~(1u << BAR_AP);
-        tc_fence_after();
         // The off-tile operands are consumed: the v tile of this chunk can land in their region.
         if (tid == 0) {
             mbar_arrive_expect_tx(&bars[BAR_V], 16384);
@@ -520,17 +557,34 @@ __global__ void __launch_bounds__(NT, 1)
             float x[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                float acc = 0.f;
+                float a0 = 0.f, a1 = 0.f;  // two chains halve the dependent-FMA latency
 #pragma unroll
-                for (int m = 0; m < i; ++m) acc = fmaf(As[(16 * b + i) * SA + 16 * b + m], x[m], acc);
-                x[i] = (i == col) ? 1.f : (i < col ? 0.f : -acc);
+                for (int m = 0; m < i; ++m) {
+                    if (m & 1) a1 = fmaf(As[(16 * b + i) * SA + 16 * b + m], x[m], a1);
+                    else a0 = fmaf(As[(16 * b + i) * SA + 16 * b + m], x[m], a0);
+                }
+                x[i] = (i == col) ? 1.f : (i < col ? 0.f : -(a0 + a1));
             }
+            const float bcol = sbeta[16 * b + col];
+            __nv_bfloat16 *Tb = reinterpret_cast<__nv_bfloat16 *>(sm + SM_T);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) Xs[(16 * b + i) * SA + 16 * b + col] = x[i];
-        } else if (tid < 192) {
-            const int z = tid - 64;  // 0..127: rows 0..15 cols 16..31, then rows 32..47 cols 48..63
-            const int blk = z >> 6, rr = (z & 63) >> 2, cq = (z & 3) * 4;
-            *reinterpret_cast<float4 *>(Xs + (32 * blk + rr) * SA + 32 * blk + 16 + cq) = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < 16; ++i) {
+                Xs[(16 * b + i) * SA + 16 * b + col] = x[i];
+                Tb[kmajor_offset(16 * b + i, 16 * b + col, C) / 2] = __float2bfloat16_rn(x[i] * bcol);
+            }
+        } else {
+            const int z = tid - 64;  // 0..191
+            if (z < 128) {  // X rows 0..15 cols 16..31, rows 32..47 cols 48..63 (read by the merges)
+                const int blk = z >> 6, rr = (z & 63) >> 2, cq = (z & 3) * 4;
+                *reinterpret_cast<float4 *>(Xs + (32 * blk + rr) * SA + 32 * blk + 16 + cq) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            // T: the six strictly-upper 16 x 16 blocks, 16 rows x 2 chunks each
+            const int bi = z >> 5, rr = (z & 31) >> 1, hf = z & 1;
+            const int I = bi < 3 ? 0 : (bi < 5 ? 1 : 2);
+            const int J = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
+            *reinterpret_cast<uint4 *>(sm + SM_T + kmajor_offset(16 * I + rr, 16 * J + 8 * hf, C)) =
+                make_uint4(0u, 0u, 0u, 0u);
         }
         __syncthreads();
         // (b) 16 -> 32: X_{2p+1,2p} = -X_{2p+1,2p+1} A_{2p+1,2p} X_{2p,2p} (warp p, tf32 mma)
@@ -548,6 +602,7 @@ __global__ void __launch_bounds__(NT, 1)
             for (int nt = 0; nt < 2; ++nt) {
                 warp_mma_16x8<16>(acc, Xs + 16 * I * SA + 16 * I, SA, Yp + 8 * nt, SA, lane);
                 warp_store_16x8(Xs + 16 * I * SA + 16 * J + 8 * nt, SA, acc, -1.f, lane);
+                store_t_16x8(sm + SM_T, 16 * I, 16 * J + 8 * nt, acc, sbeta, lane);
             }
         }
         __syncthreads();
@@ -560,70 +615,42 @@ __global__ void __launch_bounds__(NT, 1)
             warp_store_16x8(Y + 16 * mt * SA + 8 * nt, SA, acc, 1.f, lane);
             __syncthreads();
             warp_mma_16x8<32>(acc, Xs + (32 + 16 * mt) * SA + 32, SA, Y + 8 * nt, SA, lane);
-            warp_store_16x8(Xs + (32 + 16 * mt) * SA + 8 * nt, SA, acc, -1.f, lane);
+            store_t_16x8(sm + SM_T, 32 + 16 * mt, 8 * nt, acc, sbeta, lane);
         }
         __syncthreads();
 
-        // T = X Diag(beta) (lower triangle) as the bf16 operand; its region held [K+; Q+].
+        // ---- 6. U = T V - T (K+ S): -(K+ S)^T goes to TMEM as MMA2's second A operand ----------
         if (!(ok = wait_all(&bars[BAR_M1], par))) break;
         pending &= ~(1u << BAR_M1);
-        {
-            const int i = 8 * warp + (tid & 7);
-            const int jq = (tid >> 3) & 3;
-            float tv[8];
-#pragma unroll
-            for (int hlf = 0; hlf < 2; ++hlf) {
-                const int j0 = 16 * jq + 8 * hlf;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int jj = j0 + q;
-                    tv[q] = (jj <= i) ? Xs[i * SA + jj] * sbeta[jj] : 0.f;
-                }
-                st_chunk(sm, SM_T + kmajor_offset(i, j0, C), tv);
-            }
-        }
         tc_fence_after();
-
-        // ---- 6. R = V - K+ S  (thread: d_v lane ev, rows 32*eh..+31) ------------------------
-        if (!(ok = wait_all(&bars[BAR_V], par))) break;
-        pending &= ~(1u << BAR_V);
         {
             float ks[32];
             tmem_ld32(tmem + tq + TM_D1 + 32 * eh, ks);
             tmem_ld_wait();
-            const uint32_t vcol = (uint32_t)((ev >> 6) * 8192 + ((ev & 7) << 1));
-            const int vchunk = (ev & 63) >> 3;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int r = 32 * eh + i;
-                const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                    sm + SM_VT + vcol + r * 128 + ((vchunk ^ (r & 7)) << 4)));
-                ks[i] = (r < len) ? vv - ks[i] : 0.f;
-            }
-            st_row32(sm + SM_RT, ev, 32 * eh, C, ks);
+            uint32_t w[16];
+            pack32(ks, w, -1.f);
+            tmem_st16(tmem + tq + TM_RA + 16 * eh, w);
+            tmem_st_wait();
         }
+        if (!(ok = wait_all(&bars[BAR_V], par))) break;  // also orders the T stores above
+        pending &= ~(1u << BAR_V);
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
         if (tid == 0) {
-            issue_mma(tmem + TM_U, sb + SM_RT, sb + SM_T, C, C / 16, idesc_bf16(128, 64), false);
+            // V^T straight from its TMA tile (MN-major A), then the -(K+ S)^T part from TMEM.
+#pragma unroll 1
+            for (int st = 0; st < C / 16; ++st)
+                mma_bf16(tmem + TM_U, sdesc_sw128(sb + SM_VT + 2048u * st, 8192u, 1024u),
+                         sdesc(sb + SM_T + 256u * st, 128u, 1024u), idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
+#pragma unroll 1
+            for (int st = 0; st < C / 16; ++st)
+                mma_bf16_tmem_a(tmem + TM_U, tmem + TM_RA + 8 * st, sdesc(sb + SM_T + 256u * st, 128u, 1024u),
+                                idesc_bf16(128, 64), 1u);
             mma_commit(&bars[BAR_M2]);
         }
         pending |= 1u << BAR_M2;
-
-        // State decay S <- S Diag(gam_last) while U is computed.
-#pragma unroll 1
-        for (int cb = 0; cb < 2; ++cb) {
-            const int k0 = 64 * eh + 32 * cb;
-            float sv[32];
-            tmem_ld32(tmem + tq + TM_S + k0, sv);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) sv[i] *= cst[CST_GC * 128 + k0 + i];
-            tmem_st32(tmem + tq + TM_S + k0, sv);
-        }
-        tmem_st_wait();
 
         if (!(ok = wait_all(&bars[BAR_M2], par))) break;
         pending &= ~(1u << BAR_M2);
@@ -632,18 +659,27 @@ __global__ void __launch_bounds__(NT, 1)
             float u[32];
             tmem_ld32(tmem + tq + TM_U + 32 * eh, u);
             tmem_ld_wait();
-            st_row32(sm + SM_RT, ev, 32 * eh, C, u);  // U^T replaces R^T (MMA2 has finished)
+            uint32_t w[16];
+            pack32(u, w, 1.f);
+            tmem_st16(tmem + tq + TM_RA + 16 * eh, w);  // U^T replaces -(K+ S)^T (MMA2 has finished)
+            tmem_st_wait();
         }
-        fence_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
         if (tid == 0) {
-            issue_mma(tmem + TM_D1 + 64, sb + SM_RT, sb + SM_P, C, C / 16, idesc_bf16(128, 64), true);
-            issue_mma(tmem + TM_S, sb + SM_RT, sb + SM_KH, C, C / 16, idesc_bf16(128, 128), true);
+#pragma unroll 1
+            for (int st = 0; st < C / 16; ++st)
+                mma_bf16_tmem_a(tmem + TM_D1 + 64, tmem + TM_RA + 8 * st, sdesc(sb + SM_P + 256u * st, 128u, 1024u),
+                                idesc_bf16(128, 64), 1u);
+#pragma unroll 1
+            for (int st = 0; st < C / 16; ++st)
+                mma_bf16_tmem_a(tmem + TM_S, tmem + TM_RA + 8 * st, sdesc_sw128(sb + SM_KH + 2048u * st, 8192u, 1024u),
+                                idesc_bf16(128, 128) | kIdescBMajorMN, 1u);
             mma_commit(&bars[BAR_M34]);
         }
         pending |= 1u << BAR_M34;
+        if (c + 1 < nchunks && !(ok = step1(c + 1))) break;
         if (!(ok = wait_all(&bars[BAR_M34], par))) break;
         pending &= ~(1u << BAR_M34);
         tc_fence_after();
@@ -663,8 +699,11 @@ __global__ void __launch_bounds__(NT, 1)
             float sv[32];
             tmem_ld32(tmem + tq + TM_S + k0, sv);
             tmem_ld_wait();
-            st_row32(sm + SM_S, ev, k0, D, sv);
+            uint32_t w[16];
+            pack32(sv, w, 1.f);
+            tmem_st16(tmem + tq + TM_SA + k0 / 2, w);
         }
+        tmem_st_wait();
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
