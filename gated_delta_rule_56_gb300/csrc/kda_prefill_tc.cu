@@ -53,7 +53,9 @@ using namespace tc;
 
 constexpr int C = 64;     // chunk length
 constexpr int D = 128;    // d_k == d_v
-constexpr int NT = 256;   // threads per CTA
+constexpr int NT = 256;   // compute threads (warps 0..7)
+constexpr int kIssuer = NT / 32;  // warp 8 issues every MMA and TMA copy
+constexpr int NTHREADS = NT + 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
 
@@ -70,14 +72,14 @@ constexpr uint32_t SM_X = SM_AP + 64 * SA * 4;            //   then X = (I+A)^{-
 constexpr uint32_t SM_P = SM_X + 64 * SA * 4;             //   then P bf16 operand [64 x 64]
 constexpr uint32_t SM_OFF = SM_AP + 49152;                // off tile operands (32 KB), see below
 constexpr uint32_t SM_Y = SM_OFF;                         //   then solve scratch fp32 [32 x 68]
-constexpr uint32_t SM_OST = SM_OFF;                       //   then O staging bf16 [64 x 128]
 constexpr uint32_t SM_VT = SM_OFF + 16384;                //   then the v tile (TMA, like q/k/g)
-constexpr uint32_t SM_MISC = SM_OFF + 32768;
+constexpr uint32_t SM_OST = SM_OFF + 32768;               // O staging bf16 [64 x 128]
+constexpr uint32_t SM_MISC = SM_OST + 16384;
 constexpr uint32_t SM_REF = SM_MISC;                      // fp32 [4][128]: Gam_15, Gam_31, Gam_47, Gam_63
 constexpr uint32_t SM_CST = SM_REF + 2048;                // fp32 [9][128] per-channel factors
 constexpr uint32_t SM_BETA = SM_CST + 4608;               // fp32 [64]
-constexpr uint32_t SM_BAR = SM_BETA + 256;                // 5 mbarriers
-constexpr uint32_t SM_TPTR = SM_BAR + 64;                 // TMEM base address
+constexpr uint32_t SM_BAR = SM_BETA + 256;                // mbarriers
+constexpr uint32_t SM_TPTR = SM_BAR + 128;                // TMEM base address
 constexpr uint32_t SM_USED = SM_TPTR + 16;
 constexpr uint32_t SMEM_BYTES = SM_USED + 1024;           // + alignment slack
 static_assert(SM_P + 8192 <= SM_OFF, "solve buffers overflow their region");
@@ -95,7 +97,8 @@ constexpr uint32_t TM_AP = 0, TM_OFF = 64, TM_RA = 96, TM_D1 = 128, TM_U = 256, 
 constexpr uint32_t TM_COLS = 512;
 
 // Barriers.
-enum { BAR_TMA = 0, BAR_AP, BAR_M1, BAR_M2, BAR_M34, BAR_V, BAR_N };
+// BAR_OPS / BAR_RREADY / BAR_UREADY: the compute threads' operands are ready (256 arrivals each).
+enum { BAR_TMA = 0, BAR_AP, BAR_M1, BAR_M2, BAR_M34, BAR_V, BAR_OPS, BAR_RREADY, BAR_UREADY, BAR_N };
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -186,10 +189,22 @@ __device__ __forceinline__ void store_t_16x8(uint8_t *Tbase, int r0, int c0, con
     *reinterpret_cast<uint32_t *>(Tbase + kmajor_offset(r0 + g + 8, cc, 64)) = pack_bf16(acc[2] * b0, acc[3] * b1);
 }
 
-// All threads wait on `bar`; true only if every thread saw the phase complete.
+// Barrier over the compute threads only (named barrier 1): the issuer warp never joins it.
+__device__ __forceinline__ void sync_compute() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
+
+// All compute threads wait on `bar`; true only if every one of them saw the phase complete.
 __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
-    const bool ok = mbar_wait(bar, parity, kWaitNs);
-    return !__syncthreads_or(!ok);
+    const uint32_t bad = mbar_wait(bar, parity, kWaitNs) ? 0u : 1u;
+    uint32_t any;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(any)
+        : "r"(bad), "n"(NT)
+        : "memory");
+    return any == 0;
 }
 
 // Issue `steps` K-steps of one MMA (both operands K-major no-swizzle in shared memory).
@@ -208,7 +223,7 @@ struct Maps {
     CUtensorMap q, k, g, v;
 };
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NTHREADS, 1)
     kda_prefill_tc_kernel(const __grid_constant__ Maps maps, const RunParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -245,7 +260,8 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_relinquish();
     }
     if (tid == 32) {
-        for (int b = 0; b < BAR_N; ++b) mbar_init(&bars[b], 1);
+        for (int b = 0; b < BAR_N; ++b)
+            mbar_init(&bars[b], (b == BAR_OPS || b == BAR_RREADY || b == BAR_UREADY) ? NT : 1);
         fence_mbar_init();
     }
     if (tid == 64) {
@@ -268,7 +284,7 @@ __global__ void __launch_bounds__(NT, 1)
 
     // Initial state -> TMEM (fp32) and the bf16 S^T operand.
 #pragma unroll 1
-    for (int cb = 0; cb < 2; ++cb) {
+    for (int cb = 0; cb < 2 && warp < kIssuer; ++cb) {
         const int k0 = 64 * eh + 32 * cb;
         float buf[32];
 #pragma unroll
@@ -294,25 +310,101 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     tc_fence_after();
 
-    bool ok = true;
-    uint32_t pending = 0;    // barriers with an operation in flight (bit b = bars[b])
-    uint32_t tma_par = 0;    // parity of the TMA phase in flight (chunk index & 1)
-    if (nchunks > 0) pending |= 1u << BAR_TMA;
-    // Operand mapping: channels 8j..8j+7, rows rlo + 8 * (4 * mh + m) for m = 0..3.
-    const int rlo = lane & 7;
-    const int j = 4 * (warp & 3) + (lane >> 3);
-    const int mh = warp >> 2;
-    float gm[4][8];  // Gam of the operand mapping's 4 rows x 8 channels (current chunk)
-    // Step 1 of chunk cc: wait for its q/k/g tiles, Gam = cumsum of g into gm, the reference
-    // rows and per-channel factors into shared memory, beta into sbeta. Runs for chunk c + 1
-    // while the last MMAs of chunk c are in flight. False if the TMA wait ran out.
-    auto step1 = [&](int cc) -> bool {
+    if (warp == kIssuer) {
+        // ---------------------------------------------------------------- issuer warp --------
+        if (lane == 0) {
+            bool iok = true;
+            uint32_t pend = nchunks > 0 ? (1u << BAR_TMA) : 0u;  // operations in flight
+            uint32_t tpar = 0;                                    // parity of the TMA phase in flight
+            int cc = 0;
+#pragma unroll 1
+            for (; cc < nchunks; ++cc) {
+                const uint32_t par = (uint32_t)(cc & 1);
+                const long long row0 = bos + (long long)cc * C;
+                if (!(iok = mbar_wait(&bars[BAR_OPS], par, kWaitNs))) break;
+                pend = 0;  // the compute side saw this chunk's tiles and every earlier MMA complete
+                tc_fence_after();
+                issue_mma(tmem + TM_AP, sb + SM_AP, sb + SM_APB, D, D / 16, idesc_bf16(128, 64), false);
+                issue_mma(tmem + TM_OFF, sb + SM_OFF, sb + SM_OFF, D, D / 16, idesc_bf16(128, 32), false);
+                mma_commit(&bars[BAR_AP]);
+#pragma unroll 1
+                for (int st = 0; st < D / 16; ++st)
+                    mma_bf16_tmem_a(tmem + TM_D1, tmem + TM_SA + 8 * st, sdesc(sb + SM_KQ + 256u * st, 128u, 2048u),
+                                    idesc_bf16(128, 128), st > 0);
+                mma_commit(&bars[BAR_M1]);
+                pend |= (1u << BAR_AP) | (1u << BAR_M1);
+                if (cc + 1 < nchunks) {  // this chunk's q/k/g tiles are consumed: fetch the next ones
+                    const int nr = (int)(row0 + C);
+                    mbar_arrive_expect_tx(&bars[BAR_TMA], 3 * 16384);
+                    for (int b = 0; b < 2; ++b) {
+                        tma_load_3d(sm + SM_Q + 8192 * b, &maps.q, &bars[BAR_TMA], 64 * b, h, nr);
+                        tma_load_3d(sm + SM_K + 8192 * b, &maps.k, &bars[BAR_TMA], 64 * b, h, nr);
+                        tma_load_3d(sm + SM_G + 8192 * b, &maps.g, &bars[BAR_TMA], 64 * b, h, nr);
+                    }
+                    pend |= 1u << BAR_TMA;
+                    tpar = (uint32_t)((cc + 1) & 1);
+                }
+                // The off-tile operands are consumed: the v tile of this chunk lands in their region.
+                if (!(iok = mbar_wait(&bars[BAR_AP], par, kWaitNs))) break;
+                pend &= ~(1u << BAR_AP);
+                mbar_arrive_expect_tx(&bars[BAR_V], 16384);
+                tma_load_3d(sm + SM_VT, &maps.v, &bars[BAR_V], 0, h, (int)row0);
+                tma_load_3d(sm + SM_VT + 8192, &maps.v, &bars[BAR_V], 64, h, (int)row0);
+                pend |= 1u << BAR_V;
+                if (!(iok = mbar_wait(&bars[BAR_V], par, kWaitNs))) break;
+                pend &= ~(1u << BAR_V);
+                if (!(iok = mbar_wait(&bars[BAR_RREADY], par, kWaitNs))) break;
+                tc_fence_after();
+                // U^T = V^T T^T (V tile as an MN-major A operand) + (-(K+ S)^T from TMEM) T^T
+#pragma unroll 1
+                for (int st = 0; st < C / 16; ++st)
+                    mma_bf16(tmem + TM_U, sdesc_sw128(sb + SM_VT + 2048u * st, 8192u, 1024u),
+                             sdesc(sb + SM_T + 256u * st, 128u, 1024u), idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
+#pragma unroll 1
+                for (int st = 0; st < C / 16; ++st)
+                    mma_bf16_tmem_a(tmem + TM_U, tmem + TM_RA + 8 * st, sdesc(sb + SM_T + 256u * st, 128u, 1024u),
+                                    idesc_bf16(128, 64), 1u);
+                mma_commit(&bars[BAR_M2]);
+                pend |= 1u << BAR_M2;
+                if (!(iok = mbar_wait(&bars[BAR_UREADY], par, kWaitNs))) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int st = 0; st < C / 16; ++st)
+                    mma_bf16_tmem_a(tmem + TM_D1 + 64, tmem + TM_RA + 8 * st, sdesc(sb + SM_P + 256u * st, 128u, 1024u),
+                                    idesc_bf16(128, 64), 1u);
+#pragma unroll 1
+                for (int st = 0; st < C / 16; ++st)
+                    mma_bf16_tmem_a(tmem + TM_S, tmem + TM_RA + 8 * st, sdesc_sw128(sb + SM_KH + 2048u * st, 8192u, 1024u),
+                                    idesc_bf16(128, 128) | kIdescBMajorMN, 1u);
+                mma_commit(&bars[BAR_M34]);
+                pend |= 1u << BAR_M34;
+            }
+            if (!iok) {
+                atomicOr(p.err, kErrTimeout);
+                // Drain what was issued (bounded), so no MMA or copy is in flight at exit.
+                const uint32_t par = (uint32_t)(cc & 1);
+                for (int b = 0; b < BAR_N; ++b)
+                    if (pend & (1u << b)) (void)mbar_wait(&bars[b], b == BAR_TMA ? tpar : par, kWaitNs);
+            }
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------------------------- compute warps --------
+        bool ok = true;
+        // Operand mapping: channels 8j..8j+7, rows rlo + 8 * (4 * mh + m) for m = 0..3.
+        const int rlo = lane & 7;
+        const int j = 4 * (warp & 3) + (lane >> 3);
+        const int mh = warp >> 2;
+        float gm[4][8];  // Gam of the operand mapping's 4 rows x 8 channels (current chunk)
+        // Step 1 of chunk cc: wait for its q/k/g tiles, Gam = cumsum of g into gm, the reference
+        // rows and per-channel factors into shared memory, beta into sbeta. Runs for chunk c + 1
+        // while the last MMAs of chunk c are in flight. False if the TMA wait ran out.
+        auto step1 = [&](int cc) -> bool {
         const long long r0 = bos + (long long)cc * C;
         const int ln = (int)min((long long)C, eos - r0);
         float bet = 0.f;
         if (tid < C && tid < ln) bet = __bfloat162float(bg[(size_t)(r0 + tid) * H + h]);
         if (!wait_all(&bars[BAR_TMA], (uint32_t)(cc & 1))) return false;
-        pending &= ~(1u << BAR_TMA);
 
         // ---- 1. Gam = cumsum_r g within the chunk, per key channel --------------------------
         // A warp holds 32 consecutive rows of 32 channels: scan over the 8 lanes of a row
@@ -359,7 +451,7 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         if (tid < C) sbeta[tid] = bet;
-        __syncthreads();
+        sync_compute();
         if (mh) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -382,18 +474,18 @@ __global__ void __launch_bounds__(NT, 1)
             cst[CST_E63G31 * 128 + ch] = ex2((G63 - G31) * kLog2e);
             cst[CST_GC * 128 + ch] = ex2(G63 * kLog2e);
         }
-        __syncthreads();
+        sync_compute();
 
         return true;
     };
 
-    int c = 0;
-    if (nchunks > 0) ok = step1(0);
+        int c = 0;
+        if (nchunks > 0) ok = step1(0);
 #pragma unroll 1
-    for (; ok && c < nchunks; ++c) {
-        const uint32_t par = (uint32_t)(c & 1);
-        const long long row0 = bos + (long long)c * C;
-        const int len = (int)min((long long)C, eos - row0);
+        for (; ok && c < nchunks; ++c) {
+            const uint32_t par = (uint32_t)(c & 1);
+            const long long row0 = bos + (long long)c * C;
+            const int len = (int)min((long long)C, eos - row0);
 
         // ---- 2. decay-scaled operands -----------------------------------------------------
         {
@@ -456,16 +548,9 @@ __global__ void __launch_bounds__(NT, 1)
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        mbar_arrive(&bars[BAR_OPS]);
 
-        // ---- 3. intra-chunk tiles; the state decay runs in their shadow ------------------------
-        if (tid == 0) {
-            issue_mma(tmem + TM_AP, sb + SM_AP, sb + SM_APB, D, D / 16, idesc_bf16(128, 64), false);
-            issue_mma(tmem + TM_OFF, sb + SM_OFF, sb + SM_OFF, D, D / 16, idesc_bf16(128, 32), false);
-            mma_commit(&bars[BAR_AP]);
-        }
-        pending |= 1u << BAR_AP;
+        // ---- 3. the state decay runs in the shadow of the intra-chunk tiles -----------------
         // S <- S Diag(gam_last): the state in TMEM is next read by MMA4 of this chunk.
 #pragma unroll 1
         for (int cb = 0; cb < 2; ++cb) {
@@ -481,38 +566,7 @@ __global__ void __launch_bounds__(NT, 1)
 
         // ---- 4. A (fp32, for the solve) and P (bf16 operand) out of TMEM -------------------
         if (!(ok = wait_all(&bars[BAR_AP], par))) break;
-        pending &= ~(1u << BAR_AP);
         tc_fence_after();
-        // MMA1 and the next chunk's tiles are issued from warp 4, whose share of the epilogue
-        // below is zero-filling (its rows sit above the diagonal), so the issue wait is hidden.
-        if (tid == 128) {
-#pragma unroll 1
-            for (int st = 0; st < D / 16; ++st)
-                mma_bf16_tmem_a(tmem + TM_D1, tmem + TM_SA + 8 * st, sdesc(sb + SM_KQ + 256u * st, 128u, 2048u),
-                                idesc_bf16(128, 128), st > 0);
-            mma_commit(&bars[BAR_M1]);
-            if (c + 1 < nchunks) {
-                const int nr = (int)(row0 + C);
-                mbar_arrive_expect_tx(&bars[BAR_TMA], 3 * 16384);
-                for (int b = 0; b < 2; ++b) {
-                    tma_load_3d(sm + SM_Q + 8192 * b, &maps.q, &bars[BAR_TMA], 64 * b, h, nr);
-                    tma_load_3d(sm + SM_K + 8192 * b, &maps.k, &bars[BAR_TMA], 64 * b, h, nr);
-                    tma_load_3d(sm + SM_G + 8192 * b, &maps.g, &bars[BAR_TMA], 64 * b, h, nr);
-                }
-            }
-        }
-        pending |= 1u << BAR_M1;
-        if (c + 1 < nchunks) {
-            pending |= 1u << BAR_TMA;
-            tma_par = (uint32_t)((c + 1) & 1);
-        }
-        // The off-tile operands are consumed: the v tile of this chunk can land in their region.
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&bars[BAR_V], 16384);
-            tma_load_3d(sm + SM_VT, &maps.v, &bars[BAR_V], 0, h, (int)row0);
-            tma_load_3d(sm + SM_VT + 8192, &maps.v, &bars[BAR_V], 64, h, (int)row0);
-        }
-        pending |= 1u << BAR_V;
         {
             const int L = 32 * (warp & 3) + lane;
             const int i = L & 63;
@@ -547,81 +601,129 @@ __global__ void __launch_bounds__(NT, 1)
                 st_row32(sm + SM_P, i, j0, C, vals);
             }
         }
-        __syncthreads();
+        sync_compute();
 
-        // ---- 5. X = (I + A)^{-1} ------------------------------------------------------------
-        // (a) the four 16 x 16 diagonal blocks by forward substitution (one column per thread);
-        //     two strictly-upper 16 x 16 blocks that the 32 x 32 products read are zeroed.
-        if (tid < 64) {
-            const int b = tid >> 4, col = tid & 15;
-            float x[16];
+        // ---- 5. X = (I + A)^{-1}, written to T = X Diag(beta) as it completes ------------------
+        // (a) warp b < 4 inverts the 16 x 16 diagonal block b by doubling: four 4 x 4 blocks in
+        //     closed form, then 4 -> 8 -> 16 merges X21 = -X22 (A21 X11); warps 4..7 zero the
+        //     strictly-upper blocks of T and the two upper blocks of X the merges read.
+        if (warp < 4) {
+            const int B0 = 16 * warp;
+            float *Yw = reinterpret_cast<float *>(sm + SM_Y) + warp * (16 * 17);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float a0 = 0.f, a1 = 0.f;  // two chains halve the dependent-FMA latency
-#pragma unroll
-                for (int m = 0; m < i; ++m) {
-                    if (m & 1) a1 = fmaf(As[(16 * b + i) * SA + 16 * b + m], x[m], a1);
-                    else a0 = fmaf(As[(16 * b + i) * SA + 16 * b + m], x[m], a0);
-                }
-                x[i] = (i == col) ? 1.f : (i < col ? 0.f : -(a0 + a1));
+            for (int q = 0; q < 3; ++q) {  // zero the upper 4 x 4 blocks of the diagonal block
+                const int e = lane + 32 * q;   // 96 entries: 6 blocks x 16
+                const int blk = e >> 4, rr = (e >> 2) & 3, cc = e & 3;
+                const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                Xs[(B0 + 4 * bi + rr) * SA + B0 + 4 * bj + cc] = 0.f;
             }
-            const float bcol = sbeta[16 * b + col];
-            __nv_bfloat16 *Tb = reinterpret_cast<__nv_bfloat16 *>(sm + SM_T);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                Xs[(16 * b + i) * SA + 16 * b + col] = x[i];
-                Tb[kmajor_offset(16 * b + i, 16 * b + col, C) / 2] = __float2bfloat16_rn(x[i] * bcol);
-            }
-        } else {
-            const int z = tid - 64;  // 0..191
-            if (z < 128) {  // X rows 0..15 cols 16..31, rows 32..47 cols 48..63 (read by the merges)
-                const int blk = z >> 6, rr = (z & 63) >> 2, cq = (z & 3) * 4;
-                *reinterpret_cast<float4 *>(Xs + (32 * blk + rr) * SA + 32 * blk + 16 + cq) =
-                    make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            // T: the six strictly-upper 16 x 16 blocks, 16 rows x 2 chunks each
-            const int bi = z >> 5, rr = (z & 31) >> 1, hf = z & 1;
-            const int I = bi < 3 ? 0 : (bi < 5 ? 1 : 2);
-            const int J = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
-            *reinterpret_cast<uint4 *>(sm + SM_T + kmajor_offset(16 * I + rr, 16 * J + 8 * hf, C)) =
-                make_uint4(0u, 0u, 0u, 0u);
-        }
-        __syncthreads();
-        // (b) 16 -> 32: X_{2p+1,2p} = -X_{2p+1,2p+1} A_{2p+1,2p} X_{2p,2p} (warp p, tf32 mma)
-        if (warp < 2) {
-            const int I = 2 * warp + 1, J = 2 * warp;
-            float *Yp = reinterpret_cast<float *>(sm + SM_Y) + 16 * warp * SA;
-            float acc[4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                warp_mma_16x8<16>(acc, As + 16 * I * SA + 16 * J, SA, Xs + 16 * J * SA + 16 * J + 8 * nt, SA, lane);
-                warp_store_16x8(Yp + 8 * nt, SA, acc, 1.f, lane);
+            if (lane < 4) {  // 4 x 4 unit lower-triangular inverse in closed form
+                const int o = B0 + 4 * lane;
+                const float a10 = As[(o + 1) * SA + o], a20 = As[(o + 2) * SA + o], a21 = As[(o + 2) * SA + o + 1];
+                const float a30 = As[(o + 3) * SA + o], a31 = As[(o + 3) * SA + o + 1], a32 = As[(o + 3) * SA + o + 2];
+                const float x10 = -a10, x21 = -a21, x32 = -a32;
+                const float x20 = -fmaf(a21, x10, a20);
+                const float x31 = -fmaf(a32, x21, a31);
+                const float x30 = -fmaf(a32, x20, fmaf(a31, x10, a30));
+                float *X0 = Xs + o * SA + o;
+                X0[0] = 1.f;      X0[1] = 0.f;      X0[2] = 0.f;      X0[3] = 0.f;
+                X0[SA] = x10;     X0[SA + 1] = 1.f; X0[SA + 2] = 0.f; X0[SA + 3] = 0.f;
+                X0[2 * SA] = x20; X0[2 * SA + 1] = x21; X0[2 * SA + 2] = 1.f; X0[2 * SA + 3] = 0.f;
+                X0[3 * SA] = x30; X0[3 * SA + 1] = x31; X0[3 * SA + 2] = x32; X0[3 * SA + 3] = 1.f;
             }
             __syncwarp();
+            {  // 4 -> 8: lane = (half q, row r, column c) of the two 4 x 4 blocks X21
+                const int q = lane >> 4, r = (lane >> 2) & 3, cc = lane & 3;
+                const int o = B0 + 8 * q;
+                float y = 0.f;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                warp_mma_16x8<16>(acc, Xs + 16 * I * SA + 16 * I, SA, Yp + 8 * nt, SA, lane);
-                warp_store_16x8(Xs + 16 * I * SA + 16 * J + 8 * nt, SA, acc, -1.f, lane);
-                store_t_16x8(sm + SM_T, 16 * I, 16 * J + 8 * nt, acc, sbeta, lane);
+                for (int m = 0; m < 4; ++m) y = fmaf(As[(o + 4 + r) * SA + o + m], Xs[(o + m) * SA + o + cc], y);
+                Yw[(4 * q + r) * 17 + cc] = y;
+                __syncwarp();
+                float x = 0.f;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) x = fmaf(Xs[(o + 4 + r) * SA + o + 4 + m], Yw[(4 * q + m) * 17 + cc], x);
+                Xs[(o + 4 + r) * SA + o + cc] = -x;
+            }
+            __syncwarp();
+            {  // 8 -> 16: X21 (8 x 8), two entries per lane
+                const int r = lane >> 2, c0 = (lane & 3) * 2;
+                float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const float am = As[(B0 + 8 + r) * SA + B0 + m];
+                    y0 = fmaf(am, Xs[(B0 + m) * SA + B0 + c0], y0);
+                    y1 = fmaf(am, Xs[(B0 + m) * SA + B0 + c0 + 1], y1);
+                }
+                Yw[r * 17 + c0] = y0;
+                Yw[r * 17 + c0 + 1] = y1;
+                __syncwarp();
+                float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const float xm = Xs[(B0 + 8 + r) * SA + B0 + 8 + m];
+                    x0 = fmaf(xm, Yw[m * 17 + c0], x0);
+                    x1 = fmaf(xm, Yw[m * 17 + c0 + 1], x1);
+                }
+                Xs[(B0 + 8 + r) * SA + B0 + c0] = -x0;
+                Xs[(B0 + 8 + r) * SA + B0 + c0 + 1] = -x1;
+            }
+            __syncwarp();
+            {  // T of the diagonal block: one 16-byte chunk (row r, 8 columns) per lane
+                const int r = lane >> 1, h8 = (lane & 1) * 8;
+                float tv[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) tv[q] = Xs[(B0 + r) * SA + B0 + h8 + q] * sbeta[B0 + h8 + q];
+                st_chunk(sm, SM_T + kmajor_offset(B0 + r, B0 + h8, C), tv);
+            }
+        } else {
+            const int z = tid - 128;  // 0..127
+            // X rows 0..15 cols 16..31 and rows 32..47 cols 48..63 (read by the 32 -> 64 merge)
+            const int blk = z >> 6, rr = (z & 63) >> 2, cq = (z & 3) * 4;
+            *reinterpret_cast<float4 *>(Xs + (32 * blk + rr) * SA + 32 * blk + 16 + cq) = make_float4(0.f, 0.f, 0.f, 0.f);
+            // T: the six strictly-upper 16 x 16 blocks (192 chunks of 16 bytes)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int e = z + 128 * q;
+                if (e < 192) {
+                    const int bi = e >> 5, r2 = (e & 31) >> 1, hf = e & 1;
+                    const int I = bi < 3 ? 0 : (bi < 5 ? 1 : 2);
+                    const int J = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
+                    *reinterpret_cast<uint4 *>(sm + SM_T + kmajor_offset(16 * I + r2, 16 * J + 8 * hf, C)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
             }
         }
-        __syncthreads();
+        sync_compute();
+        // (b) 16 -> 32: warp (p, nt) < 4 computes column tile nt of X_{2p+1,2p} (tf32 mma)
+        if (warp < 4) {
+            const int pp = warp >> 1, nt = warp & 1;
+            const int I = 2 * pp + 1, J = 2 * pp;
+            float *Yb = reinterpret_cast<float *>(sm + SM_Y + 4352) + 16 * pp * SA;
+            float acc[4];
+            warp_mma_16x8<16>(acc, As + 16 * I * SA + 16 * J, SA, Xs + 16 * J * SA + 16 * J + 8 * nt, SA, lane);
+            warp_store_16x8(Yb + 8 * nt, SA, acc, 1.f, lane);
+            __syncwarp();
+            warp_mma_16x8<16>(acc, Xs + 16 * I * SA + 16 * I, SA, Yb + 8 * nt, SA, lane);
+            warp_store_16x8(Xs + 16 * I * SA + 16 * J + 8 * nt, SA, acc, -1.f, lane);
+            store_t_16x8(sm + SM_T, 16 * I, 16 * J + 8 * nt, acc, sbeta, lane);
+        }
+        sync_compute();
         // (c) 32 -> 64: X_BA = -X_BB A_BA X_AA with 32 x 32 blocks; warp w owns one 16 x 8 tile.
         {
             const int mt = warp >> 2, nt = warp & 3;
-            float *Y = reinterpret_cast<float *>(sm + SM_Y);
+            float *Y = reinterpret_cast<float *>(sm + SM_Y + 4352);
             float acc[4];
             warp_mma_16x8<32>(acc, As + (32 + 16 * mt) * SA, SA, Xs + 8 * nt, SA, lane);
             warp_store_16x8(Y + 16 * mt * SA + 8 * nt, SA, acc, 1.f, lane);
-            __syncthreads();
+            sync_compute();
             warp_mma_16x8<32>(acc, Xs + (32 + 16 * mt) * SA + 32, SA, Y + 8 * nt, SA, lane);
             store_t_16x8(sm + SM_T, 32 + 16 * mt, 8 * nt, acc, sbeta, lane);
         }
-        __syncthreads();
 
         // ---- 6. U = T V - T (K+ S): -(K+ S)^T goes to TMEM as MMA2's second A operand ----------
         if (!(ok = wait_all(&bars[BAR_M1], par))) break;
-        pending &= ~(1u << BAR_M1);
         tc_fence_after();
         {
             float ks[32];
@@ -632,28 +734,11 @@ __global__ void __launch_bounds__(NT, 1)
             tmem_st16(tmem + tq + TM_RA + 16 * eh, w);
             tmem_st_wait();
         }
-        if (!(ok = wait_all(&bars[BAR_V], par))) break;  // also orders the T stores above
-        pending &= ~(1u << BAR_V);
-        fence_async_smem();
+        fence_async_smem();  // the T stores of the solve
         tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-            // V^T straight from its TMA tile (MN-major A), then the -(K+ S)^T part from TMEM.
-#pragma unroll 1
-            for (int st = 0; st < C / 16; ++st)
-                mma_bf16(tmem + TM_U, sdesc_sw128(sb + SM_VT + 2048u * st, 8192u, 1024u),
-                         sdesc(sb + SM_T + 256u * st, 128u, 1024u), idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
-#pragma unroll 1
-            for (int st = 0; st < C / 16; ++st)
-                mma_bf16_tmem_a(tmem + TM_U, tmem + TM_RA + 8 * st, sdesc(sb + SM_T + 256u * st, 128u, 1024u),
-                                idesc_bf16(128, 64), 1u);
-            mma_commit(&bars[BAR_M2]);
-        }
-        pending |= 1u << BAR_M2;
+        mbar_arrive(&bars[BAR_RREADY]);
 
         if (!(ok = wait_all(&bars[BAR_M2], par))) break;
-        pending &= ~(1u << BAR_M2);
         tc_fence_after();
         {
             float u[32];
@@ -665,23 +750,10 @@ __global__ void __launch_bounds__(NT, 1)
             tmem_st_wait();
         }
         tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-#pragma unroll 1
-            for (int st = 0; st < C / 16; ++st)
-                mma_bf16_tmem_a(tmem + TM_D1 + 64, tmem + TM_RA + 8 * st, sdesc(sb + SM_P + 256u * st, 128u, 1024u),
-                                idesc_bf16(128, 64), 1u);
-#pragma unroll 1
-            for (int st = 0; st < C / 16; ++st)
-                mma_bf16_tmem_a(tmem + TM_S, tmem + TM_RA + 8 * st, sdesc_sw128(sb + SM_KH + 2048u * st, 8192u, 1024u),
-                                idesc_bf16(128, 128) | kIdescBMajorMN, 1u);
-            mma_commit(&bars[BAR_M34]);
-        }
-        pending |= 1u << BAR_M34;
+        mbar_arrive(&bars[BAR_UREADY]);
+
         if (c + 1 < nchunks && !(ok = step1(c + 1))) break;
         if (!(ok = wait_all(&bars[BAR_M34], par))) break;
-        pending &= ~(1u << BAR_M34);
         tc_fence_after();
 
         // ---- 7. O out (staged through shared memory); S^T (bf16) for the next MMA1 ---------
@@ -704,10 +776,7 @@ __global__ void __launch_bounds__(NT, 1)
             tmem_st16(tmem + tq + TM_SA + k0 / 2, w);
         }
         tmem_st_wait();
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        sync_compute();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int idx = tid + NT * q;  // 1024 chunks of 16 bytes: row idx / 16, chunk idx % 16
@@ -716,26 +785,23 @@ __global__ void __launch_bounds__(NT, 1)
                 *reinterpret_cast<uint4 *>(og + ((size_t)(row0 + r) * H + h) * D + 8 * c16) =
                     *reinterpret_cast<const uint4 *>(sm + SM_OST + r * 256 + 16 * c16);
         }
-    }
-
-    if (ok) {
-        if (p.fin) {
-#pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-                const int k0 = 64 * eh + 32 * cb;
-                float sv[32];
-                tmem_ld32(tmem + tq + TM_S + k0, sv);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) __stcs(p.fin + state_off + (size_t)(k0 + i) * D + ev, sv[i]);
-            }
         }
-    } else {
-        if (tid == 0) atomicOr(p.err, kErrTimeout);
-        // Drain what this CTA issued (bounded), so no MMA or copy is in flight at exit.
-        const uint32_t par = (uint32_t)(c & 1);
-        for (int b = 0; b < BAR_N; ++b)
-            if (pending & (1u << b)) (void)mbar_wait(&bars[b], b == BAR_TMA ? tma_par : par, kWaitNs);
+
+        if (ok) {
+            if (p.fin) {
+#pragma unroll 1
+                for (int cb = 0; cb < 2; ++cb) {
+                    const int k0 = 64 * eh + 32 * cb;
+                    float sv[32];
+                    tmem_ld32(tmem + tq + TM_S + k0, sv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) __stcs(p.fin + state_off + (size_t)(k0 + i) * D + ev, sv[i]);
+                }
+            }
+        } else if (tid == 0) {
+            atomicOr(p.err, kErrTimeout);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -799,7 +865,7 @@ cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
     if (!encode_map(&maps.q, p.q, rows, p.H) || !encode_map(&maps.k, p.k, rows, p.H) ||
         !encode_map(&maps.g, p.g, rows, p.H) || !encode_map(&maps.v, p.v, rows, p.H))
         return cudaErrorInvalidValue;
-    kda_prefill_tc_kernel<<<(unsigned)(p.n_seqs * p.H), NT, SMEM_BYTES, s>>>(maps, p);
+    kda_prefill_tc_kernel<<<(unsigned)(p.n_seqs * p.H), NTHREADS, SMEM_BYTES, s>>>(maps, p);
     return cudaGetLastError();
 }
 
