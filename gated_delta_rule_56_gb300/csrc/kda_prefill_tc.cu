@@ -97,8 +97,11 @@ constexpr uint32_t TM_AP = 0, TM_OFF = 64, TM_RA = 96, TM_D1 = 128, TM_U = 256, 
 constexpr uint32_t TM_COLS = 512;
 
 // Barriers.
-// BAR_OPS / BAR_RREADY / BAR_UREADY: the compute threads' operands are ready (256 arrivals each).
-enum { BAR_TMA = 0, BAR_AP, BAR_M1, BAR_M2, BAR_M34, BAR_V, BAR_OPS, BAR_RREADY, BAR_UREADY, BAR_N };
+// BAR_OPS .. BAR_UREADY: something the compute threads produce is ready (256 arrivals each): the
+// intra-chunk operands, the bf16 state copy (and O of the previous chunk read out), T,
+// -(K+ S)^T, U^T.
+enum { BAR_TMA = 0, BAR_AP, BAR_M1, BAR_M2, BAR_M34, BAR_V, BAR_OPS, BAR_SREADY, BAR_TREADY, BAR_RREADY, BAR_UREADY,
+       BAR_N };
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     if (tid == 32) {
         for (int b = 0; b < BAR_N; ++b)
-            mbar_init(&bars[b], (b == BAR_OPS || b == BAR_RREADY || b == BAR_UREADY) ? NT : 1);
+            mbar_init(&bars[b], b >= BAR_OPS ? NT : 1);
         fence_mbar_init();
     }
     if (tid == 64) {
@@ -327,12 +330,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 issue_mma(tmem + TM_AP, sb + SM_AP, sb + SM_APB, D, D / 16, idesc_bf16(128, 64), false);
                 issue_mma(tmem + TM_OFF, sb + SM_OFF, sb + SM_OFF, D, D / 16, idesc_bf16(128, 32), false);
                 mma_commit(&bars[BAR_AP]);
-#pragma unroll 1
-                for (int st = 0; st < D / 16; ++st)
-                    mma_bf16_tmem_a(tmem + TM_D1, tmem + TM_SA + 8 * st, sdesc(sb + SM_KQ + 256u * st, 128u, 2048u),
-                                    idesc_bf16(128, 128), st > 0);
-                mma_commit(&bars[BAR_M1]);
-                pend |= (1u << BAR_AP) | (1u << BAR_M1);
+                pend |= 1u << BAR_AP;
                 if (cc + 1 < nchunks) {  // this chunk's q/k/g tiles are consumed: fetch the next ones
                     const int nr = (int)(row0 + C);
                     mbar_arrive_expect_tx(&bars[BAR_TMA], 3 * 16384);
@@ -344,6 +342,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     pend |= 1u << BAR_TMA;
                     tpar = (uint32_t)((cc + 1) & 1);
                 }
+                // MMA1 once the bf16 state copy is in TMEM (and O of the previous chunk is read out)
+                if (!(iok = mbar_wait(&bars[BAR_SREADY], par, kWaitNs))) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int st = 0; st < D / 16; ++st)
+                    mma_bf16_tmem_a(tmem + TM_D1, tmem + TM_SA + 8 * st, sdesc(sb + SM_KQ + 256u * st, 128u, 2048u),
+                                    idesc_bf16(128, 128), st > 0);
+                mma_commit(&bars[BAR_M1]);
+                pend |= 1u << BAR_M1;
                 // The off-tile operands are consumed: the v tile of this chunk lands in their region.
                 if (!(iok = mbar_wait(&bars[BAR_AP], par, kWaitNs))) break;
                 pend &= ~(1u << BAR_AP);
@@ -353,13 +360,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 pend |= 1u << BAR_V;
                 if (!(iok = mbar_wait(&bars[BAR_V], par, kWaitNs))) break;
                 pend &= ~(1u << BAR_V);
-                if (!(iok = mbar_wait(&bars[BAR_RREADY], par, kWaitNs))) break;
-                tc_fence_after();
-                // U^T = V^T T^T (V tile as an MN-major A operand) + (-(K+ S)^T from TMEM) T^T
+                if (!(iok = mbar_wait(&bars[BAR_TREADY], par, kWaitNs))) break;
+                // U^T = V^T T^T (V tile as an MN-major A operand) + (-(K+ S)^T from TMEM) T^T; the
+                // first half runs while the compute warps move -(K+ S)^T into TMEM.
 #pragma unroll 1
                 for (int st = 0; st < C / 16; ++st)
                     mma_bf16(tmem + TM_U, sdesc_sw128(sb + SM_VT + 2048u * st, 8192u, 1024u),
                              sdesc(sb + SM_T + 256u * st, 128u, 1024u), idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
+                if (!(iok = mbar_wait(&bars[BAR_RREADY], par, kWaitNs))) break;
+                tc_fence_after();
 #pragma unroll 1
                 for (int st = 0; st < C / 16; ++st)
                     mma_bf16_tmem_a(tmem + TM_U, tmem + TM_RA + 8 * st, sdesc(sb + SM_T + 256u * st, 128u, 1024u),
@@ -479,7 +488,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         return true;
     };
 
+        // O of a finished chunk (in TMEM columns 192..255) -> staging -> 16-byte coalesced stores.
+        auto write_o = [&](long long r0, int ln) {
+            float ov[32];
+            tmem_ld32(tmem + tq + TM_D1 + 64 + 32 * eh, ov);
+            tmem_ld_wait();
+            __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(sm + SM_OST);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ost[(32 * eh + i) * D + ev] = __float2bfloat16_rn(ov[i]);
+            sync_compute();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int idx = tid + NT * q;  // 1024 chunks of 16 bytes: row idx / 16, chunk idx % 16
+                const int r = idx >> 4, c16 = idx & 15;
+                if (r < ln)
+                    *reinterpret_cast<uint4 *>(og + ((size_t)(r0 + r) * H + h) * D + 8 * c16) =
+                        *reinterpret_cast<const uint4 *>(sm + SM_OST + r * 256 + 16 * c16);
+            }
+        };
+
         int c = 0;
+        long long prev_row0 = 0;
+        int prev_len = 0;
         if (nchunks > 0) ok = step1(0);
 #pragma unroll 1
         for (; ok && c < nchunks; ++c) {
@@ -549,6 +579,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(&bars[BAR_OPS]);
+
+        // ---- 2b. while the intra-chunk tiles run: O of the previous chunk, then the bf16 copy
+        //          of the state for MMA1 (the initial state's copy was made before the loop).
+        if (c > 0) {
+            write_o(prev_row0, prev_len);
+#pragma unroll 1
+            for (int cb = 0; cb < 2; ++cb) {
+                const int k0 = 64 * eh + 32 * cb;
+                float sv[32];
+                tmem_ld32(tmem + tq + TM_S + k0, sv);
+                tmem_ld_wait();
+                uint32_t w[16];
+                pack32(sv, w, 1.f);
+                tmem_st16(tmem + tq + TM_SA + k0 / 2, w);
+            }
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars[BAR_SREADY]);
 
         // ---- 3. the state decay runs in the shadow of the intra-chunk tiles -----------------
         // S <- S Diag(gam_last): the state in TMEM is next read by MMA4 of this chunk.
@@ -723,6 +772,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
 
         // ---- 6. U = T V - T (K+ S): -(K+ S)^T goes to TMEM as MMA2's second A operand ----------
+        fence_async_smem();  // the T stores of the solve
+        mbar_arrive(&bars[BAR_TREADY]);
         if (!(ok = wait_all(&bars[BAR_M1], par))) break;
         tc_fence_after();
         {
@@ -734,7 +785,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_st16(tmem + tq + TM_RA + 16 * eh, w);
             tmem_st_wait();
         }
-        fence_async_smem();  // the T stores of the solve
         tc_fence_before();
         mbar_arrive(&bars[BAR_RREADY]);
 
@@ -756,37 +806,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!(ok = wait_all(&bars[BAR_M34], par))) break;
         tc_fence_after();
 
-        // ---- 7. O out (staged through shared memory); S^T (bf16) for the next MMA1 ---------
-        {
-            float ov[32];
-            tmem_ld32(tmem + tq + TM_D1 + 64 + 32 * eh, ov);
-            tmem_ld_wait();
-            __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(sm + SM_OST);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ost[(32 * eh + i) * D + ev] = __float2bfloat16_rn(ov[i]);
-        }
-#pragma unroll 1
-        for (int cb = 0; cb < 2; ++cb) {
-            const int k0 = 64 * eh + 32 * cb;
-            float sv[32];
-            tmem_ld32(tmem + tq + TM_S + k0, sv);
-            tmem_ld_wait();
-            uint32_t w[16];
-            pack32(sv, w, 1.f);
-            tmem_st16(tmem + tq + TM_SA + k0 / 2, w);
-        }
-        tmem_st_wait();
-        sync_compute();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int idx = tid + NT * q;  // 1024 chunks of 16 bytes: row idx / 16, chunk idx % 16
-            const int r = idx >> 4, c16 = idx & 15;
-            if (r < len)
-                *reinterpret_cast<uint4 *>(og + ((size_t)(row0 + r) * H + h) * D + 8 * c16) =
-                    *reinterpret_cast<const uint4 *>(sm + SM_OST + r * 256 + 16 * c16);
-        }
+        prev_row0 = row0;
+        prev_len = len;
         }
 
+        if (ok && nchunks > 0) write_o(prev_row0, prev_len);  // O of the last chunk
         if (ok) {
             if (p.fin) {
 #pragma unroll 1
