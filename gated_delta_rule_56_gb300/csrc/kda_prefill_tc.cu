@@ -534,37 +534,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int r = rlo + 8 * (4 * mh + m);
-                const bool live = r < len;
+                const bool live = r < len;  // rows past the sequence end act as identity tokens
                 const uint4 kw = *reinterpret_cast<const uint4 *>(sm + SM_K + tile_chunk(r, j));
                 const uint4 qw = *reinterpret_cast<const uint4 *>(sm + SM_Q + tile_chunk(r, j));
-                const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w}, qq[4] = {qw.x, qw.y, qw.z, qw.w};
+                const uint32_t kk[4] = {live ? kw.x : 0u, live ? kw.y : 0u, live ? kw.z : 0u, live ? kw.w : 0u};
+                const uint32_t qq[4] = {live ? qw.x : 0u, live ? qw.y : 0u, live ? qw.z : 0u, live ? qw.w : 0u};
                 float apk[8], apq[8], apb[8], ofr_k[8], ofr_q[8], kp[8], qp[8], kh[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float kv = live ? ((i & 1) ? bf_hi(kk[i >> 1]) : bf_lo(kk[i >> 1])) : 0.f;
-                    const float qv = live ? ((i & 1) ? bf_hi(qq[i >> 1]) : bf_lo(qq[i >> 1])) : 0.f;
+                    const float kv = (i & 1) ? bf_hi(kk[i >> 1]) : bf_lo(kk[i >> 1]);
+                    const float qv = (i & 1) ? bf_hi(qq[i >> 1]) : bf_lo(qq[i >> 1]);
                     // |Gam_r - ref| <= 80 for g in [-5, 0]; the clamp only keeps factors finite
                     // (no 0 * inf) for gates outside that range.
                     const float e = fminf(fmaxf((gm[m][i] - ref[i]) * kLog2e, -126.f), 126.f);
                     const float f = ex2(e), fi = ex2(-e);
-                    float fo, pfac, khfac;
-                    if (mh) {
-                        fo = f * fo_c[i];     // exp(Gam_r - Gam_31)
-                        pfac = fo * pe[i];    // exp(Gam_r)
-                        khfac = fi * khe[i];  // exp(Gam_63 - Gam_r)
-                    } else {
-                        fo = fi * fo_c[i];    // exp(Gam_31 - Gam_r)
-                        pfac = f * pe[i];     // exp(Gam_r)
-                        khfac = fo * khe[i];  // exp(Gam_63 - Gam_r)
-                    }
                     apk[i] = kv * f;
                     apq[i] = qv * f;
                     apb[i] = kv * fi;
-                    ofr_k[i] = kv * fo;  // rows 32..63: off-tile row (K side); rows 0..31: off-tile column
-                    ofr_q[i] = qv * fo;  // rows 32..63: off-tile row (Q side)
-                    kp[i] = kv * pfac;
-                    qp[i] = qv * pfac;
-                    kh[i] = kv * khfac;
+                    // Every other operand is one of these times a per-channel factor <= 1 (so the
+                    // product stays in range):
+                    if (mh) {                           // rows 32..63
+                        ofr_k[i] = apk[i] * fo_c[i];    // K exp(Gam_r - Gam_31): off-tile row
+                        ofr_q[i] = apq[i] * fo_c[i];    // Q exp(Gam_r - Gam_31)
+                        kp[i] = ofr_k[i] * pe[i];       // K exp(Gam_r)
+                        qp[i] = ofr_q[i] * pe[i];       // Q exp(Gam_r)
+                        kh[i] = apb[i] * khe[i];        // K exp(Gam_63 - Gam_r)
+                    } else {                            // rows 0..31
+                        ofr_k[i] = apb[i] * fo_c[i];    // K exp(Gam_31 - Gam_r): off-tile column
+                        ofr_q[i] = 0.f;
+                        kp[i] = apk[i] * pe[i];         // K exp(Gam_r)
+                        qp[i] = apq[i] * pe[i];         // Q exp(Gam_r)
+                        kh[i] = ofr_k[i] * khe[i];      // K exp(Gam_63 - Gam_r)
+                    }
                 }
                 st_chunk(sm, SM_AP + kmajor_offset(r, 8 * j, D), apk);
                 st_chunk(sm, SM_AP + kmajor_offset(64 + r, 8 * j, D), apq);
