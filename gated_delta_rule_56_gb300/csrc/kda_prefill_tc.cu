@@ -21,17 +21,24 @@
 // boundary row Gam_31, where both factors are <= 1. Every other decay factor is a product of
 // in-range terms that are <= 1, so any underflow only drops contributions below 1e-38.
 //
-// Layout of the work: one CTA of 256 threads per (sequence, head); chunks run in order.
-//   TMA: q, k, g tiles (64 rows x 128 channels, 128-byte swizzle) for the next chunk are in
-//        flight while the current one computes; the v tile is fetched once the intra-chunk
-//        tiles have retired (into their operand region); beta uses plain loads.
+// Layout of the work: one CTA per (sequence, head); chunks run in order, in two overlapped
+// streams of work carried by different warps:
+//   prep warps 0..7    everything of a chunk that does not depend on the state: Gam (cumsum of
+//                      g), the decay-scaled operands, the A/P tiles, T. They build chunk c + 1
+//                      while the state chain of chunk c runs.
+//   state warps 8..11  thread = TMEM lane = value column: the bf16 state copy, the state decay,
+//                      -(K+ S)^T and U^T as bf16 A operands in TMEM, O written to global memory.
+//   issuer warp 12     one thread issues every MMA and TMA copy, in the order the work becomes
+//                      ready; mbarriers carry each hand-off between the three.
+//   TMA: g, then q/k tiles (64 rows x 128 channels, 128-byte swizzle) of the next chunk are
+//        fetched as soon as the current ones are read; the v tile once MMA2 has read the last.
 //   TMEM (512 columns): [0,64) diagonal A|P tile, [64,96) off-diagonal tile, [96,128) the
 //        bf16 A operand -(K+ S)^T then U^T, [128,256) (K+ S | Q+ S -> O), [256,320) U,
 //        [320,448) the fp32 state S^T (lanes = d_v), [448,512) its bf16 copy (MMA1's A).
-//   MMAs (kind::f16, bf16 operands, fp32 accumulate, M = 128; "tmem" = A read from TMEM):
-//        diag  [K*f ; Q*f] x [K/f]^T              N = 64, K = 128
-//        off   [K*e ; Q*e] x [K*e']^T             N = 32, K = 128
-//        MMA1  S^T (tmem) x [K+ ; Q+]^T           N = 128, K = 128   -> (K+ S)^T, (Q+ S)^T
+//   MMAs (kind::f16, bf16 operands, fp32 accumulate; "tmem" = A read from TMEM):
+//        diag  [K*f ; Q*f] x [K/f]^T              M = 128, N = 64, K = 128
+//        off   [K*e ; Q*e] x [K*e']^T             M = 64,  N = 32, K = 128
+//        MMA1  S^T (tmem) x [K+ ; Q+]^T           M = 128, two N = 64 halves, K = 128
 //        MMA2  V^T x T^T  (V tile, MN-major)      N = 64,  K = 64    -> then += -(K+ S)^T (tmem) x T^T = U^T
 //        MMA3  U^T (tmem) x P^T  (onto (Q+ S)^T)  N = 64,  K = 64    -> O^T
 //        MMA4  U^T (tmem) x Khat  (MN-major B)    N = 128, K = 64    -> S^T
@@ -51,57 +58,64 @@ namespace {
 
 using namespace tc;
 
-constexpr int C = 64;     // chunk length
-constexpr int D = 128;    // d_k == d_v
-constexpr int NT = 256;   // compute threads (warps 0..7)
-constexpr int kIssuer = NT / 32;  // warp 8 issues every MMA and TMA copy
-constexpr int NTHREADS = NT + 32;
+constexpr int C = 64;                     // chunk length
+constexpr int D = 128;                    // d_k == d_v
+constexpr int NP = 256;                   // prep threads (warps 0..7)
+constexpr int NS = 128;                   // state threads (warps 8..11), thread = TMEM lane = d_v index
+constexpr int kStateWarp0 = NP / 32;
+constexpr int kIssuer = (NP + NS) / 32;   // warp 12 issues every MMA and TMA copy
+constexpr int NTHREADS = NP + NS + 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
 
 // Shared memory map (bytes from a 1024-byte aligned base).
 constexpr uint32_t SM_Q = 0, SM_K = 16384, SM_G = 32768;  // TMA tiles, 2 boxes x (64 rows x 128 B)
-constexpr uint32_t SM_KH = 49152;                         // Khat [64 rows x 128 ch], same swizzled layout
-constexpr uint32_t SM_KQ = SM_KH + 16384;                 // [K+ ; Q+] operand  [128 x 128]
+constexpr uint32_t SM_KH = 49152;                         // Khat, two buffers of [64 rows x 128 ch] (TMA layout)
+constexpr uint32_t SM_KQ = SM_KH + 32768;                 // [K+ ; Q+] operand  [128 x 128]
 constexpr uint32_t SM_T = SM_KQ + 32768;                  // T operand          [64 x 64]
-constexpr uint32_t SM_AP = SM_T + 8192;                   // [K*f ; Q*f]        [128 x 128]
+constexpr uint32_t SM_P = SM_T + 8192;                    // P operand          [64 x 64]
+constexpr uint32_t SM_AP = SM_P + 8192;                   // [K*f ; Q*f]        [128 x 128]
 constexpr uint32_t SM_APB = SM_AP + 32768;                // K/f                [64 x 128]
 constexpr uint32_t SA = 68;                               // row stride (floats) of A and X
 constexpr uint32_t SM_AS = SM_AP;                         //   then A  fp32 [64 x 68]
 constexpr uint32_t SM_X = SM_AP + 64 * SA * 4;            //   then X = (I+A)^{-1} fp32 [64 x 68]
-constexpr uint32_t SM_P = SM_X + 64 * SA * 4;             //   then P bf16 operand [64 x 64]
-constexpr uint32_t SM_OFF = SM_AP + 49152;                // off tile operands (32 KB), see below
-constexpr uint32_t SM_Y = SM_OFF;                         //   then solve scratch fp32 [32 x 68]
-constexpr uint32_t SM_VT = SM_OFF + 16384;                //   then the v tile (TMA, like q/k/g)
-constexpr uint32_t SM_OST = SM_OFF + 32768;               // O staging bf16 [64 x 128]
-constexpr uint32_t SM_MISC = SM_OST + 16384;
+constexpr uint32_t SM_OFF = SM_AP + 49152;                // off tile: A operand [64 x 128] ...
+constexpr uint32_t SM_OFFB = SM_OFF + 16384;              //   ... and B operand [32 x 128]
+constexpr uint32_t SM_Y = SM_OFF;                         //   then solve scratch fp32
+constexpr uint32_t SM_VT = SM_OFF + 24576;                // v tile (TMA, like q/k/g)
+constexpr uint32_t SM_MISC = SM_VT + 16384;
 constexpr uint32_t SM_REF = SM_MISC;                      // fp32 [4][128]: Gam_15, Gam_31, Gam_47, Gam_63
-constexpr uint32_t SM_CST = SM_REF + 2048;                // fp32 [9][128] per-channel factors
-constexpr uint32_t SM_BETA = SM_CST + 4608;               // fp32 [64]
+constexpr uint32_t SM_CST = SM_REF + 2048;                // fp32 [8][128] per-channel factors
+constexpr uint32_t SM_GC = SM_CST + 4096;                 // fp32 [2][128] gam_last, by chunk parity
+constexpr uint32_t SM_BETA = SM_GC + 1024;                // fp32 [64]
 constexpr uint32_t SM_BAR = SM_BETA + 256;                // mbarriers
-constexpr uint32_t SM_TPTR = SM_BAR + 128;                // TMEM base address
+constexpr uint32_t SM_TPTR = SM_BAR + 256;                // TMEM base address
 constexpr uint32_t SM_USED = SM_TPTR + 16;
 constexpr uint32_t SMEM_BYTES = SM_USED + 1024;           // + alignment slack
-static_assert(SM_P + 8192 <= SM_OFF, "solve buffers overflow their region");
+static_assert(SM_X + 64 * SA * 4 <= SM_OFF, "solve buffers overflow their region");
+static_assert(SM_Y + 4352 + 32 * SA * 4 <= SM_VT, "solve scratch overflows its region");
 static_assert(SM_KH % 1024 == 0 && SM_VT % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-// The off-diagonal tile's A operand spans the whole 32 KB region as 128 rows: rows 32..63
-// (K side) and 96..127 (Q side) hold data; its B operand (32 rows) sits in rows 0..31, and
-// rows 64..95 are never read back from the accumulator.
 
 // Per-channel factor rows in SM_CST.
-enum { CST_M0 = 0, CST_M1, CST_C0, CST_C1, CST_EM0, CST_EG31, CST_E63M1, CST_E63G31, CST_GC, CST_N };
+enum { CST_M0 = 0, CST_M1, CST_C0, CST_C1, CST_EM0, CST_EG31, CST_E63M1, CST_E63G31, CST_N };
+static_assert(CST_N * 512 <= 4096, "factor rows overflow SM_CST");
 
 // TMEM column offsets.
 constexpr uint32_t TM_AP = 0, TM_OFF = 64, TM_RA = 96, TM_D1 = 128, TM_U = 256, TM_S = 320, TM_SA = 448;
 constexpr uint32_t TM_COLS = 512;
 
-// Barriers.
-// BAR_OPS .. BAR_UREADY: something the compute threads produce is ready (256 arrivals each): the
-// intra-chunk operands, the bf16 state copy (and O of the previous chunk read out), T,
-// -(K+ S)^T, U^T.
-enum { BAR_TMA = 0, BAR_AP, BAR_M1, BAR_M2, BAR_M34, BAR_V, BAR_OPS, BAR_SREADY, BAR_TREADY, BAR_RREADY, BAR_UREADY,
-       BAR_N };
+// Barriers. Up to BAR_DRAIN: TMA copies and MMA commits (one arrival). BAR_GFREE .. BAR_TREADY:
+// the prep warps have read the g tile / built the intra-chunk operands / written T and P (NP
+// arrivals). BAR_SREADY .. BAR_UREADY: the state warps have made the bf16 state copy (and read
+// out O of the previous chunk) / -(K+ S)^T / U^T (NS arrivals).
+enum {
+    BAR_G = 0, BAR_QK, BAR_V, BAR_AP, BAR_M1, BAR_KQFREE, BAR_M2, BAR_M34, BAR_DRAIN,
+    BAR_GFREE, BAR_OPS, BAR_TREADY,
+    BAR_SREADY, BAR_RREADY, BAR_UREADY,
+    BAR_N
+};
+static_assert(BAR_N * 8 <= 256, "barrier region");
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -192,23 +206,32 @@ __device__ __forceinline__ void store_t_16x8(uint8_t *Tbase, int r0, int c0, con
     *reinterpret_cast<uint32_t *>(Tbase + kmajor_offset(r0 + g + 8, cc, 64)) = pack_bf16(acc[2] * b0, acc[3] * b1);
 }
 
-// Barrier over the compute threads only (named barrier 1): the issuer warp never joins it.
-__device__ __forceinline__ void sync_compute() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
+// Barrier over one warp group only (named barrier ID with N threads).
+template <int ID, int N>
+__device__ __forceinline__ void group_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
+}
 
-// All compute threads wait on `bar`; true only if every one of them saw the phase complete.
-__device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
+// Every thread of a warp group waits on `bar`; true only if all of them saw the phase complete,
+// so the group leaves its loop together when a wait runs out.
+template <int ID, int N>
+__device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity) {
     const uint32_t bad = mbar_wait(bar, parity, kWaitNs) ? 0u : 1u;
     uint32_t any;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(any)
-        : "r"(bad), "n"(NT)
+        : "r"(bad), "n"(ID), "n"(N)
         : "memory");
     return any == 0;
 }
+
+__device__ __forceinline__ void prep_sync() { group_sync<1, NP>(); }
+__device__ __forceinline__ bool prep_wait(uint64_t *bar, uint32_t parity) { return group_wait<1, NP>(bar, parity); }
+__device__ __forceinline__ bool state_wait(uint64_t *bar, uint32_t parity) { return group_wait<2, NS>(bar, parity); }
 
 // Issue `steps` K-steps of one MMA (both operands K-major no-swizzle in shared memory).
 __device__ __forceinline__ void issue_mma(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, int K, int steps,
@@ -219,6 +242,73 @@ __device__ __forceinline__ void issue_mma(uint32_t d_tmem, uint32_t a_smem, uint
         const uint64_t a = sdesc(a_smem + 256u * s, 128u, sbo);
         const uint64_t b = sdesc(b_smem + 256u * s, 128u, sbo);
         mma_bf16(d_tmem, a, b, idesc, (accumulate || s > 0) ? 1u : 0u);
+    }
+}
+
+// Decay-scaled bf16 operands of one row half (MH = 0: rows 0..31, MH = 1: rows 32..63) for a
+// thread's 4 rows rlo + 8 * (4 * MH + m) x 8 channels 8j..8j+7; gm holds Gam of those entries.
+// Per-channel factors (see the exponent-range note at the top):
+//   rows 0..31 : f = exp(Gam_r - Gam_15); off-tile column factor fi*c0 = exp(Gam_31 - Gam_r)
+//   rows 32..63: f = exp(Gam_r - Gam_47); off-tile row factor    f*c1  = exp(Gam_r - Gam_31)
+// Every other operand is one of K f, Q f, K / f times a per-channel factor <= 1, so each
+// product stays in range. Rows past the sequence end (r >= len) act as identity tokens.
+template <int MH>
+__device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4][8], const float *cst, int rlo,
+                                               int j, int len, uint32_t khb) {
+    float ref[8], fo_c[8], pe[8], khe[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int ch = 8 * j + i;
+        ref[i] = cst[(MH ? CST_M1 : CST_M0) * 128 + ch];  // the reference Gam, times log2(e)
+        fo_c[i] = cst[(MH ? CST_C1 : CST_C0) * 128 + ch];
+        pe[i] = cst[(MH ? CST_EG31 : CST_EM0) * 128 + ch];
+        khe[i] = cst[(MH ? CST_E63M1 : CST_E63G31) * 128 + ch];
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int r = rlo + 8 * (4 * MH + m);
+        const bool live = r < len;
+        const uint4 kw = *reinterpret_cast<const uint4 *>(sm + SM_K + tile_chunk(r, j));
+        const uint4 qw = *reinterpret_cast<const uint4 *>(sm + SM_Q + tile_chunk(r, j));
+        const uint32_t kk[4] = {live ? kw.x : 0u, live ? kw.y : 0u, live ? kw.z : 0u, live ? kw.w : 0u};
+        const uint32_t qq[4] = {live ? qw.x : 0u, live ? qw.y : 0u, live ? qw.z : 0u, live ? qw.w : 0u};
+        float apk[8], apq[8], apb[8], ofr_k[8], ofr_q[8], kp[8], qp[8], kh[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float kv = (i & 1) ? bf_hi(kk[i >> 1]) : bf_lo(kk[i >> 1]);
+            const float qv = (i & 1) ? bf_hi(qq[i >> 1]) : bf_lo(qq[i >> 1]);
+            // |Gam_r - ref| <= 80 for g in [-5, 0]; the clamp only keeps factors finite (no 0 * inf)
+            // for gates outside that range.
+            const float e = fminf(fmaxf(fmaf(gm[m][i], kLog2e, -ref[i]), -126.f), 126.f);
+            const float f = ex2(e), fi = ex2(-e);
+            apk[i] = kv * f;
+            apq[i] = qv * f;
+            apb[i] = kv * fi;
+            if (MH) {
+                ofr_k[i] = apk[i] * fo_c[i];  // K exp(Gam_r - Gam_31): off-tile row
+                ofr_q[i] = apq[i] * fo_c[i];  // Q exp(Gam_r - Gam_31)
+                kp[i] = ofr_k[i] * pe[i];     // K exp(Gam_r)
+                qp[i] = ofr_q[i] * pe[i];     // Q exp(Gam_r)
+                kh[i] = apb[i] * khe[i];      // K exp(Gam_63 - Gam_r)
+            } else {
+                ofr_k[i] = apb[i] * fo_c[i];  // K exp(Gam_31 - Gam_r): off-tile column
+                kp[i] = apk[i] * pe[i];       // K exp(Gam_r)
+                qp[i] = apq[i] * pe[i];       // Q exp(Gam_r)
+                kh[i] = ofr_k[i] * khe[i];    // K exp(Gam_63 - Gam_r)
+            }
+        }
+        st_chunk(sm, SM_AP + kmajor_offset(r, 8 * j, D), apk);
+        st_chunk(sm, SM_AP + kmajor_offset(64 + r, 8 * j, D), apq);
+        st_chunk(sm, SM_APB + kmajor_offset(r, 8 * j, D), apb);
+        if (MH) {  // off-tile A operand: rows 0..31 the K side, 32..63 the Q side
+            st_chunk(sm, SM_OFF + kmajor_offset(r - 32, 8 * j, D), ofr_k);
+            st_chunk(sm, SM_OFF + kmajor_offset(r, 8 * j, D), ofr_q);
+        } else {   // off-tile B operand
+            st_chunk(sm, SM_OFFB + kmajor_offset(r, 8 * j, D), ofr_k);
+        }
+        st_chunk(sm, SM_KQ + kmajor_offset(r, 8 * j, D), kp);
+        st_chunk(sm, SM_KQ + kmajor_offset(64 + r, 8 * j, D), qp);
+        st_chunk(sm, khb + tile_chunk(r, j), kh);  // row-major: MMA4 reads it MN-major
     }
 }
 
@@ -233,6 +323,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t sb = smem_u32(sm);
     float *refs = reinterpret_cast<float *>(sm + SM_REF);
     float *cst = reinterpret_cast<float *>(sm + SM_CST);
+    float *gcs = reinterpret_cast<float *>(sm + SM_GC);
     float *sbeta = reinterpret_cast<float *>(sm + SM_BETA);
     float *As = reinterpret_cast<float *>(sm + SM_AS);
     float *Xs = reinterpret_cast<float *>(sm + SM_X);
@@ -264,7 +355,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     if (tid == 32) {
         for (int b = 0; b < BAR_N; ++b)
-            mbar_init(&bars[b], b >= BAR_OPS ? NT : 1);
+            mbar_init(&bars[b], b < BAR_GFREE ? 1 : (b < BAR_SREADY ? NP : NS));
         fence_mbar_init();
     }
     if (tid == 64) {
@@ -278,95 +369,80 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tptr;
     const uint32_t tq = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quarter
-
-    // Epilogue mapping: TMEM lane ev (= d_v index), column half eh.
-    const int ev = tid & 127, eh = tid >> 7;
     const size_t state_off = ((size_t)n * H + h) * (size_t)D * D;
-    const __nv_bfloat16 *bg = static_cast<const __nv_bfloat16 *>(p.beta);
-    __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o);
-
-    // Initial state -> TMEM (fp32) and the bf16 S^T operand.
-#pragma unroll 1
-    for (int cb = 0; cb < 2 && warp < kIssuer; ++cb) {
-        const int k0 = 64 * eh + 32 * cb;
-        float buf[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            buf[i] = p.init ? __ldcs(p.init + state_off + (size_t)(k0 + i) * D + ev) : 0.f;
-        tmem_st32(tmem + tq + TM_S + k0, buf);
-        uint32_t w[16];
-        pack32(buf, w, 1.f);
-        tmem_st16(tmem + tq + TM_SA + k0 / 2, w);
-    }
-    tmem_st_wait();
-
-    if (tid == 0 && nchunks > 0) {
-        mbar_arrive_expect_tx(&bars[BAR_TMA], 3 * 16384);
-        for (int b = 0; b < 2; ++b) {
-            tma_load_3d(sm + SM_Q + 8192 * b, &maps.q, &bars[BAR_TMA], 64 * b, h, (int)bos);
-            tma_load_3d(sm + SM_K + 8192 * b, &maps.k, &bars[BAR_TMA], 64 * b, h, (int)bos);
-            tma_load_3d(sm + SM_G + 8192 * b, &maps.g, &bars[BAR_TMA], 64 * b, h, (int)bos);
-        }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
 
     if (warp == kIssuer) {
         // ---------------------------------------------------------------- issuer warp --------
+        // One thread walks the chunks in the order the work becomes ready: the chunk-parallel
+        // MMAs of chunk c (their operands come from the prep warps), then the state chain of
+        // chunk c (MMA1, MMA2, MMA3/4) while the prep warps already build chunk c + 1.
         if (lane == 0) {
             bool iok = true;
-            uint32_t pend = nchunks > 0 ? (1u << BAR_TMA) : 0u;  // operations in flight
-            uint32_t tpar = 0;                                    // parity of the TMA phase in flight
-            int cc = 0;
+            int last_g = -1, last_qk = -1, last_v = -1;  // chunk of the latest copy on each barrier
+            auto load_g = [&](int cc) {
+                const int r = (int)(bos + (long long)cc * C);
+                mbar_arrive_expect_tx(&bars[BAR_G], 16384);
+                tma_load_3d(sm + SM_G, &maps.g, &bars[BAR_G], 0, h, r);
+                tma_load_3d(sm + SM_G + 8192, &maps.g, &bars[BAR_G], 64, h, r);
+                last_g = cc;
+            };
+            auto load_qk = [&](int cc) {
+                const int r = (int)(bos + (long long)cc * C);
+                mbar_arrive_expect_tx(&bars[BAR_QK], 32768);
+                for (int b = 0; b < 2; ++b) {
+                    tma_load_3d(sm + SM_Q + 8192 * b, &maps.q, &bars[BAR_QK], 64 * b, h, r);
+                    tma_load_3d(sm + SM_K + 8192 * b, &maps.k, &bars[BAR_QK], 64 * b, h, r);
+                }
+                last_qk = cc;
+            };
+            auto load_v = [&](int cc) {
+                const int r = (int)(bos + (long long)cc * C);
+                mbar_arrive_expect_tx(&bars[BAR_V], 16384);
+                tma_load_3d(sm + SM_VT, &maps.v, &bars[BAR_V], 0, h, r);
+                tma_load_3d(sm + SM_VT + 8192, &maps.v, &bars[BAR_V], 64, h, r);
+                last_v = cc;
+            };
+            if (nchunks > 0) {
+                load_g(0);
+                load_qk(0);
+                load_v(0);
+            }
 #pragma unroll 1
-            for (; cc < nchunks; ++cc) {
+            for (int cc = 0; cc < nchunks; ++cc) {
                 const uint32_t par = (uint32_t)(cc & 1);
-                const long long row0 = bos + (long long)cc * C;
+                const bool more = cc + 1 < nchunks;
+                // chunk-parallel part: the g tile is read -> fetch the next one; the operands are
+                // built -> A/P tiles, and the q/k tiles are free for the next chunk.
+                if (!(iok = mbar_wait(&bars[BAR_GFREE], par, kWaitNs))) break;
+                if (more) load_g(cc + 1);
                 if (!(iok = mbar_wait(&bars[BAR_OPS], par, kWaitNs))) break;
-                pend = 0;  // the compute side saw this chunk's tiles and every earlier MMA complete
                 tc_fence_after();
                 issue_mma(tmem + TM_AP, sb + SM_AP, sb + SM_APB, D, D / 16, idesc_bf16(128, 64), false);
-                issue_mma(tmem + TM_OFF, sb + SM_OFF, sb + SM_OFF, D, D / 16, idesc_bf16(128, 32), false);
+                issue_mma(tmem + TM_OFF, sb + SM_OFF, sb + SM_OFFB, D, D / 16, idesc_bf16(64, 32), false);
                 mma_commit(&bars[BAR_AP]);
-                pend |= 1u << BAR_AP;
-                if (cc + 1 < nchunks) {  // this chunk's q/k/g tiles are consumed: fetch the next ones
-                    const int nr = (int)(row0 + C);
-                    mbar_arrive_expect_tx(&bars[BAR_TMA], 3 * 16384);
-                    for (int b = 0; b < 2; ++b) {
-                        tma_load_3d(sm + SM_Q + 8192 * b, &maps.q, &bars[BAR_TMA], 64 * b, h, nr);
-                        tma_load_3d(sm + SM_K + 8192 * b, &maps.k, &bars[BAR_TMA], 64 * b, h, nr);
-                        tma_load_3d(sm + SM_G + 8192 * b, &maps.g, &bars[BAR_TMA], 64 * b, h, nr);
-                    }
-                    pend |= 1u << BAR_TMA;
-                    tpar = (uint32_t)((cc + 1) & 1);
-                }
-                // MMA1 once the bf16 state copy is in TMEM (and O of the previous chunk is read out)
+                if (more) load_qk(cc + 1);
+                // state chain. U^T = V^T T^T first (V tile as an MN-major A operand) ...
+                if (!(iok = mbar_wait(&bars[BAR_TREADY], par, kWaitNs))) break;
+                if (!(iok = mbar_wait(&bars[BAR_V], par, kWaitNs))) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int st = 0; st < C / 16; ++st)
+                    mma_bf16(tmem + TM_U, sdesc_sw128(sb + SM_VT + 2048u * st, 8192u, 1024u),
+                             sdesc(sb + SM_T + 256u * st, 128u, 1024u), idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
+                // ... MMA1 = S^T [K+ ; Q+]^T from the bf16 state copy, the K+ half committed first ...
                 if (!(iok = mbar_wait(&bars[BAR_SREADY], par, kWaitNs))) break;
                 tc_fence_after();
 #pragma unroll 1
                 for (int st = 0; st < D / 16; ++st)
                     mma_bf16_tmem_a(tmem + TM_D1, tmem + TM_SA + 8 * st, sdesc(sb + SM_KQ + 256u * st, 128u, 2048u),
-                                    idesc_bf16(128, 128), st > 0);
+                                    idesc_bf16(128, 64), st > 0);
                 mma_commit(&bars[BAR_M1]);
-                pend |= 1u << BAR_M1;
-                // The off-tile operands are consumed: the v tile of this chunk lands in their region.
-                if (!(iok = mbar_wait(&bars[BAR_AP], par, kWaitNs))) break;
-                pend &= ~(1u << BAR_AP);
-                mbar_arrive_expect_tx(&bars[BAR_V], 16384);
-                tma_load_3d(sm + SM_VT, &maps.v, &bars[BAR_V], 0, h, (int)row0);
-                tma_load_3d(sm + SM_VT + 8192, &maps.v, &bars[BAR_V], 64, h, (int)row0);
-                pend |= 1u << BAR_V;
-                if (!(iok = mbar_wait(&bars[BAR_V], par, kWaitNs))) break;
-                pend &= ~(1u << BAR_V);
-                if (!(iok = mbar_wait(&bars[BAR_TREADY], par, kWaitNs))) break;
-                // U^T = V^T T^T (V tile as an MN-major A operand) + (-(K+ S)^T from TMEM) T^T; the
-                // first half runs while the compute warps move -(K+ S)^T into TMEM.
 #pragma unroll 1
-                for (int st = 0; st < C / 16; ++st)
-                    mma_bf16(tmem + TM_U, sdesc_sw128(sb + SM_VT + 2048u * st, 8192u, 1024u),
-                             sdesc(sb + SM_T + 256u * st, 128u, 1024u), idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
+                for (int st = 0; st < D / 16; ++st)
+                    mma_bf16_tmem_a(tmem + TM_D1 + 64, tmem + TM_SA + 8 * st,
+                                    sdesc(sb + SM_KQ + 16384u + 256u * st, 128u, 2048u), idesc_bf16(128, 64), st > 0);
+                mma_commit(&bars[BAR_KQFREE]);
+                // ... U^T += -(K+ S)^T T^T (A from TMEM) ...
                 if (!(iok = mbar_wait(&bars[BAR_RREADY], par, kWaitNs))) break;
                 tc_fence_after();
 #pragma unroll 1
@@ -374,459 +450,473 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     mma_bf16_tmem_a(tmem + TM_U, tmem + TM_RA + 8 * st, sdesc(sb + SM_T + 256u * st, 128u, 1024u),
                                     idesc_bf16(128, 64), 1u);
                 mma_commit(&bars[BAR_M2]);
-                pend |= 1u << BAR_M2;
+                if (more) {  // the v tile is consumed: fetch the next one
+                    if (!(iok = mbar_wait(&bars[BAR_M2], par, kWaitNs))) break;
+                    load_v(cc + 1);
+                }
+                // ... then O^T += U^T P^T and S^T += U^T Khat.
                 if (!(iok = mbar_wait(&bars[BAR_UREADY], par, kWaitNs))) break;
                 tc_fence_after();
 #pragma unroll 1
                 for (int st = 0; st < C / 16; ++st)
                     mma_bf16_tmem_a(tmem + TM_D1 + 64, tmem + TM_RA + 8 * st, sdesc(sb + SM_P + 256u * st, 128u, 1024u),
                                     idesc_bf16(128, 64), 1u);
+                const uint32_t khb = sb + SM_KH + 16384u * par;
 #pragma unroll 1
                 for (int st = 0; st < C / 16; ++st)
-                    mma_bf16_tmem_a(tmem + TM_S, tmem + TM_RA + 8 * st, sdesc_sw128(sb + SM_KH + 2048u * st, 8192u, 1024u),
+                    mma_bf16_tmem_a(tmem + TM_S, tmem + TM_RA + 8 * st, sdesc_sw128(khb + 2048u * st, 8192u, 1024u),
                                     idesc_bf16(128, 128) | kIdescBMajorMN, 1u);
                 mma_commit(&bars[BAR_M34]);
-                pend |= 1u << BAR_M34;
             }
             if (!iok) {
                 atomicOr(p.err, kErrTimeout);
-                // Drain what was issued (bounded), so no MMA or copy is in flight at exit.
-                const uint32_t par = (uint32_t)(cc & 1);
-                for (int b = 0; b < BAR_N; ++b)
-                    if (pend & (1u << b)) (void)mbar_wait(&bars[b], b == BAR_TMA ? tpar : par, kWaitNs);
+                // Drain what was issued (bounded), so no MMA or copy is in flight at exit. At most
+                // one copy per TMA barrier is outstanding, so its phase parity is its chunk's.
+                mma_commit(&bars[BAR_DRAIN]);
+                (void)mbar_wait(&bars[BAR_DRAIN], 0, kWaitNs);
+                if (last_g >= 0) (void)mbar_wait(&bars[BAR_G], (uint32_t)(last_g & 1), kWaitNs);
+                if (last_qk >= 0) (void)mbar_wait(&bars[BAR_QK], (uint32_t)(last_qk & 1), kWaitNs);
+                if (last_v >= 0) (void)mbar_wait(&bars[BAR_V], (uint32_t)(last_v & 1), kWaitNs);
             }
         }
         __syncwarp();
+    } else if (warp >= kStateWarp0) {
+        // --------------------------------------------------------------- state warps --------
+        // Thread v = TMEM lane v = value column v of the state. Per chunk: bf16 copy of S for
+        // MMA1, S <- S Diag(gam_last), -(K+ S)^T and U^T as bf16 A operands, O write-back.
+        const int v = tid - NP;
+        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o);
+        bool ok = true;
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {  // initial state -> TMEM (fp32) and its bf16 copy
+            const int k0 = 32 * cb;
+            float buf[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) buf[i] = p.init ? __ldcs(p.init + state_off + (size_t)(k0 + i) * D + v) : 0.f;
+            tmem_st32(tmem + tq + TM_S + k0, buf);
+            uint32_t w[16];
+            pack32(buf, w, 1.f);
+            tmem_st16(tmem + tq + TM_SA + k0 / 2, w);
+        }
+        tmem_st_wait();
+
+        // O of a finished chunk (TMEM columns TM_D1 + 64 ..+63 = its 64 tokens) straight to
+        // global memory: each warp store covers 32 consecutive value columns (64 bytes).
+        auto store_o = [&](const float (&o0)[32], const float (&o1)[32], long long r0, int ln) {
+            __nv_bfloat16 *dst = og + ((size_t)r0 * H + h) * D + v;
+            const size_t rs = (size_t)H * D;  // elements between consecutive tokens
+            if (ln == C) {
+#pragma unroll
+                for (int r = 0; r < 32; ++r, dst += rs) *dst = __float2bfloat16_rn(o0[r]);
+#pragma unroll
+                for (int r = 0; r < 32; ++r, dst += rs) *dst = __float2bfloat16_rn(o1[r]);
+            } else {
+#pragma unroll
+                for (int r = 0; r < 32; ++r, dst += rs)
+                    if (r < ln) *dst = __float2bfloat16_rn(o0[r]);
+#pragma unroll
+                for (int r = 0; r < 32; ++r, dst += rs)
+                    if (32 + r < ln) *dst = __float2bfloat16_rn(o1[r]);
+            }
+        };
+
+        long long prev_row0 = 0;
+        int prev_len = 0;
+        int c = 0;
+#pragma unroll 1
+        for (; c < nchunks; ++c) {
+            const uint32_t par = (uint32_t)(c & 1);
+            const long long row0 = bos + (long long)c * C;
+            const int len = (int)min((long long)C, eos - row0);
+            float o0[32], o1[32];
+            if (c > 0) {
+                if (!(ok = state_wait(&bars[BAR_M34], par ^ 1u))) break;
+                tc_fence_after();
+                tmem_ld32(tmem + tq + TM_D1 + 64, o0);
+                tmem_ld32(tmem + tq + TM_D1 + 96, o1);
+                tmem_ld_wait();
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    float sv[32];
+                    tmem_ld32(tmem + tq + TM_S + 32 * cb, sv);
+                    tmem_ld_wait();
+                    uint32_t w[16];
+                    pack32(sv, w, 1.f);
+                    tmem_st16(tmem + tq + TM_SA + 16 * cb, w);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            mbar_arrive(&bars[BAR_SREADY]);
+            if (c > 0) store_o(o0, o1, prev_row0, prev_len);
+
+            // S <- S Diag(gam_last) while MMA1 reads the bf16 copy; TREADY also means that the
+            // prep warps have written gam_last of this chunk.
+            if (!(ok = state_wait(&bars[BAR_TREADY], par))) break;
+            {
+                const float *gc = gcs + 128 * par;
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    float sv[32];
+                    tmem_ld32(tmem + tq + TM_S + 32 * cb, sv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sv[i] *= gc[32 * cb + i];
+                    tmem_st32(tmem + tq + TM_S + 32 * cb, sv);
+                }
+                tmem_st_wait();
+            }
+
+            if (!(ok = state_wait(&bars[BAR_M1], par))) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                float ks[32];
+                tmem_ld32(tmem + tq + TM_D1 + 32 * hh, ks);
+                tmem_ld_wait();
+                uint32_t w[16];
+                pack32(ks, w, -1.f);
+                tmem_st16(tmem + tq + TM_RA + 16 * hh, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bars[BAR_RREADY]);
+
+            if (!(ok = state_wait(&bars[BAR_M2], par))) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                float u[32];
+                tmem_ld32(tmem + tq + TM_U + 32 * hh, u);
+                tmem_ld_wait();
+                uint32_t w[16];
+                pack32(u, w, 1.f);
+                tmem_st16(tmem + tq + TM_RA + 16 * hh, w);  // U^T replaces -(K+ S)^T (MMA2 has finished)
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bars[BAR_UREADY]);
+            prev_row0 = row0;
+            prev_len = len;
+        }
+        if (ok && nchunks > 0) {  // O of the last chunk
+            ok = state_wait(&bars[BAR_M34], (uint32_t)((nchunks - 1) & 1));
+            if (ok) {
+                tc_fence_after();
+                float o0[32], o1[32];
+                tmem_ld32(tmem + tq + TM_D1 + 64, o0);
+                tmem_ld32(tmem + tq + TM_D1 + 96, o1);
+                tmem_ld_wait();
+                store_o(o0, o1, prev_row0, prev_len);
+            }
+        }
+        if (ok) {
+            if (p.fin) {
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    float sv[32];
+                    tmem_ld32(tmem + tq + TM_S + 32 * cb, sv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) __stcs(p.fin + state_off + (size_t)(32 * cb + i) * D + v, sv[i]);
+                }
+            }
+        } else if (v == 0) {
+            atomicOr(p.err, kErrTimeout);
+        }
     } else {
-        // --------------------------------------------------------------- compute warps --------
+        // ---------------------------------------------------------------- prep warps --------
+        // Everything of a chunk that does not depend on the state: Gam, the decay-scaled
+        // operands, the A/P tiles, T = (I + A)^{-1} Diag(beta). Chunk c + 1 is built here while
+        // the state warps and the issuer run the state chain of chunk c.
+        const __nv_bfloat16 *bg = static_cast<const __nv_bfloat16 *>(p.beta);
         bool ok = true;
         // Operand mapping: channels 8j..8j+7, rows rlo + 8 * (4 * mh + m) for m = 0..3.
         const int rlo = lane & 7;
         const int j = 4 * (warp & 3) + (lane >> 3);
         const int mh = warp >> 2;
         float gm[4][8];  // Gam of the operand mapping's 4 rows x 8 channels (current chunk)
-        // Step 1 of chunk cc: wait for its q/k/g tiles, Gam = cumsum of g into gm, the reference
-        // rows and per-channel factors into shared memory, beta into sbeta. Runs for chunk c + 1
-        // while the last MMAs of chunk c are in flight. False if the TMA wait ran out.
+        // Step 1 of chunk cc: wait for its g tile, Gam = cumsum of g into gm, the reference rows
+        // and per-channel factors into shared memory, beta into sbeta. False if a wait ran out.
         auto step1 = [&](int cc) -> bool {
-        const long long r0 = bos + (long long)cc * C;
-        const int ln = (int)min((long long)C, eos - r0);
-        float bet = 0.f;
-        if (tid < C && tid < ln) bet = __bfloat162float(bg[(size_t)(r0 + tid) * H + h]);
-        if (!wait_all(&bars[BAR_TMA], (uint32_t)(cc & 1))) return false;
+            const long long r0 = bos + (long long)cc * C;
+            const int ln = (int)min((long long)C, eos - r0);
+            float bet = 0.f;
+            if (tid < C && tid < ln) bet = __bfloat162float(bg[(size_t)(r0 + tid) * H + h]);
+            if (!prep_wait(&bars[BAR_G], (uint32_t)(cc & 1))) return false;
 
-        // ---- 1. Gam = cumsum_r g within the chunk, per key channel --------------------------
-        // A warp holds 32 consecutive rows of 32 channels: scan over the 8 lanes of a row
-        // group with shuffles, then over the 4 row groups in registers; the second row half
-        // then adds Gam_31.
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int r = rlo + 8 * (4 * mh + m);
-            const uint4 w = *reinterpret_cast<const uint4 *>(sm + SM_G + tile_chunk(r, j));
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) gm[m][i] = r < ln ? ((i & 1) ? bf_hi(ww[i >> 1]) : bf_lo(ww[i >> 1])) : 0.f;
-        }
-#pragma unroll
-        for (int d = 1; d < 8; d <<= 1) {
+            // ---- 1. Gam = cumsum_r g within the chunk, per key channel ----------------------
+            // A warp holds 32 consecutive rows of 32 channels: scan over the 8 lanes of a row
+            // group with shuffles, then over the 4 row groups in registers; the second row half
+            // then adds Gam_31.
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
+                const int r = rlo + 8 * (4 * mh + m);
+                const uint4 w = *reinterpret_cast<const uint4 *>(sm + SM_G + tile_chunk(r, j));
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float t = __shfl_up_sync(0xffffffffu, gm[m][i], d, 8);
-                    if (rlo >= d) gm[m][i] += t;
+                for (int i = 0; i < 8; ++i) gm[m][i] = r < ln ? ((i & 1) ? bf_hi(ww[i >> 1]) : bf_lo(ww[i >> 1])) : 0.f;
+            }
+            mbar_arrive(&bars[BAR_GFREE]);  // this thread's g values are in registers
+#pragma unroll
+            for (int d = 1; d < 8; d <<= 1) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float t = __shfl_up_sync(0xffffffffu, gm[m][i], d, 8);
+                        if (rlo >= d) gm[m][i] += t;
+                    }
                 }
             }
-        }
-        {
-            float run[8];
+            {
+                float run[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) run[i] = 0.f;
+                for (int i = 0; i < 8; ++i) run[i] = 0.f;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
+                for (int m = 0; m < 4; ++m) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float total = __shfl_sync(0xffffffffu, gm[m][i], 7, 8);
-                    gm[m][i] += run[i];
-                    run[i] += total;
+                    for (int i = 0; i < 8; ++i) {
+                        const float total = __shfl_sync(0xffffffffu, gm[m][i], 7, 8);
+                        gm[m][i] += run[i];
+                        run[i] += total;
+                    }
                 }
             }
-        }
-        if (rlo == 7) {  // rows 15 and 31 of the half (half-local sums for the second half)
+            if (rlo == 7) {  // rows 15 and 31 of the half (half-local sums for the second half)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                refs[(2 * mh) * 128 + 8 * j + i] = gm[1][i];
-                refs[(2 * mh + 1) * 128 + 8 * j + i] = gm[3][i];
+                for (int i = 0; i < 8; ++i) {
+                    refs[(2 * mh) * 128 + 8 * j + i] = gm[1][i];
+                    refs[(2 * mh + 1) * 128 + 8 * j + i] = gm[3][i];
+                }
             }
-        }
-        if (tid < C) sbeta[tid] = bet;
-        sync_compute();
-        if (mh) {
+            if (tid < C) sbeta[tid] = bet;
+            prep_sync();
+            if (mh) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float g31 = refs[128 + 8 * j + i];
+                for (int i = 0; i < 8; ++i) {
+                    const float g31 = refs[128 + 8 * j + i];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) gm[m][i] += g31;
+                    for (int m = 0; m < 4; ++m) gm[m][i] += g31;
+                }
             }
-        }
-        if (tid < 128) {
-            const int ch = tid;
-            const float G15 = refs[ch], G31 = refs[128 + ch];
-            const float G47 = refs[256 + ch] + G31, G63 = refs[384 + ch] + G31;
-            cst[CST_M0 * 128 + ch] = G15;
-            cst[CST_M1 * 128 + ch] = G47;
-            cst[CST_C0 * 128 + ch] = ex2((G31 - G15) * kLog2e);
-            cst[CST_C1 * 128 + ch] = ex2((G47 - G31) * kLog2e);
-            cst[CST_EM0 * 128 + ch] = ex2(G15 * kLog2e);
-            cst[CST_EG31 * 128 + ch] = ex2(G31 * kLog2e);
-            cst[CST_E63M1 * 128 + ch] = ex2((G63 - G47) * kLog2e);
-            cst[CST_E63G31 * 128 + ch] = ex2((G63 - G31) * kLog2e);
-            cst[CST_GC * 128 + ch] = ex2(G63 * kLog2e);
-        }
-        sync_compute();
-
-        return true;
-    };
-
-        // O of a finished chunk (in TMEM columns 192..255) -> staging -> 16-byte coalesced stores.
-        auto write_o = [&](long long r0, int ln) {
-            float ov[32];
-            tmem_ld32(tmem + tq + TM_D1 + 64 + 32 * eh, ov);
-            tmem_ld_wait();
-            __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(sm + SM_OST);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ost[(32 * eh + i) * D + ev] = __float2bfloat16_rn(ov[i]);
-            sync_compute();
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int idx = tid + NT * q;  // 1024 chunks of 16 bytes: row idx / 16, chunk idx % 16
-                const int r = idx >> 4, c16 = idx & 15;
-                if (r < ln)
-                    *reinterpret_cast<uint4 *>(og + ((size_t)(r0 + r) * H + h) * D + 8 * c16) =
-                        *reinterpret_cast<const uint4 *>(sm + SM_OST + r * 256 + 16 * c16);
+            if (tid < 128) {
+                const int ch = tid;
+                const float G15 = refs[ch], G31 = refs[128 + ch];
+                const float G47 = refs[256 + ch] + G31, G63 = refs[384 + ch] + G31;
+                cst[CST_M0 * 128 + ch] = G15 * kLog2e;
+                cst[CST_M1 * 128 + ch] = G47 * kLog2e;
+                cst[CST_C0 * 128 + ch] = ex2((G31 - G15) * kLog2e);
+                cst[CST_C1 * 128 + ch] = ex2((G47 - G31) * kLog2e);
+                cst[CST_EM0 * 128 + ch] = ex2(G15 * kLog2e);
+                cst[CST_EG31 * 128 + ch] = ex2(G31 * kLog2e);
+                cst[CST_E63M1 * 128 + ch] = ex2((G63 - G47) * kLog2e);
+                cst[CST_E63G31 * 128 + ch] = ex2((G63 - G31) * kLog2e);
+                gcs[128 * (cc & 1) + ch] = ex2(G63 * kLog2e);
             }
+            prep_sync();
+            return true;
         };
 
-        int c = 0;
-        long long prev_row0 = 0;
-        int prev_len = 0;
         if (nchunks > 0) ok = step1(0);
 #pragma unroll 1
-        for (; ok && c < nchunks; ++c) {
+        for (int c = 0; ok && c < nchunks; ++c) {
             const uint32_t par = (uint32_t)(c & 1);
             const long long row0 = bos + (long long)c * C;
             const int len = (int)min((long long)C, eos - row0);
 
-        // ---- 2. decay-scaled operands -----------------------------------------------------
-        {
-            // Per-channel factors of this row half (see the exponent-range note at the top):
-            //   rows 0..31 : f = exp(Gam_r - Gam_15); off-tile column factor fi*c0 = exp(Gam_31 - Gam_r)
-            //   rows 32..63: f = exp(Gam_r - Gam_47); off-tile row factor    f*c1  = exp(Gam_r - Gam_31)
-            float ref[8], fo_c[8], pe[8], khe[8];
+            // ---- 2. decay-scaled operands (once MMA1 of the previous chunk has read [K+ ; Q+]) --
+            if (!(ok = prep_wait(&bars[BAR_QK], par))) break;
+            if (c > 0 && !(ok = prep_wait(&bars[BAR_KQFREE], par ^ 1u))) break;
+            if (mh)
+                build_operands<1>(sm, gm, cst, rlo, j, len, SM_KH + 16384u * par);
+            else
+                build_operands<0>(sm, gm, cst, rlo, j, len, SM_KH + 16384u * par);
+            fence_async_smem();
+            mbar_arrive(&bars[BAR_OPS]);
+
+            // ---- 3. A (fp32, for the solve) and P (bf16 operand) out of TMEM --------------------
+            // The diagonal tile (M = 128) holds row i of A (lanes 0..63) and of P (lanes 64..127);
+            // the off-diagonal tile (M = 64) holds its 64 rows in lanes 0..15 of each lane quarter:
+            // A rows 32..47, 48..63, then P rows 32..47, 48..63. P is overwritten only once MMA3 of
+            // the previous chunk has read it (its commit also covers MMA2, the reader of T).
+            if (!(ok = prep_wait(&bars[BAR_AP], par))) break;
+            if (c > 0 && !(ok = prep_wait(&bars[BAR_M34], par ^ 1u))) break;
+            tc_fence_after();
+            {
+                const int q = warp & 3;
+                float vals[32];
+                if (warp < 4) {
+                    const int L = 32 * q + lane;
+                    const int i = L & 63;
+                    const int j0 = (q & 1) ? 32 : 0;  // the diagonal half of row i
+                    tmem_ld32(tmem + tq + TM_AP + j0, vals);
+                    tmem_ld_wait();
+                    if (L < 64) {
+                        const float b = sbeta[i];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int ch = 8 * j + i;
-                ref[i] = cst[(mh ? CST_M1 : CST_M0) * 128 + ch];
-                fo_c[i] = cst[(mh ? CST_C1 : CST_C0) * 128 + ch];
-                pe[i] = cst[(mh ? CST_EG31 : CST_EM0) * 128 + ch];
-                khe[i] = cst[(mh ? CST_E63M1 : CST_E63G31) * 128 + ch];
-            }
+                        for (int k = 0; k < 32; k += 4) {
+                            float4 w;
+                            w.x = (j0 + k + 0 < i) ? vals[k + 0] * b : 0.f;
+                            w.y = (j0 + k + 1 < i) ? vals[k + 1] * b : 0.f;
+                            w.z = (j0 + k + 2 < i) ? vals[k + 2] * b : 0.f;
+                            w.w = (j0 + k + 3 < i) ? vals[k + 3] * b : 0.f;
+                            *reinterpret_cast<float4 *>(As + i * SA + j0 + k) = w;
+                        }
+                    } else {
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int r = rlo + 8 * (4 * mh + m);
-                const bool live = r < len;  // rows past the sequence end act as identity tokens
-                const uint4 kw = *reinterpret_cast<const uint4 *>(sm + SM_K + tile_chunk(r, j));
-                const uint4 qw = *reinterpret_cast<const uint4 *>(sm + SM_Q + tile_chunk(r, j));
-                const uint32_t kk[4] = {live ? kw.x : 0u, live ? kw.y : 0u, live ? kw.z : 0u, live ? kw.w : 0u};
-                const uint32_t qq[4] = {live ? qw.x : 0u, live ? qw.y : 0u, live ? qw.z : 0u, live ? qw.w : 0u};
-                float apk[8], apq[8], apb[8], ofr_k[8], ofr_q[8], kp[8], qp[8], kh[8];
+                        for (int k = 0; k < 32; ++k) vals[k] = (j0 + k <= i) ? vals[k] : 0.f;
+                        st_row32(sm + SM_P, i, j0, C, vals);
+                        if (j0 == 0) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float kv = (i & 1) ? bf_hi(kk[i >> 1]) : bf_lo(kk[i >> 1]);
-                    const float qv = (i & 1) ? bf_hi(qq[i >> 1]) : bf_lo(qq[i >> 1]);
-                    // |Gam_r - ref| <= 80 for g in [-5, 0]; the clamp only keeps factors finite
-                    // (no 0 * inf) for gates outside that range.
-                    const float e = fminf(fmaxf((gm[m][i] - ref[i]) * kLog2e, -126.f), 126.f);
-                    const float f = ex2(e), fi = ex2(-e);
-                    apk[i] = kv * f;
-                    apq[i] = qv * f;
-                    apb[i] = kv * fi;
-                    // Every other operand is one of these times a per-channel factor <= 1 (so the
-                    // product stays in range):
-                    if (mh) {                           // rows 32..63
-                        ofr_k[i] = apk[i] * fo_c[i];    // K exp(Gam_r - Gam_31): off-tile row
-                        ofr_q[i] = apq[i] * fo_c[i];    // Q exp(Gam_r - Gam_31)
-                        kp[i] = ofr_k[i] * pe[i];       // K exp(Gam_r)
-                        qp[i] = ofr_q[i] * pe[i];       // Q exp(Gam_r)
-                        kh[i] = apb[i] * khe[i];        // K exp(Gam_63 - Gam_r)
-                    } else {                            // rows 0..31
-                        ofr_k[i] = apb[i] * fo_c[i];    // K exp(Gam_31 - Gam_r): off-tile column
-                        ofr_q[i] = 0.f;
-                        kp[i] = apk[i] * pe[i];         // K exp(Gam_r)
-                        qp[i] = apq[i] * pe[i];         // Q exp(Gam_r)
-                        kh[i] = ofr_k[i] * khe[i];      // K exp(Gam_63 - Gam_r)
+                            for (int k = 0; k < 32; ++k) vals[k] = 0.f;
+                            st_row32(sm + SM_P, i, 32, C, vals);
+                        }
+                    }
+                } else {
+                    tmem_ld32(tmem + tq + TM_OFF, vals);
+                    tmem_ld_wait();
+                    if (lane < 16) {
+                        const int i = 32 + 16 * (q & 1) + lane;
+                        if (q < 2) {
+                            const float b = sbeta[i];
+#pragma unroll
+                            for (int k = 0; k < 32; k += 4)
+                                *reinterpret_cast<float4 *>(As + i * SA + k) =
+                                    make_float4(vals[k] * b, vals[k + 1] * b, vals[k + 2] * b, vals[k + 3] * b);
+                        } else {
+                            st_row32(sm + SM_P, i, 0, C, vals);
+                        }
                     }
                 }
-                st_chunk(sm, SM_AP + kmajor_offset(r, 8 * j, D), apk);
-                st_chunk(sm, SM_AP + kmajor_offset(64 + r, 8 * j, D), apq);
-                st_chunk(sm, SM_APB + kmajor_offset(r, 8 * j, D), apb);
-                st_chunk(sm, SM_OFF + kmajor_offset(r, 8 * j, D), ofr_k);
-                if (mh) st_chunk(sm, SM_OFF + kmajor_offset(64 + r, 8 * j, D), ofr_q);
-                st_chunk(sm, SM_KQ + kmajor_offset(r, 8 * j, D), kp);
-                st_chunk(sm, SM_KQ + kmajor_offset(64 + r, 8 * j, D), qp);
-                st_chunk(sm, SM_KH + tile_chunk(r, j), kh);  // row-major: MMA4 reads it MN-major
             }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        mbar_arrive(&bars[BAR_OPS]);
+            prep_sync();
 
-        // ---- 2b. while the intra-chunk tiles run: O of the previous chunk, then the bf16 copy
-        //          of the state for MMA1 (the initial state's copy was made before the loop).
-        if (c > 0) {
-            write_o(prev_row0, prev_len);
-#pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-                const int k0 = 64 * eh + 32 * cb;
-                float sv[32];
-                tmem_ld32(tmem + tq + TM_S + k0, sv);
-                tmem_ld_wait();
-                uint32_t w[16];
-                pack32(sv, w, 1.f);
-                tmem_st16(tmem + tq + TM_SA + k0 / 2, w);
-            }
-            tmem_st_wait();
-        }
-        tc_fence_before();
-        mbar_arrive(&bars[BAR_SREADY]);
-
-        // ---- 3. the state decay runs in the shadow of the intra-chunk tiles -----------------
-        // S <- S Diag(gam_last): the state in TMEM is next read by MMA4 of this chunk.
-#pragma unroll 1
-        for (int cb = 0; cb < 2; ++cb) {
-            const int k0 = 64 * eh + 32 * cb;
-            float sv[32];
-            tmem_ld32(tmem + tq + TM_S + k0, sv);
-            tmem_ld_wait();
+            // ---- 4. X = (I + A)^{-1}, written to T = X Diag(beta) as it completes ---------------
+            // (a) warp b < 4 inverts the 16 x 16 diagonal block b by doubling: four 4 x 4 blocks
+            //     in closed form, then 4 -> 8 -> 16 merges X21 = -X22 (A21 X11); warps 4..7 zero
+            //     the strictly-upper blocks of T and the two upper blocks of X the merges read.
+            if (warp < 4) {
+                const int B0 = 16 * warp;
+                float *Yw = reinterpret_cast<float *>(sm + SM_Y) + warp * (16 * 17);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sv[i] *= cst[CST_GC * 128 + k0 + i];
-            tmem_st32(tmem + tq + TM_S + k0, sv);
-        }
-        tmem_st_wait();
-
-        // ---- 4. A (fp32, for the solve) and P (bf16 operand) out of TMEM -------------------
-        if (!(ok = wait_all(&bars[BAR_AP], par))) break;
-        tc_fence_after();
-        {
-            const int L = 32 * (warp & 3) + lane;
-            const int i = L & 63;
-            const bool pside = L >= 64;
-            const int jh = warp >> 2;
-            float vals[32];
-            if (jh == 0) {
-                tmem_ld32(tmem + tq + ((i < 32) ? TM_AP : TM_OFF), vals);
-                tmem_ld_wait();
-            } else if (i >= 32) {
-                tmem_ld32(tmem + tq + TM_AP + 32, vals);
-                tmem_ld_wait();
-            } else {
-#pragma unroll
-                for (int q = 0; q < 32; ++q) vals[q] = 0.f;
-            }
-            const int j0 = 32 * jh;
-            if (!pside) {
-                const float b = sbeta[i];
-#pragma unroll
-                for (int q = 0; q < 32; q += 4) {
-                    float4 w;
-                    w.x = (j0 + q + 0 < i) ? vals[q + 0] * b : 0.f;
-                    w.y = (j0 + q + 1 < i) ? vals[q + 1] * b : 0.f;
-                    w.z = (j0 + q + 2 < i) ? vals[q + 2] * b : 0.f;
-                    w.w = (j0 + q + 3 < i) ? vals[q + 3] * b : 0.f;
-                    *reinterpret_cast<float4 *>(As + i * SA + j0 + q) = w;
+                for (int q = 0; q < 3; ++q) {  // zero the upper 4 x 4 blocks of the diagonal block
+                    const int e = lane + 32 * q;   // 96 entries: 6 blocks x 16
+                    const int blk = e >> 4, rr = (e >> 2) & 3, cc = e & 3;
+                    const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                    const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                    Xs[(B0 + 4 * bi + rr) * SA + B0 + 4 * bj + cc] = 0.f;
                 }
-            } else {
-#pragma unroll
-                for (int q = 0; q < 32; ++q) vals[q] = (j0 + q <= i) ? vals[q] : 0.f;
-                st_row32(sm + SM_P, i, j0, C, vals);
-            }
-        }
-        sync_compute();
-
-        // ---- 5. X = (I + A)^{-1}, written to T = X Diag(beta) as it completes ------------------
-        // (a) warp b < 4 inverts the 16 x 16 diagonal block b by doubling: four 4 x 4 blocks in
-        //     closed form, then 4 -> 8 -> 16 merges X21 = -X22 (A21 X11); warps 4..7 zero the
-        //     strictly-upper blocks of T and the two upper blocks of X the merges read.
-        if (warp < 4) {
-            const int B0 = 16 * warp;
-            float *Yw = reinterpret_cast<float *>(sm + SM_Y) + warp * (16 * 17);
-#pragma unroll
-            for (int q = 0; q < 3; ++q) {  // zero the upper 4 x 4 blocks of the diagonal block
-                const int e = lane + 32 * q;   // 96 entries: 6 blocks x 16
-                const int blk = e >> 4, rr = (e >> 2) & 3, cc = e & 3;
-                const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                Xs[(B0 + 4 * bi + rr) * SA + B0 + 4 * bj + cc] = 0.f;
-            }
-            if (lane < 4) {  // 4 x 4 unit lower-triangular inverse in closed form
-                const int o = B0 + 4 * lane;
-                const float a10 = As[(o + 1) * SA + o], a20 = As[(o + 2) * SA + o], a21 = As[(o + 2) * SA + o + 1];
-                const float a30 = As[(o + 3) * SA + o], a31 = As[(o + 3) * SA + o + 1], a32 = As[(o + 3) * SA + o + 2];
-                const float x10 = -a10, x21 = -a21, x32 = -a32;
-                const float x20 = -fmaf(a21, x10, a20);
-                const float x31 = -fmaf(a32, x21, a31);
-                const float x30 = -fmaf(a32, x20, fmaf(a31, x10, a30));
-                float *X0 = Xs + o * SA + o;
-                X0[0] = 1.f;      X0[1] = 0.f;      X0[2] = 0.f;      X0[3] = 0.f;
-                X0[SA] = x10;     X0[SA + 1] = 1.f; X0[SA + 2] = 0.f; X0[SA + 3] = 0.f;
-                X0[2 * SA] = x20; X0[2 * SA + 1] = x21; X0[2 * SA + 2] = 1.f; X0[2 * SA + 3] = 0.f;
-                X0[3 * SA] = x30; X0[3 * SA + 1] = x31; X0[3 * SA + 2] = x32; X0[3 * SA + 3] = 1.f;
-            }
-            __syncwarp();
-            {  // 4 -> 8: lane = (half q, row r, column c) of the two 4 x 4 blocks X21
-                const int q = lane >> 4, r = (lane >> 2) & 3, cc = lane & 3;
-                const int o = B0 + 8 * q;
-                float y = 0.f;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) y = fmaf(As[(o + 4 + r) * SA + o + m], Xs[(o + m) * SA + o + cc], y);
-                Yw[(4 * q + r) * 17 + cc] = y;
+                if (lane < 4) {  // 4 x 4 unit lower-triangular inverse in closed form
+                    const int o = B0 + 4 * lane;
+                    const float a10 = As[(o + 1) * SA + o], a20 = As[(o + 2) * SA + o], a21 = As[(o + 2) * SA + o + 1];
+                    const float a30 = As[(o + 3) * SA + o], a31 = As[(o + 3) * SA + o + 1], a32 = As[(o + 3) * SA + o + 2];
+                    const float x10 = -a10, x21 = -a21, x32 = -a32;
+                    const float x20 = -fmaf(a21, x10, a20);
+                    const float x31 = -fmaf(a32, x21, a31);
+                    const float x30 = -fmaf(a32, x20, fmaf(a31, x10, a30));
+                    float *X0 = Xs + o * SA + o;
+                    X0[0] = 1.f;      X0[1] = 0.f;      X0[2] = 0.f;      X0[3] = 0.f;
+                    X0[SA] = x10;     X0[SA + 1] = 1.f; X0[SA + 2] = 0.f; X0[SA + 3] = 0.f;
+                    X0[2 * SA] = x20; X0[2 * SA + 1] = x21; X0[2 * SA + 2] = 1.f; X0[2 * SA + 3] = 0.f;
+                    X0[3 * SA] = x30; X0[3 * SA + 1] = x31; X0[3 * SA + 2] = x32; X0[3 * SA + 3] = 1.f;
+                }
                 __syncwarp();
-                float x = 0.f;
+                {  // 4 -> 8: lane = (half q, row r, column c) of the two 4 x 4 blocks X21
+                    const int q = lane >> 4, r = (lane >> 2) & 3, cc = lane & 3;
+                    const int o = B0 + 8 * q;
+                    float y = 0.f;
 #pragma unroll
-                for (int m = 0; m < 4; ++m) x = fmaf(Xs[(o + 4 + r) * SA + o + 4 + m], Yw[(4 * q + m) * 17 + cc], x);
-                Xs[(o + 4 + r) * SA + o + cc] = -x;
-            }
-            __syncwarp();
-            {  // 8 -> 16: X21 (8 x 8), two entries per lane
-                const int r = lane >> 2, c0 = (lane & 3) * 2;
-                float y0 = 0.f, y1 = 0.f;
+                    for (int m = 0; m < 4; ++m) y = fmaf(As[(o + 4 + r) * SA + o + m], Xs[(o + m) * SA + o + cc], y);
+                    Yw[(4 * q + r) * 17 + cc] = y;
+                    __syncwarp();
+                    float x = 0.f;
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const float am = As[(B0 + 8 + r) * SA + B0 + m];
-                    y0 = fmaf(am, Xs[(B0 + m) * SA + B0 + c0], y0);
-                    y1 = fmaf(am, Xs[(B0 + m) * SA + B0 + c0 + 1], y1);
+                    for (int m = 0; m < 4; ++m) x = fmaf(Xs[(o + 4 + r) * SA + o + 4 + m], Yw[(4 * q + m) * 17 + cc], x);
+                    Xs[(o + 4 + r) * SA + o + cc] = -x;
                 }
-                Yw[r * 17 + c0] = y0;
-                Yw[r * 17 + c0 + 1] = y1;
                 __syncwarp();
-                float x0 = 0.f, x1 = 0.f;
+                {  // 8 -> 16: X21 (8 x 8), two entries per lane
+                    const int r = lane >> 2, c0 = (lane & 3) * 2;
+                    float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const float xm = Xs[(B0 + 8 + r) * SA + B0 + 8 + m];
-                    x0 = fmaf(xm, Yw[m * 17 + c0], x0);
-                    x1 = fmaf(xm, Yw[m * 17 + c0 + 1], x1);
+                    for (int m = 0; m < 8; ++m) {
+                        const float am = As[(B0 + 8 + r) * SA + B0 + m];
+                        y0 = fmaf(am, Xs[(B0 + m) * SA + B0 + c0], y0);
+                        y1 = fmaf(am, Xs[(B0 + m) * SA + B0 + c0 + 1], y1);
+                    }
+                    Yw[r * 17 + c0] = y0;
+                    Yw[r * 17 + c0 + 1] = y1;
+                    __syncwarp();
+                    float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        const float xm = Xs[(B0 + 8 + r) * SA + B0 + 8 + m];
+                        x0 = fmaf(xm, Yw[m * 17 + c0], x0);
+                        x1 = fmaf(xm, Yw[m * 17 + c0 + 1], x1);
+                    }
+                    Xs[(B0 + 8 + r) * SA + B0 + c0] = -x0;
+                    Xs[(B0 + 8 + r) * SA + B0 + c0 + 1] = -x1;
                 }
-                Xs[(B0 + 8 + r) * SA + B0 + c0] = -x0;
-                Xs[(B0 + 8 + r) * SA + B0 + c0 + 1] = -x1;
-            }
-            __syncwarp();
-            {  // T of the diagonal block: one 16-byte chunk (row r, 8 columns) per lane
-                const int r = lane >> 1, h8 = (lane & 1) * 8;
-                float tv[8];
+                __syncwarp();
+                {  // T of the diagonal block: one 16-byte chunk (row r, 8 columns) per lane
+                    const int r = lane >> 1, h8 = (lane & 1) * 8;
+                    float tv[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) tv[q] = Xs[(B0 + r) * SA + B0 + h8 + q] * sbeta[B0 + h8 + q];
-                st_chunk(sm, SM_T + kmajor_offset(B0 + r, B0 + h8, C), tv);
-            }
-        } else {
-            const int z = tid - 128;  // 0..127
-            // X rows 0..15 cols 16..31 and rows 32..47 cols 48..63 (read by the 32 -> 64 merge)
-            const int blk = z >> 6, rr = (z & 63) >> 2, cq = (z & 3) * 4;
-            *reinterpret_cast<float4 *>(Xs + (32 * blk + rr) * SA + 32 * blk + 16 + cq) = make_float4(0.f, 0.f, 0.f, 0.f);
-            // T: the six strictly-upper 16 x 16 blocks (192 chunks of 16 bytes)
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int e = z + 128 * q;
-                if (e < 192) {
-                    const int bi = e >> 5, r2 = (e & 31) >> 1, hf = e & 1;
-                    const int I = bi < 3 ? 0 : (bi < 5 ? 1 : 2);
-                    const int J = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
-                    *reinterpret_cast<uint4 *>(sm + SM_T + kmajor_offset(16 * I + r2, 16 * J + 8 * hf, C)) =
-                        make_uint4(0u, 0u, 0u, 0u);
+                    for (int q = 0; q < 8; ++q) tv[q] = Xs[(B0 + r) * SA + B0 + h8 + q] * sbeta[B0 + h8 + q];
+                    st_chunk(sm, SM_T + kmajor_offset(B0 + r, B0 + h8, C), tv);
                 }
-            }
-        }
-        sync_compute();
-        // (b) 16 -> 32: warp (p, nt) < 4 computes column tile nt of X_{2p+1,2p} (tf32 mma)
-        if (warp < 4) {
-            const int pp = warp >> 1, nt = warp & 1;
-            const int I = 2 * pp + 1, J = 2 * pp;
-            float *Yb = reinterpret_cast<float *>(sm + SM_Y + 4352) + 16 * pp * SA;
-            float acc[4];
-            warp_mma_16x8<16>(acc, As + 16 * I * SA + 16 * J, SA, Xs + 16 * J * SA + 16 * J + 8 * nt, SA, lane);
-            warp_store_16x8(Yb + 8 * nt, SA, acc, 1.f, lane);
-            __syncwarp();
-            warp_mma_16x8<16>(acc, Xs + 16 * I * SA + 16 * I, SA, Yb + 8 * nt, SA, lane);
-            warp_store_16x8(Xs + 16 * I * SA + 16 * J + 8 * nt, SA, acc, -1.f, lane);
-            store_t_16x8(sm + SM_T, 16 * I, 16 * J + 8 * nt, acc, sbeta, lane);
-        }
-        sync_compute();
-        // (c) 32 -> 64: X_BA = -X_BB A_BA X_AA with 32 x 32 blocks; warp w owns one 16 x 8 tile.
-        {
-            const int mt = warp >> 2, nt = warp & 3;
-            float *Y = reinterpret_cast<float *>(sm + SM_Y + 4352);
-            float acc[4];
-            warp_mma_16x8<32>(acc, As + (32 + 16 * mt) * SA, SA, Xs + 8 * nt, SA, lane);
-            warp_store_16x8(Y + 16 * mt * SA + 8 * nt, SA, acc, 1.f, lane);
-            sync_compute();
-            warp_mma_16x8<32>(acc, Xs + (32 + 16 * mt) * SA + 32, SA, Y + 8 * nt, SA, lane);
-            store_t_16x8(sm + SM_T, 32 + 16 * mt, 8 * nt, acc, sbeta, lane);
-        }
-
-        // ---- 6. U = T V - T (K+ S): -(K+ S)^T goes to TMEM as MMA2's second A operand ----------
-        fence_async_smem();  // the T stores of the solve
-        mbar_arrive(&bars[BAR_TREADY]);
-        if (!(ok = wait_all(&bars[BAR_M1], par))) break;
-        tc_fence_after();
-        {
-            float ks[32];
-            tmem_ld32(tmem + tq + TM_D1 + 32 * eh, ks);
-            tmem_ld_wait();
-            uint32_t w[16];
-            pack32(ks, w, -1.f);
-            tmem_st16(tmem + tq + TM_RA + 16 * eh, w);
-            tmem_st_wait();
-        }
-        tc_fence_before();
-        mbar_arrive(&bars[BAR_RREADY]);
-
-        if (!(ok = wait_all(&bars[BAR_M2], par))) break;
-        tc_fence_after();
-        {
-            float u[32];
-            tmem_ld32(tmem + tq + TM_U + 32 * eh, u);
-            tmem_ld_wait();
-            uint32_t w[16];
-            pack32(u, w, 1.f);
-            tmem_st16(tmem + tq + TM_RA + 16 * eh, w);  // U^T replaces -(K+ S)^T (MMA2 has finished)
-            tmem_st_wait();
-        }
-        tc_fence_before();
-        mbar_arrive(&bars[BAR_UREADY]);
-
-        if (c + 1 < nchunks && !(ok = step1(c + 1))) break;
-        if (!(ok = wait_all(&bars[BAR_M34], par))) break;
-        tc_fence_after();
-
-        prev_row0 = row0;
-        prev_len = len;
-        }
-
-        if (ok && nchunks > 0) write_o(prev_row0, prev_len);  // O of the last chunk
-        if (ok) {
-            if (p.fin) {
-#pragma unroll 1
-                for (int cb = 0; cb < 2; ++cb) {
-                    const int k0 = 64 * eh + 32 * cb;
-                    float sv[32];
-                    tmem_ld32(tmem + tq + TM_S + k0, sv);
-                    tmem_ld_wait();
+            } else {
+                const int z = tid - 128;  // 0..127
+                // X rows 0..15 cols 16..31 and rows 32..47 cols 48..63 (read by the 32 -> 64 merge)
+                const int blk = z >> 6, rr = (z & 63) >> 2, cq = (z & 3) * 4;
+                *reinterpret_cast<float4 *>(Xs + (32 * blk + rr) * SA + 32 * blk + 16 + cq) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
+                // T: the six strictly-upper 16 x 16 blocks (192 chunks of 16 bytes)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) __stcs(p.fin + state_off + (size_t)(k0 + i) * D + ev, sv[i]);
+                for (int q = 0; q < 2; ++q) {
+                    const int e = z + 128 * q;
+                    if (e < 192) {
+                        const int bi = e >> 5, r2 = (e & 31) >> 1, hf = e & 1;
+                        const int I = bi < 3 ? 0 : (bi < 5 ? 1 : 2);
+                        const int J = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
+                        *reinterpret_cast<uint4 *>(sm + SM_T + kmajor_offset(16 * I + r2, 16 * J + 8 * hf, C)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
             }
-        } else if (tid == 0) {
-            atomicOr(p.err, kErrTimeout);
+            prep_sync();
+            // (b) 16 -> 32: warp (p, nt) < 4 computes column tile nt of X_{2p+1,2p} (tf32 mma)
+            if (warp < 4) {
+                const int pp = warp >> 1, nt = warp & 1;
+                const int I = 2 * pp + 1, J = 2 * pp;
+                float *Yb = reinterpret_cast<float *>(sm + SM_Y + 4352) + 16 * pp * SA;
+                float acc[4];
+                warp_mma_16x8<16>(acc, As + 16 * I * SA + 16 * J, SA, Xs + 16 * J * SA + 16 * J + 8 * nt, SA, lane);
+                warp_store_16x8(Yb + 8 * nt, SA, acc, 1.f, lane);
+                __syncwarp();
+                warp_mma_16x8<16>(acc, Xs + 16 * I * SA + 16 * I, SA, Yb + 8 * nt, SA, lane);
+                warp_store_16x8(Xs + 16 * I * SA + 16 * J + 8 * nt, SA, acc, -1.f, lane);
+                store_t_16x8(sm + SM_T, 16 * I, 16 * J + 8 * nt, acc, sbeta, lane);
+            }
+            prep_sync();
+            // (c) 32 -> 64: X_BA = -X_BB A_BA X_AA with 32 x 32 blocks; warp w owns one 16 x 8 tile.
+            {
+                const int mt = warp >> 2, nt = warp & 3;
+                float *Y = reinterpret_cast<float *>(sm + SM_Y + 4352);
+                float acc[4];
+                warp_mma_16x8<32>(acc, As + (32 + 16 * mt) * SA, SA, Xs + 8 * nt, SA, lane);
+                warp_store_16x8(Y + 16 * mt * SA + 8 * nt, SA, acc, 1.f, lane);
+                prep_sync();
+                warp_mma_16x8<32>(acc, Xs + (32 + 16 * mt) * SA + 32, SA, Y + 8 * nt, SA, lane);
+                store_t_16x8(sm + SM_T, 32 + 16 * mt, 8 * nt, acc, sbeta, lane);
+            }
+            fence_async_smem();  // the T and P stores
+            mbar_arrive(&bars[BAR_TREADY]);
+
+            if (c + 1 < nchunks && !(ok = step1(c + 1))) break;
         }
+        if (!ok && tid == 0) atomicOr(p.err, kErrTimeout);
     }
     tc_fence_before();
     __syncthreads();
