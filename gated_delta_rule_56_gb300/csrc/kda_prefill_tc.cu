@@ -233,18 +233,6 @@ __device__ __forceinline__ void prep_sync() { group_sync<1, NP>(); }
 __device__ __forceinline__ bool prep_wait(uint64_t *bar, uint32_t parity) { return group_wait<1, NP>(bar, parity); }
 __device__ __forceinline__ bool state_wait(uint64_t *bar, uint32_t parity) { return group_wait<2, NS>(bar, parity); }
 
-// Issue `steps` K-steps of one MMA (both operands K-major no-swizzle in shared memory).
-__device__ __forceinline__ void issue_mma(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, int K, int steps,
-                                          uint32_t idesc, bool accumulate) {
-    const uint32_t sbo = (uint32_t)K * 16u;
-#pragma unroll 1
-    for (int s = 0; s < steps; ++s) {
-        const uint64_t a = sdesc(a_smem + 256u * s, 128u, sbo);
-        const uint64_t b = sdesc(b_smem + 256u * s, 128u, sbo);
-        mma_bf16(d_tmem, a, b, idesc, (accumulate || s > 0) ? 1u : 0u);
-    }
-}
-
 // Decay-scaled bf16 operands of one row half (MH = 0: rows 0..31, MH = 1: rows 32..63) for a
 // thread's 4 rows rlo + 8 * (4 * MH + m) x 8 channels 8j..8j+7; gm holds Gam of those entries.
 // Per-channel factors (see the exponent-range note at the top):
@@ -373,111 +361,137 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (warp == kIssuer) {
         // ---------------------------------------------------------------- issuer warp --------
-        // One thread walks the chunks in the order the work becomes ready: the chunk-parallel
-        // MMAs of chunk c (their operands come from the prep warps), then the state chain of
-        // chunk c (MMA1, MMA2, MMA3/4) while the prep warps already build chunk c + 1.
-        if (lane == 0) {
-            bool iok = true;
-            int last_g = -1, last_qk = -1, last_v = -1;  // chunk of the latest copy on each barrier
-            auto load_g = [&](int cc) {
-                const int r = (int)(bos + (long long)cc * C);
+        // The whole warp walks the chunks (one elected lane issues each MMA and copy) in the
+        // order the work becomes ready: the chunk-parallel MMAs of chunk c (their operands come
+        // from the prep warps), then the state chain of chunk c (MMA1, MMA2, MMA3/4) while the
+        // prep warps already build chunk c + 1. Every K step is unrolled and its descriptor is a
+        // constant step from the first.
+        auto wait = [&](int b, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(&bars[b], parity, kWaitNs));
+        };
+        bool iok = true;
+        int last_g = -1, last_qk = -1, last_v = -1;  // chunk of the latest copy on each barrier
+        auto load_g = [&](int cc) {
+            const int r = (int)(bos + (long long)cc * C);
+            if (elect_one()) {
                 mbar_arrive_expect_tx(&bars[BAR_G], 16384);
                 tma_load_3d(sm + SM_G, &maps.g, &bars[BAR_G], 0, h, r);
                 tma_load_3d(sm + SM_G + 8192, &maps.g, &bars[BAR_G], 64, h, r);
-                last_g = cc;
-            };
-            auto load_qk = [&](int cc) {
-                const int r = (int)(bos + (long long)cc * C);
+            }
+            __syncwarp();
+            last_g = cc;
+        };
+        auto load_qk = [&](int cc) {
+            const int r = (int)(bos + (long long)cc * C);
+            if (elect_one()) {
                 mbar_arrive_expect_tx(&bars[BAR_QK], 32768);
                 for (int b = 0; b < 2; ++b) {
                     tma_load_3d(sm + SM_Q + 8192 * b, &maps.q, &bars[BAR_QK], 64 * b, h, r);
                     tma_load_3d(sm + SM_K + 8192 * b, &maps.k, &bars[BAR_QK], 64 * b, h, r);
                 }
-                last_qk = cc;
-            };
-            auto load_v = [&](int cc) {
-                const int r = (int)(bos + (long long)cc * C);
+            }
+            __syncwarp();
+            last_qk = cc;
+        };
+        auto load_v = [&](int cc) {
+            const int r = (int)(bos + (long long)cc * C);
+            if (elect_one()) {
                 mbar_arrive_expect_tx(&bars[BAR_V], 16384);
                 tma_load_3d(sm + SM_VT, &maps.v, &bars[BAR_V], 0, h, r);
                 tma_load_3d(sm + SM_VT + 8192, &maps.v, &bars[BAR_V], 64, h, r);
-                last_v = cc;
-            };
-            if (nchunks > 0) {
-                load_g(0);
-                load_qk(0);
-                load_v(0);
             }
+            __syncwarp();
+            last_v = cc;
+        };
+        // First-step descriptors of every operand.
+        const uint64_t d_ap = sdesc(sb + SM_AP, 128u, 2048u), d_apb = sdesc(sb + SM_APB, 128u, 2048u);
+        const uint64_t d_offa = sdesc(sb + SM_OFF, 128u, 2048u), d_offb = sdesc(sb + SM_OFFB, 128u, 2048u);
+        const uint64_t d_k = sdesc(sb + SM_KQ, 128u, 2048u), d_q = sdesc(sb + SM_KQ + 16384u, 128u, 2048u);
+        const uint64_t d_v = sdesc_sw128(sb + SM_VT, 8192u, 1024u);
+        const uint64_t d_t = sdesc(sb + SM_T, 128u, 1024u), d_p = sdesc(sb + SM_P, 128u, 1024u);
+        const uint64_t d_kh0 = sdesc_sw128(sb + SM_KH, 8192u, 1024u);
+        const uint64_t d_kh1 = sdesc_sw128(sb + SM_KH + 16384u, 8192u, 1024u);
+        if (nchunks > 0) {
+            load_g(0);
+            load_qk(0);
+            load_v(0);
+        }
 #pragma unroll 1
-            for (int cc = 0; cc < nchunks; ++cc) {
-                const uint32_t par = (uint32_t)(cc & 1);
-                const bool more = cc + 1 < nchunks;
-                // chunk-parallel part: the g tile is read -> fetch the next one; the operands are
-                // built -> A/P tiles, and the q/k tiles are free for the next chunk.
-                if (!(iok = mbar_wait(&bars[BAR_GFREE], par, kWaitNs))) break;
-                if (more) load_g(cc + 1);
-                if (!(iok = mbar_wait(&bars[BAR_OPS], par, kWaitNs))) break;
-                tc_fence_after();
-                issue_mma(tmem + TM_AP, sb + SM_AP, sb + SM_APB, D, D / 16, idesc_bf16(128, 64), false);
-                issue_mma(tmem + TM_OFF, sb + SM_OFF, sb + SM_OFFB, D, D / 16, idesc_bf16(64, 32), false);
-                mma_commit(&bars[BAR_AP]);
-                if (more) load_qk(cc + 1);
-                // state chain. U^T = V^T T^T first (V tile as an MN-major A operand) ...
-                if (!(iok = mbar_wait(&bars[BAR_TREADY], par, kWaitNs))) break;
-                if (!(iok = mbar_wait(&bars[BAR_V], par, kWaitNs))) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int st = 0; st < C / 16; ++st)
-                    mma_bf16(tmem + TM_U, sdesc_sw128(sb + SM_VT + 2048u * st, 8192u, 1024u),
-                             sdesc(sb + SM_T + 256u * st, 128u, 1024u), idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
-                // ... MMA1 = S^T [K+ ; Q+]^T from the bf16 state copy, the K+ half committed first ...
-                if (!(iok = mbar_wait(&bars[BAR_SREADY], par, kWaitNs))) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int st = 0; st < D / 16; ++st)
-                    mma_bf16_tmem_a(tmem + TM_D1, tmem + TM_SA + 8 * st, sdesc(sb + SM_KQ + 256u * st, 128u, 2048u),
-                                    idesc_bf16(128, 64), st > 0);
-                mma_commit(&bars[BAR_M1]);
-#pragma unroll 1
-                for (int st = 0; st < D / 16; ++st)
-                    mma_bf16_tmem_a(tmem + TM_D1 + 64, tmem + TM_SA + 8 * st,
-                                    sdesc(sb + SM_KQ + 16384u + 256u * st, 128u, 2048u), idesc_bf16(128, 64), st > 0);
-                mma_commit(&bars[BAR_KQFREE]);
-                // ... U^T += -(K+ S)^T T^T (A from TMEM) ...
-                if (!(iok = mbar_wait(&bars[BAR_RREADY], par, kWaitNs))) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int st = 0; st < C / 16; ++st)
-                    mma_bf16_tmem_a(tmem + TM_U, tmem + TM_RA + 8 * st, sdesc(sb + SM_T + 256u * st, 128u, 1024u),
-                                    idesc_bf16(128, 64), 1u);
-                mma_commit(&bars[BAR_M2]);
-                if (more) {  // the v tile is consumed: fetch the next one
-                    if (!(iok = mbar_wait(&bars[BAR_M2], par, kWaitNs))) break;
-                    load_v(cc + 1);
-                }
-                // ... then O^T += U^T P^T and S^T += U^T Khat.
-                if (!(iok = mbar_wait(&bars[BAR_UREADY], par, kWaitNs))) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int st = 0; st < C / 16; ++st)
-                    mma_bf16_tmem_a(tmem + TM_D1 + 64, tmem + TM_RA + 8 * st, sdesc(sb + SM_P + 256u * st, 128u, 1024u),
-                                    idesc_bf16(128, 64), 1u);
-                const uint32_t khb = sb + SM_KH + 16384u * par;
-#pragma unroll 1
-                for (int st = 0; st < C / 16; ++st)
-                    mma_bf16_tmem_a(tmem + TM_S, tmem + TM_RA + 8 * st, sdesc_sw128(khb + 2048u * st, 8192u, 1024u),
-                                    idesc_bf16(128, 128) | kIdescBMajorMN, 1u);
-                mma_commit(&bars[BAR_M34]);
+        for (int cc = 0; cc < nchunks; ++cc) {
+            const uint32_t par = (uint32_t)(cc & 1);
+            const bool more = cc + 1 < nchunks;
+            // chunk-parallel part: the g tile is read -> fetch the next one; the operands are
+            // built -> A/P tiles, and the q/k tiles are free for the next chunk.
+            if (!(iok = wait(BAR_GFREE, par))) break;
+            if (more) load_g(cc + 1);
+            if (!(iok = wait(BAR_OPS, par))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < D / 16; ++st)
+                mma_bf16_warp(tmem + TM_AP, d_ap + kDescStepKmajor * st, d_apb + kDescStepKmajor * st,
+                              idesc_bf16(128, 64), st > 0);
+#pragma unroll
+            for (int st = 0; st < D / 16; ++st)
+                mma_bf16_warp(tmem + TM_OFF, d_offa + kDescStepKmajor * st, d_offb + kDescStepKmajor * st,
+                              idesc_bf16(64, 32), st > 0);
+            mma_commit_warp(&bars[BAR_AP]);
+            if (more) load_qk(cc + 1);
+            // state chain. U^T = V^T T^T first (V tile as an MN-major A operand) ...
+            if (!(iok = wait(BAR_TREADY, par))) break;
+            if (!(iok = wait(BAR_V, par))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < C / 16; ++st)
+                mma_bf16_warp(tmem + TM_U, d_v + kDescStepMN128 * st, d_t + kDescStepKmajor * st,
+                              idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
+            // ... MMA1 = S^T [K+ ; Q+]^T from the bf16 state copy, the K+ half committed first ...
+            if (!(iok = wait(BAR_SREADY, par))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < D / 16; ++st)
+                mma_bf16_tmem_a_warp(tmem + TM_D1, tmem + TM_SA + 8 * st, d_k + kDescStepKmajor * st,
+                                     idesc_bf16(128, 64), st > 0);
+            mma_commit_warp(&bars[BAR_M1]);
+#pragma unroll
+            for (int st = 0; st < D / 16; ++st)
+                mma_bf16_tmem_a_warp(tmem + TM_D1 + 64, tmem + TM_SA + 8 * st, d_q + kDescStepKmajor * st,
+                                     idesc_bf16(128, 64), st > 0);
+            mma_commit_warp(&bars[BAR_KQFREE]);
+            // ... U^T += -(K+ S)^T T^T (A from TMEM) ...
+            if (!(iok = wait(BAR_RREADY, par))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < C / 16; ++st)
+                mma_bf16_tmem_a_warp(tmem + TM_U, tmem + TM_RA + 8 * st, d_t + kDescStepKmajor * st,
+                                     idesc_bf16(128, 64), 1u);
+            mma_commit_warp(&bars[BAR_M2]);
+            if (more) {  // the v tile is consumed: fetch the next one
+                if (!(iok = wait(BAR_M2, par))) break;
+                load_v(cc + 1);
             }
-            if (!iok) {
-                atomicOr(p.err, kErrTimeout);
-                // Drain what was issued (bounded), so no MMA or copy is in flight at exit. At most
-                // one copy per TMA barrier is outstanding, so its phase parity is its chunk's.
-                mma_commit(&bars[BAR_DRAIN]);
-                (void)mbar_wait(&bars[BAR_DRAIN], 0, kWaitNs);
-                if (last_g >= 0) (void)mbar_wait(&bars[BAR_G], (uint32_t)(last_g & 1), kWaitNs);
-                if (last_qk >= 0) (void)mbar_wait(&bars[BAR_QK], (uint32_t)(last_qk & 1), kWaitNs);
-                if (last_v >= 0) (void)mbar_wait(&bars[BAR_V], (uint32_t)(last_v & 1), kWaitNs);
-            }
+            // ... then O^T += U^T P^T and S^T += U^T Khat.
+            if (!(iok = wait(BAR_UREADY, par))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < C / 16; ++st)
+                mma_bf16_tmem_a_warp(tmem + TM_D1 + 64, tmem + TM_RA + 8 * st, d_p + kDescStepKmajor * st,
+                                     idesc_bf16(128, 64), 1u);
+            const uint64_t d_kh = par ? d_kh1 : d_kh0;
+#pragma unroll
+            for (int st = 0; st < C / 16; ++st)
+                mma_bf16_tmem_a_warp(tmem + TM_S, tmem + TM_RA + 8 * st, d_kh + kDescStepMN128 * st,
+                                     idesc_bf16(128, 128) | kIdescBMajorMN, 1u);
+            mma_commit_warp(&bars[BAR_M34]);
+        }
+        if (!iok) {
+            if (lane == 0) atomicOr(p.err, kErrTimeout);
+            // Drain what was issued (bounded), so no MMA or copy is in flight at exit. At most one
+            // copy per TMA barrier is outstanding, so its phase parity is its chunk's.
+            mma_commit_warp(&bars[BAR_DRAIN]);
+            (void)mbar_wait(&bars[BAR_DRAIN], 0, kWaitNs);
+            if (last_g >= 0) (void)mbar_wait(&bars[BAR_G], (uint32_t)(last_g & 1), kWaitNs);
+            if (last_qk >= 0) (void)mbar_wait(&bars[BAR_QK], (uint32_t)(last_qk & 1), kWaitNs);
+            if (last_v >= 0) (void)mbar_wait(&bars[BAR_V], (uint32_t)(last_v & 1), kWaitNs);
         }
         __syncwarp();
     } else if (warp >= kStateWarp0) {
