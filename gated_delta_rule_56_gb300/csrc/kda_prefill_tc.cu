@@ -86,9 +86,9 @@ constexpr uint32_t SM_VT = SM_OFF + 24576;                // v tile (TMA, like q
 constexpr uint32_t SM_MISC = SM_VT + 16384;
 constexpr uint32_t SM_REF = SM_MISC;                      // fp32 [4][128]: Gam_15, Gam_31, Gam_47, Gam_63
 constexpr uint32_t SM_CST = SM_REF + 2048;                // fp32 [8][128] per-channel factors
-constexpr uint32_t SM_GC = SM_CST + 4096;                 // fp32 [2][128] gam_last, by chunk parity
-constexpr uint32_t SM_BETA = SM_GC + 1024;                // fp32 [64]
-constexpr uint32_t SM_BAR = SM_BETA + 256;                // mbarriers
+constexpr uint32_t SM_GC = SM_CST + 4096;                 // fp32 [3][128] gam_last, by chunk index mod 3
+constexpr uint32_t SM_BETA = SM_GC + 1536;                // fp32 [2][64] beta, by chunk parity
+constexpr uint32_t SM_BAR = SM_BETA + 512;                // mbarriers
 constexpr uint32_t SM_TPTR = SM_BAR + 256;                // TMEM base address
 constexpr uint32_t SM_USED = SM_TPTR + 16;
 constexpr uint32_t SMEM_BYTES = SM_USED + 1024;           // + alignment slack
@@ -105,13 +105,12 @@ static_assert(CST_N * 512 <= 4096, "factor rows overflow SM_CST");
 constexpr uint32_t TM_AP = 0, TM_OFF = 64, TM_RA = 96, TM_D1 = 128, TM_U = 256, TM_S = 320, TM_SA = 448;
 constexpr uint32_t TM_COLS = 512;
 
-// Barriers. Up to BAR_DRAIN: TMA copies and MMA commits (one arrival). BAR_GFREE .. BAR_TREADY:
-// the prep warps have read the g tile / built the intra-chunk operands / written T and P (NP
-// arrivals). BAR_SREADY .. BAR_UREADY: the state warps have made the bf16 state copy (and read
+// Barriers. Up to BAR_DRAIN: TMA copies and MMA commits (one arrival). BAR_OPS, BAR_TREADY: the
+// prep warps have built the intra-chunk operands / written T and P (NP arrivals). BAR_SREADY .. BAR_UREADY: the state warps have made the bf16 state copy (and read
 // out O of the previous chunk) / -(K+ S)^T / U^T (NS arrivals).
 enum {
     BAR_G = 0, BAR_QK, BAR_V, BAR_AP, BAR_M1, BAR_KQFREE, BAR_M2, BAR_M34, BAR_DRAIN,
-    BAR_GFREE, BAR_OPS, BAR_TREADY,
+    BAR_OPS, BAR_TREADY,
     BAR_SREADY, BAR_RREADY, BAR_UREADY,
     BAR_N
 };
@@ -343,7 +342,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     if (tid == 32) {
         for (int b = 0; b < BAR_N; ++b)
-            mbar_init(&bars[b], b < BAR_GFREE ? 1 : (b < BAR_SREADY ? NP : NS));
+            mbar_init(&bars[b], b < BAR_OPS ? 1 : (b < BAR_SREADY ? NP : NS));
         fence_mbar_init();
     }
     if (tid == 64) {
@@ -365,7 +364,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // order the work becomes ready: the chunk-parallel MMAs of chunk c (their operands come
         // from the prep warps), then the state chain of chunk c (MMA1, MMA2, MMA3/4) while the
         // prep warps already build chunk c + 1. Every K step is unrolled and its descriptor is a
-        // constant step from the first.
+        // constant step from the first. The g tiles after the first are fetched by the prep warps.
         auto wait = [&](int b, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, mbar_wait(&bars[b], parity, kWaitNs));
         };
@@ -420,10 +419,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int cc = 0; cc < nchunks; ++cc) {
             const uint32_t par = (uint32_t)(cc & 1);
             const bool more = cc + 1 < nchunks;
-            // chunk-parallel part: the g tile is read -> fetch the next one; the operands are
-            // built -> A/P tiles, and the q/k tiles are free for the next chunk.
-            if (!(iok = wait(BAR_GFREE, par))) break;
-            if (more) load_g(cc + 1);
+            // chunk-parallel part: the operands are built -> A/P tiles, and the q/k tiles are free
+            // for the next chunk.
             if (!(iok = wait(BAR_OPS, par))) break;
             tc_fence_after();
 #pragma unroll
@@ -568,7 +565,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // prep warps have written gam_last of this chunk.
             if (!(ok = state_wait(&bars[BAR_TREADY], par))) break;
             {
-                const float *gc = gcs + 128 * par;
+                const float *gc = gcs + 128 * (c % 3);
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     float sv[32];
@@ -650,14 +647,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int j = 4 * (warp & 3) + (lane >> 3);
         const int mh = warp >> 2;
         float gm[4][8];  // Gam of the operand mapping's 4 rows x 8 channels (current chunk)
+        int g_inflight = -1;  // chunk of a g-tile copy issued here and not yet waited for
         // Step 1 of chunk cc: wait for its g tile, Gam = cumsum of g into gm, the reference rows
-        // and per-channel factors into shared memory, beta into sbeta. False if a wait ran out.
+        // and per-channel factors into shared memory, beta into its sbeta buffer; then fetch the
+        // next g tile. Runs while the A/P MMAs of chunk cc - 1 are in flight. False if a wait ran
+        // out.
         auto step1 = [&](int cc) -> bool {
             const long long r0 = bos + (long long)cc * C;
             const int ln = (int)min((long long)C, eos - r0);
             float bet = 0.f;
             if (tid < C && tid < ln) bet = __bfloat162float(bg[(size_t)(r0 + tid) * H + h]);
             if (!prep_wait(&bars[BAR_G], (uint32_t)(cc & 1))) return false;
+            g_inflight = -1;
 
             // ---- 1. Gam = cumsum_r g within the chunk, per key channel ----------------------
             // A warp holds 32 consecutive rows of 32 channels: scan over the 8 lanes of a row
@@ -671,7 +672,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) gm[m][i] = r < ln ? ((i & 1) ? bf_hi(ww[i >> 1]) : bf_lo(ww[i >> 1])) : 0.f;
             }
-            mbar_arrive(&bars[BAR_GFREE]);  // this thread's g values are in registers
 #pragma unroll
             for (int d = 1; d < 8; d <<= 1) {
 #pragma unroll
@@ -704,8 +704,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     refs[(2 * mh + 1) * 128 + 8 * j + i] = gm[3][i];
                 }
             }
-            if (tid < C) sbeta[tid] = bet;
+            if (tid < C) sbeta[64 * (cc & 1) + tid] = bet;
             prep_sync();
+            if (tid == 0 && cc + 1 < nchunks) {  // every prep thread has read the g tile
+                const int r = (int)(bos + (long long)(cc + 1) * C);
+                mbar_arrive_expect_tx(&bars[BAR_G], 16384);
+                tma_load_3d(sm + SM_G, &maps.g, &bars[BAR_G], 0, h, r);
+                tma_load_3d(sm + SM_G + 8192, &maps.g, &bars[BAR_G], 64, h, r);
+                g_inflight = cc + 1;
+            }
             if (mh) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -726,7 +733,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 cst[CST_EG31 * 128 + ch] = ex2(G31 * kLog2e);
                 cst[CST_E63M1 * 128 + ch] = ex2((G63 - G47) * kLog2e);
                 cst[CST_E63G31 * 128 + ch] = ex2((G63 - G31) * kLog2e);
-                gcs[128 * (cc & 1) + ch] = ex2(G63 * kLog2e);
+                gcs[128 * (cc % 3) + ch] = ex2(G63 * kLog2e);
             }
             prep_sync();
             return true;
@@ -749,6 +756,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             fence_async_smem();
             mbar_arrive(&bars[BAR_OPS]);
 
+            // ---- step 1 of the next chunk while the A/P MMAs run --------------------------------
+            if (c + 1 < nchunks && !(ok = step1(c + 1))) break;
+            const float *sbc = sbeta + 64 * par;  // beta of this chunk
+
             // ---- 3. A (fp32, for the solve) and P (bf16 operand) out of TMEM --------------------
             // The diagonal tile (M = 128) holds row i of A (lanes 0..63) and of P (lanes 64..127);
             // the off-diagonal tile (M = 64) holds its 64 rows in lanes 0..15 of each lane quarter:
@@ -767,7 +778,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tmem_ld32(tmem + tq + TM_AP + j0, vals);
                     tmem_ld_wait();
                     if (L < 64) {
-                        const float b = sbeta[i];
+                        const float b = sbc[i];
 #pragma unroll
                         for (int k = 0; k < 32; k += 4) {
                             float4 w;
@@ -793,7 +804,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (lane < 16) {
                         const int i = 32 + 16 * (q & 1) + lane;
                         if (q < 2) {
-                            const float b = sbeta[i];
+                            const float b = sbc[i];
 #pragma unroll
                             for (int k = 0; k < 32; k += 4)
                                 *reinterpret_cast<float4 *>(As + i * SA + k) =
@@ -877,7 +888,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int r = lane >> 1, h8 = (lane & 1) * 8;
                     float tv[8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) tv[q] = Xs[(B0 + r) * SA + B0 + h8 + q] * sbeta[B0 + h8 + q];
+                    for (int q = 0; q < 8; ++q) tv[q] = Xs[(B0 + r) * SA + B0 + h8 + q] * sbc[B0 + h8 + q];
                     st_chunk(sm, SM_T + kmajor_offset(B0 + r, B0 + h8, C), tv);
                 }
             } else {
@@ -911,7 +922,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 warp_mma_16x8<16>(acc, Xs + 16 * I * SA + 16 * I, SA, Yb + 8 * nt, SA, lane);
                 warp_store_16x8(Xs + 16 * I * SA + 16 * J + 8 * nt, SA, acc, -1.f, lane);
-                store_t_16x8(sm + SM_T, 16 * I, 16 * J + 8 * nt, acc, sbeta, lane);
+                store_t_16x8(sm + SM_T, 16 * I, 16 * J + 8 * nt, acc, sbc, lane);
             }
             prep_sync();
             // (c) 32 -> 64: X_BA = -X_BB A_BA X_AA with 32 x 32 blocks; warp w owns one 16 x 8 tile.
@@ -923,14 +934,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 warp_store_16x8(Y + 16 * mt * SA + 8 * nt, SA, acc, 1.f, lane);
                 prep_sync();
                 warp_mma_16x8<32>(acc, Xs + (32 + 16 * mt) * SA + 32, SA, Y + 8 * nt, SA, lane);
-                store_t_16x8(sm + SM_T, 32 + 16 * mt, 8 * nt, acc, sbeta, lane);
+                store_t_16x8(sm + SM_T, 32 + 16 * mt, 8 * nt, acc, sbc, lane);
             }
             fence_async_smem();  // the T and P stores
             mbar_arrive(&bars[BAR_TREADY]);
-
-            if (c + 1 < nchunks && !(ok = step1(c + 1))) break;
         }
-        if (!ok && tid == 0) atomicOr(p.err, kErrTimeout);
+        if (!ok && tid == 0) {
+            atomicOr(p.err, kErrTimeout);
+            if (g_inflight >= 0) (void)mbar_wait(&bars[BAR_G], (uint32_t)(g_inflight & 1), kWaitNs);
+        }
     }
     tc_fence_before();
     __syncthreads();
