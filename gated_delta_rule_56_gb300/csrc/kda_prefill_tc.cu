@@ -433,15 +433,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                               idesc_bf16(64, 32), st > 0);
             mma_commit_warp(&bars[BAR_AP]);
             if (more) load_qk(cc + 1);
-            // state chain. U^T = V^T T^T first (V tile as an MN-major A operand) ...
-            if (!(iok = wait(BAR_TREADY, par))) break;
-            if (!(iok = wait(BAR_V, par))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int st = 0; st < C / 16; ++st)
-                mma_bf16_warp(tmem + TM_U, d_v + kDescStepMN128 * st, d_t + kDescStepKmajor * st,
-                              idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
-            // ... MMA1 = S^T [K+ ; Q+]^T from the bf16 state copy, the K+ half committed first ...
+            // state chain. MMA1 = S^T [K+ ; Q+]^T from the bf16 state copy as soon as the operands
+            // and the copy exist, the K+ half committed first ...
             if (!(iok = wait(BAR_SREADY, par))) break;
             tc_fence_after();
 #pragma unroll
@@ -454,6 +447,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mma_bf16_tmem_a_warp(tmem + TM_D1 + 64, tmem + TM_SA + 8 * st, d_q + kDescStepKmajor * st,
                                      idesc_bf16(128, 64), st > 0);
             mma_commit_warp(&bars[BAR_KQFREE]);
+            // ... U^T = V^T T^T once T exists (V tile as an MN-major A operand) ...
+            if (!(iok = wait(BAR_TREADY, par))) break;
+            if (!(iok = wait(BAR_V, par))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < C / 16; ++st)
+                mma_bf16_warp(tmem + TM_U, d_v + kDescStepMN128 * st, d_t + kDescStepKmajor * st,
+                              idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
             // ... U^T += -(K+ S)^T T^T (A from TMEM) ...
             if (!(iok = wait(BAR_RREADY, par))) break;
             tc_fence_after();
@@ -557,13 +558,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 tmem_st_wait();
             }
+            // OPS of chunk c: its operands, and gam_last written by its step 1, are in place. Waited
+            // before SREADY, so OPS of chunk c + 1 (which needs MMA1 of chunk c) cannot have
+            // completed yet and the parity cannot alias.
+            if (!(ok = state_wait(&bars[BAR_OPS], par))) break;
             tc_fence_before();
             mbar_arrive(&bars[BAR_SREADY]);
             if (c > 0) store_o(o0, o1, prev_row0, prev_len);
 
-            // S <- S Diag(gam_last) while MMA1 reads the bf16 copy; TREADY also means that the
-            // prep warps have written gam_last of this chunk.
-            if (!(ok = state_wait(&bars[BAR_TREADY], par))) break;
+            // S <- S Diag(gam_last) while MMA1 reads the bf16 copy.
             {
                 const float *gc = gcs + 128 * (c % 3);
 #pragma unroll 1
@@ -648,6 +651,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int mh = warp >> 2;
         float gm[4][8];  // Gam of the operand mapping's 4 rows x 8 channels (current chunk)
         int g_inflight = -1;  // chunk of a g-tile copy issued here and not yet waited for
+        // beta of token tid of a chunk, loaded one step ahead (raw bf16 bits, converted when used)
+        auto load_beta = [&](int cc) -> uint32_t {
+            const long long r0 = bos + (long long)cc * C;
+            if (tid < C && r0 + tid < eos)
+                return *reinterpret_cast<const uint16_t *>(bg + (size_t)(r0 + tid) * H + h);
+            return 0u;
+        };
+        uint32_t beta_next = nchunks > 0 ? load_beta(0) : 0u;
         // Step 1 of chunk cc: wait for its g tile, Gam = cumsum of g into gm, the reference rows
         // and per-channel factors into shared memory, beta into its sbeta buffer; then fetch the
         // next g tile. Runs while the A/P MMAs of chunk cc - 1 are in flight. False if a wait ran
@@ -655,8 +666,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         auto step1 = [&](int cc) -> bool {
             const long long r0 = bos + (long long)cc * C;
             const int ln = (int)min((long long)C, eos - r0);
-            float bet = 0.f;
-            if (tid < C && tid < ln) bet = __bfloat162float(bg[(size_t)(r0 + tid) * H + h]);
+            const float bet = __uint_as_float(beta_next << 16);
+            if (cc + 1 < nchunks) beta_next = load_beta(cc + 1);
             if (!prep_wait(&bars[BAR_G], (uint32_t)(cc & 1))) return false;
             g_inflight = -1;
 
