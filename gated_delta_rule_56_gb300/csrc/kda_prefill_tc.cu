@@ -68,24 +68,27 @@ constexpr int NTHREADS = NP + NS + 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
 
-// Shared memory map (bytes from a 1024-byte aligned base).
+// Shared memory map (bytes from a 1024-byte aligned base). The decay-scaled operands (and the TMA
+// tiles) use the 128-byte-swizzled K-major layout: in an R-row operand, the 16-byte chunk (row r,
+// channels 8j..8j+7) sits at sw_chunk(r, j, R) (rows of 128 B = 64 channels, 8-row atoms of 1 KB,
+// the second 64 channels R * 128 bytes further on), so the 8 chunks of one row are bank-free.
 constexpr uint32_t SM_Q = 0, SM_K = 16384, SM_G = 32768;  // TMA tiles, 2 boxes x (64 rows x 128 B)
 constexpr uint32_t SM_KH = 49152;                         // Khat, two buffers of [64 rows x 128 ch] (TMA layout)
-constexpr uint32_t SM_KQ = SM_KH + 32768;                 // [K+ ; Q+] operand  [128 x 128]
+constexpr uint32_t SM_KQ = SM_KH + 32768;                 // [K+ ; Q+] operand  [128 rows x 128]
 constexpr uint32_t SM_T = SM_KQ + 32768;                  // T operand          [64 x 64]
 constexpr uint32_t SM_P = SM_T + 8192;                    // P operand          [64 x 64]
-constexpr uint32_t SM_AP = SM_P + 8192;                   // [K*f ; Q*f]        [128 x 128]
-constexpr uint32_t SM_APB = SM_AP + 32768;                // K/f                [64 x 128]
+constexpr uint32_t SM_AP = SM_P + 8192;                   // [K*f ; Q*f]        [128 rows x 128]
+constexpr uint32_t SM_APB = SM_AP + 32768;                // K/f                [64 rows x 128]
 constexpr uint32_t SA = 68;                               // row stride (floats) of A and X
 constexpr uint32_t SM_AS = SM_AP;                         //   then A  fp32 [64 x 68]
 constexpr uint32_t SM_X = SM_AP + 64 * SA * 4;            //   then X = (I+A)^{-1} fp32 [64 x 68]
-constexpr uint32_t SM_OFF = SM_AP + 49152;                // off tile: A operand [64 x 128] ...
-constexpr uint32_t SM_OFFB = SM_OFF + 16384;              //   ... and B operand [32 x 128]
+constexpr uint32_t SM_OFF = SM_AP + 49152;                // off tile: A operand [64 rows x 128] ...
+constexpr uint32_t SM_OFFB = SM_OFF + 16384;              //   ... and B operand [32 rows x 128]
 constexpr uint32_t SM_Y = SM_OFF;                         //   then solve scratch fp32
 constexpr uint32_t SM_VT = SM_OFF + 24576;                // v tile (TMA, like q/k/g)
 constexpr uint32_t SM_MISC = SM_VT + 16384;
-constexpr uint32_t SM_REF = SM_MISC;                      // fp32 [4][128]: Gam_15, Gam_31, Gam_47, Gam_63
-constexpr uint32_t SM_CST = SM_REF + 2048;                // fp32 [8][128] per-channel factors
+constexpr uint32_t SM_WT = SM_MISC;                       // fp32 [4][128]: sums of g over each 16-row block
+constexpr uint32_t SM_CST = SM_WT + 2048;                // fp32 [8][128] per-channel factors
 constexpr uint32_t SM_GC = SM_CST + 4096;                 // fp32 [3][128] gam_last, by chunk index mod 3
 constexpr uint32_t SM_BETA = SM_GC + 1536;                // fp32 [2][64] beta, by chunk parity
 constexpr uint32_t SM_BAR = SM_BETA + 512;                // mbarriers
@@ -94,7 +97,9 @@ constexpr uint32_t SM_USED = SM_TPTR + 16;
 constexpr uint32_t SMEM_BYTES = SM_USED + 1024;           // + alignment slack
 static_assert(SM_X + 64 * SA * 4 <= SM_OFF, "solve buffers overflow their region");
 static_assert(SM_Y + 4352 + 32 * SA * 4 <= SM_VT, "solve scratch overflows its region");
-static_assert(SM_KH % 1024 == 0 && SM_VT % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(SM_KH % 1024 == 0 && SM_KQ % 1024 == 0 && SM_AP % 1024 == 0 && SM_APB % 1024 == 0 &&
+                  SM_OFF % 1024 == 0 && SM_OFFB % 1024 == 0 && SM_VT % 1024 == 0,
+              "swizzled tiles need 1024-byte alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // Per-channel factor rows in SM_CST.
@@ -106,12 +111,13 @@ constexpr uint32_t TM_AP = 0, TM_OFF = 64, TM_RA = 96, TM_D1 = 128, TM_U = 256, 
 constexpr uint32_t TM_COLS = 512;
 
 // Barriers. Up to BAR_DRAIN: TMA copies and MMA commits (one arrival). BAR_OPS, BAR_TREADY: the
-// prep warps have built the intra-chunk operands / written T and P (NP arrivals). BAR_SREADY .. BAR_UREADY: the state warps have made the bf16 state copy (and read
-// out O of the previous chunk) / -(K+ S)^T / U^T (NS arrivals).
+// prep warps have built the intra-chunk operands / written T (NP arrivals). BAR_SREADY ..
+// BAR_EPIDONE: the state warps have made the bf16 state copy (and read out O of the previous
+// chunk) / -(K+ S)^T / U^T / A, P and the diagonal blocks of the inverse (NS arrivals).
 enum {
     BAR_G = 0, BAR_QK, BAR_V, BAR_AP, BAR_M1, BAR_KQFREE, BAR_M2, BAR_M34, BAR_DRAIN,
     BAR_OPS, BAR_TREADY,
-    BAR_SREADY, BAR_RREADY, BAR_UREADY,
+    BAR_SREADY, BAR_RREADY, BAR_UREADY, BAR_EPIDONE,
     BAR_N
 };
 static_assert(BAR_N * 8 <= 256, "barrier region");
@@ -125,11 +131,12 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Offset of the 16-byte chunk (row r, channels 8j..8j+7) in a 64-row TMA tile stored as two
-// 64-channel boxes with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t tile_chunk(int r, int j) {
-    return (uint32_t)((j >> 3) * 8192 + r * 128 + (((j & 7) ^ (r & 7)) << 4));
+// Offset of the 16-byte chunk (row r, channels 8j..8j+7) in an R-row operand in the 128-byte
+// swizzled K-major layout (a 64-row TMA tile of two 64-channel boxes is the R = 64 case).
+__device__ __forceinline__ uint32_t sw_chunk(int r, int j, int R) {
+    return (uint32_t)((j >> 3) * (R * 128) + (r >> 3) * 1024 + (r & 7) * 128 + (((j & 7) ^ (r & 7)) << 4));
 }
+__device__ __forceinline__ uint32_t tile_chunk(int r, int j) { return sw_chunk(r, j, 64); }
 
 __device__ __forceinline__ void st_chunk(uint8_t *base, uint32_t off, const float (&v)[8]) {
     uint4 w;
@@ -231,16 +238,17 @@ __device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity) {
 __device__ __forceinline__ void prep_sync() { group_sync<1, NP>(); }
 __device__ __forceinline__ bool prep_wait(uint64_t *bar, uint32_t parity) { return group_wait<1, NP>(bar, parity); }
 __device__ __forceinline__ bool state_wait(uint64_t *bar, uint32_t parity) { return group_wait<2, NS>(bar, parity); }
+__device__ __forceinline__ void state_sync() { group_sync<2, NS>(); }
 
 // Decay-scaled bf16 operands of one row half (MH = 0: rows 0..31, MH = 1: rows 32..63) for a
-// thread's 4 rows rlo + 8 * (4 * MH + m) x 8 channels 8j..8j+7; gm holds Gam of those entries.
+// thread's 4 rows r0..r0+3 x 8 channels 8j..8j+7; gm holds Gam of those entries.
 // Per-channel factors (see the exponent-range note at the top):
 //   rows 0..31 : f = exp(Gam_r - Gam_15); off-tile column factor fi*c0 = exp(Gam_31 - Gam_r)
 //   rows 32..63: f = exp(Gam_r - Gam_47); off-tile row factor    f*c1  = exp(Gam_r - Gam_31)
 // Every other operand is one of K f, Q f, K / f times a per-channel factor <= 1, so each
 // product stays in range. Rows past the sequence end (r >= len) act as identity tokens.
 template <int MH>
-__device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4][8], const float *cst, int rlo,
+__device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4][8], const float *cst, int r0,
                                                int j, int len, uint32_t khb) {
     float ref[8], fo_c[8], pe[8], khe[8];
 #pragma unroll
@@ -253,7 +261,7 @@ __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4]
     }
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        const int r = rlo + 8 * (4 * MH + m);
+        const int r = r0 + m;
         const bool live = r < len;
         const uint4 kw = *reinterpret_cast<const uint4 *>(sm + SM_K + tile_chunk(r, j));
         const uint4 qw = *reinterpret_cast<const uint4 *>(sm + SM_Q + tile_chunk(r, j));
@@ -284,18 +292,166 @@ __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4]
                 kh[i] = ofr_k[i] * khe[i];    // K exp(Gam_63 - Gam_r)
             }
         }
-        st_chunk(sm, SM_AP + kmajor_offset(r, 8 * j, D), apk);
-        st_chunk(sm, SM_AP + kmajor_offset(64 + r, 8 * j, D), apq);
-        st_chunk(sm, SM_APB + kmajor_offset(r, 8 * j, D), apb);
+        st_chunk(sm, SM_AP + sw_chunk(r, j, 128), apk);
+        st_chunk(sm, SM_AP + sw_chunk(64 + r, j, 128), apq);
+        st_chunk(sm, SM_APB + sw_chunk(r, j, 64), apb);
         if (MH) {  // off-tile A operand: rows 0..31 the K side, 32..63 the Q side
-            st_chunk(sm, SM_OFF + kmajor_offset(r - 32, 8 * j, D), ofr_k);
-            st_chunk(sm, SM_OFF + kmajor_offset(r, 8 * j, D), ofr_q);
+            st_chunk(sm, SM_OFF + sw_chunk(r - 32, j, 64), ofr_k);
+            st_chunk(sm, SM_OFF + sw_chunk(r, j, 64), ofr_q);
         } else {   // off-tile B operand
-            st_chunk(sm, SM_OFFB + kmajor_offset(r, 8 * j, D), ofr_k);
+            st_chunk(sm, SM_OFFB + sw_chunk(r, j, 32), ofr_k);
         }
-        st_chunk(sm, SM_KQ + kmajor_offset(r, 8 * j, D), kp);
-        st_chunk(sm, SM_KQ + kmajor_offset(64 + r, 8 * j, D), qp);
-        st_chunk(sm, khb + tile_chunk(r, j), kh);  // row-major: MMA4 reads it MN-major
+        st_chunk(sm, SM_KQ + sw_chunk(r, j, 128), kp);
+        st_chunk(sm, SM_KQ + sw_chunk(64 + r, j, 128), qp);
+        st_chunk(sm, khb + tile_chunk(r, j), kh);  // the same layout: MMA4 reads it MN-major
+    }
+}
+
+// Read the A/P tiles of TMEM lane quarter q (one warp) into A (fp32, strictly lower, rows scaled
+// by beta) and the P operand (bf16, lower triangle). The diagonal tile (M = 128) holds row i of A
+// (lanes 0..63) and of P (lanes 64..127); the off-diagonal tile (M = 64) holds its 64 rows in
+// lanes 0..15 of each lane quarter: A rows 32..47, 48..63, then P rows 32..47, 48..63.
+__device__ __forceinline__ void ap_readout(uint8_t *sm, float *As, uint32_t tmem_q, int q, int lane,
+                                           const float *sbc) {
+    float vals[32];
+    {
+        const int L = 32 * q + lane;
+        const int i = L & 63;
+        const int j0 = (q & 1) ? 32 : 0;  // the diagonal half of row i
+        tmem_ld32(tmem_q + TM_AP + j0, vals);
+        tmem_ld_wait();
+        if (L < 64) {
+            const float b = sbc[i];
+#pragma unroll
+            for (int k = 0; k < 32; k += 4) {
+                float4 w;
+                w.x = (j0 + k + 0 < i) ? vals[k + 0] * b : 0.f;
+                w.y = (j0 + k + 1 < i) ? vals[k + 1] * b : 0.f;
+                w.z = (j0 + k + 2 < i) ? vals[k + 2] * b : 0.f;
+                w.w = (j0 + k + 3 < i) ? vals[k + 3] * b : 0.f;
+                *reinterpret_cast<float4 *>(As + i * SA + j0 + k) = w;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) vals[k] = (j0 + k <= i) ? vals[k] : 0.f;
+            st_row32(sm + SM_P, i, j0, C, vals);
+            if (j0 == 0) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) vals[k] = 0.f;
+                st_row32(sm + SM_P, i, 32, C, vals);
+            }
+        }
+    }
+    tmem_ld32(tmem_q + TM_OFF, vals);
+    tmem_ld_wait();
+    if (lane < 16) {
+        const int i = 32 + 16 * (q & 1) + lane;
+        if (q < 2) {
+            const float b = sbc[i];
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+                *reinterpret_cast<float4 *>(As + i * SA + k) =
+                    make_float4(vals[k] * b, vals[k + 1] * b, vals[k + 2] * b, vals[k + 3] * b);
+        } else {
+            st_row32(sm + SM_P, i, 0, C, vals);
+        }
+    }
+}
+
+// (I + A)^{-1} on the 16 x 16 diagonal block w (one warp), by doubling: four 4 x 4 blocks in
+// closed form, then 4 -> 8 -> 16 merges X21 = -X22 (A21 X11); then its block of T = X Diag(beta).
+__device__ __forceinline__ void solve_diag_block(uint8_t *sm, const float *As, float *Xs, int warp, int lane,
+                                                 const float *sbc) {
+    const int B0 = 16 * warp;
+    float *Yw = reinterpret_cast<float *>(sm + SM_Y) + warp * (16 * 17);
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {  // zero the upper 4 x 4 blocks of the diagonal block
+        const int e = lane + 32 * q;   // 96 entries: 6 blocks x 16
+        const int blk = e >> 4, rr = (e >> 2) & 3, cc = e & 3;
+        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        Xs[(B0 + 4 * bi + rr) * SA + B0 + 4 * bj + cc] = 0.f;
+    }
+    if (lane < 4) {  // 4 x 4 unit lower-triangular inverse in closed form
+        const int o = B0 + 4 * lane;
+        const float a10 = As[(o + 1) * SA + o], a20 = As[(o + 2) * SA + o], a21 = As[(o + 2) * SA + o + 1];
+        const float a30 = As[(o + 3) * SA + o], a31 = As[(o + 3) * SA + o + 1], a32 = As[(o + 3) * SA + o + 2];
+        const float x10 = -a10, x21 = -a21, x32 = -a32;
+        const float x20 = -fmaf(a21, x10, a20);
+        const float x31 = -fmaf(a32, x21, a31);
+        const float x30 = -fmaf(a32, x20, fmaf(a31, x10, a30));
+        float *X0 = Xs + o * SA + o;
+        X0[0] = 1.f;      X0[1] = 0.f;      X0[2] = 0.f;      X0[3] = 0.f;
+        X0[SA] = x10;     X0[SA + 1] = 1.f; X0[SA + 2] = 0.f; X0[SA + 3] = 0.f;
+        X0[2 * SA] = x20; X0[2 * SA + 1] = x21; X0[2 * SA + 2] = 1.f; X0[2 * SA + 3] = 0.f;
+        X0[3 * SA] = x30; X0[3 * SA + 1] = x31; X0[3 * SA + 2] = x32; X0[3 * SA + 3] = 1.f;
+    }
+    __syncwarp();
+    {  // 4 -> 8: lane = (half q, row r, column c) of the two 4 x 4 blocks X21
+        const int q = lane >> 4, r = (lane >> 2) & 3, cc = lane & 3;
+        const int o = B0 + 8 * q;
+        float y = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) y = fmaf(As[(o + 4 + r) * SA + o + m], Xs[(o + m) * SA + o + cc], y);
+        Yw[(4 * q + r) * 17 + cc] = y;
+        __syncwarp();
+        float x = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) x = fmaf(Xs[(o + 4 + r) * SA + o + 4 + m], Yw[(4 * q + m) * 17 + cc], x);
+        Xs[(o + 4 + r) * SA + o + cc] = -x;
+    }
+    __syncwarp();
+    {  // 8 -> 16: X21 (8 x 8), two entries per lane
+        const int r = lane >> 2, c0 = (lane & 3) * 2;
+        float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const float am = As[(B0 + 8 + r) * SA + B0 + m];
+            y0 = fmaf(am, Xs[(B0 + m) * SA + B0 + c0], y0);
+            y1 = fmaf(am, Xs[(B0 + m) * SA + B0 + c0 + 1], y1);
+        }
+        Yw[r * 17 + c0] = y0;
+        Yw[r * 17 + c0 + 1] = y1;
+        __syncwarp();
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const float xm = Xs[(B0 + 8 + r) * SA + B0 + 8 + m];
+            x0 = fmaf(xm, Yw[m * 17 + c0], x0);
+            x1 = fmaf(xm, Yw[m * 17 + c0 + 1], x1);
+        }
+        Xs[(B0 + 8 + r) * SA + B0 + c0] = -x0;
+        Xs[(B0 + 8 + r) * SA + B0 + c0 + 1] = -x1;
+    }
+    __syncwarp();
+    {  // T of the diagonal block: one 16-byte chunk (row r, 8 columns) per lane
+        const int r = lane >> 1, h8 = (lane & 1) * 8;
+        float tv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) tv[q] = Xs[(B0 + r) * SA + B0 + h8 + q] * sbc[B0 + h8 + q];
+        st_chunk(sm, SM_T + kmajor_offset(B0 + r, B0 + h8, C), tv);
+    }
+}
+
+// Zero fills of the inverse (thread z of 128): the two upper X blocks the 32 -> 64 merge reads
+// (rows 0..15 x cols 16..31, rows 32..47 x cols 48..63) and the six strictly-upper 16 x 16 blocks
+// of T.
+__device__ __forceinline__ void solve_zero_fill(uint8_t *sm, float *Xs, int z) {
+    // X rows 0..15 cols 16..31 and rows 32..47 cols 48..63 (read by the 32 -> 64 merge)
+    const int blk = z >> 6, rr = (z & 63) >> 2, cq = (z & 3) * 4;
+    *reinterpret_cast<float4 *>(Xs + (32 * blk + rr) * SA + 32 * blk + 16 + cq) =
+        make_float4(0.f, 0.f, 0.f, 0.f);
+    // T: the six strictly-upper 16 x 16 blocks (192 chunks of 16 bytes)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int e = z + 128 * q;
+        if (e < 192) {
+            const int bi = e >> 5, r2 = (e & 31) >> 1, hf = e & 1;
+            const int I = bi < 3 ? 0 : (bi < 5 ? 1 : 2);
+            const int J = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
+            *reinterpret_cast<uint4 *>(sm + SM_T + kmajor_offset(16 * I + r2, 16 * J + 8 * hf, C)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
     }
 }
 
@@ -308,7 +464,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
-    float *refs = reinterpret_cast<float *>(sm + SM_REF);
+    float *wts = reinterpret_cast<float *>(sm + SM_WT);
     float *cst = reinterpret_cast<float *>(sm + SM_CST);
     float *gcs = reinterpret_cast<float *>(sm + SM_GC);
     float *sbeta = reinterpret_cast<float *>(sm + SM_BETA);
@@ -403,9 +559,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             last_v = cc;
         };
         // First-step descriptors of every operand.
-        const uint64_t d_ap = sdesc(sb + SM_AP, 128u, 2048u), d_apb = sdesc(sb + SM_APB, 128u, 2048u);
-        const uint64_t d_offa = sdesc(sb + SM_OFF, 128u, 2048u), d_offb = sdesc(sb + SM_OFFB, 128u, 2048u);
-        const uint64_t d_k = sdesc(sb + SM_KQ, 128u, 2048u), d_q = sdesc(sb + SM_KQ + 16384u, 128u, 2048u);
+        // K-major 128-byte-swizzled operands: K step st starts 32 B further in the 128-byte row,
+        // and channels 64..127 (st >= 4) in the next atom column, R * 128 bytes on.
+        auto ksw = [](int st, uint32_t rows) -> uint64_t {
+            return (uint64_t)(((uint32_t)(st >> 2) * rows * 128u + (uint32_t)(st & 3) * 32u) >> 4);
+        };
+        const uint64_t d_ap = sdesc_sw128(sb + SM_AP, 16u, 1024u), d_apb = sdesc_sw128(sb + SM_APB, 16u, 1024u);
+        const uint64_t d_offa = sdesc_sw128(sb + SM_OFF, 16u, 1024u), d_offb = sdesc_sw128(sb + SM_OFFB, 16u, 1024u);
+        const uint64_t d_k = sdesc_sw128(sb + SM_KQ, 16u, 1024u), d_q = sdesc_sw128(sb + SM_KQ + 8192u, 16u, 1024u);
         const uint64_t d_v = sdesc_sw128(sb + SM_VT, 8192u, 1024u);
         const uint64_t d_t = sdesc(sb + SM_T, 128u, 1024u), d_p = sdesc(sb + SM_P, 128u, 1024u);
         const uint64_t d_kh0 = sdesc_sw128(sb + SM_KH, 8192u, 1024u);
@@ -425,12 +586,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_after();
 #pragma unroll
             for (int st = 0; st < D / 16; ++st)
-                mma_bf16_warp(tmem + TM_AP, d_ap + kDescStepKmajor * st, d_apb + kDescStepKmajor * st,
-                              idesc_bf16(128, 64), st > 0);
+                mma_bf16_warp(tmem + TM_AP, d_ap + ksw(st, 128), d_apb + ksw(st, 64), idesc_bf16(128, 64), st > 0);
 #pragma unroll
             for (int st = 0; st < D / 16; ++st)
-                mma_bf16_warp(tmem + TM_OFF, d_offa + kDescStepKmajor * st, d_offb + kDescStepKmajor * st,
-                              idesc_bf16(64, 32), st > 0);
+                mma_bf16_warp(tmem + TM_OFF, d_offa + ksw(st, 64), d_offb + ksw(st, 32), idesc_bf16(64, 32), st > 0);
             mma_commit_warp(&bars[BAR_AP]);
             if (more) load_qk(cc + 1);
             // state chain. MMA1 = S^T [K+ ; Q+]^T from the bf16 state copy as soon as the operands
@@ -439,13 +598,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_after();
 #pragma unroll
             for (int st = 0; st < D / 16; ++st)
-                mma_bf16_tmem_a_warp(tmem + TM_D1, tmem + TM_SA + 8 * st, d_k + kDescStepKmajor * st,
-                                     idesc_bf16(128, 64), st > 0);
+                mma_bf16_tmem_a_warp(tmem + TM_D1, tmem + TM_SA + 8 * st, d_k + ksw(st, 128), idesc_bf16(128, 64),
+                                     st > 0);
             mma_commit_warp(&bars[BAR_M1]);
 #pragma unroll
             for (int st = 0; st < D / 16; ++st)
-                mma_bf16_tmem_a_warp(tmem + TM_D1 + 64, tmem + TM_SA + 8 * st, d_q + kDescStepKmajor * st,
-                                     idesc_bf16(128, 64), st > 0);
+                mma_bf16_tmem_a_warp(tmem + TM_D1 + 64, tmem + TM_SA + 8 * st, d_q + ksw(st, 128), idesc_bf16(128, 64),
+                                     st > 0);
             mma_commit_warp(&bars[BAR_KQFREE]);
             // ... U^T = V^T T^T once T exists (V tile as an MN-major A operand) ...
             if (!(iok = wait(BAR_TREADY, par))) break;
@@ -564,6 +723,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!(ok = state_wait(&bars[BAR_OPS], par))) break;
             tc_fence_before();
             mbar_arrive(&bars[BAR_SREADY]);
+
+            // A and P out of TMEM and the 16 x 16 diagonal blocks of (I + A)^{-1}, while the prep
+            // warps run step 1 of the next chunk; they merge the blocks once EPIDONE is signalled.
+            // P is rewritten only after MMA3 of the previous chunk (M34 above).
+            if (!(ok = state_wait(&bars[BAR_AP], par))) break;
+            tc_fence_after();
+            {
+                const float *sbc = sbeta + 64 * par;
+                ap_readout(sm, As, tmem + tq, warp & 3, lane, sbc);
+                state_sync();
+                solve_diag_block(sm, As, Xs, warp & 3, lane, sbc);
+                solve_zero_fill(sm, Xs, v);
+            }
+            fence_async_smem();  // T and P are read by MMAs
+            mbar_arrive(&bars[BAR_EPIDONE]);
             if (c > 0) store_o(o0, o1, prev_row0, prev_len);
 
             // S <- S Diag(gam_last) while MMA1 reads the bf16 copy.
@@ -645,11 +819,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // the state warps and the issuer run the state chain of chunk c.
         const __nv_bfloat16 *bg = static_cast<const __nv_bfloat16 *>(p.beta);
         bool ok = true;
-        // Operand mapping: channels 8j..8j+7, rows rlo + 8 * (4 * mh + m) for m = 0..3.
-        const int rlo = lane & 7;
-        const int j = 4 * (warp & 3) + (lane >> 3);
-        const int mh = warp >> 2;
-        float gm[4][8];  // Gam of the operand mapping's 4 rows x 8 channels (current chunk)
+        // Thread mapping: channels 8j..8j+7 (j = 8 * (warp >> 2) + lane % 8, the fastest index
+        // across lanes), rows tr0 .. tr0 + 3 with tr0 = 16 * (warp % 4) + 4 * (lane / 8).
+        const int j = 8 * (warp >> 2) + (lane & 7);
+        const int rq = lane >> 3;
+        const int rb = warp & 3;  // 16-row block
+        const int tr0 = 16 * rb + 4 * rq;
+        const int mh = rb >> 1;
+        float gm[4][8];  // Gam of the thread's 4 rows x 8 channels (current chunk)
         int g_inflight = -1;  // chunk of a g-tile copy issued here and not yet waited for
         // beta of token tid of a chunk, loaded one step ahead (raw bf16 bits, converted when used)
         auto load_beta = [&](int cc) -> uint32_t {
@@ -671,48 +848,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!prep_wait(&bars[BAR_G], (uint32_t)(cc & 1))) return false;
             g_inflight = -1;
 
-            // ---- 1. Gam = cumsum_r g within the chunk, per key channel ----------------------
-            // A warp holds 32 consecutive rows of 32 channels: scan over the 8 lanes of a row
-            // group with shuffles, then over the 4 row groups in registers; the second row half
-            // then adds Gam_31.
+            // ---- 1. Gam = cumsum_r g within the chunk, per key channel --------------------------
+            // A thread's own 4 rows in registers, then across the 4 lanes of a 16-row block (two
+            // shuffle steps), then across the four blocks through shared memory.
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                const int r = rlo + 8 * (4 * mh + m);
+                const int r = tr0 + m;
                 const uint4 w = *reinterpret_cast<const uint4 *>(sm + SM_G + tile_chunk(r, j));
                 const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) gm[m][i] = r < ln ? ((i & 1) ? bf_hi(ww[i >> 1]) : bf_lo(ww[i >> 1])) : 0.f;
-            }
-#pragma unroll
-            for (int d = 1; d < 8; d <<= 1) {
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float t = __shfl_up_sync(0xffffffffu, gm[m][i], d, 8);
-                        if (rlo >= d) gm[m][i] += t;
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    const float x = r < ln ? ((i & 1) ? bf_hi(ww[i >> 1]) : bf_lo(ww[i >> 1])) : 0.f;
+                    gm[m][i] = m ? gm[m - 1][i] + x : x;
                 }
             }
             {
-                float run[8];
+                float incl[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) run[i] = 0.f;
+                for (int i = 0; i < 8; ++i) incl[i] = gm[3][i];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
+                for (int d = 8; d < 32; d <<= 1) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float total = __shfl_sync(0xffffffffu, gm[m][i], 7, 8);
-                        gm[m][i] += run[i];
-                        run[i] += total;
+                        const float t = __shfl_up_sync(0xffffffffu, incl[i], d);
+                        if (lane >= d) incl[i] += t;
                     }
                 }
-            }
-            if (rlo == 7) {  // rows 15 and 31 of the half (half-local sums for the second half)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    refs[(2 * mh) * 128 + 8 * j + i] = gm[1][i];
-                    refs[(2 * mh + 1) * 128 + 8 * j + i] = gm[3][i];
+                    const float excl = incl[i] - gm[3][i];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) gm[m][i] += excl;
+                }
+                if (rq == 3) {  // the 16-row block's sums
+                    *reinterpret_cast<float4 *>(wts + 128 * rb + 8 * j) = make_float4(incl[0], incl[1], incl[2], incl[3]);
+                    *reinterpret_cast<float4 *>(wts + 128 * rb + 8 * j + 4) = make_float4(incl[4], incl[5], incl[6], incl[7]);
                 }
             }
             if (tid < C) sbeta[64 * (cc & 1) + tid] = bet;
@@ -724,18 +894,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tma_load_3d(sm + SM_G + 8192, &maps.g, &bars[BAR_G], 64, h, r);
                 g_inflight = cc + 1;
             }
-            if (mh) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float g31 = refs[128 + 8 * j + i];
+            for (int pb = 0; pb < 3; ++pb) {  // add the sums of the earlier 16-row blocks
+                if (pb < rb) {
+                    const float4 a0 = *reinterpret_cast<const float4 *>(wts + 128 * pb + 8 * j);
+                    const float4 a1 = *reinterpret_cast<const float4 *>(wts + 128 * pb + 8 * j + 4);
+                    const float add[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) gm[m][i] += g31;
+                    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) gm[m][i] += add[i];
+                    }
                 }
             }
             if (tid < 128) {
                 const int ch = tid;
-                const float G15 = refs[ch], G31 = refs[128 + ch];
-                const float G47 = refs[256 + ch] + G31, G63 = refs[384 + ch] + G31;
+                const float G15 = wts[ch], G31 = G15 + wts[128 + ch];
+                const float G47 = G31 + wts[256 + ch], G63 = G47 + wts[384 + ch];
                 cst[CST_M0 * 128 + ch] = G15 * kLog2e;
                 cst[CST_M1 * 128 + ch] = G47 * kLog2e;
                 cst[CST_C0 * 128 + ch] = ex2((G31 - G15) * kLog2e);
@@ -761,9 +936,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!(ok = prep_wait(&bars[BAR_QK], par))) break;
             if (c > 0 && !(ok = prep_wait(&bars[BAR_KQFREE], par ^ 1u))) break;
             if (mh)
-                build_operands<1>(sm, gm, cst, rlo, j, len, SM_KH + 16384u * par);
+                build_operands<1>(sm, gm, cst, tr0, j, len, SM_KH + 16384u * par);
             else
-                build_operands<0>(sm, gm, cst, rlo, j, len, SM_KH + 16384u * par);
+                build_operands<0>(sm, gm, cst, tr0, j, len, SM_KH + 16384u * par);
             fence_async_smem();
             mbar_arrive(&bars[BAR_OPS]);
 
@@ -771,157 +946,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (c + 1 < nchunks && !(ok = step1(c + 1))) break;
             const float *sbc = sbeta + 64 * par;  // beta of this chunk
 
-            // ---- 3. A (fp32, for the solve) and P (bf16 operand) out of TMEM --------------------
-            // The diagonal tile (M = 128) holds row i of A (lanes 0..63) and of P (lanes 64..127);
-            // the off-diagonal tile (M = 64) holds its 64 rows in lanes 0..15 of each lane quarter:
-            // A rows 32..47, 48..63, then P rows 32..47, 48..63. P is overwritten only once MMA3 of
-            // the previous chunk has read it (its commit also covers MMA2, the reader of T).
-            if (!(ok = prep_wait(&bars[BAR_AP], par))) break;
-            if (c > 0 && !(ok = prep_wait(&bars[BAR_M34], par ^ 1u))) break;
-            tc_fence_after();
-            {
-                const int q = warp & 3;
-                float vals[32];
-                if (warp < 4) {
-                    const int L = 32 * q + lane;
-                    const int i = L & 63;
-                    const int j0 = (q & 1) ? 32 : 0;  // the diagonal half of row i
-                    tmem_ld32(tmem + tq + TM_AP + j0, vals);
-                    tmem_ld_wait();
-                    if (L < 64) {
-                        const float b = sbc[i];
-#pragma unroll
-                        for (int k = 0; k < 32; k += 4) {
-                            float4 w;
-                            w.x = (j0 + k + 0 < i) ? vals[k + 0] * b : 0.f;
-                            w.y = (j0 + k + 1 < i) ? vals[k + 1] * b : 0.f;
-                            w.z = (j0 + k + 2 < i) ? vals[k + 2] * b : 0.f;
-                            w.w = (j0 + k + 3 < i) ? vals[k + 3] * b : 0.f;
-                            *reinterpret_cast<float4 *>(As + i * SA + j0 + k) = w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) vals[k] = (j0 + k <= i) ? vals[k] : 0.f;
-                        st_row32(sm + SM_P, i, j0, C, vals);
-                        if (j0 == 0) {
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) vals[k] = 0.f;
-                            st_row32(sm + SM_P, i, 32, C, vals);
-                        }
-                    }
-                } else {
-                    tmem_ld32(tmem + tq + TM_OFF, vals);
-                    tmem_ld_wait();
-                    if (lane < 16) {
-                        const int i = 32 + 16 * (q & 1) + lane;
-                        if (q < 2) {
-                            const float b = sbc[i];
-#pragma unroll
-                            for (int k = 0; k < 32; k += 4)
-                                *reinterpret_cast<float4 *>(As + i * SA + k) =
-                                    make_float4(vals[k] * b, vals[k + 1] * b, vals[k + 2] * b, vals[k + 3] * b);
-                        } else {
-                            st_row32(sm + SM_P, i, 0, C, vals);
-                        }
-                    }
-                }
-            }
-            prep_sync();
-
-            // ---- 4. X = (I + A)^{-1}, written to T = X Diag(beta) as it completes ---------------
-            // (a) warp b < 4 inverts the 16 x 16 diagonal block b by doubling: four 4 x 4 blocks
-            //     in closed form, then 4 -> 8 -> 16 merges X21 = -X22 (A21 X11); warps 4..7 zero
-            //     the strictly-upper blocks of T and the two upper blocks of X the merges read.
-            if (warp < 4) {
-                const int B0 = 16 * warp;
-                float *Yw = reinterpret_cast<float *>(sm + SM_Y) + warp * (16 * 17);
-#pragma unroll
-                for (int q = 0; q < 3; ++q) {  // zero the upper 4 x 4 blocks of the diagonal block
-                    const int e = lane + 32 * q;   // 96 entries: 6 blocks x 16
-                    const int blk = e >> 4, rr = (e >> 2) & 3, cc = e & 3;
-                    const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                    const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                    Xs[(B0 + 4 * bi + rr) * SA + B0 + 4 * bj + cc] = 0.f;
-                }
-                if (lane < 4) {  // 4 x 4 unit lower-triangular inverse in closed form
-                    const int o = B0 + 4 * lane;
-                    const float a10 = As[(o + 1) * SA + o], a20 = As[(o + 2) * SA + o], a21 = As[(o + 2) * SA + o + 1];
-                    const float a30 = As[(o + 3) * SA + o], a31 = As[(o + 3) * SA + o + 1], a32 = As[(o + 3) * SA + o + 2];
-                    const float x10 = -a10, x21 = -a21, x32 = -a32;
-                    const float x20 = -fmaf(a21, x10, a20);
-                    const float x31 = -fmaf(a32, x21, a31);
-                    const float x30 = -fmaf(a32, x20, fmaf(a31, x10, a30));
-                    float *X0 = Xs + o * SA + o;
-                    X0[0] = 1.f;      X0[1] = 0.f;      X0[2] = 0.f;      X0[3] = 0.f;
-                    X0[SA] = x10;     X0[SA + 1] = 1.f; X0[SA + 2] = 0.f; X0[SA + 3] = 0.f;
-                    X0[2 * SA] = x20; X0[2 * SA + 1] = x21; X0[2 * SA + 2] = 1.f; X0[2 * SA + 3] = 0.f;
-                    X0[3 * SA] = x30; X0[3 * SA + 1] = x31; X0[3 * SA + 2] = x32; X0[3 * SA + 3] = 1.f;
-                }
-                __syncwarp();
-                {  // 4 -> 8: lane = (half q, row r, column c) of the two 4 x 4 blocks X21
-                    const int q = lane >> 4, r = (lane >> 2) & 3, cc = lane & 3;
-                    const int o = B0 + 8 * q;
-                    float y = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) y = fmaf(As[(o + 4 + r) * SA + o + m], Xs[(o + m) * SA + o + cc], y);
-                    Yw[(4 * q + r) * 17 + cc] = y;
-                    __syncwarp();
-                    float x = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) x = fmaf(Xs[(o + 4 + r) * SA + o + 4 + m], Yw[(4 * q + m) * 17 + cc], x);
-                    Xs[(o + 4 + r) * SA + o + cc] = -x;
-                }
-                __syncwarp();
-                {  // 8 -> 16: X21 (8 x 8), two entries per lane
-                    const int r = lane >> 2, c0 = (lane & 3) * 2;
-                    float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        const float am = As[(B0 + 8 + r) * SA + B0 + m];
-                        y0 = fmaf(am, Xs[(B0 + m) * SA + B0 + c0], y0);
-                        y1 = fmaf(am, Xs[(B0 + m) * SA + B0 + c0 + 1], y1);
-                    }
-                    Yw[r * 17 + c0] = y0;
-                    Yw[r * 17 + c0 + 1] = y1;
-                    __syncwarp();
-                    float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        const float xm = Xs[(B0 + 8 + r) * SA + B0 + 8 + m];
-                        x0 = fmaf(xm, Yw[m * 17 + c0], x0);
-                        x1 = fmaf(xm, Yw[m * 17 + c0 + 1], x1);
-                    }
-                    Xs[(B0 + 8 + r) * SA + B0 + c0] = -x0;
-                    Xs[(B0 + 8 + r) * SA + B0 + c0 + 1] = -x1;
-                }
-                __syncwarp();
-                {  // T of the diagonal block: one 16-byte chunk (row r, 8 columns) per lane
-                    const int r = lane >> 1, h8 = (lane & 1) * 8;
-                    float tv[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) tv[q] = Xs[(B0 + r) * SA + B0 + h8 + q] * sbc[B0 + h8 + q];
-                    st_chunk(sm, SM_T + kmajor_offset(B0 + r, B0 + h8, C), tv);
-                }
-            } else {
-                const int z = tid - 128;  // 0..127
-                // X rows 0..15 cols 16..31 and rows 32..47 cols 48..63 (read by the 32 -> 64 merge)
-                const int blk = z >> 6, rr = (z & 63) >> 2, cq = (z & 3) * 4;
-                *reinterpret_cast<float4 *>(Xs + (32 * blk + rr) * SA + 32 * blk + 16 + cq) =
-                    make_float4(0.f, 0.f, 0.f, 0.f);
-                // T: the six strictly-upper 16 x 16 blocks (192 chunks of 16 bytes)
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int e = z + 128 * q;
-                    if (e < 192) {
-                        const int bi = e >> 5, r2 = (e & 31) >> 1, hf = e & 1;
-                        const int I = bi < 3 ? 0 : (bi < 5 ? 1 : 2);
-                        const int J = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
-                        *reinterpret_cast<uint4 *>(sm + SM_T + kmajor_offset(16 * I + r2, 16 * J + 8 * hf, C)) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
-            }
-            prep_sync();
+            // ---- 3. X = (I + A)^{-1}, written to T = X Diag(beta) as it completes ---------------
+            // The state warps have read A and P out of TMEM and inverted the 16 x 16 diagonal
+            // blocks (with the zero fills); the block merges run here.
+            if (!(ok = prep_wait(&bars[BAR_EPIDONE], par))) break;
             // (b) 16 -> 32: warp (p, nt) < 4 computes column tile nt of X_{2p+1,2p} (tf32 mma)
             if (warp < 4) {
                 const int pp = warp >> 1, nt = warp & 1;
@@ -947,7 +975,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 warp_mma_16x8<32>(acc, Xs + (32 + 16 * mt) * SA + 32, SA, Y + 8 * nt, SA, lane);
                 store_t_16x8(sm + SM_T, 32 + 16 * mt, 8 * nt, acc, sbc, lane);
             }
-            fence_async_smem();  // the T and P stores
+            fence_async_smem();  // the T stores
             mbar_arrive(&bars[BAR_TREADY]);
         }
         if (!ok && tid == 0) {
