@@ -456,7 +456,7 @@ __device__ __forceinline__ void solve_zero_fill(uint8_t *sm, float *Xs, int z) {
 }
 
 struct Maps {
-    CUtensorMap q, k, g, v;
+    CUtensorMap q, k, g, v, o;
 };
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -506,6 +506,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         prefetch_tensormap(&maps.k);
         prefetch_tensormap(&maps.g);
         prefetch_tensormap(&maps.v);
+        prefetch_tensormap(&maps.o);
     }
     tc_fence_before();
     __syncthreads();
@@ -659,15 +660,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o);
         bool ok = true;
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {  // initial state -> TMEM (fp32) and its bf16 copy
+        for (int cb = 0; cb < 4; ++cb) {  // initial state -> TMEM (fp32)
             const int k0 = 32 * cb;
             float buf[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) buf[i] = p.init ? __ldcs(p.init + state_off + (size_t)(k0 + i) * D + v) : 0.f;
             tmem_st32(tmem + tq + TM_S + k0, buf);
-            uint32_t w[16];
-            pack32(buf, w, 1.f);
-            tmem_st16(tmem + tq + TM_SA + k0 / 2, w);
         }
         tmem_st_wait();
 
@@ -691,6 +689,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         };
 
+        // O of a finished chunk through the T/P region (free from M34 of that chunk until the next
+        // chunk's A/P read-out) in the TMA tile layout, then one bulk tensor store per 64 channels.
+        // A ragged chunk that does not end the tensor takes plain stores, so rows of the next
+        // sequence are never written.
+        const long long total_rows = p.cu_seqlens ? (long long)p.T : (long long)p.n_seqs * p.T;
+        uint32_t ost[8];  // offset of (row b, value column v) in the staged tile, b = row % 8
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+            ost[b] = (uint32_t)((v >> 6) * 8192 + b * 128 + ((((v >> 3) & 7) ^ b) << 4) + (v & 7) * 2);
+        auto write_o = [&](const float (&o0)[32], const float (&o1)[32], long long r0, int ln) {
+            if (ln == C || r0 + ln >= total_rows) {  // rows past the tensor end are not written
+#pragma unroll
+                for (int r = 0; r < 32; ++r)
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + SM_T + ost[r & 7] + (r & ~7) * 128) = __float2bfloat16_rn(o0[r]);
+#pragma unroll
+                for (int r = 0; r < 32; ++r)
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + SM_T + ost[r & 7] + (32 + (r & ~7)) * 128) =
+                        __float2bfloat16_rn(o1[r]);
+                fence_async_smem();
+                state_sync();
+                if (v == 0) {
+                    tma_store_3d(&maps.o, sm + SM_T, 0, h, (int)r0);
+                    tma_store_3d(&maps.o, sm + SM_T + 8192, 64, h, (int)r0);
+                    bulk_commit();
+                }
+            } else {
+                store_o(o0, o1, r0, ln);
+            }
+        };
+
         long long prev_row0 = 0;
         int prev_len = 0;
         int c = 0;
@@ -699,13 +727,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t par = (uint32_t)(c & 1);
             const long long row0 = bos + (long long)c * C;
             const int len = (int)min((long long)C, eos - row0);
-            float o0[32], o1[32];
-            if (c > 0) {
+            if (c > 0) {  // O of the previous chunk, once MMA3 and MMA4 of it have completed
                 if (!(ok = state_wait(&bars[BAR_M34], par ^ 1u))) break;
                 tc_fence_after();
+                float o0[32], o1[32];
                 tmem_ld32(tmem + tq + TM_D1 + 64, o0);
                 tmem_ld32(tmem + tq + TM_D1 + 96, o1);
                 tmem_ld_wait();
+                write_o(o0, o1, prev_row0, prev_len);
+            }
+            // OPS of chunk c: its operands, and gam_last written by its step 1, are in place. Waited
+            // before SREADY, so OPS of chunk c + 1 (which needs MMA1 of chunk c) cannot have
+            // completed yet and the parity cannot alias.
+            if (!(ok = state_wait(&bars[BAR_OPS], par))) break;
+            // One pass over the state: its bf16 copy for MMA1, and S <- S Diag(gam_last) for MMA4.
+            {
+                const float *gc = gcs + 128 * (c % 3);
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     float sv[32];
@@ -714,13 +751,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     uint32_t w[16];
                     pack32(sv, w, 1.f);
                     tmem_st16(tmem + tq + TM_SA + 16 * cb, w);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sv[i] *= gc[32 * cb + i];
+                    tmem_st32(tmem + tq + TM_S + 32 * cb, sv);
                 }
                 tmem_st_wait();
             }
-            // OPS of chunk c: its operands, and gam_last written by its step 1, are in place. Waited
-            // before SREADY, so OPS of chunk c + 1 (which needs MMA1 of chunk c) cannot have
-            // completed yet and the parity cannot alias.
-            if (!(ok = state_wait(&bars[BAR_OPS], par))) break;
             tc_fence_before();
             mbar_arrive(&bars[BAR_SREADY]);
 
@@ -729,6 +765,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // P is rewritten only after MMA3 of the previous chunk (M34 above).
             if (!(ok = state_wait(&bars[BAR_AP], par))) break;
             tc_fence_after();
+            if (v == 0) bulk_wait_read_all();  // the O store has read the T/P region
+            state_sync();
             {
                 const float *sbc = sbeta + 64 * par;
                 ap_readout(sm, As, tmem + tq, warp & 3, lane, sbc);
@@ -738,22 +776,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             fence_async_smem();  // T and P are read by MMAs
             mbar_arrive(&bars[BAR_EPIDONE]);
-            if (c > 0) store_o(o0, o1, prev_row0, prev_len);
-
-            // S <- S Diag(gam_last) while MMA1 reads the bf16 copy.
-            {
-                const float *gc = gcs + 128 * (c % 3);
-#pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
-                    float sv[32];
-                    tmem_ld32(tmem + tq + TM_S + 32 * cb, sv);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) sv[i] *= gc[32 * cb + i];
-                    tmem_st32(tmem + tq + TM_S + 32 * cb, sv);
-                }
-                tmem_st_wait();
-            }
 
             if (!(ok = state_wait(&bars[BAR_M1], par))) break;
             tc_fence_after();
@@ -795,9 +817,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tmem_ld32(tmem + tq + TM_D1 + 64, o0);
                 tmem_ld32(tmem + tq + TM_D1 + 96, o1);
                 tmem_ld_wait();
-                store_o(o0, o1, prev_row0, prev_len);
+                write_o(o0, o1, prev_row0, prev_len);
             }
         }
+        if (v == 0) bulk_wait_all();  // every O store is complete (and has read shared memory)
         if (ok) {
             if (p.fin) {
 #pragma unroll 1
@@ -1043,7 +1066,8 @@ cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
     const long long rows = p.cu_seqlens ? (long long)p.T : (long long)p.n_seqs * p.T;
     Maps maps;
     if (!encode_map(&maps.q, p.q, rows, p.H) || !encode_map(&maps.k, p.k, rows, p.H) ||
-        !encode_map(&maps.g, p.g, rows, p.H) || !encode_map(&maps.v, p.v, rows, p.H))
+        !encode_map(&maps.g, p.g, rows, p.H) || !encode_map(&maps.v, p.v, rows, p.H) ||
+        !encode_map(&maps.o, p.o, rows, p.H))
         return cudaErrorInvalidValue;
     kda_prefill_tc_kernel<<<(unsigned)(p.n_seqs * p.H), NTHREADS, SMEM_BYTES, s>>>(maps, p);
     return cudaGetLastError();
