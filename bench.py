@@ -372,7 +372,7 @@ def _oracle_pairs(ki, dev, pairs, tokens):
 def cpu_baseline(ki, dev, pairs=None, tokens=None):
     import oracle
     cores = oracle.max_threads()
-    pairs = pairs or max(cores, 32)
+    pairs = pairs or max(4 * cores, 32)  # about 20 s of work on the host's cores
     tokens = tokens or PF["T"]
     probs = _oracle_pairs(ki, dev, pairs, tokens)
     # One call over all sampled pairs so OpenMP spreads them over the cores.
@@ -384,7 +384,8 @@ def cpu_baseline(ki, dev, pairs=None, tokens=None):
     return {"value": token_heads / PF["H"] / dt, "unit": "tokens/s", "cores": min(cores, pairs),
             "kind": "oracle",
             "sample": f"fp64 recurrence over {pairs} (batch row, head) pairs x {tokens} tokens of the "
-                      f"B=4 T=8192 H=32 d=128 workload ({token_heads} token-heads, {dt:.2f} s wall); "
+                      f"B=4 T=8192 H=32 d=128 workload ({token_heads} token-heads, {dt:.2f} s wall, "
+                      f"{dt * min(cores, pairs):.0f} core-seconds); "
                       f"tokens/s = token-heads/s / 32 heads"}
 
 

@@ -23,27 +23,34 @@
 //
 // Layout of the work: one CTA per (sequence, head); chunks run in order, in two overlapped
 // streams of work carried by different warps:
-//   prep warps 0..7    everything of a chunk that does not depend on the state: Gam (cumsum of
-//                      g), the decay-scaled operands, the A/P tiles, T. They build chunk c + 1
-//                      while the state chain of chunk c runs.
-//   state warps 8..11  thread = TMEM lane = value column: the bf16 state copy, the state decay,
-//                      -(K+ S)^T and U^T as bf16 A operands in TMEM, O written to global memory.
-//   issuer warp 12     one thread issues every MMA and TMA copy, in the order the work becomes
-//                      ready; mbarriers carry each hand-off between the three.
-//   TMA: g, then q/k tiles (64 rows x 128 channels, 128-byte swizzle) of the next chunk are
-//        fetched as soon as the current ones are read; the v tile once MMA2 has read the last.
+//   prep warps 0..7    the state-independent work of a chunk: Gam (cumsum of g, thread = 4
+//                      consecutive rows x 8 channels), the decay-scaled operands, and the block
+//                      merges of T = (I + A)^{-1} Diag(beta). While the A/P MMAs of chunk c run
+//                      they already compute Gam of chunk c + 1.
+//   state warps 8..11  thread = TMEM lane = value column: O of chunk c - 1 out (staged in shared
+//                      memory, one TMA tensor store), the bf16 state copy fused with the decay
+//                      S <- S Diag(gam_last), A and P out of TMEM and the 16 x 16 diagonal blocks
+//                      of the inverse, -(K+ S)^T and U^T as bf16 A operands in TMEM.
+//   issuer warp 12     the whole warp walks the chunks and one elected lane issues every MMA and
+//                      TMA copy, in the order the work becomes ready; mbarriers carry each
+//                      hand-off between the three groups.
+//   TMA: g (fetched by the prep warps), q/k of the next chunk as soon as the current ones are
+//        read, v once MMA2 has read the last; every tile 64 rows x 128 channels, 128-byte swizzle.
 //   TMEM (512 columns): [0,64) diagonal A|P tile, [64,96) off-diagonal tile, [96,128) the
 //        bf16 A operand -(K+ S)^T then U^T, [128,256) (K+ S | Q+ S -> O), [256,320) U,
 //        [320,448) the fp32 state S^T (lanes = d_v), [448,512) its bf16 copy (MMA1's A).
-//   MMAs (kind::f16, bf16 operands, fp32 accumulate; "tmem" = A read from TMEM):
+//   MMAs (kind::f16, bf16 operands, fp32 accumulate; "tmem" = A read from TMEM; shared-memory
+//   operands in the 128-byte-swizzled layout):
 //        diag  [K*f ; Q*f] x [K/f]^T              M = 128, N = 64, K = 128
 //        off   [K*e ; Q*e] x [K*e']^T             M = 64,  N = 32, K = 128
 //        MMA1  S^T (tmem) x [K+ ; Q+]^T           M = 128, two N = 64 halves, K = 128
 //        MMA2  V^T x T^T  (V tile, MN-major)      N = 64,  K = 64    -> then += -(K+ S)^T (tmem) x T^T = U^T
 //        MMA3  U^T (tmem) x P^T  (onto (Q+ S)^T)  N = 64,  K = 64    -> O^T
 //        MMA4  U^T (tmem) x Khat  (MN-major B)    N = 128, K = 64    -> S^T
-//   The 64 x 64 triangular inverse: 16 x 16 diagonal blocks by forward substitution on CUDA
-//   cores, then the 16->32 and 32->64 block merges as tf32 warp-level MMAs.
+//   MMA1 starts as soon as the operands and the state copy exist, so it is done long before the
+//   prep warps overwrite [K+ ; Q+] with the next chunk.
+//   The 64 x 64 triangular inverse: 16 x 16 diagonal blocks by doubling on CUDA cores, then the
+//   16->32 and 32->64 block merges as tf32 warp-level MMAs.
 // Every mbarrier wait is bounded; on time-out the CTA records kErrTimeout, drains what it
 // issued (again bounded), frees its TMEM and exits.
 #include <cudaTypedefs.h>

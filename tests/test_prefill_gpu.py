@@ -88,6 +88,28 @@ def test_varlen_small_with_empty_sequence():
     torch.testing.assert_close(s[3], x["initial_state"][3], rtol=0, atol=0)
 
 
+@pytest.mark.parametrize("lengths", [[100, 20], [64, 5, 64, 3], [70, 1, 57]])
+def test_varlen_ragged_chunk_next_to_short_sequence(lengths):
+    """A ragged last chunk whose 64-row window reaches into a following short sequence (which
+    may end the tensor): every output row must still be that of its own sequence."""
+    x = ki.varlen_inputs(lengths, 3, 128, 128, device=DEV, seed=11)
+    o, s = run(x)
+    ro, rs = ref(x)
+    assert_close(o, ro, "o")
+    assert_close(s, rs, "final_state")
+
+
+@pytest.mark.parametrize("T", [100, 130])
+def test_batch_ragged_tail_next_to_following_row(T):
+    """Batched layout with T % 64 != 0: the last chunk of batch row b ends inside the rows of
+    batch row b + 1, whose outputs must be left to their own chunks."""
+    x = ki.prefill_inputs(3, T, 2, 128, 128, device=DEV, seed=12, state_std=0.02)
+    o, s = run(x)
+    ro, rs = ref(x)
+    assert_close(o, ro, "o")
+    assert_close(s, rs, "final_state")
+
+
 def test_zero_tokens_returns_initial_state():
     x = ki.prefill_inputs(2, 0, 2, 128, 128, device=DEV, seed=4, state_std=0.02)
     o, s = run(x)
