@@ -70,6 +70,8 @@ def load():
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_version.argtypes = []
         lib.kda_version.restype = _i
+        lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _vp]
+        lib.kda_selftest_wait_timeout.restype = _i
         _lib = lib
         return lib
 
@@ -184,6 +186,16 @@ def decode_step(q, k, v, g, beta, state, o=None):
                                  _ptr(beta), _ptr(state), _ptr(o), _stream(dev))
     _raise_if(st)
     return o
+
+
+def selftest_wait_timeout(limit_ns: int, device=None):
+    """Queue the library's bounded-wait self-test on the current stream of `device`: a kernel
+    waits `limit_ns` ns on an mbarrier phase nothing completes and records a time-out in the
+    device error word, which the next check_status() raises as KDA_ERR_TIMEOUT."""
+    lib = load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _raise_if(lib.kda_selftest_wait_timeout(int(limit_ns), _stream(dev)))
 
 
 def check_status(device=None):

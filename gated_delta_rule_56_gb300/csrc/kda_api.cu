@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "kda_internal.h"
+#include "kda_tc.cuh"
 
 namespace kda {
 namespace {
@@ -52,6 +53,17 @@ kda_status check_ptr(const void *p, const char *name, bool need_align) {
     return KDA_OK;
 }
 
+// One thread waits, bounded, on an mbarrier phase that nothing completes (count 1, no arrival),
+// with the library's own bounded wait, and records the time-out like a pipeline wait would.
+__global__ void wait_timeout_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+        if (!tc::mbar_wait(&bar, 0, limit_ns)) atomicOr(&g_error_word, kErrTimeout);
+    }
+}
+
 kda_status launched(cudaError_t e, const char *what) {
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
     return ok();
@@ -80,6 +92,13 @@ using namespace kda;
 extern "C" {
 
 int kda_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+kda_status kda_selftest_wait_timeout(uint64_t limit_ns, kda_stream_t stream) {
+    if (limit_ns < 1 || limit_ns > 1000000000ull)
+        return fail(KDA_ERR_INVALID_ARG, "limit_ns=%llu must be in [1, 1e9]", (unsigned long long)limit_ns);
+    wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns);
+    return launched(cudaGetLastError(), "wait_timeout_kernel");
+}
 
 const char *kda_status_string(kda_status status) {
     switch (status) {

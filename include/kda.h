@@ -111,6 +111,18 @@ KDA_API kda_status kda_decode_step(kda_dtype dtype, int N, int H, int dk, int dv
  */
 KDA_API kda_status kda_check_status(kda_stream_t stream);
 
+/*
+ * kda_selftest_wait_timeout -- diagnostic for the library's failure detection (the pages have no
+ * counterpart: it exists so that a caller or a test can see a stalled pipeline being reported).
+ * Queues on `stream` one small kernel whose thread waits, bounded by `limit_ns` nanoseconds of
+ * %globaltimer, on an mbarrier phase that nothing completes -- the same bounded wait that every
+ * pipeline wait of the prefill kernel uses -- then records KDA_ERR_TIMEOUT in the device error
+ * word and exits normally; the context stays usable. limit_ns must be in [1, 1e9].
+ * Returns KDA_OK once queued (the timeout itself is reported by kda_check_status),
+ * KDA_ERR_INVALID_ARG for an out-of-range limit, KDA_ERR_CUDA if the launch failed.
+ */
+KDA_API kda_status kda_selftest_wait_timeout(uint64_t limit_ns, kda_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 KDA_API const char *kda_status_string(kda_status status);
 

@@ -98,6 +98,12 @@ def test_decode_rejects_bad_arguments_on_host(lib, case, expect):
     assert st == expect, (case, kda.status_string(st), kda.last_error())
 
 
+@pytest.mark.parametrize("limit", [0, 10**9 + 1])
+def test_selftest_rejects_bad_limit_on_host(lib, limit):
+    assert lib.kda_selftest_wait_timeout(limit, None) == 1  # KDA_ERR_INVALID_ARG, nothing launched
+    assert b"limit_ns" in lib.kda_last_error()
+
+
 def test_binding_rejects_cpu_tensors():
     import torch
     x = torch.zeros(1, 4, 1, 32, dtype=torch.bfloat16)
