@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=("varlen", "long"), default=None,
+                    help="time one of the other prefill workloads instead of the headline (one JSON line): "
+                         "varlen = 64 packed sequences of U[128, 16384] tokens with initial states; "
+                         "long = one sequence of 1,048,576 tokens (B=1, H=32)")
     ap.add_argument("--ncu-case", choices=("prefill", "decode"),
                     help="run two launches of the small profiling case (for ncu) and exit")
     args = ap.parse_args()
@@ -423,6 +427,54 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_workload(args):
+    """The other prefill workloads, timed like the headline: varlen (64 sequences with lengths
+    uniform in [128, 16384], seed 0, initial states N(0, 0.02)) or long (B=1, T=1,048,576)."""
+    import gated_delta_rule_56_gb300 as kda
+    import kda_inputs as ki
+    from gated_delta_rule_56_gb300.build import build
+    build()
+    kda.load()
+    dev = torch.device("cuda", 0)
+    H, d = PF["H"], PF["d"]
+    if args.workload == "varlen":
+        lengths = ki.varlen_lengths(64, 128, 16384, seed=0)
+        x = ki.varlen_inputs(lengths, H, d, d, device=dev, seed=0)
+        tokens, n_seq = int(lengths.sum()), int(lengths.numel())
+        kw = dict(cu_seqlens=x["cu_seqlens"], initial_state=x["initial_state"])
+        alg = tokens * H * (4 * d * 2 + 2 + 2 * d) + 2 * n_seq * H * d * d * 4
+        name = f"KDA chunked prefill, varlen: {n_seq} sequences (lengths U[128,16384], seed 0, {tokens} tokens) H={H} dk=dv={d} bf16, fp32 initial states"
+    else:
+        T = 1 << 20
+        x = ki.prefill_inputs(1, T, H, d, d, device=dev, seed=0)
+        tokens, n_seq = T, 1
+        kw = {}
+        alg = prefill_bytes(1, T, H, d)
+        name = f"KDA chunked prefill, long context: B=1 T={T} H={H} dk=dv={d} bf16, zero init"
+    args_in = [x[n] for n in NAMES]
+
+    def step(_i):
+        kda.prefill(*args_in, **kw)
+
+    step(0)
+    kda.check_status()
+    peak_bw, _peak_tc, peak_kind = measured_peaks()
+    steps, warmup = max(1, min(args.steps, 20)), max(3, min(args.warmup, 5))
+    with ClockSampler(dev) as clk:
+        total_ms, per = time_steps(step, steps, warmup, Ranks(1))
+    kda.check_status()
+    kernel_ms = statistics.mean(per)
+    achieved = alg / (kernel_ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": f"KDA prefill tokens/s ({args.workload})", "value": tokens / (kernel_ms / 1e3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": steps, "warmup": warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic", "config": {"workload": name, "ctas": n_seq * H},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s",
+                     "frac": achieved / peak_bw, "peak_source": peak_kind, "alg_bytes_per_launch": alg,
+                     "kernel_ms": kernel_ms},
+        "gpu_launches": steps, "clocks": clk.summary()}), flush=True)
+
+
 def ncu_case(kind):
     """Small cases sized for an ncu capture: inputs larger than L2, a few hundred MB on the
     device. prefill: B=4 T=2048 H=32 d=128 (128 CTAs); decode: N=64 H=32 d=128 (2048 CTAs)."""
@@ -448,6 +500,9 @@ def main():
     args = parse()
     if args.ncu_case:
         ncu_case(args.ncu_case)
+        return
+    if args.workload:
+        run_workload(args)
         return
     if args.impl == "reference":
         run_reference(args)
