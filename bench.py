@@ -52,10 +52,11 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("varlen", "long"), default=None,
+    ap.add_argument("--workload", choices=("varlen", "long", "gated"), default=None,
                     help="time one of the other prefill workloads instead of the headline (one JSON line): "
                          "varlen = 64 packed sequences of U[128, 16384] tokens with initial states; "
-                         "long = one sequence of 1,048,576 tokens (B=1, H=32)")
+                         "long = one sequence of 1,048,576 tokens (B=1, H=32); "
+                         "gated = the headline shape with gate logits (decays formed in the kernel)")
     ap.add_argument("--ncu-case", choices=("prefill", "decode"),
                     help="run two launches of the small profiling case (for ncu) and exit")
     args = ap.parse_args()
@@ -444,13 +445,21 @@ def run_workload(args):
         kw = dict(cu_seqlens=x["cu_seqlens"], initial_state=x["initial_state"])
         alg = tokens * H * (4 * d * 2 + 2 + 2 * d) + 2 * n_seq * H * d * d * 4
         name = f"KDA chunked prefill, varlen: {n_seq} sequences (lengths U[128,16384], seed 0, {tokens} tokens) H={H} dk=dv={d} bf16, fp32 initial states"
-    else:
+    elif args.workload == "long":
         T = 1 << 20
         x = ki.prefill_inputs(1, T, H, d, d, device=dev, seed=0)
         tokens, n_seq = T, 1
         kw = {}
         alg = prefill_bytes(1, T, H, d)
         name = f"KDA chunked prefill, long context: B=1 T={T} H={H} dk=dv={d} bf16, zero init"
+    else:
+        B, T = PF["B"], PF["T"]
+        x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)
+        x["g"] = ki.gate_logits_like(x["g"], seed=1)  # logits x; the kernel forms g = -5 sigmoid(x)
+        tokens, n_seq = B * T, B
+        kw = dict(gate_bound=5.0)
+        alg = prefill_bytes(B, T, H, d)
+        name = f"KDA chunked prefill with gate logits (g = -5 sigmoid(x) in the kernel): B={B} T={T} H={H} dk=dv={d} bf16, zero init"
     args_in = [x[n] for n in NAMES]
 
     def step(_i):

@@ -70,6 +70,12 @@ def load():
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_version.argtypes = []
         lib.kda_version.restype = _i
+        lib.kda_prefill_gated.argtypes = [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp,
+                                          _vp, ctypes.c_float, _vp, ctypes.c_size_t, _vp]
+        lib.kda_prefill_gated.restype = _i
+        lib.kda_decode_step_gated.argtypes = [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                              ctypes.c_float, _vp]
+        lib.kda_decode_step_gated.restype = _i
         lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _vp]
         lib.kda_selftest_wait_timeout.restype = _i
         _lib = lib
@@ -115,13 +121,14 @@ def _check(name, t, dtype, shape, device):
 
 
 def prefill(q, k, v, g, beta, cu_seqlens=None, initial_state=None, output_final_state=True,
-            o=None, final_state=None):
+            o=None, final_state=None, gate_bound=None):
     """Chunked KDA prefill on the GPU.
 
     q, k, g [B, T, H, dk]; v [B, T, H, dv]; beta [B, T, H]; all bf16 or all fp32, on one CUDA
     device. With ``cu_seqlens`` (int32 [N+1] on the device) B must be 1 and the rows are
-    packed sequences. ``initial_state``: fp32 [N, H, dk, dv] or None (zeros).
-    Returns (o [B, T, H, dv], final_state [N, H, dk, dv] fp32 or None).
+    packed sequences. ``initial_state``: fp32 [N, H, dk, dv] or None (zeros). With
+    ``gate_bound`` A, ``g`` holds gate logits x and the kernels use g = -A * sigmoid(x)
+    (kda_prefill_gated). Returns (o [B, T, H, dv], final_state [N, H, dk, dv] fp32 or None).
     """
     lib = load()
     if q.dtype not in _DTYPES:
@@ -155,16 +162,22 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, initial_state=None, output_final_
     ws_bytes = int(lib.kda_prefill_workspace_size(dt, B, T, H, dk, dv, N))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
     with torch.cuda.device(dev):
-        st = lib.kda_prefill(dt, B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                             _ptr(cu_seqlens), N, _ptr(initial_state), _ptr(o), _ptr(final_state),
-                             _ptr(ws), ws_bytes, _stream(dev))
+        if gate_bound is None:
+            st = lib.kda_prefill(dt, B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                 _ptr(cu_seqlens), N, _ptr(initial_state), _ptr(o), _ptr(final_state),
+                                 _ptr(ws), ws_bytes, _stream(dev))
+        else:
+            st = lib.kda_prefill_gated(dt, B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                       _ptr(cu_seqlens), N, _ptr(initial_state), _ptr(o), _ptr(final_state),
+                                       float(gate_bound), _ptr(ws), ws_bytes, _stream(dev))
     _raise_if(st)
     return o, final_state
 
 
-def decode_step(q, k, v, g, beta, state, o=None):
+def decode_step(q, k, v, g, beta, state, o=None, gate_bound=None):
     """One KDA decode token for N sequences; ``state`` (fp32 [N, H, dk, dv]) is updated in
-    place. q, k, g [N, H, dk]; v [N, H, dv]; beta [N, H]. Returns o [N, H, dv]."""
+    place. q, k, g [N, H, dk]; v [N, H, dv]; beta [N, H]. With ``gate_bound`` A, ``g`` holds gate
+    logits x and g = -A * sigmoid(x) is used (kda_decode_step_gated). Returns o [N, H, dv]."""
     lib = load()
     if q.dtype not in _DTYPES:
         raise TypeError(f"unsupported dtype {q.dtype}")
@@ -182,8 +195,12 @@ def decode_step(q, k, v, g, beta, state, o=None):
     else:
         _check("o", o, q.dtype, (N, H, dv), dev)
     with torch.cuda.device(dev):
-        st = lib.kda_decode_step(_DTYPES[q.dtype], N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                                 _ptr(beta), _ptr(state), _ptr(o), _stream(dev))
+        if gate_bound is None:
+            st = lib.kda_decode_step(_DTYPES[q.dtype], N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                     _ptr(beta), _ptr(state), _ptr(o), _stream(dev))
+        else:
+            st = lib.kda_decode_step_gated(_DTYPES[q.dtype], N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                           _ptr(beta), _ptr(state), _ptr(o), float(gate_bound), _stream(dev))
     _raise_if(st)
     return o
 

@@ -89,6 +89,97 @@ unsigned *device_error_word() {
 
 using namespace kda;
 
+namespace kda {
+namespace {
+
+// The common body of kda_prefill and kda_prefill_gated.
+kda_status prefill_impl(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,
+                               const void *k, const void *v, const void *g, const void *beta,
+                               const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,
+                               float *final_state, float gate_bound, kda_stream_t stream) {
+    kda_status st;
+    if ((st = check_dtype(dtype)) != KDA_OK) return st;
+    if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "negative size B=%d T=%d H=%d", B, T, H);
+    if ((st = check_head(dk, dv)) != KDA_OK) return st;
+    if (cu_seqlens) {
+        if (B != 1) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens requires B == 1 (got B=%d)", B);
+        if (n_seqs < 0) return fail(KDA_ERR_INVALID_ARG, "n_seqs=%d is negative", n_seqs);
+        if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is not 4-byte aligned");
+    } else {
+        n_seqs = B;
+    }
+    const long long rows = (long long)B * T;
+    if ((long long)n_seqs * H > 0x7fffffffLL) return fail(KDA_ERR_INVALID_ARG, "too many (sequence, head) pairs");
+    if (rows * H * (long long)(dk > dv ? dk : dv) > (1LL << 46))
+        return fail(KDA_ERR_INVALID_ARG, "tensor too large");
+    if (rows > 0) {
+        if ((st = check_ptr(q, "q", true)) || (st = check_ptr(k, "k", true)) ||
+            (st = check_ptr(v, "v", true)) || (st = check_ptr(g, "g", true)) ||
+            (st = check_ptr(o, "o", true)) || (st = check_ptr(beta, "beta", false)))
+            return st;
+        if ((reinterpret_cast<uintptr_t>(beta) & (dtype == KDA_BF16 ? 1u : 3u)) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "beta is not aligned to its element size");
+    }
+    if (initial_state && !aligned16(initial_state))
+        return fail(KDA_ERR_INVALID_ARG, "initial_state is not 16-byte aligned");
+    if (final_state && !aligned16(final_state))
+        return fail(KDA_ERR_INVALID_ARG, "final_state is not 16-byte aligned");
+    if ((long long)n_seqs * H == 0) return ok();
+
+    RunParams p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    p.cu_seqlens = cu_seqlens;
+    p.init = initial_state;
+    p.fin = final_state;
+    p.o = o;
+    p.T = T;
+    p.H = H;
+    p.n_seqs = n_seqs;
+    p.err = device_error_word();
+    p.gate_bound = gate_bound;
+    if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word: %s",
+                            cudaGetErrorString(cudaGetLastError()));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (tc_prefill_supported(dtype, dk, dv, p)) return launched(launch_tc_prefill(p, s), "tensor-core prefill");
+    return launched(launch_recurrent(dtype, dk, dv, p, s), "recurrent prefill");
+}
+
+// The common body of kda_decode_step and kda_decode_step_gated.
+kda_status decode_impl(kda_dtype dtype, int N, int H, int dk, int dv, const void *q, const void *k,
+                       const void *v, const void *g, const void *beta, float *state, void *o, float gate_bound,
+                       kda_stream_t stream) {
+    kda_status st;
+    if ((st = check_dtype(dtype)) != KDA_OK) return st;
+    if (N < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "negative size N=%d H=%d", N, H);
+    if ((st = check_head(dk, dv)) != KDA_OK) return st;
+    if ((long long)N * H == 0) return ok();
+    if ((long long)N * H > 0x7fffffffLL) return fail(KDA_ERR_INVALID_ARG, "too many (sequence, head) pairs");
+    if ((st = check_ptr(q, "q", true)) || (st = check_ptr(k, "k", true)) || (st = check_ptr(v, "v", true)) ||
+        (st = check_ptr(g, "g", true)) || (st = check_ptr(o, "o", true)) ||
+        (st = check_ptr(state, "state", true)) || (st = check_ptr(beta, "beta", false)))
+        return st;
+    if ((reinterpret_cast<uintptr_t>(beta) & (dtype == KDA_BF16 ? 1u : 3u)) != 0)
+        return fail(KDA_ERR_INVALID_ARG, "beta is not aligned to its element size");
+
+    RunParams p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    p.cu_seqlens = nullptr;
+    p.init = state;
+    p.fin = state;
+    p.o = o;
+    p.T = 1;
+    p.H = H;
+    p.n_seqs = N;
+    p.err = device_error_word();
+    p.gate_bound = gate_bound;
+    if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word");
+    return launched(launch_recurrent(dtype, dk, dv, p, reinterpret_cast<cudaStream_t>(stream)), "decode step");
+}
+
+}  // namespace
+}  // namespace kda
+
 extern "C" {
 
 int kda_version(void) { return 1 * 10000 + 0 * 100 + 0; }
@@ -123,83 +214,37 @@ kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int dv, con
                        const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,
                        float *final_state, void *workspace, size_t workspace_bytes,
                        kda_stream_t stream) {
-    kda_status st;
-    if ((st = check_dtype(dtype)) != KDA_OK) return st;
-    if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "negative size B=%d T=%d H=%d", B, T, H);
-    if ((st = check_head(dk, dv)) != KDA_OK) return st;
-    if (cu_seqlens) {
-        if (B != 1) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens requires B == 1 (got B=%d)", B);
-        if (n_seqs < 0) return fail(KDA_ERR_INVALID_ARG, "n_seqs=%d is negative", n_seqs);
-        if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
-            return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is not 4-byte aligned");
-    } else {
-        n_seqs = B;
-    }
     (void)workspace;
     (void)workspace_bytes;
-    const long long rows = (long long)B * T;
-    if ((long long)n_seqs * H > 0x7fffffffLL) return fail(KDA_ERR_INVALID_ARG, "too many (sequence, head) pairs");
-    if (rows * H * (long long)(dk > dv ? dk : dv) > (1LL << 46))
-        return fail(KDA_ERR_INVALID_ARG, "tensor too large");
-    if (rows > 0) {
-        if ((st = check_ptr(q, "q", true)) || (st = check_ptr(k, "k", true)) ||
-            (st = check_ptr(v, "v", true)) || (st = check_ptr(g, "g", true)) ||
-            (st = check_ptr(o, "o", true)) || (st = check_ptr(beta, "beta", false)))
-            return st;
-        if ((reinterpret_cast<uintptr_t>(beta) & (dtype == KDA_BF16 ? 1u : 3u)) != 0)
-            return fail(KDA_ERR_INVALID_ARG, "beta is not aligned to its element size");
-    }
-    if (initial_state && !aligned16(initial_state))
-        return fail(KDA_ERR_INVALID_ARG, "initial_state is not 16-byte aligned");
-    if (final_state && !aligned16(final_state))
-        return fail(KDA_ERR_INVALID_ARG, "final_state is not 16-byte aligned");
-    if ((long long)n_seqs * H == 0) return ok();
+    return prefill_impl(dtype, B, T, H, dk, dv, q, k, v, g, beta, cu_seqlens, n_seqs, initial_state, o,
+                        final_state, 0.f, stream);
+}
 
-    RunParams p{};
-    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
-    p.cu_seqlens = cu_seqlens;
-    p.init = initial_state;
-    p.fin = final_state;
-    p.o = o;
-    p.T = T;
-    p.H = H;
-    p.n_seqs = n_seqs;
-    p.err = device_error_word();
-    if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word: %s",
-                            cudaGetErrorString(cudaGetLastError()));
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (tc_prefill_supported(dtype, dk, dv, p)) return launched(launch_tc_prefill(p, s), "tensor-core prefill");
-    return launched(launch_recurrent(dtype, dk, dv, p, s), "recurrent prefill");
+kda_status kda_prefill_gated(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,
+                             const void *k, const void *v, const void *gate_logits, const void *beta,
+                             const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,
+                             float *final_state, float gate_bound, void *workspace, size_t workspace_bytes,
+                             kda_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    if (!(gate_bound > 0.f && gate_bound <= 1e4f))
+        return fail(KDA_ERR_INVALID_ARG, "gate_bound=%g must be in (0, 1e4]", (double)gate_bound);
+    return prefill_impl(dtype, B, T, H, dk, dv, q, k, v, gate_logits, beta, cu_seqlens, n_seqs, initial_state,
+                        o, final_state, gate_bound, stream);
 }
 
 kda_status kda_decode_step(kda_dtype dtype, int N, int H, int dk, int dv, const void *q, const void *k,
                            const void *v, const void *g, const void *beta, float *state, void *o,
                            kda_stream_t stream) {
-    kda_status st;
-    if ((st = check_dtype(dtype)) != KDA_OK) return st;
-    if (N < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "negative size N=%d H=%d", N, H);
-    if ((st = check_head(dk, dv)) != KDA_OK) return st;
-    if ((long long)N * H == 0) return ok();
-    if ((long long)N * H > 0x7fffffffLL) return fail(KDA_ERR_INVALID_ARG, "too many (sequence, head) pairs");
-    if ((st = check_ptr(q, "q", true)) || (st = check_ptr(k, "k", true)) || (st = check_ptr(v, "v", true)) ||
-        (st = check_ptr(g, "g", true)) || (st = check_ptr(o, "o", true)) ||
-        (st = check_ptr(state, "state", true)) || (st = check_ptr(beta, "beta", false)))
-        return st;
-    if ((reinterpret_cast<uintptr_t>(beta) & (dtype == KDA_BF16 ? 1u : 3u)) != 0)
-        return fail(KDA_ERR_INVALID_ARG, "beta is not aligned to its element size");
+    return decode_impl(dtype, N, H, dk, dv, q, k, v, g, beta, state, o, 0.f, stream);
+}
 
-    RunParams p{};
-    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
-    p.cu_seqlens = nullptr;
-    p.init = state;
-    p.fin = state;
-    p.o = o;
-    p.T = 1;
-    p.H = H;
-    p.n_seqs = N;
-    p.err = device_error_word();
-    if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word");
-    return launched(launch_recurrent(dtype, dk, dv, p, reinterpret_cast<cudaStream_t>(stream)), "decode step");
+kda_status kda_decode_step_gated(kda_dtype dtype, int N, int H, int dk, int dv, const void *q, const void *k,
+                                 const void *v, const void *gate_logits, const void *beta, float *state, void *o,
+                                 float gate_bound, kda_stream_t stream) {
+    if (!(gate_bound > 0.f && gate_bound <= 1e4f))
+        return fail(KDA_ERR_INVALID_ARG, "gate_bound=%g must be in (0, 1e4]", (double)gate_bound);
+    return decode_impl(dtype, N, H, dk, dv, q, k, v, gate_logits, beta, state, o, gate_bound, stream);
 }
 
 kda_status kda_check_status(kda_stream_t stream) {

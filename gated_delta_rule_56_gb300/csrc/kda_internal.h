@@ -23,6 +23,7 @@ struct RunParams {
     int H;
     int n_seqs;
     unsigned *err;              // device error word
+    float gate_bound;           // 0: g holds log-decays; > 0: g holds logits x, g = -gate_bound * sigmoid(x)
 };
 
 // Device error word of the current device (created on first use).

@@ -466,6 +466,8 @@ struct Maps {
     CUtensorMap q, k, g, v, o;
 };
 
+// GATED: the g tensor holds logits x and the kernel forms g = -p.gate_bound * sigmoid(x).
+template <bool GATED>
 __global__ void __launch_bounds__(NTHREADS, 1)
     kda_prefill_tc_kernel(const __grid_constant__ Maps maps, const RunParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -888,7 +890,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float x = r < ln ? ((i & 1) ? bf_hi(ww[i >> 1]) : bf_lo(ww[i >> 1])) : 0.f;
+                    float x = (i & 1) ? bf_hi(ww[i >> 1]) : bf_lo(ww[i >> 1]);
+                    if (GATED) x = __fdividef(-p.gate_bound, 1.f + ex2(-x * kLog2e));  // scaled sigmoid
+                    x = r < ln ? x : 0.f;
                     gm[m][i] = m ? gm[m - 1][i] + x : x;
                 }
             }
@@ -1064,8 +1068,11 @@ cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
         if (!attr_set[dev]) {
-            e = cudaFuncSetAttribute(kda_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(kda_prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)SMEM_BYTES);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kda_prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
             if (e != cudaSuccess) return e;
             attr_set[dev] = true;
         }
@@ -1076,7 +1083,10 @@ cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
         !encode_map(&maps.g, p.g, rows, p.H) || !encode_map(&maps.v, p.v, rows, p.H) ||
         !encode_map(&maps.o, p.o, rows, p.H))
         return cudaErrorInvalidValue;
-    kda_prefill_tc_kernel<<<(unsigned)(p.n_seqs * p.H), NTHREADS, SMEM_BYTES, s>>>(maps, p);
+    if (p.gate_bound > 0.f)
+        kda_prefill_tc_kernel<true><<<(unsigned)(p.n_seqs * p.H), NTHREADS, SMEM_BYTES, s>>>(maps, p);
+    else
+        kda_prefill_tc_kernel<false><<<(unsigned)(p.n_seqs * p.H), NTHREADS, SMEM_BYTES, s>>>(maps, p);
     return cudaGetLastError();
 }
 

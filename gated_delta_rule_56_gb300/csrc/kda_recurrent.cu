@@ -107,7 +107,9 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
         if (tid < DK) {
             sk[buf][tid] = load_elem(k, rr * DK + tid);
             sq[buf][tid] = load_elem(q, rr * DK + tid);
-            sa[buf][tid] = expf(load_elem(g, rr * DK + tid));
+            float gv = load_elem(g, rr * DK + tid);
+            if (p.gate_bound > 0.f) gv = -p.gate_bound / (1.f + expf(-gv));  // scaled sigmoid of a logit
+            sa[buf][tid] = expf(gv);
         } else if (tid < DK + DV) {
             sv[buf][tid - DK] = load_elem(v, rr * DV + (tid - DK));
         }

@@ -104,6 +104,28 @@ KDA_API kda_status kda_decode_step(kda_dtype dtype, int N, int H, int dk, int dv
                            const void *beta, float *state, void *o, kda_stream_t stream);
 
 /*
+ * kda_prefill_gated / kda_decode_step_gated -- kda_prefill / kda_decode_step with the gate given
+ * as raw logits x (same layout and dtype as g) instead of log-decays: the kernels form
+ * g = -gate_bound * sigmoid(x) per element, the scaled sigmoid whose lower bound makes the decay
+ * bounded ("Kimi K3 Explained", researchpapers.dev, "Architecture at a glance"; the workloads'
+ * log-decay is -5 sigmoid(N(0,1))). g then lies in (-gate_bound, 0); the accuracy statement for
+ * g in [-5, 0] covers gate_bound <= 5. gate_bound must be finite and in (0, 1e4], else
+ * KDA_ERR_INVALID_ARG. Every other argument, and the return values, as the plain forms.
+ */
+KDA_API kda_status kda_prefill_gated(kda_dtype dtype, int B, int T, int H, int dk, int dv,
+                                     const void *q, const void *k, const void *v,
+                                     const void *gate_logits, const void *beta,
+                                     const int32_t *cu_seqlens, int n_seqs,
+                                     const float *initial_state, void *o, float *final_state,
+                                     float gate_bound, void *workspace, size_t workspace_bytes,
+                                     kda_stream_t stream);
+
+KDA_API kda_status kda_decode_step_gated(kda_dtype dtype, int N, int H, int dk, int dv,
+                                         const void *q, const void *k, const void *v,
+                                         const void *gate_logits, const void *beta, float *state,
+                                         void *o, float gate_bound, kda_stream_t stream);
+
+/*
  * kda_check_status -- synchronise `stream`, then read and clear the device error word of the
  * current device. Returns KDA_OK, KDA_ERR_INVALID_ARG (bad cu_seqlens seen by a kernel),
  * KDA_ERR_TIMEOUT (a bounded pipeline wait gave up; that (sequence, head) is left

@@ -57,6 +57,13 @@ def prefill_inputs(B, T, H, dk, dv, dtype=torch.bfloat16, seed=0, device="cpu",
     return out
 
 
+def gate_logits_like(g: torch.Tensor, seed=0) -> torch.Tensor:
+    """Gate logits x ~ N(0, 1) with the shape, dtype and device of a log-decay tensor; the
+    log-decay of the workloads is then -5 sigmoid(x)."""
+    gen = _generator(seed, g.device)
+    return torch.randn(g.shape, generator=gen, device=g.device, dtype=torch.float32).to(g.dtype)
+
+
 def varlen_lengths(n_seqs, lo, hi, seed=0):
     """Sequence lengths drawn uniformly from the integers in [lo, hi]."""
     gen = _generator(seed, "cpu")

@@ -11,6 +11,7 @@ Public functions take CPU tensors or arrays in the KDA layouts and return fp64 n
 * ``literal(...)``: same, with the d_k x d_k transition formed explicitly (small cases)
 * ``chunked(..., chunk=64, dump=False)`` -> (o, final_state[, intermediates])
 * ``decode_step(q, k, v, g, beta, state)`` -> (o, new_state): one token of the recurrence.
+* ``scaled_sigmoid_gate(x, bound)`` -> g = -bound * sigmoid(x) (log-decays from gate logits).
 
 Layouts: q, k, g [B, T, H, d_k]; v [B, T, H, d_v]; beta [B, T, H]; with ``cu_seqlens``
 (int [N+1]) B must be 1 and the rows of sequence n are cu[n]..cu[n+1]-1. States are
@@ -50,6 +51,8 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
 
 
 def _declare(lib):
+    lib.kda_oracle_scaled_sigmoid_gate.argtypes = [ctypes.c_int64, _dp, ctypes.c_double, _dp]
+    lib.kda_oracle_scaled_sigmoid_gate.restype = ctypes.c_int
     lib.kda_oracle_recurrent.argtypes = [ctypes.c_int, _i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
     lib.kda_oracle_recurrent.restype = ctypes.c_int
@@ -179,6 +182,16 @@ def chunked(q, k, v, g, beta, cu_seqlens=None, initial_state=None, chunk=64, n_t
     """The chunkwise form; with dump=True also returns per-chunk intermediates of the
     first (sequence, head) pair (flat fp64 arrays, chunk after chunk)."""
     return _run("chunked", q, k, v, g, beta, cu_seqlens, initial_state, n_threads, chunk, dump)
+
+
+def scaled_sigmoid_gate(x, bound):
+    """Log-decays from gate logits: g = -bound * sigmoid(x) elementwise, fp64, same shape as x."""
+    x = _f64(x)
+    g = np.empty_like(x)
+    rc = load_library().kda_oracle_scaled_sigmoid_gate(x.size, x.ctypes.data_as(_dp), float(bound), g.ctypes.data_as(_dp))
+    if rc != 0:
+        raise ValueError(f"kda_oracle_scaled_sigmoid_gate returned {rc}")
+    return g
 
 
 def decode_step(q, k, v, g, beta, state, n_threads=0):

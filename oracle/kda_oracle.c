@@ -26,6 +26,10 @@
  *                           which is the same product expanded (no other rewriting).
  *  kda_oracle_literal    -- the same recurrence with the d_k x d_k transition matrix
  *                           formed explicitly; O(d_k^2 d_v) per token, for small cases.
+ *  kda_oracle_scaled_sigmoid_gate -- the log-decay from gate logits, g = -bound * sigmoid(x)
+ *                           per element ("Kimi K3 Explained", researchpapers.dev, "Architecture
+ *                           at a glance": the log-decay is bounded below through a scaled
+ *                           sigmoid); the bound's value is not on the pages (the workloads use 5).
  *  kda_oracle_chunked    -- a separately written chunkwise form of the same recurrence
  *                           (per-chunk cumulative log-decay, the strictly lower intra-chunk
  *                           matrix, a triangular solve for the delta corrections, one state
@@ -340,6 +344,16 @@ int kda_oracle_chunked(int n_seqs, const int64_t *cu, int H, int dk, int dv, int
         free(ws);
     }
     return failed ? KDA_ORACLE_ENOMEM : 0;
+}
+
+int kda_oracle_scaled_sigmoid_gate(int64_t n, const double *x, double bound, double *g)
+{
+    if (n < 0 || !x || !g || !(bound > 0.0)) return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        const double sig = 1.0 / (1.0 + exp(-x[i]));  /* the logistic function */
+        g[i] = -bound * sig;
+    }
+    return 0;
 }
 
 int kda_oracle_max_threads(void)

@@ -98,6 +98,16 @@ def test_decode_rejects_bad_arguments_on_host(lib, case, expect):
     assert st == expect, (case, kda.status_string(st), kda.last_error())
 
 
+@pytest.mark.parametrize("bound", [0.0, -1.0, float("nan"), 2e4])
+def test_gated_entry_points_reject_bad_bound_on_host(lib, bound):
+    import ctypes
+    st = lib.kda_prefill_gated(0, 1, 4, 1, 128, 128, *([None] * 5), None, 1, None, None, None,
+                               ctypes.c_float(bound), None, 0, None)
+    assert st == 1 and b"gate_bound" in lib.kda_last_error()
+    st = lib.kda_decode_step_gated(0, 1, 1, 128, 128, *([None] * 5), None, None, ctypes.c_float(bound), None)
+    assert st == 1 and b"gate_bound" in lib.kda_last_error()
+
+
 @pytest.mark.parametrize("limit", [0, 10**9 + 1])
 def test_selftest_rejects_bad_limit_on_host(lib, limit):
     assert lib.kda_selftest_wait_timeout(limit, None) == 1  # KDA_ERR_INVALID_ARG, nothing launched

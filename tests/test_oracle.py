@@ -336,3 +336,34 @@ def test_pins_catch_planted_mistakes(tmp_path, idx):
             except AssertionError:
                 caught.append(pin.__name__)
     assert caught, f"no pin caught the planted mistake: {desc}"
+
+
+# ---------------------------------------------------------------- gate from logits -------
+# g = -A sigmoid(x): the scaled sigmoid that bounds the log-decay ("Kimi K3 Explained",
+# researchpapers.dev, "Architecture at a glance"). Pinned by closed forms of the logistic
+# function, not by re-evaluating it.
+
+def test_gate_closed_forms():
+    A = 5.0
+    x = np.array([0.0, math.log(3.0), -math.log(3.0), math.log(7.0)])
+    g = oracle.scaled_sigmoid_gate(x, A)
+    np.testing.assert_allclose(g, [-A / 2, -A * 3 / 4, -A / 4, -A * 7 / 8], rtol=0, atol=1e-15)
+
+
+def test_gate_symmetry_slope_and_range():
+    A = 3.25
+    x = np.linspace(-30.0, 30.0, 601)
+    g = oracle.scaled_sigmoid_gate(x, A)
+    gm = oracle.scaled_sigmoid_gate(-x, A)
+    np.testing.assert_allclose(g + gm, -A, rtol=0, atol=1e-14)        # sigma(x) + sigma(-x) = 1
+    assert np.all(np.diff(g) < 0) and np.all(g < 0) and np.all(g > -A)  # decreasing, in (-A, 0)
+    h = 1e-6                                                            # slope at 0 is -A / 4
+    slope = (oracle.scaled_sigmoid_gate(np.array([h]), A)[0] - oracle.scaled_sigmoid_gate(np.array([-h]), A)[0]) / (2 * h)
+    assert abs(slope + A / 4) < 1e-8
+    np.testing.assert_allclose(oracle.scaled_sigmoid_gate(np.array([-50.0, 50.0]), A), [-A * math.exp(-50.0), -A],
+                               rtol=1e-12, atol=0)
+
+
+def test_gate_rejects_bad_bound():
+    with pytest.raises(ValueError):
+        oracle.scaled_sigmoid_gate(np.zeros(3), 0.0)
