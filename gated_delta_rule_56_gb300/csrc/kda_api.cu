@@ -94,9 +94,10 @@ namespace {
 
 // The common body of kda_prefill and kda_prefill_gated.
 kda_status prefill_impl(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,
-                               const void *k, const void *v, const void *g, const void *beta,
-                               const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,
-                               float *final_state, float gate_bound, kda_stream_t stream) {
+                        const void *k, const void *v, const void *g, const void *beta,
+                        const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,
+                        float *final_state, float gate_bound, void *workspace, size_t workspace_bytes,
+                        kda_stream_t stream) {
     kda_status st;
     if ((st = check_dtype(dtype)) != KDA_OK) return st;
     if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "negative size B=%d T=%d H=%d", B, T, H);
@@ -141,7 +142,14 @@ kda_status prefill_impl(kda_dtype dtype, int B, int T, int H, int dk, int dv, co
     if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word: %s",
                             cudaGetErrorString(cudaGetLastError()));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (tc_prefill_supported(dtype, dk, dv, p)) return launched(launch_tc_prefill(p, s), "tensor-core prefill");
+    if (tc_prefill_supported(dtype, dk, dv, p)) {
+        // A few long sequences: split them along the sequence when the caller gave the workspace.
+        const size_t seg_bytes = segmented_workspace_bytes(dtype, B, T, H, dk, dv, cu_seqlens != nullptr);
+        if (seg_bytes && workspace && workspace_bytes >= seg_bytes &&
+            (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0)
+            return launched(launch_segmented_prefill(p, B, workspace, workspace_bytes, s), "segmented prefill");
+        return launched(launch_tc_prefill(p, s), "tensor-core prefill");
+    }
     return launched(launch_recurrent(dtype, dk, dv, p, s), "recurrent prefill");
 }
 
@@ -205,8 +213,8 @@ const char *kda_status_string(kda_status status) {
 const char *kda_last_error(void) { return g_last_error; }
 
 size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv, int n_seqs) {
-    (void)dtype; (void)B; (void)T; (void)H; (void)dk; (void)dv; (void)n_seqs;
-    return 0;
+    if (B < 0 || T < 0 || H < 0) return 0;
+    return segmented_workspace_bytes(dtype, B, T, H, dk, dv, n_seqs != B);
 }
 
 kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,
@@ -214,10 +222,8 @@ kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int dv, con
                        const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,
                        float *final_state, void *workspace, size_t workspace_bytes,
                        kda_stream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     return prefill_impl(dtype, B, T, H, dk, dv, q, k, v, g, beta, cu_seqlens, n_seqs, initial_state, o,
-                        final_state, 0.f, stream);
+                        final_state, 0.f, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_prefill_gated(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,
@@ -225,12 +231,10 @@ kda_status kda_prefill_gated(kda_dtype dtype, int B, int T, int H, int dk, int d
                              const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,
                              float *final_state, float gate_bound, void *workspace, size_t workspace_bytes,
                              kda_stream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     if (!(gate_bound > 0.f && gate_bound <= 1e4f))
         return fail(KDA_ERR_INVALID_ARG, "gate_bound=%g must be in (0, 1e4]", (double)gate_bound);
     return prefill_impl(dtype, B, T, H, dk, dv, q, k, v, gate_logits, beta, cu_seqlens, n_seqs, initial_state,
-                        o, final_state, gate_bound, stream);
+                        o, final_state, gate_bound, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_decode_step(kda_dtype dtype, int N, int H, int dk, int dv, const void *q, const void *k,

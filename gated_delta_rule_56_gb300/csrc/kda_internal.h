@@ -1,6 +1,7 @@
 // kda_internal.h -- declarations shared by the translation units of libkda.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -24,6 +25,11 @@ struct RunParams {
     int n_seqs;
     unsigned *err;              // device error word
     float gate_bound;           // 0: g holds log-decays; > 0: g holds logits x, g = -gate_bound * sigmoid(x)
+    // Tensor-core kernel only (segment transitions of the segmented long-sequence prefill):
+    bool zero_v;                // v taken as 0 (the v tensor is not read)
+    bool identity_init;         // initial state = identity (needs d_k == d_v; init is not read)
+    int max_chunks;             // > 0: only the first max_chunks chunks of every sequence are run
+    const uint8_t *skip;        // non-null: the CTA of (sequence n, head h) exits at once if skip[n*H + h]
 };
 
 // Device error word of the current device (created on first use).
@@ -35,5 +41,15 @@ cudaError_t launch_recurrent(kda_dtype dtype, int dk, int dv, const RunParams &p
 // Tensor-core chunked prefill (bf16, dk == dv == 128).
 bool tc_prefill_supported(kda_dtype dtype, int dk, int dv, const RunParams &p);
 cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s);
+
+// TMA map of a bf16 [rows, H, 128] tensor in boxes of 64 rows x 64 channels (128-byte swizzle),
+// the tile of the tensor-core kernels. False if the driver's encoder is unavailable or rejects it.
+bool encode_row_tile_map(CUtensorMap *map, const void *base, long long rows, int H);
+
+// Segmented prefill of few long sequences (see kda_segmented.cu): workspace bytes it needs for
+// this call (0: the call is not eligible), and the launch sequence.
+size_t segmented_workspace_bytes(kda_dtype dtype, int B, int T, int H, int dk, int dv, bool varlen);
+cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace, size_t workspace_bytes,
+                                     cudaStream_t s);
 
 }  // namespace kda

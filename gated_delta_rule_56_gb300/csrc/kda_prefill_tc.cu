@@ -499,7 +499,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bos = (long long)n * p.T;
         eos = bos + p.T;
     }
-    const int nchunks = (int)((eos - bos + C - 1) / C);
+    int nchunks = (int)((eos - bos + C - 1) / C);
+    if (p.max_chunks > 0 && nchunks > p.max_chunks) nchunks = p.max_chunks;
+    if (p.skip && p.skip[(size_t)n * H + h]) return;
 
     if (warp == 0) {
         tmem_alloc(tptr, TM_COLS);
@@ -584,7 +586,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (nchunks > 0) {
             load_g(0);
             load_qk(0);
-            load_v(0);
+            if (!p.zero_v) load_v(0);
         }
 #pragma unroll 1
         for (int cc = 0; cc < nchunks; ++cc) {
@@ -616,23 +618,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mma_bf16_tmem_a_warp(tmem + TM_D1 + 64, tmem + TM_SA + 8 * st, d_q + ksw(st, 128), idesc_bf16(128, 64),
                                      st > 0);
             mma_commit_warp(&bars[BAR_KQFREE]);
-            // ... U^T = V^T T^T once T exists (V tile as an MN-major A operand) ...
+            // ... U^T = V^T T^T once T exists (V tile as an MN-major A operand; skipped for v = 0) ...
             if (!(iok = wait(BAR_TREADY, par))) break;
-            if (!(iok = wait(BAR_V, par))) break;
-            tc_fence_after();
+            if (!p.zero_v) {
+                if (!(iok = wait(BAR_V, par))) break;
+                tc_fence_after();
 #pragma unroll
-            for (int st = 0; st < C / 16; ++st)
-                mma_bf16_warp(tmem + TM_U, d_v + kDescStepMN128 * st, d_t + kDescStepKmajor * st,
-                              idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
+                for (int st = 0; st < C / 16; ++st)
+                    mma_bf16_warp(tmem + TM_U, d_v + kDescStepMN128 * st, d_t + kDescStepKmajor * st,
+                                  idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
+            }
             // ... U^T += -(K+ S)^T T^T (A from TMEM) ...
             if (!(iok = wait(BAR_RREADY, par))) break;
             tc_fence_after();
 #pragma unroll
             for (int st = 0; st < C / 16; ++st)
                 mma_bf16_tmem_a_warp(tmem + TM_U, tmem + TM_RA + 8 * st, d_t + kDescStepKmajor * st,
-                                     idesc_bf16(128, 64), 1u);
+                                     idesc_bf16(128, 64), (!p.zero_v || st > 0) ? 1u : 0u);
             mma_commit_warp(&bars[BAR_M2]);
-            if (more) {  // the v tile is consumed: fetch the next one
+            if (more && !p.zero_v) {  // the v tile is consumed: fetch the next one
                 if (!(iok = wait(BAR_M2, par))) break;
                 load_v(cc + 1);
             }
@@ -673,7 +677,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int k0 = 32 * cb;
             float buf[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) buf[i] = p.init ? __ldcs(p.init + state_off + (size_t)(k0 + i) * D + v) : 0.f;
+            for (int i = 0; i < 32; ++i)
+                buf[i] = p.identity_init ? (k0 + i == v ? 1.f : 0.f)
+                                         : (p.init ? __ldcs(p.init + state_off + (size_t)(k0 + i) * D + v) : 0.f);
             tmem_st32(tmem + tq + TM_S + k0, buf);
         }
         tmem_st_wait();
@@ -1050,6 +1056,10 @@ bool encode_map(CUtensorMap *map, const void *base, long long rows, int H) {
 }
 
 }  // namespace
+
+bool encode_row_tile_map(CUtensorMap *map, const void *base, long long rows, int H) {
+    return encode_map(map, base, rows, H);
+}
 
 bool tc_prefill_supported(kda_dtype dtype, int dk, int dv, const RunParams &p) {
     if (dtype != KDA_BF16 || dk != D || dv != D) return false;

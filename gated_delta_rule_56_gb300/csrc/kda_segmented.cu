@@ -1,0 +1,404 @@
+// kda_segmented.cu -- prefill of a few long sequences, split along the sequence so that more
+// CTAs than (sequence, head) pairs share the work.
+//
+// The recurrence of "Kimi Delta Attention: the linear core" (maidul-haque blog) is linear in the
+// state: over a segment p of a sequence, S_t = M_{p,t} S_start + S^loc_t, where S^loc_t is the
+// state reached from zero and M_{p,t} the product of the segment's per-token transitions
+// (I - beta k k^T) Diag(exp g) up to t. The read-out is then
+//     o_t = S_t^T q_t = (S^loc_t)^T q_t + S_start^T (M_{p,t}^T q_t) = o^loc_t + S_start^T qt_t.
+// Both parts come from the chunked tensor-core kernel run over the segments as independent
+// sequences: from a zero state (o^loc, S^loc at the segment end), and with v = 0 from the identity
+// (its read-out is qt_t = M_{p,t}^T q_t, its final state the segment transition M_p). Then
+//     S_start of segment 0 = the initial state,  S_start of p + 1 = M_p S_start(p) + S^loc(p)
+// (a short scan per (sequence, head), which also gives the final state), and one GEMM per tile
+// of tokens adds S_start^T qt_t to o^loc. Exact up to rounding; at most twice the work of one
+// pass, spread over P times as many CTAs.
+//
+// The transition run first covers only the first kHorizon rows of every segment. With v = 0 a
+// state that is exactly zero stays exactly zero (every later MMA multiplies zeros), so where M is
+// all zeros after the horizon, every later qt_t and the segment transition are exactly zero and
+// the rest of the run is skipped. Only the (segment, head) pairs whose M is not yet zero (slowly
+// decaying gates) run the whole segment again.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kda_internal.h"
+#include "kda_tc.cuh"
+
+namespace kda {
+namespace {
+
+using namespace tc;
+
+constexpr int D = 128;                      // d_k == d_v
+constexpr int CT = 128;                     // tokens per correction tile
+constexpr int kMinSegRows = 32 * 64;        // segments of at least 32 chunks
+constexpr int kMaxSegments = 8;
+constexpr int kHorizon = 4 * 64;            // rows of the first transition run
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
+
+struct Plan {
+    int P = 0;        // segments per sequence
+    int Ls = 0;       // rows per segment (the last one may be shorter)
+    size_t off_cu = 0, off_qt = 0, off_sloc = 0, off_mtr = 0, off_sst = 0, off_done = 0, bytes = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Segment count and workspace layout, or P == 0 when a single pass is the better choice.
+Plan make_plan(int B, int T, int H) {
+    Plan pl;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return pl;
+    const long long pairs = (long long)B * H;
+    if (pairs <= 0 || T <= 0) return pl;
+    long long P = sms / pairs;
+    if (P > kMaxSegments) P = kMaxSegments;
+    if (P > T / kMinSegRows) P = T / kMinSegRows;
+    if (P < 2) return pl;
+    const long long per = (T + P - 1) / P;
+    pl.Ls = (int)((per + 63) / 64 * 64);
+    pl.P = (int)((T + pl.Ls - 1) / pl.Ls);
+    const long long segs = (long long)B * pl.P;
+    size_t off = 0;
+    pl.off_cu = off;
+    off = align256(off + (size_t)(segs + 1) * 4);
+    pl.off_qt = off;
+    off = align256(off + (size_t)B * T * H * D * 2);
+    pl.off_sloc = off;
+    off = align256(off + (size_t)segs * H * D * D * 4);
+    pl.off_mtr = off;
+    off = align256(off + (size_t)segs * H * D * D * 4);
+    pl.off_sst = off;
+    off = align256(off + (size_t)segs * H * D * D * 2);
+    pl.off_done = off;
+    off = align256(off + (size_t)segs * H);
+    pl.bytes = off;
+    return pl;
+}
+
+// cu_seqlens of the segments as packed sequences: segment p of sequence b covers rows
+// b*T + p*Ls .. b*T + min((p+1)*Ls, T) - 1.
+__global__ void seg_bounds_kernel(int32_t *cu, int B, int T, int P, int Ls) {
+    const int n = B * P;
+    for (int i = threadIdx.x; i <= n; i += blockDim.x) {
+        if (i == n) {
+            cu[i] = B * T;
+        } else {
+            const int b = i / P, p = i % P;
+            cu[i] = b * T + p * Ls;
+        }
+    }
+}
+
+// done[i] = 1 when the transition of (segment, head) i after the horizon is exactly zero (nothing
+// further to compute), else 0. One CTA of 256 threads per pair.
+__global__ void __launch_bounds__(256) seg_done_kernel(const float *__restrict__ mtr, uint8_t *__restrict__ done) {
+    const float4 *m = reinterpret_cast<const float4 *>(mtr + (size_t)blockIdx.x * D * D);
+    bool zero = true;
+    for (int e = threadIdx.x; e < D * D / 4; e += 256) {
+        const float4 x = m[e];
+        zero = zero && x.x == 0.f && x.y == 0.f && x.z == 0.f && x.w == 0.f;
+    }
+    zero = __syncthreads_and(zero) != 0;
+    if (threadIdx.x == 0) done[blockIdx.x] = zero ? 1 : 0;
+}
+
+// One CTA per (sequence b, head h): S_start(0) = init (or 0), S_start(p+1) = M_p S_start(p) + S^loc(p);
+// S_start(p) is stored transposed in bf16 (the B operand of the correction GEMM), and the state
+// after the last segment is the final state. Thread (ti, tj) owns the 8 x 8 block at (8 ti, 8 tj).
+__global__ void __launch_bounds__(256) seg_scan_kernel(const float *__restrict__ mtr, const float *__restrict__ sloc,
+                                                       const float *__restrict__ init, float *__restrict__ fin,
+                                                       __nv_bfloat16 *__restrict__ sst, int P, int H) {
+    extern __shared__ float S[];  // [128][132]
+    constexpr int LD = 132;
+    const int bh = blockIdx.x, b = bh / H, h = bh % H, tid = threadIdx.x;
+    const int ti = tid >> 4, tj = tid & 15;
+    for (int e = tid; e < D * D; e += 256)
+        S[(e >> 7) * LD + (e & 127)] = init ? init[(size_t)bh * D * D + e] : 0.f;
+    __syncthreads();
+#pragma unroll 1
+    for (int p = 0; p < P; ++p) {
+        const size_t s = (size_t)(b * P + p) * H + h;
+        for (int e = tid; e < D * D; e += 256) {  // S_start^T: row v, column k
+            const int v = e >> 7, k = e & 127;
+            sst[s * D * D + e] = __float2bfloat16_rn(S[k * LD + v]);
+        }
+        const float *M = mtr + s * D * D, *L = sloc + s * D * D;
+        float acc[8][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = L[(8 * ti + i) * D + 8 * tj + j];
+#pragma unroll 2
+        for (int k = 0; k < D; ++k) {
+            float a[8], c[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = M[(8 * ti + i) * D + k];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) c[j] = S[k * LD + 8 * tj + j];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], c[j], acc[i][j]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) S[(8 * ti + i) * LD + 8 * tj + j] = acc[i][j];
+        __syncthreads();
+    }
+    if (fin)
+        for (int e = tid; e < D * D; e += 256) fin[(size_t)bh * D * D + e] = S[(e >> 7) * LD + (e & 127)];
+}
+
+// Offset of the 16-byte chunk (row r, channels 8j..8j+7) of an R-row operand in the
+// 128-byte-swizzled K-major layout (the layout of the TMA tiles).
+__device__ __forceinline__ uint32_t sw_chunk(int r, int j, int R) {
+    return (uint32_t)((j >> 3) * (R * 128) + (r >> 3) * 1024 + (r & 7) * 128 + (((j & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint64_t ksw(int st, uint32_t rows) {
+    return (uint64_t)(((uint32_t)(st >> 2) * rows * 128u + (uint32_t)(st & 3) * 32u) >> 4);
+}
+
+// max |x| over a block of 128 threads; a NaN anywhere makes the result NaN.
+__device__ __forceinline__ float block_absmax(float m, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float t = __shfl_xor_sync(0xffffffffu, m, o);
+        m = (t > m || t != t) ? t : m;
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) r = (red[w] > r || red[w] != red[w]) ? red[w] : r;
+    return r;
+}
+
+__device__ __forceinline__ float absmax_bf16x8(const uint4 w, float m) {
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float lo = fabsf(__uint_as_float(ww[e] << 16)), hi = fabsf(__uint_as_float(ww[e] & 0xffff0000u));
+        m = (lo > m || lo != lo) ? lo : m;
+        m = (hi > m || hi != hi) ? hi : m;
+    }
+    return m;
+}
+
+// o[t] += S_start^T qt[t] over kTilesPerCta tiles of 128 tokens of segment p (blockIdx.y = b * P + p)
+// and head blockIdx.z: per tile D = qt_tile (128 x 128) x S_start (128 x 128) on the tensor core
+// (A: the qt tile by TMA, B: S_start^T, loaded once), then o read, added and written back row by
+// row (thread = token). A tile whose correction is bounded by 128 max|S_start| max|qt| < 1e-30 is
+// left as it is (qt decays with the segment transition; such a term cannot change a bf16 output).
+constexpr int kTilesPerCta = 8;
+constexpr float kNegligible = 1e-30f;
+
+__global__ void __launch_bounds__(128) seg_correct_kernel(const __grid_constant__ CUtensorMap qt_map,
+                                                          const __nv_bfloat16 *__restrict__ sst,
+                                                          const uint8_t *__restrict__ done,
+                                                          __nv_bfloat16 *__restrict__ o, int T, int H, int Ls,
+                                                          int P, int p0, unsigned *err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sA = sm, *sB = sm + 32768;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + 65536);
+    uint32_t *tptr = reinterpret_cast<uint32_t *>(sm + 65536 + 16);
+    float *red = reinterpret_cast<float *>(sm + 65536 + 32);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seg = blockIdx.y, b = seg / P, p = seg % P, h = blockIdx.z;
+    if (p < p0) return;  // S_start is zero: nothing to add
+    const long long lo = (long long)p * Ls;
+    // qt is exactly zero past the horizon where the transition run stopped early (and not stored).
+    const long long hi = min(lo + (done[(size_t)seg * H + h] ? (long long)kHorizon : (long long)Ls), (long long)T);
+    const long long first = lo + (long long)blockIdx.x * kTilesPerCta * CT;
+    if (first >= hi) return;
+
+    if (warp == 0) {
+        tmem_alloc(tptr, 128);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+    }
+    const __nv_bfloat16 *src = sst + ((size_t)seg * H + h) * D * D;
+    float smax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int idx = tid + 128 * i, r = idx >> 4, j = idx & 15;
+        const uint4 w = *reinterpret_cast<const uint4 *>(src + r * D + 8 * j);
+        smax = absmax_bf16x8(w, smax);
+        *reinterpret_cast<uint4 *>(sB + sw_chunk(r, j, 128)) = w;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tptr;
+    smax = block_absmax(smax, red);
+
+    bool ok = true;
+    uint32_t ncopy = 0, nmma = 0;  // copies and MMA groups issued (their barrier phases)
+    const uint64_t da = sdesc_sw128(smem_u32(sA), 16u, 1024u), db = sdesc_sw128(smem_u32(sB), 16u, 1024u);
+#pragma unroll 1
+    for (int t = 0; t < kTilesPerCta && ok; ++t) {
+        const long long r0 = first + (long long)t * CT;
+        if (r0 >= hi) break;
+        const int nrows = (int)min((long long)CT, hi - r0);
+        const long long row = (long long)b * T + r0;  // packed row of the tile start
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bars[0], 32768);
+            for (int rb = 0; rb < 2; ++rb)
+                for (int cb = 0; cb < 2; ++cb)  // rows past the tensor read as 0; past the segment are not stored
+                    tma_load_3d(sA + cb * 16384 + rb * 8192, &qt_map, &bars[0], 64 * cb, h, (int)(row + 64 * rb));
+        }
+        ok = __syncthreads_and(mbar_wait(&bars[0], ncopy & 1u, kWaitNs)) != 0;
+        ++ncopy;
+        if (!ok) break;
+        float qmax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) qmax = absmax_bf16x8(*reinterpret_cast<const uint4 *>(sA + 16 * (tid + 128 * i)), qmax);
+        qmax = block_absmax(qmax, red);
+        if (qmax * smax * 128.f < kNegligible) {  // false for NaN: a NaN is always propagated
+            __syncthreads();                      // everyone has read sA before the next copy
+            continue;
+        }
+        if (warp == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < D / 16; ++st)
+                mma_bf16_warp(tmem, da + ksw(st, 128), db + ksw(st, 128), idesc_bf16(128, 128), st > 0);
+            mma_commit_warp(&bars[1]);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars[1], nmma & 1u, kWaitNs)) != 0;
+        ++nmma;
+        if (!ok) break;
+        tc_fence_after();
+        const int rl = 32 * warp + lane;  // tile row = TMEM lane
+        __nv_bfloat16 *orow = o + ((size_t)(row + rl) * H + h) * D;
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+            float acc[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * cb, acc);
+            tmem_ld_wait();
+            if (rl < nrows) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 w = *reinterpret_cast<const uint4 *>(orow + 32 * cb + 8 * q);
+                    uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo_v = __uint_as_float(ww[e] << 16) + acc[8 * q + 2 * e];
+                        const float hi_v = __uint_as_float(ww[e] & 0xffff0000u) + acc[8 * q + 2 * e + 1];
+                        ww[e] = pack_bf16(lo_v, hi_v);
+                    }
+                    *reinterpret_cast<uint4 *>(orow + 32 * cb + 8 * q) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();  // TMEM read out and sA consumed before the next tile
+        tc_fence_after();
+    }
+    if (!ok && tid == 0) {  // a wait ran out: record it, and leave nothing in flight (bounded)
+        atomicOr(err, kErrTimeout);
+        (void)mbar_wait(&bars[0], (ncopy - 1) & 1u, kWaitNs);
+        if (nmma) (void)mbar_wait(&bars[1], (nmma - 1) & 1u, kWaitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+constexpr int kScanSmem = 128 * 132 * 4;
+constexpr int kCorrectSmem = 65536 + 64 + 1024;  // A, B, barriers, TMEM address, block max
+
+}  // namespace
+
+size_t segmented_workspace_bytes(kda_dtype dtype, int B, int T, int H, int dk, int dv, bool varlen) {
+    if (dtype != KDA_BF16 || dk != D || dv != D || varlen) return 0;
+    if ((long long)B * T >= 0x7fffffffLL - 64) return 0;
+    return make_plan(B, T, H).bytes;
+}
+
+cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace, size_t workspace_bytes,
+                                     cudaStream_t s) {
+    const int T = p.T, H = p.H;
+    const Plan pl = make_plan(B, T, H);
+    if (pl.P < 2 || workspace_bytes < pl.bytes || !workspace) return cudaErrorInvalidValue;
+    static std::mutex mu;
+    static bool attr_set[256] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+        if (!attr_set[dev]) {
+            e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(seg_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCorrectSmem);
+            if (e != cudaSuccess) return e;
+            attr_set[dev] = true;
+        }
+    }
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *cu = reinterpret_cast<int32_t *>(ws + pl.off_cu);
+    __nv_bfloat16 *qt = reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_qt);
+    float *sloc = reinterpret_cast<float *>(ws + pl.off_sloc);
+    float *mtr = reinterpret_cast<float *>(ws + pl.off_mtr);
+    __nv_bfloat16 *sst = reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_sst);
+    uint8_t *done = ws + pl.off_done;
+    const int segs = B * pl.P;
+
+    seg_bounds_kernel<<<1, 256, 0, s>>>(cu, B, T, pl.P, pl.Ls);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // Pass 1: the segments from a zero state (o^loc into o, S^loc into the workspace).
+    RunParams pa = p;
+    pa.cu_seqlens = cu;
+    pa.n_seqs = segs;
+    pa.T = B * T;
+    pa.init = nullptr;
+    pa.fin = sloc;
+    pa.zero_v = false;
+    pa.identity_init = false;
+    pa.max_chunks = 0;
+    pa.skip = nullptr;
+    if ((e = launch_tc_prefill(pa, s)) != cudaSuccess) return e;
+    // Pass 2: v = 0 from the identity (qt = M^T q into the workspace, M at the segment ends): first
+    // up to the horizon, then, for the pairs whose M is not zero there, over the whole segment.
+    RunParams pb = pa;
+    pb.zero_v = true;
+    pb.identity_init = true;
+    pb.o = qt;
+    pb.fin = mtr;
+    pb.max_chunks = kHorizon / 64;
+    if ((e = launch_tc_prefill(pb, s)) != cudaSuccess) return e;
+    seg_done_kernel<<<(unsigned)(segs * H), 256, 0, s>>>(mtr, done);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    pb.max_chunks = 0;
+    pb.skip = done;
+    if ((e = launch_tc_prefill(pb, s)) != cudaSuccess) return e;
+    // Start states of the segments and the final state.
+    seg_scan_kernel<<<(unsigned)(B * H), 256, kScanSmem, s>>>(mtr, sloc, p.init, p.fin, sst, pl.P, H);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // o += S_start^T qt, skipped for segment 0 when the initial state is zero.
+    CUtensorMap qt_map;
+    if (!encode_row_tile_map(&qt_map, qt, (long long)B * T, H)) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)((pl.Ls + CT * kTilesPerCta - 1) / (CT * kTilesPerCta)), (unsigned)segs, (unsigned)H);
+    seg_correct_kernel<<<grid, 128, kCorrectSmem, s>>>(qt_map, sst, done, static_cast<__nv_bfloat16 *>(p.o), T, H,
+                                                       pl.Ls, pl.P, p.init ? 0 : 1, p.err);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

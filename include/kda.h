@@ -76,8 +76,15 @@ typedef enum {
  * initial_state  fp32 [N, H, dk, dv] or NULL (zero state).
  * o            output [B, T, H, dv], same dtype as the inputs. Every row is written.
  * final_state  fp32 [N, H, dk, dv] or NULL (not written). May alias initial_state.
- * workspace, workspace_bytes  device scratch of at least kda_prefill_workspace_size() bytes
- *              (NULL / 0 when that size is 0).
+ * workspace, workspace_bytes  device scratch, 256-byte aligned, of at least
+ *              kda_prefill_workspace_size() bytes; or NULL / 0. Only a split call uses it: when
+ *              few long sequences cannot fill the GPU (bf16, dk == dv == 128, no cu_seqlens), each
+ *              is cut into segments run side by side and joined through the segment transitions
+ *              (the state after a segment is linear in the state before it: "Inside Kimi K3's
+ *              Architecture", "Kimi Delta Attention: the linear core"). Without a large enough
+ *              workspace the same call runs one pass per sequence, with the same result up to
+ *              rounding. The caller owns the workspace; it must not be used by other work on
+ *              other streams until this call's work is done.
  * Alignment: all pointers 16-byte aligned. Rows of q, k, v, g, o are contiguous.
  * Returns KDA_OK once the work is queued on `stream`.
  */
@@ -87,7 +94,10 @@ KDA_API kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int
                        const float *initial_state, void *o, float *final_state,
                        void *workspace, size_t workspace_bytes, kda_stream_t stream);
 
-/* Bytes of device workspace kda_prefill needs for these sizes (0 when none). */
+/* Bytes of device workspace with which kda_prefill splits these sizes along the sequence, or 0
+ * when it would not split them. The split follows the current device's SM count (0 when no device
+ * is visible). n_seqs != B means packed sequences (cu_seqlens), which are never split, so 0; a
+ * packed call needs no workspace whatever this returns. The same sizes apply to kda_prefill_gated. */
 KDA_API size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv,
                                   int n_seqs);
 

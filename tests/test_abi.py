@@ -39,8 +39,12 @@ def test_status_strings_and_version(lib):
     assert kda.version() >= 10000
 
 
-def test_workspace_size_is_zero(lib):
+def test_workspace_size_is_zero_when_not_split(lib):
+    # Many (sequence, head) pairs, packed sequences, fp32 or small heads: one pass, no workspace.
     assert lib.kda_prefill_workspace_size(0, 4, 8192, 32, 128, 128, 4) == 0
+    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 128, 128, 64) == 0   # varlen
+    assert lib.kda_prefill_workspace_size(1, 1, 1 << 20, 32, 128, 128, 1) == 0    # fp32
+    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 64, 64, 1) == 0      # d = 64
 
 
 FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: validation fails first
