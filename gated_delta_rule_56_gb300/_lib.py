@@ -76,6 +76,11 @@ def load():
         lib.kda_decode_step_gated.argtypes = [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                               ctypes.c_float, _vp]
         lib.kda_decode_step_gated.restype = _i
+        lib.kda_prefill_noalloc.argtypes = [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp,
+                                            _vp, _vp, _vp]
+        lib.kda_prefill_noalloc.restype = _i
+        lib.kda_prefill_noalloc_capacity.argtypes = []
+        lib.kda_prefill_noalloc_capacity.restype = ctypes.c_size_t
         lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _vp]
         lib.kda_selftest_wait_timeout.restype = _i
         _lib = lib

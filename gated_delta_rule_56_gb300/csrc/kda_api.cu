@@ -69,6 +69,32 @@ kda_status launched(cudaError_t e, const char *what) {
     return ok();
 }
 
+// Scratch of kda_prefill_noalloc: one array per device, placed when the module loads, so that
+// the call allocates nothing. 32 MiB holds the split of about 100 K token-heads.
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+__device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+struct StaticScratch {
+    void *addr = nullptr;
+    cudaEvent_t last = nullptr;  // recorded after the latest call that used the scratch
+};
+
+// Looks up the scratch address and creates the ordering event once per device.
+StaticScratch *static_scratch(int dev) {
+    static StaticScratch slots[256];
+    if (dev < 0 || dev >= 256) return nullptr;
+    StaticScratch &sc = slots[dev];
+    if (!sc.addr) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess) return nullptr;
+        if (cudaEventCreateWithFlags(&sc.last, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+        sc.addr = addr;
+    }
+    return &sc;
+}
+
+std::mutex g_static_scratch_mu;
+
 }  // namespace
 
 unsigned *device_error_word() {
@@ -235,6 +261,38 @@ kda_status kda_prefill_gated(kda_dtype dtype, int B, int T, int H, int dk, int d
         return fail(KDA_ERR_INVALID_ARG, "gate_bound=%g must be in (0, 1e4]", (double)gate_bound);
     return prefill_impl(dtype, B, T, H, dk, dv, q, k, v, gate_logits, beta, cu_seqlens, n_seqs, initial_state,
                         o, final_state, gate_bound, workspace, workspace_bytes, stream);
+}
+
+size_t kda_prefill_noalloc_capacity(void) { return kStaticScratchBytes; }
+
+kda_status kda_prefill_noalloc(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,
+                               const void *k, const void *v, const void *g, const void *beta,
+                               const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,
+                               float *final_state, kda_stream_t stream) {
+    const size_t need = (B < 0 || T < 0 || H < 0)
+                            ? 0
+                            : segmented_workspace_bytes(dtype, B, T, H, dk, dv, cu_seqlens != nullptr);
+    if (need > kStaticScratchBytes)
+        return fail(KDA_ERR_UNSUPPORTED, "this call needs %zu bytes of scratch; the static scratch holds %zu",
+                    need, kStaticScratchBytes);
+    if (need == 0)
+        return prefill_impl(dtype, B, T, H, dk, dv, q, k, v, g, beta, cu_seqlens, n_seqs, initial_state, o,
+                            final_state, 0.f, nullptr, 0, stream);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    StaticScratch *sc = static_scratch(dev);
+    if (!sc) return fail(KDA_ERR_CUDA, "static scratch: %s", cudaGetErrorString(cudaGetLastError()));
+    // Calls on different streams share the scratch: each waits for the previous one's work.
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((e = cudaStreamWaitEvent(s, sc->last, 0)) != cudaSuccess)
+        return fail(KDA_ERR_CUDA, "ordering on the static scratch: %s", cudaGetErrorString(e));
+    const kda_status st = prefill_impl(dtype, B, T, H, dk, dv, q, k, v, g, beta, cu_seqlens, n_seqs,
+                                       initial_state, o, final_state, 0.f, sc->addr, kStaticScratchBytes, stream);
+    if (st == KDA_OK && (e = cudaEventRecord(sc->last, s)) != cudaSuccess)
+        return fail(KDA_ERR_CUDA, "ordering on the static scratch: %s", cudaGetErrorString(e));
+    return st;
 }
 
 kda_status kda_decode_step(kda_dtype dtype, int N, int H, int dk, int dv, const void *q, const void *k,

@@ -102,6 +102,25 @@ KDA_API size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, 
                                   int n_seqs);
 
 /*
+ * kda_prefill_noalloc -- kda_prefill without a caller workspace and without any allocation: a
+ * call that is split along the sequence uses a fixed scratch array compiled into the library
+ * (one per device, kda_prefill_noalloc_capacity() bytes, placed when the library's device code
+ * is loaded). The pages describe no such call; it exists for callers that cannot hand over
+ * device memory. Arguments as kda_prefill, without workspace / workspace_bytes; results
+ * identical to kda_prefill with a workspace. Returns KDA_ERR_UNSUPPORTED, before anything is
+ * queued, when kda_prefill_workspace_size() for the call exceeds the capacity. Calls that use the
+ * scratch are ordered on the device (each waits for the previous one, whatever its stream).
+ */
+KDA_API kda_status kda_prefill_noalloc(kda_dtype dtype, int B, int T, int H, int dk, int dv,
+                                       const void *q, const void *k, const void *v, const void *g,
+                                       const void *beta, const int32_t *cu_seqlens, int n_seqs,
+                                       const float *initial_state, void *o, float *final_state,
+                                       kda_stream_t stream);
+
+/* Bytes of the fixed scratch array kda_prefill_noalloc uses. */
+KDA_API size_t kda_prefill_noalloc_capacity(void);
+
+/*
  * kda_decode_step -- one token of the recurrence for N independent sequences.
  *
  * q, k, g  [N, H, dk]; v [N, H, dv]; beta [N, H]; o [N, H, dv]; all `dtype`.

@@ -47,6 +47,12 @@ def test_workspace_size_is_zero_when_not_split(lib):
     assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 64, 64, 1) == 0      # d = 64
 
 
+def test_noalloc_capacity_and_argument_checks(lib):
+    assert lib.kda_prefill_noalloc_capacity() == 32 << 20
+    # Sizes are checked before the scratch is looked at (no device needed to reject them).
+    assert lib.kda_prefill_noalloc(0, -1, 8, 1, 128, 128, *([None] * 6), 1, None, None, None, None) == 1
+
+
 FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: validation fails first
 
 

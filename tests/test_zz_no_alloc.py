@@ -1,0 +1,56 @@
+"""kda_prefill_noalloc: the prefill without a caller workspace, on the library's fixed scratch
+array. Its results must equal kda_prefill's with a workspace, call after call."""
+
+import pytest
+import torch
+
+import gated_delta_rule_56_gb300 as kda
+import kda_inputs as ki
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+NAMES = ("q", "k", "v", "g", "beta")
+KDA_ERR_UNSUPPORTED = 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return kda.load()
+
+
+def _noalloc(lib, x, B, T, H, init):
+    o = torch.full_like(x["v"], float("nan"))
+    fin = torch.full((B, H, 128, 128), float("nan"), device=DEV)
+    st = lib.kda_prefill_noalloc(0, B, T, H, 128, 128, *(x[n].data_ptr() for n in NAMES), None, B,
+                                 None if init is None else init.data_ptr(), o.data_ptr(), fin.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+    return st, o, fin
+
+
+@pytest.mark.parametrize("B,T,H", [(1, 8192, 2), (2, 300, 3)])
+def test_noalloc_equals_prefill_on_two_calls(lib, B, T, H):
+    need = lib.kda_prefill_workspace_size(0, B, T, H, 128, 128, B)
+    assert need <= lib.kda_prefill_noalloc_capacity()
+    if T == 8192:
+        assert need > 0, "this shape should be split along the sequence (and use the scratch)"
+    for seed in (61, 62):
+        x = ki.prefill_inputs(B, T, H, 128, 128, device=DEV, seed=seed, state_std=0.02)
+        init = x["initial_state"]
+        o_ref, s_ref = kda.prefill(*(x[n] for n in NAMES), initial_state=init)
+        st, o, fin = _noalloc(lib, x, B, T, H, init)
+        assert st == 0, lib.kda_last_error()
+        kda.check_status()
+        assert torch.equal(o, o_ref)
+        assert torch.equal(fin, s_ref)
+
+
+def test_noalloc_rejects_a_call_larger_than_its_scratch(lib):
+    B, T, H = 1, 65536, 2
+    need = lib.kda_prefill_workspace_size(0, B, T, H, 128, 128, B)
+    assert need > lib.kda_prefill_noalloc_capacity()
+    x = ki.prefill_inputs(B, T, H, 128, 128, device=DEV, seed=63)
+    st, o, _fin = _noalloc(lib, x, B, T, H, None)
+    assert st == KDA_ERR_UNSUPPORTED
+    assert b"static scratch" in lib.kda_last_error()
+    kda.check_status()
+    assert torch.isnan(o).all(), "nothing may be queued for a rejected call"
