@@ -12,6 +12,7 @@ Public functions take CPU tensors or arrays in the KDA layouts and return fp64 n
 * ``chunked(..., chunk=64, dump=False)`` -> (o, final_state[, intermediates])
 * ``decode_step(q, k, v, g, beta, state)`` -> (o, new_state): one token of the recurrence.
 * ``scaled_sigmoid_gate(x, bound)`` -> g = -bound * sigmoid(x) (log-decays from gate logits).
+* ``l2_normalize(x, eps=1e-6)`` -> rows along the last axis divided by sqrt(sum x^2 + eps).
 
 Layouts: q, k, g [B, T, H, d_k]; v [B, T, H, d_v]; beta [B, T, H]; with ``cu_seqlens``
 (int [N+1]) B must be 1 and the rows of sequence n are cu[n]..cu[n+1]-1. States are
@@ -53,6 +54,8 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
 def _declare(lib):
     lib.kda_oracle_scaled_sigmoid_gate.argtypes = [ctypes.c_int64, _dp, ctypes.c_double, _dp]
     lib.kda_oracle_scaled_sigmoid_gate.restype = ctypes.c_int
+    lib.kda_oracle_l2_normalize.argtypes = [ctypes.c_int64, ctypes.c_int64, _dp, ctypes.c_double, _dp]
+    lib.kda_oracle_l2_normalize.restype = ctypes.c_int
     lib.kda_oracle_recurrent.argtypes = [ctypes.c_int, _i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
     lib.kda_oracle_recurrent.restype = ctypes.c_int
@@ -192,6 +195,18 @@ def scaled_sigmoid_gate(x, bound):
     if rc != 0:
         raise ValueError(f"kda_oracle_scaled_sigmoid_gate returned {rc}")
     return g
+
+
+def l2_normalize(x, eps=1e-6):
+    """Each row along the last axis divided by sqrt(sum of squares + eps), fp64, same shape."""
+    x = _f64(x)
+    y = np.empty_like(x)
+    d = x.shape[-1] if x.ndim else 0
+    rows = x.size // d if d else 0
+    rc = load_library().kda_oracle_l2_normalize(rows, d, x.ctypes.data_as(_dp), float(eps), y.ctypes.data_as(_dp))
+    if rc != 0:
+        raise ValueError(f"kda_oracle_l2_normalize returned {rc}")
+    return y
 
 
 def decode_step(q, k, v, g, beta, state, n_threads=0):

@@ -30,6 +30,10 @@
  *                           per element ("Kimi K3 Explained", researchpapers.dev, "Architecture
  *                           at a glance": the log-decay is bounded below through a scaled
  *                           sigmoid); the bound's value is not on the pages (the workloads use 5).
+ *  kda_oracle_l2_normalize -- each row of d values divided by sqrt(sum of its squares + eps).
+ *                           The pages do not describe this step; the workloads feed q and k as
+ *                           unit vectors per (token, head), and the library can form them in its
+ *                           kernels. The eps (1e-6 there) only keeps a zero row finite.
  *  kda_oracle_chunked    -- a separately written chunkwise form of the same recurrence
  *                           (per-chunk cumulative log-decay, the strictly lower intra-chunk
  *                           matrix, a triangular solve for the delta corrections, one state
@@ -352,6 +356,18 @@ int kda_oracle_scaled_sigmoid_gate(int64_t n, const double *x, double bound, dou
     for (int64_t i = 0; i < n; ++i) {
         const double sig = 1.0 / (1.0 + exp(-x[i]));  /* the logistic function */
         g[i] = -bound * sig;
+    }
+    return 0;
+}
+
+int kda_oracle_l2_normalize(int64_t rows, int64_t d, const double *x, double eps, double *y)
+{
+    if (rows < 0 || d <= 0 || !x || !y || !(eps >= 0.0)) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        double ss = 0.0;
+        for (int64_t i = 0; i < d; ++i) ss += x[r * d + i] * x[r * d + i];
+        const double norm = sqrt(ss + eps);
+        for (int64_t i = 0; i < d; ++i) y[r * d + i] = norm > 0.0 ? x[r * d + i] / norm : 0.0;
     }
     return 0;
 }

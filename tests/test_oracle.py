@@ -271,6 +271,48 @@ def test_bad_arguments_are_rejected():
         oracle.recurrent(*_args(x), initial_state=torch.zeros(2, 1, 4, 4))
 
 
+# ---------------------------------------------------------------- q/k L2 normalisation -----
+# y = x / sqrt(sum x^2 + eps) per row. Pinned by Pythagorean rows (exact unit vectors with
+# rational entries), the closed form for a one-hot row, and invariants of a norm.
+
+def test_l2_pythagorean_rows():
+    x = np.array([[3.0, 4.0, 0.0], [1.0, 2.0, 2.0], [2.0, -3.0, 6.0], [0.0, 0.0, -5.0]])
+    y = oracle.l2_normalize(x, eps=0.0)
+    np.testing.assert_allclose(y, [[0.6, 0.8, 0.0], [1 / 3, 2 / 3, 2 / 3], [2 / 7, -3 / 7, 6 / 7], [0.0, 0.0, -1.0]],
+                               rtol=0, atol=1e-15)
+
+
+def test_l2_eps_one_hot_and_zero_rows():
+    eps = 1e-6
+    x = np.zeros((3, 128))
+    x[0, 17] = 1.0
+    x[1, 5] = -2.0
+    y = oracle.l2_normalize(x, eps=eps)
+    assert y[0, 17] == pytest.approx(1.0 / math.sqrt(1.0 + eps), rel=1e-15)
+    assert y[1, 5] == pytest.approx(-2.0 / math.sqrt(4.0 + eps), rel=1e-15)
+    assert np.count_nonzero(y[:2]) == 2 and np.all(y[2] == 0.0)  # zero row stays zero
+
+
+def test_l2_invariants():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((5, 4, 64))
+    y = oracle.l2_normalize(x, eps=0.0)
+    np.testing.assert_allclose((y * y).sum(-1), 1.0, rtol=0, atol=1e-14)           # unit rows
+    np.testing.assert_allclose(oracle.l2_normalize(3.5 * x, eps=0.0), y, rtol=0, atol=1e-15)  # scale-free
+    np.testing.assert_allclose(oracle.l2_normalize(-x, eps=0.0), -y, rtol=0, atol=0)
+    cos = (y * x).sum(-1) / np.sqrt((x * x).sum(-1))                                  # same direction
+    np.testing.assert_allclose(cos, 1.0, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(oracle.l2_normalize(x[2, 1], eps=0.0), y[2, 1], rtol=0, atol=0)  # rows independent
+    ye = oracle.l2_normalize(x, eps=1e-6)                                             # eps shrinks the norm
+    ss = (x * x).sum(-1)
+    np.testing.assert_allclose((ye * ye).sum(-1), ss / (ss + 1e-6), rtol=1e-13, atol=0)
+
+
+def test_l2_rejects_bad_eps():
+    with pytest.raises(ValueError):
+        oracle.l2_normalize(np.ones((2, 3)), eps=-1.0)
+
+
 # -------------------------------------------------------------- planted-mistake detection --
 
 _PINS = [
@@ -305,6 +347,33 @@ _MUTANTS = [
      "    for (int i = 0; i < dk; ++i)\n        for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] += k[i] * u[j];\n    /* o_t = S_t^T q_t */",
      "    /* o_t = S_t^T q_t */"),
 ]
+
+
+_L2_PINS = [test_l2_pythagorean_rows, test_l2_eps_one_hot_and_zero_rows, test_l2_invariants]
+_L2_MUTANTS = [
+    ("no square root", "const double norm = sqrt(ss + eps);", "const double norm = ss + eps;"),
+    ("eps outside the root", "const double norm = sqrt(ss + eps);", "const double norm = sqrt(ss) + eps;"),
+    ("sum of |x| instead of squares", "ss += x[r * d + i] * x[r * d + i];", "ss += fabs(x[r * d + i]);"),
+    ("row stride off by one", "ss += x[r * d + i] * x[r * d + i];", "ss += x[r * (d - 1) + i] * x[r * (d - 1) + i];"),
+    ("multiply by the norm", "y[r * d + i] = norm > 0.0 ? x[r * d + i] / norm : 0.0;",
+     "y[r * d + i] = x[r * d + i] * norm;"),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(_L2_MUTANTS)))
+def test_l2_pins_catch_planted_mistakes(tmp_path, idx):
+    desc, old, new = _L2_MUTANTS[idx]
+    text = open(oracle._SRC).read()
+    assert text.count(old) == 1, f"mutation site not found: {desc}"
+    path = _build_mutant(tmp_path, text.replace(old, new, 1), 100 + idx)
+    caught = []
+    with oracle.use_library(path):
+        for pin in _L2_PINS:
+            try:
+                pin()
+            except AssertionError:
+                caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake: {desc}"
 
 
 def _build_mutant(tmp_path, src_text, i):
