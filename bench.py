@@ -52,11 +52,12 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("varlen", "long", "gated"), default=None,
+    ap.add_argument("--workload", choices=("varlen", "long", "gated", "l2norm"), default=None,
                     help="time one of the other prefill workloads instead of the headline (one JSON line): "
                          "varlen = 64 packed sequences of U[128, 16384] tokens with initial states; "
                          "long = one sequence of 1,048,576 tokens (B=1, H=32); "
-                         "gated = the headline shape with gate logits (decays formed in the kernel)")
+                         "gated = the headline shape with gate logits (decays formed in the kernel); "
+                         "l2norm = the headline shape with raw q/k rows L2-normalised in the kernel")
     ap.add_argument("--ncu-case", choices=("prefill", "decode"),
                     help="run two launches of the small profiling case (for ncu) and exit")
     args = ap.parse_args()
@@ -452,6 +453,14 @@ def run_workload(args):
         kw = {}
         alg = prefill_bytes(1, T, H, d)
         name = f"KDA chunked prefill, long context: B=1 T={T} H={H} dk=dv={d} bf16, zero init"
+    elif args.workload == "l2norm":
+        B, T = PF["B"], PF["T"]
+        x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)
+        x["q"], x["k"] = ki.raw_qk_like(x["q"], seed=1), ki.raw_qk_like(x["k"], seed=2)
+        tokens, n_seq = B * T, B
+        kw = dict(qk_l2norm=True)
+        alg = prefill_bytes(B, T, H, d)
+        name = f"KDA chunked prefill with q/k L2 normalisation in the kernel: B={B} T={T} H={H} dk=dv={d} bf16, zero init"
     else:
         B, T = PF["B"], PF["T"]
         x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)

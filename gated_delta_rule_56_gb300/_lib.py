@@ -76,6 +76,12 @@ def load():
         lib.kda_decode_step_gated.argtypes = [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                               ctypes.c_float, _vp]
         lib.kda_decode_step_gated.restype = _i
+        lib.kda_prefill_ex.argtypes = [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp,
+                                       _vp, ctypes.POINTER(KDAOptions), _vp, ctypes.c_size_t, _vp]
+        lib.kda_prefill_ex.restype = _i
+        lib.kda_decode_step_ex.argtypes = [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                           ctypes.POINTER(KDAOptions), _vp]
+        lib.kda_decode_step_ex.restype = _i
         lib.kda_prefill_noalloc.argtypes = [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp,
                                             _vp, _vp, _vp]
         lib.kda_prefill_noalloc.restype = _i
@@ -85,6 +91,16 @@ def load():
         lib.kda_selftest_wait_timeout.restype = _i
         _lib = lib
         return lib
+
+
+class KDAOptions(ctypes.Structure):
+    """kda_options of include/kda.h (struct_size first; zero fields are the defaults)."""
+    _fields_ = [("struct_size", ctypes.c_size_t), ("gate_bound", ctypes.c_float), ("qk_l2norm", ctypes.c_int)]
+
+
+def _options(gate_bound, qk_l2norm):
+    return KDAOptions(ctypes.sizeof(KDAOptions), 0.0 if gate_bound is None else float(gate_bound),
+                      1 if qk_l2norm else 0)
 
 
 def status_string(status: int) -> str:
@@ -126,14 +142,16 @@ def _check(name, t, dtype, shape, device):
 
 
 def prefill(q, k, v, g, beta, cu_seqlens=None, initial_state=None, output_final_state=True,
-            o=None, final_state=None, gate_bound=None):
+            o=None, final_state=None, gate_bound=None, qk_l2norm=False):
     """Chunked KDA prefill on the GPU.
 
     q, k, g [B, T, H, dk]; v [B, T, H, dv]; beta [B, T, H]; all bf16 or all fp32, on one CUDA
     device. With ``cu_seqlens`` (int32 [N+1] on the device) B must be 1 and the rows are
     packed sequences. ``initial_state``: fp32 [N, H, dk, dv] or None (zeros). With
     ``gate_bound`` A, ``g`` holds gate logits x and the kernels use g = -A * sigmoid(x)
-    (kda_prefill_gated). Returns (o [B, T, H, dv], final_state [N, H, dk, dv] fp32 or None).
+    (kda_prefill_gated). With ``qk_l2norm`` the kernels divide every row of q and k by
+    sqrt(sum x^2 + 1e-6) (kda_prefill_ex). Returns (o [B, T, H, dv], final_state [N, H, dk, dv]
+    fp32 or None).
     """
     lib = load()
     if q.dtype not in _DTYPES:
@@ -167,7 +185,12 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, initial_state=None, output_final_
     ws_bytes = int(lib.kda_prefill_workspace_size(dt, B, T, H, dk, dv, N))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
     with torch.cuda.device(dev):
-        if gate_bound is None:
+        if qk_l2norm:
+            opt = _options(gate_bound, qk_l2norm)
+            st = lib.kda_prefill_ex(dt, B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                    _ptr(cu_seqlens), N, _ptr(initial_state), _ptr(o), _ptr(final_state),
+                                    ctypes.byref(opt), _ptr(ws), ws_bytes, _stream(dev))
+        elif gate_bound is None:
             st = lib.kda_prefill(dt, B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                  _ptr(cu_seqlens), N, _ptr(initial_state), _ptr(o), _ptr(final_state),
                                  _ptr(ws), ws_bytes, _stream(dev))
@@ -179,10 +202,11 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, initial_state=None, output_final_
     return o, final_state
 
 
-def decode_step(q, k, v, g, beta, state, o=None, gate_bound=None):
+def decode_step(q, k, v, g, beta, state, o=None, gate_bound=None, qk_l2norm=False):
     """One KDA decode token for N sequences; ``state`` (fp32 [N, H, dk, dv]) is updated in
     place. q, k, g [N, H, dk]; v [N, H, dv]; beta [N, H]. With ``gate_bound`` A, ``g`` holds gate
-    logits x and g = -A * sigmoid(x) is used (kda_decode_step_gated). Returns o [N, H, dv]."""
+    logits x and g = -A * sigmoid(x) is used (kda_decode_step_gated). With ``qk_l2norm`` the
+    rows of q and k are L2-normalised in the kernel (kda_decode_step_ex). Returns o [N, H, dv]."""
     lib = load()
     if q.dtype not in _DTYPES:
         raise TypeError(f"unsupported dtype {q.dtype}")
@@ -200,7 +224,11 @@ def decode_step(q, k, v, g, beta, state, o=None, gate_bound=None):
     else:
         _check("o", o, q.dtype, (N, H, dv), dev)
     with torch.cuda.device(dev):
-        if gate_bound is None:
+        if qk_l2norm:
+            opt = _options(gate_bound, qk_l2norm)
+            st = lib.kda_decode_step_ex(_DTYPES[q.dtype], N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                        _ptr(beta), _ptr(state), _ptr(o), ctypes.byref(opt), _stream(dev))
+        elif gate_bound is None:
             st = lib.kda_decode_step(_DTYPES[q.dtype], N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                      _ptr(beta), _ptr(state), _ptr(o), _stream(dev))
         else:

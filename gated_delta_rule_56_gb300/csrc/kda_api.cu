@@ -5,6 +5,7 @@
 // that passed. Conditions only the device can see are OR-ed into a per-device error word.
 #include <cstdarg>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "kda_internal.h"
@@ -118,11 +119,35 @@ using namespace kda;
 namespace kda {
 namespace {
 
-// The common body of kda_prefill and kda_prefill_gated.
+// The caller's options, read up to the size it was compiled with (later fields keep their
+// defaults), and checked. NULL means all defaults.
+kda_status read_options(const kda_options *user, kda_options &opt) {
+    opt = kda_options{};
+    opt.struct_size = sizeof(kda_options);
+    if (!user) return KDA_OK;
+    if (user->struct_size < sizeof(size_t) || user->struct_size > 4096)
+        return fail(KDA_ERR_INVALID_ARG, "kda_options.struct_size=%zu is not the size of a kda_options",
+                    user->struct_size);
+    const size_t n = user->struct_size < sizeof(kda_options) ? user->struct_size : sizeof(kda_options);
+    memcpy(&opt, user, n);
+    opt.struct_size = sizeof(kda_options);
+    if (!(opt.gate_bound == 0.f || (opt.gate_bound > 0.f && opt.gate_bound <= 1e4f)))
+        return fail(KDA_ERR_INVALID_ARG, "gate_bound=%g must be 0 or in (0, 1e4]", (double)opt.gate_bound);
+    return KDA_OK;
+}
+
+kda_options gate_only(float gate_bound) {
+    kda_options opt{};
+    opt.struct_size = sizeof(kda_options);
+    opt.gate_bound = gate_bound;
+    return opt;
+}
+
+// The common body of kda_prefill, kda_prefill_gated and kda_prefill_ex.
 kda_status prefill_impl(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,
                         const void *k, const void *v, const void *g, const void *beta,
                         const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,
-                        float *final_state, float gate_bound, void *workspace, size_t workspace_bytes,
+                        float *final_state, const kda_options &opt, void *workspace, size_t workspace_bytes,
                         kda_stream_t stream) {
     kda_status st;
     if ((st = check_dtype(dtype)) != KDA_OK) return st;
@@ -164,7 +189,8 @@ kda_status prefill_impl(kda_dtype dtype, int B, int T, int H, int dk, int dv, co
     p.H = H;
     p.n_seqs = n_seqs;
     p.err = device_error_word();
-    p.gate_bound = gate_bound;
+    p.gate_bound = opt.gate_bound;
+    p.qk_l2norm = opt.qk_l2norm != 0;
     if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word: %s",
                             cudaGetErrorString(cudaGetLastError()));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -179,10 +205,10 @@ kda_status prefill_impl(kda_dtype dtype, int B, int T, int H, int dk, int dv, co
     return launched(launch_recurrent(dtype, dk, dv, p, s), "recurrent prefill");
 }
 
-// The common body of kda_decode_step and kda_decode_step_gated.
+// The common body of kda_decode_step, kda_decode_step_gated and kda_decode_step_ex.
 kda_status decode_impl(kda_dtype dtype, int N, int H, int dk, int dv, const void *q, const void *k,
-                       const void *v, const void *g, const void *beta, float *state, void *o, float gate_bound,
-                       kda_stream_t stream) {
+                       const void *v, const void *g, const void *beta, float *state, void *o,
+                       const kda_options &opt, kda_stream_t stream) {
     kda_status st;
     if ((st = check_dtype(dtype)) != KDA_OK) return st;
     if (N < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "negative size N=%d H=%d", N, H);
@@ -206,7 +232,8 @@ kda_status decode_impl(kda_dtype dtype, int N, int H, int dk, int dv, const void
     p.H = H;
     p.n_seqs = N;
     p.err = device_error_word();
-    p.gate_bound = gate_bound;
+    p.gate_bound = opt.gate_bound;
+    p.qk_l2norm = opt.qk_l2norm != 0;
     if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word");
     return launched(launch_recurrent(dtype, dk, dv, p, reinterpret_cast<cudaStream_t>(stream)), "decode step");
 }
@@ -249,7 +276,18 @@ kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int dv, con
                        float *final_state, void *workspace, size_t workspace_bytes,
                        kda_stream_t stream) {
     return prefill_impl(dtype, B, T, H, dk, dv, q, k, v, g, beta, cu_seqlens, n_seqs, initial_state, o,
-                        final_state, 0.f, workspace, workspace_bytes, stream);
+                        final_state, gate_only(0.f), workspace, workspace_bytes, stream);
+}
+
+kda_status kda_prefill_ex(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q, const void *k,
+                          const void *v, const void *g, const void *beta, const int32_t *cu_seqlens, int n_seqs,
+                          const float *initial_state, void *o, float *final_state, const kda_options *options,
+                          void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+    kda_options opt;
+    const kda_status st = read_options(options, opt);
+    if (st != KDA_OK) return st;
+    return prefill_impl(dtype, B, T, H, dk, dv, q, k, v, g, beta, cu_seqlens, n_seqs, initial_state, o,
+                        final_state, opt, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_prefill_gated(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,
@@ -260,7 +298,7 @@ kda_status kda_prefill_gated(kda_dtype dtype, int B, int T, int H, int dk, int d
     if (!(gate_bound > 0.f && gate_bound <= 1e4f))
         return fail(KDA_ERR_INVALID_ARG, "gate_bound=%g must be in (0, 1e4]", (double)gate_bound);
     return prefill_impl(dtype, B, T, H, dk, dv, q, k, v, gate_logits, beta, cu_seqlens, n_seqs, initial_state,
-                        o, final_state, gate_bound, workspace, workspace_bytes, stream);
+                        o, final_state, gate_only(gate_bound), workspace, workspace_bytes, stream);
 }
 
 size_t kda_prefill_noalloc_capacity(void) { return kStaticScratchBytes; }
@@ -277,7 +315,7 @@ kda_status kda_prefill_noalloc(kda_dtype dtype, int B, int T, int H, int dk, int
                     need, kStaticScratchBytes);
     if (need == 0)
         return prefill_impl(dtype, B, T, H, dk, dv, q, k, v, g, beta, cu_seqlens, n_seqs, initial_state, o,
-                            final_state, 0.f, nullptr, 0, stream);
+                            final_state, gate_only(0.f), nullptr, 0, stream);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
@@ -289,7 +327,8 @@ kda_status kda_prefill_noalloc(kda_dtype dtype, int B, int T, int H, int dk, int
     if ((e = cudaStreamWaitEvent(s, sc->last, 0)) != cudaSuccess)
         return fail(KDA_ERR_CUDA, "ordering on the static scratch: %s", cudaGetErrorString(e));
     const kda_status st = prefill_impl(dtype, B, T, H, dk, dv, q, k, v, g, beta, cu_seqlens, n_seqs,
-                                       initial_state, o, final_state, 0.f, sc->addr, kStaticScratchBytes, stream);
+                                       initial_state, o, final_state, gate_only(0.f), sc->addr, kStaticScratchBytes,
+                                       stream);
     if (st == KDA_OK && (e = cudaEventRecord(sc->last, s)) != cudaSuccess)
         return fail(KDA_ERR_CUDA, "ordering on the static scratch: %s", cudaGetErrorString(e));
     return st;
@@ -298,7 +337,16 @@ kda_status kda_prefill_noalloc(kda_dtype dtype, int B, int T, int H, int dk, int
 kda_status kda_decode_step(kda_dtype dtype, int N, int H, int dk, int dv, const void *q, const void *k,
                            const void *v, const void *g, const void *beta, float *state, void *o,
                            kda_stream_t stream) {
-    return decode_impl(dtype, N, H, dk, dv, q, k, v, g, beta, state, o, 0.f, stream);
+    return decode_impl(dtype, N, H, dk, dv, q, k, v, g, beta, state, o, gate_only(0.f), stream);
+}
+
+kda_status kda_decode_step_ex(kda_dtype dtype, int N, int H, int dk, int dv, const void *q, const void *k,
+                              const void *v, const void *g, const void *beta, float *state, void *o,
+                              const kda_options *options, kda_stream_t stream) {
+    kda_options opt;
+    const kda_status st = read_options(options, opt);
+    if (st != KDA_OK) return st;
+    return decode_impl(dtype, N, H, dk, dv, q, k, v, g, beta, state, o, opt, stream);
 }
 
 kda_status kda_decode_step_gated(kda_dtype dtype, int N, int H, int dk, int dv, const void *q, const void *k,
@@ -306,7 +354,7 @@ kda_status kda_decode_step_gated(kda_dtype dtype, int N, int H, int dk, int dv, 
                                  float gate_bound, kda_stream_t stream) {
     if (!(gate_bound > 0.f && gate_bound <= 1e4f))
         return fail(KDA_ERR_INVALID_ARG, "gate_bound=%g must be in (0, 1e4]", (double)gate_bound);
-    return decode_impl(dtype, N, H, dk, dv, q, k, v, gate_logits, beta, state, o, gate_bound, stream);
+    return decode_impl(dtype, N, H, dk, dv, q, k, v, gate_logits, beta, state, o, gate_only(gate_bound), stream);
 }
 
 kda_status kda_check_status(kda_stream_t stream) {

@@ -28,6 +28,7 @@ struct RunParams {
     // Tensor-core kernel only (segment transitions of the segmented long-sequence prefill):
     bool zero_v;                // v taken as 0 (the v tensor is not read)
     bool identity_init;         // initial state = identity (needs d_k == d_v; init is not read)
+    bool qk_l2norm;             // q and k rows divided by sqrt(sum x^2 + 1e-6) in the kernel
     int max_chunks;             // > 0: only the first max_chunks chunks of every sequence are run
     const uint8_t *skip;        // non-null: the CTA of (sequence n, head h) exits at once if skip[n*H + h]
 };

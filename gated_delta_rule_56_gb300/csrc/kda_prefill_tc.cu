@@ -100,7 +100,8 @@ constexpr uint32_t SM_GC = SM_CST + 4096;                 // fp32 [3][128] gam_l
 constexpr uint32_t SM_BETA = SM_GC + 1536;                // fp32 [2][64] beta, by chunk parity
 constexpr uint32_t SM_BAR = SM_BETA + 512;                // mbarriers
 constexpr uint32_t SM_TPTR = SM_BAR + 256;                // TMEM base address
-constexpr uint32_t SM_USED = SM_TPTR + 16;
+constexpr uint32_t SM_NRM = SM_TPTR + 16;                 // fp32 [2 halves][k, q][64]: sums of squares
+constexpr uint32_t SM_USED = SM_NRM + 1024;
 constexpr uint32_t SMEM_BYTES = SM_USED + 1024;           // + alignment slack
 static_assert(SM_X + 64 * SA * 4 <= SM_OFF, "solve buffers overflow their region");
 static_assert(SM_Y + 4352 + 32 * SA * 4 <= SM_VT, "solve scratch overflows its region");
@@ -254,9 +255,66 @@ __device__ __forceinline__ void state_sync() { group_sync<2, NS>(); }
 //   rows 32..63: f = exp(Gam_r - Gam_47); off-tile row factor    f*c1  = exp(Gam_r - Gam_31)
 // Every other operand is one of K f, Q f, K / f times a per-channel factor <= 1, so each
 // product stays in range. Rows past the sequence end (r >= len) act as identity tokens.
-template <int MH>
+// Sums of squares of this thread's 4 rows r0..r0+3 of k and q over all 128 channels, for the
+// L2 norms. Each thread sums the squares of its 8 channels; the 8 lanes of a row group reduce
+// the 8 sums by halving exchanges (lane i ends with sum i: k rows 0..3, then q rows 0..3) and
+// store them, one channel half per warp, in shared memory; after the barrier of the two warps
+// that share the rows (w and w + 4) each thread adds the halves (row_inv_norm). Rows past the
+// sequence end count as zero.
+__device__ __forceinline__ void row_square_sums(uint8_t *sm, int r0, int j, int len) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float v[8];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const bool live = r0 + m < len;
+        const uint4 kw = *reinterpret_cast<const uint4 *>(sm + SM_K + tile_chunk(r0 + m, j));
+        const uint4 qw = *reinterpret_cast<const uint4 *>(sm + SM_Q + tile_chunk(r0 + m, j));
+        const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w}, qq[4] = {qw.x, qw.y, qw.z, qw.w};
+        float sk = 0.f, sq = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float kv = (i & 1) ? bf_hi(kk[i >> 1]) : bf_lo(kk[i >> 1]);
+            const float qv = (i & 1) ? bf_hi(qq[i >> 1]) : bf_lo(qq[i >> 1]);
+            sk = fmaf(kv, kv, sk);
+            sq = fmaf(qv, qv, sq);
+        }
+        v[m] = live ? sk : 0.f;
+        v[4 + m] = live ? sq : 0.f;
+    }
+    const int i = lane & 7;
+    float w4[4], w2[2];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const bool hi = (i & 4) != 0;
+        w4[t] = (hi ? v[4 + t] : v[t]) + __shfl_xor_sync(0xffffffffu, hi ? v[t] : v[4 + t], 4);
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const bool hi = (i & 2) != 0;
+        w2[t] = (hi ? w4[2 + t] : w4[t]) + __shfl_xor_sync(0xffffffffu, hi ? w4[t] : w4[2 + t], 2);
+    }
+    const bool hi = (i & 1) != 0;
+    const float tot = (hi ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, hi ? w2[0] : w2[1], 1);
+    float *nrm = reinterpret_cast<float *>(sm + SM_NRM);
+    nrm[((warp >> 2) * 2 + (i >> 2)) * 64 + r0 + (i & 3)] = tot;
+    switch (warp & 3) {  // constant barrier IDs 3..6, one per pair of warps
+        case 0: group_sync<3, 64>(); break;
+        case 1: group_sync<4, 64>(); break;
+        case 2: group_sync<5, 64>(); break;
+        default: group_sync<6, 64>(); break;
+    }
+}
+
+// 1 / sqrt(sum x^2 + 1e-6) of row r of k (kq = 0) or q (kq = 1), after row_square_sums.
+__device__ __forceinline__ float row_inv_norm(const uint8_t *sm, int kq, int r) {
+    const float *nrm = reinterpret_cast<const float *>(sm + SM_NRM);
+    return rsqrtf(nrm[kq * 64 + r] + nrm[(2 + kq) * 64 + r] + 1e-6f);
+}
+
+template <int MH, bool NORM>
 __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4][8], const float *cst, int r0,
                                                int j, int len, uint32_t khb) {
+    if (NORM) row_square_sums(sm, r0, j, len);
     float ref[8], fo_c[8], pe[8], khe[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -274,11 +332,16 @@ __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4]
         const uint4 qw = *reinterpret_cast<const uint4 *>(sm + SM_Q + tile_chunk(r, j));
         const uint32_t kk[4] = {live ? kw.x : 0u, live ? kw.y : 0u, live ? kw.z : 0u, live ? kw.w : 0u};
         const uint32_t qq[4] = {live ? qw.x : 0u, live ? qw.y : 0u, live ? qw.z : 0u, live ? qw.w : 0u};
+        const float nk = NORM ? row_inv_norm(sm, 0, r) : 1.f, nq = NORM ? row_inv_norm(sm, 1, r) : 1.f;
         float apk[8], apq[8], apb[8], ofr_k[8], ofr_q[8], kp[8], qp[8], kh[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float kv = (i & 1) ? bf_hi(kk[i >> 1]) : bf_lo(kk[i >> 1]);
-            const float qv = (i & 1) ? bf_hi(qq[i >> 1]) : bf_lo(qq[i >> 1]);
+            float kv = (i & 1) ? bf_hi(kk[i >> 1]) : bf_lo(kk[i >> 1]);
+            float qv = (i & 1) ? bf_hi(qq[i >> 1]) : bf_lo(qq[i >> 1]);
+            if (NORM) {
+                kv *= nk;
+                qv *= nq;
+            }
             // |Gam_r - ref| <= 80 for g in [-5, 0]; the clamp only keeps factors finite (no 0 * inf)
             // for gates outside that range.
             const float e = fminf(fmaxf(fmaf(gm[m][i], kLog2e, -ref[i]), -126.f), 126.f);
@@ -467,7 +530,8 @@ struct Maps {
 };
 
 // GATED: the g tensor holds logits x and the kernel forms g = -p.gate_bound * sigmoid(x).
-template <bool GATED>
+// NORM: q and k rows are divided by their L2 norms (sqrt(sum x^2 + 1e-6)) as they are read.
+template <bool GATED, bool NORM>
 __global__ void __launch_bounds__(NTHREADS, 1)
     kda_prefill_tc_kernel(const __grid_constant__ Maps maps, const RunParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -976,9 +1040,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!(ok = prep_wait(&bars[BAR_QK], par))) break;
             if (c > 0 && !(ok = prep_wait(&bars[BAR_KQFREE], par ^ 1u))) break;
             if (mh)
-                build_operands<1>(sm, gm, cst, tr0, j, len, SM_KH + 16384u * par);
+                build_operands<1, NORM>(sm, gm, cst, tr0, j, len, SM_KH + 16384u * par);
             else
-                build_operands<0>(sm, gm, cst, tr0, j, len, SM_KH + 16384u * par);
+                build_operands<0, NORM>(sm, gm, cst, tr0, j, len, SM_KH + 16384u * par);
             fence_async_smem();
             mbar_arrive(&bars[BAR_OPS]);
 
@@ -1078,11 +1142,12 @@ cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
         if (!attr_set[dev]) {
-            e = cudaFuncSetAttribute(kda_prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)SMEM_BYTES);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(kda_prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+            const void *fns[4] = {(const void *)kda_prefill_tc_kernel<false, false>,
+                                  (const void *)kda_prefill_tc_kernel<true, false>,
+                                  (const void *)kda_prefill_tc_kernel<false, true>,
+                                  (const void *)kda_prefill_tc_kernel<true, true>};
+            for (int f = 0; f < 4 && e == cudaSuccess; ++f)
+                e = cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
             if (e != cudaSuccess) return e;
             attr_set[dev] = true;
         }
@@ -1093,10 +1158,16 @@ cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
         !encode_map(&maps.g, p.g, rows, p.H) || !encode_map(&maps.v, p.v, rows, p.H) ||
         !encode_map(&maps.o, p.o, rows, p.H))
         return cudaErrorInvalidValue;
-    if (p.gate_bound > 0.f)
-        kda_prefill_tc_kernel<true><<<(unsigned)(p.n_seqs * p.H), NTHREADS, SMEM_BYTES, s>>>(maps, p);
+    const dim3 grid((unsigned)(p.n_seqs * p.H));
+    const bool gated = p.gate_bound > 0.f;
+    if (gated && p.qk_l2norm)
+        kda_prefill_tc_kernel<true, true><<<grid, NTHREADS, SMEM_BYTES, s>>>(maps, p);
+    else if (gated)
+        kda_prefill_tc_kernel<true, false><<<grid, NTHREADS, SMEM_BYTES, s>>>(maps, p);
+    else if (p.qk_l2norm)
+        kda_prefill_tc_kernel<false, true><<<grid, NTHREADS, SMEM_BYTES, s>>>(maps, p);
     else
-        kda_prefill_tc_kernel<false><<<(unsigned)(p.n_seqs * p.H), NTHREADS, SMEM_BYTES, s>>>(maps, p);
+        kda_prefill_tc_kernel<false, false><<<grid, NTHREADS, SMEM_BYTES, s>>>(maps, p);
     return cudaGetLastError();
 }
 

@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
     Tin *o = static_cast<Tin *>(p.o);
 
     __shared__ float sk[2][DK], sq[2][DK], sa[2][DK], sv[2][DV], sb[2];
-    __shared__ float red_k[2][kWarps][DV], red_q[2][kWarps][DV], red_qk[2][kWarps];
+    __shared__ float red_k[2][kWarps][DV], red_q[2][kWarps][DV], red_qk[2][3][kWarps];
 
     const int row0 = w * RPW, col0 = l * CPL;
     const size_t state_off = ((size_t)n * H + h) * DK * DV;
@@ -117,13 +117,15 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
         __syncthreads();
 
         // Decay the owned rows and form partial column sums of k^T S' and q^T S'.
-        float pk[CPL], pq[CPL], pqk = 0.f;
+        float pk[CPL], pq[CPL], pqk = 0.f, pkk = 0.f, pqq = 0.f;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) pk[c] = pq[c] = 0.f;
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
             const float a = sa[buf][row0 + r], kk = sk[buf][row0 + r], qq = sq[buf][row0 + r];
             pqk = fmaf(kk, qq, pqk);
+            pkk = fmaf(kk, kk, pkk);
+            pqq = fmaf(qq, qq, pqq);
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
                 s[r][c] *= a;
@@ -136,12 +138,25 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
             red_k[buf][w][col0 + c] = pk[c];
             red_q[buf][w][col0 + c] = pq[c];
         }
-        if (l == 0) red_qk[buf][w] = pqk;
+        if (l == 0) {
+            red_qk[buf][0][w] = pqk;
+            red_qk[buf][1][w] = pkk;
+            red_qk[buf][2][w] = pqq;
+        }
         __syncthreads();
 
-        float qk = 0.f;
+        float qk = 0.f, kk2 = 0.f, qq2 = 0.f;
 #pragma unroll
-        for (int i = 0; i < kWarps; ++i) qk += red_qk[buf][i];
+        for (int i = 0; i < kWarps; ++i) {
+            qk += red_qk[buf][0][i];
+            kk2 += red_qk[buf][1][i];
+            qq2 += red_qk[buf][2][i];
+        }
+        // L2-normalised q and k are q / |q|, k / |k|: every use of k and q is linear in it, so
+        // the norms scale the reductions and the write instead of the inputs.
+        const float nk = p.qk_l2norm ? rsqrtf(kk2 + 1e-6f) : 1.f;
+        const float nq = p.qk_l2norm ? rsqrtf(qq2 + 1e-6f) : 1.f;
+        qk *= nk * nq;
         const float b = sb[buf];
         float u[CPL], oo[CPL];
 #pragma unroll
@@ -152,12 +167,12 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
                 ks += red_k[buf][i][col0 + c];
                 qs += red_q[buf][i][col0 + c];
             }
-            u[c] = b * (sv[buf][col0 + c] - ks);
-            oo[c] = fmaf(qk, u[c], qs);
+            u[c] = b * (sv[buf][col0 + c] - ks * nk);
+            oo[c] = fmaf(qk, u[c], qs * nq);
         }
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
-            const float kk = sk[buf][row0 + r];
+            const float kk = sk[buf][row0 + r] * nk;
 #pragma unroll
             for (int c = 0; c < CPL; ++c) s[r][c] = fmaf(kk, u[c], s[r][c]);
         }

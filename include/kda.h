@@ -60,6 +60,21 @@ typedef enum {
 } kda_dtype;
 
 /*
+ * Options of kda_prefill_ex and kda_decode_step_ex. Zero the struct, set struct_size to
+ * sizeof(kda_options), then set the fields wanted; all zero means the plain kda_prefill /
+ * kda_decode_step. The library reads only the first struct_size bytes, so a caller built
+ * against an older, shorter kda_options keeps working (later fields take their defaults).
+ */
+typedef struct kda_options {
+    size_t struct_size; /* sizeof(kda_options) as the caller compiled it */
+    float gate_bound;   /* 0: g holds log-decays. > 0 (at most 1e4): g holds gate logits x and
+                           the kernels form g = -gate_bound * sigmoid(x), as kda_prefill_gated */
+    int qk_l2norm;      /* non-zero: every row of q and of k (d_k values of one token and head)
+                           is divided by sqrt(sum of its squares + 1e-6) in the kernels. The pages
+                           do not describe this step; the workloads feed q and k as unit vectors */
+} kda_options;
+
+/*
  * kda_prefill -- run the recurrence over whole sequences (chunked prefill).
  *
  * dtype        element type of q, k, v, g, beta and o.
@@ -100,6 +115,24 @@ KDA_API kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int
  * packed call needs no workspace whatever this returns. The same sizes apply to kda_prefill_gated. */
 KDA_API size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv,
                                   int n_seqs);
+
+/*
+ * kda_prefill_ex / kda_decode_step_ex -- kda_prefill / kda_decode_step with options (see
+ * kda_options; NULL = none). Returns KDA_ERR_INVALID_ARG for a struct_size below sizeof(size_t)
+ * or above 4096, or a gate_bound that is negative, not finite or above 1e4; every other
+ * argument and return value as the plain forms.
+ */
+KDA_API kda_status kda_prefill_ex(kda_dtype dtype, int B, int T, int H, int dk, int dv,
+                                  const void *q, const void *k, const void *v, const void *g,
+                                  const void *beta, const int32_t *cu_seqlens, int n_seqs,
+                                  const float *initial_state, void *o, float *final_state,
+                                  const kda_options *options, void *workspace, size_t workspace_bytes,
+                                  kda_stream_t stream);
+
+KDA_API kda_status kda_decode_step_ex(kda_dtype dtype, int N, int H, int dk, int dv,
+                                      const void *q, const void *k, const void *v, const void *g,
+                                      const void *beta, float *state, void *o,
+                                      const kda_options *options, kda_stream_t stream);
 
 /*
  * kda_prefill_noalloc -- kda_prefill without a caller workspace and without any allocation: a

@@ -64,6 +64,16 @@ def gate_logits_like(g: torch.Tensor, seed=0) -> torch.Tensor:
     return torch.randn(g.shape, generator=gen, device=g.device, dtype=torch.float32).to(g.dtype)
 
 
+def raw_qk_like(q: torch.Tensor, seed=0) -> torch.Tensor:
+    """Un-normalised q or k rows for the in-kernel L2 normalisation: N(0, 1) entries times one
+    scale per (token, head) drawn log-uniformly from [e^-1.5, e^1.5], with the shape, dtype and
+    device of `q`."""
+    gen = _generator(seed, q.device)
+    x = torch.randn(q.shape, generator=gen, device=q.device, dtype=torch.float32)
+    scale = torch.exp(torch.empty(*q.shape[:-1], 1, device=q.device).uniform_(-1.5, 1.5, generator=gen))
+    return (x * scale).to(q.dtype)
+
+
 def varlen_lengths(n_seqs, lo, hi, seed=0):
     """Sequence lengths drawn uniformly from the integers in [lo, hi]."""
     gen = _generator(seed, "cpu")

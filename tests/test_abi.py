@@ -53,6 +53,24 @@ def test_noalloc_capacity_and_argument_checks(lib):
     assert lib.kda_prefill_noalloc(0, -1, 8, 1, 128, 128, *([None] * 6), 1, None, None, None, None) == 1
 
 
+def test_options_are_checked_before_anything_runs(lib):
+    import ctypes
+    from gated_delta_rule_56_gb300._lib import KDAOptions
+    assert ctypes.sizeof(KDAOptions) == 16  # size_t, float, int: the C layout of kda_options
+    null6 = [None] * 6
+    for bad in (KDAOptions(0, 0.0, 0), KDAOptions(4, 0.0, 0), KDAOptions(5000, 0.0, 1),
+                KDAOptions(16, -1.0, 0), KDAOptions(16, float("nan"), 0), KDAOptions(16, 2e4, 1)):
+        assert lib.kda_prefill_ex(0, 1, 64, 1, 128, 128, *null6, 1, None, None, None, ctypes.byref(bad),
+                                  None, 0, None) == 1
+        assert lib.kda_decode_step_ex(0, 1, 1, 128, 128, *[None] * 7, ctypes.byref(bad), None) == 1
+    # A caller built against a shorter struct (gate_bound only) is accepted: qk_l2norm defaults to 0,
+    # and the call then fails on its NULL tensors, not on the options.
+    short = KDAOptions(12, 0.0, 1)
+    assert lib.kda_prefill_ex(0, 1, 64, 1, 128, 128, *null6, 1, None, None, None, ctypes.byref(short),
+                              None, 0, None) == 1
+    assert b"NULL" in lib.kda_last_error()
+
+
 FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: validation fails first
 
 
