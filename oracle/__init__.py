@@ -13,6 +13,7 @@ Public functions take CPU tensors or arrays in the KDA layouts and return fp64 n
 * ``decode_step(q, k, v, g, beta, state)`` -> (o, new_state): one token of the recurrence.
 * ``scaled_sigmoid_gate(x, bound)`` -> g = -bound * sigmoid(x) (log-decays from gate logits).
 * ``l2_normalize(x, eps=1e-6)`` -> rows along the last axis divided by sqrt(sum x^2 + eps).
+* ``output_gate(o, z)`` -> o * sigmoid(z) (the output gate).
 
 Layouts: q, k, g [B, T, H, d_k]; v [B, T, H, d_v]; beta [B, T, H]; with ``cu_seqlens``
 (int [N+1]) B must be 1 and the rows of sequence n are cu[n]..cu[n+1]-1. States are
@@ -54,6 +55,8 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
 def _declare(lib):
     lib.kda_oracle_scaled_sigmoid_gate.argtypes = [ctypes.c_int64, _dp, ctypes.c_double, _dp]
     lib.kda_oracle_scaled_sigmoid_gate.restype = ctypes.c_int
+    lib.kda_oracle_output_gate.argtypes = [ctypes.c_int64, _dp, _dp, _dp]
+    lib.kda_oracle_output_gate.restype = ctypes.c_int
     lib.kda_oracle_l2_normalize.argtypes = [ctypes.c_int64, ctypes.c_int64, _dp, ctypes.c_double, _dp]
     lib.kda_oracle_l2_normalize.restype = ctypes.c_int
     lib.kda_oracle_recurrent.argtypes = [ctypes.c_int, _i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -195,6 +198,18 @@ def scaled_sigmoid_gate(x, bound):
     if rc != 0:
         raise ValueError(f"kda_oracle_scaled_sigmoid_gate returned {rc}")
     return g
+
+
+def output_gate(o, z):
+    """o * sigmoid(z) elementwise, fp64, shape of o (z must have the same shape)."""
+    o, z = _f64(o), _f64(z)
+    if o.shape != z.shape:
+        raise ValueError(f"output_gate: shapes {o.shape} and {z.shape} differ")
+    y = np.empty_like(o)
+    rc = load_library().kda_oracle_output_gate(o.size, o.ctypes.data_as(_dp), z.ctypes.data_as(_dp), y.ctypes.data_as(_dp))
+    if rc != 0:
+        raise ValueError(f"kda_oracle_output_gate returned {rc}")
+    return y
 
 
 def l2_normalize(x, eps=1e-6):

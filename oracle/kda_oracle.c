@@ -34,6 +34,10 @@
  *                           The pages do not describe this step; the workloads feed q and k as
  *                           unit vectors per (token, head), and the library can form them in its
  *                           kernels. The eps (1e-6 there) only keeps a zero row finite.
+ *  kda_oracle_output_gate -- y = o * sigmoid(z) per element: the output gate, an input-dependent
+ *                           full-rank projection z ("Kimi K3 Explained", researchpapers.dev,
+ *                           "Architecture at a glance"); the pages name no activation, the
+ *                           logistic function is the plain reading.
  *  kda_oracle_chunked    -- a separately written chunkwise form of the same recurrence
  *                           (per-chunk cumulative log-decay, the strictly lower intra-chunk
  *                           matrix, a triangular solve for the delta corrections, one state
@@ -369,6 +373,13 @@ int kda_oracle_l2_normalize(int64_t rows, int64_t d, const double *x, double eps
         const double norm = sqrt(ss + eps);
         for (int64_t i = 0; i < d; ++i) y[r * d + i] = norm > 0.0 ? x[r * d + i] / norm : 0.0;
     }
+    return 0;
+}
+
+int kda_oracle_output_gate(int64_t n, const double *o, const double *z, double *y)
+{
+    if (n < 0 || !o || !z || !y) return -1;
+    for (int64_t i = 0; i < n; ++i) y[i] = o[i] / (1.0 + exp(-z[i]));
     return 0;
 }
 

@@ -313,6 +313,33 @@ def test_l2_rejects_bad_eps():
         oracle.l2_normalize(np.ones((2, 3)), eps=-1.0)
 
 
+# ---------------------------------------------------------------- output gate --------------
+# y = o * sigmoid(z). Pinned by closed forms of the logistic function at 0 and +-log(3), its
+# limits, and linearity in o.
+
+def test_output_gate_closed_forms():
+    o = np.array([2.0, -4.0, 8.0, 1.5, -3.0, 7.0])
+    z = np.array([0.0, math.log(3.0), -math.log(3.0), 60.0, -60.0, math.log(7.0)])
+    y = oracle.output_gate(o, z)
+    np.testing.assert_allclose(y[:3], [1.0, -3.0, 2.0], rtol=0, atol=1e-15)
+    assert y[3] == pytest.approx(1.5, rel=1e-15) and abs(y[4]) < 1e-25
+    assert y[5] == pytest.approx(7.0 * 7.0 / 8.0, rel=1e-15)
+
+
+def test_output_gate_linear_in_o_and_symmetric():
+    rng = np.random.default_rng(3)
+    o, o2, z = rng.standard_normal((3, 4, 5, 16))
+    y = oracle.output_gate(o, z)
+    np.testing.assert_allclose(oracle.output_gate(o + 2.5 * o2, z), y + 2.5 * oracle.output_gate(o2, z),
+                               rtol=0, atol=1e-13)
+    np.testing.assert_allclose(y + oracle.output_gate(o, -z), o, rtol=0, atol=1e-14)  # s(z) + s(-z) = 1
+
+
+def test_output_gate_rejects_shape_mismatch():
+    with pytest.raises(ValueError):
+        oracle.output_gate(np.zeros((2, 3)), np.zeros((3, 2)))
+
+
 # -------------------------------------------------------------- planted-mistake detection --
 
 _PINS = [
@@ -347,6 +374,31 @@ _MUTANTS = [
      "    for (int i = 0; i < dk; ++i)\n        for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] += k[i] * u[j];\n    /* o_t = S_t^T q_t */",
      "    /* o_t = S_t^T q_t */"),
 ]
+
+
+_GATE_PINS = [test_output_gate_closed_forms, test_output_gate_linear_in_o_and_symmetric]
+_GATE_MUTANTS = [
+    ("sigmoid of -z", "y[i] = o[i] / (1.0 + exp(-z[i]));", "y[i] = o[i] / (1.0 + exp(z[i]));"),
+    ("gate added instead of multiplied", "y[i] = o[i] / (1.0 + exp(-z[i]));", "y[i] = o[i] + 1.0 / (1.0 + exp(-z[i]));"),
+    ("z as the gate", "y[i] = o[i] / (1.0 + exp(-z[i]));", "y[i] = o[i] * z[i];"),
+    ("exp(-z) without the 1", "y[i] = o[i] / (1.0 + exp(-z[i]));", "y[i] = o[i] / exp(-z[i]);"),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(_GATE_MUTANTS)))
+def test_output_gate_pins_catch_planted_mistakes(tmp_path, idx):
+    desc, old, new = _GATE_MUTANTS[idx]
+    text = open(oracle._SRC).read()
+    assert text.count(old) == 1, f"mutation site not found: {desc}"
+    path = _build_mutant(tmp_path, text.replace(old, new, 1), 200 + idx)
+    caught = []
+    with oracle.use_library(path):
+        for pin in _GATE_PINS:
+            try:
+                pin()
+            except AssertionError:
+                caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake: {desc}"
 
 
 _L2_PINS = [test_l2_pythagorean_rows, test_l2_eps_one_hot_and_zero_rows, test_l2_invariants]
