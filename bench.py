@@ -52,12 +52,13 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("varlen", "long", "gated", "l2norm"), default=None,
+    ap.add_argument("--workload", choices=("varlen", "long", "gated", "l2norm", "outgate"), default=None,
                     help="time one of the other prefill workloads instead of the headline (one JSON line): "
                          "varlen = 64 packed sequences of U[128, 16384] tokens with initial states; "
                          "long = one sequence of 1,048,576 tokens (B=1, H=32); "
                          "gated = the headline shape with gate logits (decays formed in the kernel); "
-                         "l2norm = the headline shape with raw q/k rows L2-normalised in the kernel")
+                         "l2norm = the headline shape with raw q/k rows L2-normalised in the kernel; "
+                         "outgate = the headline shape with the output gate o * sigmoid(z) in the kernel")
     ap.add_argument("--ncu-case", choices=("prefill", "decode"),
                     help="run two launches of the small profiling case (for ncu) and exit")
     args = ap.parse_args()
@@ -453,6 +454,13 @@ def run_workload(args):
         kw = {}
         alg = prefill_bytes(1, T, H, d)
         name = f"KDA chunked prefill, long context: B=1 T={T} H={H} dk=dv={d} bf16, zero init"
+    elif args.workload == "outgate":
+        B, T = PF["B"], PF["T"]
+        x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)
+        tokens, n_seq = B * T, B
+        kw = dict(out_gate=ki.gate_logits_like(x["v"], seed=3))  # z ~ N(0, 1): o * sigmoid(z) is stored
+        alg = prefill_bytes(B, T, H, d) + tokens * H * d * 2    # + the gate input z (bf16)
+        name = f"KDA chunked prefill with the output gate o*sigmoid(z) in the kernel: B={B} T={T} H={H} dk=dv={d} bf16, zero init"
     elif args.workload == "l2norm":
         B, T = PF["B"], PF["T"]
         x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)

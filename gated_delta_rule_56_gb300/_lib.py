@@ -95,12 +95,21 @@ def load():
 
 class KDAOptions(ctypes.Structure):
     """kda_options of include/kda.h (struct_size first; zero fields are the defaults)."""
-    _fields_ = [("struct_size", ctypes.c_size_t), ("gate_bound", ctypes.c_float), ("qk_l2norm", ctypes.c_int)]
+    _fields_ = [("struct_size", ctypes.c_size_t), ("gate_bound", ctypes.c_float), ("qk_l2norm", ctypes.c_int),
+                ("initial_state_indices", ctypes.c_void_p), ("final_state_indices", ctypes.c_void_p),
+                ("state_pool_size", ctypes.c_int), ("out_gate", ctypes.c_void_p)]
 
 
-def _options(gate_bound, qk_l2norm):
+def _options(gate_bound, qk_l2norm, init_idx=None, fin_idx=None, pool=0, out_gate=None):
     return KDAOptions(ctypes.sizeof(KDAOptions), 0.0 if gate_bound is None else float(gate_bound),
-                      1 if qk_l2norm else 0)
+                      1 if qk_l2norm else 0, None if init_idx is None else init_idx.data_ptr(),
+                      None if fin_idx is None else fin_idx.data_ptr(), int(pool),
+                      None if out_gate is None else out_gate.data_ptr())
+
+
+def _check_indices(name, idx, n, dev):
+    if idx is not None:
+        _check(name, idx, torch.int32, (n,), dev)
 
 
 def status_string(status: int) -> str:
@@ -142,7 +151,8 @@ def _check(name, t, dtype, shape, device):
 
 
 def prefill(q, k, v, g, beta, cu_seqlens=None, initial_state=None, output_final_state=True,
-            o=None, final_state=None, gate_bound=None, qk_l2norm=False):
+            o=None, final_state=None, gate_bound=None, qk_l2norm=False, initial_state_indices=None,
+            final_state_indices=None, out_gate=None):
     """Chunked KDA prefill on the GPU.
 
     q, k, g [B, T, H, dk]; v [B, T, H, dv]; beta [B, T, H]; all bf16 or all fp32, on one CUDA
@@ -150,8 +160,11 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, initial_state=None, output_final_
     packed sequences. ``initial_state``: fp32 [N, H, dk, dv] or None (zeros). With
     ``gate_bound`` A, ``g`` holds gate logits x and the kernels use g = -A * sigmoid(x)
     (kda_prefill_gated). With ``qk_l2norm`` the kernels divide every row of q and k by
-    sqrt(sum x^2 + 1e-6) (kda_prefill_ex). Returns (o [B, T, H, dv], final_state [N, H, dk, dv]
-    fp32 or None).
+    sqrt(sum x^2 + 1e-6) (kda_prefill_ex). With ``initial_state_indices`` / ``final_state_indices``
+    (int32 [N] on the device) the matching state tensor is a pool [P, H, dk, dv] and sequence n
+    reads / writes slot idx[n] (negative: zero start / no write); ``final_state`` must then be
+    given. With ``out_gate`` z (the layout and dtype of o) the kernels store o * sigmoid(z).
+    Returns (o [B, T, H, dv], final_state [N, H, dk, dv] fp32 (or the pool) or None).
     """
     lib = load()
     if q.dtype not in _DTYPES:
@@ -171,22 +184,36 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, initial_state=None, output_final_
         N = cu_seqlens.numel() - 1
     else:
         N = B
+    pools = [t.shape[0] for t, i in ((initial_state, initial_state_indices), (final_state, final_state_indices))
+             if t is not None and i is not None and t.dim() == 4]
+    if len(set(pools)) > 1:
+        raise ValueError("initial and final state pools must have the same number of slots")
+    pool = pools[0] if pools else 0
+    _check_indices("initial_state_indices", initial_state_indices, N, dev)
+    _check_indices("final_state_indices", final_state_indices, N, dev)
     if initial_state is not None:
-        _check("initial_state", initial_state, torch.float32, (N, H, dk, dv), dev)
+        n0 = pool if initial_state_indices is not None else N
+        _check("initial_state", initial_state, torch.float32, (n0, H, dk, dv), dev)
     if o is None:
         o = torch.empty(B, T, H, dv, dtype=q.dtype, device=dev)
     else:
         _check("o", o, q.dtype, (B, T, H, dv), dev)
+    if final_state_indices is not None and final_state is None:
+        raise ValueError("final_state_indices needs final_state (the pool)")
+    if out_gate is not None:
+        _check("out_gate", out_gate, q.dtype, (B, T, H, dv), dev)
     if final_state is None and output_final_state:
         final_state = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
     elif final_state is not None:
-        _check("final_state", final_state, torch.float32, (N, H, dk, dv), dev)
+        n1 = pool if final_state_indices is not None else N
+        _check("final_state", final_state, torch.float32, (n1, H, dk, dv), dev)
     dt = _DTYPES[q.dtype]
     ws_bytes = int(lib.kda_prefill_workspace_size(dt, B, T, H, dk, dv, N))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
     with torch.cuda.device(dev):
-        if qk_l2norm:
-            opt = _options(gate_bound, qk_l2norm)
+        if (qk_l2norm or initial_state_indices is not None or final_state_indices is not None
+                or out_gate is not None):
+            opt = _options(gate_bound, qk_l2norm, initial_state_indices, final_state_indices, pool, out_gate)
             st = lib.kda_prefill_ex(dt, B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                     _ptr(cu_seqlens), N, _ptr(initial_state), _ptr(o), _ptr(final_state),
                                     ctypes.byref(opt), _ptr(ws), ws_bytes, _stream(dev))
@@ -202,11 +229,16 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, initial_state=None, output_final_
     return o, final_state
 
 
-def decode_step(q, k, v, g, beta, state, o=None, gate_bound=None, qk_l2norm=False):
+def decode_step(q, k, v, g, beta, state, o=None, gate_bound=None, qk_l2norm=False, state_indices=None,
+                final_state_indices=None, out_gate=None):
     """One KDA decode token for N sequences; ``state`` (fp32 [N, H, dk, dv]) is updated in
     place. q, k, g [N, H, dk]; v [N, H, dv]; beta [N, H]. With ``gate_bound`` A, ``g`` holds gate
     logits x and g = -A * sigmoid(x) is used (kda_decode_step_gated). With ``qk_l2norm`` the
-    rows of q and k are L2-normalised in the kernel (kda_decode_step_ex). Returns o [N, H, dv]."""
+    rows of q and k are L2-normalised in the kernel (kda_decode_step_ex). With ``state_indices``
+    (int32 [N] on the device) ``state`` is a pool [P, H, dk, dv]: sequence n reads slot
+    state_indices[n] (negative: zero state) and writes slot final_state_indices[n] (default: the
+    same slot; negative: not written). With ``out_gate`` z [N, H, dv] the kernel stores
+    o * sigmoid(z). Returns o [N, H, dv]."""
     lib = load()
     if q.dtype not in _DTYPES:
         raise TypeError(f"unsupported dtype {q.dtype}")
@@ -218,14 +250,21 @@ def decode_step(q, k, v, g, beta, state, o=None, gate_bound=None, qk_l2norm=Fals
     for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("g", g, (N, H, dk)),
                          ("v", v, (N, H, dv)), ("beta", beta, (N, H))):
         _check(name, t, q.dtype, shp, dev)
-    _check("state", state, torch.float32, (N, H, dk, dv), dev)
+    if final_state_indices is not None and state_indices is None:
+        raise ValueError("final_state_indices needs state_indices")
+    _check_indices("state_indices", state_indices, N, dev)
+    _check_indices("final_state_indices", final_state_indices, N, dev)
+    pool = state.shape[0] if state_indices is not None and state.dim() == 4 else 0
+    _check("state", state, torch.float32, (pool if state_indices is not None else N, H, dk, dv), dev)
+    if out_gate is not None:
+        _check("out_gate", out_gate, q.dtype, (N, H, dv), dev)
     if o is None:
         o = torch.empty(N, H, dv, dtype=q.dtype, device=dev)
     else:
         _check("o", o, q.dtype, (N, H, dv), dev)
     with torch.cuda.device(dev):
-        if qk_l2norm:
-            opt = _options(gate_bound, qk_l2norm)
+        if qk_l2norm or state_indices is not None or out_gate is not None:
+            opt = _options(gate_bound, qk_l2norm, state_indices, final_state_indices, pool, out_gate)
             st = lib.kda_decode_step_ex(_DTYPES[q.dtype], N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                         _ptr(beta), _ptr(state), _ptr(o), ctypes.byref(opt), _stream(dev))
         elif gate_bound is None:

@@ -133,6 +133,16 @@ kda_status read_options(const kda_options *user, kda_options &opt) {
     opt.struct_size = sizeof(kda_options);
     if (!(opt.gate_bound == 0.f || (opt.gate_bound > 0.f && opt.gate_bound <= 1e4f)))
         return fail(KDA_ERR_INVALID_ARG, "gate_bound=%g must be 0 or in (0, 1e4]", (double)opt.gate_bound);
+    if (opt.initial_state_indices || opt.final_state_indices) {
+        if (opt.state_pool_size <= 0)
+            return fail(KDA_ERR_INVALID_ARG, "state_pool_size=%d must be positive when state indices are given",
+                        opt.state_pool_size);
+        if ((reinterpret_cast<uintptr_t>(opt.initial_state_indices) & 3u) ||
+            (reinterpret_cast<uintptr_t>(opt.final_state_indices) & 3u))
+            return fail(KDA_ERR_INVALID_ARG, "state index arrays must be 4-byte aligned");
+    }
+    if (opt.out_gate && !aligned16(opt.out_gate))
+        return fail(KDA_ERR_INVALID_ARG, "out_gate is not 16-byte aligned");
     return KDA_OK;
 }
 
@@ -191,6 +201,14 @@ kda_status prefill_impl(kda_dtype dtype, int B, int T, int H, int dk, int dv, co
     p.err = device_error_word();
     p.gate_bound = opt.gate_bound;
     p.qk_l2norm = opt.qk_l2norm != 0;
+    if (opt.initial_state_indices && !initial_state)
+        return fail(KDA_ERR_INVALID_ARG, "initial_state_indices given without initial_state (the pool)");
+    if (opt.final_state_indices && !final_state)
+        return fail(KDA_ERR_INVALID_ARG, "final_state_indices given without final_state (the pool)");
+    p.init_idx = opt.initial_state_indices;
+    p.fin_idx = opt.final_state_indices;
+    p.pool = opt.state_pool_size;
+    p.out_gate = opt.out_gate;
     if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word: %s",
                             cudaGetErrorString(cudaGetLastError()));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -234,6 +252,12 @@ kda_status decode_impl(kda_dtype dtype, int N, int H, int dk, int dv, const void
     p.err = device_error_word();
     p.gate_bound = opt.gate_bound;
     p.qk_l2norm = opt.qk_l2norm != 0;
+    if (opt.final_state_indices && !opt.initial_state_indices)
+        return fail(KDA_ERR_INVALID_ARG, "decode: final_state_indices needs initial_state_indices");
+    p.init_idx = opt.initial_state_indices;
+    p.fin_idx = opt.final_state_indices ? opt.final_state_indices : opt.initial_state_indices;
+    p.pool = opt.state_pool_size;
+    p.out_gate = opt.out_gate;
     if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word");
     return launched(launch_recurrent(dtype, dk, dv, p, reinterpret_cast<cudaStream_t>(stream)), "decode step");
 }
@@ -365,6 +389,8 @@ kda_status kda_check_status(kda_stream_t stream) {
     if (e == cudaSuccess && word) e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "error word: %s", cudaGetErrorString(e));
     if (word & kErrTimeout) return fail(KDA_ERR_TIMEOUT, "a device-side wait gave up (error word 0x%x)", word);
+    if (word & kErrBadIndex)
+        return fail(KDA_ERR_INVALID_ARG, "a state index is at or past the pool end (error word 0x%x)", word);
     if (word & kErrBadSeqlens)
         return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is not a non-decreasing list ending at T (error word 0x%x)", word);
     return ok();

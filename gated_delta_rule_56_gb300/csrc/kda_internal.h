@@ -11,7 +11,7 @@
 namespace kda {
 
 // Bits of the per-device error word (see kda_check_status).
-enum : unsigned { kErrBadSeqlens = 1u, kErrTimeout = 2u };
+enum : unsigned { kErrBadSeqlens = 1u, kErrTimeout = 2u, kErrBadIndex = 4u };
 
 // Arguments of one prefill or decode launch, already validated on the host.
 struct RunParams {
@@ -29,6 +29,10 @@ struct RunParams {
     bool zero_v;                // v taken as 0 (the v tensor is not read)
     bool identity_init;         // initial state = identity (needs d_k == d_v; init is not read)
     bool qk_l2norm;             // q and k rows divided by sqrt(sum x^2 + 1e-6) in the kernel
+    const int32_t *init_idx;    // non-null: init is a pool; sequence n starts from state init_idx[n] (< 0: zero)
+    const int32_t *fin_idx;     // non-null: fin is a pool; sequence n ends in state fin_idx[n] (< 0: not written)
+    int pool;                   // states in the pool(s) when an index array is given
+    const void *out_gate;       // non-null: o is multiplied by sigmoid(out_gate) (same layout and dtype as o)
     int max_chunks;             // > 0: only the first max_chunks chunks of every sequence are run
     const uint8_t *skip;        // non-null: the CTA of (sequence n, head h) exits at once if skip[n*H + h]
 };
@@ -52,5 +56,23 @@ bool encode_row_tile_map(CUtensorMap *map, const void *base, long long rows, int
 size_t segmented_workspace_bytes(kda_dtype dtype, int B, int T, int H, int dk, int dv, bool varlen);
 cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace, size_t workspace_bytes,
                                      cudaStream_t s);
+
+// Element offset of the state of (sequence n, head h) in a state tensor of d x d blocks, or -1
+// when the sequence has none there. Without an index array the tensor holds one state per
+// sequence; with one it is a pool of `pool` states and idx[n] picks the slot (negative: none; at
+// or past the pool end: none, and kErrBadIndex is raised).
+__device__ __forceinline__ long long state_slot_offset(const int32_t *idx, int pool, int n, int H, int h,
+                                                       int d, unsigned *err) {
+    long long slot = n;
+    if (idx) {
+        slot = idx[n];
+        if (slot < 0) return -1;
+        if (slot >= pool) {
+            atomicOr(err, kErrBadIndex);
+            return -1;
+        }
+    }
+    return (slot * H + h) * (long long)d * d;
+}
 
 }  // namespace kda

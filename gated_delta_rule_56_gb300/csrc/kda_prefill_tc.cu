@@ -529,11 +529,46 @@ struct Maps {
     CUtensorMap q, k, g, v, o;
 };
 
-// GATED: the g tensor holds logits x and the kernel forms g = -p.gate_bound * sigmoid(x).
-// NORM: q and k rows are divided by their L2 norms (sqrt(sum x^2 + 1e-6)) as they are read.
-template <bool GATED, bool NORM>
+// Flags of a kernel instance:
+// kGated: the g tensor holds logits x and the kernel forms g = -p.gate_bound * sigmoid(x).
+// kNorm: q and k rows are divided by their L2 norms (sqrt(sum x^2 + 1e-6)) as they are read.
+// kOutGate: O is multiplied by sigmoid(p.out_gate) before it is stored.
+enum : int { kGated = 1, kNorm = 2, kOutGate = 4 };
+
+// The gate rows (this head) of one chunk's O tile, read while the tile is staged: a thread takes
+// 8 of its 1024 16-byte chunks (row e / 16, channels 8 (e % 16) ..), scales the staged bf16 O by
+// sigmoid(z) in fp32 and writes it back in place. Rows at or past `ln` are left alone (they are
+// past the tensor end and are not stored).
+__device__ __forceinline__ void gate_staged_o(uint8_t *sm, const __nv_bfloat16 *zg, long long r0, int ln, int H,
+                                              int h, int v) {
+    uint4 z[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = v + 128 * i, row = e >> 4, cj = e & 15;
+        z[i] = row < ln ? __ldg(reinterpret_cast<const uint4 *>(zg + ((size_t)(r0 + row) * H + h) * D + 8 * cj))
+                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = v + 128 * i, row = e >> 4, cj = e & 15;
+        uint4 *po = reinterpret_cast<uint4 *>(sm + SM_T + (cj >> 3) * 8192 + row * 128 + (((cj & 7) ^ (row & 7)) << 4));
+        const uint4 ov = *po;
+        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, zw[4] = {z[i].x, z[i].y, z[i].z, z[i].w};
+        uint32_t rw[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float s0 = __fdividef(1.f, 1.f + ex2(-bf_lo(zw[q]) * kLog2e));
+            const float s1 = __fdividef(1.f, 1.f + ex2(-bf_hi(zw[q]) * kLog2e));
+            rw[q] = pack_bf16(bf_lo(ow[q]) * s0, bf_hi(ow[q]) * s1);
+        }
+        *po = make_uint4(rw[0], rw[1], rw[2], rw[3]);
+    }
+}
+
+template <int F>
 __global__ void __launch_bounds__(NTHREADS, 1)
     kda_prefill_tc_kernel(const __grid_constant__ Maps maps, const RunParams p) {
+    constexpr bool GATED = (F & kGated) != 0, NORM = (F & kNorm) != 0, OGATE = (F & kOutGate) != 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
@@ -588,7 +623,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tptr;
     const uint32_t tq = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quarter
-    const size_t state_off = ((size_t)n * H + h) * (size_t)D * D;
 
     if (warp == kIssuer) {
         // ---------------------------------------------------------------- issuer warp --------
@@ -736,6 +770,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int v = tid - NP;
         __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o);
         bool ok = true;
+        const long long init_off = p.init ? state_slot_offset(p.init_idx, p.pool, n, H, h, D, p.err) : -1;
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {  // initial state -> TMEM (fp32)
             const int k0 = 32 * cb;
@@ -743,17 +778,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
                 buf[i] = p.identity_init ? (k0 + i == v ? 1.f : 0.f)
-                                         : (p.init ? __ldcs(p.init + state_off + (size_t)(k0 + i) * D + v) : 0.f);
+                                         : (init_off >= 0 ? __ldcs(p.init + init_off + (size_t)(k0 + i) * D + v) : 0.f);
             tmem_st32(tmem + tq + TM_S + k0, buf);
         }
         tmem_st_wait();
 
         // O of a finished chunk (TMEM columns TM_D1 + 64 ..+63 = its 64 tokens) straight to
         // global memory: each warp store covers 32 consecutive value columns (64 bytes).
+        const __nv_bfloat16 *zg = static_cast<const __nv_bfloat16 *>(p.out_gate);
         auto store_o = [&](const float (&o0)[32], const float (&o1)[32], long long r0, int ln) {
             __nv_bfloat16 *dst = og + ((size_t)r0 * H + h) * D + v;
             const size_t rs = (size_t)H * D;  // elements between consecutive tokens
-            if (ln == C) {
+            if (OGATE) {  // a ragged chunk: gate each stored element
+                const __nv_bfloat16 *zr = zg + ((size_t)r0 * H + h) * D + v;
+#pragma unroll
+                for (int r = 0; r < 32; ++r, dst += rs, zr += rs)
+                    if (r < ln) *dst = __float2bfloat16_rn(o0[r] * __fdividef(1.f, 1.f + ex2(-__bfloat162float(*zr) * kLog2e)));
+#pragma unroll
+                for (int r = 0; r < 32; ++r, dst += rs, zr += rs)
+                    if (32 + r < ln) *dst = __float2bfloat16_rn(o1[r] * __fdividef(1.f, 1.f + ex2(-__bfloat162float(*zr) * kLog2e)));
+            } else if (ln == C) {
 #pragma unroll
                 for (int r = 0; r < 32; ++r, dst += rs) *dst = __float2bfloat16_rn(o0[r]);
 #pragma unroll
@@ -786,6 +830,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int r = 0; r < 32; ++r)
                     *reinterpret_cast<__nv_bfloat16 *>(sm + SM_T + ost[r & 7] + (32 + (r & ~7)) * 128) =
                         __float2bfloat16_rn(o1[r]);
+                if (OGATE) {
+                    state_sync();  // the whole tile is staged
+                    gate_staged_o(sm, zg, r0, (int)min((long long)C, total_rows - r0), H, h, v);
+                }
                 fence_async_smem();
                 state_sync();
                 if (v == 0) {
@@ -806,6 +854,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t par = (uint32_t)(c & 1);
             const long long row0 = bos + (long long)c * C;
             const int len = (int)min((long long)C, eos - row0);
+            if (OGATE && (v >> 1) < len)  // this chunk's gate rows into L2 (read when its O is written)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(zg + ((size_t)(row0 + (v >> 1)) * H + h) * D + 64 * (v & 1)));
             if (c > 0) {  // O of the previous chunk, once MMA3 and MMA4 of it have completed
                 if (!(ok = state_wait(&bars[BAR_M34], par ^ 1u))) break;
                 tc_fence_after();
@@ -901,14 +951,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (v == 0) bulk_wait_all();  // every O store is complete (and has read shared memory)
         if (ok) {
-            if (p.fin) {
+            const long long fin_off = p.fin ? state_slot_offset(p.fin_idx, p.pool, n, H, h, D, p.err) : -1;
+            if (fin_off >= 0) {
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     float sv[32];
                     tmem_ld32(tmem + tq + TM_S + 32 * cb, sv);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) __stcs(p.fin + state_off + (size_t)(32 * cb + i) * D + v, sv[i]);
+                    for (int i = 0; i < 32; ++i) __stcs(p.fin + fin_off + (size_t)(32 * cb + i) * D + v, sv[i]);
                 }
             }
         } else if (v == 0) {
@@ -1132,6 +1183,13 @@ bool tc_prefill_supported(kda_dtype dtype, int dk, int dv, const RunParams &p) {
     return tensor_map_encoder() != nullptr;
 }
 
+// One instance per combination of the flags, indexed by them.
+const void *const kTcKernels[8] = {
+    (const void *)kda_prefill_tc_kernel<0>, (const void *)kda_prefill_tc_kernel<1>,
+    (const void *)kda_prefill_tc_kernel<2>, (const void *)kda_prefill_tc_kernel<3>,
+    (const void *)kda_prefill_tc_kernel<4>, (const void *)kda_prefill_tc_kernel<5>,
+    (const void *)kda_prefill_tc_kernel<6>, (const void *)kda_prefill_tc_kernel<7>};
+
 cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
     static std::mutex mu;
     static bool attr_set[256] = {};
@@ -1142,12 +1200,8 @@ cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
         if (!attr_set[dev]) {
-            const void *fns[4] = {(const void *)kda_prefill_tc_kernel<false, false>,
-                                  (const void *)kda_prefill_tc_kernel<true, false>,
-                                  (const void *)kda_prefill_tc_kernel<false, true>,
-                                  (const void *)kda_prefill_tc_kernel<true, true>};
-            for (int f = 0; f < 4 && e == cudaSuccess; ++f)
-                e = cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+            for (int f = 0; f < 8 && e == cudaSuccess; ++f)
+                e = cudaFuncSetAttribute(kTcKernels[f], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
             if (e != cudaSuccess) return e;
             attr_set[dev] = true;
         }
@@ -1158,17 +1212,9 @@ cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
         !encode_map(&maps.g, p.g, rows, p.H) || !encode_map(&maps.v, p.v, rows, p.H) ||
         !encode_map(&maps.o, p.o, rows, p.H))
         return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)(p.n_seqs * p.H));
-    const bool gated = p.gate_bound > 0.f;
-    if (gated && p.qk_l2norm)
-        kda_prefill_tc_kernel<true, true><<<grid, NTHREADS, SMEM_BYTES, s>>>(maps, p);
-    else if (gated)
-        kda_prefill_tc_kernel<true, false><<<grid, NTHREADS, SMEM_BYTES, s>>>(maps, p);
-    else if (p.qk_l2norm)
-        kda_prefill_tc_kernel<false, true><<<grid, NTHREADS, SMEM_BYTES, s>>>(maps, p);
-    else
-        kda_prefill_tc_kernel<false, false><<<grid, NTHREADS, SMEM_BYTES, s>>>(maps, p);
-    return cudaGetLastError();
+    const int f = (p.gate_bound > 0.f ? kGated : 0) | (p.qk_l2norm ? kNorm : 0) | (p.out_gate ? kOutGate : 0);
+    void *args[] = {(void *)&maps, (void *)&p};
+    return cudaLaunchKernel(kTcKernels[f], dim3((unsigned)(p.n_seqs * p.H)), dim3(NTHREADS), args, SMEM_BYTES, s);
 }
 
 }  // namespace kda

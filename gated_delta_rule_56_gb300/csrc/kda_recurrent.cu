@@ -89,12 +89,14 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
     __shared__ float red_k[2][kWarps][DV], red_q[2][kWarps][DV], red_qk[2][3][kWarps];
 
     const int row0 = w * RPW, col0 = l * CPL;
-    const size_t state_off = ((size_t)n * H + h) * DK * DV;
+    static_assert(DK == DV, "square states");
+    const long long init_off = p.init ? state_slot_offset(p.init_idx, p.pool, n, H, h, DK, p.err) : -1;
+    const long long fin_off = p.fin ? state_slot_offset(p.fin_idx, p.pool, n, H, h, DK, p.err) : -1;
     float s[RPW][CPL];
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
-        if (p.init) {
-            load_state<CPL>(p.init + state_off + (size_t)(row0 + r) * DV + col0, s[r]);
+        if (init_off >= 0) {
+            load_state<CPL>(p.init + init_off + (size_t)(row0 + r) * DV + col0, s[r]);
         } else {
 #pragma unroll
             for (int c = 0; c < CPL; ++c) s[r][c] = 0.f;
@@ -177,15 +179,20 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
             for (int c = 0; c < CPL; ++c) s[r][c] = fmaf(kk, u[c], s[r][c]);
         }
         if (w == 0) {
+            const Tin *z = static_cast<const Tin *>(p.out_gate);
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) store_elem(o, rr * DV + col0 + c, oo[c]);
+            for (int c = 0; c < CPL; ++c) {
+                float ov = oo[c];
+                if (z) ov *= 1.f / (1.f + expf(-load_elem(z, rr * DV + col0 + c)));  // output gate sigmoid(z)
+                store_elem(o, rr * DV + col0 + c, ov);
+            }
         }
     }
 
-    if (p.fin) {
+    if (fin_off >= 0) {
 #pragma unroll
         for (int r = 0; r < RPW; ++r)
-            store_state<CPL>(p.fin + state_off + (size_t)(row0 + r) * DV + col0, s[r]);
+            store_state<CPL>(p.fin + fin_off + (size_t)(row0 + r) * DV + col0, s[r]);
     }
 }
 

@@ -112,13 +112,16 @@ __global__ void __launch_bounds__(256) seg_done_kernel(const float *__restrict__
 // after the last segment is the final state. Thread (ti, tj) owns the 8 x 8 block at (8 ti, 8 tj).
 __global__ void __launch_bounds__(256) seg_scan_kernel(const float *__restrict__ mtr, const float *__restrict__ sloc,
                                                        const float *__restrict__ init, float *__restrict__ fin,
-                                                       __nv_bfloat16 *__restrict__ sst, int P, int H) {
+                                                       const int32_t *init_idx, const int32_t *fin_idx, int pool,
+                                                       unsigned *err, __nv_bfloat16 *__restrict__ sst, int P, int H) {
     extern __shared__ float S[];  // [128][132]
     constexpr int LD = 132;
     const int bh = blockIdx.x, b = bh / H, h = bh % H, tid = threadIdx.x;
     const int ti = tid >> 4, tj = tid & 15;
+    const long long init_off = init ? state_slot_offset(init_idx, pool, b, H, h, D, err) : -1;
+    const long long fin_off = fin ? state_slot_offset(fin_idx, pool, b, H, h, D, err) : -1;
     for (int e = tid; e < D * D; e += 256)
-        S[(e >> 7) * LD + (e & 127)] = init ? init[(size_t)bh * D * D + e] : 0.f;
+        S[(e >> 7) * LD + (e & 127)] = init_off >= 0 ? init[init_off + e] : 0.f;
     __syncthreads();
 #pragma unroll 1
     for (int p = 0; p < P; ++p) {
@@ -152,8 +155,8 @@ __global__ void __launch_bounds__(256) seg_scan_kernel(const float *__restrict__
             for (int j = 0; j < 8; ++j) S[(8 * ti + i) * LD + 8 * tj + j] = acc[i][j];
         __syncthreads();
     }
-    if (fin)
-        for (int e = tid; e < D * D; e += 256) fin[(size_t)bh * D * D + e] = S[(e >> 7) * LD + (e & 127)];
+    if (fin_off >= 0)
+        for (int e = tid; e < D * D; e += 256) fin[fin_off + e] = S[(e >> 7) * LD + (e & 127)];
 }
 
 // Offset of the 16-byte chunk (row r, channels 8j..8j+7) of an R-row operand in the
@@ -204,7 +207,8 @@ constexpr float kNegligible = 1e-30f;
 __global__ void __launch_bounds__(128) seg_correct_kernel(const __grid_constant__ CUtensorMap qt_map,
                                                           const __nv_bfloat16 *__restrict__ sst,
                                                           const uint8_t *__restrict__ done,
-                                                          __nv_bfloat16 *__restrict__ o, int T, int H, int Ls,
+                                                          __nv_bfloat16 *__restrict__ o,
+                                                          const __nv_bfloat16 *__restrict__ zg, int T, int H, int Ls,
                                                           int P, int p0, unsigned *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -285,6 +289,8 @@ __global__ void __launch_bounds__(128) seg_correct_kernel(const __grid_constant_
         tc_fence_after();
         const int rl = 32 * warp + lane;  // tile row = TMEM lane
         __nv_bfloat16 *orow = o + ((size_t)(row + rl) * H + h) * D;
+        // With an output gate the local pass stored sigmoid(z) o_loc, so the correction adds sigmoid(z) S^T qt.
+        const __nv_bfloat16 *zrow = zg ? zg + ((size_t)(row + rl) * H + h) * D : nullptr;
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
             float acc[32];
@@ -295,6 +301,15 @@ __global__ void __launch_bounds__(128) seg_correct_kernel(const __grid_constant_
                 for (int q = 0; q < 4; ++q) {
                     uint4 w = *reinterpret_cast<const uint4 *>(orow + 32 * cb + 8 * q);
                     uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                    if (zrow) {
+                        const uint4 z = __ldg(reinterpret_cast<const uint4 *>(zrow + 32 * cb + 8 * q));
+                        const uint32_t zw[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            acc[8 * q + 2 * e] *= __fdividef(1.f, 1.f + __expf(-__uint_as_float(zw[e] << 16)));
+                            acc[8 * q + 2 * e + 1] *= __fdividef(1.f, 1.f + __expf(-__uint_as_float(zw[e] & 0xffff0000u)));
+                        }
+                    }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float lo_v = __uint_as_float(ww[e] << 16) + acc[8 * q + 2 * e];
@@ -374,6 +389,8 @@ cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace,
     pa.identity_init = false;
     pa.max_chunks = 0;
     pa.skip = nullptr;
+    pa.init_idx = nullptr;
+    pa.fin_idx = nullptr;
     if ((e = launch_tc_prefill(pa, s)) != cudaSuccess) return e;
     // Pass 2: v = 0 from the identity (qt = M^T q into the workspace, M at the segment ends): first
     // up to the horizon, then, for the pairs whose M is not zero there, over the whole segment.
@@ -383,6 +400,8 @@ cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace,
     pb.o = qt;
     pb.fin = mtr;
     pb.max_chunks = kHorizon / 64;
+    pb.out_gate = nullptr;  // its "o" is qt
+    pb.qk_l2norm = p.qk_l2norm;
     if ((e = launch_tc_prefill(pb, s)) != cudaSuccess) return e;
     seg_done_kernel<<<(unsigned)(segs * H), 256, 0, s>>>(mtr, done);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -390,13 +409,15 @@ cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace,
     pb.skip = done;
     if ((e = launch_tc_prefill(pb, s)) != cudaSuccess) return e;
     // Start states of the segments and the final state.
-    seg_scan_kernel<<<(unsigned)(B * H), 256, kScanSmem, s>>>(mtr, sloc, p.init, p.fin, sst, pl.P, H);
+    seg_scan_kernel<<<(unsigned)(B * H), 256, kScanSmem, s>>>(mtr, sloc, p.init, p.fin, p.init_idx, p.fin_idx,
+                                                              p.pool, p.err, sst, pl.P, H);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // o += S_start^T qt, skipped for segment 0 when the initial state is zero.
     CUtensorMap qt_map;
     if (!encode_row_tile_map(&qt_map, qt, (long long)B * T, H)) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)((pl.Ls + CT * kTilesPerCta - 1) / (CT * kTilesPerCta)), (unsigned)segs, (unsigned)H);
-    seg_correct_kernel<<<grid, 128, kCorrectSmem, s>>>(qt_map, sst, done, static_cast<__nv_bfloat16 *>(p.o), T, H,
+    seg_correct_kernel<<<grid, 128, kCorrectSmem, s>>>(qt_map, sst, done, static_cast<__nv_bfloat16 *>(p.o),
+                                                       static_cast<const __nv_bfloat16 *>(p.out_gate), T, H,
                                                        pl.Ls, pl.P, p.init ? 0 : 1, p.err);
     return cudaGetLastError();
 }

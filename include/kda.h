@@ -72,6 +72,21 @@ typedef struct kda_options {
     int qk_l2norm;      /* non-zero: every row of q and of k (d_k values of one token and head)
                            is divided by sqrt(sum of its squares + 1e-6) in the kernels. The pages
                            do not describe this step; the workloads feed q and k as unit vectors */
+    /* Indexed state pool (serving with a prefill cache: "How Kimi K3 works", benebsworth, "KDA:
+     * a fixed memory instead of a growing bill"). With an index array, the matching state pointer
+     * is a pool fp32 [state_pool_size, H, dk, dv] and sequence n uses slot idx[n]: a negative slot
+     * means a zero initial state / no final-state write; a slot >= state_pool_size is treated the
+     * same way and sets KDA_ERR_INVALID_ARG in the error word (kda_check_status). Slots written by
+     * a call must not be read or written by any other sequence of that call. */
+    const int32_t *initial_state_indices; /* NULL or int32 [N] on the device */
+    const int32_t *final_state_indices;   /* NULL or int32 [N] on the device. Decode: NULL means
+                                             the slots of initial_state_indices (in place) */
+    int state_pool_size;                  /* slots in the pool; > 0 when an index array is given */
+    /* Output gate ("Kimi K3 Explained", researchpapers.dev, "Architecture at a glance": the output
+     * gate is an input-dependent full-rank projection). NULL, or that projection's output z with
+     * the layout and dtype of o ([B,T,H,dv] prefill, [N,H,dv] decode), 16-byte aligned: o is
+     * stored as o * sigmoid(z). The pages name no activation; the sigmoid is the plain reading. */
+    const void *out_gate;
 } kda_options;
 
 /*

@@ -56,13 +56,18 @@ def test_noalloc_capacity_and_argument_checks(lib):
 def test_options_are_checked_before_anything_runs(lib):
     import ctypes
     from gated_delta_rule_56_gb300._lib import KDAOptions
-    assert ctypes.sizeof(KDAOptions) == 16  # size_t, float, int: the C layout of kda_options
+    assert ctypes.sizeof(KDAOptions) == 48  # size_t, float, int, 2 pointers, int (+4 padding), pointer
     null6 = [None] * 6
     for bad in (KDAOptions(0, 0.0, 0), KDAOptions(4, 0.0, 0), KDAOptions(5000, 0.0, 1),
                 KDAOptions(16, -1.0, 0), KDAOptions(16, float("nan"), 0), KDAOptions(16, 2e4, 1)):
         assert lib.kda_prefill_ex(0, 1, 64, 1, 128, 128, *null6, 1, None, None, None, ctypes.byref(bad),
                                   None, 0, None) == 1
         assert lib.kda_decode_step_ex(0, 1, 1, 128, 128, *[None] * 7, ctypes.byref(bad), None) == 1
+    # State indices need a positive pool size and 4-byte alignment.
+    for bad in (KDAOptions(48, 0.0, 0, FAKE, None, 0), KDAOptions(48, 0.0, 0, None, FAKE + 2, 8),
+                KDAOptions(48, 0.0, 0, None, None, 0, FAKE + 8)):  # out_gate not 16-byte aligned
+        assert lib.kda_prefill_ex(0, 1, 64, 1, 128, 128, *null6, 1, None, None, None, ctypes.byref(bad),
+                                  None, 0, None) == 1
     # A caller built against a shorter struct (gate_bound only) is accepted: qk_l2norm defaults to 0,
     # and the call then fails on its NULL tensors, not on the options.
     short = KDAOptions(12, 0.0, 1)
