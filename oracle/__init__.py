@@ -14,6 +14,8 @@ Public functions take CPU tensors or arrays in the KDA layouts and return fp64 n
 * ``scaled_sigmoid_gate(x, bound)`` -> g = -bound * sigmoid(x) (log-decays from gate logits).
 * ``l2_normalize(x, eps=1e-6)`` -> rows along the last axis divided by sqrt(sum x^2 + eps).
 * ``output_gate(o, z)`` -> o * sigmoid(z) (the output gate).
+* ``backward(q, k, v, g, beta, d_o, d_final_state=None, ...)`` -> gradients (dict) of
+  sum(d_o * o) + sum(d_final_state * final_state).
 
 Layouts: q, k, g [B, T, H, d_k]; v [B, T, H, d_v]; beta [B, T, H]; with ``cu_seqlens``
 (int [N+1]) B must be 1 and the rows of sequence n are cu[n]..cu[n+1]-1. States are
@@ -55,6 +57,9 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
 def _declare(lib):
     lib.kda_oracle_scaled_sigmoid_gate.argtypes = [ctypes.c_int64, _dp, ctypes.c_double, _dp]
     lib.kda_oracle_scaled_sigmoid_gate.restype = ctypes.c_int
+    lib.kda_oracle_backward.argtypes = [ctypes.c_int, _i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
+    lib.kda_oracle_backward.restype = ctypes.c_int
     lib.kda_oracle_output_gate.argtypes = [ctypes.c_int64, _dp, _dp, _dp]
     lib.kda_oracle_output_gate.restype = ctypes.c_int
     lib.kda_oracle_l2_normalize.argtypes = [ctypes.c_int64, ctypes.c_int64, _dp, ctypes.c_double, _dp]
@@ -188,6 +193,32 @@ def chunked(q, k, v, g, beta, cu_seqlens=None, initial_state=None, chunk=64, n_t
     """The chunkwise form; with dump=True also returns per-chunk intermediates of the
     first (sequence, head) pair (flat fp64 arrays, chunk after chunk)."""
     return _run("chunked", q, k, v, g, beta, cu_seqlens, initial_state, n_threads, chunk, dump)
+
+
+def backward(q, k, v, g, beta, d_o, d_final_state=None, cu_seqlens=None, initial_state=None):
+    """Gradients of L = sum(d_o * o) + sum(d_final_state * final_state) through the recurrence.
+    Returns a dict of fp64 arrays: dq, dk, dg [B,T,H,dk], dv [B,T,H,dv], dbeta [B,T,H] and
+    d_initial_state [N,H,dk,dv] (the gradient with respect to the initial state, zeros or not)."""
+    q, k, v, g, beta, cu, B, T, H, dk, dv = _flatten(q, k, v, g, beta, cu_seqlens)
+    N = cu.size - 1
+    init = _f64(initial_state)
+    if init is not None and init.shape != (N, H, dk, dv):
+        raise ValueError(f"initial_state must be {(N, H, dk, dv)}, got {init.shape}")
+    do = _f64(d_o).reshape(B * T, H, dv)
+    dfin = _f64(d_final_state)
+    if dfin is not None and dfin.shape != (N, H, dk, dv):
+        raise ValueError(f"d_final_state must be {(N, H, dk, dv)}, got {dfin.shape}")
+    out = dict(dq=np.zeros((B * T, H, dk)), dk=np.zeros((B * T, H, dk)), dv=np.zeros((B * T, H, dv)),
+               dg=np.zeros((B * T, H, dk)), dbeta=np.zeros((B * T, H)), d_initial_state=np.zeros((N, H, dk, dv)))
+    rc = load_library().kda_oracle_backward(
+        ctypes.c_int(N), cu.ctypes.data_as(_i64p), H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+        _ptr(init), _ptr(do), _ptr(dfin), *(_ptr(out[n]) for n in ("dq", "dk", "dv", "dg", "dbeta", "d_initial_state")))
+    if rc != 0:
+        raise RuntimeError(f"oracle backward failed with code {rc}")
+    for n, d in (("dq", dk), ("dk", dk), ("dg", dk), ("dv", dv)):
+        out[n] = out[n].reshape(B, T, H, d)
+    out["dbeta"] = out["dbeta"].reshape(B, T, H)
+    return out
 
 
 def scaled_sigmoid_gate(x, bound):

@@ -34,6 +34,12 @@
  *                           The pages do not describe this step; the workloads feed q and k as
  *                           unit vectors per (token, head), and the library can form them in its
  *                           kernels. The eps (1e-6 there) only keeps a zero row finite.
+ *  kda_oracle_backward  -- gradients of L = sum(do * o) + sum(d_final * S_final) with respect
+ *                           to q, k, v, g, beta and the initial state, by reverse-mode
+ *                           differentiation of the recurrence token by token (the pages train
+ *                           the model but give no gradient method; this is the adjoint of the
+ *                           steps above, in reverse order: read-out, write, delta correction,
+ *                           decay). The states before each token are kept from a forward pass.
  *  kda_oracle_output_gate -- y = o * sigmoid(z) per element: the output gate, an input-dependent
  *                           full-rank projection z ("Kimi K3 Explained", researchpapers.dev,
  *                           "Architecture at a glance"); the pages name no activation, the
@@ -153,6 +159,102 @@ int kda_oracle_recurrent(int n_seqs, const int64_t *cu, int H, int dk, int dv,
 {
     problem_t p = {n_seqs, H, dk, dv, cu, q, k, v, g, beta, init_state, o, final_state};
     return run_recurrent(&p, n_threads);
+}
+
+/* ------------------------------------------------------------- backward pass ---------- */
+
+/*
+ * Reverse sweep of one (sequence, head). Per token, with S_prev the state before it:
+ *   forward pieces  Sd = Diag(alpha) S_prev, w = v - Sd^T k, u = beta w, S = Sd + k u^T, o = S^T q
+ *   adjoints        dq = S do;  dS += q do^T;  du = dS^T k;  dk = dS u;  dbeta = du . w;
+ *                   dv = beta du;  dSd = dS - k (beta du)^T;  dk -= Sd (beta du);
+ *                   dg = rowsum(dSd * Sd);  dS_prev = Diag(alpha) dSd
+ */
+int kda_oracle_backward(int n_seqs, const int64_t *cu, int H, int dk, int dv, const double *q,
+                        const double *k, const double *v, const double *g, const double *beta,
+                        const double *init_state, const double *d_o, const double *d_final,
+                        double *dq, double *dkk, double *dvv, double *dg, double *dbeta,
+                        double *d_init)
+{
+    problem_t p = {n_seqs, H, dk, dv, cu, q, k, v, g, beta, init_state, dq, NULL};
+    int err = check_problem(&p);
+    if (err) return err;
+    if (cu[n_seqs] > cu[0] && (!d_o || !dkk || !dvv || !dg || !dbeta)) return KDA_ORACLE_EBADARG;
+    const size_t ss = (size_t)dk * dv;
+    for (int n = 0; n < n_seqs; ++n)
+        for (int h = 0; h < H; ++h) {
+            const int64_t t0 = cu[n], len = cu[n + 1] - cu[n];
+            double *hist = malloc(sizeof(double) * (ss * (size_t)(len + 4) + 2 * (size_t)dv));
+            if (!hist) return KDA_ORACLE_ENOMEM;
+            double *Sd = hist + ss * (size_t)len, *St = Sd + ss, *dS = St + ss, *dSd = dS + ss;
+            double *w = dSd + ss, *du = w + dv;
+            /* forward: hist[t] = state before token t0 + t */
+            load_state(&p, n, h, Sd);
+            for (int64_t t = 0; t < len; ++t) {
+                size_t r = (size_t)(t0 + t) * H + h;
+                memcpy(hist + ss * (size_t)t, Sd, ss * sizeof(double));
+                recurrent_token(dk, dv, q + r * dk, k + r * dk, v + r * dv, g + r * dk, beta[r], Sd, St, w);
+            }
+            if (d_final) memcpy(dS, d_final + ((size_t)n * H + h) * ss, ss * sizeof(double));
+            else memset(dS, 0, ss * sizeof(double));
+            for (int64_t t = len - 1; t >= 0; --t) {
+                size_t r = (size_t)(t0 + t) * H + h;
+                const double *kt = k + r * dk, *qt = q + r * dk, *vt = v + r * dv, *gt = g + r * dk;
+                const double *dot = d_o + r * dv, bt = beta[r];
+                const double *Sp = hist + ss * (size_t)t;
+                for (int i = 0; i < dk; ++i) {
+                    double a = exp(gt[i]);
+                    for (int j = 0; j < dv; ++j) Sd[(size_t)i * dv + j] = a * Sp[(size_t)i * dv + j];
+                }
+                for (int j = 0; j < dv; ++j) {
+                    double kv = 0.0;
+                    for (int i = 0; i < dk; ++i) kv += Sd[(size_t)i * dv + j] * kt[i];
+                    w[j] = vt[j] - kv;
+                }
+                for (int i = 0; i < dk; ++i)
+                    for (int j = 0; j < dv; ++j) St[(size_t)i * dv + j] = Sd[(size_t)i * dv + j] + kt[i] * bt * w[j];
+                /* o = S^T q */
+                for (int i = 0; i < dk; ++i) {
+                    double acc = 0.0;
+                    for (int j = 0; j < dv; ++j) acc += St[(size_t)i * dv + j] * dot[j];
+                    dq[r * dk + i] = acc;
+                }
+                for (int i = 0; i < dk; ++i)
+                    for (int j = 0; j < dv; ++j) dS[(size_t)i * dv + j] += qt[i] * dot[j];
+                /* S = Sd + k u^T */
+                double db = 0.0;
+                for (int j = 0; j < dv; ++j) {
+                    double acc = 0.0;
+                    for (int i = 0; i < dk; ++i) acc += kt[i] * dS[(size_t)i * dv + j];
+                    du[j] = acc;
+                    db += acc * w[j];
+                }
+                dbeta[r] = db;
+                for (int j = 0; j < dv; ++j) dvv[r * dv + j] = bt * du[j];
+                for (int i = 0; i < dk; ++i) {
+                    double acc = 0.0;
+                    for (int j = 0; j < dv; ++j)
+                        acc += dS[(size_t)i * dv + j] * bt * w[j] - Sd[(size_t)i * dv + j] * bt * du[j];
+                    dkk[r * dk + i] = acc;
+                }
+                /* u = beta (v - Sd^T k): the k-read of Sd */
+                for (int i = 0; i < dk; ++i)
+                    for (int j = 0; j < dv; ++j)
+                        dSd[(size_t)i * dv + j] = dS[(size_t)i * dv + j] - kt[i] * bt * du[j];
+                /* Sd = Diag(alpha) S_prev */
+                for (int i = 0; i < dk; ++i) {
+                    double a = exp(gt[i]), acc = 0.0;
+                    for (int j = 0; j < dv; ++j) {
+                        acc += dSd[(size_t)i * dv + j] * Sd[(size_t)i * dv + j];
+                        dS[(size_t)i * dv + j] = a * dSd[(size_t)i * dv + j];
+                    }
+                    dg[r * dk + i] = acc;
+                }
+            }
+            if (d_init) memcpy(d_init + ((size_t)n * H + h) * ss, dS, ss * sizeof(double));
+            free(hist);
+        }
+    return 0;
 }
 
 /* ------------------------------------------------------ literal transition form ------- */

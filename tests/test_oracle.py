@@ -488,3 +488,97 @@ def test_gate_symmetry_slope_and_range():
 def test_gate_rejects_bad_bound():
     with pytest.raises(ValueError):
         oracle.scaled_sigmoid_gate(np.zeros(3), 0.0)
+
+
+# ---------------------------------------------------------------- backward pass -------------
+# Gradients of L = sum(do * o) + sum(dS * S_final). Pinned by central finite differences of the
+# forward oracle (itself pinned above) and by the closed form of a single token from a zero state.
+
+def _bwd_case(seed=11, dk=3, dv=2, lengths=(4, 3), H=2):
+    rng = np.random.default_rng(seed)
+    T = sum(lengths)
+    x = dict(q=rng.standard_normal((1, T, H, dk)), k=rng.standard_normal((1, T, H, dk)) * 0.6,
+             v=rng.standard_normal((1, T, H, dv)), g=-rng.uniform(0.05, 1.5, (1, T, H, dk)),
+             beta=rng.uniform(0.2, 0.9, (1, T, H)))
+    N = len(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    init = rng.standard_normal((N, H, dk, dv)) * 0.5
+    do = rng.standard_normal((1, T, H, dv))
+    dfin = rng.standard_normal((N, H, dk, dv))
+    return x, cu, init, do, dfin
+
+
+def _loss(x, cu, init, do, dfin):
+    o, fin = oracle.recurrent(*(x[n] for n in ("q", "k", "v", "g", "beta")), cu_seqlens=cu, initial_state=init)
+    return float((o * do).sum() + (fin * dfin).sum())
+
+
+def test_backward_matches_central_differences():
+    x, cu, init, do, dfin = _bwd_case()
+    grads = oracle.backward(*(x[n] for n in ("q", "k", "v", "g", "beta")), do, dfin, cu_seqlens=cu,
+                            initial_state=init)
+    h = 1e-6
+    for name, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta"), (None, "d_initial_state")):
+        base = init if name is None else x[name]
+        fd = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            saved = base[idx]
+            base[idx] = saved + h
+            lp = _loss(x, cu, init, do, dfin)
+            base[idx] = saved - h
+            lm = _loss(x, cu, init, do, dfin)
+            base[idx] = saved
+            fd[idx] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(grads[gname], fd, rtol=1e-6, atol=1e-7, err_msg=gname)
+
+
+def test_backward_single_token_closed_form():
+    # From a zero state one token gives S = beta k v^T and o = beta (q.k) v, so with dS_final = 0:
+    # dq = beta (v.do) k, dk = beta (v.do) q, dv = beta (q.k) do, dbeta = (q.k)(v.do), dg = 0 (it
+    # multiplies the zero state), and, since S1 = (I - beta k k^T) Diag(alpha) S0 + beta k v^T,
+    # dS0 = Diag(alpha) (q - beta (k.q) k) do^T.
+    rng = np.random.default_rng(5)
+    q, k, v, do = rng.standard_normal(4), rng.standard_normal(4), rng.standard_normal(3), rng.standard_normal(3)
+    b = 0.7
+    r = lambda a: a.reshape(1, 1, 1, -1)
+    grads = oracle.backward(r(q), r(k), r(v), r(-np.full(4, 0.3)), np.full((1, 1, 1), b), r(do))
+    qk, vdo = q @ k, v @ do
+    np.testing.assert_allclose(grads["dq"].ravel(), b * vdo * k, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(grads["dk"].ravel(), b * vdo * q, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(grads["dv"].ravel(), b * qk * do, rtol=1e-13, atol=1e-14)
+    assert grads["dbeta"].item() == pytest.approx(qk * vdo, rel=1e-13)
+    assert np.all(grads["dg"] == 0.0)
+    ds0 = np.outer(np.exp(-0.3) * (q - b * qk * k), do)
+    np.testing.assert_allclose(grads["d_initial_state"].reshape(4, 3), ds0, rtol=1e-13, atol=1e-14)
+
+
+_BWD_PINS = [test_backward_matches_central_differences, test_backward_single_token_closed_form]
+_BWD_MUTANTS = [
+    ("state gradient not decayed", "dS[(size_t)i * dv + j] = a * dSd[(size_t)i * dv + j];",
+     "dS[(size_t)i * dv + j] = dSd[(size_t)i * dv + j];"),
+    ("dropped k-read term of dSd", "dSd[(size_t)i * dv + j] = dS[(size_t)i * dv + j] - kt[i] * bt * du[j];",
+     "dSd[(size_t)i * dv + j] = dS[(size_t)i * dv + j];"),
+    ("wrong sign in dk", "acc += dS[(size_t)i * dv + j] * bt * w[j] - Sd[(size_t)i * dv + j] * bt * du[j];",
+     "acc += dS[(size_t)i * dv + j] * bt * w[j] + Sd[(size_t)i * dv + j] * bt * du[j];"),
+    ("dv without beta", "dvv[r * dv + j] = bt * du[j];", "dvv[r * dv + j] = du[j];"),
+    ("read-out gradient from the pre-write state", "acc += St[(size_t)i * dv + j] * dot[j];",
+     "acc += Sd[(size_t)i * dv + j] * dot[j];"),
+    ("dg against the undecayed state", "acc += dSd[(size_t)i * dv + j] * Sd[(size_t)i * dv + j];",
+     "acc += dSd[(size_t)i * dv + j] * Sp[(size_t)i * dv + j];"),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(_BWD_MUTANTS)))
+def test_backward_pins_catch_planted_mistakes(tmp_path, idx):
+    desc, old, new = _BWD_MUTANTS[idx]
+    text = open(oracle._SRC).read()
+    assert text.count(old) == 1, f"mutation site not found: {desc}"
+    path = _build_mutant(tmp_path, text.replace(old, new, 1), 300 + idx)
+    caught = []
+    with oracle.use_library(path):
+        for pin in _BWD_PINS:
+            try:
+                pin()
+            except AssertionError:
+                caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake: {desc}"
