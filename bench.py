@@ -35,6 +35,12 @@ if ROOT not in sys.path:
 import torch  # noqa: E402
 
 METRIC = "KDA prefill tokens/s and decode tokens/s on 1 GB300; % of roofline"
+# Backward: algorithmic fp32 flops per state element per token (a forward step to rebuild the
+# state: decay 1, k-read 2, write 2; the reverse step: decay 1, k-read 2, dq 2, q do^T 2, dS^T k 2,
+# dk 3, dSd 2, dg 2, decay 1) and the fp32 FMA peak (152 SMs x 128 lanes x 2 flops x 2.07 GHz).
+BWD_FLOPS_PER_ELEM = 22
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
 PF = dict(B=4, T=8192, H=32, d=128, chunk=64)
 DEC = dict(N=256, H=32, d=128, steps=1000)
 NAMES = ("q", "k", "v", "g", "beta")
@@ -52,13 +58,14 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("varlen", "long", "gated", "l2norm", "outgate"), default=None,
+    ap.add_argument("--workload", choices=("varlen", "long", "gated", "l2norm", "outgate", "backward"), default=None,
                     help="time one of the other prefill workloads instead of the headline (one JSON line): "
                          "varlen = 64 packed sequences of U[128, 16384] tokens with initial states; "
                          "long = one sequence of 1,048,576 tokens (B=1, H=32); "
                          "gated = the headline shape with gate logits (decays formed in the kernel); "
                          "l2norm = the headline shape with raw q/k rows L2-normalised in the kernel; "
-                         "outgate = the headline shape with the output gate o * sigmoid(z) in the kernel")
+                         "outgate = the headline shape with the output gate o * sigmoid(z) in the kernel; "
+                         "backward = all gradients of the headline shape (kda_backward)")
     ap.add_argument("--ncu-case", choices=("prefill", "decode"),
                     help="run two launches of the small profiling case (for ncu) and exit")
     args = ap.parse_args()
@@ -454,6 +461,13 @@ def run_workload(args):
         kw = {}
         alg = prefill_bytes(1, T, H, d)
         name = f"KDA chunked prefill, long context: B=1 T={T} H={H} dk=dv={d} bf16, zero init"
+    elif args.workload == "backward":
+        B, T = PF["B"], PF["T"]
+        x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)
+        tokens, n_seq = B * T, B
+        kw = dict(d_o=ki.gate_logits_like(x["v"], seed=4))  # dL/do ~ N(0, 1)
+        alg = tokens * H * BWD_FLOPS_PER_ELEM * d * d       # algorithmic fp32 flops (ALU-bound)
+        name = f"KDA backward (all gradients, fp32 on CUDA cores): B={B} T={T} H={H} dk=dv={d} bf16 inputs"
     elif args.workload == "outgate":
         B, T = PF["B"], PF["T"]
         x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)
@@ -481,11 +495,14 @@ def run_workload(args):
     # A call that the library splits along the sequence (few long sequences; it asks for a
     # workspace) launches 7 kernels: segment bounds, the local pass, the transition pass up to the
     # horizon, the zero test, the transition pass over the rest, the scan and the correction.
-    split = args.workload != "varlen" and kda.load().kda_prefill_workspace_size(0, n_seq, tokens // n_seq, H, d, d, n_seq) > 0
+    split = args.workload not in ("varlen", "backward") and kda.load().kda_prefill_workspace_size(0, n_seq, tokens // n_seq, H, d, d, n_seq) > 0
     launches_per_step = 7 if split else 1
 
     def step(_i):
-        kda.prefill(*args_in, **kw)
+        if args.workload == "backward":
+            kda.backward(*args_in, kw["d_o"])
+        else:
+            kda.prefill(*args_in, **kw)
 
     step(0)
     kda.check_status()
@@ -496,13 +513,20 @@ def run_workload(args):
     kda.check_status()
     kernel_ms = statistics.mean(per)
     achieved = alg / (kernel_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s", "frac": achieved / peak_bw,
+            "peak_source": peak_kind, "alg_bytes_per_launch": alg, "kernel_ms": kernel_ms}
+    if args.workload == "backward":  # fp32 FMA pipes: 152 SMs x 128 lanes x 2 flops x 2.07 GHz
+        roof = {"bound": "alu", "achieved": alg / (kernel_ms / 1e3) / 1e12, "peak": FP32_ALU_TFLOPS,
+                "unit": "TFLOP/s", "frac": alg / (kernel_ms / 1e3) / 1e12 / FP32_ALU_TFLOPS,
+                "peak_source": "derived from unit counts and the maximum SM clock", "alg_flops_per_launch": alg,
+                "kernel_ms": kernel_ms}
+        launches_per_step = 5  # four zero fills and the backward kernel
     print(json.dumps({
-        "metric": f"KDA prefill tokens/s ({args.workload})", "value": tokens / (kernel_ms / 1e3), "unit": "tokens/s",
+        "metric": f"KDA {'backward' if args.workload == 'backward' else 'prefill'} tokens/s ({args.workload})",
+        "value": tokens / (kernel_ms / 1e3), "unit": "tokens/s",
         "n_gpus": 1, "steps": steps, "warmup": warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
         "dtype": "bf16", "data": "synthetic", "config": {"workload": name, "pairs": n_seq * H, "split_along_sequence": bool(split)},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s",
-                     "frac": achieved / peak_bw, "peak_source": peak_kind, "alg_bytes_per_launch": alg,
-                     "kernel_ms": kernel_ms},
+        "roofline": roof,
         "gpu_launches": steps * launches_per_step, "clocks": clk.summary()}), flush=True)
 
 

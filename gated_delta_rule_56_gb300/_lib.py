@@ -82,6 +82,10 @@ def load():
         lib.kda_decode_step_ex.argtypes = [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                            ctypes.POINTER(KDAOptions), _vp]
         lib.kda_decode_step_ex.restype = _i
+        lib.kda_backward.argtypes = [_i, _i, _i, _i, _i, _i] + [_vp] * 6 + [_i] + [_vp] * 10 + [ctypes.c_size_t, _vp]
+        lib.kda_backward.restype = _i
+        lib.kda_backward_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+        lib.kda_backward_workspace_size.restype = ctypes.c_size_t
         lib.kda_prefill_noalloc.argtypes = [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp,
                                             _vp, _vp, _vp]
         lib.kda_prefill_noalloc.restype = _i
@@ -275,6 +279,50 @@ def decode_step(q, k, v, g, beta, state, o=None, gate_bound=None, qk_l2norm=Fals
                                            _ptr(beta), _ptr(state), _ptr(o), float(gate_bound), _stream(dev))
     _raise_if(st)
     return o
+
+
+def backward(q, k, v, g, beta, d_o, cu_seqlens=None, initial_state=None, d_final_state=None,
+             want_d_initial_state=True):
+    """Gradients of sum(d_o * o) + sum(d_final_state * final_state) through ``prefill`` (plain
+    log-decays g). Inputs as ``prefill``; d_o has the layout and dtype of o; d_final_state fp32
+    [N, H, dk, dv] or None. Returns a dict of fp32 tensors: dq, dk, dg [B, T, H, dk], dv
+    [B, T, H, dv], dbeta [B, T, H] and d_initial_state [N, H, dk, dv] (or None)."""
+    lib = load()
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t, shp in (("q", q, (B, T, H, dk)), ("k", k, (B, T, H, dk)), ("g", g, (B, T, H, dk)),
+                         ("v", v, (B, T, H, dv)), ("beta", beta, (B, T, H)), ("d_o", d_o, (B, T, H, dv))):
+        _check(name, t, q.dtype, shp, dev)
+    if cu_seqlens is not None:
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+            raise ValueError("cu_seqlens must be a 1-D int32 tensor [N+1]")
+        _check("cu_seqlens", cu_seqlens, torch.int32, (cu_seqlens.numel(),), dev)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    for name, t in (("initial_state", initial_state), ("d_final_state", d_final_state)):
+        if t is not None:
+            _check(name, t, torch.float32, (N, H, dk, dv), dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = dict(dq=torch.empty(B, T, H, dk, **f32), dk=torch.empty(B, T, H, dk, **f32),
+               dv=torch.empty(B, T, H, dv, **f32), dg=torch.empty(B, T, H, dk, **f32),
+               dbeta=torch.empty(B, T, H, **f32),
+               d_initial_state=torch.empty(N, H, dk, dv, **f32) if want_d_initial_state else None)
+    dt = _DTYPES[q.dtype]
+    ws_bytes = int(lib.kda_backward_workspace_size(dt, B, T, H, dk, dv, N))
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.kda_backward(dt, B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                              _ptr(cu_seqlens), N, _ptr(initial_state), _ptr(d_o), _ptr(d_final_state),
+                              *(_ptr(out[n]) for n in ("dq", "dk", "dv", "dg", "dbeta", "d_initial_state")),
+                              _ptr(ws), ws_bytes, _stream(dev))
+    _raise_if(st)
+    return out
 
 
 def selftest_wait_timeout(limit_ns: int, device=None):

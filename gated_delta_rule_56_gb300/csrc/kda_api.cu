@@ -358,6 +358,63 @@ kda_status kda_prefill_noalloc(kda_dtype dtype, int B, int T, int H, int dk, int
     return st;
 }
 
+size_t kda_backward_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv, int n_seqs) {
+    (void)dtype;
+    if (B < 0 || T < 0 || H <= 0 || dk != dv || dk <= 0) return 0;
+    return backward_workspace_bytes((int)((long long)B * T > 0x7fffffffLL ? 0x7fffffff : (long long)B * T),
+                                    n_seqs > B ? n_seqs : B, H, dk);
+}
+
+kda_status kda_backward(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q, const void *k,
+                        const void *v, const void *g, const void *beta, const int32_t *cu_seqlens, int n_seqs,
+                        const float *initial_state, const void *d_o, const float *d_final_state, float *dq,
+                        float *dk_out, float *dv_out, float *dg, float *dbeta, float *d_initial_state,
+                        void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+    kda_status st;
+    if ((st = check_dtype(dtype)) != KDA_OK) return st;
+    if (B < 0 || T < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "negative size B=%d T=%d H=%d", B, T, H);
+    if ((st = check_head(dk, dv)) != KDA_OK) return st;
+    if (cu_seqlens) {
+        if (B != 1) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens requires B == 1 (got B=%d)", B);
+        if (n_seqs < 0) return fail(KDA_ERR_INVALID_ARG, "n_seqs=%d is negative", n_seqs);
+        if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is not 4-byte aligned");
+    } else {
+        n_seqs = B;
+    }
+    const long long rows = (long long)B * T;
+    if ((long long)n_seqs * H > 0x7fffffffLL || rows > 0x7fffffffLL)
+        return fail(KDA_ERR_INVALID_ARG, "too many rows or (sequence, head) pairs");
+    if ((long long)n_seqs * H == 0) return ok();
+    if (rows > 0) {
+        if ((st = check_ptr(q, "q", true)) || (st = check_ptr(k, "k", true)) || (st = check_ptr(v, "v", true)) ||
+            (st = check_ptr(g, "g", true)) || (st = check_ptr(beta, "beta", false)) ||
+            (st = check_ptr(d_o, "d_o", true)) || (st = check_ptr(dq, "dq", true)) ||
+            (st = check_ptr(dk_out, "dk", true)) || (st = check_ptr(dv_out, "dv", true)) ||
+            (st = check_ptr(dg, "dg", true)) || (st = check_ptr(dbeta, "dbeta", false)))
+            return st;
+    }
+    if ((initial_state && !aligned16(initial_state)) || (d_final_state && !aligned16(d_final_state)) ||
+        (d_initial_state && !aligned16(d_initial_state)))
+        return fail(KDA_ERR_INVALID_ARG, "state pointers must be 16-byte aligned");
+    const size_t need = backward_workspace_bytes((int)rows, n_seqs, H, dk);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+        return fail(KDA_ERR_INVALID_ARG, "workspace: %zu bytes at a 16-byte aligned address needed, got %zu",
+                    need, workspace ? workspace_bytes : (size_t)0);
+    RunParams p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    p.cu_seqlens = cu_seqlens;
+    p.init = initial_state;
+    p.T = T;
+    p.H = H;
+    p.n_seqs = n_seqs;
+    p.err = device_error_word();
+    if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word");
+    return launched(launch_backward(dtype, dk, p, d_o, d_final_state, dq, dk_out, dv_out, dg, dbeta,
+                                    d_initial_state, workspace, reinterpret_cast<cudaStream_t>(stream)),
+                    "backward");
+}
+
 kda_status kda_decode_step(kda_dtype dtype, int N, int H, int dk, int dv, const void *q, const void *k,
                            const void *v, const void *g, const void *beta, float *state, void *o,
                            kda_stream_t stream) {

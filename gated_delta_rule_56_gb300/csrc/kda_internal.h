@@ -57,6 +57,12 @@ size_t segmented_workspace_bytes(kda_dtype dtype, int B, int T, int H, int dk, i
 cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace, size_t workspace_bytes,
                                      cudaStream_t s);
 
+// Backward pass (see kda_backward.cu): workspace bytes for the state checkpoints, and the launch.
+size_t backward_workspace_bytes(int T_total, int n_seqs, int H, int d);
+cudaError_t launch_backward(kda_dtype dtype, int d, const RunParams &p, const void *d_o, const float *d_fin,
+                            float *dq, float *dk, float *dv, float *dg, float *dbeta, float *d_init, void *ws,
+                            cudaStream_t s);
+
 // Element offset of the state of (sequence n, head h) in a state tensor of d x d blocks, or -1
 // when the sequence has none there. Without an index array the tensor holds one state per
 // sequence; with one it is a pool of `pool` states and idx[n] picks the slot (negative: none; at

@@ -150,6 +150,34 @@ KDA_API kda_status kda_decode_step_ex(kda_dtype dtype, int N, int H, int dk, int
                                       const kda_options *options, kda_stream_t stream);
 
 /*
+ * kda_backward -- gradients of L = sum(d_o * o) + sum(d_final_state * final_state) through
+ * kda_prefill's computation (plain log-decays; no options), on CUDA cores in fp32. The pages
+ * train the model ("Kimi K3 Explained", researchpapers.dev, "Architecture at a glance") but give
+ * no gradient method: this is reverse-mode differentiation of the token recurrence.
+ *
+ * dtype, B, T, H, dk, dv, q, k, v, g, beta, cu_seqlens, n_seqs, initial_state: as kda_prefill.
+ * d_o          [B, T, H, dv] in `dtype`: dL/do.
+ * d_final_state  fp32 [N, H, dk, dv] or NULL (zero): dL/dS_final.
+ * dq, dk, dg   fp32 [B, T, H, dk]; dv fp32 [B, T, H, dv]; dbeta fp32 [B, T, H]: written in full
+ *              (dg is with respect to the log-decay g).
+ * d_initial_state  fp32 [N, H, dk, dv] or NULL (not written): dL/dS_initial (also without an
+ *              initial state: the gradient at the zero state).
+ * workspace    device scratch of at least kda_backward_workspace_size() bytes, 16-byte aligned,
+ *              owned by the caller (state checkpoints every 64 tokens, 64 KiB per head for d=128).
+ * Supported: dk == dv in {32, 64, 128}; bf16 or fp32 inputs. Alignment as kda_prefill.
+ */
+KDA_API kda_status kda_backward(kda_dtype dtype, int B, int T, int H, int dk, int dv,
+                                const void *q, const void *k, const void *v, const void *g,
+                                const void *beta, const int32_t *cu_seqlens, int n_seqs,
+                                const float *initial_state, const void *d_o, const float *d_final_state,
+                                float *dq, float *dk_out, float *dv_out, float *dg, float *dbeta,
+                                float *d_initial_state, void *workspace, size_t workspace_bytes,
+                                kda_stream_t stream);
+
+/* Bytes of workspace kda_backward needs for these sizes (an upper bound for any n_seqs <= max(B, n_seqs)). */
+KDA_API size_t kda_backward_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv, int n_seqs);
+
+/*
  * kda_prefill_noalloc -- kda_prefill without a caller workspace and without any allocation: a
  * call that is split along the sequence uses a fixed scratch array compiled into the library
  * (one per device, kda_prefill_noalloc_capacity() bytes, placed when the library's device code
