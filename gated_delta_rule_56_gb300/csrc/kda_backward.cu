@@ -14,8 +14,10 @@
 // thread ever needs another column's state. The reverse sweep needs the state before every
 // token: a forward sweep stores the column state every kChunk tokens (global workspace); each
 // chunk is then replayed from its checkpoint keeping the state every kSub tokens in registers,
-// and each token's state is rebuilt from the nearest of those (at most kSub - 1 steps). dq, dk,
-// dg and dbeta are sums over all columns: per kSub tokens the warps add their parts in shared
+// and each token's state is rebuilt from the nearest of those (at most kSub - 1 steps). A
+// chunk's inputs (k, exp g, q as fp32 rows, beta, and v, dO of the CTA's columns) are staged in
+// shared memory once per CTA, so every step reads them there. dq, dk, dg and dbeta are sums over
+// all columns: per kSub tokens the warps add their parts in shared
 // memory, then the CTA adds the block to the fp32 outputs with global atomics (one per column
 // block); dv and dS_initial belong to one column and are stored directly.
 #include "kda_internal.h"
@@ -37,35 +39,63 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-// Per-token inputs a lane needs: its rows of k (and a = exp g), beta and v of the warp's column.
-template <typename Tin, int RPL>
-struct Tok {
-    float k[RPL], a[RPL], beta, v;
-    __device__ __forceinline__ void load(const RunParams &p, size_t r, int row0, int j, int DV) {
-        const Tin *kk = static_cast<const Tin *>(p.k) + r * (RPL * 32) + row0;
-        const Tin *gg = static_cast<const Tin *>(p.g) + r * (RPL * 32) + row0;
-#pragma unroll
-        for (int i = 0; i < RPL; ++i) {
-            k[i] = ld(kk, i);
-            a[i] = expf(ld(gg, i));
-        }
-        beta = ld(static_cast<const Tin *>(p.beta), r);
-        v = ld(static_cast<const Tin *>(p.v), r * DV + j);
-    }
+// Shared-memory layout of one staged chunk (kChunk tokens) for head size DK.
+template <int DK>
+struct Stage {
+    static constexpr int K = 0;                              // fp32 [kChunk][DK]: k
+    static constexpr int A = K + kChunk * DK;                // fp32 [kChunk][DK]: exp(g)
+    static constexpr int Q = A + kChunk * DK;                // fp32 [kChunk][DK]: q
+    static constexpr int V = Q + kChunk * DK;                // fp32 [kChunk][kCols]: v of the CTA's columns
+    static constexpr int DO = V + kChunk * kCols;            // fp32 [kChunk][kCols]: dO of those columns
+    static constexpr int B = DO + kChunk * kCols;            // fp32 [kChunk]: beta
+    static constexpr int ACC = B + kChunk;                   // fp32 [kSub][3][DK]: dq, dk, dg sums
+    static constexpr int ACCB = ACC + kSub * 3 * DK;         // fp32 [kSub]: dbeta sums
+    static constexpr int FLOATS = ACCB + kSub;
+    static constexpr size_t BYTES = FLOATS * sizeof(float);
 };
 
-// One forward token on the lane's rows of one column.
-template <typename Tin, int RPL>
-__device__ __forceinline__ void step(float (&S)[RPL], const Tok<Tin, RPL> &t) {
+// Stage the inputs of tokens [c0, c0 + kChunk) (rows past eos read as identity tokens: k = 0,
+// exp g = 1). With `rev` also q and dO, which only the reverse sweep reads.
+template <typename Tin, int DK>
+__device__ __forceinline__ void stage_chunk(float *sm, const RunParams &p, const Tin *dop, long long c0,
+                                            long long eos, int H, int h, int j0, bool rev) {
+    using L = Stage<DK>;
+    const Tin *kp = static_cast<const Tin *>(p.k), *gp = static_cast<const Tin *>(p.g);
+    const Tin *qp = static_cast<const Tin *>(p.q), *vp = static_cast<const Tin *>(p.v);
+    const Tin *bp = static_cast<const Tin *>(p.beta);
+    for (int e = threadIdx.x; e < kChunk * DK; e += kThreads) {
+        const int t = e / DK, i = e % DK;
+        const bool live = c0 + t < eos;
+        const size_t r = ((size_t)(c0 + t) * H + h) * DK + i;
+        sm[L::K + e] = live ? ld(kp, r) : 0.f;
+        sm[L::A + e] = live ? expf(ld(gp, r)) : 1.f;
+        if (rev) sm[L::Q + e] = live ? ld(qp, r) : 0.f;
+    }
+    for (int e = threadIdx.x; e < kChunk * kCols; e += kThreads) {
+        const int t = e / kCols, c = e % kCols;
+        const bool live = c0 + t < eos;
+        const size_t r = ((size_t)(c0 + t) * H + h) * DK + j0 + c;
+        sm[L::V + e] = live ? ld(vp, r) : 0.f;
+        if (rev) sm[L::DO + e] = live ? ld(dop, r) : 0.f;
+    }
+    for (int t = threadIdx.x; t < kChunk; t += kThreads)
+        sm[L::B + t] = c0 + t < eos ? ld(bp, (size_t)(c0 + t) * H + h) : 0.f;
+}
+
+// One forward token (index tt of the staged chunk) on the lane's rows of column `col`.
+template <int DK, int RPL>
+__device__ __forceinline__ void step(float (&S)[RPL], const float *sm, int tt, int row0, int col) {
+    using L = Stage<DK>;
+    const float *k = sm + L::K + tt * DK + row0, *a = sm + L::A + tt * DK + row0;
     float ks = 0.f;
 #pragma unroll
     for (int i = 0; i < RPL; ++i) {
-        S[i] *= t.a[i];
-        ks = fmaf(t.k[i], S[i], ks);
+        S[i] *= a[i];
+        ks = fmaf(k[i], S[i], ks);
     }
-    const float u = t.beta * (t.v - warp_sum(ks));
+    const float u = sm[L::B + tt] * (sm[L::V + tt * kCols + col] - warp_sum(ks));
 #pragma unroll
-    for (int i = 0; i < RPL; ++i) S[i] = fmaf(t.k[i], u, S[i]);
+    for (int i = 0; i < RPL; ++i) S[i] = fmaf(k[i], u, S[i]);
 }
 
 template <typename Tin, int DK>
@@ -73,12 +103,14 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(RunParams p, const v
                                                           float *dq, float *dk, float *dv, float *dg,
                                                           float *dbeta, float *d_init, float *ck) {
     constexpr int DV = DK, RPL = DK / 32;
-    __shared__ float acc[kSub][3][DK];  // dq, dk, dg of the current kSub tokens, summed over columns
-    __shared__ float accb[kSub];        // dbeta
+    using L = Stage<DK>;
+    extern __shared__ float sm[];
+    float *acc = sm + L::ACC, *accb = sm + L::ACCB;
     const int H = p.H, h = blockIdx.x % H, n = blockIdx.x / H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int j = blockIdx.y * kCols + warp;  // this warp's value column
+    const int j0 = blockIdx.y * kCols, j = j0 + warp;  // this warp's value column
     const int row0 = lane * RPL;
+    const Tin *dop = static_cast<const Tin *>(d_o);
 
     long long bos, eos;
     if (p.cu_seqlens) {
@@ -97,7 +129,7 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(RunParams p, const v
     const int nchunks = (int)((eos - bos + kChunk - 1) / kChunk);
     auto ck_ptr = [&](int c) { return ck + (((size_t)(ck0 + c) * H + h) * DV + j) * DK + row0; };
 
-    for (int e = threadIdx.x; e < kSub * 3 * DK; e += kThreads) (&acc[0][0][0])[e] = 0.f;
+    for (int e = threadIdx.x; e < kSub * 3 * DK; e += kThreads) acc[e] = 0.f;
     if (threadIdx.x < kSub) accb[threadIdx.x] = 0.f;
 
     const size_t sbase = ((size_t)n * H + h) * DK * DV;
@@ -107,26 +139,26 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(RunParams p, const v
 
     // Forward sweep: the column state at every chunk start.
     for (int c = 0; c < nchunks; ++c) {
+        const long long c0 = bos + (long long)c * kChunk;
         float *dst = ck_ptr(c);
 #pragma unroll
         for (int i = 0; i < RPL; ++i) dst[i] = S[i];
-        const long long t1 = min(bos + (long long)(c + 1) * kChunk, eos);
-        for (long long t = bos + (long long)c * kChunk; t < t1; ++t) {
-            Tok<Tin, RPL> tk;
-            tk.load(p, (size_t)t * H + h, row0, j, DV);
-            step<Tin, RPL>(S, tk);
-        }
+        __syncthreads();  // the previous chunk's inputs are no longer read
+        stage_chunk<Tin, DK>(sm, p, dop, c0, eos, H, h, j0, false);
+        __syncthreads();
+        const int nt = (int)min((long long)kChunk, eos - c0);
+        for (int tt = 0; tt < nt; ++tt) step<DK, RPL>(S, sm, tt, row0, warp);
     }
 
     float dS[RPL];
 #pragma unroll
     for (int i = 0; i < RPL; ++i) dS[i] = d_fin ? d_fin[sbase + (size_t)(row0 + i) * DV + j] : 0.f;
-    __syncthreads();  // accumulators zeroed
 
-    const Tin *qp = static_cast<const Tin *>(p.q);
-    const Tin *dop = static_cast<const Tin *>(d_o);
     for (int c = nchunks - 1; c >= 0; --c) {
         const long long c0 = bos + (long long)c * kChunk;
+        __syncthreads();
+        stage_chunk<Tin, DK>(sm, p, dop, c0, eos, H, h, j0, true);
+        __syncthreads();
         // Replay the chunk from its checkpoint, keeping the state every kSub tokens.
         float sub[kChunk / kSub][RPL];
         {
@@ -134,78 +166,68 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(RunParams p, const v
 #pragma unroll
             for (int i = 0; i < RPL; ++i) S[i] = src[i];
         }
+        const int nt = (int)min((long long)kChunk, eos - c0);
 #pragma unroll
         for (int s = 0; s < kChunk / kSub; ++s) {
 #pragma unroll
             for (int i = 0; i < RPL; ++i) sub[s][i] = S[i];
-            const long long t1 = min(c0 + (long long)(s + 1) * kSub, eos);
-            for (long long t = c0 + (long long)s * kSub; t < t1; ++t) {
-                Tok<Tin, RPL> tk;
-                tk.load(p, (size_t)t * H + h, row0, j, DV);
-                step<Tin, RPL>(S, tk);
-            }
+            const int t1 = min((s + 1) * kSub, nt);
+            for (int tt = s * kSub; tt < t1; ++tt) step<DK, RPL>(S, sm, tt, row0, warp);
         }
 #pragma unroll
         for (int s = kChunk / kSub - 1; s >= 0; --s) {
-            const long long tb = c0 + (long long)s * kSub;
-            if (tb >= eos) continue;  // uniform over the CTA
-            const long long te = min(tb + kSub, eos);
-            for (long long t = te - 1; t >= tb; --t) {
-                // The state before token t, rebuilt from the register checkpoint.
+            const int tb = s * kSub;
+            if (tb >= nt) continue;  // uniform over the CTA
+            const int te = min(tb + kSub, nt);
+            for (int tt = te - 1; tt >= tb; --tt) {
+                // The state before token tt, rebuilt from the register checkpoint.
 #pragma unroll
                 for (int i = 0; i < RPL; ++i) S[i] = sub[s][i];
-                for (long long u = tb; u < t; ++u) {
-                    Tok<Tin, RPL> tk;
-                    tk.load(p, (size_t)u * H + h, row0, j, DV);
-                    step<Tin, RPL>(S, tk);
-                }
-                const size_t r = (size_t)t * H + h;
-                Tok<Tin, RPL> tk;
-                tk.load(p, r, row0, j, DV);
-                const float dov = ld(dop, r * DV + j);
-                float q[RPL], Sd[RPL], ks = 0.f;
+                for (int u = tb; u < tt; ++u) step<DK, RPL>(S, sm, u, row0, warp);
+                const float *k = sm + L::K + tt * DK + row0, *a = sm + L::A + tt * DK + row0;
+                const float *q = sm + L::Q + tt * DK + row0;
+                const float beta = sm[L::B + tt], dov = sm[L::DO + tt * kCols + warp];
+                float Sd[RPL], ks = 0.f;
 #pragma unroll
                 for (int i = 0; i < RPL; ++i) {
-                    q[i] = ld(qp, r * DK + row0 + i);
-                    Sd[i] = tk.a[i] * S[i];
-                    ks = fmaf(tk.k[i], Sd[i], ks);
+                    Sd[i] = a[i] * S[i];
+                    ks = fmaf(k[i], Sd[i], ks);
                 }
-                const float w = tk.v - warp_sum(ks), u = tk.beta * w;
+                const float w = sm[L::V + tt * kCols + warp] - warp_sum(ks), u = beta * w;
                 float kd = 0.f;
-                const int tt = (int)(t - tb);
+                const int t_ = tt - tb;
 #pragma unroll
                 for (int i = 0; i < RPL; ++i) {
-                    atomicAdd(&acc[tt][0][row0 + i], fmaf(tk.k[i], u, Sd[i]) * dov);  // dq: S' do
+                    atomicAdd(&acc[(t_ * 3 + 0) * DK + row0 + i], fmaf(k[i], u, Sd[i]) * dov);  // dq: S' do
                     dS[i] = fmaf(q[i], dov, dS[i]);
-                    kd = fmaf(tk.k[i], dS[i], kd);
+                    kd = fmaf(k[i], dS[i], kd);
                 }
-                const float du = warp_sum(kd), bdu = tk.beta * du;
+                const float du = warp_sum(kd), bdu = beta * du;
                 if (lane == 0) {
-                    dv[r * DV + j] = bdu;
-                    atomicAdd(&accb[tt], du * w);
+                    dv[((size_t)(c0 + tt) * H + h) * DV + j] = bdu;
+                    atomicAdd(&accb[t_], du * w);
                 }
 #pragma unroll
                 for (int i = 0; i < RPL; ++i) {
-                    atomicAdd(&acc[tt][1][row0 + i], dS[i] * u - Sd[i] * bdu);  // dk
-                    const float dsd = dS[i] - tk.k[i] * bdu;
-                    atomicAdd(&acc[tt][2][row0 + i], dsd * Sd[i]);               // dg
-                    dS[i] = tk.a[i] * dsd;
+                    atomicAdd(&acc[(t_ * 3 + 1) * DK + row0 + i], dS[i] * u - Sd[i] * bdu);  // dk
+                    const float dsd = dS[i] - k[i] * bdu;
+                    atomicAdd(&acc[(t_ * 3 + 2) * DK + row0 + i], dsd * Sd[i]);               // dg
+                    dS[i] = a[i] * dsd;
                 }
             }
             // This block of tokens is complete in shared memory: add it to the outputs.
             __syncthreads();
-            const int nt = (int)(te - tb);
+            const int nb = te - tb;
             for (int e = threadIdx.x; e < kSub * 3 * DK; e += kThreads) {
                 const int t_ = e / (3 * DK), which = (e / DK) % 3, i = e % DK;
-                float *a = &(&acc[0][0][0])[e];
-                if (t_ < nt) {
+                if (t_ < nb) {
                     float *out = which == 0 ? dq : (which == 1 ? dk : dg);
-                    atomicAdd(out + ((size_t)(tb + t_) * H + h) * DK + i, *a);
+                    atomicAdd(out + ((size_t)(c0 + tb + t_) * H + h) * DK + i, acc[e]);
                 }
-                *a = 0.f;
+                acc[e] = 0.f;
             }
             if (threadIdx.x < kSub) {
-                if ((int)threadIdx.x < nt) atomicAdd(dbeta + (size_t)(tb + threadIdx.x) * H + h, accb[threadIdx.x]);
+                if ((int)threadIdx.x < nb) atomicAdd(dbeta + (size_t)(c0 + tb + threadIdx.x) * H + h, accb[threadIdx.x]);
                 accb[threadIdx.x] = 0.f;
             }
             __syncthreads();
@@ -222,17 +244,26 @@ __global__ void zero_kernel(float *__restrict__ x, size_t n) {
         x[i] = 0.f;
 }
 
+template <typename Tin, int DK>
+cudaError_t launch_dk(const dim3 &grid, const RunParams &p, const void *d_o, const float *d_fin, float *dq,
+                      float *dk, float *dv, float *dg, float *dbeta, float *d_init, float *ck, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(backward_kernel<Tin, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Stage<DK>::BYTES);
+    if (e != cudaSuccess) return e;
+    backward_kernel<Tin, DK><<<grid, kThreads, Stage<DK>::BYTES, s>>>(p, d_o, d_fin, dq, dk, dv, dg, dbeta, d_init, ck);
+    return cudaGetLastError();
+}
+
 template <typename Tin>
 cudaError_t launch_typed(int d, const RunParams &p, const void *d_o, const float *d_fin, float *dq, float *dk,
                          float *dv, float *dg, float *dbeta, float *d_init, float *ck, cudaStream_t s) {
     const dim3 grid((unsigned)(p.n_seqs * p.H), (unsigned)(d / kCols));
     switch (d) {
-        case 32: backward_kernel<Tin, 32><<<grid, kThreads, 0, s>>>(p, d_o, d_fin, dq, dk, dv, dg, dbeta, d_init, ck); break;
-        case 64: backward_kernel<Tin, 64><<<grid, kThreads, 0, s>>>(p, d_o, d_fin, dq, dk, dv, dg, dbeta, d_init, ck); break;
-        case 128: backward_kernel<Tin, 128><<<grid, kThreads, 0, s>>>(p, d_o, d_fin, dq, dk, dv, dg, dbeta, d_init, ck); break;
+        case 32: return launch_dk<Tin, 32>(grid, p, d_o, d_fin, dq, dk, dv, dg, dbeta, d_init, ck, s);
+        case 64: return launch_dk<Tin, 64>(grid, p, d_o, d_fin, dq, dk, dv, dg, dbeta, d_init, ck, s);
+        case 128: return launch_dk<Tin, 128>(grid, p, d_o, d_fin, dq, dk, dv, dg, dbeta, d_init, ck, s);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace
