@@ -25,7 +25,7 @@
 namespace kda {
 namespace {
 
-constexpr int kCols = 8;    // value columns (warps) per CTA
+constexpr int kCols = 16;   // value columns (warps) per CTA
 constexpr int kChunk = 64;  // tokens between stored checkpoints
 constexpr int kSub = 8;     // tokens between register checkpoints
 constexpr int kThreads = kCols * 32;
@@ -39,73 +39,91 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-// Shared-memory layout of one staged chunk (kChunk tokens) for head size DK.
-template <int DK>
+// Shared-memory layout (bytes) of one staged chunk (kChunk tokens) for head size DK. k and q
+// keep the input type (bf16 rows are exact), the decays are stored as exp(g) in fp32.
+template <int DK, typename Tin>
 struct Stage {
-    static constexpr int K = 0;                              // fp32 [kChunk][DK]: k
-    static constexpr int A = K + kChunk * DK;                // fp32 [kChunk][DK]: exp(g)
-    static constexpr int Q = A + kChunk * DK;                // fp32 [kChunk][DK]: q
-    static constexpr int V = Q + kChunk * DK;                // fp32 [kChunk][kCols]: v of the CTA's columns
-    static constexpr int DO = V + kChunk * kCols;            // fp32 [kChunk][kCols]: dO of those columns
-    static constexpr int B = DO + kChunk * kCols;            // fp32 [kChunk]: beta
-    static constexpr int ACC = B + kChunk;                   // fp32 [kSub][3][DK]: dq, dk, dg sums
-    static constexpr int ACCB = ACC + kSub * 3 * DK;         // fp32 [kSub]: dbeta sums
-    static constexpr int FLOATS = ACCB + kSub;
-    static constexpr size_t BYTES = FLOATS * sizeof(float);
+    static constexpr size_t A = 0;                                  // fp32 [kChunk][DK]: exp(g)
+    static constexpr size_t V = A + kChunk * DK * 4;                // fp32 [kChunk][kCols]: v of the CTA's columns
+    static constexpr size_t DO = V + kChunk * kCols * 4;            // fp32 [kChunk][kCols]: dO of those columns
+    static constexpr size_t B = DO + kChunk * kCols * 4;            // fp32 [kChunk]: beta
+    static constexpr size_t ACC = B + kChunk * 4;                   // fp32 [kSub][3][DK]: dq, dk, dg sums
+    static constexpr size_t ACCB = ACC + kSub * 3 * DK * 4;         // fp32 [kSub]: dbeta sums
+    static constexpr size_t K = ACCB + kSub * 4;                    // Tin [kChunk][DK]: k
+    static constexpr size_t Q = K + kChunk * DK * sizeof(Tin);      // Tin [kChunk][DK]: q
+    static constexpr size_t BYTES = Q + kChunk * DK * sizeof(Tin);
+    static_assert(K % 16 == 0 && Q % 16 == 0, "row alignment");
+    __device__ static float *f(uint8_t *sm, size_t off) { return reinterpret_cast<float *>(sm + off); }
+    __device__ static Tin *t(uint8_t *sm, size_t off) { return reinterpret_cast<Tin *>(sm + off); }
 };
+
+// RPL consecutive elements of a staged row, widened to fp32.
+template <int RPL>
+__device__ __forceinline__ void row_load(const float *p, float (&x)[RPL]) {
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) x[i] = p[i];
+}
+template <int RPL>
+__device__ __forceinline__ void row_load(const __nv_bfloat16 *p, float (&x)[RPL]) {
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) x[i] = __bfloat162float(p[i]);
+}
 
 // Stage the inputs of tokens [c0, c0 + kChunk) (rows past eos read as identity tokens: k = 0,
 // exp g = 1). With `rev` also q and dO, which only the reverse sweep reads.
 template <typename Tin, int DK>
-__device__ __forceinline__ void stage_chunk(float *sm, const RunParams &p, const Tin *dop, long long c0,
+__device__ __forceinline__ void stage_chunk(uint8_t *sm, const RunParams &p, const Tin *dop, long long c0,
                                             long long eos, int H, int h, int j0, bool rev) {
-    using L = Stage<DK>;
+    using L = Stage<DK, Tin>;
     const Tin *kp = static_cast<const Tin *>(p.k), *gp = static_cast<const Tin *>(p.g);
     const Tin *qp = static_cast<const Tin *>(p.q), *vp = static_cast<const Tin *>(p.v);
     const Tin *bp = static_cast<const Tin *>(p.beta);
+    const Tin zero = Tin(0.f);
     for (int e = threadIdx.x; e < kChunk * DK; e += kThreads) {
         const int t = e / DK, i = e % DK;
         const bool live = c0 + t < eos;
         const size_t r = ((size_t)(c0 + t) * H + h) * DK + i;
-        sm[L::K + e] = live ? ld(kp, r) : 0.f;
-        sm[L::A + e] = live ? expf(ld(gp, r)) : 1.f;
-        if (rev) sm[L::Q + e] = live ? ld(qp, r) : 0.f;
+        L::t(sm, L::K)[e] = live ? kp[r] : zero;
+        L::f(sm, L::A)[e] = live ? expf(ld(gp, r)) : 1.f;
+        if (rev) L::t(sm, L::Q)[e] = live ? qp[r] : zero;
     }
     for (int e = threadIdx.x; e < kChunk * kCols; e += kThreads) {
         const int t = e / kCols, c = e % kCols;
         const bool live = c0 + t < eos;
         const size_t r = ((size_t)(c0 + t) * H + h) * DK + j0 + c;
-        sm[L::V + e] = live ? ld(vp, r) : 0.f;
-        if (rev) sm[L::DO + e] = live ? ld(dop, r) : 0.f;
+        L::f(sm, L::V)[e] = live ? ld(vp, r) : 0.f;
+        if (rev) L::f(sm, L::DO)[e] = live ? ld(dop, r) : 0.f;
     }
     for (int t = threadIdx.x; t < kChunk; t += kThreads)
-        sm[L::B + t] = c0 + t < eos ? ld(bp, (size_t)(c0 + t) * H + h) : 0.f;
+        L::f(sm, L::B)[t] = c0 + t < eos ? ld(bp, (size_t)(c0 + t) * H + h) : 0.f;
 }
 
 // One forward token (index tt of the staged chunk) on the lane's rows of column `col`.
-template <int DK, int RPL>
-__device__ __forceinline__ void step(float (&S)[RPL], const float *sm, int tt, int row0, int col) {
-    using L = Stage<DK>;
-    const float *k = sm + L::K + tt * DK + row0, *a = sm + L::A + tt * DK + row0;
+template <typename Tin, int DK, int RPL>
+__device__ __forceinline__ void step(float (&S)[RPL], uint8_t *sm, int tt, int row0, int col) {
+    using L = Stage<DK, Tin>;
+    float k[RPL];
+    row_load<RPL>(L::t(sm, L::K) + tt * DK + row0, k);
+    const float *a = L::f(sm, L::A) + tt * DK + row0;
     float ks = 0.f;
 #pragma unroll
     for (int i = 0; i < RPL; ++i) {
         S[i] *= a[i];
         ks = fmaf(k[i], S[i], ks);
     }
-    const float u = sm[L::B + tt] * (sm[L::V + tt * kCols + col] - warp_sum(ks));
+    const float u = L::f(sm, L::B)[tt] * (L::f(sm, L::V)[tt * kCols + col] - warp_sum(ks));
 #pragma unroll
     for (int i = 0; i < RPL; ++i) S[i] = fmaf(k[i], u, S[i]);
 }
 
 template <typename Tin, int DK>
-__global__ void __launch_bounds__(kThreads) backward_kernel(RunParams p, const void *d_o, const float *d_fin,
+__global__ void __launch_bounds__(kThreads, 2) backward_kernel(RunParams p, const void *d_o, const float *d_fin,
                                                           float *dq, float *dk, float *dv, float *dg,
                                                           float *dbeta, float *d_init, float *ck) {
     constexpr int DV = DK, RPL = DK / 32;
-    using L = Stage<DK>;
-    extern __shared__ float sm[];
-    float *acc = sm + L::ACC, *accb = sm + L::ACCB;
+    using L = Stage<DK, Tin>;
+    extern __shared__ __align__(16) uint8_t sm[];
+    float *acc = L::f(sm, L::ACC), *accb = L::f(sm, L::ACCB);
     const int H = p.H, h = blockIdx.x % H, n = blockIdx.x / H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j0 = blockIdx.y * kCols, j = j0 + warp;  // this warp's value column
@@ -147,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(RunParams p, const v
         stage_chunk<Tin, DK>(sm, p, dop, c0, eos, H, h, j0, false);
         __syncthreads();
         const int nt = (int)min((long long)kChunk, eos - c0);
-        for (int tt = 0; tt < nt; ++tt) step<DK, RPL>(S, sm, tt, row0, warp);
+        for (int tt = 0; tt < nt; ++tt) step<Tin, DK, RPL>(S, sm, tt, row0, warp);
     }
 
     float dS[RPL];
@@ -172,7 +190,7 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(RunParams p, const v
 #pragma unroll
             for (int i = 0; i < RPL; ++i) sub[s][i] = S[i];
             const int t1 = min((s + 1) * kSub, nt);
-            for (int tt = s * kSub; tt < t1; ++tt) step<DK, RPL>(S, sm, tt, row0, warp);
+            for (int tt = s * kSub; tt < t1; ++tt) step<Tin, DK, RPL>(S, sm, tt, row0, warp);
         }
 #pragma unroll
         for (int s = kChunk / kSub - 1; s >= 0; --s) {
@@ -183,17 +201,19 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(RunParams p, const v
                 // The state before token tt, rebuilt from the register checkpoint.
 #pragma unroll
                 for (int i = 0; i < RPL; ++i) S[i] = sub[s][i];
-                for (int u = tb; u < tt; ++u) step<DK, RPL>(S, sm, u, row0, warp);
-                const float *k = sm + L::K + tt * DK + row0, *a = sm + L::A + tt * DK + row0;
-                const float *q = sm + L::Q + tt * DK + row0;
-                const float beta = sm[L::B + tt], dov = sm[L::DO + tt * kCols + warp];
+                for (int u = tb; u < tt; ++u) step<Tin, DK, RPL>(S, sm, u, row0, warp);
+                float k[RPL], q[RPL];
+                row_load<RPL>(L::t(sm, L::K) + tt * DK + row0, k);
+                row_load<RPL>(L::t(sm, L::Q) + tt * DK + row0, q);
+                const float *a = L::f(sm, L::A) + tt * DK + row0;
+                const float beta = L::f(sm, L::B)[tt], dov = L::f(sm, L::DO)[tt * kCols + warp];
                 float Sd[RPL], ks = 0.f;
 #pragma unroll
                 for (int i = 0; i < RPL; ++i) {
                     Sd[i] = a[i] * S[i];
                     ks = fmaf(k[i], Sd[i], ks);
                 }
-                const float w = sm[L::V + tt * kCols + warp] - warp_sum(ks), u = beta * w;
+                const float w = L::f(sm, L::V)[tt * kCols + warp] - warp_sum(ks), u = beta * w;
                 float kd = 0.f;
                 const int t_ = tt - tb;
 #pragma unroll
@@ -248,9 +268,9 @@ template <typename Tin, int DK>
 cudaError_t launch_dk(const dim3 &grid, const RunParams &p, const void *d_o, const float *d_fin, float *dq,
                       float *dk, float *dv, float *dg, float *dbeta, float *d_init, float *ck, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(backward_kernel<Tin, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Stage<DK>::BYTES);
+                                         (int)Stage<DK, Tin>::BYTES);
     if (e != cudaSuccess) return e;
-    backward_kernel<Tin, DK><<<grid, kThreads, Stage<DK>::BYTES, s>>>(p, d_o, d_fin, dq, dk, dv, dg, dbeta, d_init, ck);
+    backward_kernel<Tin, DK><<<grid, kThreads, Stage<DK, Tin>::BYTES, s>>>(p, d_o, d_fin, dq, dk, dv, dg, dbeta, d_init, ck);
     return cudaGetLastError();
 }
 

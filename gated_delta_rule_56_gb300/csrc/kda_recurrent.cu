@@ -54,7 +54,9 @@ __device__ __forceinline__ void store_state(float *p, const float (&x)[CPL]) {
     }
 }
 
-template <typename Tin, int DK, int DV>
+// EXT: the instance that also serves q/k L2 normalisation and the output gate; the plain
+// instance carries neither (the decode step runs at the register limit).
+template <typename Tin, int DK, int DV, bool EXT>
 __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
     static_assert(DK % kWarps == 0 && DV % 32 == 0 && DK + DV <= kThreads, "head size");
     constexpr int RPW = DK / kWarps;  // key rows per warp
@@ -89,9 +91,9 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
     __shared__ float red_k[2][kWarps][DV], red_q[2][kWarps][DV], red_qk[2][3][kWarps];
 
     const int row0 = w * RPW, col0 = l * CPL;
+    const bool norm = EXT && p.qk_l2norm;
     static_assert(DK == DV, "square states");
     const long long init_off = p.init ? state_slot_offset(p.init_idx, p.pool, n, H, h, DK, p.err) : -1;
-    const long long fin_off = p.fin ? state_slot_offset(p.fin_idx, p.pool, n, H, h, DK, p.err) : -1;
     float s[RPW][CPL];
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
@@ -126,8 +128,10 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
         for (int r = 0; r < RPW; ++r) {
             const float a = sa[buf][row0 + r], kk = sk[buf][row0 + r], qq = sq[buf][row0 + r];
             pqk = fmaf(kk, qq, pqk);
-            pkk = fmaf(kk, kk, pkk);
-            pqq = fmaf(qq, qq, pqq);
+            if (norm) {
+                pkk = fmaf(kk, kk, pkk);
+                pqq = fmaf(qq, qq, pqq);
+            }
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
                 s[r][c] *= a;
@@ -142,23 +146,30 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
         }
         if (l == 0) {
             red_qk[buf][0][w] = pqk;
-            red_qk[buf][1][w] = pkk;
-            red_qk[buf][2][w] = pqq;
+            if (norm) {
+                red_qk[buf][1][w] = pkk;
+                red_qk[buf][2][w] = pqq;
+            }
         }
         __syncthreads();
 
-        float qk = 0.f, kk2 = 0.f, qq2 = 0.f;
+        float qk = 0.f;
 #pragma unroll
-        for (int i = 0; i < kWarps; ++i) {
-            qk += red_qk[buf][0][i];
-            kk2 += red_qk[buf][1][i];
-            qq2 += red_qk[buf][2][i];
-        }
+        for (int i = 0; i < kWarps; ++i) qk += red_qk[buf][0][i];
         // L2-normalised q and k are q / |q|, k / |k|: every use of k and q is linear in it, so
         // the norms scale the reductions and the write instead of the inputs.
-        const float nk = p.qk_l2norm ? rsqrtf(kk2 + 1e-6f) : 1.f;
-        const float nq = p.qk_l2norm ? rsqrtf(qq2 + 1e-6f) : 1.f;
-        qk *= nk * nq;
+        float nk = 1.f, nq = 1.f;
+        if (norm) {
+            float kk2 = 0.f, qq2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < kWarps; ++i) {
+                kk2 += red_qk[buf][1][i];
+                qq2 += red_qk[buf][2][i];
+            }
+            nk = rsqrtf(kk2 + 1e-6f);
+            nq = rsqrtf(qq2 + 1e-6f);
+            qk *= nk * nq;
+        }
         const float b = sb[buf];
         float u[CPL], oo[CPL];
 #pragma unroll
@@ -179,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
             for (int c = 0; c < CPL; ++c) s[r][c] = fmaf(kk, u[c], s[r][c]);
         }
         if (w == 0) {
-            const Tin *z = static_cast<const Tin *>(p.out_gate);
+            const Tin *z = EXT ? static_cast<const Tin *>(p.out_gate) : nullptr;
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
                 float ov = oo[c];
@@ -189,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
         }
     }
 
+    const long long fin_off = p.fin ? state_slot_offset(p.fin_idx, p.pool, n, H, h, DK, p.err) : -1;
     if (fin_off >= 0) {
 #pragma unroll
         for (int r = 0; r < RPW; ++r)
@@ -199,10 +211,14 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(RunParams p) {
 template <typename Tin>
 cudaError_t launch_typed(int d, const RunParams &p, cudaStream_t s) {
     const dim3 grid((unsigned)(p.n_seqs * p.H)), block(kThreads);
-    switch (d) {
-        case 32: recurrent_kernel<Tin, 32, 32><<<grid, block, 0, s>>>(p); break;
-        case 64: recurrent_kernel<Tin, 64, 64><<<grid, block, 0, s>>>(p); break;
-        case 128: recurrent_kernel<Tin, 128, 128><<<grid, block, 0, s>>>(p); break;
+    const bool ext = p.qk_l2norm || p.out_gate;
+    switch (d * 2 + (ext ? 1 : 0)) {
+        case 64: recurrent_kernel<Tin, 32, 32, false><<<grid, block, 0, s>>>(p); break;
+        case 65: recurrent_kernel<Tin, 32, 32, true><<<grid, block, 0, s>>>(p); break;
+        case 128: recurrent_kernel<Tin, 64, 64, false><<<grid, block, 0, s>>>(p); break;
+        case 129: recurrent_kernel<Tin, 64, 64, true><<<grid, block, 0, s>>>(p); break;
+        case 256: recurrent_kernel<Tin, 128, 128, false><<<grid, block, 0, s>>>(p); break;
+        case 257: recurrent_kernel<Tin, 128, 128, true><<<grid, block, 0, s>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
