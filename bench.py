@@ -66,7 +66,7 @@ def parse():
                          "l2norm = the headline shape with raw q/k rows L2-normalised in the kernel; "
                          "outgate = the headline shape with the output gate o * sigmoid(z) in the kernel; "
                          "backward = all gradients of the headline shape (kda_backward)")
-    ap.add_argument("--ncu-case", choices=("prefill", "decode"),
+    ap.add_argument("--ncu-case", choices=("prefill", "decode", "backward"),
                     help="run two launches of the small profiling case (for ncu) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -532,7 +532,8 @@ def run_workload(args):
 
 def ncu_case(kind):
     """Small cases sized for an ncu capture: inputs larger than L2, a few hundred MB on the
-    device. prefill: B=4 T=2048 H=32 d=128 (128 CTAs); decode: N=64 H=32 d=128 (2048 CTAs)."""
+    device. prefill: B=4 T=2048 H=32 d=128 (128 CTAs); decode: N=64 H=32 d=128 (2048 CTAs);
+    backward: B=2 T=1024 H=32 d=128 (512 CTAs)."""
     import gated_delta_rule_56_gb300 as kda
     import kda_inputs as ki
     from gated_delta_rule_56_gb300.build import build
@@ -542,6 +543,11 @@ def ncu_case(kind):
         x = ki.prefill_inputs(4, 2048, 32, 128, 128, device=dev, seed=0)
         for _ in range(2):
             o, _s = kda.prefill(*(x[n] for n in NAMES))
+    elif kind == "backward":
+        x = ki.prefill_inputs(2, 1024, 32, 128, 128, device=dev, seed=0)
+        do = ki.gate_logits_like(x["v"], seed=4)
+        for _ in range(2):
+            o = kda.backward(*(x[n] for n in NAMES), do)["dq"]
     else:
         x = ki.decode_inputs(2, 64, 32, 128, 128, device=dev, seed=0)
         st = x["state"].clone()

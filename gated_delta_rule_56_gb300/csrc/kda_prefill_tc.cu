@@ -535,12 +535,11 @@ struct Maps {
 // kOutGate: O is multiplied by sigmoid(p.out_gate) before it is stored.
 enum : int { kGated = 1, kNorm = 2, kOutGate = 4 };
 
-// The gate rows (this head) of one chunk's O tile, read while the tile is staged: a thread takes
-// 8 of its 1024 16-byte chunks (row e / 16, channels 8 (e % 16) ..), scales the staged bf16 O by
-// sigmoid(z) in fp32 and writes it back in place. Rows at or past `ln` are left alone (they are
-// past the tensor end and are not stored).
-__device__ __forceinline__ void gate_staged_o(uint8_t *sm, const __nv_bfloat16 *zg, long long r0, int ln, int H,
-                                              int h, int v) {
+// The gate rows z (this head) of one chunk into the O staging tile, in the tile's own layout: a
+// thread copies 8 of the 1024 16-byte chunks (row e / 16, channels 8 (e % 16) ..). Rows at or past
+// `ln` (past the tensor end, never stored) get zeros.
+__device__ __forceinline__ void stage_gate_rows(uint8_t *sm, const __nv_bfloat16 *zg, long long r0, int ln, int H,
+                                                int h, int v) {
     uint4 z[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -551,17 +550,7 @@ __device__ __forceinline__ void gate_staged_o(uint8_t *sm, const __nv_bfloat16 *
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int e = v + 128 * i, row = e >> 4, cj = e & 15;
-        uint4 *po = reinterpret_cast<uint4 *>(sm + SM_T + (cj >> 3) * 8192 + row * 128 + (((cj & 7) ^ (row & 7)) << 4));
-        const uint4 ov = *po;
-        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, zw[4] = {z[i].x, z[i].y, z[i].z, z[i].w};
-        uint32_t rw[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float s0 = __fdividef(1.f, 1.f + ex2(-bf_lo(zw[q]) * kLog2e));
-            const float s1 = __fdividef(1.f, 1.f + ex2(-bf_hi(zw[q]) * kLog2e));
-            rw[q] = pack_bf16(bf_lo(ow[q]) * s0, bf_hi(ow[q]) * s1);
-        }
-        *po = make_uint4(rw[0], rw[1], rw[2], rw[3]);
+        *reinterpret_cast<uint4 *>(sm + SM_T + (cj >> 3) * 8192 + row * 128 + (((cj & 7) ^ (row & 7)) << 4)) = z[i];
     }
 }
 
@@ -823,17 +812,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ost[b] = (uint32_t)((v >> 6) * 8192 + b * 128 + ((((v >> 3) & 7) ^ b) << 4) + (v & 7) * 2);
         auto write_o = [&](const float (&o0)[32], const float (&o1)[32], long long r0, int ln) {
             if (ln == C || r0 + ln >= total_rows) {  // rows past the tensor end are not written
-#pragma unroll
-                for (int r = 0; r < 32; ++r)
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + SM_T + ost[r & 7] + (r & ~7) * 128) = __float2bfloat16_rn(o0[r]);
-#pragma unroll
-                for (int r = 0; r < 32; ++r)
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + SM_T + ost[r & 7] + (32 + (r & ~7)) * 128) =
-                        __float2bfloat16_rn(o1[r]);
                 if (OGATE) {
-                    state_sync();  // the whole tile is staged
-                    gate_staged_o(sm, zg, r0, (int)min((long long)C, total_rows - r0), H, h, v);
+                    // z into the tile first; each thread then scales its fp32 O by sigmoid(z) read
+                    // from the element it overwrites, so O is rounded to bf16 once.
+                    stage_gate_rows(sm, zg, r0, (int)min((long long)C, total_rows - r0), H, h, v);
+                    state_sync();
                 }
+                // 8 rows at a time: the 8 gate values are read before any of the 8 stores.
+                auto put8 = [&](const float (&o)[32], int r8, int base) {
+                    float sg[8];
+#pragma unroll
+                    for (int b = 0; b < 8; ++b)
+                        sg[b] = OGATE ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                            sm + SM_T + ost[b] + (base + r8) * 128))
+                                      : 0.f;
+#pragma unroll
+                    for (int b = 0; b < 8; ++b) {
+                        float x = o[r8 + b];
+                        if (OGATE) x *= __fdividef(1.f, 1.f + ex2(-sg[b] * kLog2e));
+                        *reinterpret_cast<__nv_bfloat16 *>(sm + SM_T + ost[b] + (base + r8) * 128) =
+                            __float2bfloat16_rn(x);
+                    }
+                };
+#pragma unroll
+                for (int r8 = 0; r8 < 32; r8 += 8) put8(o0, r8, 0);
+#pragma unroll
+                for (int r8 = 0; r8 < 32; r8 += 8) put8(o1, r8, 32);
                 fence_async_smem();
                 state_sync();
                 if (v == 0) {

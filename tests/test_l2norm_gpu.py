@@ -26,15 +26,16 @@ def _raw(x, seed):
     return x
 
 
-def _unit(t, rounded=True):
-    """The oracle's normalisation of the raw rows, rounded to the input dtype by default: the
-    kernels feed their products with normalised rows at that precision (bf16 operands), the
-    same rounding a caller's own pre-normalised bf16 rows carry into the plain call."""
+def _unit(t, rounded=False):
+    """The oracle's fp64 normalisation of the raw rows; with `rounded`, rounded to the input
+    dtype, the precision at which the kernels feed their products with the rows (bf16 operands).
+    A single token's output is the cancelling sum (q.k) u, whose relative error that operand
+    rounding dominates; there the reference carries the same rounding."""
     y = oracle.l2_normalize(t.cpu())
     return torch.from_numpy(y).to(t.dtype) if rounded else y
 
 
-def _ref(x, g=None, rounded=True):
+def _ref(x, g=None, rounded=False):
     cu = x.get("cu_seqlens")
     init = x.get("initial_state")
     return oracle.recurrent(_unit(x["q"], rounded), _unit(x["k"], rounded), x["v"].cpu(),
@@ -48,13 +49,9 @@ def test_l2norm_prefill_tensor_core_path(B, T, H):
     x = _raw(ki.prefill_inputs(B, T, H, 128, 128, device=DEV, seed=71, state_std=0.02), seed=72)
     o, s = kda.prefill(*(x[n] for n in NAMES), initial_state=x["initial_state"], qk_l2norm=True)
     kda.check_status()
-    ro, rs = _ref(x)
+    ro, rs = _ref(x, rounded=T == 1)  # one token: its output is a cancelling sum, see _unit
     assert_close(o, ro, "o")
     assert_close(s, rs, "final_state")
-    if T > 1:  # away from the single-token case the unrounded normalisation is within the bar too
-        ro, rs = _ref(x, rounded=False)
-        assert_close(o, ro, "o")
-        assert_close(s, rs, "final_state")
 
 
 def test_l2norm_prefill_varlen():

@@ -202,3 +202,14 @@ def test_long_context_sampled_heads():
         log_bound = x["g"][0, T - M:, h].float().max(dim=-1).values.sum().item() + math.log(max(bv, 1e-30))
         assert log_bound < math.log(1e-12), log_bound
         assert_close(s[0, h], rs[0, 0], f"final_state (h={h})")
+        # Outputs across the places where a split call joins segments (T/4, T/2, 3T/4 for 4 or 2
+        # segments): the oracle from a zero state M tokens earlier, with the same bound on what
+        # the earlier tokens can add (|o_t| moves by at most that bound times |q_t|).
+        for R in (T // 4, T // 2, 3 * T // 4):
+            a, b = R - 64, R + 512
+            win = pair(x, 0, h, rows=(a - M, b))
+            ro, _ = oracle.recurrent(*win.values())
+            bv = (x["beta"][0, :a - M, h].float() * x["v"][0, :a - M, h].float().norm(dim=-1)).sum().item()
+            log_bound = x["g"][0, a - M:a, h].float().max(dim=-1).values.sum().item() + math.log(max(bv, 1e-30))
+            assert log_bound < math.log(1e-12), log_bound
+            assert_close(o[0, a:b, h], ro[0, M:, 0], f"o[{a}:{b}] (h={h})")
