@@ -53,6 +53,12 @@
 //   16->32 and 32->64 block merges as tf32 warp-level MMAs.
 // Every mbarrier wait is bounded; on time-out the CTA records kErrTimeout, drains what it
 // issued (again bounded), frees its TMEM and exits.
+//
+// Instances (template flags, chosen at launch): gate logits (g = -bound * sigmoid(x) formed as
+// g is read), q/k L2 normalisation (row sums of squares before the operands are built) and the
+// output gate (O scaled by sigmoid(z) as it is staged). The same kernel also runs the passes of
+// the split long-sequence prefill (kda_segmented.cu): v taken as zero, the identity as the start
+// state, a cap on the chunks run, and a per-(sequence, head) skip list.
 #include <cudaTypedefs.h>
 
 #include <mutex>

@@ -19,8 +19,8 @@
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream).
  *    Argument errors are found on the host and returned before anything is launched.
  *    A launch failure returns KDA_ERR_CUDA. Conditions only the device can see (a
- *    cu_seqlens array that is not monotonic, a pipeline wait that ran out) are recorded in a
- *    per-device error word that kda_check_status() returns.
+ *    cu_seqlens array that is not monotonic, a state slot past the pool end, a pipeline wait
+ *    that ran out) are recorded in a per-device error word that kda_check_status() returns.
  *  - Layouts are row-major and dense: q, k, g [B, T, H, d_k]; v, o [B, T, H, d_v];
  *    beta [B, T, H]; states [N, H, d_k, d_v] (fp32, row index = key channel).
  *  - Accuracy is stated for g in [-5, 0] (the scaled-sigmoid bound with constant 5): inputs
@@ -48,7 +48,7 @@ typedef struct CUstream_st *kda_stream_t; /* same type as cudaStream_t */
 
 typedef enum {
     KDA_OK = 0,
-    KDA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, bad cu_seqlens */
+    KDA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, bad cu_seqlens or slot */
     KDA_ERR_UNSUPPORTED = 2, /* well-formed request this build has no kernel for */
     KDA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
     KDA_ERR_TIMEOUT = 4      /* a device-side pipeline wait gave up (kda_check_status) */
@@ -232,9 +232,9 @@ KDA_API kda_status kda_decode_step_gated(kda_dtype dtype, int N, int H, int dk, 
 
 /*
  * kda_check_status -- synchronise `stream`, then read and clear the device error word of the
- * current device. Returns KDA_OK, KDA_ERR_INVALID_ARG (bad cu_seqlens seen by a kernel),
- * KDA_ERR_TIMEOUT (a bounded pipeline wait gave up; that (sequence, head) is left
- * unfinished) or KDA_ERR_CUDA (the synchronisation itself failed).
+ * current device. Returns KDA_OK, KDA_ERR_INVALID_ARG (bad cu_seqlens or a state slot past
+ * the pool end seen by a kernel), KDA_ERR_TIMEOUT (a bounded pipeline wait gave up; that
+ * (sequence, head) is left unfinished) or KDA_ERR_CUDA (the synchronisation itself failed).
  */
 KDA_API kda_status kda_check_status(kda_stream_t stream);
 
