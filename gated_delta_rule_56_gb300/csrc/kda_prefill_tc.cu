@@ -106,8 +106,8 @@ constexpr uint32_t SM_GC = SM_CST + 4096;                 // fp32 [3][128] gam_l
 constexpr uint32_t SM_BETA = SM_GC + 1536;                // fp32 [2][64] beta, by chunk parity
 constexpr uint32_t SM_BAR = SM_BETA + 512;                // mbarriers
 constexpr uint32_t SM_TPTR = SM_BAR + 256;                // TMEM base address
-constexpr uint32_t SM_NRM = SM_TPTR + 16;                 // fp32 [2 halves][k, q][64]: sums of squares
-constexpr uint32_t SM_USED = SM_NRM + 1024;
+constexpr uint32_t SM_NRM = SM_TPTR + 16;                 // fp32 [3 chunks][k, q][64]: row sums of squares
+constexpr uint32_t SM_USED = SM_NRM + 1536;
 constexpr uint32_t SMEM_BYTES = SM_USED + 1024;           // + alignment slack
 static_assert(SM_X + 64 * SA * 4 <= SM_OFF, "solve buffers overflow their region");
 static_assert(SM_Y + 4352 + 32 * SA * 4 <= SM_VT, "solve scratch overflows its region");
@@ -261,21 +261,34 @@ __device__ __forceinline__ void state_sync() { group_sync<2, NS>(); }
 //   rows 32..63: f = exp(Gam_r - Gam_47); off-tile row factor    f*c1  = exp(Gam_r - Gam_31)
 // Every other operand is one of K f, Q f, K / f times a per-channel factor <= 1, so each
 // product stays in range. Rows past the sequence end (r >= len) act as identity tokens.
-// Sums of squares of this thread's 4 rows r0..r0+3 of k and q over all 128 channels, for the
-// L2 norms. Each thread sums the squares of its 8 channels; the 8 lanes of a row group reduce
-// the 8 sums by halving exchanges (lane i ends with sum i: k rows 0..3, then q rows 0..3) and
-// store them, one channel half per warp, in shared memory; after the barrier of the two warps
-// that share the rows (w and w + 4) each thread adds the halves (row_inv_norm). Rows past the
-// sequence end count as zero.
-__device__ __forceinline__ void row_square_sums(uint8_t *sm, int r0, int j, int len) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Row sums of squares of k and q for the L2 normalisation, one buffer per chunk index mod 3:
+// step 1 of chunk c adds into buffer c % 3 (and zeroes buffer (c + 1) % 3, last read by the
+// operands of chunk c - 2); the operands of chunk c read it after step 1's closing barrier.
+// The thread's 4 rows x 8 channels of q and k come from global memory (the same lines the TMA
+// fetches for the operands later). Each thread sums its 8 channels per row; the 8 lanes of a row
+// group reduce the 8 sums (4 k rows, 4 q rows) by halving exchanges, lane i ending with sum i,
+// and add it to the row's entry, which the warp holding the other channel half adds to as well.
+struct QKRows {
+    uint4 k[4], q[4];
+};
+
+__device__ __forceinline__ void load_qk_rows(QKRows &x, const __nv_bfloat16 *qg, const __nv_bfloat16 *kg,
+                                             long long row0, int ln, int H, int h, int r0, int j) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const bool live = r0 + m < ln;
+        const size_t e = ((size_t)(row0 + r0 + m) * H + h) * D + 8 * j;
+        x.k[m] = live ? __ldg(reinterpret_cast<const uint4 *>(kg + e)) : make_uint4(0u, 0u, 0u, 0u);
+        x.q[m] = live ? __ldg(reinterpret_cast<const uint4 *>(qg + e)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+__device__ __forceinline__ void add_row_square_sums(float *nrm, const QKRows &x, int r0, int lane) {
     float v[8];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        const bool live = r0 + m < len;
-        const uint4 kw = *reinterpret_cast<const uint4 *>(sm + SM_K + tile_chunk(r0 + m, j));
-        const uint4 qw = *reinterpret_cast<const uint4 *>(sm + SM_Q + tile_chunk(r0 + m, j));
-        const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w}, qq[4] = {qw.x, qw.y, qw.z, qw.w};
+        const uint32_t kk[4] = {x.k[m].x, x.k[m].y, x.k[m].z, x.k[m].w};
+        const uint32_t qq[4] = {x.q[m].x, x.q[m].y, x.q[m].z, x.q[m].w};
         float sk = 0.f, sq = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -284,8 +297,8 @@ __device__ __forceinline__ void row_square_sums(uint8_t *sm, int r0, int j, int 
             sk = fmaf(kv, kv, sk);
             sq = fmaf(qv, qv, sq);
         }
-        v[m] = live ? sk : 0.f;
-        v[4 + m] = live ? sq : 0.f;
+        v[m] = sk;
+        v[4 + m] = sq;
     }
     const int i = lane & 7;
     float w4[4], w2[2];
@@ -301,26 +314,17 @@ __device__ __forceinline__ void row_square_sums(uint8_t *sm, int r0, int j, int 
     }
     const bool hi = (i & 1) != 0;
     const float tot = (hi ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, hi ? w2[0] : w2[1], 1);
-    float *nrm = reinterpret_cast<float *>(sm + SM_NRM);
-    nrm[((warp >> 2) * 2 + (i >> 2)) * 64 + r0 + (i & 3)] = tot;
-    switch (warp & 3) {  // constant barrier IDs 3..6, one per pair of warps
-        case 0: group_sync<3, 64>(); break;
-        case 1: group_sync<4, 64>(); break;
-        case 2: group_sync<5, 64>(); break;
-        default: group_sync<6, 64>(); break;
-    }
+    atomicAdd(nrm + (i >> 2) * 64 + r0 + (i & 3), tot);
 }
 
-// 1 / sqrt(sum x^2 + 1e-6) of row r of k (kq = 0) or q (kq = 1), after row_square_sums.
-__device__ __forceinline__ float row_inv_norm(const uint8_t *sm, int kq, int r) {
-    const float *nrm = reinterpret_cast<const float *>(sm + SM_NRM);
-    return rsqrtf(nrm[kq * 64 + r] + nrm[(2 + kq) * 64 + r] + 1e-6f);
+// 1 / sqrt(sum x^2 + 1e-6) of row r of k (kq = 0) or q (kq = 1) from a completed buffer.
+__device__ __forceinline__ float row_inv_norm(const float *nrm, int kq, int r) {
+    return rsqrtf(nrm[kq * 64 + r] + 1e-6f);
 }
 
 template <int MH, bool NORM>
 __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4][8], const float *cst, int r0,
-                                               int j, int len, uint32_t khb) {
-    if (NORM) row_square_sums(sm, r0, j, len);
+                                               int j, int len, uint32_t khb, const float *nrm) {
     float ref[8], fo_c[8], pe[8], khe[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -338,7 +342,7 @@ __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4]
         const uint4 qw = *reinterpret_cast<const uint4 *>(sm + SM_Q + tile_chunk(r, j));
         const uint32_t kk[4] = {live ? kw.x : 0u, live ? kw.y : 0u, live ? kw.z : 0u, live ? kw.w : 0u};
         const uint32_t qq[4] = {live ? qw.x : 0u, live ? qw.y : 0u, live ? qw.z : 0u, live ? qw.w : 0u};
-        const float nk = NORM ? row_inv_norm(sm, 0, r) : 1.f, nq = NORM ? row_inv_norm(sm, 1, r) : 1.f;
+        const float nk = NORM ? row_inv_norm(nrm, 0, r) : 1.f, nq = NORM ? row_inv_norm(nrm, 1, r) : 1.f;
         float apk[8], apq[8], apb[8], ofr_k[8], ofr_q[8], kp[8], qp[8], kh[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -571,6 +575,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float *cst = reinterpret_cast<float *>(sm + SM_CST);
     float *gcs = reinterpret_cast<float *>(sm + SM_GC);
     float *sbeta = reinterpret_cast<float *>(sm + SM_BETA);
+    float *nrmb = reinterpret_cast<float *>(sm + SM_NRM);
     float *As = reinterpret_cast<float *>(sm + SM_AS);
     float *Xs = reinterpret_cast<float *>(sm + SM_X);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM_BAR);
@@ -606,6 +611,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&bars[b], b < BAR_OPS ? 1 : (b < BAR_SREADY ? NP : NS));
         fence_mbar_init();
     }
+    if (NORM)  // the row-sum buffer of chunk 0 starts at zero (step 1 zeroes the later ones)
+        for (int e = tid; e < 384; e += NTHREADS) nrmb[e] = 0.f;
     if (tid == 64) {
         prefetch_tensormap(&maps.q);
         prefetch_tensormap(&maps.k);
@@ -1006,6 +1013,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         auto step1 = [&](int cc) -> bool {
             const long long r0 = bos + (long long)cc * C;
             const int ln = (int)min((long long)C, eos - r0);
+            QKRows qk;
+            if (NORM) {  // in flight while the cumsum runs
+                load_qk_rows(qk, static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
+                             r0, ln, H, h, tr0, j);
+                if (tid < 128) nrmb[128 * ((cc + 1) % 3) + tid] = 0.f;
+            }
             const float bet = __uint_as_float(beta_next << 16);
             if (cc + 1 < nchunks) beta_next = load_beta(cc + 1);
             if (!prep_wait(&bars[BAR_G], (uint32_t)(cc & 1))) return false;
@@ -1051,6 +1064,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             if (tid < C) sbeta[64 * (cc & 1) + tid] = bet;
+            if (NORM) add_row_square_sums(nrmb + 128 * (cc % 3), qk, tr0, lane);
             prep_sync();
             if (tid == 0 && cc + 1 < nchunks) {  // every prep thread has read the g tile
                 const int r = (int)(bos + (long long)(cc + 1) * C);
@@ -1101,9 +1115,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!(ok = prep_wait(&bars[BAR_QK], par))) break;
             if (c > 0 && !(ok = prep_wait(&bars[BAR_KQFREE], par ^ 1u))) break;
             if (mh)
-                build_operands<1, NORM>(sm, gm, cst, tr0, j, len, SM_KH + 16384u * par);
+                build_operands<1, NORM>(sm, gm, cst, tr0, j, len, SM_KH + 16384u * par, nrmb + 128 * (c % 3));
             else
-                build_operands<0, NORM>(sm, gm, cst, tr0, j, len, SM_KH + 16384u * par);
+                build_operands<0, NORM>(sm, gm, cst, tr0, j, len, SM_KH + 16384u * par, nrmb + 128 * (c % 3));
             fence_async_smem();
             mbar_arrive(&bars[BAR_OPS]);
 
