@@ -47,7 +47,7 @@ NAMES = ("q", "k", "v", "g", "beta")
 L2_BYTES = 129 * 2 ** 20
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
@@ -70,7 +70,7 @@ def parse():
                          "backward = all gradients of the headline shape (kda_backward)")
     ap.add_argument("--ncu-case", choices=("prefill", "decode", "backward"),
                     help="run two launches of the small profiling case (for ncu) and exit")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     return args
@@ -79,19 +79,28 @@ def parse():
 # ------------------------------------------------------------------------ ranks ---------
 
 class Ranks:
-    def __init__(self, gpus):
+    """One process per GPU (RANK / LOCAL_RANK / WORLD_SIZE from the launcher). The ranks share
+    nothing on the data path (each runs its own copy of the workload); they meet only in the
+    barriers around the timed region and in the max over ranks of its duration. NCCL on GPUs;
+    `backend="gloo"` with `device="cpu"` runs the same logic on host processes."""
+
+    def __init__(self, gpus, backend=None, device=None):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         if self.world != gpus:
             raise SystemExit(f"--gpus {gpus} but WORLD_SIZE={self.world}")
+        self.device = torch.device(device) if device else torch.device("cuda", self.local)
         self.dist = None
         if self.world > 1:
             import torch.distributed as dist
-            dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            if (backend or "nccl") == "nccl":
+                dist.init_process_group("nccl", device_id=self.device)
+            else:
+                dist.init_process_group(backend)
             self.dist = dist
-        torch.cuda.set_device(self.local)
-        self.device = torch.device("cuda", self.local)
+        if self.device.type == "cuda":
+            torch.cuda.set_device(self.device)
 
     def barrier(self):
         if self.dist:
@@ -107,6 +116,10 @@ class Ranks:
     def close(self):
         if self.dist:
             self.dist.destroy_process_group()
+
+    def job_throughput(self, units_per_rank: float, ms: float) -> float:
+        """Whole-job rate: the units every rank processed over the slowest rank's time."""
+        return self.world * units_per_rank / (self.max(ms) / 1e3)
 
 
 # ---------------------------------------------------------------------- clocks ----------
@@ -272,10 +285,10 @@ def run_ours(args):
     with ClockSampler(dev) as clk:
         total_ms, per = time_steps(step, args.steps, args.warmup, ranks)
     kda.check_status()
+    tokens = B * T
+    value = ranks.job_throughput(tokens * args.steps, total_ms)
     total_ms = ranks.max(total_ms)
     ms = total_ms / args.steps
-    tokens = B * T
-    value = args.gpus * tokens * args.steps / (total_ms / 1e3)
     kernel_ms = statistics.mean(per)
     alg = prefill_bytes(B, T, H, d)
     achieved = alg / (kernel_ms / 1e3) / 1e9
@@ -378,10 +391,11 @@ def run_e2e(args, kda, x, ranks, tokens):
     total_ms = run(steps)
     ranks.barrier()
     kda.check_status()
+    value = ranks.job_throughput(tokens * steps, total_ms)
     total_ms = ranks.max(total_ms)
     h2d = sum(host[n].numel() * host[n].element_size() for n in NAMES)
     d2h = o_h[0].numel() * o_h[0].element_size() + fin_h[0].numel() * fin_h[0].element_size()
-    return {"value": args.gpus * tokens * steps / (total_ms / 1e3), "unit": "tokens/s", "steps": steps,
+    return {"value": value, "unit": "tokens/s", "steps": steps,
             "ms_per_step": total_ms / steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "gpu_launches": steps,
             "pipeline": f"upload step i on {len(s_ups)} streams, compute i-1, download i-2"}
@@ -401,6 +415,7 @@ def run_decode(args, kda, ki, ranks, peak_bw, peak_kind):
 
     total_ms, per = time_steps(step, steps, 10, ranks)
     kda.check_status()
+    value = ranks.job_throughput(N * steps, total_ms)
     total_ms = ranks.max(total_ms)
     ms = total_ms / steps
     alg = decode_bytes(N, H, d)
@@ -408,7 +423,7 @@ def run_decode(args, kda, ki, ranks, peak_bw, peak_kind):
     achieved = alg / (kernel_ms / 1e3) / 1e9
     return {"metric": "KDA decode tokens/s (one token for each of N=256 sequences per step, H=32, "
                       "dk=dv=128, bf16 in, fp32 state)",
-            "value": args.gpus * N * steps / (total_ms / 1e3), "unit": "tokens/s", "steps": steps,
+            "value": value, "unit": "tokens/s", "steps": steps,
             "ms_per_step": ms, "gpu_launches": steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s",
                          "frac": achieved / peak_bw, "peak_source": peak_kind,
