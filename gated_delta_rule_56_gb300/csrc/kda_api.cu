@@ -96,7 +96,56 @@ StaticScratch *static_scratch(int dev) {
 
 std::mutex g_static_scratch_mu;
 
+// Longest-first order of packed sequences: one CTA sorts (length, index) keys (length
+// descending, index ascending among equals) with a bitonic network in shared memory. The
+// tensor-core kernel then starts the longest sequences' CTAs first, so the last CTAs to start are
+// short ones and the tail of the launch is short. A malformed cu_seqlens still gives a
+// permutation (its lengths are clamped); the kernel reports it as before.
+constexpr int kSortThreads = 1024;
+__global__ void __launch_bounds__(kSortThreads) order_by_length_kernel(const int32_t *__restrict__ cu, int n,
+                                                                        int32_t *__restrict__ order) {
+    __shared__ unsigned long long key[kMaxOrderedSeqs];
+    int m = 1;
+    while (m < n) m <<= 1;
+    for (int i = threadIdx.x; i < m; i += kSortThreads) {
+        if (i < n) {
+            const long long len = (long long)cu[i + 1] - cu[i];
+            const unsigned inv = 0x7fffffffu - (unsigned)(len < 0 ? 0 : (len > 0x7fffffff ? 0x7fffffff : len));
+            key[i] = ((unsigned long long)inv << 32) | (unsigned)i;
+        } else {
+            key[i] = ~0ull;
+        }
+    }
+    __syncthreads();
+    for (int size = 2; size <= m; size <<= 1)
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < m; i += kSortThreads) {
+                const int jx = i ^ stride;
+                if (jx > i) {
+                    const bool up = (i & size) == 0;
+                    const unsigned long long a = key[i], b = key[jx];
+                    if ((a > b) == up) {
+                        key[i] = b;
+                        key[jx] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    for (int i = threadIdx.x; i < n; i += kSortThreads) order[i] = (int32_t)(key[i] & 0xffffffffu);
+}
+
 }  // namespace
+
+size_t order_workspace_bytes(kda_dtype dtype, int dk, int dv, int n_seqs) {
+    if (dtype != KDA_BF16 || dk != 128 || dv != 128 || n_seqs < 2 || n_seqs > kMaxOrderedSeqs) return 0;
+    return ((size_t)n_seqs * sizeof(int32_t) + 255) / 256 * 256;
+}
+
+cudaError_t launch_order_by_length(const int32_t *cu_seqlens, int n_seqs, int32_t *order, cudaStream_t s) {
+    order_by_length_kernel<<<1, kSortThreads, 0, s>>>(cu_seqlens, n_seqs, order);
+    return cudaGetLastError();
+}
 
 unsigned *device_error_word() {
     static std::mutex mu;
@@ -213,6 +262,15 @@ kda_status prefill_impl(kda_dtype dtype, int B, int T, int H, int dk, int dv, co
                             cudaGetErrorString(cudaGetLastError()));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (tc_prefill_supported(dtype, dk, dv, p)) {
+        // Packed sequences: start the longest first when the caller gave the workspace for the order.
+        const size_t ord_bytes = cu_seqlens ? order_workspace_bytes(dtype, dk, dv, n_seqs) : 0;
+        if (ord_bytes && workspace && workspace_bytes >= ord_bytes &&
+            (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0) {
+            int32_t *order = static_cast<int32_t *>(workspace);
+            const cudaError_t e = launch_order_by_length(cu_seqlens, n_seqs, order, s);
+            if (e != cudaSuccess) return launched(e, "sequence order");
+            p.order = order;
+        }
         // A few long sequences: split them along the sequence when the caller gave the workspace.
         const size_t seg_bytes = segmented_workspace_bytes(dtype, B, T, H, dk, dv, cu_seqlens != nullptr);
         if (seg_bytes && workspace && workspace_bytes >= seg_bytes &&
@@ -291,7 +349,8 @@ const char *kda_last_error(void) { return g_last_error; }
 
 size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv, int n_seqs) {
     if (B < 0 || T < 0 || H < 0) return 0;
-    return segmented_workspace_bytes(dtype, B, T, H, dk, dv, n_seqs != B);
+    if (n_seqs != B) return order_workspace_bytes(dtype, dk, dv, n_seqs);  // packed sequences
+    return segmented_workspace_bytes(dtype, B, T, H, dk, dv, false);
 }
 
 kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,
@@ -331,9 +390,9 @@ kda_status kda_prefill_noalloc(kda_dtype dtype, int B, int T, int H, int dk, int
                                const void *k, const void *v, const void *g, const void *beta,
                                const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,
                                float *final_state, kda_stream_t stream) {
-    const size_t need = (B < 0 || T < 0 || H < 0)
-                            ? 0
-                            : segmented_workspace_bytes(dtype, B, T, H, dk, dv, cu_seqlens != nullptr);
+    const size_t need = (B < 0 || T < 0 || H < 0) ? 0
+                        : cu_seqlens ? order_workspace_bytes(dtype, dk, dv, n_seqs)
+                                     : segmented_workspace_bytes(dtype, B, T, H, dk, dv, false);
     if (need > kStaticScratchBytes)
         return fail(KDA_ERR_UNSUPPORTED, "this call needs %zu bytes of scratch; the static scratch holds %zu",
                     need, kStaticScratchBytes);

@@ -33,6 +33,7 @@ struct RunParams {
     const int32_t *fin_idx;     // non-null: fin is a pool; sequence n ends in state fin_idx[n] (< 0: not written)
     int pool;                   // states in the pool(s) when an index array is given
     const void *out_gate;       // non-null: o is multiplied by sigmoid(out_gate) (same layout and dtype as o)
+    const int32_t *order;       // non-null: CTA block b / H runs sequence order[b / H] (a permutation)
     int max_chunks;             // > 0: only the first max_chunks chunks of every sequence are run
     const uint8_t *skip;        // non-null: the CTA of (sequence n, head h) exits at once if skip[n*H + h]
 };
@@ -56,6 +57,11 @@ bool encode_row_tile_map(CUtensorMap *map, const void *base, long long rows, int
 size_t segmented_workspace_bytes(kda_dtype dtype, int B, int T, int H, int dk, int dv, bool varlen);
 cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace, size_t workspace_bytes,
                                      cudaStream_t s);
+
+// Longest-first launch order of packed sequences (see kda_api.cu): workspace bytes and the sort.
+constexpr int kMaxOrderedSeqs = 4096;
+size_t order_workspace_bytes(kda_dtype dtype, int dk, int dv, int n_seqs);
+cudaError_t launch_order_by_length(const int32_t *cu_seqlens, int n_seqs, int32_t *order, cudaStream_t s);
 
 // Backward pass (see kda_backward.cu): workspace bytes for the state checkpoints, and the launch.
 size_t backward_workspace_bytes(int T_total, int n_seqs, int H, int d);

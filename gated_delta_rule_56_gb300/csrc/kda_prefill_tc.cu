@@ -584,7 +584,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = p.H;
     const int h = blockIdx.x % H;
-    const int n = blockIdx.x / H;
+    const int n = p.order ? p.order[blockIdx.x / H] : (int)(blockIdx.x / H);
 
     long long bos, eos;
     if (p.cu_seqlens) {

@@ -107,7 +107,10 @@ typedef struct kda_options {
  * o            output [B, T, H, dv], same dtype as the inputs. Every row is written.
  * final_state  fp32 [N, H, dk, dv] or NULL (not written). May alias initial_state.
  * workspace, workspace_bytes  device scratch, 256-byte aligned, of at least
- *              kda_prefill_workspace_size() bytes; or NULL / 0. Only a split call uses it: when
+ *              kda_prefill_workspace_size() bytes; or NULL / 0. Packed bf16 d=128 sequences (2 to
+ *              4096 of them) use 4 bytes per sequence for a longest-first launch order (a sort of
+ *              cu_seqlens by length on the device), which shortens the tail of the launch; the
+ *              results are the same without it. A split call uses it for more: when
  *              few long sequences cannot fill the GPU (bf16, dk == dv == 128, no cu_seqlens), each
  *              is cut into segments run side by side and joined through the segment transitions
  *              (the state after a segment is linear in the state before it: "Inside Kimi K3's
@@ -124,10 +127,11 @@ KDA_API kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int
                        const float *initial_state, void *o, float *final_state,
                        void *workspace, size_t workspace_bytes, kda_stream_t stream);
 
-/* Bytes of device workspace with which kda_prefill splits these sizes along the sequence, or 0
- * when it would not split them. The split follows the current device's SM count (0 when no device
- * is visible). n_seqs != B means packed sequences (cu_seqlens), which are never split, so 0; a
- * packed call needs no workspace whatever this returns. The same sizes apply to kda_prefill_gated. */
+/* Bytes of device workspace kda_prefill can use for these sizes, or 0. n_seqs != B means packed
+ * sequences (cu_seqlens): the launch order, 4 bytes per sequence rounded up to 256, for bf16
+ * dk == dv == 128 and 2 <= n_seqs <= 4096. Otherwise the split along the sequence, which follows
+ * the current device's SM count (0 when no device is visible or the call would not split). The
+ * same sizes apply to kda_prefill_gated and kda_prefill_ex. */
 KDA_API size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv,
                                   int n_seqs);
 

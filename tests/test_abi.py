@@ -40,11 +40,21 @@ def test_status_strings_and_version(lib):
 
 
 def test_workspace_size_is_zero_when_not_split(lib):
-    # Many (sequence, head) pairs, packed sequences, fp32 or small heads: one pass, no workspace.
+    # Many (sequence, head) pairs, fp32 or small heads: one pass, no workspace.
     assert lib.kda_prefill_workspace_size(0, 4, 8192, 32, 128, 128, 4) == 0
-    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 128, 128, 64) == 0   # varlen
     assert lib.kda_prefill_workspace_size(1, 1, 1 << 20, 32, 128, 128, 1) == 0    # fp32
     assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 64, 64, 1) == 0      # d = 64
+
+
+def test_workspace_size_of_packed_sequences(lib):
+    # Packed bf16 d=128 sequences: 4 bytes per sequence for the longest-first launch order,
+    # rounded up to 256; none for one sequence, more than 4096, fp32 or other head sizes.
+    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 128, 128, 64) == 256
+    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 128, 128, 100) == 512
+    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 128, 128, 4096) == 4096 * 4
+    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 128, 128, 4097) == 0
+    assert lib.kda_prefill_workspace_size(1, 1, 1 << 20, 32, 128, 128, 64) == 0
+    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 64, 64, 64) == 0
 
 
 def test_noalloc_capacity_and_argument_checks(lib):

@@ -213,3 +213,20 @@ def test_long_context_sampled_heads():
             log_bound = x["g"][0, a - M:a, h].float().max(dim=-1).values.sum().item() + math.log(max(bv, 1e-30))
             assert log_bound < math.log(1e-12), log_bound
             assert_close(o[0, a:b, h], ro[0, M:, 0], f"o[{a}:{b}] (h={h})")
+
+
+def test_varlen_longest_first_order_changes_nothing():
+    """With the workspace the packed sequences launch longest first; every (sequence, head) is
+    computed the same way, so the results equal the natural-order launch bit for bit."""
+    x = ki.varlen_inputs([70, 1, 130, 64, 2000, 5, 640], 2, 128, 128, device=DEV, seed=13)
+    lib = kda.load()
+    n = x["cu_seqlens"].numel() - 1
+    assert lib.kda_prefill_workspace_size(0, 1, x["q"].shape[1], 2, 128, 128, n) > 0
+    o1, s1 = run(x)
+    o2, s2 = torch.empty_like(o1), torch.empty_like(s1)
+    st = lib.kda_prefill(0, 1, x["q"].shape[1], 2, 128, 128, *(x[m].data_ptr() for m in NAMES),
+                         x["cu_seqlens"].data_ptr(), n, x["initial_state"].data_ptr(), o2.data_ptr(),
+                         s2.data_ptr(), None, 0, torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    kda.check_status()
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
