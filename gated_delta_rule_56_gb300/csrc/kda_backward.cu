@@ -290,6 +290,7 @@ cudaError_t launch_typed(int d, const RunParams &p, const void *d_o, const float
 
 size_t backward_workspace_bytes(int T_total, int n_seqs, int H, int d) {
     if (T_total < 0 || n_seqs < 0 || H <= 0 || d <= 0) return 0;
+    if (d == 128) return backward_chunked_workspace_bytes(T_total, n_seqs, H);
     return ((size_t)T_total / kChunk + (size_t)n_seqs + 1) * (size_t)H * d * d * sizeof(float);
 }
 
@@ -297,6 +298,8 @@ cudaError_t launch_backward(kda_dtype dtype, int d, const RunParams &p, const vo
                             float *dq, float *dk, float *dv, float *dg, float *dbeta, float *d_init, void *ws,
                             cudaStream_t s) {
     if ((long long)p.n_seqs * p.H == 0) return cudaSuccess;
+    if (d == 128)  // chunkwise on 16-token tiles (kda_backward_chunked.cu); writes every output itself
+        return launch_backward_chunked(dtype, p, d_o, d_fin, dq, dk, dv, dg, dbeta, d_init, ws, s);
     const long long rows = p.cu_seqlens ? (long long)p.T : (long long)p.n_seqs * p.T;
     const size_t nk = (size_t)rows * p.H * d;
     // dq, dk, dg and dbeta are sums of atomic adds: start them at zero (dv is stored directly).

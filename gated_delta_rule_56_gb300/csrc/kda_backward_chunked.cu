@@ -1,0 +1,471 @@
+// kda_backward_chunked.cu -- gradients of the KDA recurrence for d_k = d_v = 128, chunkwise.
+//
+// The same gradients as kda_backward.cu (L = sum(dO * O) + sum(dS_final * S_final); dq, dk, dv,
+// dg, dbeta, dS_initial in fp32), computed over chunks of C = 16 tokens in the chunkwise form of
+// the recurrence ("Kimi K3 Explained", researchpapers.dev, "Architecture at a glance": the
+// chunkwise computation runs on dense tiles). Per chunk, with S the state at its start,
+// Gam = cumsum of g over the chunk's rows (per channel), gam = exp(Gam), gC = gam of the last row:
+//     Kp = K gam, Km = K / gam, Qp = Q gam, Kc = K gC / gam               (element-wise)
+//     Ab = Kp Km^T,  A = strict_lower(Diag(beta) Ab),  X = (I + A)^{-1},  T = X Diag(beta)
+//     R = V - Kp S,  U = T R,  P = lower(Qp Km^T),  O = Qp S + P U,  S' = Diag(gC) S + Kc^T U
+// and its adjoint, given dO and dS' (the gradient w.r.t. the next chunk's start state):
+//     dU = P^T dO + Kc dS',  dR = T^T dU (= dV),  dP = lower(dO U^T),  dT = dU R^T,
+//     dX = dT Diag(beta),  dbeta = colsum(X * dT) + rowsum(dA * Ab),  dA = strict_lower(-X^T dX X^T),
+//     dQp = dO S^T + dP Km,  dKp = -dR S^T + (Diag(beta) dA) Km,
+//     dKm = dP^T Qp + (Diag(beta) dA)^T Kp,  dKc = U dS'^T,  dgC = rowsum(dS' * S),
+//     dK = dKp gam + dKm / gam + dKc gC / gam,  dQ = dQp gam,
+//     dGam = dKp Kp - dKm Km + dQp Qp - dKc Kc  (+ colsum(dKc Kc) + dgC gC on the last row),
+//     dg = reverse cumsum of dGam over the rows,  dS = Qp^T dO - Kp^T dR + Diag(gC) dS'.
+// With g >= -5 a 16-row chunk keeps gam and 1/gam within e^{+-80}, inside fp32, so the chunk needs
+// no sub-tiling; each exponent is clamped to +-87 so out-of-range gates stay finite.
+//
+// One CTA of 512 threads per (sequence, head) holds S and dS (fp32, 128 x 128, rows padded to
+// 129 floats so that both row and column reads are free of bank conflicts) and the chunk's
+// 16 x 128 tiles in shared memory; every product runs on the CUDA cores in fp32. A forward sweep
+// stores the state at every chunk start in the workspace; the reverse sweep reads it back.
+// All columns live in one CTA, so every gradient is written directly (no atomics).
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int D = 128;
+constexpr int C = 16;                  // tokens per chunk
+constexpr int NT = 512;                // threads per CTA
+constexpr int LS = D + 1;              // row stride of S and dS (floats)
+constexpr int LT = D + 4;              // row stride of a 16 x 128 tile (floats; 16-byte rows)
+constexpr int LM = C + 1;              // row stride of a 16 x 16 matrix
+
+// Shared-memory layout (floats).
+constexpr int O_S = 0;
+constexpr int O_DS = O_S + D * LS;
+constexpr int O_GAM = O_DS + D * LS;   // tiles of C x LT
+constexpr int O_QP = O_GAM + C * LT;
+constexpr int O_KP = O_QP + C * LT;
+constexpr int O_KM = O_KP + C * LT;
+constexpr int O_R = O_KM + C * LT;     // V, then R = V - Kp S
+constexpr int O_U = O_R + C * LT;
+constexpr int O_DO = O_U + C * LT;
+constexpr int O_DU = O_DO + C * LT;
+constexpr int O_DR = O_DU + C * LT;
+constexpr int O_DG = O_DR + C * LT;
+constexpr int O_AB = O_DG + C * LT;    // 16 x 16 matrices of C x LM
+constexpr int O_X = O_AB + C * LM;
+constexpr int O_T = O_X + C * LM;
+constexpr int O_P = O_T + C * LM;
+constexpr int O_DP = O_P + C * LM;
+constexpr int O_DT = O_DP + C * LM;
+constexpr int O_DAB = O_DT + C * LM;   // Diag(beta) dA
+constexpr int O_M = O_DAB + C * LM;    // scratch 16 x 16
+constexpr int O_BETA = O_M + C * LM;   // [C]
+constexpr int O_DB = O_BETA + C;       // [C] dbeta
+constexpr int O_GC = O_DB + C;         // [D] gC
+constexpr int O_DGC = O_GC + D;        // [D] dgC gC + colsum(dKc Kc)
+constexpr int FLOATS = O_DGC + D;
+constexpr size_t SMEM = (size_t)FLOATS * sizeof(float);
+static_assert(SMEM <= 232448, "shared memory budget");
+
+__device__ __forceinline__ float ld(const float *p, size_t i) { return __ldg(p + i); }
+__device__ __forceinline__ float ld(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
+
+// Load the chunk's rows [t0, t0 + n) of a [rows, H, D] tensor into a C x LT tile (rows past n = 0).
+template <typename Tin>
+__device__ __forceinline__ void load_tile(float *tile, const Tin *src, long long t0, int n, int H, int h) {
+    for (int e = threadIdx.x; e < C * D; e += NT) {
+        const int r = e / D, i = e % D;
+        tile[r * LT + i] = r < n ? ld(src, ((size_t)(t0 + r) * H + h) * D + i) : 0.f;
+    }
+}
+
+// gam = exp(cumsum g) per channel over the chunk (rows past n: g = 0), gC = its last row.
+template <typename Tin>
+__device__ __forceinline__ void gate_tile(float *sm, const Tin *g, long long t0, int n, int H, int h) {
+    if (threadIdx.x < D) {
+        const int i = threadIdx.x;
+        float G = 0.f;
+        for (int r = 0; r < C; ++r) {
+            if (r < n) G += ld(g, ((size_t)(t0 + r) * H + h) * D + i);
+            sm[O_GAM + r * LT + i] = __expf(fminf(fmaxf(G, -87.f), 87.f));
+        }
+        sm[O_GC + i] = sm[O_GAM + (C - 1) * LT + i];
+    }
+}
+
+// out[r][j] (16 x 128) = sum_i a[r][i] * B[i][j] with B 128 x 128 at row stride LS; thread t
+// takes column j = t % 128 and rows 4 (t / 128) .. + 3.
+__device__ __forceinline__ void tile_times_state(float (&acc)[4], const float *a, const float *B) {
+    const int j = threadIdx.x % D, r0 = 4 * (threadIdx.x / D);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < D; i += 4) {
+        const float b0 = B[(i + 0) * LS + j], b1 = B[(i + 1) * LS + j];
+        const float b2 = B[(i + 2) * LS + j], b3 = B[(i + 3) * LS + j];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 x = *reinterpret_cast<const float4 *>(a + (r0 + q) * LT + i);
+            acc[q] = fmaf(x.x, b0, fmaf(x.y, b1, fmaf(x.z, b2, fmaf(x.w, b3, acc[q]))));
+        }
+    }
+}
+
+// M[r][s] (16 x 16) = sum_i a[r][i] * b[s][i] over the 128 channels; one output per thread of the
+// first 256, the two halves of the channel sum by thread pairs.
+__device__ __forceinline__ void tile_times_tile_t(float *M, const float *a, const float *b) {
+    const int t = threadIdx.x, o = t >> 1, half = t & 1;
+    const int r = o / C, s = o % C;
+    float acc = 0.f;
+    const float *ar = a + r * LT + 64 * half, *bs = b + s * LT + 64 * half;
+#pragma unroll 4
+    for (int i = 0; i < 64; i += 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(ar + i), y = *reinterpret_cast<const float4 *>(bs + i);
+        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    if (half == 0) M[r * LM + s] = acc;
+}
+
+// The chunk's gate products and triangular factors: Kp, Km, (Qp), Ab, A -> X, T, (P).
+__device__ __forceinline__ void chunk_factors(float *sm, const float *K, bool with_q) {
+    for (int e = threadIdx.x; e < C * D; e += NT) {
+        const int r = e / D, i = e % D;
+        const float gm = sm[O_GAM + r * LT + i], k = K[r * LT + i];
+        sm[O_KP + r * LT + i] = k * gm;
+        sm[O_KM + r * LT + i] = __fdividef(k, gm);
+        if (with_q) sm[O_QP + r * LT + i] *= gm;  // Q was loaded into the Qp tile
+    }
+    __syncthreads();
+    tile_times_tile_t(sm + O_AB, sm + O_KP, sm + O_KM);
+    if (with_q) {
+        __syncthreads();
+        tile_times_tile_t(sm + O_P, sm + O_QP, sm + O_KM);
+    }
+    __syncthreads();
+    // X = (I + A)^{-1} for the unit lower-triangular I + A, A = strict_lower(Diag(beta) Ab): column
+    // j by forward substitution (one thread per column); T = X Diag(beta).
+    if (threadIdx.x < C) {
+        const int j = threadIdx.x;
+        float x[C];
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+            float v = (i == j) ? 1.f : 0.f;
+            if (i > j) {
+                const float bi = sm[O_BETA + i];
+#pragma unroll
+                for (int k = 0; k < C; ++k)
+                    if (k >= j && k < i) v = fmaf(-bi * sm[O_AB + i * LM + k], x[k], v);
+            }
+            x[i] = v;
+        }
+        const float bj = sm[O_BETA + j];
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+            sm[O_X + i * LM + j] = x[i];
+            sm[O_T + i * LM + j] = x[i] * bj;
+        }
+    }
+    if (with_q) {  // P = lower(Qp Km^T)
+        for (int e = threadIdx.x; e < C * C; e += NT) {
+            const int r = e / C, s = e % C;
+            if (s > r) sm[O_P + r * LM + s] = 0.f;
+        }
+    }
+    __syncthreads();
+}
+
+// R = V - Kp S (in the R tile, which holds V), then U = T R.
+__device__ __forceinline__ void chunk_u(float *sm) {
+    float acc[4];
+    tile_times_state(acc, sm + O_KP, sm + O_S);
+    const int j = threadIdx.x % D, r0 = 4 * (threadIdx.x / D);
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sm[O_R + (r0 + q) * LT + j] -= acc[q];
+    __syncthreads();
+    for (int e = threadIdx.x; e < C * D; e += NT) {
+        const int r = e / D, i = e % D;
+        float u = 0.f;
+#pragma unroll
+        for (int s = 0; s < C; ++s) u = fmaf(sm[O_T + r * LM + s], sm[O_R + s * LT + i], u);
+        sm[O_U + r * LT + i] = u;
+    }
+    __syncthreads();
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, const void *d_o, const float *d_fin,
+                                                                 float *dq, float *dk, float *dv, float *dg,
+                                                                 float *dbeta, float *d_init, float *ck) {
+    extern __shared__ float sm[];
+    const int H = p.H, h = blockIdx.x % H, n = blockIdx.x / H, tid = threadIdx.x;
+    long long bos, eos;
+    if (p.cu_seqlens) {
+        bos = p.cu_seqlens[n];
+        eos = p.cu_seqlens[n + 1];
+        if (bos < 0 || eos < bos || eos > p.T || (n == 0 && bos != 0) || (n == p.n_seqs - 1 && eos != p.T)) {
+            if (tid == 0) atomicOr(p.err, kErrBadSeqlens);
+            return;
+        }
+    } else {
+        bos = (long long)n * p.T;
+        eos = bos + p.T;
+    }
+    const int nc = (int)((eos - bos + C - 1) / C);
+    const long long ck0 = bos / C + n;  // this sequence's checkpoint slots (never overlap the next's)
+    auto ck_at = [&](int c) { return ck + ((size_t)(ck0 + c) * H + h) * D * D; };
+    const Tin *Kg = static_cast<const Tin *>(p.k), *Qg = static_cast<const Tin *>(p.q);
+    const Tin *Vg = static_cast<const Tin *>(p.v), *Gg = static_cast<const Tin *>(p.g);
+    const Tin *Bg = static_cast<const Tin *>(p.beta), *DOg = static_cast<const Tin *>(d_o);
+    const size_t sbase = ((size_t)n * H + h) * D * D;
+    float *S = sm + O_S, *dS = sm + O_DS;
+
+    for (int e = tid; e < D * D; e += NT) S[(e / D) * LS + e % D] = p.init ? p.init[sbase + e] : 0.f;
+    __syncthreads();
+
+    // ---- forward sweep: the state at every chunk start into the workspace ----------------------
+    for (int c = 0; c < nc; ++c) {
+        const long long t0 = bos + (long long)c * C;
+        const int len = (int)min((long long)C, eos - t0);
+        float *dst = ck_at(c);
+        for (int e = tid; e < D * D; e += NT) dst[e] = S[(e / D) * LS + e % D];
+        load_tile(sm + O_DU, Kg, t0, len, H, h);  // K in the dU tile (free in the forward sweep)
+        load_tile(sm + O_R, Vg, t0, len, H, h);
+        if (tid < C) sm[O_BETA + tid] = tid < len ? ld(Bg, (size_t)(t0 + tid) * H + h) : 0.f;
+        gate_tile(sm, Gg, t0, len, H, h);
+        __syncthreads();
+        chunk_factors(sm, sm + O_DU, false);
+        chunk_u(sm);
+        // S <- Diag(gC) S + Kc^T U, Kc = Km gC: thread takes column j, rows 32 (t / 128) .. + 31.
+        {
+            const int j = tid % D, i0 = 32 * (tid / D);
+            float acc[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) acc[q] = S[(i0 + q) * LS + j] * sm[O_GC + i0 + q];
+#pragma unroll 2
+            for (int r = 0; r < C; ++r) {
+                const float u = sm[O_U + r * LT + j];
+#pragma unroll
+                for (int q = 0; q < 32; q += 4) {
+                    const float4 km = *reinterpret_cast<const float4 *>(sm + O_KM + r * LT + i0 + q);
+                    acc[q + 0] = fmaf(km.x * sm[O_GC + i0 + q + 0], u, acc[q + 0]);
+                    acc[q + 1] = fmaf(km.y * sm[O_GC + i0 + q + 1], u, acc[q + 1]);
+                    acc[q + 2] = fmaf(km.z * sm[O_GC + i0 + q + 2], u, acc[q + 2]);
+                    acc[q + 3] = fmaf(km.w * sm[O_GC + i0 + q + 3], u, acc[q + 3]);
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) S[(i0 + q) * LS + j] = acc[q];
+        }
+        __syncthreads();
+    }
+
+    // ---- reverse sweep ---------------------------------------------------------------------------
+    for (int e = tid; e < D * D; e += NT) dS[(e / D) * LS + e % D] = d_fin ? d_fin[sbase + e] : 0.f;
+    for (int c = nc - 1; c >= 0; --c) {
+        const long long t0 = bos + (long long)c * C;
+        const int len = (int)min((long long)C, eos - t0);
+        __syncthreads();
+        {
+            const float *src = ck_at(c);
+            for (int e = tid; e < D * D; e += NT) S[(e / D) * LS + e % D] = src[e];
+        }
+        load_tile(sm + O_DU, Kg, t0, len, H, h);  // K, until the factors are formed
+        load_tile(sm + O_QP, Qg, t0, len, H, h);
+        load_tile(sm + O_R, Vg, t0, len, H, h);
+        load_tile(sm + O_DO, DOg, t0, len, H, h);
+        if (tid < C) sm[O_BETA + tid] = tid < len ? ld(Bg, (size_t)(t0 + tid) * H + h) : 0.f;
+        if (tid < D) sm[O_DGC + tid] = 0.f;
+        gate_tile(sm, Gg, t0, len, H, h);
+        __syncthreads();
+        chunk_factors(sm, sm + O_DU, true);
+        chunk_u(sm);
+        // dU = P^T dO + Kc dS  (Kc dS = Diag-free: Kc[r][i] = Km[r][i] gC[i])
+        {
+            const int j = tid % D, r0 = 4 * (tid / D);
+            float acc[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] = 0.f;
+#pragma unroll 4
+            for (int i = 0; i < D; ++i) {
+                const float b = dS[i * LS + j] * sm[O_GC + i];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[q] = fmaf(sm[O_KM + (r0 + q) * LT + i], b, acc[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float x = acc[q];
+#pragma unroll
+                for (int s = 0; s < C; ++s) x = fmaf(sm[O_P + s * LM + r0 + q], sm[O_DO + s * LT + j], x);
+                sm[O_DU + (r0 + q) * LT + j] = x;
+            }
+        }
+        __syncthreads();
+        // dR = T^T dU (= dV, stored), dP = lower(dO U^T), dT = dU R^T
+        for (int e = tid; e < C * D; e += NT) {
+            const int r = e / D, i = e % D;
+            float x = 0.f;
+#pragma unroll
+            for (int s = 0; s < C; ++s) x = fmaf(sm[O_T + s * LM + r], sm[O_DU + s * LT + i], x);
+            sm[O_DR + r * LT + i] = x;
+            if (r < len) dv[((size_t)(t0 + r) * H + h) * D + i] = x;
+        }
+        tile_times_tile_t(sm + O_DP, sm + O_DO, sm + O_U);
+        __syncthreads();
+        tile_times_tile_t(sm + O_DT, sm + O_DU, sm + O_R);
+        __syncthreads();
+        // dX = dT Diag(beta); dbeta = colsum(X * dT) + rowsum(dA * Ab); dA = strict_lower(-X^T dX X^T)
+        if (tid < C * C) {  // M = dX X^T
+            const int r = tid / C, s = tid % C;
+            float x = 0.f;
+#pragma unroll
+            for (int k = 0; k < C; ++k) x = fmaf(sm[O_DT + r * LM + k] * sm[O_BETA + k], sm[O_X + s * LM + k], x);
+            sm[O_M + r * LM + s] = x;
+            if (s > r) sm[O_DP + r * LM + s] = 0.f;  // dP = lower(dO U^T)
+        }
+        __syncthreads();
+        if (tid < C * C) {  // dAb = Diag(beta) strict_lower(-X^T M)
+            const int r = tid / C, s = tid % C;
+            float x = 0.f;
+#pragma unroll
+            for (int k = 0; k < C; ++k) x = fmaf(sm[O_X + k * LM + r], sm[O_M + k * LM + s], x);
+            const float da = s < r ? -x : 0.f;
+            sm[O_DAB + r * LM + s] = da * sm[O_BETA + r];
+            sm[O_P + r * LM + s] = da * sm[O_AB + r * LM + s];  // dA * Ab (P is no longer needed)
+        }
+        __syncthreads();
+        if (tid < C) {
+            const int j = tid;
+            float x = 0.f;
+#pragma unroll
+            for (int i = 0; i < C; ++i) x = fmaf(sm[O_X + i * LM + j], sm[O_DT + i * LM + j], x);
+#pragma unroll
+            for (int s = 0; s < C; ++s) x += sm[O_P + j * LM + s];
+            if (j < len) dbeta[(size_t)(t0 + j) * H + h] = x;
+        }
+        // Per (r, i): dQp, dKp, dKm, dKc -> dq, dk and dGam. Thread: channel i = t % 128, rows
+        // 4 (t / 128) .. + 3.
+        {
+            const int i = tid % D, r0 = 4 * (tid / D);
+            float aq[4], ak[4], ac[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) aq[q] = ak[q] = ac[q] = 0.f;
+            float dgc = 0.f;
+#pragma unroll 2
+            for (int j = 0; j < D; j += 4) {
+                float s4[4], ds4[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    s4[m] = S[i * LS + j + m];
+                    ds4[m] = dS[i * LS + j + m];
+                }
+                if (r0 == 0) dgc = fmaf(ds4[0], s4[0], fmaf(ds4[1], s4[1], fmaf(ds4[2], s4[2], fmaf(ds4[3], s4[3], dgc))));
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 o = *reinterpret_cast<const float4 *>(sm + O_DO + (r0 + q) * LT + j);
+                    const float4 rr = *reinterpret_cast<const float4 *>(sm + O_DR + (r0 + q) * LT + j);
+                    const float4 u = *reinterpret_cast<const float4 *>(sm + O_U + (r0 + q) * LT + j);
+                    aq[q] = fmaf(o.x, s4[0], fmaf(o.y, s4[1], fmaf(o.z, s4[2], fmaf(o.w, s4[3], aq[q]))));
+                    ak[q] = fmaf(rr.x, s4[0], fmaf(rr.y, s4[1], fmaf(rr.z, s4[2], fmaf(rr.w, s4[3], ak[q]))));
+                    ac[q] = fmaf(u.x, ds4[0], fmaf(u.y, ds4[1], fmaf(u.z, ds4[2], fmaf(u.w, ds4[3], ac[q]))));
+                }
+            }
+            const float gc = sm[O_GC + i];
+            float colsum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int r = r0 + q;
+                float dqp = aq[q], dkp = -ak[q], dkm = 0.f;
+#pragma unroll
+                for (int s = 0; s < C; ++s) {
+                    const float kms = sm[O_KM + s * LT + i];
+                    dqp = fmaf(sm[O_DP + r * LM + s], kms, dqp);
+                    dkp = fmaf(sm[O_DAB + r * LM + s], kms, dkp);
+                    dkm = fmaf(sm[O_DP + s * LM + r], sm[O_QP + s * LT + i], dkm);
+                    dkm = fmaf(sm[O_DAB + s * LM + r], sm[O_KP + s * LT + i], dkm);
+                }
+                const float gm = sm[O_GAM + r * LT + i];
+                const float kp = sm[O_KP + r * LT + i], km = sm[O_KM + r * LT + i], qp = sm[O_QP + r * LT + i];
+                const float kc = km * gc, dkc = ac[q];
+                const float dkv = dkp * gm + __fdividef(dkm, gm) + dkc * __fdividef(gc, gm);
+                const float dqv = dqp * gm;
+                sm[O_DG + r * LT + i] = dkp * kp - dkm * km + dqp * qp - dkc * kc;
+                colsum = fmaf(dkc, kc, colsum);
+                if (r < len) {
+                    const size_t o = ((size_t)(t0 + r) * H + h) * D + i;
+                    dq[o] = dqv;
+                    dk[o] = dkv;
+                }
+            }
+            atomicAdd(&sm[O_DGC + i], colsum + (r0 == 0 ? dgc * gc : 0.f));
+        }
+        __syncthreads();
+        // dg = reverse cumsum of dGam over the chunk's rows (the last row of the chunk, len - 1 for
+        // a short final chunk, also takes the gC terms).
+        if (tid < D) {
+            const int i = tid;
+            float acc = sm[O_DGC + i];
+            for (int r = C - 1; r >= 0; --r) {
+                if (r < len) {
+                    acc += sm[O_DG + r * LT + i];
+                    dg[((size_t)(t0 + r) * H + h) * D + i] = acc;
+                }
+            }
+        }
+        // dS <- Qp^T dO - Kp^T dR + Diag(gC) dS: thread takes column j, rows 32 (t / 128) .. + 31.
+        {
+            const int j = tid % D, i0 = 32 * (tid / D);
+            float acc[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) acc[q] = dS[(i0 + q) * LS + j] * sm[O_GC + i0 + q];
+#pragma unroll 2
+            for (int r = 0; r < C; ++r) {
+                const float o = sm[O_DO + r * LT + j], rr = sm[O_DR + r * LT + j];
+#pragma unroll
+                for (int q = 0; q < 32; q += 4) {
+                    const float4 qp = *reinterpret_cast<const float4 *>(sm + O_QP + r * LT + i0 + q);
+                    const float4 kp = *reinterpret_cast<const float4 *>(sm + O_KP + r * LT + i0 + q);
+                    acc[q + 0] = fmaf(qp.x, o, fmaf(-kp.x, rr, acc[q + 0]));
+                    acc[q + 1] = fmaf(qp.y, o, fmaf(-kp.y, rr, acc[q + 1]));
+                    acc[q + 2] = fmaf(qp.z, o, fmaf(-kp.z, rr, acc[q + 2]));
+                    acc[q + 3] = fmaf(qp.w, o, fmaf(-kp.w, rr, acc[q + 3]));
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) dS[(i0 + q) * LS + j] = acc[q];
+        }
+    }
+    __syncthreads();
+    if (d_init)
+        for (int e = tid; e < D * D; e += NT) d_init[sbase + e] = dS[(e / D) * LS + e % D];
+}
+
+}  // namespace
+
+size_t backward_chunked_workspace_bytes(int T_total, int n_seqs, int H) {
+    if (T_total < 0 || n_seqs < 0 || H <= 0) return 0;
+    return ((size_t)T_total / C + (size_t)n_seqs + 1) * (size_t)H * D * D * sizeof(float);
+}
+
+cudaError_t launch_backward_chunked(kda_dtype dtype, const RunParams &p, const void *d_o, const float *d_fin,
+                                    float *dq, float *dk, float *dv, float *dg, float *dbeta, float *d_init,
+                                    void *ws, cudaStream_t s) {
+    if ((long long)p.n_seqs * p.H == 0) return cudaSuccess;
+    const dim3 grid((unsigned)(p.n_seqs * p.H));
+    float *ck = static_cast<float *>(ws);
+    cudaError_t e;
+    if (dtype == KDA_BF16) {
+        e = cudaFuncSetAttribute(backward_chunked_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SMEM);
+        if (e != cudaSuccess) return e;
+        backward_chunked_kernel<__nv_bfloat16><<<grid, NT, SMEM, s>>>(p, d_o, d_fin, dq, dk, dv, dg, dbeta, d_init, ck);
+    } else {
+        e = cudaFuncSetAttribute(backward_chunked_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+        if (e != cudaSuccess) return e;
+        backward_chunked_kernel<float><<<grid, NT, SMEM, s>>>(p, d_o, d_fin, dq, dk, dv, dg, dbeta, d_init, ck);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

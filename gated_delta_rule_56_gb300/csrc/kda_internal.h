@@ -65,6 +65,10 @@ cudaError_t launch_order_by_length(const int32_t *cu_seqlens, int n_seqs, int32_
 
 // Backward pass (see kda_backward.cu): workspace bytes for the state checkpoints, and the launch.
 size_t backward_workspace_bytes(int T_total, int n_seqs, int H, int d);
+size_t backward_chunked_workspace_bytes(int T_total, int n_seqs, int H);
+cudaError_t launch_backward_chunked(kda_dtype dtype, const RunParams &p, const void *d_o, const float *d_fin,
+                                    float *dq, float *dk, float *dv, float *dg, float *dbeta, float *d_init,
+                                    void *ws, cudaStream_t s);
 cudaError_t launch_backward(kda_dtype dtype, int d, const RunParams &p, const void *d_o, const float *d_fin,
                             float *dq, float *dk, float *dv, float *dg, float *dbeta, float *d_init, void *ws,
                             cudaStream_t s);
