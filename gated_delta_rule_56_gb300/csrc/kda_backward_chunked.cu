@@ -66,6 +66,29 @@ constexpr size_t SMEM = (size_t)FLOATS * sizeof(float);
 static_assert(SMEM <= 232448, "shared memory budget");
 
 __device__ __forceinline__ float ld(const float *p, size_t i) { return __ldg(p + i); }
+
+// 4-byte asynchronous copies global -> shared (the destination rows are 129 floats apart, so
+// 16-byte copies would not be aligned); the thread waits for all of its own with cp_async_wait.
+__device__ __forceinline__ void cp_async4(float *dst, const float *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// The 128-byte lines of rows [t0, t0 + n) of a [rows, H, D] tensor for head h into L2, ahead of
+// their use (one line per thread at most; D elements of Tin per row).
+template <typename Tin>
+__device__ __forceinline__ void prefetch_rows(const Tin *src, long long t0, int n, int H, int h, int slot) {
+    constexpr int kLines = D * (int)sizeof(Tin) / 128;  // lines per row
+    const int e = (int)threadIdx.x - slot * C * kLines;
+    if (e >= 0 && e < n * kLines) {
+        const char *a = reinterpret_cast<const char *>(src + ((size_t)(t0 + e / kLines) * H + h) * D) + 128 * (e % kLines);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    }
+}
 __device__ __forceinline__ float ld(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
 
 // Load the chunk's rows [t0, t0 + n) of a [rows, H, D] tensor into a C x LT tile (rows past n = 0).
@@ -228,6 +251,13 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         const int len = (int)min((long long)C, eos - t0);
         float *dst = ck_at(c);
         for (int e = tid; e < D * D; e += NT) dst[e] = S[(e / D) * LS + e % D];
+        if (c + 1 < nc) {  // the next chunk's rows into L2
+            const long long t1 = t0 + C;
+            const int l1 = (int)min((long long)C, eos - t1);
+            prefetch_rows(Kg, t1, l1, H, h, 0);
+            prefetch_rows(Vg, t1, l1, H, h, 1);
+            prefetch_rows(Gg, t1, l1, H, h, 2);
+        }
         load_tile(sm + O_DU, Kg, t0, len, H, h);  // K in the dU tile (free in the forward sweep)
         load_tile(sm + O_R, Vg, t0, len, H, h);
         if (tid < C) sm[O_BETA + tid] = tid < len ? ld(Bg, (size_t)(t0 + tid) * H + h) : 0.f;
@@ -266,9 +296,18 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         const long long t0 = bos + (long long)c * C;
         const int len = (int)min((long long)C, eos - t0);
         __syncthreads();
-        {
+        if (c == nc - 1) {  // later chunks' start states arrive by cp.async during the chunk after them
             const float *src = ck_at(c);
             for (int e = tid; e < D * D; e += NT) S[(e / D) * LS + e % D] = src[e];
+        } else {
+            cp_async_wait();
+        }
+        if (c > 0) {  // the previous chunk's rows into L2
+            const long long tp = t0 - C;
+            prefetch_rows(Kg, tp, C, H, h, 0);
+            prefetch_rows(Qg, tp, C, H, h, 1);
+            prefetch_rows(Vg, tp, C, H, h, 2);
+            prefetch_rows(DOg, tp, C, H, h, 3);
         }
         load_tile(sm + O_DU, Kg, t0, len, H, h);  // K, until the factors are formed
         load_tile(sm + O_QP, Qg, t0, len, H, h);
@@ -400,6 +439,10 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
             atomicAdd(&sm[O_DGC + i], colsum + (r0 == 0 ? dgc * gc : 0.f));
         }
         __syncthreads();
+        if (c > 0) {  // S is read no more in this chunk: fetch the previous chunk's start state
+            const float *src = ck_at(c - 1);
+            for (int e = tid; e < D * D; e += NT) cp_async4(S + (e / D) * LS + e % D, src + e);
+        }
         // dg = reverse cumsum of dGam over the chunk's rows (the last row of the chunk, len - 1 for
         // a short final chunk, also takes the gC terms).
         if (tid < D) {
