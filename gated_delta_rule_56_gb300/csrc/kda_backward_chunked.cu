@@ -91,27 +91,42 @@ __device__ __forceinline__ void prefetch_rows(const Tin *src, long long t0, int 
 }
 __device__ __forceinline__ float ld(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
 
-// Load the chunk's rows [t0, t0 + n) of a [rows, H, D] tensor into a C x LT tile (rows past n = 0).
-template <typename Tin>
-__device__ __forceinline__ void load_tile(float *tile, const Tin *src, long long t0, int n, int H, int h) {
-    for (int e = threadIdx.x; e < C * D; e += NT) {
-        const int r = e / D, i = e % D;
-        tile[r * LT + i] = r < n ? ld(src, ((size_t)(t0 + r) * H + h) * D + i) : 0.f;
-    }
-}
-
-// gam = exp(cumsum g) per channel over the chunk (rows past n: g = 0), gC = its last row.
-template <typename Tin>
-__device__ __forceinline__ void gate_tile(float *sm, const Tin *g, long long t0, int n, int H, int h) {
+// gam = exp(cumsum g) per channel over the chunk from the staged g tile (rows past n hold 0),
+// gC = its last row.
+__device__ __forceinline__ void gate_tile(float *sm, const float *gt) {
     if (threadIdx.x < D) {
         const int i = threadIdx.x;
         float G = 0.f;
+#pragma unroll
         for (int r = 0; r < C; ++r) {
-            if (r < n) G += ld(g, ((size_t)(t0 + r) * H + h) * D + i);
+            G += gt[r * LT + i];
             sm[O_GAM + r * LT + i] = __expf(fminf(fmaxf(G, -87.f), 87.f));
         }
         sm[O_GC + i] = sm[O_GAM + (C - 1) * LT + i];
     }
+}
+
+// Stage up to five [rows, H, D] tensors' chunk rows [t0, t0 + n) into C x LT tiles (rows past n
+// = 0): every load of the thread is issued before any store, so their latencies overlap.
+template <typename Tin, int NTEN>
+__device__ __forceinline__ void load_tiles(float *const (&dst)[NTEN], const Tin *const (&src)[NTEN], long long t0,
+                                           int n, int H, int h) {
+    constexpr int PER = C * D / NT;  // elements per thread per tensor
+    float v[NTEN][PER];
+#pragma unroll
+    for (int a = 0; a < NTEN; ++a)
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            const int e = threadIdx.x + q * NT, r = e / D, i = e % D;
+            v[a][q] = r < n ? ld(src[a], ((size_t)(t0 + r) * H + h) * D + i) : 0.f;
+        }
+#pragma unroll
+    for (int a = 0; a < NTEN; ++a)
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            const int e = threadIdx.x + q * NT, r = e / D, i = e % D;
+            dst[a][r * LT + i] = v[a][q];
+        }
 }
 
 // out[r][j] (16 x 128) = sum_i a[r][i] * B[i][j] with B 128 x 128 at row stride LS; thread t
@@ -258,10 +273,14 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
             prefetch_rows(Vg, t1, l1, H, h, 1);
             prefetch_rows(Gg, t1, l1, H, h, 2);
         }
-        load_tile(sm + O_DU, Kg, t0, len, H, h);  // K in the dU tile (free in the forward sweep)
-        load_tile(sm + O_R, Vg, t0, len, H, h);
+        {  // K in the dU tile and g in the dG tile (both free in the forward sweep), V in the R tile
+            float *const dst[3] = {sm + O_DU, sm + O_R, sm + O_DG};
+            const Tin *const src[3] = {Kg, Vg, Gg};
+            load_tiles<Tin, 3>(dst, src, t0, len, H, h);
+        }
         if (tid < C) sm[O_BETA + tid] = tid < len ? ld(Bg, (size_t)(t0 + tid) * H + h) : 0.f;
-        gate_tile(sm, Gg, t0, len, H, h);
+        __syncthreads();
+        gate_tile(sm, sm + O_DG);
         __syncthreads();
         chunk_factors(sm, sm + O_DU, false);
         chunk_u(sm);
@@ -308,14 +327,17 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
             prefetch_rows(Qg, tp, C, H, h, 1);
             prefetch_rows(Vg, tp, C, H, h, 2);
             prefetch_rows(DOg, tp, C, H, h, 3);
+            prefetch_rows(Gg, tp, C, H, h, 4);
         }
-        load_tile(sm + O_DU, Kg, t0, len, H, h);  // K, until the factors are formed
-        load_tile(sm + O_QP, Qg, t0, len, H, h);
-        load_tile(sm + O_R, Vg, t0, len, H, h);
-        load_tile(sm + O_DO, DOg, t0, len, H, h);
+        {  // K in the dU tile until the factors are formed, g in the dG tile until gam is formed
+            float *const dst[5] = {sm + O_DU, sm + O_QP, sm + O_R, sm + O_DO, sm + O_DG};
+            const Tin *const src[5] = {Kg, Qg, Vg, DOg, Gg};
+            load_tiles<Tin, 5>(dst, src, t0, len, H, h);
+        }
         if (tid < C) sm[O_BETA + tid] = tid < len ? ld(Bg, (size_t)(t0 + tid) * H + h) : 0.f;
         if (tid < D) sm[O_DGC + tid] = 0.f;
-        gate_tile(sm, Gg, t0, len, H, h);
+        __syncthreads();
+        gate_tile(sm, sm + O_DG);
         __syncthreads();
         chunk_factors(sm, sm + O_DU, true);
         chunk_u(sm);
