@@ -34,7 +34,7 @@ constexpr int C = 16;                  // tokens per chunk
 constexpr int NT = 512;                // threads per CTA
 constexpr int LS = D + 1;              // row stride of S and dS (floats)
 constexpr int LT = D + 4;              // row stride of a 16 x 128 tile (floats; 16-byte rows)
-constexpr int LM = C + 1;              // row stride of a 16 x 16 matrix
+constexpr int LM = C + 4;              // row stride of a 16 x 16 matrix (16-byte rows)
 
 // Shared-memory layout (floats).
 constexpr int O_S = 0;
@@ -57,7 +57,8 @@ constexpr int O_DP = O_P + C * LM;
 constexpr int O_DT = O_DP + C * LM;
 constexpr int O_DAB = O_DT + C * LM;   // Diag(beta) dA
 constexpr int O_M = O_DAB + C * LM;    // scratch 16 x 16
-constexpr int O_BETA = O_M + C * LM;   // [C]
+constexpr int O_TT = O_M + C * LM;     // T transposed
+constexpr int O_BETA = O_TT + C * LM;  // [C]
 constexpr int O_DB = O_BETA + C;       // [C] dbeta
 constexpr int O_GC = O_DB + C;         // [D] gC
 constexpr int O_DGC = O_GC + D;        // [D] dgC gC + colsum(dKc Kc)
@@ -163,13 +164,16 @@ __device__ __forceinline__ void tile_times_tile_t(float *M, const float *a, cons
     if (half == 0) M[r * LM + s] = acc;
 }
 
-// The chunk's gate products and triangular factors: Kp, Km, (Qp), Ab, A -> X, T, (P).
-__device__ __forceinline__ void chunk_factors(float *sm, const float *K, bool with_q) {
+// The chunk's gate products and triangular factors: Kp, Km, Kc (into the tile `kc`), (Qp), Ab,
+// A -> X, T (and T transposed), (P).
+__device__ __forceinline__ void chunk_factors(float *sm, const float *K, float *kc, bool with_q) {
     for (int e = threadIdx.x; e < C * D; e += NT) {
         const int r = e / D, i = e % D;
         const float gm = sm[O_GAM + r * LT + i], k = K[r * LT + i];
+        const float km = __fdividef(k, gm);
         sm[O_KP + r * LT + i] = k * gm;
-        sm[O_KM + r * LT + i] = __fdividef(k, gm);
+        sm[O_KM + r * LT + i] = km;
+        kc[r * LT + i] = km * sm[O_GC + i];
         if (with_q) sm[O_QP + r * LT + i] *= gm;  // Q was loaded into the Qp tile
     }
     __syncthreads();
@@ -200,6 +204,7 @@ __device__ __forceinline__ void chunk_factors(float *sm, const float *K, bool wi
         for (int i = 0; i < C; ++i) {
             sm[O_X + i * LM + j] = x[i];
             sm[O_T + i * LM + j] = x[i] * bj;
+            sm[O_TT + j * LM + i] = x[i] * bj;
         }
     }
     if (with_q) {  // P = lower(Qp Km^T)
@@ -220,12 +225,20 @@ __device__ __forceinline__ void chunk_u(float *sm) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) sm[O_R + (r0 + q) * LT + j] -= acc[q];
     __syncthreads();
-    for (int e = threadIdx.x; e < C * D; e += NT) {
-        const int r = e / D, i = e % D;
-        float u = 0.f;
+    {  // U[r][i] = sum_s T[r][s] R[s][i]: thread takes channel i and rows r0 .. r0 + 3
+        const int i = threadIdx.x % D, r0 = 4 * (threadIdx.x / D);
+        float u[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int s = 0; s < C; ++s) u = fmaf(sm[O_T + r * LM + s], sm[O_R + s * LT + i], u);
-        sm[O_U + r * LT + i] = u;
+        for (int s = 0; s < C; ++s) {
+            const float rs = sm[O_R + s * LT + i];
+            const float4 t = *reinterpret_cast<const float4 *>(sm + O_TT + s * LM + r0);
+            u[0] = fmaf(t.x, rs, u[0]);
+            u[1] = fmaf(t.y, rs, u[1]);
+            u[2] = fmaf(t.z, rs, u[2]);
+            u[3] = fmaf(t.w, rs, u[3]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sm[O_U + (r0 + q) * LT + i] = u[q];
     }
     __syncthreads();
 }
@@ -282,9 +295,9 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         __syncthreads();
         gate_tile(sm, sm + O_DG);
         __syncthreads();
-        chunk_factors(sm, sm + O_DU, false);
+        chunk_factors(sm, sm + O_DU, sm + O_DR, false);
         chunk_u(sm);
-        // S <- Diag(gC) S + Kc^T U, Kc = Km gC: thread takes column j, rows 32 (t / 128) .. + 31.
+        // S <- Diag(gC) S + Kc^T U (Kc in the dR tile): thread takes column j, rows 32 (t / 128) .. + 31.
         {
             const int j = tid % D, i0 = 32 * (tid / D);
             float acc[32];
@@ -295,11 +308,11 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
                 const float u = sm[O_U + r * LT + j];
 #pragma unroll
                 for (int q = 0; q < 32; q += 4) {
-                    const float4 km = *reinterpret_cast<const float4 *>(sm + O_KM + r * LT + i0 + q);
-                    acc[q + 0] = fmaf(km.x * sm[O_GC + i0 + q + 0], u, acc[q + 0]);
-                    acc[q + 1] = fmaf(km.y * sm[O_GC + i0 + q + 1], u, acc[q + 1]);
-                    acc[q + 2] = fmaf(km.z * sm[O_GC + i0 + q + 2], u, acc[q + 2]);
-                    acc[q + 3] = fmaf(km.w * sm[O_GC + i0 + q + 3], u, acc[q + 3]);
+                    const float4 kc = *reinterpret_cast<const float4 *>(sm + O_DR + r * LT + i0 + q);
+                    acc[q + 0] = fmaf(kc.x, u, acc[q + 0]);
+                    acc[q + 1] = fmaf(kc.y, u, acc[q + 1]);
+                    acc[q + 2] = fmaf(kc.z, u, acc[q + 2]);
+                    acc[q + 3] = fmaf(kc.w, u, acc[q + 3]);
                 }
             }
             __syncthreads();
@@ -339,37 +352,45 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         __syncthreads();
         gate_tile(sm, sm + O_DG);
         __syncthreads();
-        chunk_factors(sm, sm + O_DU, true);
+        chunk_factors(sm, sm + O_DU, sm + O_DG, true);  // Kc in the dG tile until dGam is formed
         chunk_u(sm);
-        // dU = P^T dO + Kc dS  (Kc dS = Diag-free: Kc[r][i] = Km[r][i] gC[i])
+        // dU = P^T dO + Kc dS
         {
             const int j = tid % D, r0 = 4 * (tid / D);
             float acc[4];
+            tile_times_state(acc, sm + O_DG, dS);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[q] = 0.f;
-#pragma unroll 4
-            for (int i = 0; i < D; ++i) {
-                const float b = dS[i * LS + j] * sm[O_GC + i];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[q] = fmaf(sm[O_KM + (r0 + q) * LT + i], b, acc[q]);
+            for (int s = 0; s < C; ++s) {
+                const float o = sm[O_DO + s * LT + j];
+                const float4 pr = *reinterpret_cast<const float4 *>(sm + O_P + s * LM + r0);
+                acc[0] = fmaf(pr.x, o, acc[0]);
+                acc[1] = fmaf(pr.y, o, acc[1]);
+                acc[2] = fmaf(pr.z, o, acc[2]);
+                acc[3] = fmaf(pr.w, o, acc[3]);
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float x = acc[q];
-#pragma unroll
-                for (int s = 0; s < C; ++s) x = fmaf(sm[O_P + s * LM + r0 + q], sm[O_DO + s * LT + j], x);
-                sm[O_DU + (r0 + q) * LT + j] = x;
-            }
+            for (int q = 0; q < 4; ++q) sm[O_DU + (r0 + q) * LT + j] = acc[q];
         }
         __syncthreads();
         // dR = T^T dU (= dV, stored), dP = lower(dO U^T), dT = dU R^T
-        for (int e = tid; e < C * D; e += NT) {
-            const int r = e / D, i = e % D;
-            float x = 0.f;
+        {  // dR[r][i] = sum_s T[s][r] dU[s][i]: thread takes channel i and rows r0 .. r0 + 3
+            const int i = tid % D, r0 = 4 * (tid / D);
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int s = 0; s < C; ++s) x = fmaf(sm[O_T + s * LM + r], sm[O_DU + s * LT + i], x);
-            sm[O_DR + r * LT + i] = x;
-            if (r < len) dv[((size_t)(t0 + r) * H + h) * D + i] = x;
+            for (int s = 0; s < C; ++s) {
+                const float du = sm[O_DU + s * LT + i];
+                const float4 t = *reinterpret_cast<const float4 *>(sm + O_T + s * LM + r0);
+                x[0] = fmaf(t.x, du, x[0]);
+                x[1] = fmaf(t.y, du, x[1]);
+                x[2] = fmaf(t.z, du, x[2]);
+                x[3] = fmaf(t.w, du, x[3]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int r = r0 + q;
+                sm[O_DR + r * LT + i] = x[q];
+                if (r < len) dv[((size_t)(t0 + r) * H + h) * D + i] = x[q];
+            }
         }
         tile_times_tile_t(sm + O_DP, sm + O_DO, sm + O_U);
         __syncthreads();
