@@ -157,7 +157,8 @@ KDA_API kda_status kda_decode_step_ex(kda_dtype dtype, int N, int H, int dk, int
  * kda_backward -- gradients of L = sum(d_o * o) + sum(d_final_state * final_state) through
  * kda_prefill's computation (plain log-decays; no options), on CUDA cores in fp32. The pages
  * train the model ("Kimi K3 Explained", researchpapers.dev, "Architecture at a glance") but give
- * no gradient method: this is reverse-mode differentiation of the token recurrence.
+ * no gradient method: this is reverse-mode differentiation of the recurrence (for d = 128 taken
+ * of its chunkwise form on 16-token chunks; the result is the same up to rounding).
  *
  * dtype, B, T, H, dk, dv, q, k, v, g, beta, cu_seqlens, n_seqs, initial_state: as kda_prefill.
  * d_o          [B, T, H, dv] in `dtype`: dL/do.
@@ -167,7 +168,8 @@ KDA_API kda_status kda_decode_step_ex(kda_dtype dtype, int N, int H, int dk, int
  * d_initial_state  fp32 [N, H, dk, dv] or NULL (not written): dL/dS_initial (also without an
  *              initial state: the gradient at the zero state).
  * workspace    device scratch of at least kda_backward_workspace_size() bytes, 16-byte aligned,
- *              owned by the caller (state checkpoints every 64 tokens, 64 KiB per head for d=128).
+ *              owned by the caller: the state at every chunk start (every 16 tokens for d = 128,
+ *              every 64 for d = 32, 64), d * d * 4 bytes per head and chunk.
  * Supported: dk == dv in {32, 64, 128}; bf16 or fp32 inputs. Alignment as kda_prefill.
  */
 KDA_API kda_status kda_backward(kda_dtype dtype, int B, int T, int H, int dk, int dv,
