@@ -20,7 +20,7 @@
 // no sub-tiling; each exponent is clamped to +-87 so out-of-range gates stay finite.
 //
 // One CTA of 512 threads per (sequence, head) holds S and dS (fp32, 128 x 128, rows padded to
-// 129 floats so that both row and column reads are free of bank conflicts) and the chunk's
+// 132 floats so that both column reads and 16-byte row reads are free of bank conflicts) and the chunk's
 // 16 x 128 tiles in shared memory; every product runs on the CUDA cores in fp32. A forward sweep
 // stores the state at every chunk start in the workspace; the reverse sweep reads it back.
 // All columns live in one CTA, so every gradient is written directly (no atomics).
@@ -32,7 +32,10 @@ namespace {
 constexpr int D = 128;
 constexpr int C = 16;                  // tokens per chunk
 constexpr int NT = 512;                // threads per CTA
-constexpr int LS = D + 1;              // row stride of S and dS (floats)
+constexpr int LS = D + 4;              // row stride of S and dS (floats): 16-byte rows, and row i
+                                       // starts 33 i 16-byte units in (i mod 8 distinct), so both
+                                       // column reads and 16-byte row reads across rows are free of
+                                       // bank conflicts
 constexpr int LT = D + 4;              // row stride of a 16 x 128 tile (floats; 16-byte rows)
 constexpr int LM = C + 4;              // row stride of a 16 x 16 matrix (16-byte rows)
 
@@ -68,10 +71,10 @@ static_assert(SMEM <= 232448, "shared memory budget");
 
 __device__ __forceinline__ float ld(const float *p, size_t i) { return __ldg(p + i); }
 
-// 4-byte asynchronous copies global -> shared (the destination rows are 129 floats apart, so
-// 16-byte copies would not be aligned); the thread waits for all of its own with cp_async_wait.
-__device__ __forceinline__ void cp_async4(float *dst, const float *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+// 16-byte asynchronous copies global -> shared; the thread waits for all of its own with
+// cp_async_wait.
+__device__ __forceinline__ void cp_async16(float *dst, const float *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
                  "l"(src)
                  : "memory");
 }
@@ -435,12 +438,9 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
             float dgc = 0.f;
 #pragma unroll 2
             for (int j = 0; j < D; j += 4) {
-                float s4[4], ds4[4];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    s4[m] = S[i * LS + j + m];
-                    ds4[m] = dS[i * LS + j + m];
-                }
+                const float4 sv = *reinterpret_cast<const float4 *>(S + i * LS + j);
+                const float4 dsv = *reinterpret_cast<const float4 *>(dS + i * LS + j);
+                const float s4[4] = {sv.x, sv.y, sv.z, sv.w}, ds4[4] = {dsv.x, dsv.y, dsv.z, dsv.w};
                 if (r0 == 0) dgc = fmaf(ds4[0], s4[0], fmaf(ds4[1], s4[1], fmaf(ds4[2], s4[2], fmaf(ds4[3], s4[3], dgc))));
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         __syncthreads();
         if (c > 0) {  // S is read no more in this chunk: fetch the previous chunk's start state
             const float *src = ck_at(c - 1);
-            for (int e = tid; e < D * D; e += NT) cp_async4(S + (e / D) * LS + e % D, src + e);
+            for (int e = 4 * tid; e < D * D; e += 4 * NT) cp_async16(S + (e / D) * LS + e % D, src + e);
         }
         // dg = reverse cumsum of dGam over the chunk's rows (the last row of the chunk, len - 1 for
         // a short final chunk, also takes the gC terms).
