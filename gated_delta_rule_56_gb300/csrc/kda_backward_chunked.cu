@@ -21,7 +21,8 @@
 //
 // One CTA of 512 threads per (sequence, head) holds S and dS (fp32, 128 x 128, rows padded to
 // 132 floats so that both column reads and 16-byte row reads are free of bank conflicts) and the chunk's
-// 16 x 128 tiles in shared memory; every product runs on the CUDA cores in fp32. A forward sweep
+// 16 x 128 tiles in shared memory; the large products run on the tensor cores (3 x tf32, see
+// mma3), the small ones and the element-wise steps on the CUDA cores in fp32. A forward sweep
 // stores the state at every chunk start in the workspace; the reverse sweep reads it back.
 // All columns live in one CTA, so every gradient is written directly (no atomics).
 #include "kda_internal.h"
@@ -133,21 +134,46 @@ __device__ __forceinline__ void load_tiles(float *const (&dst)[NTEN], const Tin 
         }
 }
 
-// out[r][j] (16 x 128) = sum_i a[r][i] * B[i][j] with B 128 x 128 at row stride LS; thread t
-// takes column j = t % 128 and rows 4 (t / 128) .. + 3.
-__device__ __forceinline__ void tile_times_state(float (&acc)[4], const float *a, const float *B) {
-    const int j = threadIdx.x % D, r0 = 4 * (threadIdx.x / D);
+// ---- products on the tensor cores: warp-level mma.sync m16n8k8 with tf32 operands. Every fp32
+// operand x is split into a tf32 high part and the tf32 rounding of the rest, and a product is
+// taken as lo*hi + hi*lo + hi*hi (the lo*lo term is below fp32 rounding), so the result keeps
+// fp32 accuracy. Fragment of lane l (g = l / 4, t = l % 4): A (16 x 8) rows g, g + 8 and columns
+// t, t + 4; B (8 x 8) rows t, t + 4 and column g; C (16 x 8) rows g, g + 8, columns 2t, 2t + 1.
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(x - __uint_as_float(hi)));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// c += a b for fp32 fragments a (A layout) and b (B layout).
+__device__ __forceinline__ void mma3(float (&c)[4], const float (&a)[4], const float (&b)[2]) {
+    uint32_t ah[4], al[4], bh[2], bl[2];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q] = 0.f;
+    for (int q = 0; q < 4; ++q) split_tf32(a[q], ah[q], al[q]);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) split_tf32(b[q], bh[q], bl[q]);
+    mma_tf32(c, al, bh);
+    mma_tf32(c, ah, bl);
+    mma_tf32(c, ah, bh);
+}
+
+// c (rows g, g + 8 x columns n0 + 2t, + 1 of a 16 x 128 result) = a (16 x 128 tile) B (128 x 128
+// at row stride LS), for the warp's 8 columns n0 .. n0 + 7.
+__device__ __forceinline__ void tile_times_state(float (&c)[4], const float *a, const float *B, int n0) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c[q] = 0.f;
 #pragma unroll 4
-    for (int i = 0; i < D; i += 4) {
-        const float b0 = B[(i + 0) * LS + j], b1 = B[(i + 1) * LS + j];
-        const float b2 = B[(i + 2) * LS + j], b3 = B[(i + 3) * LS + j];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 x = *reinterpret_cast<const float4 *>(a + (r0 + q) * LT + i);
-            acc[q] = fmaf(x.x, b0, fmaf(x.y, b1, fmaf(x.z, b2, fmaf(x.w, b3, acc[q]))));
-        }
+    for (int k = 0; k < D; k += 8) {
+        const float af[4] = {a[g * LT + k + t], a[(g + 8) * LT + k + t], a[g * LT + k + t + 4], a[(g + 8) * LT + k + t + 4]};
+        const float bf[2] = {B[(k + t) * LS + n0 + g], B[(k + t + 4) * LS + n0 + g]};
+        mma3(c, af, bf);
     }
 }
 
@@ -219,14 +245,18 @@ __device__ __forceinline__ void chunk_factors(float *sm, const float *K, float *
     __syncthreads();
 }
 
-// R = V - Kp S (in the R tile, which holds V), then U = T R.
+// R = V - Kp S (in the R tile, which holds V; warp w takes columns 8 w .. + 7), then U = T R.
 __device__ __forceinline__ void chunk_u(float *sm) {
-    float acc[4];
-    tile_times_state(acc, sm + O_KP, sm + O_S);
-    const int j = threadIdx.x % D, r0 = 4 * (threadIdx.x / D);
-    __syncthreads();
-#pragma unroll
-    for (int q = 0; q < 4; ++q) sm[O_R + (r0 + q) * LT + j] -= acc[q];
+    {
+        const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, n0 = 8 * (threadIdx.x >> 5);
+        float c[4];
+        tile_times_state(c, sm + O_KP, sm + O_S, n0);
+        float *R = sm + O_R;
+        R[g * LT + n0 + 2 * t] -= c[0];
+        R[g * LT + n0 + 2 * t + 1] -= c[1];
+        R[(g + 8) * LT + n0 + 2 * t] -= c[2];
+        R[(g + 8) * LT + n0 + 2 * t + 1] -= c[3];
+    }
     __syncthreads();
     {  // U[r][i] = sum_s T[r][s] R[s][i]: thread takes channel i and rows r0 .. r0 + 3
         const int i = threadIdx.x % D, r0 = 4 * (threadIdx.x / D);
@@ -244,6 +274,51 @@ __device__ __forceinline__ void chunk_u(float *sm) {
         for (int q = 0; q < 4; ++q) sm[O_U + (r0 + q) * LT + i] = u[q];
     }
     __syncthreads();
+}
+
+// X (128 x 128, row stride LS) <- Diag(gC) X + A1^T B1 + A2^T B2 for 16 x 128 tiles A1, B1, A2, B2
+// (A2 may be null). Warp w takes rows 16 (w / 2) .. + 15 and columns 64 (w % 2) .. + 63; every
+// element of X is read and written by the one thread holding it.
+__device__ __forceinline__ void state_update(float *X, const float *gc, const float *A1, const float *B1,
+                                             const float *A2, const float *B2) {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int m0 = 16 * (w >> 1), nb0 = 64 * (w & 1);
+    float af1[2][4], af2[2][4];
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {  // the A fragments (k = token rows 8 ks ..) of this row block
+        const int k = 8 * ks;
+        af1[ks][0] = A1[(k + t) * LT + m0 + g];
+        af1[ks][1] = A1[(k + t) * LT + m0 + g + 8];
+        af1[ks][2] = A1[(k + t + 4) * LT + m0 + g];
+        af1[ks][3] = A1[(k + t + 4) * LT + m0 + g + 8];
+        if (A2) {
+            af2[ks][0] = A2[(k + t) * LT + m0 + g];
+            af2[ks][1] = A2[(k + t) * LT + m0 + g + 8];
+            af2[ks][2] = A2[(k + t + 4) * LT + m0 + g];
+            af2[ks][3] = A2[(k + t + 4) * LT + m0 + g + 8];
+        }
+    }
+    const float g0 = gc[m0 + g], g8 = gc[m0 + g + 8];
+#pragma unroll 2
+    for (int nb = 0; nb < 64; nb += 8) {
+        const int n = nb0 + nb;
+        float *x0 = X + (m0 + g) * LS + n + 2 * t, *x8 = X + (m0 + g + 8) * LS + n + 2 * t;
+        float c[4] = {x0[0] * g0, x0[1] * g0, x8[0] * g8, x8[1] * g8};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            const int k = 8 * ks;
+            const float b1[2] = {B1[(k + t) * LT + n + g], B1[(k + t + 4) * LT + n + g]};
+            mma3(c, af1[ks], b1);
+            if (A2) {
+                const float b2[2] = {B2[(k + t) * LT + n + g], B2[(k + t + 4) * LT + n + g]};
+                mma3(c, af2[ks], b2);
+            }
+        }
+        x0[0] = c[0];
+        x0[1] = c[1];
+        x8[0] = c[2];
+        x8[1] = c[3];
+    }
 }
 
 template <typename Tin>
@@ -300,28 +375,8 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         __syncthreads();
         chunk_factors(sm, sm + O_DU, sm + O_DR, false);
         chunk_u(sm);
-        // S <- Diag(gC) S + Kc^T U (Kc in the dR tile): thread takes column j, rows 32 (t / 128) .. + 31.
-        {
-            const int j = tid % D, i0 = 32 * (tid / D);
-            float acc[32];
-#pragma unroll
-            for (int q = 0; q < 32; ++q) acc[q] = S[(i0 + q) * LS + j] * sm[O_GC + i0 + q];
-#pragma unroll 2
-            for (int r = 0; r < C; ++r) {
-                const float u = sm[O_U + r * LT + j];
-#pragma unroll
-                for (int q = 0; q < 32; q += 4) {
-                    const float4 kc = *reinterpret_cast<const float4 *>(sm + O_DR + r * LT + i0 + q);
-                    acc[q + 0] = fmaf(kc.x, u, acc[q + 0]);
-                    acc[q + 1] = fmaf(kc.y, u, acc[q + 1]);
-                    acc[q + 2] = fmaf(kc.z, u, acc[q + 2]);
-                    acc[q + 3] = fmaf(kc.w, u, acc[q + 3]);
-                }
-            }
-            __syncthreads();
-#pragma unroll
-            for (int q = 0; q < 32; ++q) S[(i0 + q) * LS + j] = acc[q];
-        }
+        // S <- Diag(gC) S + Kc^T U (Kc in the dR tile)
+        state_update(S, sm + O_GC, sm + O_DR, sm + O_U, nullptr, nullptr);
         __syncthreads();
     }
 
@@ -357,22 +412,23 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         __syncthreads();
         chunk_factors(sm, sm + O_DU, sm + O_DG, true);  // Kc in the dG tile until dGam is formed
         chunk_u(sm);
-        // dU = P^T dO + Kc dS
+        // dU = Kc dS + P^T dO (warp w: columns 8 w .. + 7)
         {
-            const int j = tid % D, r0 = 4 * (tid / D);
-            float acc[4];
-            tile_times_state(acc, sm + O_DG, dS);
+            const int lane = tid & 31, g = lane >> 2, t = lane & 3, n0 = 8 * (tid >> 5);
+            float c[4];
+            tile_times_state(c, sm + O_DG, dS, n0);
 #pragma unroll
-            for (int s = 0; s < C; ++s) {
-                const float o = sm[O_DO + s * LT + j];
-                const float4 pr = *reinterpret_cast<const float4 *>(sm + O_P + s * LM + r0);
-                acc[0] = fmaf(pr.x, o, acc[0]);
-                acc[1] = fmaf(pr.y, o, acc[1]);
-                acc[2] = fmaf(pr.z, o, acc[2]);
-                acc[3] = fmaf(pr.w, o, acc[3]);
+            for (int k = 0; k < C; k += 8) {  // P^T (16 x 16) dO (16 x 128)
+                const float af[4] = {sm[O_P + (k + t) * LM + g], sm[O_P + (k + t) * LM + g + 8],
+                                     sm[O_P + (k + t + 4) * LM + g], sm[O_P + (k + t + 4) * LM + g + 8]};
+                const float bf[2] = {sm[O_DO + (k + t) * LT + n0 + g], sm[O_DO + (k + t + 4) * LT + n0 + g]};
+                mma3(c, af, bf);
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) sm[O_DU + (r0 + q) * LT + j] = acc[q];
+            float *dU = sm + O_DU;
+            dU[g * LT + n0 + 2 * t] = c[0];
+            dU[g * LT + n0 + 2 * t + 1] = c[1];
+            dU[(g + 8) * LT + n0 + 2 * t] = c[2];
+            dU[(g + 8) * LT + n0 + 2 * t + 1] = c[3];
         }
         __syncthreads();
         // dR = T^T dU (= dV, stored), dP = lower(dO U^T), dT = dU R^T
@@ -428,36 +484,57 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
             for (int s = 0; s < C; ++s) x += sm[O_P + j * LM + s];
             if (j < len) dbeta[(size_t)(t0 + j) * H + h] = x;
         }
-        // Per (r, i): dQp, dKp, dKm, dKc -> dq, dk and dGam. Thread: channel i = t % 128, rows
-        // 4 (t / 128) .. + 3.
+        // dO S^T, dR S^T and U dS^T (16 x 128 each; warp w: channels 8 w .. + 7), then, with S and
+        // dS read no more, into the R, dU and U tiles.
+        {
+            const int lane = tid & 31, g = lane >> 2, t = lane & 3, n0 = 8 * (tid >> 5);
+            float cq[4] = {0.f, 0.f, 0.f, 0.f}, ckp[4] = {0.f, 0.f, 0.f, 0.f}, cc[4] = {0.f, 0.f, 0.f, 0.f};
+            const float *dO = sm + O_DO, *dR = sm + O_DR, *U = sm + O_U;
+#pragma unroll 2
+            for (int k = 0; k < D; k += 8) {
+                const float bs[2] = {S[(n0 + g) * LS + k + t], S[(n0 + g) * LS + k + t + 4]};
+                const float bd[2] = {dS[(n0 + g) * LS + k + t], dS[(n0 + g) * LS + k + t + 4]};
+                const float ao[4] = {dO[g * LT + k + t], dO[(g + 8) * LT + k + t], dO[g * LT + k + t + 4],
+                                     dO[(g + 8) * LT + k + t + 4]};
+                const float ar[4] = {dR[g * LT + k + t], dR[(g + 8) * LT + k + t], dR[g * LT + k + t + 4],
+                                     dR[(g + 8) * LT + k + t + 4]};
+                const float au[4] = {U[g * LT + k + t], U[(g + 8) * LT + k + t], U[g * LT + k + t + 4],
+                                     U[(g + 8) * LT + k + t + 4]};
+                mma3(cq, ao, bs);
+                mma3(ckp, ar, bs);
+                mma3(cc, au, bd);
+            }
+            if (tid < D) {  // dgC = rowsum(dS * S) for channel tid
+                float dgc = 0.f;
+                for (int j = 0; j < D; j += 4) {
+                    const float4 sv = *reinterpret_cast<const float4 *>(S + tid * LS + j);
+                    const float4 dsv = *reinterpret_cast<const float4 *>(dS + tid * LS + j);
+                    dgc = fmaf(dsv.x, sv.x, fmaf(dsv.y, sv.y, fmaf(dsv.z, sv.z, fmaf(dsv.w, sv.w, dgc))));
+                }
+                atomicAdd(&sm[O_DGC + tid], dgc * sm[O_GC + tid]);
+            }
+            __syncthreads();  // every warp is done with dO, dR and U as operands
+            float *T1 = sm + O_R, *T2 = sm + O_DU, *T3 = sm + O_U;
+            const int e0 = g * LT + n0 + 2 * t, e8 = (g + 8) * LT + n0 + 2 * t;
+            T1[e0] = cq[0]; T1[e0 + 1] = cq[1]; T1[e8] = cq[2]; T1[e8 + 1] = cq[3];
+            T2[e0] = ckp[0]; T2[e0 + 1] = ckp[1]; T2[e8] = ckp[2]; T2[e8 + 1] = ckp[3];
+            T3[e0] = cc[0]; T3[e0 + 1] = cc[1]; T3[e8] = cc[2]; T3[e8 + 1] = cc[3];
+        }
+        __syncthreads();
+        if (c > 0) {  // S is read no more in this chunk: fetch the previous chunk's start state
+            const float *src = ck_at(c - 1);
+            for (int e = 4 * tid; e < D * D; e += 4 * NT) cp_async16(S + (e / D) * LS + e % D, src + e);
+        }
+        // Per (r, i): dQp, dKp, dKm, dKc -> dq, dk and dGam (thread: channel i = t % 128, rows
+        // 4 (t / 128) .. + 3).
         {
             const int i = tid % D, r0 = 4 * (tid / D);
-            float aq[4], ak[4], ac[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) aq[q] = ak[q] = ac[q] = 0.f;
-            float dgc = 0.f;
-#pragma unroll 2
-            for (int j = 0; j < D; j += 4) {
-                const float4 sv = *reinterpret_cast<const float4 *>(S + i * LS + j);
-                const float4 dsv = *reinterpret_cast<const float4 *>(dS + i * LS + j);
-                const float s4[4] = {sv.x, sv.y, sv.z, sv.w}, ds4[4] = {dsv.x, dsv.y, dsv.z, dsv.w};
-                if (r0 == 0) dgc = fmaf(ds4[0], s4[0], fmaf(ds4[1], s4[1], fmaf(ds4[2], s4[2], fmaf(ds4[3], s4[3], dgc))));
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 o = *reinterpret_cast<const float4 *>(sm + O_DO + (r0 + q) * LT + j);
-                    const float4 rr = *reinterpret_cast<const float4 *>(sm + O_DR + (r0 + q) * LT + j);
-                    const float4 u = *reinterpret_cast<const float4 *>(sm + O_U + (r0 + q) * LT + j);
-                    aq[q] = fmaf(o.x, s4[0], fmaf(o.y, s4[1], fmaf(o.z, s4[2], fmaf(o.w, s4[3], aq[q]))));
-                    ak[q] = fmaf(rr.x, s4[0], fmaf(rr.y, s4[1], fmaf(rr.z, s4[2], fmaf(rr.w, s4[3], ak[q]))));
-                    ac[q] = fmaf(u.x, ds4[0], fmaf(u.y, ds4[1], fmaf(u.z, ds4[2], fmaf(u.w, ds4[3], ac[q]))));
-                }
-            }
             const float gc = sm[O_GC + i];
             float colsum = 0.f;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int r = r0 + q;
-                float dqp = aq[q], dkp = -ak[q], dkm = 0.f;
+                float dqp = sm[O_R + r * LT + i], dkp = -sm[O_DU + r * LT + i], dkm = 0.f;
 #pragma unroll
                 for (int s = 0; s < C; ++s) {
                     const float kms = sm[O_KM + s * LT + i];
@@ -468,7 +545,7 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
                 }
                 const float gm = sm[O_GAM + r * LT + i];
                 const float kp = sm[O_KP + r * LT + i], km = sm[O_KM + r * LT + i], qp = sm[O_QP + r * LT + i];
-                const float kc = km * gc, dkc = ac[q];
+                const float kc = km * gc, dkc = sm[O_U + r * LT + i];
                 const float dkv = dkp * gm + __fdividef(dkm, gm) + dkc * __fdividef(gc, gm);
                 const float dqv = dqp * gm;
                 sm[O_DG + r * LT + i] = dkp * kp - dkm * km + dqp * qp - dkc * kc;
@@ -479,13 +556,9 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
                     dk[o] = dkv;
                 }
             }
-            atomicAdd(&sm[O_DGC + i], colsum + (r0 == 0 ? dgc * gc : 0.f));
+            atomicAdd(&sm[O_DGC + i], colsum);
         }
         __syncthreads();
-        if (c > 0) {  // S is read no more in this chunk: fetch the previous chunk's start state
-            const float *src = ck_at(c - 1);
-            for (int e = 4 * tid; e < D * D; e += 4 * NT) cp_async16(S + (e / D) * LS + e % D, src + e);
-        }
         // dg = reverse cumsum of dGam over the chunk's rows (the last row of the chunk, len - 1 for
         // a short final chunk, also takes the gC terms).
         if (tid < D) {
@@ -498,29 +571,11 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
                 }
             }
         }
-        // dS <- Qp^T dO - Kp^T dR + Diag(gC) dS: thread takes column j, rows 32 (t / 128) .. + 31.
-        {
-            const int j = tid % D, i0 = 32 * (tid / D);
-            float acc[32];
-#pragma unroll
-            for (int q = 0; q < 32; ++q) acc[q] = dS[(i0 + q) * LS + j] * sm[O_GC + i0 + q];
-#pragma unroll 2
-            for (int r = 0; r < C; ++r) {
-                const float o = sm[O_DO + r * LT + j], rr = sm[O_DR + r * LT + j];
-#pragma unroll
-                for (int q = 0; q < 32; q += 4) {
-                    const float4 qp = *reinterpret_cast<const float4 *>(sm + O_QP + r * LT + i0 + q);
-                    const float4 kp = *reinterpret_cast<const float4 *>(sm + O_KP + r * LT + i0 + q);
-                    acc[q + 0] = fmaf(qp.x, o, fmaf(-kp.x, rr, acc[q + 0]));
-                    acc[q + 1] = fmaf(qp.y, o, fmaf(-kp.y, rr, acc[q + 1]));
-                    acc[q + 2] = fmaf(qp.z, o, fmaf(-kp.z, rr, acc[q + 2]));
-                    acc[q + 3] = fmaf(qp.w, o, fmaf(-kp.w, rr, acc[q + 3]));
-                }
-            }
-            __syncthreads();
-#pragma unroll
-            for (int q = 0; q < 32; ++q) dS[(i0 + q) * LS + j] = acc[q];
-        }
+        // dS <- Diag(gC) dS + Qp^T dO - Kp^T dR (-dR in the dG tile's place is not free: negate
+        // dR in place, it is read no more)
+        for (int e = tid; e < C * D; e += NT) sm[O_DR + (e / D) * LT + e % D] *= -1.f;
+        __syncthreads();
+        state_update(dS, sm + O_GC, sm + O_QP, sm + O_DO, sm + O_KP, sm + O_DR);
     }
     __syncthreads();
     if (d_init)
