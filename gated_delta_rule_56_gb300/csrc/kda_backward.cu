@@ -303,7 +303,10 @@ cudaError_t launch_backward(kda_dtype dtype, int d, const RunParams &p, const vo
     const long long rows = p.cu_seqlens ? (long long)p.T : (long long)p.n_seqs * p.T;
     const size_t nk = (size_t)rows * p.H * d;
     // dq, dk, dg and dbeta are sums of atomic adds: start them at zero (dv is stored directly).
-    const unsigned zb = 4 * 152;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaGetLastError();
+    const unsigned zb = 4u * (unsigned)sms;  // four 256-thread blocks per SM
     zero_kernel<<<zb, 256, 0, s>>>(dq, nk);
     zero_kernel<<<zb, 256, 0, s>>>(dk, nk);
     zero_kernel<<<zb, 256, 0, s>>>(dg, nk);

@@ -52,3 +52,14 @@ def test_backward_long_memory_across_chunks():
     x = ki.prefill_inputs(1, 300, 2, 64, 64, dtype=torch.float32, device=DEV, seed=126, state_std=0.02)
     x["g"] = x["g"] * 0.01
     _check(x, _do(x, 127), init=x["initial_state"])
+
+
+def test_backward_varlen_with_empty_sequence_and_states():
+    """A zero-length sequence passes its d_final_state straight through as d_initial_state."""
+    x = ki.varlen_inputs([33, 0, 17], 2, 128, 128, device=DEV, seed=128)
+    dfin = torch.randn(3, 2, 128, 128, device=DEV, generator=torch.Generator(device=DEV).manual_seed(129))
+    _check(x, _do(x, 130), dfin=dfin, cu=x["cu_seqlens"], init=x["initial_state"])
+    got = kda.backward(*(x[n] for n in NAMES), _do(x, 130), cu_seqlens=x["cu_seqlens"],
+                       initial_state=x["initial_state"], d_final_state=dfin)
+    kda.check_status()
+    assert torch.equal(got["d_initial_state"][1], dfin[1])

@@ -54,3 +54,20 @@ def test_noalloc_rejects_a_call_larger_than_its_scratch(lib):
     assert b"static scratch" in lib.kda_last_error()
     kda.check_status()
     assert torch.isnan(o).all(), "nothing may be queued for a rejected call"
+
+
+def test_noalloc_packed_sequences_equal_prefill(lib):
+    """Packed sequences take their longest-first launch order from the static scratch."""
+    x = ki.varlen_inputs([300, 5, 1200, 64], 2, 128, 128, device=DEV, seed=64)
+    n = x["cu_seqlens"].numel() - 1
+    T = x["q"].shape[1]
+    assert 0 < lib.kda_prefill_workspace_size(0, 1, T, 2, 128, 128, n) <= lib.kda_prefill_noalloc_capacity()
+    o_ref, s_ref = kda.prefill(*(x[m] for m in NAMES), cu_seqlens=x["cu_seqlens"], initial_state=x["initial_state"])
+    o = torch.empty_like(o_ref)
+    fin = torch.empty_like(s_ref)
+    st = lib.kda_prefill_noalloc(0, 1, T, 2, 128, 128, *(x[m].data_ptr() for m in NAMES), x["cu_seqlens"].data_ptr(), n,
+                                 x["initial_state"].data_ptr(), o.data_ptr(), fin.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+    assert st == 0, lib.kda_last_error()
+    kda.check_status()
+    assert torch.equal(o, o_ref) and torch.equal(fin, s_ref)
