@@ -177,20 +177,24 @@ __device__ __forceinline__ void tile_times_state(float (&c)[4], const float *a, 
     }
 }
 
-// M[r][s] (16 x 16) = sum_i a[r][i] * b[s][i] over the 128 channels; one output per thread of the
-// first 256, the two halves of the channel sum by thread pairs.
-__device__ __forceinline__ void tile_times_tile_t(float *M, const float *a, const float *b) {
-    const int t = threadIdx.x, o = t >> 1, half = t & 1;
-    const int r = o / C, s = o % C;
-    float acc = 0.f;
-    const float *ar = a + r * LT + 64 * half, *bs = b + s * LT + 64 * half;
+// M[r][s] (16 x 16) = sum_i a[r][i] * b[s][i] over the 128 channels, on the tensor cores by the
+// two warps w0 and w0 + 1 (one 8-column block each; other warps return at once). Two such
+// products on different warps run side by side.
+__device__ __forceinline__ void tile_times_tile_t(float *M, const float *a, const float *b, int w0) {
+    const int w = (threadIdx.x >> 5) - w0;
+    if (w < 0 || w > 1) return;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, n0 = 8 * w;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-    for (int i = 0; i < 64; i += 4) {
-        const float4 x = *reinterpret_cast<const float4 *>(ar + i), y = *reinterpret_cast<const float4 *>(bs + i);
-        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+    for (int k = 0; k < D; k += 8) {
+        const float af[4] = {a[g * LT + k + t], a[(g + 8) * LT + k + t], a[g * LT + k + t + 4], a[(g + 8) * LT + k + t + 4]};
+        const float bf[2] = {b[(n0 + g) * LT + k + t], b[(n0 + g) * LT + k + t + 4]};
+        mma3(c, af, bf);
     }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    if (half == 0) M[r * LM + s] = acc;
+    M[g * LM + n0 + 2 * t] = c[0];
+    M[g * LM + n0 + 2 * t + 1] = c[1];
+    M[(g + 8) * LM + n0 + 2 * t] = c[2];
+    M[(g + 8) * LM + n0 + 2 * t + 1] = c[3];
 }
 
 // The chunk's gate products and triangular factors: Kp, Km, Kc (into the tile `kc`), (Qp), Ab,
@@ -206,11 +210,8 @@ __device__ __forceinline__ void chunk_factors(float *sm, const float *K, float *
         if (with_q) sm[O_QP + r * LT + i] *= gm;  // Q was loaded into the Qp tile
     }
     __syncthreads();
-    tile_times_tile_t(sm + O_AB, sm + O_KP, sm + O_KM);
-    if (with_q) {
-        __syncthreads();
-        tile_times_tile_t(sm + O_P, sm + O_QP, sm + O_KM);
-    }
+    tile_times_tile_t(sm + O_AB, sm + O_KP, sm + O_KM, 0);
+    if (with_q) tile_times_tile_t(sm + O_P, sm + O_QP, sm + O_KM, 2);
     __syncthreads();
     // X = (I + A)^{-1} for the unit lower-triangular I + A, A = strict_lower(Diag(beta) Ab): column
     // j by forward substitution (one thread per column); T = X Diag(beta).
@@ -451,9 +452,8 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
                 if (r < len) dv[((size_t)(t0 + r) * H + h) * D + i] = x[q];
             }
         }
-        tile_times_tile_t(sm + O_DP, sm + O_DO, sm + O_U);
-        __syncthreads();
-        tile_times_tile_t(sm + O_DT, sm + O_DU, sm + O_R);
+        tile_times_tile_t(sm + O_DP, sm + O_DO, sm + O_U, 4);  // on warps 4-5 and 6-7, after their share
+        tile_times_tile_t(sm + O_DT, sm + O_DU, sm + O_R, 6);  // of dR (neither reads dR)
         __syncthreads();
         // dX = dT Diag(beta); dbeta = colsum(X * dT) + rowsum(dA * Ab); dA = strict_lower(-X^T dX X^T)
         if (tid < C * C) {  // M = dX X^T
