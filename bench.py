@@ -530,7 +530,7 @@ def run_workload(args):
         tokens, n_seq = B * T, B
         kw = dict(d_o=ki.gate_logits_like(x["v"], seed=4))  # dL/do ~ N(0, 1)
         alg = tokens * H * BWD_FLOPS_PER_ELEM * d * d       # algorithmic fp32 flops (ALU-bound)
-        name = f"KDA backward (all gradients, fp32 on CUDA cores): B={B} T={T} H={H} dk=dv={d} bf16 inputs"
+        name = f"KDA backward (all gradients, fp32 state, tf32 tensor-core products): B={B} T={T} H={H} dk=dv={d} bf16 inputs"
     elif args.workload == "outgate":
         B, T = PF["B"], PF["T"]
         x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)

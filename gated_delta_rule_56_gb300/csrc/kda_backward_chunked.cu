@@ -134,11 +134,17 @@ __device__ __forceinline__ void load_tiles(float *const (&dst)[NTEN], const Tin 
         }
 }
 
-// ---- products on the tensor cores: warp-level mma.sync m16n8k8 with tf32 operands. Every fp32
-// operand x is split into a tf32 high part and the tf32 rounding of the rest, and a product is
-// taken as lo*hi + hi*lo + hi*hi (the lo*lo term is below fp32 rounding), so the result keeps
-// fp32 accuracy. Fragment of lane l (g = l / 4, t = l % 4): A (16 x 8) rows g, g + 8 and columns
-// t, t + 4; B (8 x 8) rows t, t + 4 and column g; C (16 x 8) rows g, g + 8, columns 2t, 2t + 1.
+// ---- products on the tensor cores: warp-level mma.sync m16n8k8 with tf32 operands. With SPLIT = 3
+// every fp32 operand x is split into a tf32 high part and the tf32 rounding of the rest, and a
+// product is taken as lo*hi + hi*lo + hi*hi (the lo*lo term is below fp32 rounding), so the result
+// keeps fp32 accuracy; with SPLIT = 1 a product is the single tf32 one. The 16 x 16 chunk factors
+// (Ab, P, dP, dT) always take SPLIT = 3: they cost little and feed the cancelling sums behind dbeta
+// and dq, whose error single tf32 products there raise tenfold. The state-sized products take
+// SPLIT = 3 for fp32 inputs and SPLIT = 1 for bf16 inputs (rounded to 2^-9 already, coarser than
+// tf32's 2^-11): gradients then agree with the fp64 adjoint to about 3e-4 relative (Frobenius)
+// instead of 2e-6, in three quarters of the time.
+// Fragment of lane l (g = l / 4, t = l % 4): A (16 x 8) rows g, g + 8 and columns t, t + 4;
+// B (8 x 8) rows t, t + 4 and column g; C (16 x 8) rows g, g + 8, columns 2t, 2t + 1.
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(x - __uint_as_float(hi)));
@@ -152,19 +158,28 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], 
 }
 
 // c += a b for fp32 fragments a (A layout) and b (B layout).
+template <int SPLIT>
 __device__ __forceinline__ void mma3(float (&c)[4], const float (&a)[4], const float (&b)[2]) {
     uint32_t ah[4], al[4], bh[2], bl[2];
+    if (SPLIT == 3) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) split_tf32(a[q], ah[q], al[q]);
+        for (int q = 0; q < 4; ++q) split_tf32(a[q], ah[q], al[q]);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) split_tf32(b[q], bh[q], bl[q]);
-    mma_tf32(c, al, bh);
-    mma_tf32(c, ah, bl);
+        for (int q = 0; q < 2; ++q) split_tf32(b[q], bh[q], bl[q]);
+        mma_tf32(c, al, bh);
+        mma_tf32(c, ah, bl);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(ah[q]) : "f"(a[q]));
+#pragma unroll
+        for (int q = 0; q < 2; ++q) asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(bh[q]) : "f"(b[q]));
+    }
     mma_tf32(c, ah, bh);
 }
 
 // c (rows g, g + 8 x columns n0 + 2t, + 1 of a 16 x 128 result) = a (16 x 128 tile) B (128 x 128
 // at row stride LS), for the warp's 8 columns n0 .. n0 + 7.
+template <int SPLIT>
 __device__ __forceinline__ void tile_times_state(float (&c)[4], const float *a, const float *B, int n0) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
@@ -173,13 +188,13 @@ __device__ __forceinline__ void tile_times_state(float (&c)[4], const float *a, 
     for (int k = 0; k < D; k += 8) {
         const float af[4] = {a[g * LT + k + t], a[(g + 8) * LT + k + t], a[g * LT + k + t + 4], a[(g + 8) * LT + k + t + 4]};
         const float bf[2] = {B[(k + t) * LS + n0 + g], B[(k + t + 4) * LS + n0 + g]};
-        mma3(c, af, bf);
+        mma3<SPLIT>(c, af, bf);
     }
 }
 
 // M[r][s] (16 x 16) = sum_i a[r][i] * b[s][i] over the 128 channels, on the tensor cores by the
-// two warps w0 and w0 + 1 (one 8-column block each; other warps return at once). Two such
-// products on different warps run side by side.
+// two warps w0 and w0 + 1 (one 8-column block each; other warps return at once), at fp32 accuracy.
+// Two such products on different warps run side by side.
 __device__ __forceinline__ void tile_times_tile_t(float *M, const float *a, const float *b, int w0) {
     const int w = (threadIdx.x >> 5) - w0;
     if (w < 0 || w > 1) return;
@@ -189,7 +204,7 @@ __device__ __forceinline__ void tile_times_tile_t(float *M, const float *a, cons
     for (int k = 0; k < D; k += 8) {
         const float af[4] = {a[g * LT + k + t], a[(g + 8) * LT + k + t], a[g * LT + k + t + 4], a[(g + 8) * LT + k + t + 4]};
         const float bf[2] = {b[(n0 + g) * LT + k + t], b[(n0 + g) * LT + k + t + 4]};
-        mma3(c, af, bf);
+        mma3<3>(c, af, bf);
     }
     M[g * LM + n0 + 2 * t] = c[0];
     M[g * LM + n0 + 2 * t + 1] = c[1];
@@ -247,11 +262,12 @@ __device__ __forceinline__ void chunk_factors(float *sm, const float *K, float *
 }
 
 // R = V - Kp S (in the R tile, which holds V; warp w takes columns 8 w .. + 7), then U = T R.
+template <int SPLIT>
 __device__ __forceinline__ void chunk_u(float *sm) {
     {
         const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, n0 = 8 * (threadIdx.x >> 5);
         float c[4];
-        tile_times_state(c, sm + O_KP, sm + O_S, n0);
+        tile_times_state<SPLIT>(c, sm + O_KP, sm + O_S, n0);
         float *R = sm + O_R;
         R[g * LT + n0 + 2 * t] -= c[0];
         R[g * LT + n0 + 2 * t + 1] -= c[1];
@@ -280,6 +296,7 @@ __device__ __forceinline__ void chunk_u(float *sm) {
 // X (128 x 128, row stride LS) <- Diag(gC) X + A1^T B1 + A2^T B2 for 16 x 128 tiles A1, B1, A2, B2
 // (A2 may be null). Warp w takes rows 16 (w / 2) .. + 15 and columns 64 (w % 2) .. + 63; every
 // element of X is read and written by the one thread holding it.
+template <int SPLIT>
 __device__ __forceinline__ void state_update(float *X, const float *gc, const float *A1, const float *B1,
                                              const float *A2, const float *B2) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -309,10 +326,10 @@ __device__ __forceinline__ void state_update(float *X, const float *gc, const fl
         for (int ks = 0; ks < 2; ++ks) {
             const int k = 8 * ks;
             const float b1[2] = {B1[(k + t) * LT + n + g], B1[(k + t + 4) * LT + n + g]};
-            mma3(c, af1[ks], b1);
+            mma3<SPLIT>(c, af1[ks], b1);
             if (A2) {
                 const float b2[2] = {B2[(k + t) * LT + n + g], B2[(k + t + 4) * LT + n + g]};
-                mma3(c, af2[ks], b2);
+                mma3<SPLIT>(c, af2[ks], b2);
             }
         }
         x0[0] = c[0];
@@ -326,6 +343,7 @@ template <typename Tin>
 __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, const void *d_o, const float *d_fin,
                                                                  float *dq, float *dk, float *dv, float *dg,
                                                                  float *dbeta, float *d_init, float *ck) {
+    constexpr int SPLIT = sizeof(Tin) == 4 ? 3 : 1;  // products at the precision class of the inputs
     extern __shared__ float sm[];
     const int H = p.H, h = blockIdx.x % H, n = blockIdx.x / H, tid = threadIdx.x;
     long long bos, eos;
@@ -375,9 +393,9 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         gate_tile(sm, sm + O_DG);
         __syncthreads();
         chunk_factors(sm, sm + O_DU, sm + O_DR, false);
-        chunk_u(sm);
+        chunk_u<SPLIT>(sm);
         // S <- Diag(gC) S + Kc^T U (Kc in the dR tile)
-        state_update(S, sm + O_GC, sm + O_DR, sm + O_U, nullptr, nullptr);
+        state_update<SPLIT>(S, sm + O_GC, sm + O_DR, sm + O_U, nullptr, nullptr);
         __syncthreads();
     }
 
@@ -412,18 +430,18 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         gate_tile(sm, sm + O_DG);
         __syncthreads();
         chunk_factors(sm, sm + O_DU, sm + O_DG, true);  // Kc in the dG tile until dGam is formed
-        chunk_u(sm);
+        chunk_u<SPLIT>(sm);
         // dU = Kc dS + P^T dO (warp w: columns 8 w .. + 7)
         {
             const int lane = tid & 31, g = lane >> 2, t = lane & 3, n0 = 8 * (tid >> 5);
             float c[4];
-            tile_times_state(c, sm + O_DG, dS, n0);
+            tile_times_state<SPLIT>(c, sm + O_DG, dS, n0);
 #pragma unroll
             for (int k = 0; k < C; k += 8) {  // P^T (16 x 16) dO (16 x 128)
                 const float af[4] = {sm[O_P + (k + t) * LM + g], sm[O_P + (k + t) * LM + g + 8],
                                      sm[O_P + (k + t + 4) * LM + g], sm[O_P + (k + t + 4) * LM + g + 8]};
                 const float bf[2] = {sm[O_DO + (k + t) * LT + n0 + g], sm[O_DO + (k + t + 4) * LT + n0 + g]};
-                mma3(c, af, bf);
+                mma3<SPLIT>(c, af, bf);
             }
             float *dU = sm + O_DU;
             dU[g * LT + n0 + 2 * t] = c[0];
@@ -500,9 +518,9 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
                                      dR[(g + 8) * LT + k + t + 4]};
                 const float au[4] = {U[g * LT + k + t], U[(g + 8) * LT + k + t], U[g * LT + k + t + 4],
                                      U[(g + 8) * LT + k + t + 4]};
-                mma3(cq, ao, bs);
-                mma3(ckp, ar, bs);
-                mma3(cc, au, bd);
+                mma3<SPLIT>(cq, ao, bs);
+                mma3<SPLIT>(ckp, ar, bs);
+                mma3<SPLIT>(cc, au, bd);
             }
             if (tid < D) {  // dgC = rowsum(dS * S) for channel tid
                 float dgc = 0.f;
@@ -575,7 +593,7 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         // dR in place, it is read no more)
         for (int e = tid; e < C * D; e += NT) sm[O_DR + (e / D) * LT + e % D] *= -1.f;
         __syncthreads();
-        state_update(dS, sm + O_GC, sm + O_QP, sm + O_DO, sm + O_KP, sm + O_DR);
+        state_update<SPLIT>(dS, sm + O_GC, sm + O_QP, sm + O_DO, sm + O_KP, sm + O_DR);
     }
     __syncthreads();
     if (d_init)

@@ -155,10 +155,15 @@ KDA_API kda_status kda_decode_step_ex(kda_dtype dtype, int N, int H, int dk, int
 
 /*
  * kda_backward -- gradients of L = sum(d_o * o) + sum(d_final_state * final_state) through
- * kda_prefill's computation (plain log-decays; no options), on CUDA cores in fp32. The pages
+ * kda_prefill's computation (plain log-decays; no options), with an fp32 state. The pages
  * train the model ("Kimi K3 Explained", researchpapers.dev, "Architecture at a glance") but give
  * no gradient method: this is reverse-mode differentiation of the recurrence (for d = 128 taken
  * of its chunkwise form on 16-token chunks; the result is the same up to rounding).
+ * Precision for d = 128: the products run on the tensor cores in tf32. For fp32 inputs every
+ * product is taken to fp32 accuracy (split operands, three tf32 products); for bf16 inputs the
+ * products with the 128 x 128 states are single tf32 products, and the gradients agree with an
+ * exact computation to about 3e-4 relative (Frobenius norm) instead of about 2e-6. d = 32, 64
+ * compute on the CUDA cores in fp32.
  *
  * dtype, B, T, H, dk, dv, q, k, v, g, beta, cu_seqlens, n_seqs, initial_state: as kda_prefill.
  * d_o          [B, T, H, dv] in `dtype`: dL/do.

@@ -21,13 +21,16 @@ def _built():
     kda.load()
 
 
-def _check(x, do, dfin=None, cu=None, init=None):
+def _check(x, do, dfin=None, cu=None, init=None, rel_frob=None):
     got = kda.backward(*(x[n] for n in NAMES), do, cu_seqlens=cu, initial_state=init, d_final_state=dfin)
     kda.check_status()
     ref = oracle.backward(*(x[n].cpu() for n in NAMES), do.cpu(), None if dfin is None else dfin.cpu(),
                           cu_seqlens=None if cu is None else cu.cpu(), initial_state=None if init is None else init.cpu())
     for name in GRADS:
-        assert_close(got[name], ref[name], name)
+        if rel_frob is None:
+            assert_close(got[name], ref[name], name)
+        else:
+            assert_close(got[name], ref[name], name, rel_frob=rel_frob)
 
 
 def _do(x, seed):
@@ -40,6 +43,15 @@ def test_backward_matches_oracle(B, T, H, d, dtype):
     x = ki.prefill_inputs(B, T, H, d, d, dtype=dtype, device=DEV, seed=121, state_std=0.02)
     dfin = torch.randn(B, H, d, d, device=DEV, generator=torch.Generator(device=DEV).manual_seed(122))
     _check(x, _do(x, 123), dfin=dfin, init=x["initial_state"])
+
+
+def test_backward_fp32_inputs_keep_fp32_accuracy():
+    """With fp32 inputs the d=128 kernel splits every tensor-core operand (three tf32 products per
+    product), so the gradients stay near fp32 rounding: well inside 5e-5 relative, where single tf32
+    products (the bf16-input instance) land near 3e-4."""
+    x = ki.prefill_inputs(2, 100, 2, 128, 128, dtype=torch.float32, device=DEV, seed=131, state_std=0.02)
+    dfin = torch.randn(2, 2, 128, 128, device=DEV, generator=torch.Generator(device=DEV).manual_seed(132))
+    _check(x, _do(x, 133), dfin=dfin, init=x["initial_state"], rel_frob=5e-5)
 
 
 def test_backward_varlen_without_states():
