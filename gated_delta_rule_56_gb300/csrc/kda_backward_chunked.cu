@@ -157,6 +157,38 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// Four 8 x 4 blocks of 32-bit words from shared memory in one instruction: ldmatrix reads 8 x 8
+// matrices of 16-bit elements, so lane l gets word (l / 4, l % 4) of each block, which is the
+// tf32 fragment layout. Lanes 8m .. 8m + 7 give the addresses of the rows of block m (16-byte
+// aligned); r[m] is the lane's word of block m.
+__device__ __forceinline__ void ldsm_x4(float (&r)[4], const float *p) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    uint32_t x0, x1, x2, x3;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                 : "r"(a)
+                 : "memory");
+    r[0] = __uint_as_float(x0);
+    r[1] = __uint_as_float(x1);
+    r[2] = __uint_as_float(x2);
+    r[3] = __uint_as_float(x3);
+}
+
+// The lane's row address for A fragments of a 16 x k row-major tile (row stride ld): blocks
+// (rows 0-7, columns k..k+3), (rows 8-15, k..k+3), (rows 0-7, k+4..k+7), (rows 8-15, k+4..k+7).
+__device__ __forceinline__ const float *a_frag_row(const float *a, int ld) {
+    const int lane = threadIdx.x & 31;
+    return a + ((lane & 7) + 8 * ((lane >> 3) & 1)) * ld + 4 * (lane >> 4);
+}
+
+// The lane's row address for the B fragments of two k steps from an n-major operand (element
+// (k, n) at b[n * ld + k]): blocks (rows n0..n0+7, columns k + 4m .. + 3), m = 0..3, give b0, b1
+// of step k and b0, b1 of step k + 8.
+__device__ __forceinline__ const float *b_frag_row(const float *b, int ld, int n0) {
+    const int lane = threadIdx.x & 31;
+    return b + (n0 + (lane & 7)) * ld + 4 * (lane >> 3);
+}
+
 // c += a b for fp32 fragments a (A layout) and b (B layout).
 template <int SPLIT>
 __device__ __forceinline__ void mma3(float (&c)[4], const float (&a)[4], const float (&b)[2]) {
@@ -182,11 +214,13 @@ __device__ __forceinline__ void mma3(float (&c)[4], const float (&a)[4], const f
 template <int SPLIT>
 __device__ __forceinline__ void tile_times_state(float (&c)[4], const float *a, const float *B, int n0) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const float *ap = a_frag_row(a, LT);
 #pragma unroll
     for (int q = 0; q < 4; ++q) c[q] = 0.f;
 #pragma unroll 4
     for (int k = 0; k < D; k += 8) {
-        const float af[4] = {a[g * LT + k + t], a[(g + 8) * LT + k + t], a[g * LT + k + t + 4], a[(g + 8) * LT + k + t + 4]};
+        float af[4];
+        ldsm_x4(af, ap + k);
         const float bf[2] = {B[(k + t) * LS + n0 + g], B[(k + t + 4) * LS + n0 + g]};
         mma3<SPLIT>(c, af, bf);
     }
@@ -199,12 +233,17 @@ __device__ __forceinline__ void tile_times_tile_t(float *M, const float *a, cons
     const int w = (threadIdx.x >> 5) - w0;
     if (w < 0 || w > 1) return;
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, n0 = 8 * w;
+    const float *ap = a_frag_row(a, LT), *bp = b_frag_row(b, LT, n0);
     float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int k = 0; k < D; k += 8) {
-        const float af[4] = {a[g * LT + k + t], a[(g + 8) * LT + k + t], a[g * LT + k + t + 4], a[(g + 8) * LT + k + t + 4]};
-        const float bf[2] = {b[(n0 + g) * LT + k + t], b[(n0 + g) * LT + k + t + 4]};
-        mma3<3>(c, af, bf);
+#pragma unroll 2
+    for (int k = 0; k < D; k += 16) {
+        float a0[4], a1[4], bb[4];
+        ldsm_x4(bb, bp + k);
+        ldsm_x4(a0, ap + k);
+        ldsm_x4(a1, ap + k + 8);
+        const float b0[2] = {bb[0], bb[1]}, b1[2] = {bb[2], bb[3]};
+        mma3<3>(c, a0, b0);
+        mma3<3>(c, a1, b1);
     }
     M[g * LM + n0 + 2 * t] = c[0];
     M[g * LM + n0 + 2 * t + 1] = c[1];
@@ -507,20 +546,26 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         {
             const int lane = tid & 31, g = lane >> 2, t = lane & 3, n0 = 8 * (tid >> 5);
             float cq[4] = {0.f, 0.f, 0.f, 0.f}, ckp[4] = {0.f, 0.f, 0.f, 0.f}, cc[4] = {0.f, 0.f, 0.f, 0.f};
-            const float *dO = sm + O_DO, *dR = sm + O_DR, *U = sm + O_U;
-#pragma unroll 2
-            for (int k = 0; k < D; k += 8) {
-                const float bs[2] = {S[(n0 + g) * LS + k + t], S[(n0 + g) * LS + k + t + 4]};
-                const float bd[2] = {dS[(n0 + g) * LS + k + t], dS[(n0 + g) * LS + k + t + 4]};
-                const float ao[4] = {dO[g * LT + k + t], dO[(g + 8) * LT + k + t], dO[g * LT + k + t + 4],
-                                     dO[(g + 8) * LT + k + t + 4]};
-                const float ar[4] = {dR[g * LT + k + t], dR[(g + 8) * LT + k + t], dR[g * LT + k + t + 4],
-                                     dR[(g + 8) * LT + k + t + 4]};
-                const float au[4] = {U[g * LT + k + t], U[(g + 8) * LT + k + t], U[g * LT + k + t + 4],
-                                     U[(g + 8) * LT + k + t + 4]};
-                mma3<SPLIT>(cq, ao, bs);
-                mma3<SPLIT>(ckp, ar, bs);
-                mma3<SPLIT>(cc, au, bd);
+            const float *pO = a_frag_row(sm + O_DO, LT), *pR = a_frag_row(sm + O_DR, LT);
+            const float *pU = a_frag_row(sm + O_U, LT);
+            const float *pS = b_frag_row(S, LS, n0), *pD = b_frag_row(dS, LS, n0);
+#pragma unroll 1
+            for (int k = 0; k < D; k += 16) {
+                float bs4[4], bd4[4];
+                ldsm_x4(bs4, pS + k);
+                ldsm_x4(bd4, pD + k);
+#pragma unroll
+                for (int hk = 0; hk < 2; ++hk) {
+                    const int kk = k + 8 * hk;
+                    float ao[4], ar[4], au[4];
+                    ldsm_x4(ao, pO + kk);
+                    ldsm_x4(ar, pR + kk);
+                    ldsm_x4(au, pU + kk);
+                    const float bs[2] = {bs4[2 * hk], bs4[2 * hk + 1]}, bd[2] = {bd4[2 * hk], bd4[2 * hk + 1]};
+                    mma3<SPLIT>(cq, ao, bs);
+                    mma3<SPLIT>(ckp, ar, bs);
+                    mma3<SPLIT>(cc, au, bd);
+                }
             }
             if (tid < D) {  // dgC = rowsum(dS * S) for channel tid
                 float dgc = 0.f;
