@@ -300,35 +300,43 @@ __device__ __forceinline__ void chunk_factors(float *sm, const float *K, float *
     __syncthreads();
 }
 
-// R = V - Kp S (in the R tile, which holds V; warp w takes columns 8 w .. + 7), then U = T R.
+// The fragment element pairs (g, n0 + 2t, + 1) and (g + 8, n0 + 2t, + 1) of a 16 x 128 tile.
+__device__ __forceinline__ float2 *frag_pair(float *tile, int row, int n0) {
+    const int t = threadIdx.x & 3;
+    return reinterpret_cast<float2 *>(tile + row * LT + n0 + 2 * t);
+}
+
+// c = M B[:, n0 .. n0 + 7] for a 16 x 16 matrix M (row stride LM) and a 16 x 128 tile B, at fp32
+// accuracy (3xtf32).
+__device__ __forceinline__ void small_times_tile(float (&c)[4], const float *M, const float *B, int n0) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const float *ap = a_frag_row(M, LM);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c[q] = 0.f;
+#pragma unroll
+    for (int k = 0; k < C; k += 8) {
+        float af[4];
+        ldsm_x4(af, ap + k);
+        const float bf[2] = {B[(k + t) * LT + n0 + g], B[(k + t + 4) * LT + n0 + g]};
+        mma3<3>(c, af, bf);
+    }
+}
+
+// R = V - Kp S (in the R tile, which holds V), then U = T R; warp w takes columns 8 w .. + 7 of
+// both, so U needs only the warp's own R columns.
 template <int SPLIT>
 __device__ __forceinline__ void chunk_u(float *sm) {
-    {
-        const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, n0 = 8 * (threadIdx.x >> 5);
-        float c[4];
-        tile_times_state<SPLIT>(c, sm + O_KP, sm + O_S, n0);
-        float *R = sm + O_R;
-        R[g * LT + n0 + 2 * t] -= c[0];
-        R[g * LT + n0 + 2 * t + 1] -= c[1];
-        R[(g + 8) * LT + n0 + 2 * t] -= c[2];
-        R[(g + 8) * LT + n0 + 2 * t + 1] -= c[3];
-    }
-    __syncthreads();
-    {  // U[r][i] = sum_s T[r][s] R[s][i]: thread takes channel i and rows r0 .. r0 + 3
-        const int i = threadIdx.x % D, r0 = 4 * (threadIdx.x / D);
-        float u[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int s = 0; s < C; ++s) {
-            const float rs = sm[O_R + s * LT + i];
-            const float4 t = *reinterpret_cast<const float4 *>(sm + O_TT + s * LM + r0);
-            u[0] = fmaf(t.x, rs, u[0]);
-            u[1] = fmaf(t.y, rs, u[1]);
-            u[2] = fmaf(t.z, rs, u[2]);
-            u[3] = fmaf(t.w, rs, u[3]);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) sm[O_U + (r0 + q) * LT + i] = u[q];
-    }
+    const int g = (threadIdx.x & 31) >> 2, n0 = 8 * (threadIdx.x >> 5);
+    float c[4];
+    tile_times_state<SPLIT>(c, sm + O_KP, sm + O_S, n0);
+    float2 *r0 = frag_pair(sm + O_R, g, n0), *r8 = frag_pair(sm + O_R, g + 8, n0);
+    const float2 x0 = *r0, x8 = *r8;
+    *r0 = make_float2(x0.x - c[0], x0.y - c[1]);
+    *r8 = make_float2(x8.x - c[2], x8.y - c[3]);
+    __syncwarp();
+    small_times_tile(c, sm + O_T, sm + O_R, n0);
+    *frag_pair(sm + O_U, g, n0) = make_float2(c[0], c[1]);
+    *frag_pair(sm + O_U, g + 8, n0) = make_float2(c[2], c[3]);
     __syncthreads();
 }
 
@@ -359,8 +367,10 @@ __device__ __forceinline__ void state_update(float *X, const float *gc, const fl
 #pragma unroll 2
     for (int nb = 0; nb < 64; nb += 8) {
         const int n = nb0 + nb;
-        float *x0 = X + (m0 + g) * LS + n + 2 * t, *x8 = X + (m0 + g + 8) * LS + n + 2 * t;
-        float c[4] = {x0[0] * g0, x0[1] * g0, x8[0] * g8, x8[1] * g8};
+        float2 *x0 = reinterpret_cast<float2 *>(X + (m0 + g) * LS + n + 2 * t);
+        float2 *x8 = reinterpret_cast<float2 *>(X + (m0 + g + 8) * LS + n + 2 * t);
+        const float2 v0 = *x0, v8 = *x8;
+        float c[4] = {v0.x * g0, v0.y * g0, v8.x * g8, v8.y * g8};
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
             const int k = 8 * ks;
@@ -371,10 +381,8 @@ __device__ __forceinline__ void state_update(float *X, const float *gc, const fl
                 mma3<SPLIT>(c, af2[ks], b2);
             }
         }
-        x0[0] = c[0];
-        x0[1] = c[1];
-        x8[0] = c[2];
-        x8[1] = c[3];
+        *x0 = make_float2(c[0], c[1]);
+        *x8 = make_float2(c[2], c[3]);
     }
 }
 
@@ -414,7 +422,8 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         const long long t0 = bos + (long long)c * C;
         const int len = (int)min((long long)C, eos - t0);
         float *dst = ck_at(c);
-        for (int e = tid; e < D * D; e += NT) dst[e] = S[(e / D) * LS + e % D];
+        for (int e = 4 * tid; e < D * D; e += 4 * NT)
+            *reinterpret_cast<float4 *>(dst + e) = *reinterpret_cast<const float4 *>(S + (e / D) * LS + e % D);
         if (c + 1 < nc) {  // the next chunk's rows into L2
             const long long t1 = t0 + C;
             const int l1 = (int)min((long long)C, eos - t1);
@@ -482,35 +491,21 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
                 const float bf[2] = {sm[O_DO + (k + t) * LT + n0 + g], sm[O_DO + (k + t + 4) * LT + n0 + g]};
                 mma3<SPLIT>(c, af, bf);
             }
-            float *dU = sm + O_DU;
-            dU[g * LT + n0 + 2 * t] = c[0];
-            dU[g * LT + n0 + 2 * t + 1] = c[1];
-            dU[(g + 8) * LT + n0 + 2 * t] = c[2];
-            dU[(g + 8) * LT + n0 + 2 * t + 1] = c[3];
+            *frag_pair(sm + O_DU, g, n0) = make_float2(c[0], c[1]);
+            *frag_pair(sm + O_DU, g + 8, n0) = make_float2(c[2], c[3]);
+            __syncwarp();
+            // dR = T^T dU (= dV, stored) on the warp's own columns of dU; T^T is kept in the Tt matrix
+            small_times_tile(c, sm + O_TT, sm + O_DU, n0);
+            *frag_pair(sm + O_DR, g, n0) = make_float2(c[0], c[1]);
+            *frag_pair(sm + O_DR, g + 8, n0) = make_float2(c[2], c[3]);
+            if (g < len) *reinterpret_cast<float2 *>(dv + ((size_t)(t0 + g) * H + h) * D + n0 + 2 * t) = make_float2(c[0], c[1]);
+            if (g + 8 < len)
+                *reinterpret_cast<float2 *>(dv + ((size_t)(t0 + g + 8) * H + h) * D + n0 + 2 * t) = make_float2(c[2], c[3]);
         }
         __syncthreads();
-        // dR = T^T dU (= dV, stored), dP = lower(dO U^T), dT = dU R^T
-        {  // dR[r][i] = sum_s T[s][r] dU[s][i]: thread takes channel i and rows r0 .. r0 + 3
-            const int i = tid % D, r0 = 4 * (tid / D);
-            float x[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int s = 0; s < C; ++s) {
-                const float du = sm[O_DU + s * LT + i];
-                const float4 t = *reinterpret_cast<const float4 *>(sm + O_T + s * LM + r0);
-                x[0] = fmaf(t.x, du, x[0]);
-                x[1] = fmaf(t.y, du, x[1]);
-                x[2] = fmaf(t.z, du, x[2]);
-                x[3] = fmaf(t.w, du, x[3]);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int r = r0 + q;
-                sm[O_DR + r * LT + i] = x[q];
-                if (r < len) dv[((size_t)(t0 + r) * H + h) * D + i] = x[q];
-            }
-        }
-        tile_times_tile_t(sm + O_DP, sm + O_DO, sm + O_U, 4);  // on warps 4-5 and 6-7, after their share
-        tile_times_tile_t(sm + O_DT, sm + O_DU, sm + O_R, 6);  // of dR (neither reads dR)
+        // dP = lower(dO U^T), dT = dU R^T
+        tile_times_tile_t(sm + O_DP, sm + O_DO, sm + O_U, 4);  // on warps 4-5 and 6-7
+        tile_times_tile_t(sm + O_DT, sm + O_DU, sm + O_R, 6);
         __syncthreads();
         // dX = dT Diag(beta); dbeta = colsum(X * dT) + rowsum(dA * Ab); dA = strict_lower(-X^T dX X^T)
         if (tid < C * C) {  // M = dX X^T
@@ -579,9 +574,12 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
             __syncthreads();  // every warp is done with dO, dR and U as operands
             float *T1 = sm + O_R, *T2 = sm + O_DU, *T3 = sm + O_U;
             const int e0 = g * LT + n0 + 2 * t, e8 = (g + 8) * LT + n0 + 2 * t;
-            T1[e0] = cq[0]; T1[e0 + 1] = cq[1]; T1[e8] = cq[2]; T1[e8 + 1] = cq[3];
-            T2[e0] = ckp[0]; T2[e0 + 1] = ckp[1]; T2[e8] = ckp[2]; T2[e8 + 1] = ckp[3];
-            T3[e0] = cc[0]; T3[e0 + 1] = cc[1]; T3[e8] = cc[2]; T3[e8 + 1] = cc[3];
+            *reinterpret_cast<float2 *>(T1 + e0) = make_float2(cq[0], cq[1]);
+            *reinterpret_cast<float2 *>(T1 + e8) = make_float2(cq[2], cq[3]);
+            *reinterpret_cast<float2 *>(T2 + e0) = make_float2(ckp[0], ckp[1]);
+            *reinterpret_cast<float2 *>(T2 + e8) = make_float2(ckp[2], ckp[3]);
+            *reinterpret_cast<float2 *>(T3 + e0) = make_float2(cc[0], cc[1]);
+            *reinterpret_cast<float2 *>(T3 + e8) = make_float2(cc[2], cc[3]);
         }
         __syncthreads();
         if (c > 0) {  // S is read no more in this chunk: fetch the previous chunk's start state
