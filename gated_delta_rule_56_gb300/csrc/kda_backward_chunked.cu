@@ -306,20 +306,33 @@ __device__ __forceinline__ float2 *frag_pair(float *tile, int row, int n0) {
     return reinterpret_cast<float2 *>(tile + row * LT + n0 + 2 * t);
 }
 
-// c = M B[:, n0 .. n0 + 7] for a 16 x 16 matrix M (row stride LM) and a 16 x 128 tile B, at fp32
-// accuracy (3xtf32).
-__device__ __forceinline__ void small_times_tile(float (&c)[4], const float *M, const float *B, int n0) {
+// c += M B[:, n0 .. n0 + 7] (TRANS: c += M^T B[:, n0 .. n0 + 7]) for a 16 x 16 matrix M (row
+// stride LM) and a 16 x 128 tile B, at fp32 accuracy (3xtf32).
+template <bool TRANS>
+__device__ __forceinline__ void small_times_tile_acc(float (&c)[4], const float *M, const float *B, int n0) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const float *ap = a_frag_row(M, LM);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) c[q] = 0.f;
-#pragma unroll
     for (int k = 0; k < C; k += 8) {
         float af[4];
-        ldsm_x4(af, ap + k);
+        if (TRANS) {
+            af[0] = M[(k + t) * LM + g];
+            af[1] = M[(k + t) * LM + g + 8];
+            af[2] = M[(k + t + 4) * LM + g];
+            af[3] = M[(k + t + 4) * LM + g + 8];
+        } else {
+            ldsm_x4(af, ap + k);
+        }
         const float bf[2] = {B[(k + t) * LT + n0 + g], B[(k + t + 4) * LT + n0 + g]};
         mma3<3>(c, af, bf);
     }
+}
+
+// c = M B[:, n0 .. n0 + 7], as above.
+__device__ __forceinline__ void small_times_tile(float (&c)[4], const float *M, const float *B, int n0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c[q] = 0.f;
+    small_times_tile_acc<false>(c, M, B, n0);
 }
 
 // R = V - Kp S (in the R tile, which holds V), then U = T R; warp w takes columns 8 w .. + 7 of
@@ -340,12 +353,12 @@ __device__ __forceinline__ void chunk_u(float *sm) {
     __syncthreads();
 }
 
-// X (128 x 128, row stride LS) <- Diag(gC) X + A1^T B1 + A2^T B2 for 16 x 128 tiles A1, B1, A2, B2
-// (A2 may be null). Warp w takes rows 16 (w / 2) .. + 15 and columns 64 (w % 2) .. + 63; every
+// X (128 x 128, row stride LS) <- Diag(gC) X + A1^T B1 + s2 A2^T B2 for 16 x 128 tiles A1, B1, A2,
+// B2 (A2 may be null). Warp w takes rows 16 (w / 2) .. + 15 and columns 64 (w % 2) .. + 63; every
 // element of X is read and written by the one thread holding it.
 template <int SPLIT>
 __device__ __forceinline__ void state_update(float *X, const float *gc, const float *A1, const float *B1,
-                                             const float *A2, const float *B2) {
+                                             const float *A2, const float *B2, float s2) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int m0 = 16 * (w >> 1), nb0 = 64 * (w & 1);
     float af1[2][4], af2[2][4];
@@ -357,10 +370,10 @@ __device__ __forceinline__ void state_update(float *X, const float *gc, const fl
         af1[ks][2] = A1[(k + t + 4) * LT + m0 + g];
         af1[ks][3] = A1[(k + t + 4) * LT + m0 + g + 8];
         if (A2) {
-            af2[ks][0] = A2[(k + t) * LT + m0 + g];
-            af2[ks][1] = A2[(k + t) * LT + m0 + g + 8];
-            af2[ks][2] = A2[(k + t + 4) * LT + m0 + g];
-            af2[ks][3] = A2[(k + t + 4) * LT + m0 + g + 8];
+            af2[ks][0] = s2 * A2[(k + t) * LT + m0 + g];
+            af2[ks][1] = s2 * A2[(k + t) * LT + m0 + g + 8];
+            af2[ks][2] = s2 * A2[(k + t + 4) * LT + m0 + g];
+            af2[ks][3] = s2 * A2[(k + t + 4) * LT + m0 + g + 8];
         }
     }
     const float g0 = gc[m0 + g], g8 = gc[m0 + g + 8];
@@ -443,7 +456,7 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
         chunk_factors(sm, sm + O_DU, sm + O_DR, false);
         chunk_u<SPLIT>(sm);
         // S <- Diag(gC) S + Kc^T U (Kc in the dR tile)
-        state_update<SPLIT>(S, sm + O_GC, sm + O_DR, sm + O_U, nullptr, nullptr);
+        state_update<SPLIT>(S, sm + O_GC, sm + O_DR, sm + O_U, nullptr, nullptr, 1.f);
         __syncthreads();
     }
 
@@ -586,38 +599,56 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
             const float *src = ck_at(c - 1);
             for (int e = 4 * tid; e < D * D; e += 4 * NT) cp_async16(S + (e / D) * LS + e % D, src + e);
         }
-        // Per (r, i): dQp, dKp, dKm, dKc -> dq, dk and dGam (thread: channel i = t % 128, rows
-        // 4 (t / 128) .. + 3).
+        // Per (r, i): dQp = dO S^T + dP Km, dKp = -dR S^T + dAb Km, dKm = dP^T Qp + dAb^T Kp and dKc
+        // (= U dS^T) -> dq, dk and dGam. Warp w takes channels 8 w .. + 7 in the fragment layout
+        // (rows g, g + 8; channels 2t, 2t + 1 of the block); the products as 3xtf32 MMAs.
         {
-            const int i = tid % D, r0 = 4 * (tid / D);
-            const float gc = sm[O_GC + i];
-            float colsum = 0.f;
+            const int lane = tid & 31, g = lane >> 2, t = lane & 3, n0 = 8 * (tid >> 5), i0 = n0 + 2 * t;
+            float cq[4], ckp[4], ckm[4] = {0.f, 0.f, 0.f, 0.f};
+            small_times_tile(cq, sm + O_DP, sm + O_KM, n0);
+            small_times_tile(ckp, sm + O_DAB, sm + O_KM, n0);
+            small_times_tile_acc<true>(ckm, sm + O_DP, sm + O_QP, n0);
+            small_times_tile_acc<true>(ckm, sm + O_DAB, sm + O_KP, n0);
+            const float2 gc = *reinterpret_cast<const float2 *>(sm + O_GC + i0);
+            float cs[2] = {0.f, 0.f};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int r = r0 + q;
-                float dqp = sm[O_R + r * LT + i], dkp = -sm[O_DU + r * LT + i], dkm = 0.f;
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = g + 8 * hh;
+                const float2 dq2 = *frag_pair(sm + O_R, r, n0), dk2 = *frag_pair(sm + O_DU, r, n0);
+                const float2 dc2 = *frag_pair(sm + O_U, r, n0), gm2 = *frag_pair(sm + O_GAM, r, n0);
+                const float2 kp2 = *frag_pair(sm + O_KP, r, n0), km2 = *frag_pair(sm + O_KM, r, n0);
+                const float2 qp2 = *frag_pair(sm + O_QP, r, n0);
+                const float dqa[2] = {dq2.x, dq2.y}, dka[2] = {dk2.x, dk2.y}, dca[2] = {dc2.x, dc2.y};
+                const float gma[2] = {gm2.x, gm2.y}, kpa[2] = {kp2.x, kp2.y}, kma[2] = {km2.x, km2.y};
+                const float qpa[2] = {qp2.x, qp2.y}, gca[2] = {gc.x, gc.y};
+                float dgo[2], dqo[2], dko[2];
 #pragma unroll
-                for (int s = 0; s < C; ++s) {
-                    const float kms = sm[O_KM + s * LT + i];
-                    dqp = fmaf(sm[O_DP + r * LM + s], kms, dqp);
-                    dkp = fmaf(sm[O_DAB + r * LM + s], kms, dkp);
-                    dkm = fmaf(sm[O_DP + s * LM + r], sm[O_QP + s * LT + i], dkm);
-                    dkm = fmaf(sm[O_DAB + s * LM + r], sm[O_KP + s * LT + i], dkm);
+                for (int u = 0; u < 2; ++u) {
+                    const float dqp = dqa[u] + cq[2 * hh + u], dkp = ckp[2 * hh + u] - dka[u];
+                    const float dkm = ckm[2 * hh + u], gm = gma[u], gcu = gca[u];
+                    const float kc = kma[u] * gcu, dkc = dca[u];
+                    dko[u] = dkp * gm + __fdividef(dkm, gm) + dkc * __fdividef(gcu, gm);
+                    dqo[u] = dqp * gm;
+                    dgo[u] = dkp * kpa[u] - dkm * kma[u] + dqp * qpa[u] - dkc * kc;
+                    cs[u] = fmaf(dkc, kc, cs[u]);
                 }
-                const float gm = sm[O_GAM + r * LT + i];
-                const float kp = sm[O_KP + r * LT + i], km = sm[O_KM + r * LT + i], qp = sm[O_QP + r * LT + i];
-                const float kc = km * gc, dkc = sm[O_U + r * LT + i];
-                const float dkv = dkp * gm + __fdividef(dkm, gm) + dkc * __fdividef(gc, gm);
-                const float dqv = dqp * gm;
-                sm[O_DG + r * LT + i] = dkp * kp - dkm * km + dqp * qp - dkc * kc;
-                colsum = fmaf(dkc, kc, colsum);
+                *frag_pair(sm + O_DG, r, n0) = make_float2(dgo[0], dgo[1]);
                 if (r < len) {
-                    const size_t o = ((size_t)(t0 + r) * H + h) * D + i;
-                    dq[o] = dqv;
-                    dk[o] = dkv;
+                    const size_t o = ((size_t)(t0 + r) * H + h) * D + i0;
+                    *reinterpret_cast<float2 *>(dq + o) = make_float2(dqo[0], dqo[1]);
+                    *reinterpret_cast<float2 *>(dk + o) = make_float2(dko[0], dko[1]);
                 }
             }
-            atomicAdd(&sm[O_DGC + i], colsum);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {  // sum over the 8 row lanes g of each channel
+                cs[u] += __shfl_xor_sync(0xffffffffu, cs[u], 4);
+                cs[u] += __shfl_xor_sync(0xffffffffu, cs[u], 8);
+                cs[u] += __shfl_xor_sync(0xffffffffu, cs[u], 16);
+            }
+            if (g == 0) {  // the warp owns these channels: no other writer now
+                sm[O_DGC + i0] += cs[0];
+                sm[O_DGC + i0 + 1] += cs[1];
+            }
         }
         __syncthreads();
         // dg = reverse cumsum of dGam over the chunk's rows (the last row of the chunk, len - 1 for
@@ -632,11 +663,8 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
                 }
             }
         }
-        // dS <- Diag(gC) dS + Qp^T dO - Kp^T dR (-dR in the dG tile's place is not free: negate
-        // dR in place, it is read no more)
-        for (int e = tid; e < C * D; e += NT) sm[O_DR + (e / D) * LT + e % D] *= -1.f;
-        __syncthreads();
-        state_update<SPLIT>(dS, sm + O_GC, sm + O_QP, sm + O_DO, sm + O_KP, sm + O_DR);
+        // dS <- Diag(gC) dS + Qp^T dO - Kp^T dR (it reads none of what the dg sums read or write)
+        state_update<SPLIT>(dS, sm + O_GC, sm + O_QP, sm + O_DO, sm + O_KP, sm + O_DR, -1.f);
     }
     __syncthreads();
     if (d_init)
