@@ -111,27 +111,28 @@ __device__ __forceinline__ void gate_tile(float *sm, const float *gt) {
     }
 }
 
+// Four consecutive elements of a row as floats (one 8-byte load for bf16, 16-byte for fp32).
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16 *p) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2 *>(p));
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u), __uint_as_float(w.y << 16),
+                       __uint_as_float(w.y & 0xffff0000u));
+}
+__device__ __forceinline__ float4 ld4(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
+
 // Stage up to five [rows, H, D] tensors' chunk rows [t0, t0 + n) into C x LT tiles (rows past n
-// = 0): every load of the thread is issued before any store, so their latencies overlap.
+// = 0); thread e takes row e / 32, channels 4 (e % 32) .. + 3 of each. Every load of the thread is
+// issued before any store, so their latencies overlap.
 template <typename Tin, int NTEN>
 __device__ __forceinline__ void load_tiles(float *const (&dst)[NTEN], const Tin *const (&src)[NTEN], long long t0,
                                            int n, int H, int h) {
-    constexpr int PER = C * D / NT;  // elements per thread per tensor
-    float v[NTEN][PER];
+    static_assert(C * D == 4 * NT, "one 4-element group per thread and tensor");
+    const int r = threadIdx.x / (D / 4), i = 4 * (threadIdx.x % (D / 4));
+    float4 v[NTEN];
 #pragma unroll
     for (int a = 0; a < NTEN; ++a)
+        v[a] = r < n ? ld4(src[a] + ((size_t)(t0 + r) * H + h) * D + i) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < PER; ++q) {
-            const int e = threadIdx.x + q * NT, r = e / D, i = e % D;
-            v[a][q] = r < n ? ld(src[a], ((size_t)(t0 + r) * H + h) * D + i) : 0.f;
-        }
-#pragma unroll
-    for (int a = 0; a < NTEN; ++a)
-#pragma unroll
-        for (int q = 0; q < PER; ++q) {
-            const int e = threadIdx.x + q * NT, r = e / D, i = e % D;
-            dst[a][r * LT + i] = v[a][q];
-        }
+    for (int a = 0; a < NTEN; ++a) *reinterpret_cast<float4 *>(dst[a] + r * LT + i) = v[a];
 }
 
 // ---- products on the tensor cores: warp-level mma.sync m16n8k8 with tf32 operands. With SPLIT = 3
@@ -254,14 +255,21 @@ __device__ __forceinline__ void tile_times_tile_t(float *M, const float *a, cons
 // The chunk's gate products and triangular factors: Kp, Km, Kc (into the tile `kc`), (Qp), Ab,
 // A -> X, T (and T transposed), (P).
 __device__ __forceinline__ void chunk_factors(float *sm, const float *K, float *kc, bool with_q) {
-    for (int e = threadIdx.x; e < C * D; e += NT) {
-        const int r = e / D, i = e % D;
-        const float gm = sm[O_GAM + r * LT + i], k = K[r * LT + i];
-        const float km = __fdividef(k, gm);
-        sm[O_KP + r * LT + i] = k * gm;
-        sm[O_KM + r * LT + i] = km;
-        kc[r * LT + i] = km * sm[O_GC + i];
-        if (with_q) sm[O_QP + r * LT + i] *= gm;  // Q was loaded into the Qp tile
+    {  // thread: row e / 32, channels 4 (e % 32) .. + 3
+        const int r = threadIdx.x / (D / 4), i = 4 * (threadIdx.x % (D / 4)), o = r * LT + i;
+        const float4 gm = *reinterpret_cast<const float4 *>(sm + O_GAM + o);
+        const float4 k = *reinterpret_cast<const float4 *>(K + o);
+        const float4 gc = *reinterpret_cast<const float4 *>(sm + O_GC + i);
+        const float4 km = make_float4(__fdividef(k.x, gm.x), __fdividef(k.y, gm.y), __fdividef(k.z, gm.z),
+                                      __fdividef(k.w, gm.w));
+        *reinterpret_cast<float4 *>(sm + O_KP + o) = make_float4(k.x * gm.x, k.y * gm.y, k.z * gm.z, k.w * gm.w);
+        *reinterpret_cast<float4 *>(sm + O_KM + o) = km;
+        *reinterpret_cast<float4 *>(kc + o) = make_float4(km.x * gc.x, km.y * gc.y, km.z * gc.z, km.w * gc.w);
+        if (with_q) {  // Q was loaded into the Qp tile
+            float4 *qp = reinterpret_cast<float4 *>(sm + O_QP + o);
+            const float4 q = *qp;
+            *qp = make_float4(q.x * gm.x, q.y * gm.y, q.z * gm.z, q.w * gm.w);
+        }
     }
     __syncthreads();
     tile_times_tile_t(sm + O_AB, sm + O_KP, sm + O_KM, 0);
@@ -557,11 +565,14 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
             const float *pO = a_frag_row(sm + O_DO, LT), *pR = a_frag_row(sm + O_DR, LT);
             const float *pU = a_frag_row(sm + O_U, LT);
             const float *pS = b_frag_row(S, LS, n0), *pD = b_frag_row(dS, LS, n0);
+            float dgc = 0.f;  // sum_j dS[n0 + g][j] S[n0 + g][j] over the lane's columns j = t (mod 4)
 #pragma unroll 1
             for (int k = 0; k < D; k += 16) {
                 float bs4[4], bd4[4];
                 ldsm_x4(bs4, pS + k);
                 ldsm_x4(bd4, pD + k);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) dgc = fmaf(bd4[m], bs4[m], dgc);
 #pragma unroll
                 for (int hk = 0; hk < 2; ++hk) {
                     const int kk = k + 8 * hk;
@@ -575,15 +586,9 @@ __global__ void __launch_bounds__(NT, 1) backward_chunked_kernel(RunParams p, co
                     mma3<SPLIT>(cc, au, bd);
                 }
             }
-            if (tid < D) {  // dgC = rowsum(dS * S) for channel tid
-                float dgc = 0.f;
-                for (int j = 0; j < D; j += 4) {
-                    const float4 sv = *reinterpret_cast<const float4 *>(S + tid * LS + j);
-                    const float4 dsv = *reinterpret_cast<const float4 *>(dS + tid * LS + j);
-                    dgc = fmaf(dsv.x, sv.x, fmaf(dsv.y, sv.y, fmaf(dsv.z, sv.z, fmaf(dsv.w, sv.w, dgc))));
-                }
-                atomicAdd(&sm[O_DGC + tid], dgc * sm[O_GC + tid]);
-            }
+            dgc += __shfl_xor_sync(0xffffffffu, dgc, 1);  // over the 4 lanes t of row n0 + g
+            dgc += __shfl_xor_sync(0xffffffffu, dgc, 2);
+            if (t == 0) sm[O_DGC + n0 + g] += dgc * sm[O_GC + n0 + g];  // the warp's own channels
             __syncthreads();  // every warp is done with dO, dR and U as operands
             float *T1 = sm + O_R, *T2 = sm + O_DU, *T3 = sm + O_U;
             const int e0 = g * LT + n0 + 2 * t, e8 = (g + 8) * LT + n0 + 2 * t;
