@@ -216,15 +216,21 @@ template <int SPLIT>
 __device__ __forceinline__ void tile_times_state(float (&c)[4], const float *a, const float *B, int n0) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const float *ap = a_frag_row(a, LT);
+    float c2[4] = {0.f, 0.f, 0.f, 0.f};  // odd k steps: two independent MMA chains
 #pragma unroll
     for (int q = 0; q < 4; ++q) c[q] = 0.f;
-#pragma unroll 4
-    for (int k = 0; k < D; k += 8) {
-        float af[4];
-        ldsm_x4(af, ap + k);
-        const float bf[2] = {B[(k + t) * LS + n0 + g], B[(k + t + 4) * LS + n0 + g]};
-        mma3<SPLIT>(c, af, bf);
+#pragma unroll 2
+    for (int k = 0; k < D; k += 16) {
+        float a0[4], a1[4];
+        ldsm_x4(a0, ap + k);
+        ldsm_x4(a1, ap + k + 8);
+        const float b0[2] = {B[(k + t) * LS + n0 + g], B[(k + t + 4) * LS + n0 + g]};
+        const float b1[2] = {B[(k + 8 + t) * LS + n0 + g], B[(k + 12 + t) * LS + n0 + g]};
+        mma3<SPLIT>(c, a0, b0);
+        mma3<SPLIT>(c2, a1, b1);
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c[q] += c2[q];
 }
 
 // M[r][s] (16 x 16) = sum_i a[r][i] * b[s][i] over the 128 channels, on the tensor cores by the
@@ -235,17 +241,21 @@ __device__ __forceinline__ void tile_times_tile_t(float *M, const float *a, cons
     if (w < 0 || w > 1) return;
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, n0 = 8 * w;
     const float *ap = a_frag_row(a, LT), *bp = b_frag_row(b, LT, n0);
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
+    float acc[4][4] = {};  // four independent MMA chains over the k steps
+#pragma unroll
     for (int k = 0; k < D; k += 16) {
         float a0[4], a1[4], bb[4];
         ldsm_x4(bb, bp + k);
         ldsm_x4(a0, ap + k);
         ldsm_x4(a1, ap + k + 8);
         const float b0[2] = {bb[0], bb[1]}, b1[2] = {bb[2], bb[3]};
-        mma3<3>(c, a0, b0);
-        mma3<3>(c, a1, b1);
+        const int q = (k >> 3) & 2;
+        mma3<3>(acc[q], a0, b0);
+        mma3<3>(acc[q + 1], a1, b1);
     }
+    float c[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c[q] = (acc[0][q] + acc[1][q]) + (acc[2][q] + acc[3][q]);
     M[g * LM + n0 + 2 * t] = c[0];
     M[g * LM + n0 + 2 * t + 1] = c[1];
     M[(g + 8) * LM + n0 + 2 * t] = c[2];
@@ -275,28 +285,66 @@ __device__ __forceinline__ void chunk_factors(float *sm, const float *K, float *
     tile_times_tile_t(sm + O_AB, sm + O_KP, sm + O_KM, 0);
     if (with_q) tile_times_tile_t(sm + O_P, sm + O_QP, sm + O_KM, 2);
     __syncthreads();
-    // X = (I + A)^{-1} for the unit lower-triangular I + A, A = strict_lower(Diag(beta) Ab): column
-    // j by forward substitution (one thread per column); T = X Diag(beta).
-    if (threadIdx.x < C) {
-        const int j = threadIdx.x;
-        float x[C];
+    // X = (I + A)^{-1} for the unit lower-triangular I + A, A = strict_lower(Diag(beta) Ab), by
+    // warp 0 in 8 x 8 blocks: the diagonal blocks X11, X22 by forward substitution (lane j < 16:
+    // column j of its block), then X21 = -X22 (A21 X11) as two 8 x 8 products (two entries per
+    // lane, A21 X11 in the M scratch), X12 = 0; then T = X Diag(beta) and its transpose.
+    static_assert(C == 16, "the blocked solve is written for 16-row chunks");
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        if (lane < C) {
+            const int j = lane, b0 = lane & 8;
+            float x[8];
 #pragma unroll
-        for (int i = 0; i < C; ++i) {
-            float v = (i == j) ? 1.f : 0.f;
-            if (i > j) {
-                const float bi = sm[O_BETA + i];
+            for (int ii = 0; ii < 8; ++ii) {
+                const int i = b0 + ii;
+                float v = (i == j) ? 1.f : 0.f;
+                if (i > j) {
+                    const float bi = sm[O_BETA + i];
 #pragma unroll
-                for (int k = 0; k < C; ++k)
-                    if (k >= j && k < i) v = fmaf(-bi * sm[O_AB + i * LM + k], x[k], v);
+                    for (int kk = 0; kk < ii; ++kk)
+                        if (b0 + kk >= j) v = fmaf(-bi * sm[O_AB + i * LM + b0 + kk], x[kk], v);
+                }
+                x[ii] = v;
             }
-            x[i] = v;
-        }
-        const float bj = sm[O_BETA + j];
 #pragma unroll
-        for (int i = 0; i < C; ++i) {
-            sm[O_X + i * LM + j] = x[i];
-            sm[O_T + i * LM + j] = x[i] * bj;
-            sm[O_TT + j * LM + i] = x[i] * bj;
+            for (int ii = 0; ii < 8; ++ii) sm[O_X + (b0 + ii) * LM + j] = x[ii];
+        }
+        __syncwarp();
+        const int i = 8 + (lane >> 2), j0 = 2 * (lane & 3);  // rows 8..15, columns j0, j0 + 1 of 0..7
+        {
+            const float bi = sm[O_BETA + i];
+            float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float a = bi * sm[O_AB + i * LM + k];
+                y0 = fmaf(a, sm[O_X + k * LM + j0], y0);
+                y1 = fmaf(a, sm[O_X + k * LM + j0 + 1], y1);
+            }
+            sm[O_M + i * LM + j0] = y0;
+            sm[O_M + i * LM + j0 + 1] = y1;
+        }
+        __syncwarp();
+        {
+            float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+            for (int k = 8; k < C; ++k) {
+                const float xk = sm[O_X + i * LM + k];
+                z0 = fmaf(xk, sm[O_M + k * LM + j0], z0);
+                z1 = fmaf(xk, sm[O_M + k * LM + j0 + 1], z1);
+            }
+            sm[O_X + i * LM + j0] = -z0;
+            sm[O_X + i * LM + j0 + 1] = -z1;
+            sm[O_X + (i - 8) * LM + 8 + j0] = 0.f;
+            sm[O_X + (i - 8) * LM + 8 + j0 + 1] = 0.f;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int e = lane; e < C * C; e += 32) {
+            const int r = e / C, c2 = e % C;
+            const float x = sm[O_X + r * LM + c2] * sm[O_BETA + c2];
+            sm[O_T + r * LM + c2] = x;
+            sm[O_TT + c2 * LM + r] = x;
         }
     }
     if (with_q) {  // P = lower(Qp Km^T)
