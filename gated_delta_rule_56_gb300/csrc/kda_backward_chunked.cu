@@ -20,11 +20,12 @@
 // no sub-tiling; each exponent is clamped to +-87 so out-of-range gates stay finite.
 //
 // One CTA of 512 threads per (sequence, head) holds S and dS (fp32, 128 x 128, rows padded to
-// 132 floats so that both column reads and 16-byte row reads are free of bank conflicts) and the chunk's
-// 16 x 128 tiles in shared memory; the large products run on the tensor cores (3 x tf32, see
-// mma3), the small ones and the element-wise steps on the CUDA cores in fp32. A forward sweep
-// stores the state at every chunk start in the workspace; the reverse sweep reads it back.
-// All columns live in one CTA, so every gradient is written directly (no atomics).
+// 132 floats: 16-byte row reads and the 8-row groups of an ldmatrix are free of bank conflicts,
+// fragment reads down a column are 2-way) and the chunk's 16 x 128 tiles in shared memory. Every
+// product runs on the tensor cores as warp MMAs (precision per product: see mma3); the triangular
+// solve and the element-wise steps run on the CUDA cores in fp32. A forward sweep stores the
+// state at every chunk start in the workspace; the reverse sweep reads it back. All columns live
+// in one CTA, so every gradient is written directly (no atomics).
 #include "kda_internal.h"
 
 namespace kda {
@@ -139,11 +140,12 @@ __device__ __forceinline__ void load_tiles(float *const (&dst)[NTEN], const Tin 
 // every fp32 operand x is split into a tf32 high part and the tf32 rounding of the rest, and a
 // product is taken as lo*hi + hi*lo + hi*hi (the lo*lo term is below fp32 rounding), so the result
 // keeps fp32 accuracy; with SPLIT = 1 a product is the single tf32 one. The 16 x 16 chunk factors
-// (Ab, P, dP, dT) always take SPLIT = 3: they cost little and feed the cancelling sums behind dbeta
-// and dq, whose error single tf32 products there raise tenfold. The state-sized products take
-// SPLIT = 3 for fp32 inputs and SPLIT = 1 for bf16 inputs (rounded to 2^-9 already, coarser than
-// tf32's 2^-11): gradients then agree with the fp64 adjoint to about 3e-4 relative (Frobenius)
-// instead of 2e-6, in three quarters of the time.
+// (Ab, P, dP, dT) and every product with a 16 x 16 factor matrix always take SPLIT = 3: they cost
+// little and feed the cancelling sums behind dbeta and dq, whose error single tf32 products there
+// raise several times. The products with the 128 x 128 states take SPLIT = 3 for fp32 inputs and
+// SPLIT = 1 for bf16 inputs (rounded to 2^-9 already, coarser than tf32's 2^-11): gradients then
+// agree with the fp64 adjoint to about 3e-4 relative (Frobenius) instead of 2e-6, in three
+// quarters of the time.
 // Fragment of lane l (g = l / 4, t = l % 4): A (16 x 8) rows g, g + 8 and columns t, t + 4;
 // B (8 x 8) rows t, t + 4 and column g; C (16 x 8) rows g, g + 8, columns 2t, 2t + 1.
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
