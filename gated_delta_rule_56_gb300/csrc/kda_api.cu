@@ -452,6 +452,9 @@ kda_status kda_backward(kda_dtype dtype, int B, int T, int H, int dk, int dv, co
             (st = check_ptr(dk_out, "dk", true)) || (st = check_ptr(dv_out, "dv", true)) ||
             (st = check_ptr(dg, "dg", true)) || (st = check_ptr(dbeta, "dbeta", false)))
             return st;
+        if ((reinterpret_cast<uintptr_t>(beta) & (dtype == KDA_BF16 ? 1u : 3u)) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "beta is not aligned to its element size");
+        if ((reinterpret_cast<uintptr_t>(dbeta) & 3u) != 0) return fail(KDA_ERR_INVALID_ARG, "dbeta is not 4-byte aligned");
     }
     if ((initial_state && !aligned16(initial_state)) || (d_final_state && !aligned16(d_final_state)) ||
         (d_initial_state && !aligned16(d_initial_state)))

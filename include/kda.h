@@ -175,7 +175,10 @@ KDA_API kda_status kda_decode_step_ex(kda_dtype dtype, int N, int H, int dk, int
  * workspace    device scratch of at least kda_backward_workspace_size() bytes, 16-byte aligned,
  *              owned by the caller: the state at every chunk start (every 16 tokens for d = 128,
  *              every 64 for d = 32, 64), d * d * 4 bytes per head and chunk.
- * Supported: dk == dv in {32, 64, 128}; bf16 or fp32 inputs. Alignment as kda_prefill.
+ * Supported: dk == dv in {32, 64, 128}; bf16 or fp32 inputs. Alignment as kda_prefill for the
+ * inputs (d_o as o); dq, dk, dv, dg and the state pointers 16-byte aligned, dbeta 4-byte aligned.
+ * Errors: KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED for malformed arguments, found on the host
+ * before anything is queued (also a workspace that is missing, short or misaligned).
  */
 KDA_API kda_status kda_backward(kda_dtype dtype, int B, int T, int H, int dk, int dv,
                                 const void *q, const void *k, const void *v, const void *g,

@@ -119,6 +119,60 @@ def test_prefill_rejects_bad_arguments_on_host(lib, case, expect):
     assert kda.last_error() != ""
 
 
+def _backward(lib, dtype=0, B=1, T=64, H=2, dk=128, dv=128, ptrs=None, cu=None, n=0, init=None, dfin=None,
+              dinit=None, ws=FAKE, ws_bytes=None):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, d_o=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, dg=FAKE, dbeta=FAKE)
+    p.update(ptrs or {})
+    if ws_bytes is None:
+        ws_bytes = lib.kda_backward_workspace_size(dtype, B, T, H, 128, 128, n)
+    return lib.kda_backward(dtype, B, T, H, dk, dv, p["q"], p["k"], p["v"], p["g"], p["beta"], cu, n, init, p["d_o"],
+                            dfin, p["dq"], p["dk"], p["dv"], p["dg"], p["dbeta"], dinit, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(dtype=7), _lib.KDA_ERR_INVALID_ARG),
+    (dict(B=-1), _lib.KDA_ERR_INVALID_ARG),
+    (dict(dk=48, dv=48), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(dk=128, dv=64), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(B=2, cu=FAKE, n=2), _lib.KDA_ERR_INVALID_ARG),
+    (dict(cu=FAKE + 2, n=1), _lib.KDA_ERR_INVALID_ARG),
+    (dict(cu=FAKE, n=-1), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ptrs=dict(q=None)), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ptrs=dict(d_o=None)), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ptrs=dict(dbeta=None)), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ptrs=dict(dq=FAKE + 8)), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ptrs=dict(d_o=FAKE + 4)), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ptrs=dict(beta=FAKE + 1)), _lib.KDA_ERR_INVALID_ARG),
+    (dict(dtype=1, ptrs=dict(beta=FAKE + 2)), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ptrs=dict(dbeta=FAKE + 2)), _lib.KDA_ERR_INVALID_ARG),
+    (dict(init=FAKE + 4), _lib.KDA_ERR_INVALID_ARG),
+    (dict(dfin=FAKE + 8), _lib.KDA_ERR_INVALID_ARG),
+    (dict(dinit=FAKE + 4), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ws=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ws=FAKE + 8), _lib.KDA_ERR_INVALID_ARG),
+    (dict(ws_bytes=1024), _lib.KDA_ERR_INVALID_ARG),
+])
+def test_backward_rejects_bad_arguments_on_host(lib, case, expect):
+    st = _backward(lib, **case)
+    assert st == expect, (case, kda.status_string(st), kda.last_error())
+    assert kda.last_error() != ""
+
+
+def test_backward_workspace_sizes(lib):
+    """One d x d fp32 state per head and chunk start (16-token chunks for d = 128, 64 for d = 32
+    and 64), plus one slot per sequence and a spare."""
+    assert lib.kda_backward_workspace_size(0, 4, 8192, 32, 128, 128, 0) == (8192 * 4 // 16 + 4 + 1) * 32 * 128 * 128 * 4
+    assert lib.kda_backward_workspace_size(1, 1, 1000, 3, 64, 64, 5) == (1000 // 64 + 5 + 1) * 3 * 64 * 64 * 4
+    assert lib.kda_backward_workspace_size(0, 1, 10, 2, 128, 64, 0) == 0  # dk != dv: unsupported
+
+
+def test_empty_backward_is_a_no_op(lib):
+    # No (sequence, head) pair: nothing is queued and no device is needed.
+    none = dict(q=None, k=None, v=None, g=None, beta=None, d_o=None, dq=None, dk=None, dv=None, dg=None, dbeta=None)
+    assert _backward(lib, B=0, ptrs=none, ws=None, ws_bytes=0) == 0
+    assert _backward(lib, H=0, ptrs=none, ws=None, ws_bytes=0) == 0
+
+
 def test_empty_prefill_is_a_no_op(lib):
     # No (sequence, head) pair: nothing is queued and no device is needed.
     assert _prefill(lib, B=0, ptrs=dict(q=None, k=None, v=None, g=None, beta=None, o=None)) == 0
