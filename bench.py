@@ -563,6 +563,9 @@ def run_workload(args):
     # horizon, the zero test, the transition pass over the rest, the scan and the correction.
     split = args.workload not in ("varlen", "backward") and kda.load().kda_prefill_workspace_size(0, n_seq, tokens // n_seq, H, d, d, n_seq) > 0
     launches_per_step = 7 if split else 1
+    # Packed sequences with the workspace: the longest-first sort of cu_seqlens, then the prefill.
+    if args.workload == "varlen" and kda.load().kda_prefill_workspace_size(0, 1, tokens, H, d, d, n_seq) > 0:
+        launches_per_step = 2
 
     def step(_i):
         if args.workload == "backward":
