@@ -220,6 +220,7 @@ def recorded_traffic(key, files):
 
 PREFILL_SOURCES = ["gated_delta_rule_56_gb300/csrc/kda_prefill_tc.cu", "gated_delta_rule_56_gb300/csrc/kda_tc.cuh"]
 DECODE_SOURCES = ["gated_delta_rule_56_gb300/csrc/kda_recurrent.cu"]
+BACKWARD_SOURCES = ["gated_delta_rule_56_gb300/csrc/kda_backward_chunked.cu"]
 
 
 def prefill_bytes(B, T, H, d):
@@ -591,6 +592,7 @@ def run_workload(args):
                 "frac": ach / peak_tf32,
                 "peak_source": f"{peak_kind} bf16 burst x 1.1/2.25 (nominal dense tf32/bf16)",
                 "alg_flops_per_launch": alg, "kernel_ms": kernel_ms,
+                "traffic": recorded_traffic("backward", existing_files(BACKWARD_SOURCES)),
                 "fp32_alu": {"peak": FP32_ALU_TFLOPS, "frac": ach / FP32_ALU_TFLOPS,
                              "peak_source": "derived from unit counts and the maximum SM clock"}}
         launches_per_step = 1  # d = 128: the chunked kernel writes every output itself (no fills)
