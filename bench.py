@@ -74,8 +74,10 @@ def parse(argv=None):
     ap.add_argument("--ncu-case", choices=("prefill", "decode", "backward"),
                     help="run two launches of the small profiling case (for ncu) and exit")
     args = ap.parse_args(argv)
-    if args.warmup < 3:
-        ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
+    # At least 3 untimed warm-up steps whatever is asked; the JSON line reports the count run.
+    args.warmup = max(args.warmup, 3)
     return args
 
 

@@ -7,6 +7,8 @@ import os
 import subprocess
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
@@ -43,3 +45,16 @@ def test_reference_arm_other_ranks_exit_without_work():
     r = _run(RANK="1", LOCAL_RANK="1", WORLD_SIZE="2")
     assert r.returncode == 0, r.stderr[-2000:]
     assert _json_lines(r.stdout) == []
+
+
+def test_bench_defaults_and_warmup_floor():
+    """No flags: one GPU, the headline arm, a bounded number of steps; never fewer than 3
+    warm-up steps (a smaller request runs 3 and the line reports 3)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    a = bench.parse([])
+    assert a.gpus == 1 and a.impl == "ours" and a.warmup >= 3 and 1 <= a.steps <= 1000 and a.workload is None
+    assert bench.parse(["--warmup", "1"]).warmup == 3
+    assert bench.parse(["--impl", "reference", "--gpus", "4", "--steps", "7", "--warmup", "9"]).warmup == 9
+    with pytest.raises(SystemExit):
+        bench.parse(["--steps", "0"])
