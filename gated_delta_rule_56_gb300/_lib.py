@@ -60,6 +60,8 @@ def load():
         lib.kda_prefill.restype = _i
         lib.kda_prefill_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
         lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+        lib.kda_prefill_split_plan.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp]
+        lib.kda_prefill_split_plan.restype = _i
         lib.kda_decode_step.argtypes = [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         lib.kda_decode_step.restype = _i
         lib.kda_check_status.argtypes = [_vp]
@@ -323,6 +325,17 @@ def backward(q, k, v, g, beta, d_o, cu_seqlens=None, initial_state=None, d_final
                               _ptr(ws), ws_bytes, _stream(dev))
     _raise_if(st)
     return out
+
+
+def prefill_split_plan(B: int, T: int, H: int, sm_count: int):
+    """How ``prefill`` splits B sequences of T tokens and H heads along the sequence on a GPU with
+    ``sm_count`` SMs (bf16, d = 128, no cu_seqlens): (segments per sequence, rows per segment,
+    workspace bytes); (0, 0, 0) for a single pass. Host arithmetic only (kda_prefill_split_plan)."""
+    lib = load()
+    P, Ls, nbytes = ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+    _raise_if(lib.kda_prefill_split_plan(int(B), int(T), int(H), int(sm_count), ctypes.byref(P), ctypes.byref(Ls),
+                                         ctypes.byref(nbytes)))
+    return P.value, Ls.value, nbytes.value
 
 
 def selftest_wait_timeout(limit_ns: int, device=None):

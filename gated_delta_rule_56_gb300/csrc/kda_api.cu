@@ -353,6 +353,16 @@ size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, 
     return segmented_workspace_bytes(dtype, B, T, H, dk, dv, false);
 }
 
+kda_status kda_prefill_split_plan(int B, int T, int H, int sm_count, int *segments, int *segment_rows,
+                                  size_t *workspace_bytes) {
+    if (!segments || !segment_rows || !workspace_bytes)
+        return fail(KDA_ERR_INVALID_ARG, "NULL output pointer");
+    if (B < 0 || T < 0 || H < 0 || sm_count < 0)
+        return fail(KDA_ERR_INVALID_ARG, "negative size B=%d T=%d H=%d sm_count=%d", B, T, H, sm_count);
+    segmented_plan_for(B, T, H, sm_count, segments, segment_rows, workspace_bytes);
+    return ok();
+}
+
 kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,
                        const void *k, const void *v, const void *g, const void *beta,
                        const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,

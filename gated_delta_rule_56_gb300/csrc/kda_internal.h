@@ -55,6 +55,9 @@ bool encode_row_tile_map(CUtensorMap *map, const void *base, long long rows, int
 // Segmented prefill of few long sequences (see kda_segmented.cu): workspace bytes it needs for
 // this call (0: the call is not eligible), and the launch sequence.
 size_t segmented_workspace_bytes(kda_dtype dtype, int B, int T, int H, int dk, int dv, bool varlen);
+// The same plan for a GPU with `sms` SMs (host arithmetic only): segments per sequence (0: not
+// split), rows per segment and workspace bytes.
+void segmented_plan_for(int B, int T, int H, int sms, int *P, int *Ls, size_t *bytes);
 cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace, size_t workspace_bytes,
                                      cudaStream_t s);
 

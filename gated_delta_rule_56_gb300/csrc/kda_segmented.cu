@@ -47,13 +47,11 @@ struct Plan {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Segment count and workspace layout, or P == 0 when a single pass is the better choice.
-Plan make_plan(int B, int T, int H) {
+// Segment count and workspace layout on a GPU with `sms` SMs, or P == 0 when a single pass is
+// the better choice.
+Plan make_plan_for(int B, int T, int H, int sms) {
     Plan pl;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return pl;
+    if (sms <= 0) return pl;
     const long long pairs = (long long)B * H;
     if (pairs <= 0 || T <= 0) return pl;
     // One wave: as many segments as fit next to each other on the SMs. (A split into several
@@ -81,6 +79,15 @@ Plan make_plan(int B, int T, int H) {
     off = align256(off + (size_t)segs * H);
     pl.bytes = off;
     return pl;
+}
+
+// The plan for the current device.
+Plan make_plan(int B, int T, int H) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return Plan{};
+    return make_plan_for(B, T, H, sms);
 }
 
 // cu_seqlens of the segments as packed sequences: segment p of sequence b covers rows
@@ -342,6 +349,13 @@ constexpr int kScanSmem = 128 * 132 * 4;
 constexpr int kCorrectSmem = 65536 + 64 + 1024;  // A, B, barriers, TMEM address, block max
 
 }  // namespace
+
+void segmented_plan_for(int B, int T, int H, int sms, int *P, int *Ls, size_t *bytes) {
+    const Plan pl = (long long)B * T >= 0x7fffffffLL - 64 ? Plan{} : make_plan_for(B, T, H, sms);
+    *P = pl.P;
+    *Ls = pl.Ls;
+    *bytes = pl.bytes;
+}
 
 size_t segmented_workspace_bytes(kda_dtype dtype, int B, int T, int H, int dk, int dv, bool varlen) {
     if (dtype != KDA_BF16 || dk != D || dv != D || varlen) return 0;

@@ -136,6 +136,21 @@ KDA_API size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, 
                                   int n_seqs);
 
 /*
+ * kda_prefill_split_plan -- how kda_prefill splits B sequences of T tokens and H heads along the
+ * sequence (bf16, dk == dv == 128, no cu_seqlens, with the workspace) on a GPU with sm_count SMs;
+ * host arithmetic only, nothing is queued and no device is needed. The state after a segment is
+ * affine in the state before it ("Inside Kimi K3's Architecture", "Kimi Delta Attention: the
+ * linear core": the per-token transition does not depend on the state), so segments run side by
+ * side and are joined exactly afterwards. Outputs: *segments = P segments per sequence (0: a
+ * single pass; P = min(8, sm_count / (B H), T / 2048) when that is at least 2), *segment_rows =
+ * rows per segment (a multiple of 64; the last segment may be shorter; 0 when not split),
+ * *workspace_bytes = what kda_prefill_workspace_size returns on such a GPU. Returns
+ * KDA_ERR_INVALID_ARG for negative sizes or a NULL output pointer.
+ */
+KDA_API kda_status kda_prefill_split_plan(int B, int T, int H, int sm_count, int *segments, int *segment_rows,
+                                          size_t *workspace_bytes);
+
+/*
  * kda_prefill_ex / kda_decode_step_ex -- kda_prefill / kda_decode_step with options (see
  * kda_options; NULL = none). Returns KDA_ERR_INVALID_ARG for a struct_size below sizeof(size_t)
  * or above 4096, or a gate_bound that is negative, not finite or above 1e4; every other

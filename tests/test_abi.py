@@ -173,6 +173,49 @@ def test_empty_backward_is_a_no_op(lib):
     assert _backward(lib, H=0, ptrs=none, ws=None, ws_bytes=0) == 0
 
 
+def test_split_plan_of_the_workloads(lib):
+    """On 152 SMs: the B=4 T=8192 H=32 shape (128 pairs) runs as one pass; the 1,048,576-token
+    sequence (32 pairs) is cut into 4 segments of 262,144 rows, one CTA per (segment, head)."""
+    assert kda.prefill_split_plan(4, 8192, 32, 152) == (0, 0, 0)
+    P, Ls, nbytes = kda.prefill_split_plan(1, 1 << 20, 32, 152)
+    assert (P, Ls) == (4, 1 << 18)
+    # the workspace holds at least the bf16 transition outputs of every row and two fp32 states
+    # per (segment, head)
+    assert nbytes % 256 == 0 and nbytes >= (1 << 20) * 32 * 128 * 2 + 2 * 4 * 32 * 128 * 128 * 4
+    assert kda.prefill_split_plan(1, 1 << 20, 32, 64) == (2, 1 << 19, kda.prefill_split_plan(1, 1 << 20, 32, 64)[2])
+    assert kda.prefill_split_plan(1, 4095, 8, 152)[0] == 0  # under two segments of 2048 rows
+    assert kda.prefill_split_plan(1, 1 << 20, 32, 0) == (0, 0, 0)  # no SMs: nothing to plan for
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_split_plan_invariants(lib, seed):
+    """Random sizes: P = min(8, SMs / pairs, T / 2048) when that is at least 2 (the rounding of the
+    rows to 64 never loses a segment here), segments of a multiple of 64 rows that cover T with
+    the last one non-empty, and B P H CTAs that fit one wave."""
+    import random
+    rnd = random.Random(seed)
+    for _ in range(300):
+        B, H, sms = rnd.randint(1, 4), rnd.randint(1, 40), rnd.choice([132, 148, 152, 160])
+        T = rnd.randint(1, 1 << 21)
+        P, Ls, nbytes = kda.prefill_split_plan(B, T, H, sms)
+        want = min(8, sms // (B * H), T // 2048)
+        if want < 2:
+            assert (P, Ls, nbytes) == (0, 0, 0), (B, T, H, sms)
+            continue
+        assert P == want, (B, T, H, sms, P, want)
+        assert Ls % 64 == 0 and (P - 1) * Ls < T <= P * Ls, (B, T, H, P, Ls)
+        assert B * P * H <= sms
+        assert nbytes % 256 == 0 and nbytes >= B * T * H * 128 * 2
+
+
+def test_split_plan_rejects_bad_arguments(lib):
+    with pytest.raises(kda.KDAError):
+        kda.prefill_split_plan(-1, 10, 2, 152)
+    with pytest.raises(kda.KDAError):
+        kda.prefill_split_plan(1, 10, 2, -5)
+    assert lib.kda_prefill_split_plan(1, 10, 2, 152, None, None, None) == _lib.KDA_ERR_INVALID_ARG
+
+
 def test_empty_prefill_is_a_no_op(lib):
     # No (sequence, head) pair: nothing is queued and no device is needed.
     assert _prefill(lib, B=0, ptrs=dict(q=None, k=None, v=None, g=None, beta=None, o=None)) == 0
