@@ -35,9 +35,10 @@ constexpr int D = 128;
 constexpr int C = 16;                  // tokens per chunk
 constexpr int NT = 512;                // threads per CTA
 constexpr int LS = D + 4;              // row stride of S and dS (floats): 16-byte rows, and row i
-                                       // starts 33 i 16-byte units in (i mod 8 distinct), so both
-                                       // column reads and 16-byte row reads across rows are free of
-                                       // bank conflicts
+                                       // starts 33 i 16-byte units in (i mod 8 distinct), so 16-byte
+                                       // reads of 8 consecutive rows (an ldmatrix phase) are free of
+                                       // bank conflicts; fragment reads down a column (rows t, t + 4
+                                       // across 8 columns) are 2-way
 constexpr int LT = D + 4;              // row stride of a 16 x 128 tile (floats; 16-byte rows)
 constexpr int LM = C + 4;              // row stride of a 16 x 16 matrix (16-byte rows)
 
@@ -64,7 +65,7 @@ constexpr int O_DAB = O_DT + C * LM;   // Diag(beta) dA
 constexpr int O_M = O_DAB + C * LM;    // scratch 16 x 16
 constexpr int O_TT = O_M + C * LM;     // T transposed
 constexpr int O_BETA = O_TT + C * LM;  // [C]
-constexpr int O_DB = O_BETA + C;       // [C] dbeta
+constexpr int O_DB = O_BETA + C;       // [C] spare (unused; keeps the offsets below)
 constexpr int O_GC = O_DB + C;         // [D] gC
 constexpr int O_DGC = O_GC + D;        // [D] dgC gC + colsum(dKc Kc)
 constexpr int FLOATS = O_DGC + D;
@@ -358,7 +359,8 @@ __device__ __forceinline__ void chunk_factors(float *sm, const float *K, float *
     __syncthreads();
 }
 
-// The fragment element pairs (g, n0 + 2t, + 1) and (g + 8, n0 + 2t, + 1) of a 16 x 128 tile.
+// Elements (row, n0 + 2t) and (row, n0 + 2t + 1) of a 16 x 128 tile as one 8-byte pair: the
+// lane's half of a C fragment row (row g or g + 8).
 __device__ __forceinline__ float2 *frag_pair(float *tile, int row, int n0) {
     const int t = threadIdx.x & 3;
     return reinterpret_cast<float2 *>(tile + row * LT + n0 + 2 * t);
