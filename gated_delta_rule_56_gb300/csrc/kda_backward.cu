@@ -20,6 +20,9 @@
 // all columns: per kSub tokens the warps add their parts in shared
 // memory, then the CTA adds the block to the fp32 outputs with global atomics (one per column
 // block); dv and dS_initial belong to one column and are stored directly.
+//
+// This kernel serves d_k = d_v in {32, 64}; launch_backward sends d = 128 to the chunkwise
+// tensor-core kernel of kda_backward_chunked.cu, which writes every output itself.
 #include "kda_internal.h"
 
 namespace kda {
