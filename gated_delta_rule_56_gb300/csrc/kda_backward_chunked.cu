@@ -141,10 +141,11 @@ __device__ __forceinline__ void load_tiles(float *const (&dst)[NTEN], const Tin 
 // every fp32 operand x is split into a tf32 high part and the tf32 rounding of the rest, and a
 // product is taken as lo*hi + hi*lo + hi*hi (the lo*lo term is below fp32 rounding), so the result
 // keeps fp32 accuracy; with SPLIT = 1 a product is the single tf32 one. The 16 x 16 chunk factors
-// (Ab, P, dP, dT) and every product with a 16 x 16 factor matrix always take SPLIT = 3: they cost
-// little and feed the cancelling sums behind dbeta and dq, whose error single tf32 products there
-// raise several times. The products with the 128 x 128 states take SPLIT = 3 for fp32 inputs and
-// SPLIT = 1 for bf16 inputs (rounded to 2^-9 already, coarser than tf32's 2^-11): gradients then
+// (Ab, P, dP, dT), U = T R, dR = T^T dU and the finishing products with dP and dAb always take
+// SPLIT = 3: they cost little and feed the cancelling sums behind dbeta and dq, whose error single
+// tf32 products there raise several times. The products with the 128 x 128 states, and P^T dO
+// (which shares its accumulator with Kc dS'), take SPLIT = 3 for fp32 inputs and SPLIT = 1 for
+// bf16 inputs (rounded to 2^-9 already, coarser than tf32's 2^-11): gradients then
 // agree with the fp64 adjoint to about 3e-4 relative (Frobenius) instead of 2e-6, in three
 // quarters of the time.
 // Fragment of lane l (g = l / 4, t = l % 4): A (16 x 8) rows g, g + 8 and columns t, t + 4;

@@ -1,0 +1,94 @@
+"""The method's degenerate cases on the GPU against the fp64 oracle.
+
+* no decay (g = 0): the state only accumulates corrected writes;
+* the decay bound on every channel (g = -5): exp(-Gam) spans e^{320} over a 64-token chunk, the
+  range the tensor-core kernel's per-half reference rows are built for (factors that underflow
+  only drop contributions below 1e-38);
+* beta = 0: nothing is written; the initial state only decays and is read;
+* k = 0: nothing is written or corrected either, through the key side.
+
+In the last two the state only decays, so their gates are scaled by 0.1 to keep it inside fp32's
+range over the sequence (with the workloads' gates it falls to ~1e-147, which fp32 holds as 0).
+A reference that is below 1e-30 everywhere (the saturated backward's gradient of the initial
+state, decayed by e^{-350}) is compared in absolute terms: the GPU's value must be as small.
+
+Tensor-core prefill (bf16, d = 128, ragged tail), the CUDA-core path (fp32, d = 64), one decode
+step and the backward (without a d_final_state: with no decay it would reach every token at full
+weight and only scale the gradients up), each with a random initial state.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_56_gb300 as kda
+import kda_inputs as ki
+import oracle
+from kda_testutil import assert_close, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+NAMES = ("q", "k", "v", "g", "beta")
+KINDS = ("no_decay", "saturated", "beta0", "k0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    kda.load()
+
+
+def _degenerate(x, kind):
+    if kind == "no_decay":
+        x["g"] = torch.zeros_like(x["g"])
+    elif kind == "saturated":
+        x["g"] = torch.full_like(x["g"], -5.0)
+    elif kind == "beta0":
+        x["beta"] = torch.zeros_like(x["beta"])
+        x["g"] = x["g"] * 0.1
+    elif kind == "k0":
+        x["k"] = torch.zeros_like(x["k"])
+        x["g"] = x["g"] * 0.1
+    return x
+
+
+def _close(got, ref, name):
+    ref64 = to64(ref)
+    if np.abs(ref64).max(initial=0.0) < 1e-30:  # below fp32's range for relative precision
+        g = to64(got)
+        assert np.all(np.isfinite(g)) and np.abs(g).max(initial=0.0) <= 1e-30, name
+        return
+    assert_close(got, ref, name)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_prefill_degenerate(kind, dtype, d):
+    x = _degenerate(ki.prefill_inputs(2, 150, 2, d, d, dtype=dtype, device=DEV, seed=41, state_std=0.02), kind)
+    o, s = kda.prefill(*(x[n] for n in NAMES), initial_state=x["initial_state"])
+    kda.check_status()
+    ro, rs = oracle.recurrent(*(x[n].cpu() for n in NAMES), initial_state=x["initial_state"].cpu())
+    _close(o, ro, f"o ({kind})")
+    _close(s, rs, f"final_state ({kind})")
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_decode_degenerate(kind):
+    x = ki.decode_inputs(1, 8, 4, 128, 128, device=DEV, seed=42)
+    x = _degenerate({n: (x[n][0] if n in NAMES else x[n]) for n in x}, kind)
+    state = x["state"].clone()
+    o = kda.decode_step(*(x[n] for n in NAMES), state)
+    kda.check_status()
+    ro, rs = oracle.decode_step(*(x[n].cpu() for n in NAMES), x["state"].cpu())
+    _close(o, ro, f"o ({kind})")
+    _close(state, rs, f"state ({kind})")
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_backward_degenerate(kind):
+    x = _degenerate(ki.prefill_inputs(1, 70, 2, 128, 128, device=DEV, seed=43, state_std=0.02), kind)
+    do = ki.gate_logits_like(x["v"], seed=44)
+    got = kda.backward(*(x[n] for n in NAMES), do, initial_state=x["initial_state"])
+    kda.check_status()
+    ref = oracle.backward(*(x[n].cpu() for n in NAMES), do.cpu(), initial_state=x["initial_state"].cpu())
+    for name in ("dq", "dk", "dv", "dg", "dbeta", "d_initial_state"):
+        _close(got[name], ref[name], f"{name} ({kind})")
