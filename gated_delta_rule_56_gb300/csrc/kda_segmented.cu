@@ -1,8 +1,8 @@
 // kda_segmented.cu -- prefill of a few long sequences, split along the sequence so that more
 // CTAs than (sequence, head) pairs share the work.
 //
-// The recurrence of "Kimi Delta Attention: the linear core" (maidul-haque blog) is linear in the
-// state: over a segment p of a sequence, S_t = M_{p,t} S_start + S^loc_t, where S^loc_t is the
+// The recurrence of "Kimi Delta Attention: the linear core" (maidul-haque blog) is affine in the
+// state (its per-token transition does not depend on it): over a segment p of a sequence, S_t = M_{p,t} S_start + S^loc_t, where S^loc_t is the
 // state reached from zero and M_{p,t} the product of the segment's per-token transitions
 // (I - beta k k^T) Diag(exp g) up to t. The read-out is then
 //     o_t = S_t^T q_t = (S^loc_t)^T q_t + S_start^T (M_{p,t}^T q_t) = o^loc_t + S_start^T qt_t.
