@@ -28,11 +28,13 @@ struct RunParams {
     // Tensor-core kernel only (segment transitions of the segmented long-sequence prefill):
     bool zero_v;                // v taken as 0 (the v tensor is not read)
     bool identity_init;         // initial state = identity (needs d_k == d_v; init is not read)
+    // Options of both the tensor-core and the recurrent kernel:
     bool qk_l2norm;             // q and k rows divided by sqrt(sum x^2 + 1e-6) in the kernel
     const int32_t *init_idx;    // non-null: init is a pool; sequence n starts from state init_idx[n] (< 0: zero)
     const int32_t *fin_idx;     // non-null: fin is a pool; sequence n ends in state fin_idx[n] (< 0: not written)
     int pool;                   // states in the pool(s) when an index array is given
     const void *out_gate;       // non-null: o is multiplied by sigmoid(out_gate) (same layout and dtype as o)
+    // Tensor-core kernel only (launch order of packed sequences; passes of the split prefill):
     const int32_t *order;       // non-null: CTA block b / H runs sequence order[b / H] (a permutation)
     int max_chunks;             // > 0: only the first max_chunks chunks of every sequence are run
     const uint8_t *skip;        // non-null: the CTA of (sequence n, head h) exits at once if skip[n*H + h]
