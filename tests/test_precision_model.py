@@ -10,6 +10,9 @@ degenerate inputs (no decay, g = -5 everywhere, beta = 0, k = 0):
   o rounded to bf16 once;
 * the d = 128 backward for bf16 inputs: tf32 rounding of the operands of the products with the
   128 x 128 states and of P^T dO, fp32-accurate (3 x tf32) products elsewhere.
+* the split along the sequence: the local pass and the transition pass (v = 0 from the identity)
+  as tensor-core prefills, the scan S_start <- M S_start + S_loc in fp32, and the correction
+  o += q~ S_start from bf16 q~ and S_start onto the already rounded o, rounded again.
 
 On GB300 the emulations reproduce the measured errors of the existing cases within about 1.5x, so
 a change of either scheme can be checked against the bar here before it reaches a GPU.
@@ -107,6 +110,21 @@ def prefill_model(q, k, v, g, beta, S0):
     return o, S
 
 
+def split_model(q, k, v, g, beta, S0, P):
+    """The split path with P segments of a multiple of 64 rows."""
+    T = q.shape[0]
+    per = -(-T // P)              # ceil(T / P)
+    Ls = -(-per // 64) * 64       # rounded up to whole chunks
+    o, S_start = np.zeros_like(v), S0.copy()
+    for t0 in range(0, T, Ls):
+        sl = slice(t0, min(t0 + Ls, T))
+        o_loc, s_loc = prefill_model(q[sl], k[sl], v[sl], g[sl], beta[sl], np.zeros_like(S0))
+        qt, M = prefill_model(q[sl], k[sl], np.zeros_like(v[sl]), g[sl], beta[sl], np.eye(S0.shape[0]))
+        o[sl] = bf16(f32(o_loc + f32(qt @ bf16(S_start))))
+        S_start = f32(f32(M @ S_start) + s_loc)
+    return o, S_start
+
+
 # ---------------------------------------------------------------- d = 128 backward, bf16 inputs ---
 
 def _bwd_forward(S, q, k, v, g, beta):
@@ -198,3 +216,17 @@ def test_backward_precision_scheme_meets_the_bar(kind):
     for n in ("dq", "dk", "dv", "dg", "dbeta"):
         _check(got[n], ref[n][0, :, 0], f"{n} ({kind})")
     _check(got["d_initial_state"], ref["d_initial_state"][0, 0], f"d_initial_state ({kind})")
+
+
+@pytest.mark.parametrize("decay", [1.0, 0.002])
+def test_split_precision_scheme_meets_the_bar(decay):
+    """8192 tokens in 4 segments, with the workloads' gates and with log-decays in (-0.01, 0) (each
+    segment's start state matters for its whole length)."""
+    x = ki.prefill_inputs(1, 8192, 1, 128, 128, seed=52, state_std=0.02)
+    x["g"] = (x["g"].float() * decay).to(torch.bfloat16)
+    ro, rs = oracle.recurrent(*(x[n] for n in NAMES), initial_state=x["initial_state"])
+    a = lambda t: t[0, :, 0].double().numpy()
+    o, S = split_model(a(x["q"]), a(x["k"]), a(x["v"]), a(x["g"]), x["beta"][0, :, 0].double().numpy(),
+                       x["initial_state"][0, 0].double().numpy(), 4)
+    _check(o, ro[0, :, 0], f"o (decay x{decay})")
+    _check(S, rs[0, 0], f"final state (decay x{decay})")
