@@ -63,6 +63,8 @@ def parse(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="leave the varlen and long-context sub-lines out of the default line")
     ap.add_argument("--workload", choices=("varlen", "long", "gated", "l2norm", "outgate", "backward"), default=None,
                     help="time one of the other prefill workloads instead of the headline (one JSON line): "
                          "varlen = 64 packed sequences of U[128, 16384] tokens with initial states; "
@@ -71,7 +73,7 @@ def parse(argv=None):
                          "l2norm = the headline shape with raw q/k rows L2-normalised in the kernel; "
                          "outgate = the headline shape with the output gate o * sigmoid(z) in the kernel; "
                          "backward = all gradients of the headline shape (kda_backward)")
-    ap.add_argument("--ncu-case", choices=("prefill", "decode", "backward"),
+    ap.add_argument("--ncu-case", choices=("prefill", "decode", "decode256", "backward", "long", "varlen"),
                     help="run two launches of the small profiling case (for ncu) and exit")
     args = ap.parse_args(argv)
     if args.steps < 1:
@@ -319,10 +321,13 @@ def run_ours(args):
 
     if not args.no_e2e:
         line["e2e"] = run_e2e(args, kda, x, ranks, tokens)
+    del x, args_in, o, fin
+    torch.cuda.empty_cache()
     if not args.no_decode:
-        del x, args_in, o, fin
-        torch.cuda.empty_cache()
         line["decode"] = run_decode(args, kda, ki, ranks, peak_bw, peak_kind)
+    if not args.no_workloads:  # the varlen and long-context workloads, timed the same way
+        for w in ("varlen", "long"):
+            line[w] = workload_line(args, w, dev, ranks)
     if ranks.rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(ki, dev)
     ranks.close()
@@ -507,44 +512,49 @@ def run_reference(args):
 
 
 def run_workload(args):
-    """The other prefill workloads, timed like the headline: varlen (64 sequences with lengths
-    uniform in [128, 16384], seed 0, initial states N(0, 0.02)) or long (B=1, T=1,048,576)."""
-    import gated_delta_rule_56_gb300 as kda
-    import kda_inputs as ki
+    """One of the other workloads on its own (one JSON line)."""
     from gated_delta_rule_56_gb300.build import build
     build()
+    print(json.dumps(workload_line(args, args.workload, torch.device("cuda", 0), Ranks(1))), flush=True)
+
+
+def workload_line(args, workload, dev, ranks):
+    """The other prefill workloads, timed like the headline: varlen (64 sequences with lengths
+    uniform in [128, 16384], seed 0, initial states N(0, 0.02)), long (B=1, T=1,048,576), the
+    headline shape with one of the options, or the backward. Returns the workload's line."""
+    import gated_delta_rule_56_gb300 as kda
+    import kda_inputs as ki
     kda.load()
-    dev = torch.device("cuda", 0)
     H, d = PF["H"], PF["d"]
-    if args.workload == "varlen":
+    if workload == "varlen":
         lengths = ki.varlen_lengths(64, 128, 16384, seed=0)
         x = ki.varlen_inputs(lengths, H, d, d, device=dev, seed=0)
         tokens, n_seq = int(lengths.sum()), int(lengths.numel())
         kw = dict(cu_seqlens=x["cu_seqlens"], initial_state=x["initial_state"])
         alg = tokens * H * (4 * d * 2 + 2 + 2 * d) + 2 * n_seq * H * d * d * 4
         name = f"KDA chunked prefill, varlen: {n_seq} sequences (lengths U[128,16384], seed 0, {tokens} tokens) H={H} dk=dv={d} bf16, fp32 initial states"
-    elif args.workload == "long":
+    elif workload == "long":
         T = 1 << 20
         x = ki.prefill_inputs(1, T, H, d, d, device=dev, seed=0)
         tokens, n_seq = T, 1
         kw = {}
         alg = prefill_bytes(1, T, H, d)
         name = f"KDA chunked prefill, long context: B=1 T={T} H={H} dk=dv={d} bf16, zero init"
-    elif args.workload == "backward":
+    elif workload == "backward":
         B, T = PF["B"], PF["T"]
         x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)
         tokens, n_seq = B * T, B
         kw = dict(d_o=ki.gate_logits_like(x["v"], seed=4))  # dL/do ~ N(0, 1)
         alg = tokens * H * BWD_FLOPS_PER_ELEM * d * d       # algorithmic flops
         name = f"KDA backward (all gradients, fp32 state, tf32 tensor-core products): B={B} T={T} H={H} dk=dv={d} bf16 inputs"
-    elif args.workload == "outgate":
+    elif workload == "outgate":
         B, T = PF["B"], PF["T"]
         x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)
         tokens, n_seq = B * T, B
         kw = dict(out_gate=ki.gate_logits_like(x["v"], seed=3))  # z ~ N(0, 1): o * sigmoid(z) is stored
         alg = prefill_bytes(B, T, H, d) + tokens * H * d * 2    # + the gate input z (bf16)
         name = f"KDA chunked prefill with the output gate o*sigmoid(z) in the kernel: B={B} T={T} H={H} dk=dv={d} bf16, zero init"
-    elif args.workload == "l2norm":
+    elif workload == "l2norm":
         B, T = PF["B"], PF["T"]
         x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)
         x["q"], x["k"] = ki.raw_qk_like(x["q"], seed=1), ki.raw_qk_like(x["k"], seed=2)
@@ -564,30 +574,34 @@ def run_workload(args):
     # A call that the library splits along the sequence (few long sequences; it asks for a
     # workspace) launches 7 kernels: segment bounds, the local pass, the transition pass up to the
     # horizon, the zero test, the transition pass over the rest, the scan and the correction.
-    split = args.workload not in ("varlen", "backward") and kda.load().kda_prefill_workspace_size(0, n_seq, tokens // n_seq, H, d, d, n_seq) > 0
+    split = workload not in ("varlen", "backward") and kda.load().kda_prefill_workspace_size(0, n_seq, tokens // n_seq, H, d, d, None, n_seq) > 0
     launches_per_step = 7 if split else 1
     # Packed sequences with the workspace: the longest-first sort of cu_seqlens, then the prefill.
-    if args.workload == "varlen" and kda.load().kda_prefill_workspace_size(0, 1, tokens, H, d, d, n_seq) > 0:
+    if workload == "varlen" and kda.load().kda_prefill_workspace_size(0, 1, tokens, H, d, d, x["cu_seqlens"].data_ptr(), n_seq) > 0:
         launches_per_step = 2
+    out = {}
+    if workload != "backward":  # outputs allocated once, outside the timed region
+        out = dict(o=torch.empty_like(x["v"]),
+                   final_state=torch.empty(n_seq, H, d, d, dtype=torch.float32, device=dev))
 
     def step(_i):
-        if args.workload == "backward":
+        if workload == "backward":
             kda.backward(*args_in, kw["d_o"])
         else:
-            kda.prefill(*args_in, **kw)
+            kda.prefill(*args_in, **kw, **out)
 
     step(0)
     kda.check_status()
     peak_bw, peak_tc, peak_kind = measured_peaks()
     steps, warmup = max(1, min(args.steps, 20)), max(3, min(args.warmup, 5))
     with ClockSampler(dev) as clk:
-        total_ms, per = time_steps(step, steps, warmup, Ranks(1))
+        total_ms, per = time_steps(step, steps, warmup, ranks)
     kda.check_status()
     kernel_ms = statistics.mean(per)
     achieved = alg / (kernel_ms / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s", "frac": achieved / peak_bw,
             "peak_source": peak_kind, "alg_bytes_per_launch": alg, "kernel_ms": kernel_ms}
-    if args.workload == "backward":  # tf32 tensor-core products; the fp32 FMA rate beside it
+    if workload == "backward":  # tf32 tensor-core products; the fp32 FMA rate beside it
         ach = alg / (kernel_ms / 1e3) / 1e12
         peak_tf32 = peak_tc * TF32_PER_BF16
         roof = {"bound": "tensor", "dtype": "tf32", "achieved": ach, "peak": peak_tf32, "unit": "TFLOP/s",
@@ -598,19 +612,26 @@ def run_workload(args):
                 "fp32_alu": {"peak": FP32_ALU_TFLOPS, "frac": ach / FP32_ALU_TFLOPS,
                              "peak_source": "derived from unit counts and the maximum SM clock"}}
         launches_per_step = 1  # d = 128: the chunked kernel writes every output itself (no fills)
-    print(json.dumps({
-        "metric": f"KDA {'backward' if args.workload == 'backward' else 'prefill'} tokens/s ({args.workload})",
-        "value": tokens / (kernel_ms / 1e3), "unit": "tokens/s",
-        "n_gpus": 1, "steps": steps, "warmup": warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
+    elif workload in ("varlen", "long"):
+        roof["traffic"] = recorded_traffic(workload, existing_files(PREFILL_SOURCES))
+    del x, args_in, kw, out
+    torch.cuda.empty_cache()
+    return {
+        "metric": f"KDA {'backward' if workload == 'backward' else 'prefill'} tokens/s ({workload})",
+        "value": ranks.job_throughput(tokens * steps, total_ms), "unit": "tokens/s",
+        "n_gpus": ranks.world, "steps": steps, "warmup": warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
         "dtype": "bf16", "data": "synthetic", "config": {"workload": name, "pairs": n_seq * H, "split_along_sequence": bool(split)},
         "roofline": roof,
-        "gpu_launches": steps * launches_per_step, "clocks": clk.summary()}), flush=True)
+        "gpu_launches": steps * launches_per_step, "clocks": clk.summary()}
 
 
 def ncu_case(kind):
-    """Small cases sized for an ncu capture: inputs larger than L2, a few hundred MB on the
-    device. prefill: B=4 T=2048 H=32 d=128 (128 CTAs); decode: N=64 H=32 d=128 (2048 CTAs);
-    backward: B=2 T=1024 H=32 d=128 (512 CTAs)."""
+    """Small cases sized for an ncu capture: inputs larger than L2, a few GB on the device at
+    most. prefill: B=4 T=2048 H=32 d=128 (128 CTAs); decode: N=64 H=32 d=128 (2048 CTAs);
+    decode256: the decode workload's own step, N=256 H=32 d=128 (a 537 MB state, past L2);
+    backward: B=2 T=1024 H=32 d=128 (512 CTAs); long: B=1 T=131,072 H=32 d=128, split along the
+    sequence like the long-context workload (its first prefill launch is the local pass); varlen:
+    the first 8 sequences of the varlen workload's lengths, H=32."""
     import gated_delta_rule_56_gb300 as kda
     import kda_inputs as ki
     from gated_delta_rule_56_gb300.build import build
@@ -620,6 +641,20 @@ def ncu_case(kind):
         x = ki.prefill_inputs(4, 2048, 32, 128, 128, device=dev, seed=0)
         for _ in range(2):
             o, _s = kda.prefill(*(x[n] for n in NAMES))
+    elif kind == "long":
+        x = ki.prefill_inputs(1, 1 << 17, 32, 128, 128, device=dev, seed=0)
+        for _ in range(2):
+            o, _s = kda.prefill(*(x[n] for n in NAMES))
+    elif kind == "varlen":
+        lengths = ki.varlen_lengths(64, 128, 16384, seed=0)[:8]
+        x = ki.varlen_inputs(lengths, 32, 128, 128, device=dev, seed=0)
+        for _ in range(2):
+            o, _s = kda.prefill(*(x[n] for n in NAMES), cu_seqlens=x["cu_seqlens"], initial_state=x["initial_state"])
+    elif kind == "decode256":
+        x = ki.decode_inputs(2, 256, 32, 128, 128, device=dev, seed=0)
+        st = x["state"].clone()
+        for t in range(2):
+            o = kda.decode_step(*(x[n][t] for n in NAMES), st)
     elif kind == "backward":
         x = ki.prefill_inputs(2, 1024, 32, 128, 128, device=dev, seed=0)
         do = ki.gate_logits_like(x["v"], seed=4)

@@ -58,8 +58,10 @@ def load():
         lib.kda_prefill.argtypes = [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp,
                                     _vp, _vp, ctypes.c_size_t, _vp]
         lib.kda_prefill.restype = _i
-        lib.kda_prefill_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+        lib.kda_prefill_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _vp, _i]
         lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+        lib.kda_prefill_workspace_size_for.argtypes = [_i, _i, _i, _i, _i, _i, _vp, _i, _i]
+        lib.kda_prefill_workspace_size_for.restype = ctypes.c_size_t
         lib.kda_prefill_split_plan.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp]
         lib.kda_prefill_split_plan.restype = _i
         lib.kda_decode_step.argtypes = [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
@@ -214,7 +216,7 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, initial_state=None, output_final_
         n1 = pool if final_state_indices is not None else N
         _check("final_state", final_state, torch.float32, (n1, H, dk, dv), dev)
     dt = _DTYPES[q.dtype]
-    ws_bytes = int(lib.kda_prefill_workspace_size(dt, B, T, H, dk, dv, N))
+    ws_bytes = int(lib.kda_prefill_workspace_size(dt, B, T, H, dk, dv, _ptr(cu_seqlens), N))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
     with torch.cuda.device(dev):
         if (qk_l2norm or initial_state_indices is not None or final_state_indices is not None

@@ -202,6 +202,29 @@ kda_options gate_only(float gate_bound) {
     return opt;
 }
 
+// Workspace a prefill call can use on a GPU with `sms` SMs: packed sequences (cu_seqlens given)
+// take the longest-first launch order, unpacked ones the split along the sequence.
+size_t prefill_workspace_bytes_for(kda_dtype dtype, int B, int T, int H, int dk, int dv, bool packed, int n_seqs,
+                                   int sms) {
+    if (B < 0 || T < 0 || H < 0 || sms < 0) return 0;
+    if (packed) return order_workspace_bytes(dtype, dk, dv, n_seqs);
+    if (dtype != KDA_BF16 || dk != 128 || dv != 128) return 0;
+    int P = 0, Ls = 0;
+    size_t bytes = 0;
+    segmented_plan_for(B, T, H, sms, &P, &Ls, &bytes);
+    return bytes;
+}
+
+// The same on the current device (0 SMs when none is visible).
+size_t prefill_workspace_bytes(kda_dtype dtype, int B, int T, int H, int dk, int dv, bool packed, int n_seqs) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        sms = 0;
+    }
+    return prefill_workspace_bytes_for(dtype, B, T, H, dk, dv, packed, n_seqs, sms);
+}
+
 // The common body of kda_prefill, kda_prefill_gated and kda_prefill_ex.
 kda_status prefill_impl(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,
                         const void *k, const void *v, const void *g, const void *beta,
@@ -325,7 +348,7 @@ kda_status decode_impl(kda_dtype dtype, int N, int H, int dk, int dv, const void
 
 extern "C" {
 
-int kda_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+int kda_version(void) { return 2 * 10000 + 0 * 100 + 0; }
 
 kda_status kda_selftest_wait_timeout(uint64_t limit_ns, kda_stream_t stream) {
     if (limit_ns < 1 || limit_ns > 1000000000ull)
@@ -347,10 +370,14 @@ const char *kda_status_string(kda_status status) {
 
 const char *kda_last_error(void) { return g_last_error; }
 
-size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv, int n_seqs) {
-    if (B < 0 || T < 0 || H < 0) return 0;
-    if (n_seqs != B) return order_workspace_bytes(dtype, dk, dv, n_seqs);  // packed sequences
-    return segmented_workspace_bytes(dtype, B, T, H, dk, dv, false);
+size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv, const int32_t *cu_seqlens,
+                                  int n_seqs) {
+    return prefill_workspace_bytes(dtype, B, T, H, dk, dv, cu_seqlens != nullptr, n_seqs);
+}
+
+size_t kda_prefill_workspace_size_for(kda_dtype dtype, int B, int T, int H, int dk, int dv, const int32_t *cu_seqlens,
+                                      int n_seqs, int sm_count) {
+    return prefill_workspace_bytes_for(dtype, B, T, H, dk, dv, cu_seqlens != nullptr, n_seqs, sm_count);
 }
 
 kda_status kda_prefill_split_plan(int B, int T, int H, int sm_count, int *segments, int *segment_rows,
@@ -400,9 +427,7 @@ kda_status kda_prefill_noalloc(kda_dtype dtype, int B, int T, int H, int dk, int
                                const void *k, const void *v, const void *g, const void *beta,
                                const int32_t *cu_seqlens, int n_seqs, const float *initial_state, void *o,
                                float *final_state, kda_stream_t stream) {
-    const size_t need = (B < 0 || T < 0 || H < 0) ? 0
-                        : cu_seqlens ? order_workspace_bytes(dtype, dk, dv, n_seqs)
-                                     : segmented_workspace_bytes(dtype, B, T, H, dk, dv, false);
+    const size_t need = prefill_workspace_bytes(dtype, B, T, H, dk, dv, cu_seqlens != nullptr, n_seqs);
     if (need > kStaticScratchBytes)
         return fail(KDA_ERR_UNSUPPORTED, "this call needs %zu bytes of scratch; the static scratch holds %zu",
                     need, kStaticScratchBytes);
@@ -422,8 +447,11 @@ kda_status kda_prefill_noalloc(kda_dtype dtype, int B, int T, int H, int dk, int
     const kda_status st = prefill_impl(dtype, B, T, H, dk, dv, q, k, v, g, beta, cu_seqlens, n_seqs,
                                        initial_state, o, final_state, gate_only(0.f), sc->addr, kStaticScratchBytes,
                                        stream);
-    if (st == KDA_OK && (e = cudaEventRecord(sc->last, s)) != cudaSuccess)
-        return fail(KDA_ERR_CUDA, "ordering on the static scratch: %s", cudaGetErrorString(e));
+    // Recorded whatever the status: a call that failed part-way may have queued kernels that use
+    // the scratch, and the next call must still wait for them. Its own failure is reported first.
+    e = cudaEventRecord(sc->last, s);
+    if (st != KDA_OK) return st;
+    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "ordering on the static scratch: %s", cudaGetErrorString(e));
     return st;
 }
 

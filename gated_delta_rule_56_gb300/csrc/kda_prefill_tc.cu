@@ -255,7 +255,12 @@ __device__ __forceinline__ bool state_wait(uint64_t *bar, uint32_t parity) { ret
 __device__ __forceinline__ void state_sync() { group_sync<2, NS>(); }
 
 // Decay-scaled bf16 operands of one row half (MH = 0: rows 0..31, MH = 1: rows 32..63) for a
-// thread's 4 rows r0..r0+3 x 8 channels 8j..8j+7; gm holds Gam of those entries.
+// thread's 4 rows r0..r0+3 x 8 channels 8j..8j+7; gm holds Gam of those entries. With the L2
+// normalisation (NORM) the operands of the A/P tiles are built from the raw q/k rows, which are
+// exact bf16 values, and the A/P read-out applies the inverse norms to the fp32 products: a
+// normalised row rounded to bf16 before the product would put an absolute error of about
+// 2^-9 / sqrt(d_k) into q.k, a large relative error where q.k is small. Only the operands of the
+// products with the state (K+, Q+, Khat) carry the norm.
 // Per-channel factors (see the exponent-range note at the top):
 //   rows 0..31 : f = exp(Gam_r - Gam_15); off-tile column factor fi*c0 = exp(Gam_31 - Gam_r)
 //   rows 32..63: f = exp(Gam_r - Gam_47); off-tile row factor    f*c1  = exp(Gam_r - Gam_31)
@@ -346,12 +351,8 @@ __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4]
         float apk[8], apq[8], apb[8], ofr_k[8], ofr_q[8], kp[8], qp[8], kh[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float kv = (i & 1) ? bf_hi(kk[i >> 1]) : bf_lo(kk[i >> 1]);
-            float qv = (i & 1) ? bf_hi(qq[i >> 1]) : bf_lo(qq[i >> 1]);
-            if (NORM) {
-                kv *= nk;
-                qv *= nq;
-            }
+            const float kv = (i & 1) ? bf_hi(kk[i >> 1]) : bf_lo(kk[i >> 1]);
+            const float qv = (i & 1) ? bf_hi(qq[i >> 1]) : bf_lo(qq[i >> 1]);
             // |Gam_r - ref| <= 80 for g in [-5, 0]; the clamp only keeps factors finite (no 0 * inf)
             // for gates outside that range.
             const float e = fminf(fmaxf(fmaf(gm[m][i], kLog2e, -ref[i]), -126.f), 126.f);
@@ -370,6 +371,11 @@ __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4]
                 kp[i] = apk[i] * pe[i];       // K exp(Gam_r)
                 qp[i] = apq[i] * pe[i];       // Q exp(Gam_r)
                 kh[i] = ofr_k[i] * khe[i];    // K exp(Gam_63 - Gam_r)
+            }
+            if (NORM) {  // the state operands take the normalised rows
+                kp[i] *= nk;
+                qp[i] *= nq;
+                kh[i] *= nk;
             }
         }
         st_chunk(sm, SM_AP + sw_chunk(r, j, 128), apk);
@@ -391,8 +397,11 @@ __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4]
 // by beta) and the P operand (bf16, lower triangle). The diagonal tile (M = 128) holds row i of A
 // (lanes 0..63) and of P (lanes 64..127); the off-diagonal tile (M = 64) holds its 64 rows in
 // lanes 0..15 of each lane quarter: A rows 32..47, 48..63, then P rows 32..47, 48..63.
+// NORM: the tiles were built from the raw rows; A_is takes nk_i nk_s and P_is takes nq_i nk_s
+// (the inverse L2 norms of k and q rows, from the chunk's row sums of squares `nrm`).
+template <bool NORM>
 __device__ __forceinline__ void ap_readout(uint8_t *sm, float *As, uint32_t tmem_q, int q, int lane,
-                                           const float *sbc) {
+                                           const float *sbc, const float *nrm) {
     float vals[32];
     {
         const int L = 32 * q + lane;
@@ -400,6 +409,11 @@ __device__ __forceinline__ void ap_readout(uint8_t *sm, float *As, uint32_t tmem
         const int j0 = (q & 1) ? 32 : 0;  // the diagonal half of row i
         tmem_ld32(tmem_q + TM_AP + j0, vals);
         tmem_ld_wait();
+        if (NORM) {
+            const float ri = row_inv_norm(nrm, L < 64 ? 0 : 1, i);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) vals[k] *= ri * row_inv_norm(nrm, 0, j0 + k);
+        }
         if (L < 64) {
             const float b = sbc[i];
 #pragma unroll
@@ -426,6 +440,11 @@ __device__ __forceinline__ void ap_readout(uint8_t *sm, float *As, uint32_t tmem
     tmem_ld_wait();
     if (lane < 16) {
         const int i = 32 + 16 * (q & 1) + lane;
+        if (NORM) {
+            const float ri = row_inv_norm(nrm, q < 2 ? 0 : 1, i);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) vals[k] *= ri * row_inv_norm(nrm, 0, k);
+        }
         if (q < 2) {
             const float b = sbc[i];
 #pragma unroll
@@ -915,7 +934,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             state_sync();
             {
                 const float *sbc = sbeta + 64 * par;
-                ap_readout(sm, As, tmem + tq, warp & 3, lane, sbc);
+                ap_readout<NORM>(sm, As, tmem + tq, warp & 3, lane, sbc, nrmb + 128 * (c % 3));
                 state_sync();
                 solve_diag_block(sm, As, Xs, warp & 3, lane, sbc);
                 solve_zero_fill(sm, Xs, v);

@@ -127,13 +127,22 @@ KDA_API kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int
                        const float *initial_state, void *o, float *final_state,
                        void *workspace, size_t workspace_bytes, kda_stream_t stream);
 
-/* Bytes of device workspace kda_prefill can use for these sizes, or 0. n_seqs != B means packed
- * sequences (cu_seqlens): the launch order, 4 bytes per sequence rounded up to 256, for bf16
- * dk == dv == 128 and 2 <= n_seqs <= 4096. Otherwise the split along the sequence, which follows
- * the current device's SM count (0 when no device is visible or the call would not split). The
- * same sizes apply to kda_prefill_gated and kda_prefill_ex. */
+/* Bytes of device workspace kda_prefill can use for a call with these arguments, or 0. Pass the
+ * same dtype, B, T, H, dk, dv, cu_seqlens and n_seqs as the call: cu_seqlens is only compared with
+ * NULL (never read, so the device pointer may be passed). Packed sequences (cu_seqlens != NULL):
+ * the launch order, 4 bytes per sequence rounded up to 256, for bf16 dk == dv == 128 and
+ * 2 <= n_seqs <= 4096 (0 for a single packed sequence). Unpacked (cu_seqlens == NULL, n_seqs
+ * ignored): the split along the sequence, which follows the current device's SM count (0 when no
+ * device is visible or the call would not split). The same sizes apply to kda_prefill_gated and
+ * kda_prefill_ex. */
 KDA_API size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv,
-                                  int n_seqs);
+                                          const int32_t *cu_seqlens, int n_seqs);
+
+/* kda_prefill_workspace_size for a GPU with sm_count SMs instead of the current device: host
+ * arithmetic only (nothing is queued, no device is needed), the same sizes the call computes with
+ * the device's own SM count. 0 for negative sizes or a negative sm_count. */
+KDA_API size_t kda_prefill_workspace_size_for(kda_dtype dtype, int B, int T, int H, int dk, int dv,
+                                              const int32_t *cu_seqlens, int n_seqs, int sm_count);
 
 /*
  * kda_prefill_split_plan -- how kda_prefill splits B sequences of T tokens and H heads along the
@@ -285,7 +294,8 @@ KDA_API const char *kda_status_string(kda_status status);
 /* Detail of the most recent failure in the calling host thread ("" if none). */
 KDA_API const char *kda_last_error(void);
 
-/* Library ABI version: major * 10000 + minor * 100 + patch. */
+/* Library ABI version: major * 10000 + minor * 100 + patch. Version 2 made packed calls to
+ * kda_prefill_workspace_size explicit (the cu_seqlens argument). */
 KDA_API int kda_version(void);
 
 #ifdef __cplusplus

@@ -39,22 +39,43 @@ def test_status_strings_and_version(lib):
     assert kda.version() >= 10000
 
 
+# cu_seqlens is only compared with NULL by the sizing calls: any non-NULL value marks a packed call.
+PACKED = ctypes.c_void_p(16)
+
+
 def test_workspace_size_is_zero_when_not_split(lib):
     # Many (sequence, head) pairs, fp32 or small heads: one pass, no workspace.
-    assert lib.kda_prefill_workspace_size(0, 4, 8192, 32, 128, 128, 4) == 0
-    assert lib.kda_prefill_workspace_size(1, 1, 1 << 20, 32, 128, 128, 1) == 0    # fp32
-    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 64, 64, 1) == 0      # d = 64
+    for f in (lambda *a: lib.kda_prefill_workspace_size(*a), lambda *a: lib.kda_prefill_workspace_size_for(*a, 152)):
+        assert f(0, 4, 8192, 32, 128, 128, None, 4) == 0
+        assert f(1, 1, 1 << 20, 32, 128, 128, None, 1) == 0    # fp32
+        assert f(0, 1, 1 << 20, 32, 64, 64, None, 1) == 0      # d = 64
 
 
 def test_workspace_size_of_packed_sequences(lib):
     # Packed bf16 d=128 sequences: 4 bytes per sequence for the longest-first launch order,
     # rounded up to 256; none for one sequence, more than 4096, fp32 or other head sizes.
-    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 128, 128, 64) == 256
-    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 128, 128, 100) == 512
-    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 128, 128, 4096) == 4096 * 4
-    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 128, 128, 4097) == 0
-    assert lib.kda_prefill_workspace_size(1, 1, 1 << 20, 32, 128, 128, 64) == 0
-    assert lib.kda_prefill_workspace_size(0, 1, 1 << 20, 32, 64, 64, 64) == 0
+    for f in (lambda *a: lib.kda_prefill_workspace_size(*a), lambda *a: lib.kda_prefill_workspace_size_for(*a, 152)):
+        assert f(0, 1, 1 << 20, 32, 128, 128, PACKED, 64) == 256
+        assert f(0, 1, 1 << 20, 32, 128, 128, PACKED, 100) == 512
+        assert f(0, 1, 1 << 20, 32, 128, 128, PACKED, 4096) == 4096 * 4
+        assert f(0, 1, 1 << 20, 32, 128, 128, PACKED, 4097) == 0
+        assert f(1, 1, 1 << 20, 32, 128, 128, PACKED, 64) == 0
+        assert f(0, 1, 1 << 20, 32, 64, 64, PACKED, 64) == 0
+
+
+def test_workspace_size_tells_one_packed_sequence_from_one_unpacked(lib):
+    """B = n_seqs = 1: with cu_seqlens the call is packed (one sequence needs no launch order and
+    is not split); without it the same sizes are split along the sequence on a 152-SM GPU, and the
+    size is the split plan's."""
+    T, H = 1 << 20, 32
+    P, Ls, split = kda.prefill_split_plan(1, T, H, 152)
+    assert P >= 2 and split > 0
+    assert lib.kda_prefill_workspace_size_for(0, 1, T, H, 128, 128, None, 1, 152) == split
+    assert lib.kda_prefill_workspace_size_for(0, 1, T, H, 128, 128, PACKED, 1, 152) == 0
+    # On the CPU no device is visible: unpacked calls are sized for 0 SMs (no split).
+    assert lib.kda_prefill_workspace_size(0, 1, T, H, 128, 128, None, 1) == 0
+    assert lib.kda_prefill_workspace_size(0, 1, T, H, 128, 128, PACKED, 1) == 0
+    assert lib.kda_prefill_workspace_size_for(0, 1, T, H, 128, 128, None, 1, -1) == 0
 
 
 def test_noalloc_capacity_and_argument_checks(lib):

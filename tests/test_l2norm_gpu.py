@@ -26,30 +26,42 @@ def _raw(x, seed):
     return x
 
 
-def _unit(t, rounded=False):
-    """The oracle's fp64 normalisation of the raw rows; with `rounded`, rounded to the input
-    dtype, the precision at which the kernels feed their products with the rows (bf16 operands).
-    A single token's output is the cancelling sum (q.k) u, whose relative error that operand
-    rounding dominates; there the reference carries the same rounding."""
-    y = oracle.l2_normalize(t.cpu())
-    return torch.from_numpy(y).to(t.dtype) if rounded else y
+def _unit(t):
+    """The oracle's fp64 normalisation of the raw rows (never rounded: the reference of every
+    case is the plain fp64 oracle fed these rows)."""
+    return oracle.l2_normalize(t.cpu())
 
 
-def _ref(x, g=None, rounded=False):
+def _ref(x, g=None):
     cu = x.get("cu_seqlens")
     init = x.get("initial_state")
-    return oracle.recurrent(_unit(x["q"], rounded), _unit(x["k"], rounded), x["v"].cpu(),
+    return oracle.recurrent(_unit(x["q"]), _unit(x["k"]), x["v"].cpu(),
                             x["g"].cpu() if g is None else g, x["beta"].cpu(),
                             cu_seqlens=None if cu is None else cu.cpu(),
                             initial_state=None if init is None else init.cpu())
 
 
-@pytest.mark.parametrize("B,T,H", [(2, 200, 3), (1, 64, 2), (1, 1, 1)])
+@pytest.mark.parametrize("B,T,H", [(2, 200, 3), (1, 64, 2), (1, 1, 1), (2, 1, 3)])
 def test_l2norm_prefill_tensor_core_path(B, T, H):
+    """Ragged, one-chunk and single-token calls. A single token's output is (q.k) beta v plus the
+    read-out of the decayed initial state, so it hinges on the cancelling sum q.k: the kernel
+    forms it from the raw rows and applies the norms to the fp32 product."""
     x = _raw(ki.prefill_inputs(B, T, H, 128, 128, device=DEV, seed=71, state_std=0.02), seed=72)
     o, s = kda.prefill(*(x[n] for n in NAMES), initial_state=x["initial_state"], qk_l2norm=True)
     kda.check_status()
-    ro, rs = _ref(x, rounded=T == 1)  # one token: its output is a cancelling sum, see _unit
+    ro, rs = _ref(x)
+    assert_close(o, ro, "o")
+    assert_close(s, rs, "final_state")
+
+
+@pytest.mark.parametrize("seed", [90, 91, 92, 93])
+def test_l2norm_single_token_one_head_many_seeds(seed):
+    """One token of one head: the relative error of o is that of one scalar, q.k, whatever its
+    size. Held to the bar against the unrounded normalisation over several draws."""
+    x = _raw(ki.prefill_inputs(1, 1, 1, 128, 128, device=DEV, seed=seed, state_std=0.02), seed=seed + 100)
+    o, s = kda.prefill(*(x[n] for n in NAMES), initial_state=x["initial_state"], qk_l2norm=True)
+    kda.check_status()
+    ro, rs = _ref(x)
     assert_close(o, ro, "o")
     assert_close(s, rs, "final_state")
 
@@ -76,7 +88,7 @@ def test_l2norm_with_gate_logits():
 
 def test_l2norm_segmented_long_sequence():
     x = _raw(ki.prefill_inputs(1, 8192, 2, 128, 128, device=DEV, seed=78, state_std=0.02), seed=79)
-    assert kda.load().kda_prefill_workspace_size(0, 1, 8192, 2, 128, 128, 1) > 0
+    assert kda.load().kda_prefill_workspace_size(0, 1, 8192, 2, 128, 128, None, 1) > 0
     o, s = kda.prefill(*(x[n] for n in NAMES), initial_state=x["initial_state"], qk_l2norm=True)
     kda.check_status()
     ro, rs = _ref(x)

@@ -58,7 +58,7 @@ def test_out_gate_prefill_varlen_ragged_chunks():
 
 def test_out_gate_segmented_long_sequence():
     x = ki.prefill_inputs(1, 8192, 2, 128, 128, device=DEV, seed=95, state_std=0.02)
-    assert kda.load().kda_prefill_workspace_size(0, 1, 8192, 2, 128, 128, 1) > 0
+    assert kda.load().kda_prefill_workspace_size(0, 1, 8192, 2, 128, 128, None, 1) > 0
     z = _z(x["v"], seed=96)
     o, s = kda.prefill(*(x[n] for n in NAMES), initial_state=x["initial_state"], out_gate=z)
     kda.check_status()

@@ -20,7 +20,7 @@ def _built():
 
 
 def _ws(B, T, H):
-    return int(kda.load().kda_prefill_workspace_size(0, B, T, H, 128, 128, B))
+    return int(kda.load().kda_prefill_workspace_size(0, B, T, H, 128, 128, None, B))
 
 
 def _ref(x, init, g=None):

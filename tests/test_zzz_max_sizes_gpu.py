@@ -28,7 +28,7 @@ def test_longest_first_order_at_4096_sequences():
     lengths = ki.varlen_lengths(n, 0, 8, seed=61)
     x = ki.varlen_inputs(lengths, H, 128, 128, device=DEV, seed=62)
     lib = kda.load()
-    assert lib.kda_prefill_workspace_size(0, 1, int(lengths.sum()), H, 128, 128, n) == n * 4  # ordered
+    assert lib.kda_prefill_workspace_size(0, 1, int(lengths.sum()), H, 128, 128, x["cu_seqlens"].data_ptr(), n) == n * 4  # ordered
     o1, s1 = kda.prefill(*(x[nm] for nm in NAMES), cu_seqlens=x["cu_seqlens"], initial_state=x["initial_state"])
     kda.check_status()
     o2, s2 = torch.empty_like(o1), torch.empty_like(s1)
