@@ -223,6 +223,7 @@ def recorded_traffic(key, files):
 
 
 PREFILL_SOURCES = ["gated_delta_rule_56_gb300/csrc/kda_prefill_tc.cu", "gated_delta_rule_56_gb300/csrc/kda_tc.cuh"]
+SPLIT_SOURCES = PREFILL_SOURCES + ["gated_delta_rule_56_gb300/csrc/kda_segmented.cu"]
 DECODE_SOURCES = ["gated_delta_rule_56_gb300/csrc/kda_recurrent.cu"]
 BACKWARD_SOURCES = ["gated_delta_rule_56_gb300/csrc/kda_backward_chunked.cu"]
 
@@ -613,7 +614,7 @@ def workload_line(args, workload, dev, ranks):
                              "peak_source": "derived from unit counts and the maximum SM clock"}}
         launches_per_step = 1  # d = 128: the chunked kernel writes every output itself (no fills)
     elif workload in ("varlen", "long"):
-        roof["traffic"] = recorded_traffic(workload, existing_files(PREFILL_SOURCES))
+        roof["traffic"] = recorded_traffic(workload, existing_files(SPLIT_SOURCES if workload == "long" else PREFILL_SOURCES))
     del x, args_in, kw, out
     torch.cuda.empty_cache()
     return {
@@ -629,7 +630,7 @@ def ncu_case(kind):
     """Small cases sized for an ncu capture: inputs larger than L2, a few GB on the device at
     most. prefill: B=4 T=2048 H=32 d=128 (128 CTAs); decode: N=64 H=32 d=128 (2048 CTAs);
     decode256: the decode workload's own step, N=256 H=32 d=128 (a 537 MB state, past L2);
-    backward: B=2 T=1024 H=32 d=128 (512 CTAs); long: B=1 T=131,072 H=32 d=128, split along the
+    backward: B=2 T=1024 H=32 d=128 (512 CTAs); long: B=1 T=65,536 H=32 d=128, split along the
     sequence like the long-context workload (its first prefill launch is the local pass); varlen:
     the first 8 sequences of the varlen workload's lengths, H=32."""
     import gated_delta_rule_56_gb300 as kda
@@ -642,7 +643,7 @@ def ncu_case(kind):
         for _ in range(2):
             o, _s = kda.prefill(*(x[n] for n in NAMES))
     elif kind == "long":
-        x = ki.prefill_inputs(1, 1 << 17, 32, 128, 128, device=dev, seed=0)
+        x = ki.prefill_inputs(1, 1 << 16, 32, 128, 128, device=dev, seed=0)
         for _ in range(2):
             o, _s = kda.prefill(*(x[n] for n in NAMES))
     elif kind == "varlen":
