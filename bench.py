@@ -615,15 +615,37 @@ def workload_line(args, workload, dev, ranks):
         launches_per_step = 1  # d = 128: the chunked kernel writes every output itself (no fills)
     elif workload in ("varlen", "long"):
         roof["traffic"] = recorded_traffic(workload, existing_files(SPLIT_SOURCES if workload == "long" else PREFILL_SOURCES))
+    packed = None
+    if workload == "long":  # the same tokens as one packed sequence (cu_seqlens = [0, T]): split on the device
+        cu = torch.tensor([0, tokens], dtype=torch.int32, device=dev)
+        pk_split = kda.load().kda_prefill_workspace_size(0, 1, tokens, H, d, d, cu.data_ptr(), 1) > 0
+
+        def step_packed(_i):
+            kda.prefill(*args_in, cu_seqlens=cu, **out)
+
+        step_packed(0)
+        kda.check_status()
+        pk_total, pk_per = time_steps(step_packed, steps, warmup, ranks)
+        kda.check_status()
+        pk_ms = statistics.mean(pk_per)
+        packed = {"value": ranks.job_throughput(tokens * steps, pk_total), "unit": "tokens/s",
+                  "ms_per_step": pk_total / steps, "kernel_ms": pk_ms,
+                  "frac": alg / (pk_ms / 1e3) / 1e9 / peak_bw, "split_along_sequence": bool(pk_split),
+                  "gpu_launches": steps * (8 if pk_split else 1),
+                  "how": "cu_seqlens = [0, T]: the segments are planned on the device (planner, local pass, "
+                         "transition pass to the horizon, zero test, rerun, scan, correction)"}
     del x, args_in, kw, out
     torch.cuda.empty_cache()
-    return {
+    line = {
         "metric": f"KDA {'backward' if workload == 'backward' else 'prefill'} tokens/s ({workload})",
         "value": ranks.job_throughput(tokens * steps, total_ms), "unit": "tokens/s",
         "n_gpus": ranks.world, "steps": steps, "warmup": warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
         "dtype": "bf16", "data": "synthetic", "config": {"workload": name, "pairs": n_seq * H, "split_along_sequence": bool(split)},
         "roofline": roof,
         "gpu_launches": steps * launches_per_step, "clocks": clk.summary()}
+    if packed:
+        line["packed"] = packed
+    return line
 
 
 def ncu_case(kind):

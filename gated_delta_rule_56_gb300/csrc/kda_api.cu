@@ -138,7 +138,9 @@ __global__ void __launch_bounds__(kSortThreads) order_by_length_kernel(const int
 }  // namespace
 
 size_t order_workspace_bytes(kda_dtype dtype, int dk, int dv, int n_seqs) {
-    if (dtype != KDA_BF16 || dk != 128 || dv != 128 || n_seqs < 2 || n_seqs > kMaxOrderedSeqs) return 0;
+    if (dtype != KDA_BF16 || dk != dv || (dk != 32 && dk != 64 && dk != 128) || n_seqs < 2 ||
+        n_seqs > kMaxOrderedSeqs)
+        return 0;
     return ((size_t)n_seqs * sizeof(int32_t) + 255) / 256 * 256;
 }
 
@@ -203,11 +205,16 @@ kda_options gate_only(float gate_bound) {
 }
 
 // Workspace a prefill call can use on a GPU with `sms` SMs: packed sequences (cu_seqlens given)
-// take the longest-first launch order, unpacked ones the split along the sequence.
+// are split along the sequence when fewer of them than SMs / H are long enough, else they take the
+// longest-first launch order; unpacked ones the split along the sequence.
 size_t prefill_workspace_bytes_for(kda_dtype dtype, int B, int T, int H, int dk, int dv, bool packed, int n_seqs,
                                    int sms) {
     if (B < 0 || T < 0 || H < 0 || sms < 0) return 0;
-    if (packed) return order_workspace_bytes(dtype, dk, dv, n_seqs);
+    if (packed) {
+        if (B != 1) return 0;
+        const size_t split = segmented_packed_workspace_bytes_for(dtype, n_seqs, T, H, dk, dv, sms);
+        return split ? split : order_workspace_bytes(dtype, dk, dv, n_seqs);
+    }
     if (dtype != KDA_BF16 || dk != 128 || dv != 128) return 0;
     int P = 0, Ls = 0;
     size_t bytes = 0;
@@ -215,14 +222,19 @@ size_t prefill_workspace_bytes_for(kda_dtype dtype, int B, int T, int H, int dk,
     return bytes;
 }
 
-// The same on the current device (0 SMs when none is visible).
-size_t prefill_workspace_bytes(kda_dtype dtype, int B, int T, int H, int dk, int dv, bool packed, int n_seqs) {
+// SMs of the current device (0 when none is visible).
+int current_sms() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         (void)cudaGetLastError();
         sms = 0;
     }
-    return prefill_workspace_bytes_for(dtype, B, T, H, dk, dv, packed, n_seqs, sms);
+    return sms;
+}
+
+// The same on the current device.
+size_t prefill_workspace_bytes(kda_dtype dtype, int B, int T, int H, int dk, int dv, bool packed, int n_seqs) {
+    return prefill_workspace_bytes_for(dtype, B, T, H, dk, dv, packed, n_seqs, current_sms());
 }
 
 // The common body of kda_prefill, kda_prefill_gated and kda_prefill_ex.
@@ -269,6 +281,7 @@ kda_status prefill_impl(kda_dtype dtype, int B, int T, int H, int dk, int dv, co
     p.o = o;
     p.T = T;
     p.H = H;
+    p.dk = dk;
     p.n_seqs = n_seqs;
     p.err = device_error_word();
     p.gate_bound = opt.gate_bound;
@@ -285,6 +298,11 @@ kda_status prefill_impl(kda_dtype dtype, int B, int T, int H, int dk, int dv, co
                             cudaGetErrorString(cudaGetLastError()));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (tc_prefill_supported(dtype, dk, dv, p)) {
+        // Few packed sequences: split the long ones along the sequence when the caller gave the workspace.
+        const size_t pk_bytes =
+            cu_seqlens ? segmented_packed_workspace_bytes_for(dtype, n_seqs, T, H, dk, dv, current_sms()) : 0;
+        if (pk_bytes && workspace && workspace_bytes >= pk_bytes && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0)
+            return launched(launch_segmented_packed_prefill(p, workspace, workspace_bytes, s), "segmented packed prefill");
         // Packed sequences: start the longest first when the caller gave the workspace for the order.
         const size_t ord_bytes = cu_seqlens ? order_workspace_bytes(dtype, dk, dv, n_seqs) : 0;
         if (ord_bytes && workspace && workspace_bytes >= ord_bytes &&
@@ -329,6 +347,7 @@ kda_status decode_impl(kda_dtype dtype, int N, int H, int dk, int dv, const void
     p.o = o;
     p.T = 1;
     p.H = H;
+    p.dk = dk;
     p.n_seqs = N;
     p.err = device_error_word();
     p.gate_bound = opt.gate_bound;
@@ -507,6 +526,7 @@ kda_status kda_backward(kda_dtype dtype, int B, int T, int H, int dk, int dv, co
     p.init = initial_state;
     p.T = T;
     p.H = H;
+    p.dk = dk;
     p.n_seqs = n_seqs;
     p.err = device_error_word();
     if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word");

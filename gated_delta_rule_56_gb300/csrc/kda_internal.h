@@ -22,6 +22,7 @@ struct RunParams {
     void *o;
     int T;                      // rows per sequence (cu_seqlens == nullptr) or packed rows
     int H;
+    int dk;                     // head size of the tensors (dk == dv); the tensor-core kernel pads it to 128
     int n_seqs;
     unsigned *err;              // device error word
     float gate_bound;           // 0: g holds log-decays; > 0: g holds logits x, g = -gate_bound * sigmoid(x)
@@ -50,9 +51,10 @@ cudaError_t launch_recurrent(kda_dtype dtype, int dk, int dv, const RunParams &p
 bool tc_prefill_supported(kda_dtype dtype, int dk, int dv, const RunParams &p);
 cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s);
 
-// TMA map of a bf16 [rows, H, 128] tensor in boxes of 64 rows x 64 channels (128-byte swizzle),
-// the tile of the tensor-core kernels. False if the driver's encoder is unavailable or rejects it.
-bool encode_row_tile_map(CUtensorMap *map, const void *base, long long rows, int H);
+// TMA map of a bf16 [rows, H, d] tensor in boxes of 64 rows x 64 channels (128-byte swizzle), the
+// tile of the tensor-core kernels (channels past d read as zeros and are not written). False if the
+// driver's encoder is unavailable or rejects it.
+bool encode_row_tile_map(CUtensorMap *map, const void *base, long long rows, int H, int d = 128);
 
 // Segmented prefill of few long sequences (see kda_segmented.cu): workspace bytes it needs for
 // this call (0: the call is not eligible), and the launch sequence.
@@ -62,6 +64,11 @@ size_t segmented_workspace_bytes(kda_dtype dtype, int B, int T, int H, int dk, i
 void segmented_plan_for(int B, int T, int H, int sms, int *P, int *Ls, size_t *bytes);
 cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace, size_t workspace_bytes,
                                      cudaStream_t s);
+// The same for packed sequences (cu_seqlens): the segments are planned on the device from the lengths.
+// Workspace bytes on a GPU with `sms` SMs (0: such a call is not split), and the launch sequence.
+size_t segmented_packed_workspace_bytes_for(kda_dtype dtype, int n_seqs, int T, int H, int dk, int dv, int sms);
+cudaError_t launch_segmented_packed_prefill(const RunParams &p, void *workspace, size_t workspace_bytes,
+                                            cudaStream_t s);
 
 // Longest-first launch order of packed sequences (see kda_api.cu): workspace bytes and the sort.
 constexpr int kMaxOrderedSeqs = 4096;

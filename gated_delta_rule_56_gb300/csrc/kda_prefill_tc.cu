@@ -278,11 +278,11 @@ struct QKRows {
 };
 
 __device__ __forceinline__ void load_qk_rows(QKRows &x, const __nv_bfloat16 *qg, const __nv_bfloat16 *kg,
-                                             long long row0, int ln, int H, int h, int r0, int j) {
+                                             long long row0, int ln, int H, int h, int r0, int j, int dg) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        const bool live = r0 + m < ln;
-        const size_t e = ((size_t)(row0 + r0 + m) * H + h) * D + 8 * j;
+        const bool live = r0 + m < ln && 8 * j < dg;
+        const size_t e = ((size_t)(row0 + r0 + m) * H + h) * dg + 8 * j;
         x.k[m] = live ? __ldg(reinterpret_cast<const uint4 *>(kg + e)) : make_uint4(0u, 0u, 0u, 0u);
         x.q[m] = live ? __ldg(reinterpret_cast<const uint4 *>(qg + e)) : make_uint4(0u, 0u, 0u, 0u);
     }
@@ -568,13 +568,14 @@ enum : int { kGated = 1, kNorm = 2, kOutGate = 4 };
 // thread copies 8 of the 1024 16-byte chunks (row e / 16, channels 8 (e % 16) ..). Rows at or past
 // `ln` (past the tensor end, never stored) get zeros.
 __device__ __forceinline__ void stage_gate_rows(uint8_t *sm, const __nv_bfloat16 *zg, long long r0, int ln, int H,
-                                                int h, int v) {
+                                                int h, int v, int dg) {
     uint4 z[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int e = v + 128 * i, row = e >> 4, cj = e & 15;
-        z[i] = row < ln ? __ldg(reinterpret_cast<const uint4 *>(zg + ((size_t)(r0 + row) * H + h) * D + 8 * cj))
-                        : make_uint4(0u, 0u, 0u, 0u);
+        z[i] = (row < ln && 8 * cj < dg)
+                   ? __ldg(reinterpret_cast<const uint4 *>(zg + ((size_t)(r0 + row) * H + h) * dg + 8 * cj))
+                   : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -602,6 +603,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = p.H;
+    const int dg = p.dk;  // head size in global memory (<= D; channels past it are zero here)
     const int h = blockIdx.x % H;
     const int n = p.order ? p.order[blockIdx.x / H] : (int)(blockIdx.x / H);
 
@@ -791,7 +793,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int v = tid - NP;
         __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o);
         bool ok = true;
-        const long long init_off = p.init ? state_slot_offset(p.init_idx, p.pool, n, H, h, D, p.err) : -1;
+        const long long init_off = p.init ? state_slot_offset(p.init_idx, p.pool, n, H, h, dg, p.err) : -1;
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {  // initial state -> TMEM (fp32)
             const int k0 = 32 * cb;
@@ -799,7 +801,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
                 buf[i] = p.identity_init ? (k0 + i == v ? 1.f : 0.f)
-                                         : (init_off >= 0 ? __ldcs(p.init + init_off + (size_t)(k0 + i) * D + v) : 0.f);
+                                         : ((init_off >= 0 && v < dg && k0 + i < dg)
+                                                ? __ldcs(p.init + init_off + (size_t)(k0 + i) * dg + v)
+                                                : 0.f);
             tmem_st32(tmem + tq + TM_S + k0, buf);
         }
         tmem_st_wait();
@@ -808,10 +812,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // global memory: each warp store covers 32 consecutive value columns (64 bytes).
         const __nv_bfloat16 *zg = static_cast<const __nv_bfloat16 *>(p.out_gate);
         auto store_o = [&](const float (&o0)[32], const float (&o1)[32], long long r0, int ln) {
-            __nv_bfloat16 *dst = og + ((size_t)r0 * H + h) * D + v;
+            if (v >= dg) return;  // a padded value column: nothing to store
+            __nv_bfloat16 *dst = og + ((size_t)r0 * H + h) * dg + v;
             const size_t rs = (size_t)H * D;  // elements between consecutive tokens
             if (OGATE) {  // a ragged chunk: gate each stored element
-                const __nv_bfloat16 *zr = zg + ((size_t)r0 * H + h) * D + v;
+                const __nv_bfloat16 *zr = zg + ((size_t)r0 * H + h) * dg + v;
 #pragma unroll
                 for (int r = 0; r < 32; ++r, dst += rs, zr += rs)
                     if (r < ln) *dst = __float2bfloat16_rn(o0[r] * __fdividef(1.f, 1.f + ex2(-__bfloat162float(*zr) * kLog2e)));
@@ -847,7 +852,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (OGATE) {
                     // z into the tile first; each thread then scales its fp32 O by sigmoid(z) read
                     // from the element it overwrites, so O is rounded to bf16 once.
-                    stage_gate_rows(sm, zg, r0, (int)min((long long)C, total_rows - r0), H, h, v);
+                    stage_gate_rows(sm, zg, r0, (int)min((long long)C, total_rows - r0), H, h, v, dg);
                     state_sync();
                 }
                 // 8 rows at a time: the 8 gate values are read before any of the 8 stores.
@@ -890,8 +895,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t par = (uint32_t)(c & 1);
             const long long row0 = bos + (long long)c * C;
             const int len = (int)min((long long)C, eos - row0);
-            if (OGATE && (v >> 1) < len)  // this chunk's gate rows into L2 (read when its O is written)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(zg + ((size_t)(row0 + (v >> 1)) * H + h) * D + 64 * (v & 1)));
+            if (OGATE && (v >> 1) < len && 64 * (v & 1) < dg)  // this chunk's gate rows into L2 (read when its O is written)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(zg + ((size_t)(row0 + (v >> 1)) * H + h) * dg + 64 * (v & 1)));
             if (c > 0) {  // O of the previous chunk, once MMA3 and MMA4 of it have completed
                 if (!(ok = state_wait(&bars[BAR_M34], par ^ 1u))) break;
                 tc_fence_after();
@@ -987,15 +992,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (v == 0) bulk_wait_all();  // every O store is complete (and has read shared memory)
         if (ok) {
-            const long long fin_off = p.fin ? state_slot_offset(p.fin_idx, p.pool, n, H, h, D, p.err) : -1;
-            if (fin_off >= 0) {
+            const long long fin_off = p.fin ? state_slot_offset(p.fin_idx, p.pool, n, H, h, dg, p.err) : -1;
+            if (fin_off >= 0 && v < dg) {
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     float sv[32];
                     tmem_ld32(tmem + tq + TM_S + 32 * cb, sv);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) __stcs(p.fin + fin_off + (size_t)(32 * cb + i) * D + v, sv[i]);
+                    for (int i = 0; i < 32; ++i)
+                        if (32 * cb + i < dg) __stcs(p.fin + fin_off + (size_t)(32 * cb + i) * dg + v, sv[i]);
                 }
             }
         } else if (v == 0) {
@@ -1035,7 +1041,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             QKRows qk;
             if (NORM) {  // in flight while the cumsum runs
                 load_qk_rows(qk, static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
-                             r0, ln, H, h, tr0, j);
+                             r0, ln, H, h, tr0, j, p.dk);
                 if (tid < 128) nrmb[128 * ((cc + 1) % 3) + tid] = 0.f;
             }
             const float bet = __uint_as_float(beta_next << 16);
@@ -1201,11 +1207,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-bool encode_map(CUtensorMap *map, const void *base, long long rows, int H) {
+bool encode_map(CUtensorMap *map, const void *base, long long rows, int H, int d) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
     cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
@@ -1215,15 +1221,20 @@ bool encode_map(CUtensorMap *map, const void *base, long long rows, int H) {
 
 }  // namespace
 
-bool encode_row_tile_map(CUtensorMap *map, const void *base, long long rows, int H) {
-    return encode_map(map, base, rows, H);
+bool encode_row_tile_map(CUtensorMap *map, const void *base, long long rows, int H, int d) {
+    return encode_map(map, base, rows, H, d);
 }
 
+// bf16 with d_k == d_v in {32, 64, 128}: smaller heads run the d = 128 kernel with the missing
+// channels zero (the tensor maps read them as zeros, the stores skip them), when the driver encodes
+// their tensor maps.
 bool tc_prefill_supported(kda_dtype dtype, int dk, int dv, const RunParams &p) {
-    if (dtype != KDA_BF16 || dk != D || dv != D) return false;
+    if (dtype != KDA_BF16 || dk != dv || (dk != 32 && dk != 64 && dk != D)) return false;
     const long long rows = p.cu_seqlens ? (long long)p.T : (long long)p.n_seqs * p.T;
     if (rows <= 0 || rows > 0x7fffffffLL - C) return false;
-    return tensor_map_encoder() != nullptr;
+    if (!tensor_map_encoder()) return false;
+    CUtensorMap probe;
+    return encode_map(&probe, p.q, rows, p.H, dk);
 }
 
 // One instance per combination of the flags, indexed by them.
@@ -1251,9 +1262,9 @@ cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
     }
     const long long rows = p.cu_seqlens ? (long long)p.T : (long long)p.n_seqs * p.T;
     Maps maps;
-    if (!encode_map(&maps.q, p.q, rows, p.H) || !encode_map(&maps.k, p.k, rows, p.H) ||
-        !encode_map(&maps.g, p.g, rows, p.H) || !encode_map(&maps.v, p.v, rows, p.H) ||
-        !encode_map(&maps.o, p.o, rows, p.H))
+    if (!encode_map(&maps.q, p.q, rows, p.H, p.dk) || !encode_map(&maps.k, p.k, rows, p.H, p.dk) ||
+        !encode_map(&maps.g, p.g, rows, p.H, p.dk) || !encode_map(&maps.v, p.v, rows, p.H, p.dk) ||
+        !encode_map(&maps.o, p.o, rows, p.H, p.dk))
         return cudaErrorInvalidValue;
     const int f = (p.gate_bound > 0.f ? kGated : 0) | (p.qk_l2norm ? kNorm : 0) | (p.out_gate ? kOutGate : 0);
     void *args[] = {(void *)&maps, (void *)&p};

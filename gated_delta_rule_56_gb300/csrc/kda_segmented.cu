@@ -105,8 +105,13 @@ __global__ void seg_bounds_kernel(int32_t *cu, int B, int T, int P, int Ls) {
 }
 
 // done[i] = 1 when the transition of (segment, head) i after the horizon is exactly zero (nothing
-// further to compute), else 0. One CTA of 256 threads per pair.
-__global__ void __launch_bounds__(256) seg_done_kernel(const float *__restrict__ mtr, uint8_t *__restrict__ done) {
+// further to compute) or the pair was not run (skip[i]), else 0. One CTA of 256 threads per pair.
+__global__ void __launch_bounds__(256) seg_done_kernel(const float *__restrict__ mtr, const uint8_t *__restrict__ skip,
+                                                       uint8_t *__restrict__ done) {
+    if (skip && skip[blockIdx.x]) {
+        if (threadIdx.x == 0) done[blockIdx.x] = 1;
+        return;
+    }
     const float4 *m = reinterpret_cast<const float4 *>(mtr + (size_t)blockIdx.x * D * D);
     bool zero = true;
     for (int e = threadIdx.x; e < D * D / 4; e += 256) {
@@ -117,25 +122,41 @@ __global__ void __launch_bounds__(256) seg_done_kernel(const float *__restrict__
     if (threadIdx.x == 0) done[blockIdx.x] = zero ? 1 : 0;
 }
 
-// One CTA per (sequence b, head h): S_start(0) = init (or 0), S_start(p+1) = M_p S_start(p) + S^loc(p);
+// One CTA per (sequence b, head h). Equal segments (seg_first == NULL: segments b*P .. b*P+P-1, all
+// run from a zero state): S_start(0) = init (or 0), S_start(p+1) = M_p S_start(p) + S^loc(p).
+// Planned segments of packed sequences (seg_first != NULL: segments seg_first[b] .. seg_first[b+1]-1,
+// the first one run from the sequence's initial state, so that its S^loc is already the state at
+// its end): S_start(first + 1) = S^loc(first), and the same recursion after it.
 // S_start(p) is stored transposed in bf16 (the B operand of the correction GEMM), and the state
 // after the last segment is the final state. Thread (ti, tj) owns the 8 x 8 block at (8 ti, 8 tj).
 __global__ void __launch_bounds__(256) seg_scan_kernel(const float *__restrict__ mtr, const float *__restrict__ sloc,
                                                        const float *__restrict__ init, float *__restrict__ fin,
                                                        const int32_t *init_idx, const int32_t *fin_idx, int pool,
-                                                       unsigned *err, __nv_bfloat16 *__restrict__ sst, int P, int H) {
+                                                       unsigned *err, __nv_bfloat16 *__restrict__ sst, int P, int H,
+                                                       const int32_t *__restrict__ seg_first) {
     extern __shared__ float S[];  // [128][132]
     constexpr int LD = 132;
     const int bh = blockIdx.x, b = bh / H, h = bh % H, tid = threadIdx.x;
     const int ti = tid >> 4, tj = tid & 15;
-    const long long init_off = init ? state_slot_offset(init_idx, pool, b, H, h, D, err) : -1;
     const long long fin_off = fin ? state_slot_offset(fin_idx, pool, b, H, h, D, err) : -1;
-    for (int e = tid; e < D * D; e += 256)
-        S[(e >> 7) * LD + (e & 127)] = init_off >= 0 ? init[init_off + e] : 0.f;
+    int s_begin, s_end;
+    if (seg_first) {
+        const int s0 = seg_first[b];
+        s_begin = s0 + 1;
+        s_end = max(seg_first[b + 1], s_begin);
+        const float *L0 = sloc + ((size_t)s0 * H + h) * D * D;
+        for (int e = tid; e < D * D; e += 256) S[(e >> 7) * LD + (e & 127)] = L0[e];
+    } else {
+        s_begin = b * P;
+        s_end = s_begin + P;
+        const long long init_off = init ? state_slot_offset(init_idx, pool, b, H, h, D, err) : -1;
+        for (int e = tid; e < D * D; e += 256)
+            S[(e >> 7) * LD + (e & 127)] = init_off >= 0 ? init[init_off + e] : 0.f;
+    }
     __syncthreads();
 #pragma unroll 1
-    for (int p = 0; p < P; ++p) {
-        const size_t s = (size_t)(b * P + p) * H + h;
+    for (int sg = s_begin; sg < s_end; ++sg) {
+        const size_t s = (size_t)sg * H + h;
         for (int e = tid; e < D * D; e += 256) {  // S_start^T: row v, column k
             const int v = e >> 7, k = e & 127;
             sst[s * D * D + e] = __float2bfloat16_rn(S[k * LD + v]);
@@ -206,11 +227,15 @@ __device__ __forceinline__ float absmax_bf16x8(const uint4 w, float m) {
     return m;
 }
 
-// o[t] += S_start^T qt[t] over kTilesPerCta tiles of 128 tokens of segment p (blockIdx.y = b * P + p)
-// and head blockIdx.z: per tile D = qt_tile (128 x 128) x S_start (128 x 128) on the tensor core
-// (A: the qt tile by TMA, B: S_start^T, loaded once), then o read, added and written back row by
-// row (thread = token). A tile whose correction is bounded by 128 max|S_start| max|qt| < 1e-30 is
-// left as it is (qt decays with the segment transition; such a term cannot change a bf16 output).
+// o[t] += S_start^T qt[t] over the tiles of 128 tokens of segment blockIdx.y and head blockIdx.z, CTA
+// x taking tiles x, x + gridDim.x, ...: per tile D = qt_tile (128 x 128) x S_start (128 x 128) on the
+// tensor core (A: the qt tile by TMA, B: S_start^T, loaded once), then o read, added and written back
+// row by row (thread = token). A tile whose correction is bounded by 128 max|S_start| max|qt| < 1e-30
+// is left as it is (qt decays with the segment transition; such a term cannot change a bf16 output).
+// Segment geometry: equal segments (seg_cu == NULL): segment b * P + p covers rows p*Ls .. of batch
+// row b (T rows each), and segments p < p0 are skipped (zero S_start); planned segments of packed
+// sequences (seg_cu != NULL): rows seg_cu[s] .. seg_cu[s+1]-1, and the first segment of a sequence
+// (is_first[s]) needs no correction.
 constexpr int kTilesPerCta = 8;
 constexpr float kNegligible = 1e-30f;
 
@@ -219,7 +244,8 @@ __global__ void __launch_bounds__(128) seg_correct_kernel(const __grid_constant_
                                                           const uint8_t *__restrict__ done,
                                                           __nv_bfloat16 *__restrict__ o,
                                                           const __nv_bfloat16 *__restrict__ zg, int T, int H, int Ls,
-                                                          int P, int p0, unsigned *err) {
+                                                          int P, int p0, const int32_t *__restrict__ seg_cu,
+                                                          const uint8_t *__restrict__ is_first, unsigned *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = sm, *sB = sm + 32768;
@@ -227,13 +253,21 @@ __global__ void __launch_bounds__(128) seg_correct_kernel(const __grid_constant_
     uint32_t *tptr = reinterpret_cast<uint32_t *>(sm + 65536 + 16);
     float *red = reinterpret_cast<float *>(sm + 65536 + 32);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int seg = blockIdx.y, b = seg / P, p = seg % P, h = blockIdx.z;
-    if (p < p0) return;  // S_start is zero: nothing to add
-    const long long lo = (long long)p * Ls;
+    const int seg = blockIdx.y, h = blockIdx.z;
+    long long base, len;  // packed row of the segment start, and its rows
+    if (seg_cu) {
+        if (is_first[seg]) return;
+        base = seg_cu[seg];
+        len = (long long)seg_cu[seg + 1] - base;
+    } else {
+        const int b = seg / P, p = seg % P;
+        if (p < p0) return;  // S_start is zero: nothing to add
+        base = (long long)b * T + (long long)p * Ls;
+        len = min((long long)Ls, (long long)T - (long long)p * Ls);
+    }
     // qt is exactly zero past the horizon where the transition run stopped early (and not stored).
-    const long long hi = min(lo + (done[(size_t)seg * H + h] ? (long long)kHorizon : (long long)Ls), (long long)T);
-    const long long first = lo + (long long)blockIdx.x * kTilesPerCta * CT;
-    if (first >= hi) return;
+    const long long hi = min(len, done[(size_t)seg * H + h] ? (long long)kHorizon : len);
+    if ((long long)blockIdx.x * CT >= hi) return;
 
     if (warp == 0) {
         tmem_alloc(tptr, 128);
@@ -264,11 +298,9 @@ __global__ void __launch_bounds__(128) seg_correct_kernel(const __grid_constant_
     uint32_t ncopy = 0, nmma = 0;  // copies and MMA groups issued (their barrier phases)
     const uint64_t da = sdesc_sw128(smem_u32(sA), 16u, 1024u), db = sdesc_sw128(smem_u32(sB), 16u, 1024u);
 #pragma unroll 1
-    for (int t = 0; t < kTilesPerCta && ok; ++t) {
-        const long long r0 = first + (long long)t * CT;
-        if (r0 >= hi) break;
+    for (long long r0 = (long long)blockIdx.x * CT; r0 < hi && ok; r0 += (long long)gridDim.x * CT) {
         const int nrows = (int)min((long long)CT, hi - r0);
-        const long long row = (long long)b * T + r0;  // packed row of the tile start
+        const long long row = base + r0;  // packed row of the tile start
         if (tid == 0) {
             mbar_arrive_expect_tx(&bars[0], 32768);
             for (int rb = 0; rb < 2; ++rb)
@@ -345,8 +377,127 @@ __global__ void __launch_bounds__(128) seg_correct_kernel(const __grid_constant_
     if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
+// Plan of the split of packed sequences, made on the device from cu_seqlens (one CTA). With
+// `slots` = SMs / H CTAs per head to fill, the target segment length is the packed rows / slots
+// (rounded up to whole chunks, at least kMinSegRows), and sequence n gets P_n = min(kMaxSegments,
+// ceil(L_n / target)) segments of equal length (whole chunks; the last one shorter). Outputs, for
+// S_max planned segments (those past the S used are empty, at row T, and skipped): seg_cu[S_max + 1]
+// (bounds as packed rows), seg_first[n + 1] (first segment of each sequence, then S), seg_init[S_max]
+// (the state slot a segment starts from: the sequence's initial state for its first segment, none for
+// the others), is_first[S_max] and skip[S_max * H] (pairs the transition run leaves out: first and
+// empty segments). A cu_seqlens that does not start at 0, decreases or does not end at T is reported
+// (kErrBadSeqlens) and planned as clamped bounds, one segment per sequence.
+__global__ void __launch_bounds__(256) seg_plan_packed_kernel(const int32_t *__restrict__ cu, int n, int T, int H,
+                                                              int slots, int S_max, const int32_t *__restrict__ init_idx,
+                                                              int32_t *__restrict__ seg_cu, int32_t *__restrict__ seg_first,
+                                                              int32_t *__restrict__ seg_init, uint8_t *__restrict__ is_first,
+                                                              uint8_t *__restrict__ skip, unsigned *err) {
+    __shared__ int used;
+    if (threadIdx.x == 0) {
+        bool bad = cu[0] != 0 || cu[n] != T;
+        for (int i = 0; i < n && !bad; ++i) bad = cu[i + 1] < cu[i];
+        if (bad) atomicOr(err, kErrBadSeqlens);
+        const long long per = ((long long)T + slots - 1) / slots;
+        const long long target = max((long long)kMinSegRows, (per + 63) / 64 * 64);
+        int sg = 0;
+        long long prev = 0;
+        for (int i = 0; i < n; ++i) {
+            long long b0 = bad ? min(max(prev, (long long)cu[i]), (long long)T) : cu[i];
+            long long b1 = bad ? min(max(b0, (long long)cu[i + 1]), (long long)T) : cu[i + 1];
+            prev = b1;
+            const long long L = b1 - b0;
+            long long P = bad ? 1 : min((long long)kMaxSegments, max(1LL, (L + target - 1) / target));
+            const long long Ls = max(64LL, ((L + P - 1) / P + 63) / 64 * 64);
+            P = max(1LL, (L + Ls - 1) / Ls);
+            seg_first[i] = sg;
+            for (int q = 0; q < P && sg < S_max; ++q, ++sg) {
+                seg_cu[sg] = (int32_t)min(b0 + q * Ls, b1);
+                seg_init[sg] = q == 0 ? (init_idx ? init_idx[i] : i) : -1;
+                is_first[sg] = q == 0 ? 1 : 0;
+            }
+        }
+        seg_first[n] = sg;
+        used = sg;
+        for (int q = sg; q <= S_max; ++q) {
+            seg_cu[q] = T;
+            if (q < S_max) {
+                seg_init[q] = -1;
+                is_first[q] = 1;
+            }
+        }
+    }
+    __syncthreads();
+    const int S = used;
+    for (int e = threadIdx.x; e < S_max * H; e += blockDim.x) {
+        const int q = e / H;
+        skip[e] = (q >= S || is_first[q] || seg_cu[q + 1] == seg_cu[q]) ? 1 : 0;
+    }
+}
+
+// Workspace layout of the packed split; bytes == 0 when such a call is not split.
+struct PackedPlan {
+    int slots = 0, S_max = 0;
+    size_t off_cu = 0, off_first = 0, off_init = 0, off_isfirst = 0, off_skip = 0, off_qt = 0, off_sloc = 0,
+           off_mtr = 0, off_sst = 0, off_done = 0, bytes = 0;
+};
+
+PackedPlan make_packed_plan_for(int n, int T, int H, int sms) {
+    PackedPlan pl;
+    if (sms <= 0 || n <= 0 || H <= 0 || T < 2 * kMinSegRows) return pl;
+    const int slots = sms / H;
+    if (slots < 2 || n >= slots) return pl;  // as many sequences as CTAs per head: nothing to gain
+    pl.slots = slots;
+    pl.S_max = (int)std::min<long long>((long long)kMaxSegments * n, (long long)n + slots);
+    const long long S = pl.S_max;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align256(off + bytes);
+        return at;
+    };
+    pl.off_cu = take((size_t)(S + 1) * 4);
+    pl.off_first = take((size_t)(n + 1) * 4);
+    pl.off_init = take((size_t)S * 4);
+    pl.off_isfirst = take((size_t)S);
+    pl.off_skip = take((size_t)S * H);
+    pl.off_qt = take((size_t)T * H * D * 2);
+    pl.off_sloc = take((size_t)S * H * D * D * 4);
+    pl.off_mtr = take((size_t)S * H * D * D * 4);
+    pl.off_sst = take((size_t)S * H * D * D * 2);
+    pl.off_done = take((size_t)S * H);
+    pl.bytes = off;
+    return pl;
+}
+
+PackedPlan make_packed_plan(int n, int T, int H) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PackedPlan{};
+    return make_packed_plan_for(n, T, H, sms);
+}
+
 constexpr int kScanSmem = 128 * 132 * 4;
 constexpr int kCorrectSmem = 65536 + 64 + 1024;  // A, B, barriers, TMEM address, block max
+
+// Shared-memory limits of the scan and correction kernels, once per device.
+cudaError_t set_segmented_attributes() {
+    static std::mutex mu;
+    static bool attr_set[256] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(seg_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCorrectSmem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    return cudaSuccess;
+}
 
 }  // namespace
 
@@ -363,27 +514,88 @@ size_t segmented_workspace_bytes(kda_dtype dtype, int B, int T, int H, int dk, i
     return make_plan(B, T, H).bytes;
 }
 
+size_t segmented_packed_workspace_bytes_for(kda_dtype dtype, int n_seqs, int T, int H, int dk, int dv, int sms) {
+    if (dtype != KDA_BF16 || dk != D || dv != D || T >= 0x7fffffff - 64) return 0;
+    return make_packed_plan_for(n_seqs, T, H, sms).bytes;
+}
+
+cudaError_t launch_segmented_packed_prefill(const RunParams &p, void *workspace, size_t workspace_bytes,
+                                            cudaStream_t s) {
+    const int T = p.T, H = p.H, n = p.n_seqs;
+    const PackedPlan pl = make_packed_plan(n, T, H);
+    if (!pl.bytes || workspace_bytes < pl.bytes || !workspace) return cudaErrorInvalidValue;
+    cudaError_t e = set_segmented_attributes();
+    if (e != cudaSuccess) return e;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *seg_cu = reinterpret_cast<int32_t *>(ws + pl.off_cu);
+    int32_t *seg_first = reinterpret_cast<int32_t *>(ws + pl.off_first);
+    int32_t *seg_init = reinterpret_cast<int32_t *>(ws + pl.off_init);
+    uint8_t *is_first = ws + pl.off_isfirst;
+    uint8_t *skip = ws + pl.off_skip;
+    __nv_bfloat16 *qt = reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_qt);
+    float *sloc = reinterpret_cast<float *>(ws + pl.off_sloc);
+    float *mtr = reinterpret_cast<float *>(ws + pl.off_mtr);
+    __nv_bfloat16 *sst = reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_sst);
+    uint8_t *done = ws + pl.off_done;
+    const int S = pl.S_max;
+
+    seg_plan_packed_kernel<<<1, 256, 0, s>>>(p.cu_seqlens, n, T, H, pl.slots, S, p.init_idx, seg_cu, seg_first,
+                                             seg_init, is_first, skip, p.err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // Pass 1: every segment; the first one of a sequence from its initial state (its end state is
+    // then that of the sequence), the others from zero (o^loc into o, S^loc into the workspace).
+    RunParams pa = p;
+    pa.cu_seqlens = seg_cu;
+    pa.n_seqs = S;
+    pa.init_idx = p.init ? seg_init : nullptr;
+    pa.pool = p.init_idx ? p.pool : n;
+    pa.fin = sloc;
+    pa.fin_idx = nullptr;
+    pa.order = nullptr;
+    pa.zero_v = false;
+    pa.identity_init = false;
+    pa.max_chunks = 0;
+    pa.skip = nullptr;
+    if ((e = launch_tc_prefill(pa, s)) != cudaSuccess) return e;
+    // Pass 2: v = 0 from the identity for the later segments (qt = M^T q into the workspace, M at the
+    // segment ends), up to the horizon, then over the rest where M is not yet zero.
+    RunParams pb = pa;
+    pb.init = nullptr;
+    pb.init_idx = nullptr;
+    pb.zero_v = true;
+    pb.identity_init = true;
+    pb.o = qt;
+    pb.fin = mtr;
+    pb.max_chunks = kHorizon / 64;
+    pb.skip = skip;
+    pb.out_gate = nullptr;  // its "o" is qt
+    if ((e = launch_tc_prefill(pb, s)) != cudaSuccess) return e;
+    seg_done_kernel<<<(unsigned)(S * H), 256, 0, s>>>(mtr, skip, done);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    pb.max_chunks = 0;
+    pb.skip = done;
+    if ((e = launch_tc_prefill(pb, s)) != cudaSuccess) return e;
+    // Start states of the later segments and the final states.
+    seg_scan_kernel<<<(unsigned)(n * H), 256, kScanSmem, s>>>(mtr, sloc, nullptr, p.fin, nullptr, p.fin_idx, p.pool,
+                                                              p.err, sst, 0, H, seg_first);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // o += S_start^T qt on the later segments.
+    CUtensorMap qt_map;
+    if (!encode_row_tile_map(&qt_map, qt, (long long)T, H)) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)kTilesPerCta, (unsigned)S, (unsigned)H);
+    seg_correct_kernel<<<grid, 128, kCorrectSmem, s>>>(qt_map, sst, done, static_cast<__nv_bfloat16 *>(p.o),
+                                                       static_cast<const __nv_bfloat16 *>(p.out_gate), T, H, 0, 1, 0,
+                                                       seg_cu, is_first, p.err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace, size_t workspace_bytes,
                                      cudaStream_t s) {
     const int T = p.T, H = p.H;
     const Plan pl = make_plan(B, T, H);
     if (pl.P < 2 || workspace_bytes < pl.bytes || !workspace) return cudaErrorInvalidValue;
-    static std::mutex mu;
-    static bool attr_set[256] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = set_segmented_attributes();
     if (e != cudaSuccess) return e;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
-        if (!attr_set[dev]) {
-            e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(seg_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCorrectSmem);
-            if (e != cudaSuccess) return e;
-            attr_set[dev] = true;
-        }
-    }
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *cu = reinterpret_cast<int32_t *>(ws + pl.off_cu);
     __nv_bfloat16 *qt = reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_qt);
@@ -420,14 +632,14 @@ cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace,
     pb.out_gate = nullptr;  // its "o" is qt
     pb.qk_l2norm = p.qk_l2norm;
     if ((e = launch_tc_prefill(pb, s)) != cudaSuccess) return e;
-    seg_done_kernel<<<(unsigned)(segs * H), 256, 0, s>>>(mtr, done);
+    seg_done_kernel<<<(unsigned)(segs * H), 256, 0, s>>>(mtr, nullptr, done);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     pb.max_chunks = 0;
     pb.skip = done;
     if ((e = launch_tc_prefill(pb, s)) != cudaSuccess) return e;
     // Start states of the segments and the final state.
     seg_scan_kernel<<<(unsigned)(B * H), 256, kScanSmem, s>>>(mtr, sloc, p.init, p.fin, p.init_idx, p.fin_idx,
-                                                              p.pool, p.err, sst, pl.P, H);
+                                                              p.pool, p.err, sst, pl.P, H, nullptr);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // o += S_start^T qt, skipped for segment 0 when the initial state is zero.
     CUtensorMap qt_map;
@@ -435,7 +647,7 @@ cudaError_t launch_segmented_prefill(const RunParams &p, int B, void *workspace,
     const dim3 grid((unsigned)((pl.Ls + CT * kTilesPerCta - 1) / (CT * kTilesPerCta)), (unsigned)segs, (unsigned)H);
     seg_correct_kernel<<<grid, 128, kCorrectSmem, s>>>(qt_map, sst, done, static_cast<__nv_bfloat16 *>(p.o),
                                                        static_cast<const __nv_bfloat16 *>(p.out_gate), T, H,
-                                                       pl.Ls, pl.P, p.init ? 0 : 1, p.err);
+                                                       pl.Ls, pl.P, p.init ? 0 : 1, nullptr, nullptr, p.err);
     return cudaGetLastError();
 }
 

@@ -107,14 +107,15 @@ typedef struct kda_options {
  * o            output [B, T, H, dv], same dtype as the inputs. Every row is written.
  * final_state  fp32 [N, H, dk, dv] or NULL (not written). May alias initial_state.
  * workspace, workspace_bytes  device scratch, 256-byte aligned, of at least
- *              kda_prefill_workspace_size() bytes; or NULL / 0. Packed bf16 d=128 sequences (2 to
+ *              kda_prefill_workspace_size() bytes; or NULL / 0. Packed bf16 sequences (2 to
  *              4096 of them) use 4 bytes per sequence for a longest-first launch order (a sort of
  *              cu_seqlens by length on the device), which shortens the tail of the launch; the
  *              results are the same without it. A split call uses it for more: when
- *              few long sequences cannot fill the GPU (bf16, dk == dv == 128, no cu_seqlens), each
+ *              few long sequences cannot fill the GPU (bf16, dk == dv == 128; packed or not), each
  *              is cut into segments run side by side and joined through the segment transitions
  *              (the state after a segment is linear in the state before it: "Inside Kimi K3's
- *              Architecture", "Kimi Delta Attention: the linear core"). Without a large enough
+ *              Architecture", "Kimi Delta Attention: the linear core"); for packed sequences the
+ *              segments are planned on the device from cu_seqlens. Without a large enough
  *              workspace the same call runs one pass per sequence, with the same result up to
  *              rounding. The caller owns the workspace; it must not be used by other work on
  *              other streams until this call's work is done.
@@ -129,12 +130,16 @@ KDA_API kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int
 
 /* Bytes of device workspace kda_prefill can use for a call with these arguments, or 0. Pass the
  * same dtype, B, T, H, dk, dv, cu_seqlens and n_seqs as the call: cu_seqlens is only compared with
- * NULL (never read, so the device pointer may be passed). Packed sequences (cu_seqlens != NULL):
- * the launch order, 4 bytes per sequence rounded up to 256, for bf16 dk == dv == 128 and
- * 2 <= n_seqs <= 4096 (0 for a single packed sequence). Unpacked (cu_seqlens == NULL, n_seqs
- * ignored): the split along the sequence, which follows the current device's SM count (0 when no
- * device is visible or the call would not split). The same sizes apply to kda_prefill_gated and
- * kda_prefill_ex. */
+ * NULL (never read, so the device pointer may be passed). bf16 only; the split needs dk == dv ==
+ * 128, the launch order dk == dv in {32, 64, 128}; the sizes follow the current device's SM count (0
+ * SMs when no device is visible).
+ * Packed sequences (cu_seqlens != NULL, B == 1): when there are fewer sequences than SMs / H and at
+ * least 4096 rows, the split along the sequence planned on the device (the packed rows of q~ in bf16,
+ * T * H * 256 bytes, plus three 128 x 128 states per segment and head for at most
+ * min(8 n_seqs, n_seqs + SMs / H) segments); otherwise the launch order, 4 bytes per sequence
+ * rounded up to 256, for 2 <= n_seqs <= 4096 (0 for a single sequence). Unpacked (cu_seqlens ==
+ * NULL, n_seqs ignored): the split along the sequence (0 when the call would not split). The same
+ * sizes apply to kda_prefill_gated and kda_prefill_ex. */
 KDA_API size_t kda_prefill_workspace_size(kda_dtype dtype, int B, int T, int H, int dk, int dv,
                                           const int32_t *cu_seqlens, int n_seqs);
 

@@ -52,30 +52,49 @@ def test_workspace_size_is_zero_when_not_split(lib):
 
 
 def test_workspace_size_of_packed_sequences(lib):
-    # Packed bf16 d=128 sequences: 4 bytes per sequence for the longest-first launch order,
-    # rounded up to 256; none for one sequence, more than 4096, fp32 or other head sizes.
+    # Packed bf16 sequences (d = 32, 64, 128: all on the tensor-core kernel): 4 bytes per sequence
+    # for the longest-first launch order, rounded up to 256; none for one sequence, more than 4096,
+    # fp32 or other head sizes.
     for f in (lambda *a: lib.kda_prefill_workspace_size(*a), lambda *a: lib.kda_prefill_workspace_size_for(*a, 152)):
         assert f(0, 1, 1 << 20, 32, 128, 128, PACKED, 64) == 256
         assert f(0, 1, 1 << 20, 32, 128, 128, PACKED, 100) == 512
         assert f(0, 1, 1 << 20, 32, 128, 128, PACKED, 4096) == 4096 * 4
         assert f(0, 1, 1 << 20, 32, 128, 128, PACKED, 4097) == 0
         assert f(1, 1, 1 << 20, 32, 128, 128, PACKED, 64) == 0
-        assert f(0, 1, 1 << 20, 32, 64, 64, PACKED, 64) == 0
+        assert f(0, 1, 1 << 20, 32, 64, 64, PACKED, 64) == 256
+        assert f(0, 1, 1 << 20, 32, 32, 32, PACKED, 64) == 256
+        assert f(0, 1, 1 << 20, 32, 96, 96, PACKED, 64) == 0
 
 
 def test_workspace_size_tells_one_packed_sequence_from_one_unpacked(lib):
-    """B = n_seqs = 1: with cu_seqlens the call is packed (one sequence needs no launch order and
-    is not split); without it the same sizes are split along the sequence on a 152-SM GPU, and the
-    size is the split plan's."""
+    """B = n_seqs = 1: the same sizes mean an unpacked call (split into equal segments on a 152-SM
+    GPU: the split plan's size) or a packed one (the packed split, planned on the device: it needs
+    the packed rows of q~ and the segment states of at most min(8 n, n + SMs / H) segments)."""
     T, H = 1 << 20, 32
     P, Ls, split = kda.prefill_split_plan(1, T, H, 152)
     assert P >= 2 and split > 0
     assert lib.kda_prefill_workspace_size_for(0, 1, T, H, 128, 128, None, 1, 152) == split
-    assert lib.kda_prefill_workspace_size_for(0, 1, T, H, 128, 128, PACKED, 1, 152) == 0
-    # On the CPU no device is visible: unpacked calls are sized for 0 SMs (no split).
+    packed = lib.kda_prefill_workspace_size_for(0, 1, T, H, 128, 128, PACKED, 1, 152)
+    s_max = min(8 * 1, 1 + 152 // H)  # 5 segments at most
+    assert packed >= T * H * 128 * 2 + s_max * H * 128 * 128 * (4 + 4 + 2)
+    assert packed < T * H * 128 * 2 + (s_max + 1) * H * 128 * 128 * (4 + 4 + 2)
+    # On the CPU no device is visible: calls are sized for 0 SMs (no split, no order for one sequence).
     assert lib.kda_prefill_workspace_size(0, 1, T, H, 128, 128, None, 1) == 0
     assert lib.kda_prefill_workspace_size(0, 1, T, H, 128, 128, PACKED, 1) == 0
     assert lib.kda_prefill_workspace_size_for(0, 1, T, H, 128, 128, None, 1, -1) == 0
+
+
+def test_workspace_size_of_the_packed_split(lib):
+    """Packed sequences are split only when there are fewer of them than SMs / H (room for more CTAs
+    per head) and at least 4096 rows; otherwise they take the launch order only."""
+    f = lambda *a: lib.kda_prefill_workspace_size_for(*a)
+    assert f(0, 1, 1 << 20, 32, 128, 128, PACKED, 64, 152) == 256          # 64 sequences: order only
+    assert f(0, 1, 1 << 20, 32, 128, 128, PACKED, 4, 152) == 256          # 152 / 32 = 4 slots: order only
+    assert f(0, 1, 1 << 20, 32, 128, 128, PACKED, 3, 152) > (1 << 20) * 32 * 256  # 3 < 4 slots: split
+    assert f(0, 1, 4095, 32, 128, 128, PACKED, 3, 152) == 256               # too short to split: order
+    assert f(0, 1, 1 << 20, 32, 128, 128, PACKED, 3, 64) == 256             # 2 slots on 64 SMs: 3 >= 2
+    assert f(1, 1, 1 << 20, 32, 128, 128, PACKED, 3, 152) == 0              # fp32: neither
+    assert f(0, 2, 1 << 20, 32, 128, 128, PACKED, 3, 152) == 0              # packed calls have B == 1
 
 
 def test_noalloc_capacity_and_argument_checks(lib):

@@ -241,3 +241,42 @@ def test_varlen_longest_first_order_changes_nothing():
     assert st == 0
     kda.check_status()
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("d", [64, 32])
+@pytest.mark.parametrize("lengths", [[200], [70, 1, 130, 0, 64, 2000]])
+def test_small_heads_bf16_tensor_core_path(d, lengths):
+    """bf16 heads of 64 or 32 channels run the tensor-core kernel with the missing channels zero:
+    ragged chunks, packed sequences (one empty), initial states, every output and final state."""
+    x = ki.varlen_inputs(lengths, 3, d, d, device=DEV, seed=14 + d)
+    o, s = run(x)
+    ro, rs = ref(x)
+    assert_close(o, ro, "o")
+    assert_close(s, rs, "final_state")
+
+
+@pytest.mark.parametrize("d", [64, 32])
+def test_small_heads_bf16_with_options(d):
+    """Gate logits, q/k L2 normalisation, the output gate and a state pool on 64/32-channel heads."""
+    H = 2
+    x = ki.varlen_inputs([150, 70], H, d, d, device=DEV, seed=16 + d)
+    xg = ki.gate_logits_like(x["g"], seed=18)
+    q, k = ki.raw_qk_like(x["q"], seed=19), ki.raw_qk_like(x["k"], seed=20)
+    z = ki.gate_logits_like(x["v"], seed=21)
+    pool = torch.randn(4, H, d, d, device=DEV) * 0.02
+    out = pool.clone()
+    idx_in = torch.tensor([2, -1], dtype=torch.int32, device=DEV)
+    idx_out = torch.tensor([0, 3], dtype=torch.int32, device=DEV)
+    o, _ = kda.prefill(q, k, x["v"], xg, x["beta"], cu_seqlens=x["cu_seqlens"], initial_state=pool, final_state=out,
+                       gate_bound=5.0, qk_l2norm=True, out_gate=z, initial_state_indices=idx_in,
+                       final_state_indices=idx_out)
+    kda.check_status()
+    init = torch.stack([pool[2], torch.zeros_like(pool[0])])
+    ro, rs = oracle.recurrent(oracle.l2_normalize(q.cpu()), oracle.l2_normalize(k.cpu()), x["v"].cpu(),
+                              oracle.scaled_sigmoid_gate(xg.cpu(), 5.0), x["beta"].cpu(),
+                              cu_seqlens=x["cu_seqlens"].cpu(), initial_state=init.cpu())
+    assert_close(o, oracle.output_gate(ro, z.cpu()), "o")
+    assert_close(out[0], rs[0], "pool[0]")
+    assert_close(out[3], rs[1], "pool[3]")
+    torch.testing.assert_close(out[1], pool[1], rtol=0, atol=0)
+    torch.testing.assert_close(out[2], pool[2], rtol=0, atol=0)
