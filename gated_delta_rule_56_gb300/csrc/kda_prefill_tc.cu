@@ -814,7 +814,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         auto store_o = [&](const float (&o0)[32], const float (&o1)[32], long long r0, int ln) {
             if (v >= dg) return;  // a padded value column: nothing to store
             __nv_bfloat16 *dst = og + ((size_t)r0 * H + h) * dg + v;
-            const size_t rs = (size_t)H * D;  // elements between consecutive tokens
+            const size_t rs = (size_t)H * dg;  // elements between consecutive tokens
             if (OGATE) {  // a ragged chunk: gate each stored element
                 const __nv_bfloat16 *zr = zg + ((size_t)r0 * H + h) * dg + v;
 #pragma unroll

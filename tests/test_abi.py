@@ -68,16 +68,19 @@ def test_workspace_size_of_packed_sequences(lib):
 
 def test_workspace_size_tells_one_packed_sequence_from_one_unpacked(lib):
     """B = n_seqs = 1: the same sizes mean an unpacked call (split into equal segments on a 152-SM
-    GPU: the split plan's size) or a packed one (the packed split, planned on the device: it needs
-    the packed rows of q~ and the segment states of at most min(8 n, n + SMs / H) segments)."""
+    GPU: the split plan's size) or a packed one (the packed split planned on the device: the packed
+    rows of q~ and the segment states; one packed sequence is planned exactly, into the same P
+    segments as the unpacked call; several into at most min(8 n, n + SMs / H))."""
     T, H = 1 << 20, 32
     P, Ls, split = kda.prefill_split_plan(1, T, H, 152)
-    assert P >= 2 and split > 0
+    assert P == 4 and split > 0
     assert lib.kda_prefill_workspace_size_for(0, 1, T, H, 128, 128, None, 1, 152) == split
     packed = lib.kda_prefill_workspace_size_for(0, 1, T, H, 128, 128, PACKED, 1, 152)
-    s_max = min(8 * 1, 1 + 152 // H)  # 5 segments at most
-    assert packed >= T * H * 128 * 2 + s_max * H * 128 * 128 * (4 + 4 + 2)
-    assert packed < T * H * 128 * 2 + (s_max + 1) * H * 128 * 128 * (4 + 4 + 2)
+    per_seg = H * 128 * 128 * (4 + 4 + 2)
+    assert T * H * 128 * 2 + P * per_seg <= packed < T * H * 128 * 2 + (P + 1) * per_seg
+    two = lib.kda_prefill_workspace_size_for(0, 1, T, H, 128, 128, PACKED, 2, 152)
+    s_max = min(8 * 2, 2 + 152 // H)  # 6
+    assert T * H * 128 * 2 + s_max * per_seg <= two < T * H * 128 * 2 + (s_max + 1) * per_seg
     # On the CPU no device is visible: calls are sized for 0 SMs (no split, no order for one sequence).
     assert lib.kda_prefill_workspace_size(0, 1, T, H, 128, 128, None, 1) == 0
     assert lib.kda_prefill_workspace_size(0, 1, T, H, 128, 128, PACKED, 1) == 0
