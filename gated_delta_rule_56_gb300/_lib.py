@@ -95,6 +95,8 @@ def load():
         lib.kda_prefill_noalloc.restype = _i
         lib.kda_prefill_noalloc_capacity.argtypes = []
         lib.kda_prefill_noalloc_capacity.restype = ctypes.c_size_t
+        lib.kda_prefill_debug_dump.argtypes = [_i, _i, _i] + [_vp] * 8 + [_vp, _i, _vp]
+        lib.kda_prefill_debug_dump.restype = _i
         lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _vp]
         lib.kda_selftest_wait_timeout.restype = _i
         _lib = lib

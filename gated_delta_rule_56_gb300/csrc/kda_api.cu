@@ -440,6 +440,39 @@ kda_status kda_prefill_gated(kda_dtype dtype, int B, int T, int H, int dk, int d
                         o, final_state, gate_only(gate_bound), workspace, workspace_bytes, stream);
 }
 
+kda_status kda_prefill_debug_dump(int B, int T, int H, const void *q, const void *k, const void *v, const void *g,
+                                  const void *beta, const float *initial_state, void *o, float *final_state,
+                                  float *dump, int dump_chunks, kda_stream_t stream) {
+    if (B < 1 || T < 1 || H < 1 || dump_chunks < 0)
+        return fail(KDA_ERR_INVALID_ARG, "B=%d T=%d H=%d dump_chunks=%d", B, T, H, dump_chunks);
+    if ((long long)B * T > 0x7fffffffLL - 64 || (long long)B * H > 0x7fffffffLL)
+        return fail(KDA_ERR_INVALID_ARG, "too large");
+    kda_status st;
+    if ((st = check_ptr(q, "q", true)) || (st = check_ptr(k, "k", true)) || (st = check_ptr(v, "v", true)) ||
+        (st = check_ptr(g, "g", true)) || (st = check_ptr(o, "o", true)) || (st = check_ptr(beta, "beta", false)) ||
+        (st = check_ptr(dump, "dump", true)))
+        return st;
+    if ((reinterpret_cast<uintptr_t>(beta) & 1u) || (initial_state && !aligned16(initial_state)) ||
+        (final_state && !aligned16(final_state)))
+        return fail(KDA_ERR_INVALID_ARG, "misaligned beta or state");
+    RunParams p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    p.init = initial_state;
+    p.fin = final_state;
+    p.o = o;
+    p.T = T;
+    p.H = H;
+    p.dk = 128;
+    p.n_seqs = B;
+    p.err = device_error_word();
+    p.dump = dump;
+    p.dump_chunks = dump_chunks;
+    if (!p.err) return fail(KDA_ERR_CUDA, "cannot reach the device error word");
+    if (!tc_prefill_supported(KDA_BF16, 128, 128, p))
+        return fail(KDA_ERR_UNSUPPORTED, "the tensor-core prefill is not available");
+    return launched(launch_tc_prefill(p, reinterpret_cast<cudaStream_t>(stream)), "tensor-core prefill (dump)");
+}
+
 size_t kda_prefill_noalloc_capacity(void) { return kStaticScratchBytes; }
 
 kda_status kda_prefill_noalloc(kda_dtype dtype, int B, int T, int H, int dk, int dv, const void *q,

@@ -39,6 +39,9 @@ struct RunParams {
     const int32_t *order;       // non-null: CTA block b / H runs sequence order[b / H] (a permutation)
     int max_chunks;             // > 0: only the first max_chunks chunks of every sequence are run
     const uint8_t *skip;        // non-null: the CTA of (sequence n, head h) exits at once if skip[n*H + h]
+    // Diagnostic (kda_prefill_debug_dump): the chunkwise intermediates of the first (sequence, head).
+    float *dump;                // non-null: plain bf16 d = 128 only
+    int dump_chunks;
 };
 
 // Device error word of the current device (created on first use).

@@ -562,7 +562,12 @@ struct Maps {
 // kGated: the g tensor holds logits x and the kernel forms g = -p.gate_bound * sigmoid(x).
 // kNorm: q and k rows are divided by their L2 norms (sqrt(sum x^2 + 1e-6)) as they are read.
 // kOutGate: O is multiplied by sigmoid(p.out_gate) before it is stored.
-enum : int { kGated = 1, kNorm = 2, kOutGate = 4 };
+// kDump: (diagnostic) the CTA of the first (sequence, head) writes the chunkwise intermediates of
+// its first p.dump_chunks chunks to p.dump (layout: kDumpFloatsPerChunk floats per chunk, see the
+// stage offsets below); the plain path only.
+enum : int { kGated = 1, kNorm = 2, kOutGate = 4, kDump = 8 };
+constexpr int kDumpGam = 0, kDumpA = 64 * 128, kDumpT = kDumpA + 64 * 64, kDumpU = kDumpT + 64 * 64,
+              kDumpS = kDumpU + 64 * 128, kDumpFloatsPerChunk = kDumpS + 128 * 128;
 
 // The gate rows z (this head) of one chunk into the O staging tile, in the tile's own layout: a
 // thread copies 8 of the 1024 16-byte chunks (row e / 16, channels 8 (e % 16) ..). Rows at or past
@@ -588,6 +593,7 @@ template <int F>
 __global__ void __launch_bounds__(NTHREADS, 1)
     kda_prefill_tc_kernel(const __grid_constant__ Maps maps, const RunParams p) {
     constexpr bool GATED = (F & kGated) != 0, NORM = (F & kNorm) != 0, OGATE = (F & kOutGate) != 0;
+    constexpr bool DUMP = (F & kDump) != 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
@@ -918,6 +924,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     float sv[32];
                     tmem_ld32(tmem + tq + TM_S + 32 * cb, sv);
                     tmem_ld_wait();
+                    if (DUMP && blockIdx.x == 0 && c < p.dump_chunks) {  // S at the chunk start, [d_k][d_v]
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            p.dump[(size_t)c * kDumpFloatsPerChunk + kDumpS + (32 * cb + i) * D + v] = sv[i];
+                    }
                     uint32_t w[16];
                     pack32(sv, w, 1.f);
                     tmem_st16(tmem + tq + TM_SA + 16 * cb, w);
@@ -941,6 +952,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const float *sbc = sbeta + 64 * par;
                 ap_readout<NORM>(sm, As, tmem + tq, warp & 3, lane, sbc, nrmb + 128 * (c % 3));
                 state_sync();
+                if (DUMP && blockIdx.x == 0 && c < p.dump_chunks)  // A (strictly lower, beta-scaled rows)
+                    for (int e = v; e < 64 * 64; e += NS) {
+                        const int r = e >> 6, s2 = e & 63;
+                        p.dump[(size_t)c * kDumpFloatsPerChunk + kDumpA + e] = s2 < r ? As[r * SA + s2] : 0.f;
+                    }
                 solve_diag_block(sm, As, Xs, warp & 3, lane, sbc);
                 solve_zero_fill(sm, Xs, v);
             }
@@ -969,6 +985,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 float u[32];
                 tmem_ld32(tmem + tq + TM_U + 32 * hh, u);
                 tmem_ld_wait();
+                if (DUMP && blockIdx.x == 0 && c < p.dump_chunks) {  // U, [token][d_v]
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        p.dump[(size_t)c * kDumpFloatsPerChunk + kDumpU + (32 * hh + i) * D + v] = u[i];
+                }
                 uint32_t w[16];
                 pack32(u, w, 1.f);
                 tmem_st16(tmem + tq + TM_RA + 16 * hh, w);  // U^T replaces -(K+ S)^T (MMA2 has finished)
@@ -1111,6 +1132,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 }
             }
+            if (DUMP && blockIdx.x == 0 && cc < p.dump_chunks) {  // Gam, [token][d_k]
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        p.dump[(size_t)cc * kDumpFloatsPerChunk + kDumpGam + (tr0 + m) * D + 8 * j + i] = gm[m][i];
+            }
             if (tid < 128) {
                 const int ch = tid;
                 const float G15 = wts[ch], G31 = G15 + wts[128 + ch];
@@ -1181,6 +1209,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             fence_async_smem();  // the T stores
             mbar_arrive(&bars[BAR_TREADY]);
+            if (DUMP && blockIdx.x == 0 && c < p.dump_chunks) {  // T = (I + A)^{-1} Diag(beta), [token][token]
+                prep_sync();
+                for (int e = tid; e < 64 * 64; e += NP) {
+                    const int r = e >> 6, s2 = e & 63;
+                    p.dump[(size_t)c * kDumpFloatsPerChunk + kDumpT + e] =
+                        __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + SM_T + kmajor_offset(r, s2, C)));
+                }
+            }
         }
         if (!ok && tid == 0) {
             atomicOr(p.err, kErrTimeout);
@@ -1238,11 +1274,12 @@ bool tc_prefill_supported(kda_dtype dtype, int dk, int dv, const RunParams &p) {
 }
 
 // One instance per combination of the flags, indexed by them.
-const void *const kTcKernels[8] = {
+const void *const kTcKernels[9] = {
     (const void *)kda_prefill_tc_kernel<0>, (const void *)kda_prefill_tc_kernel<1>,
     (const void *)kda_prefill_tc_kernel<2>, (const void *)kda_prefill_tc_kernel<3>,
     (const void *)kda_prefill_tc_kernel<4>, (const void *)kda_prefill_tc_kernel<5>,
-    (const void *)kda_prefill_tc_kernel<6>, (const void *)kda_prefill_tc_kernel<7>};
+    (const void *)kda_prefill_tc_kernel<6>, (const void *)kda_prefill_tc_kernel<7>,
+    (const void *)kda_prefill_tc_kernel<kDump>};
 
 cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
     static std::mutex mu;
@@ -1254,7 +1291,7 @@ cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
         if (!attr_set[dev]) {
-            for (int f = 0; f < 8 && e == cudaSuccess; ++f)
+            for (int f = 0; f < 9 && e == cudaSuccess; ++f)
                 e = cudaFuncSetAttribute(kTcKernels[f], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
             if (e != cudaSuccess) return e;
             attr_set[dev] = true;
@@ -1266,7 +1303,7 @@ cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s) {
         !encode_map(&maps.g, p.g, rows, p.H, p.dk) || !encode_map(&maps.v, p.v, rows, p.H, p.dk) ||
         !encode_map(&maps.o, p.o, rows, p.H, p.dk))
         return cudaErrorInvalidValue;
-    const int f = (p.gate_bound > 0.f ? kGated : 0) | (p.qk_l2norm ? kNorm : 0) | (p.out_gate ? kOutGate : 0);
+    const int f = p.dump ? 8 : (p.gate_bound > 0.f ? kGated : 0) | (p.qk_l2norm ? kNorm : 0) | (p.out_gate ? kOutGate : 0);
     void *args[] = {(void *)&maps, (void *)&p};
     return cudaLaunchKernel(kTcKernels[f], dim3((unsigned)(p.n_seqs * p.H)), dim3(NTHREADS), args, SMEM_BYTES, s);
 }

@@ -236,6 +236,26 @@ KDA_API kda_status kda_prefill_noalloc(kda_dtype dtype, int B, int T, int H, int
                                        const float *initial_state, void *o, float *final_state,
                                        kda_stream_t stream);
 
+/*
+ * kda_prefill_debug_dump -- diagnostic with no counterpart on the pages: it exists so that a test
+ * can locate a fault of the tensor-core prefill to one stage of the chunkwise form. Runs kda_prefill
+ * (bf16, dk == dv == 128, B sequences of T tokens, no cu_seqlens, no options) and, for the first
+ * (sequence, head) only, writes the kernel's intermediates of its first dump_chunks chunks of 64
+ * tokens to `dump` (fp32, device, 16-byte aligned, dump_chunks * 40960 floats), chunk after chunk:
+ *   [0, 8192)       Gam = cumsum of g within the chunk, [token][d_k] (rows past the sequence end
+ *                   repeat the last row)
+ *   [8192, 12288)   A = strict_lower(Diag(beta) (K exp Gam)(K exp -Gam)^T), [token][token]
+ *   [12288, 16384)  T = (I + A)^{-1} Diag(beta) as the kernel's bf16 operand, [token][token]
+ *   [16384, 24576)  U = T (V - (K exp Gam) S), [token][d_v]
+ *   [24576, 40960)  S at the chunk start, [d_k][d_v]
+ * (the quantities of "Kimi Delta Attention: the linear core", maidul-haque blog, in the chunkwise
+ * form). o and final_state as kda_prefill. Returns KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED on the
+ * host, else KDA_OK once queued.
+ */
+KDA_API kda_status kda_prefill_debug_dump(int B, int T, int H, const void *q, const void *k, const void *v,
+                                          const void *g, const void *beta, const float *initial_state, void *o,
+                                          float *final_state, float *dump, int dump_chunks, kda_stream_t stream);
+
 /* Bytes of the fixed scratch array kda_prefill_noalloc uses. */
 KDA_API size_t kda_prefill_noalloc_capacity(void);
 

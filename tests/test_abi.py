@@ -100,6 +100,13 @@ def test_workspace_size_of_the_packed_split(lib):
     assert f(0, 2, 1 << 20, 32, 128, 128, PACKED, 3, 152) == 0              # packed calls have B == 1
 
 
+def test_debug_dump_rejects_bad_arguments(lib):
+    # Sizes and pointers are checked on the host before the device is touched.
+    assert lib.kda_prefill_debug_dump(0, 8, 1, *([None] * 8), None, 1, None) == 1
+    assert lib.kda_prefill_debug_dump(1, 8, 1, *([None] * 8), None, -1, None) == 1
+    assert lib.kda_prefill_debug_dump(1, 8, 1, *([None] * 8), None, 1, None) == 1  # NULL pointers
+
+
 def test_noalloc_capacity_and_argument_checks(lib):
     assert lib.kda_prefill_noalloc_capacity() == 32 << 20
     # Sizes are checked before the scratch is looked at (no device needed to reject them).
