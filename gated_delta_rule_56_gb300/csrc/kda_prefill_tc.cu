@@ -27,28 +27,32 @@
 //                      consecutive rows x 8 channels), the decay-scaled operands, and the block
 //                      merges of T = (I + A)^{-1} Diag(beta). While the A/P MMAs of chunk c run
 //                      they already compute Gam of chunk c + 1.
-//   state warps 8..11  thread = TMEM lane = value column: O of chunk c - 1 out (staged in shared
-//                      memory, one TMA tensor store), the bf16 state copy fused with the decay
-//                      S <- S Diag(gam_last), A and P out of TMEM and the 16 x 16 diagonal blocks
-//                      of the inverse, -(K+ S)^T and U^T as bf16 A operands in TMEM.
+//   state warps 8..11  thread = TMEM lane = value column: the bf16 state copy fused with the
+//                      decay S <- S Diag(gam_last), A and P out of TMEM and the 16 x 16 diagonal
+//                      blocks of the inverse, -(K+ S)^T and U^T as bf16 A operands in TMEM, and O
+//                      of chunk c - 1 out (staged in shared memory, one TMA tensor store) while the
+//                      prep warps merge the inverse of chunk c.
 //   issuer warp 12     the whole warp walks the chunks and one elected lane issues every MMA and
 //                      TMA copy, in the order the work becomes ready; mbarriers carry each
 //                      hand-off between the three groups.
 //   TMA: g (fetched by the prep warps), q/k of the next chunk as soon as the current ones are
 //        read, v once MMA2 has read the last; every tile 64 rows x 128 channels, 128-byte swizzle.
 //   TMEM (512 columns): [0,64) diagonal A|P tile, [64,96) off-diagonal tile, [96,128) the
-//        bf16 A operand -(K+ S)^T then U^T, [128,256) (K+ S | Q+ S -> O), [256,320) U,
-//        [320,448) the fp32 state S^T (lanes = d_v), [448,512) its bf16 copy (MMA1's A).
+//        bf16 A operand -(K+ S)^T then U^T, [128,192) K+ S then U, [192,256) and [256,320) the
+//        Q+ S -> O accumulators of even and odd chunks (O of chunk c is read out while chunk
+//        c + 1 runs), [320,448) the fp32 state S^T (lanes = d_v), [448,512) its bf16 copy.
 //   MMAs (kind::f16, bf16 operands, fp32 accumulate; "tmem" = A read from TMEM; shared-memory
 //   operands in the 128-byte-swizzled layout):
 //        diag  [K*f ; Q*f] x [K/f]^T              M = 128, N = 64, K = 128
 //        off   [K*e ; Q*e] x [K*e']^T             M = 64,  N = 32, K = 128
 //        MMA1  S^T (tmem) x [K+ ; Q+]^T           M = 128, two N = 64 halves, K = 128
 //        MMA2  V^T x T^T  (V tile, MN-major)      N = 64,  K = 64    -> then += -(K+ S)^T (tmem) x T^T = U^T
+//                                                                      (into the columns of K+ S, once read)
 //        MMA3  U^T (tmem) x P^T  (onto (Q+ S)^T)  N = 64,  K = 64    -> O^T
 //        MMA4  U^T (tmem) x Khat  (MN-major B)    N = 128, K = 64    -> S^T
-//   MMA1 starts as soon as the operands and the state copy exist, so it is done long before the
-//   prep warps overwrite [K+ ; Q+] with the next chunk.
+//   MMA1 starts as soon as the operands and the state copy exist. Once it has read [K+ ; Q+], that
+//   region stages O of the previous chunk for its TMA store; the prep warps build the next chunk's
+//   [K+ ; Q+] there after the store has read it (KQFREE).
 //   The 64 x 64 triangular inverse: 16 x 16 diagonal blocks by doubling on CUDA cores, then the
 //   16->32 and 32->64 block merges as tf32 warp-level MMAs.
 // Every mbarrier wait is bounded; on time-out the CTA records kErrTimeout, drains what it
@@ -121,17 +125,23 @@ enum { CST_M0 = 0, CST_M1, CST_C0, CST_C1, CST_EM0, CST_EG31, CST_E63M1, CST_E63
 static_assert(CST_N * 512 <= 4096, "factor rows overflow SM_CST");
 
 // TMEM column offsets.
-constexpr uint32_t TM_AP = 0, TM_OFF = 64, TM_RA = 96, TM_D1 = 128, TM_U = 256, TM_S = 320, TM_SA = 448;
+constexpr uint32_t TM_AP = 0, TM_OFF = 64, TM_RA = 96, TM_D1 = 128, TM_S = 320, TM_SA = 448;
+// O (Q+ S, then += P U) of chunk c in one of two slots by chunk parity, so that MMA1 of chunk c + 1
+// can run before O of chunk c has been read out.
+constexpr uint32_t TM_O0 = TM_D1 + 64, TM_O1 = 256;
+__device__ __forceinline__ uint32_t o_slot(int c) { return (c & 1) ? TM_O1 : TM_O0; }
 constexpr uint32_t TM_COLS = 512;
 
-// Barriers. Up to BAR_DRAIN: TMA copies and MMA commits (one arrival). BAR_OPS, BAR_TREADY: the
-// prep warps have built the intra-chunk operands / written T (NP arrivals). BAR_SREADY ..
-// BAR_EPIDONE: the state warps have made the bf16 state copy (and read out O of the previous
-// chunk) / -(K+ S)^T / U^T / A, P and the diagonal blocks of the inverse (NS arrivals).
+// Barriers. Up to BAR_DRAIN: TMA copies and MMA commits (one arrival; BAR_M1 = the K+ half of
+// MMA1, BAR_M1Q = all of MMA1). BAR_OPS, BAR_TREADY, BAR_S1D0/1: the prep warps have built the
+// intra-chunk operands / written T / finished step 1 of an even / odd chunk (gam_last and beta in
+// place) (NP arrivals). BAR_SREADY .. BAR_KQFREE: the state warps have made the bf16 state copy /
+// -(K+ S)^T / U^T / A, P and the diagonal blocks of the inverse / released the [K+ ; Q+] region
+// (MMA1 has read it and the O store of the previous chunk has read its staging) (NS arrivals).
 enum {
-    BAR_G = 0, BAR_QK, BAR_V, BAR_AP, BAR_M1, BAR_KQFREE, BAR_M2, BAR_M34, BAR_DRAIN,
-    BAR_OPS, BAR_TREADY,
-    BAR_SREADY, BAR_RREADY, BAR_UREADY, BAR_EPIDONE,
+    BAR_G = 0, BAR_QK, BAR_V, BAR_AP, BAR_M1, BAR_M1Q, BAR_M2, BAR_M34, BAR_DRAIN,
+    BAR_OPS, BAR_TREADY, BAR_S1D0, BAR_S1D1,
+    BAR_SREADY, BAR_RREADY, BAR_UREADY, BAR_EPIDONE, BAR_KQFREE,
     BAR_N
 };
 static_assert(BAR_N * 8 <= 256, "barrier region");
@@ -142,6 +152,32 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Eight consecutive floats from 16-byte aligned shared memory.
+__device__ __forceinline__ void lds8(float (&d)[8], const float *src) {
+    const float4 a = *reinterpret_cast<const float4 *>(src), b = *reinterpret_cast<const float4 *>(src + 4);
+    d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = a.w; d[4] = b.x; d[5] = b.y; d[6] = b.z; d[7] = b.w;
+}
+// Two fp32 products in one instruction (each rounded to nearest, as two separate products).
+__device__ __forceinline__ void mul2(float &a, float &b, float x, float y) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(r)
+        : "l"(((uint64_t)__float_as_uint(b) << 32) | __float_as_uint(a)),
+          "l"(((uint64_t)__float_as_uint(y) << 32) | __float_as_uint(x)));
+    a = __uint_as_float((uint32_t)r);
+    b = __uint_as_float((uint32_t)(r >> 32));
+}
+// Two fused multiply-adds in one instruction: a = a * x + u, b = b * y + v (each rounded once).
+__device__ __forceinline__ void fma2(float &a, float &b, float x, float y, float u, float v) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r)
+        : "l"(((uint64_t)__float_as_uint(b) << 32) | __float_as_uint(a)),
+          "l"(((uint64_t)__float_as_uint(y) << 32) | __float_as_uint(x)),
+          "l"(((uint64_t)__float_as_uint(v) << 32) | __float_as_uint(u)));
+    a = __uint_as_float((uint32_t)r);
+    b = __uint_as_float((uint32_t)(r >> 32));
+}
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -331,18 +367,19 @@ template <int MH, bool NORM>
 __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4][8], const float *cst, int r0,
                                                int j, int len, uint32_t khb, const float *nrm) {
     float ref[8], fo_c[8], pe[8], khe[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int ch = 8 * j + i;
-        ref[i] = cst[(MH ? CST_M1 : CST_M0) * 128 + ch];  // the reference Gam, times log2(e)
-        fo_c[i] = cst[(MH ? CST_C1 : CST_C0) * 128 + ch];
-        pe[i] = cst[(MH ? CST_EG31 : CST_EM0) * 128 + ch];
-        khe[i] = cst[(MH ? CST_E63M1 : CST_E63G31) * 128 + ch];
-    }
-#pragma unroll
+    lds8(ref, cst + (MH ? CST_M1 : CST_M0) * 128 + 8 * j);  // the reference Gam, times log2(e)
+    lds8(fo_c, cst + (MH ? CST_C1 : CST_C0) * 128 + 8 * j);
+    lds8(pe, cst + (MH ? CST_EG31 : CST_EM0) * 128 + 8 * j);
+    lds8(khe, cst + (MH ? CST_E63M1 : CST_E63G31) * 128 + 8 * j);
+    // One row per iteration (the loop is kept rolled: the unrolled body is large, and the fetch of
+    // its instructions cost more than the loop).
+#pragma unroll 1
     for (int m = 0; m < 4; ++m) {
         const int r = r0 + m;
         const bool live = r < len;
+        float gr[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) gr[i] = m == 0 ? gm[0][i] : (m == 1 ? gm[1][i] : (m == 2 ? gm[2][i] : gm[3][i]));
         const uint4 kw = *reinterpret_cast<const uint4 *>(sm + SM_K + tile_chunk(r, j));
         const uint4 qw = *reinterpret_cast<const uint4 *>(sm + SM_Q + tile_chunk(r, j));
         const uint32_t kk[4] = {live ? kw.x : 0u, live ? kw.y : 0u, live ? kw.z : 0u, live ? kw.w : 0u};
@@ -350,32 +387,35 @@ __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4]
         const float nk = NORM ? row_inv_norm(nrm, 0, r) : 1.f, nq = NORM ? row_inv_norm(nrm, 1, r) : 1.f;
         float apk[8], apq[8], apb[8], ofr_k[8], ofr_q[8], kp[8], qp[8], kh[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float kv = (i & 1) ? bf_hi(kk[i >> 1]) : bf_lo(kk[i >> 1]);
-            const float qv = (i & 1) ? bf_hi(qq[i >> 1]) : bf_lo(qq[i >> 1]);
+        for (int i = 0; i < 8; i += 2) {  // channel pairs, two products per instruction
+            const float k0 = bf_lo(kk[i >> 1]), k1 = bf_hi(kk[i >> 1]);
+            const float q0 = bf_lo(qq[i >> 1]), q1 = bf_hi(qq[i >> 1]);
             // |Gam_r - ref| <= 80 for g in [-5, 0]; the clamp only keeps factors finite (no 0 * inf)
             // for gates outside that range.
-            const float e = fminf(fmaxf(fmaf(gm[m][i], kLog2e, -ref[i]), -126.f), 126.f);
-            const float f = ex2(e), fi = ex2(-e);
-            apk[i] = kv * f;
-            apq[i] = qv * f;
-            apb[i] = kv * fi;
+            float e0 = gr[i], e1 = gr[i + 1];
+            fma2(e0, e1, kLog2e, kLog2e, -ref[i], -ref[i + 1]);
+            e0 = fminf(fmaxf(e0, -126.f), 126.f);
+            e1 = fminf(fmaxf(e1, -126.f), 126.f);
+            const float f0 = ex2(e0), f1 = ex2(e1), fi0 = ex2(-e0), fi1 = ex2(-e1);
+            apk[i] = k0; apk[i + 1] = k1; mul2(apk[i], apk[i + 1], f0, f1);
+            apq[i] = q0; apq[i + 1] = q1; mul2(apq[i], apq[i + 1], f0, f1);
+            apb[i] = k0; apb[i + 1] = k1; mul2(apb[i], apb[i + 1], fi0, fi1);
             if (MH) {
-                ofr_k[i] = apk[i] * fo_c[i];  // K exp(Gam_r - Gam_31): off-tile row
-                ofr_q[i] = apq[i] * fo_c[i];  // Q exp(Gam_r - Gam_31)
-                kp[i] = ofr_k[i] * pe[i];     // K exp(Gam_r)
-                qp[i] = ofr_q[i] * pe[i];     // Q exp(Gam_r)
-                kh[i] = apb[i] * khe[i];      // K exp(Gam_63 - Gam_r)
+                ofr_k[i] = apk[i]; ofr_k[i + 1] = apk[i + 1]; mul2(ofr_k[i], ofr_k[i + 1], fo_c[i], fo_c[i + 1]);
+                ofr_q[i] = apq[i]; ofr_q[i + 1] = apq[i + 1]; mul2(ofr_q[i], ofr_q[i + 1], fo_c[i], fo_c[i + 1]);
+                kp[i] = ofr_k[i]; kp[i + 1] = ofr_k[i + 1]; mul2(kp[i], kp[i + 1], pe[i], pe[i + 1]);
+                qp[i] = ofr_q[i]; qp[i + 1] = ofr_q[i + 1]; mul2(qp[i], qp[i + 1], pe[i], pe[i + 1]);
+                kh[i] = apb[i]; kh[i + 1] = apb[i + 1]; mul2(kh[i], kh[i + 1], khe[i], khe[i + 1]);
             } else {
-                ofr_k[i] = apb[i] * fo_c[i];  // K exp(Gam_31 - Gam_r): off-tile column
-                kp[i] = apk[i] * pe[i];       // K exp(Gam_r)
-                qp[i] = apq[i] * pe[i];       // Q exp(Gam_r)
-                kh[i] = ofr_k[i] * khe[i];    // K exp(Gam_63 - Gam_r)
+                ofr_k[i] = apb[i]; ofr_k[i + 1] = apb[i + 1]; mul2(ofr_k[i], ofr_k[i + 1], fo_c[i], fo_c[i + 1]);
+                kp[i] = apk[i]; kp[i + 1] = apk[i + 1]; mul2(kp[i], kp[i + 1], pe[i], pe[i + 1]);
+                qp[i] = apq[i]; qp[i + 1] = apq[i + 1]; mul2(qp[i], qp[i + 1], pe[i], pe[i + 1]);
+                kh[i] = ofr_k[i]; kh[i + 1] = ofr_k[i + 1]; mul2(kh[i], kh[i + 1], khe[i], khe[i + 1]);
             }
             if (NORM) {  // the state operands take the normalised rows
-                kp[i] *= nk;
-                qp[i] *= nq;
-                kh[i] *= nk;
+                mul2(kp[i], kp[i + 1], nk, nk);
+                mul2(qp[i], qp[i + 1], nq, nq);
+                mul2(kh[i], kh[i + 1], nk, nk);
             }
         }
         st_chunk(sm, SM_AP + sw_chunk(r, j, 128), apk);
@@ -585,7 +625,7 @@ __device__ __forceinline__ void stage_gate_rows(uint8_t *sm, const __nv_bfloat16
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int e = v + 128 * i, row = e >> 4, cj = e & 15;
-        *reinterpret_cast<uint4 *>(sm + SM_T + (cj >> 3) * 8192 + row * 128 + (((cj & 7) ^ (row & 7)) << 4)) = z[i];
+        *reinterpret_cast<uint4 *>(sm + SM_KQ + (cj >> 3) * 8192 + row * 128 + (((cj & 7) ^ (row & 7)) << 4)) = z[i];
     }
 }
 
@@ -655,6 +695,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (warp == kIssuer) {
         // ---------------------------------------------------------------- issuer warp --------
+        // The TMEM base as a warp-uniform value (lane 0's), so every MMA address is uniform.
+        const uint32_t tmem = __shfl_sync(0xffffffffu, *tptr, 0);
         // The whole warp walks the chunks (one elected lane issues each MMA and copy) in the
         // order the work becomes ready: the chunk-parallel MMAs of chunk c (their operands come
         // from the prep warps), then the state chain of chunk c (MMA1, MMA2, MMA3/4) while the
@@ -742,25 +784,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mma_commit_warp(&bars[BAR_M1]);
 #pragma unroll
             for (int st = 0; st < D / 16; ++st)
-                mma_bf16_tmem_a_warp(tmem + TM_D1 + 64, tmem + TM_SA + 8 * st, d_q + ksw(st, 128), idesc_bf16(128, 64),
+                mma_bf16_tmem_a_warp(tmem + o_slot(cc), tmem + TM_SA + 8 * st, d_q + ksw(st, 128), idesc_bf16(128, 64),
                                      st > 0);
-            mma_commit_warp(&bars[BAR_KQFREE]);
-            // ... U^T = V^T T^T once T exists (V tile as an MN-major A operand; skipped for v = 0) ...
+            mma_commit_warp(&bars[BAR_M1Q]);
+            // ... U^T = V^T T^T - (K+ S)^T T^T once T exists and -(K+ S)^T has been read out of
+            // TM_D1, which U^T then takes over (V tile as an MN-major A operand, skipped for v = 0;
+            // the second product reads -(K+ S)^T from TMEM) ...
             if (!(iok = wait(BAR_TREADY, par))) break;
+            if (!(iok = wait(BAR_RREADY, par))) break;
+            if (!p.zero_v && !(iok = wait(BAR_V, par))) break;
+            tc_fence_after();
             if (!p.zero_v) {
-                if (!(iok = wait(BAR_V, par))) break;
-                tc_fence_after();
 #pragma unroll
                 for (int st = 0; st < C / 16; ++st)
-                    mma_bf16_warp(tmem + TM_U, d_v + kDescStepMN128 * st, d_t + kDescStepKmajor * st,
+                    mma_bf16_warp(tmem + TM_D1, d_v + kDescStepMN128 * st, d_t + kDescStepKmajor * st,
                                   idesc_bf16(128, 64) | kIdescAMajorMN, st > 0);
             }
-            // ... U^T += -(K+ S)^T T^T (A from TMEM) ...
-            if (!(iok = wait(BAR_RREADY, par))) break;
-            tc_fence_after();
 #pragma unroll
             for (int st = 0; st < C / 16; ++st)
-                mma_bf16_tmem_a_warp(tmem + TM_U, tmem + TM_RA + 8 * st, d_t + kDescStepKmajor * st,
+                mma_bf16_tmem_a_warp(tmem + TM_D1, tmem + TM_RA + 8 * st, d_t + kDescStepKmajor * st,
                                      idesc_bf16(128, 64), (!p.zero_v || st > 0) ? 1u : 0u);
             mma_commit_warp(&bars[BAR_M2]);
             if (more && !p.zero_v) {  // the v tile is consumed: fetch the next one
@@ -772,7 +814,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_after();
 #pragma unroll
             for (int st = 0; st < C / 16; ++st)
-                mma_bf16_tmem_a_warp(tmem + TM_D1 + 64, tmem + TM_RA + 8 * st, d_p + kDescStepKmajor * st,
+                mma_bf16_tmem_a_warp(tmem + o_slot(cc), tmem + TM_RA + 8 * st, d_p + kDescStepKmajor * st,
                                      idesc_bf16(128, 64), 1u);
             const uint64_t d_kh = par ? d_kh1 : d_kh0;
 #pragma unroll
@@ -844,8 +886,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         };
 
-        // O of a finished chunk through the T/P region (free from M34 of that chunk until the next
-        // chunk's A/P read-out) in the TMA tile layout, then one bulk tensor store per 64 channels.
+        // O of a finished chunk through the [K+ ; Q+] region (free from MMA1 of the next chunk until
+        // the prep warps build the chunk after it) in the TMA tile layout, then one bulk tensor store
+        // per 64 channels.
         // A ragged chunk that does not end the tensor takes plain stores, so rows of the next
         // sequence are never written.
         const long long total_rows = p.cu_seqlens ? (long long)p.T : (long long)p.n_seqs * p.T;
@@ -867,13 +910,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int b = 0; b < 8; ++b)
                         sg[b] = OGATE ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                            sm + SM_T + ost[b] + (base + r8) * 128))
+                                            sm + SM_KQ + ost[b] + (base + r8) * 128))
                                       : 0.f;
 #pragma unroll
                     for (int b = 0; b < 8; ++b) {
                         float x = o[r8 + b];
                         if (OGATE) x *= __fdividef(1.f, 1.f + ex2(-sg[b] * kLog2e));
-                        *reinterpret_cast<__nv_bfloat16 *>(sm + SM_T + ost[b] + (base + r8) * 128) =
+                        *reinterpret_cast<__nv_bfloat16 *>(sm + SM_KQ + ost[b] + (base + r8) * 128) =
                             __float2bfloat16_rn(x);
                     }
                 };
@@ -884,8 +927,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 fence_async_smem();
                 state_sync();
                 if (v == 0) {
-                    tma_store_3d(&maps.o, sm + SM_T, 0, h, (int)r0);
-                    tma_store_3d(&maps.o, sm + SM_T + 8192, 64, h, (int)r0);
+                    tma_store_3d(&maps.o, sm + SM_KQ, 0, h, (int)r0);
+                    tma_store_3d(&maps.o, sm + SM_KQ + 8192, 64, h, (int)r0);
                     bulk_commit();
                 }
             } else {
@@ -893,6 +936,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         };
 
+        // O of chunk cc (its TMEM slot) out through the staging tile; then the [K+ ; Q+] region is
+        // released to the prep warps (KQFREE) once the store has read it.
+        auto flush_o = [&](int cc, long long r0, int ln) {
+            float o0[32], o1[32];
+            tmem_ld32(tmem + tq + o_slot(cc), o0);
+            tmem_ld32(tmem + tq + o_slot(cc) + 32, o1);
+            tmem_ld_wait();
+            write_o(o0, o1, r0, ln);
+            if (v == 0) bulk_wait_read_all();
+        };
         long long prev_row0 = 0;
         int prev_len = 0;
         int c = 0;
@@ -903,19 +956,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int len = (int)min((long long)C, eos - row0);
             if (OGATE && (v >> 1) < len && 64 * (v & 1) < dg)  // this chunk's gate rows into L2 (read when its O is written)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(zg + ((size_t)(row0 + (v >> 1)) * H + h) * dg + 64 * (v & 1)));
-            if (c > 0) {  // O of the previous chunk, once MMA3 and MMA4 of it have completed
-                if (!(ok = state_wait(&bars[BAR_M34], par ^ 1u))) break;
-                tc_fence_after();
-                float o0[32], o1[32];
-                tmem_ld32(tmem + tq + TM_D1 + 64, o0);
-                tmem_ld32(tmem + tq + TM_D1 + 96, o1);
-                tmem_ld_wait();
-                write_o(o0, o1, prev_row0, prev_len);
-            }
-            // OPS of chunk c: its operands, and gam_last written by its step 1, are in place. Waited
-            // before SREADY, so OPS of chunk c + 1 (which needs MMA1 of chunk c) cannot have
-            // completed yet and the parity cannot alias.
-            if (!(ok = state_wait(&bars[BAR_OPS], par))) break;
+            // The state after chunk c - 1 (MMA4) and gam_last of chunk c (its step 1).
+            if (c > 0 && !(ok = state_wait(&bars[BAR_M34], par ^ 1u))) break;
+            if (!(ok = state_wait(&bars[c & 1 ? BAR_S1D1 : BAR_S1D0], (uint32_t)((c >> 1) & 1)))) break;
+            tc_fence_after();
             // One pass over the state: its bf16 copy for MMA1, and S <- S Diag(gam_last) for MMA4.
             {
                 const float *gc = gcs + 128 * (c % 3);
@@ -933,7 +977,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     pack32(sv, w, 1.f);
                     tmem_st16(tmem + tq + TM_SA + 16 * cb, w);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) sv[i] *= gc[32 * cb + i];
+                    for (int i = 0; i < 32; i += 8) {
+                        float gv[8];
+                        lds8(gv, gc + 32 * cb + i);
+#pragma unroll
+                        for (int t = 0; t < 8; t += 2) mul2(sv[i + t], sv[i + t + 1], gv[t], gv[t + 1]);
+                    }
                     tmem_st32(tmem + tq + TM_S + 32 * cb, sv);
                 }
                 tmem_st_wait();
@@ -941,13 +990,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             mbar_arrive(&bars[BAR_SREADY]);
 
-            // A and P out of TMEM and the 16 x 16 diagonal blocks of (I + A)^{-1}, while the prep
-            // warps run step 1 of the next chunk; they merge the blocks once EPIDONE is signalled.
-            // P is rewritten only after MMA3 of the previous chunk (M34 above).
+            // A and P out of TMEM and the 16 x 16 diagonal blocks of (I + A)^{-1}; the prep warps
+            // merge the blocks once EPIDONE is signalled. P and T are rewritten only after MMA2 and
+            // MMA3 of the previous chunk (M34 above).
             if (!(ok = state_wait(&bars[BAR_AP], par))) break;
             tc_fence_after();
-            if (v == 0) bulk_wait_read_all();  // the O store has read the T/P region
-            state_sync();
             {
                 const float *sbc = sbeta + 64 * par;
                 ap_readout<NORM>(sm, As, tmem + tq, warp & 3, lane, sbc, nrmb + 128 * (c % 3));
@@ -978,12 +1025,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             mbar_arrive(&bars[BAR_RREADY]);
 
+            // O of the previous chunk, while the prep warps merge the inverse: staged in the
+            // [K+ ; Q+] region once MMA1 of this chunk has read it.
+            if (!(ok = state_wait(&bars[BAR_M1Q], par))) break;
+            tc_fence_after();
+            if (c > 0) flush_o(c - 1, prev_row0, prev_len);
+            mbar_arrive(&bars[BAR_KQFREE]);
+
             if (!(ok = state_wait(&bars[BAR_M2], par))) break;
             tc_fence_after();
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
                 float u[32];
-                tmem_ld32(tmem + tq + TM_U + 32 * hh, u);
+                tmem_ld32(tmem + tq + TM_D1 + 32 * hh, u);
                 tmem_ld_wait();
                 if (DUMP && blockIdx.x == 0 && c < p.dump_chunks) {  // U, [token][d_v]
 #pragma unroll
@@ -1004,11 +1058,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ok = state_wait(&bars[BAR_M34], (uint32_t)((nchunks - 1) & 1));
             if (ok) {
                 tc_fence_after();
-                float o0[32], o1[32];
-                tmem_ld32(tmem + tq + TM_D1 + 64, o0);
-                tmem_ld32(tmem + tq + TM_D1 + 96, o1);
-                tmem_ld_wait();
-                write_o(o0, o1, prev_row0, prev_len);
+                flush_o(nchunks - 1, prev_row0, prev_len);
             }
         }
         if (v == 0) bulk_wait_all();  // every O store is complete (and has read shared memory)
@@ -1154,6 +1204,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 gcs[128 * (cc % 3) + ch] = ex2(G63 * kLog2e);
             }
             prep_sync();
+            mbar_arrive(&bars[(cc & 1) ? BAR_S1D1 : BAR_S1D0]);  // gam_last and beta of chunk cc are in place
             return true;
         };
 
