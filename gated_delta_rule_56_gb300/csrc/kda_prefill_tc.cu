@@ -304,7 +304,8 @@ __device__ __forceinline__ void state_sync() { group_sync<2, NS>(); }
 // product stays in range. Rows past the sequence end (r >= len) act as identity tokens.
 // Row sums of squares of k and q for the L2 normalisation, one buffer per chunk index mod 3:
 // step 1 of chunk c adds into buffer c % 3 (and zeroes buffer (c + 1) % 3, last read by the
-// operands of chunk c - 2); the operands of chunk c read it after step 1's closing barrier.
+// operands of chunk c - 2), then replaces each sum s by 1 / sqrt(s + 1e-6); the operands and the
+// A/P read-out of chunk c read it after step 1's closing barrier.
 // The thread's 4 rows x 8 channels of q and k come from global memory (the same lines the TMA
 // fetches for the operands later). Each thread sums its 8 channels per row; the 8 lanes of a row
 // group reduce the 8 sums (4 k rows, 4 q rows) by halving exchanges, lane i ending with sum i,
@@ -358,10 +359,9 @@ __device__ __forceinline__ void add_row_square_sums(float *nrm, const QKRows &x,
     atomicAdd(nrm + (i >> 2) * 64 + r0 + (i & 3), tot);
 }
 
-// 1 / sqrt(sum x^2 + 1e-6) of row r of k (kq = 0) or q (kq = 1) from a completed buffer.
-__device__ __forceinline__ float row_inv_norm(const float *nrm, int kq, int r) {
-    return rsqrtf(nrm[kq * 64 + r] + 1e-6f);
-}
+// 1 / sqrt(sum x^2 + 1e-6) of row r of k (kq = 0) or q (kq = 1) from a completed buffer (step 1
+// turns the sums into these values once, between its two barriers).
+__device__ __forceinline__ float row_inv_norm(const float *nrm, int kq, int r) { return nrm[kq * 64 + r]; }
 
 template <int MH, bool NORM>
 __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4][8], const float *cst, int r0,
@@ -1188,6 +1188,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         p.dump[(size_t)cc * kDumpFloatsPerChunk + kDumpGam + (tr0 + m) * D + 8 * j + i] = gm[m][i];
+            }
+            if (NORM && tid < 128) {  // the row sums of squares are complete: inverse norms in place
+                float *nb = nrmb + 128 * (cc % 3) + tid;
+                *nb = rsqrtf(*nb + 1e-6f);
             }
             if (tid < 128) {
                 const int ch = tid;
