@@ -202,10 +202,15 @@ def test_long_context_every_head():
     earlier tokens can move the final state by at most prod_t max_c exp(g_t,c) * ||S_{T-M}||_F,
     which the test computes from the data and requires to be negligible. Outputs where a split
     call joins segments (T/4, T/2, 3T/4): the oracle from a zero state M tokens earlier, under the
-    same bound (|o_t| moves by at most that bound times |q_t|)."""
+    same bound (|o_t| moves by at most that bound times |q_t|). The same tokens passed as one
+    packed sequence (cu_seqlens = [0, T], segments planned on the device) are cut into the same
+    segments and give the same bits, so every check below holds for both calls."""
     T, H, d, M, P = 1 << 20, 32, 128, 2048, 32768
     x = ki.prefill_inputs(1, T, H, d, d, device=DEV, seed=0)
     o, s = run(x)
+    op, sp = run(dict(x, cu_seqlens=torch.tensor([0, T], dtype=torch.int32, device=DEV)))
+    assert torch.equal(op, o) and torch.equal(sp, s)
+    del op, sp
     ro, _ = oracle.recurrent(*(x[n][:, :P].cpu() for n in NAMES))
     oh = o[0, :P].cpu()
     for h in range(H):
