@@ -65,14 +65,17 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
                     help="leave the varlen and long-context sub-lines out of the default line")
-    ap.add_argument("--workload", choices=("varlen", "long", "gated", "l2norm", "outgate", "backward"), default=None,
+    ap.add_argument("--workload", choices=("varlen", "long", "gated", "l2norm", "outgate", "backward", "fp32", "d64"),
+                    default=None,
                     help="time one of the other prefill workloads instead of the headline (one JSON line): "
                          "varlen = 64 packed sequences of U[128, 16384] tokens with initial states; "
                          "long = one sequence of 1,048,576 tokens (B=1, H=32); "
                          "gated = the headline shape with gate logits (decays formed in the kernel); "
                          "l2norm = the headline shape with raw q/k rows L2-normalised in the kernel; "
                          "outgate = the headline shape with the output gate o * sigmoid(z) in the kernel; "
-                         "backward = all gradients of the headline shape (kda_backward)")
+                         "backward = all gradients of the headline shape (kda_backward); "
+                         "fp32 = the small fp32 configuration B=1 T=256 H=2 d=64 (tf32 tensor-core kernel); "
+                         "d64 = the headline shape with heads of 64 channels (bf16)")
     ap.add_argument("--ncu-case", choices=("prefill", "decode", "decode256", "backward", "long", "varlen"),
                     help="run two launches of the small profiling case (for ncu) and exit")
     args = ap.parse_args(argv)
@@ -555,6 +558,21 @@ def workload_line(args, workload, dev, ranks):
         kw = dict(out_gate=ki.gate_logits_like(x["v"], seed=3))  # z ~ N(0, 1): o * sigmoid(z) is stored
         alg = prefill_bytes(B, T, H, d) + tokens * H * d * 2    # + the gate input z (bf16)
         name = f"KDA chunked prefill with the output gate o*sigmoid(z) in the kernel: B={B} T={T} H={H} dk=dv={d} bf16, zero init"
+    elif workload == "fp32":
+        # the small fp32 configuration: B=1 T=256 H=2 d=64 (the tf32 tensor-core kernel)
+        B, T, H, d = 1, 256, 2, 64
+        x = ki.prefill_inputs(B, T, H, d, d, dtype=torch.float32, device=dev, seed=0)
+        tokens, n_seq = B * T, B
+        kw = {}
+        alg = tokens * H * (4 * d * 4 + 4 + 4 * d) + n_seq * H * d * d * 4
+        name = f"KDA chunked prefill fp32 (tf32 tensor-core kernel): B={B} T={T} H={H} dk=dv={d}, zero init"
+    elif workload == "d64":
+        B, T, d = PF["B"], PF["T"], 64
+        x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)
+        tokens, n_seq = B * T, B
+        kw = {}
+        alg = prefill_bytes(B, T, H, d)
+        name = f"KDA chunked prefill, heads of 64 channels (the d=128 tensor-core kernel, missing channels zero): B={B} T={T} H={H} dk=dv={d} bf16, zero init"
     elif workload == "l2norm":
         B, T = PF["B"], PF["T"]
         x = ki.prefill_inputs(B, T, H, d, d, device=dev, seed=0)
@@ -575,7 +593,8 @@ def workload_line(args, workload, dev, ranks):
     # A call that the library splits along the sequence (few long sequences; it asks for a
     # workspace) launches 7 kernels: segment bounds, the local pass, the transition pass up to the
     # horizon, the zero test, the transition pass over the rest, the scan and the correction.
-    split = workload not in ("varlen", "backward") and kda.load().kda_prefill_workspace_size(0, n_seq, tokens // n_seq, H, d, d, None, n_seq) > 0
+    dt_code = 1 if workload == "fp32" else 0  # kda_dtype of the inputs
+    split = workload not in ("varlen", "backward") and kda.load().kda_prefill_workspace_size(dt_code, n_seq, tokens // n_seq, H, d, d, None, n_seq) > 0
     launches_per_step = 7 if split else 1
     # Packed sequences with the workspace: the longest-first sort of cu_seqlens, then the prefill.
     if workload == "varlen" and kda.load().kda_prefill_workspace_size(0, 1, tokens, H, d, d, x["cu_seqlens"].data_ptr(), n_seq) > 0:
@@ -640,7 +659,8 @@ def workload_line(args, workload, dev, ranks):
         "metric": f"KDA {'backward' if workload == 'backward' else 'prefill'} tokens/s ({workload})",
         "value": ranks.job_throughput(tokens * steps, total_ms), "unit": "tokens/s",
         "n_gpus": ranks.world, "steps": steps, "warmup": warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
-        "dtype": "bf16", "data": "synthetic", "config": {"workload": name, "pairs": n_seq * H, "split_along_sequence": bool(split)},
+        "dtype": "tf32" if workload == "fp32" else "bf16", "data": "synthetic",
+        "config": {"workload": name, "pairs": n_seq * H, "split_along_sequence": bool(split)},
         "roofline": roof,
         "gpu_launches": steps * launches_per_step, "clocks": clk.summary()}
     if packed:

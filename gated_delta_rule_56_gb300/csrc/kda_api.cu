@@ -319,6 +319,7 @@ kda_status prefill_impl(kda_dtype dtype, int B, int T, int H, int dk, int dv, co
             return launched(launch_segmented_prefill(p, B, workspace, workspace_bytes, s), "segmented prefill");
         return launched(launch_tc_prefill(p, s), "tensor-core prefill");
     }
+    if (tf32_prefill_supported(dtype, dk, dv, p)) return launched(launch_tf32_prefill(p, s), "tf32 tensor-core prefill");
     return launched(launch_recurrent(dtype, dk, dv, p, s), "recurrent prefill");
 }
 

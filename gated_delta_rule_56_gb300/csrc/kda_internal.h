@@ -54,6 +54,11 @@ cudaError_t launch_recurrent(kda_dtype dtype, int dk, int dv, const RunParams &p
 bool tc_prefill_supported(kda_dtype dtype, int dk, int dv, const RunParams &p);
 cudaError_t launch_tc_prefill(const RunParams &p, cudaStream_t s);
 
+// Tensor-core chunked prefill in tf32 (fp32, dk == dv in {32, 64}, without the L2 normalisation
+// and the output gate).
+bool tf32_prefill_supported(kda_dtype dtype, int dk, int dv, const RunParams &p);
+cudaError_t launch_tf32_prefill(const RunParams &p, cudaStream_t s);
+
 // TMA map of a bf16 [rows, H, d] tensor in boxes of 64 rows x 64 channels (128-byte swizzle), the
 // tile of the tensor-core kernels (channels past d read as zeros and are not written). False if the
 // driver's encoder is unavailable or rejects it.

@@ -54,7 +54,8 @@ def test_gated_prefill_varlen():
     assert_close(s, rs, "final_state")
 
 
-def test_gated_prefill_fp32_recurrent_path():
+def test_gated_prefill_fp32_tf32_path():
+    """fp32 with gate logits runs the tf32 tensor-core kernel (heads of 64 channels)."""
     x = _gated(ki.prefill_inputs(1, 96, 2, 64, 64, dtype=torch.float32, device=DEV, seed=35, state_std=0.02),
                seed=36)
     o, s = kda.prefill(x["q"], x["k"], x["v"], x["x"], x["beta"], initial_state=x["initial_state"], gate_bound=2.0)

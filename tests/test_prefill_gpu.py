@@ -52,7 +52,7 @@ def pair(x, b, h, rows=None):
 
 
 def test_fp32_small_head_matches_oracle():
-    """fp32 inputs, B=1, T=256, H=2, d=64, zero initial state."""
+    """fp32 inputs, B=1, T=256, H=2, d=64, zero initial state (the tf32 tensor-core kernel)."""
     x = ki.prefill_inputs(1, 256, 2, 64, 64, dtype=torch.float32, device=DEV, seed=0)
     o, s = run(x)
     ro, rs = ref(x)
