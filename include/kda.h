@@ -120,6 +120,11 @@ typedef struct kda_options {
  *              rounding. The caller owns the workspace; it must not be used by other work on
  *              other streams until this call's work is done.
  * Alignment: all pointers 16-byte aligned. Rows of q, k, v, g, o are contiguous.
+ * Paths: bf16 runs the chunked tensor-core kernel (bf16 operands, fp32 accumulation; heads of
+ * 32 or 64 channels with the missing channels zero). fp32 with dk == dv in {32, 64} runs a
+ * chunked tensor-core kernel in tf32 (operands rounded to tf32, fp32 accumulation and state);
+ * fp32 with dk == dv == 128, or with the L2 normalisation or the output gate of kda_prefill_ex,
+ * runs the token-by-token recurrence on the CUDA cores in fp32.
  * Returns KDA_OK once the work is queued on `stream`.
  */
 KDA_API kda_status kda_prefill(kda_dtype dtype, int B, int T, int H, int dk, int dv,
