@@ -178,6 +178,40 @@ __device__ __forceinline__ void fma2(float &a, float &b, float x, float y, float
     a = __uint_as_float((uint32_t)r);
     b = __uint_as_float((uint32_t)(r >> 32));
 }
+
+// 16 TMEM lanes x 64 fp32 columns in the MMA-fragment layout (tcgen05.ld 16x256b, 8 repetitions):
+// register 4k + 0/1 = (lane g, columns 8k + 2t, + 1), 4k + 2/3 = (lane g + 8, the same columns),
+// with g = thread / 4 and t = thread % 4 of the warp; taddr's lane field selects the 16 lanes.
+__device__ __forceinline__ void tmem_ld_frag64(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// The inverse of stmatrix_x4_trans: four 8 x 8 bf16 matrices read transposed into fragments.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t saddr, uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "r"(saddr)
+                 : "memory");
+}
+
+// Four 8 x 8 bf16 matrices, each stored transposed: lane 8i + j gives the address of row j of
+// the transpose of matrix i; each thread's register i holds its fragment of matrix i.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a),
+                 "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -886,65 +920,66 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         };
 
-        // O of a finished chunk through the [K+ ; Q+] region (free from MMA1 of the next chunk until
-        // the prep warps build the chunk after it) in the TMA tile layout, then one bulk tensor store
-        // per 64 channels.
-        // A ragged chunk that does not end the tensor takes plain stores, so rows of the next
+        // O of chunk cc (its TMEM slot) out. A chunk that is full (or ends the tensor: rows past its
+        // end are not written) goes through the [K+ ; Q+] region (free from MMA1 of the next chunk
+        // until the prep warps build the chunk after it) in the TMA tile layout, one bulk tensor
+        // store per 64 channels, after which the region is released to the prep warps (KQFREE). A
+        // ragged chunk that does not end the tensor takes plain stores, so rows of the next
         // sequence are never written.
         const long long total_rows = p.cu_seqlens ? (long long)p.T : (long long)p.n_seqs * p.T;
-        uint32_t ost[8];  // offset of (row b, value column v) in the staged tile, b = row % 8
-#pragma unroll
-        for (int b = 0; b < 8; ++b)
-            ost[b] = (uint32_t)((v >> 6) * 8192 + b * 128 + ((((v >> 3) & 7) ^ b) << 4) + (v & 7) * 2);
-        auto write_o = [&](const float (&o0)[32], const float (&o1)[32], long long r0, int ln) {
-            if (ln == C || r0 + ln >= total_rows) {  // rows past the tensor end are not written
+        auto flush_o = [&](int cc, long long r0, int ln) {
+            if (ln == C || r0 + ln >= total_rows) {
+                // The warp's 32 value columns x 64 tokens in the MMA-fragment layout, bf16 pairs of
+                // consecutive tokens, stored transposed by stmatrix straight into the TMA tile
+                // layout (16 bytes = 8 value columns of one token per row of each matrix).
+                const uint32_t lq = (uint32_t)(32 * (warp & 3));
+                uint32_t f0[32], f1[32];
+                tmem_ld_frag64(tmem + (lq << 16) + o_slot(cc), f0);
+                tmem_ld_frag64(tmem + ((lq + 16) << 16) + o_slot(cc), f1);
+                tmem_ld_wait();
+                const int i4 = lane >> 3, jr = lane & 7;
+                const int cj = (int)((lq + 16 * (i4 >> 1) + 8 * (i4 & 1)) >> 3);  // 8-column chunk of matrix i4
+                const uint32_t abase = sb + SM_KQ + (uint32_t)((cj >> 3) * 8192);
                 if (OGATE) {
-                    // z into the tile first; each thread then scales its fp32 O by sigmoid(z) read
-                    // from the element it overwrites, so O is rounded to bf16 once.
+                    // z into the tile first; each O value is scaled by sigmoid(z) read back in the
+                    // same fragment layout, so O is rounded to bf16 once.
                     stage_gate_rows(sm, zg, r0, (int)min((long long)C, total_rows - r0), H, h, v, dg);
                     state_sync();
                 }
-                // 8 rows at a time: the 8 gate values are read before any of the 8 stores.
-                auto put8 = [&](const float (&o)[32], int r8, int base) {
-                    float sg[8];
+                auto gate = [&](float x, float z) { return x * __fdividef(1.f, 1.f + ex2(-z * kLog2e)); };
 #pragma unroll
-                    for (int b = 0; b < 8; ++b)
-                        sg[b] = OGATE ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                            sm + SM_KQ + ost[b] + (base + r8) * 128))
-                                      : 0.f;
-#pragma unroll
-                    for (int b = 0; b < 8; ++b) {
-                        float x = o[r8 + b];
-                        if (OGATE) x *= __fdividef(1.f, 1.f + ex2(-sg[b] * kLog2e));
-                        *reinterpret_cast<__nv_bfloat16 *>(sm + SM_KQ + ost[b] + (base + r8) * 128) =
-                            __float2bfloat16_rn(x);
+                for (int k = 0; k < 8; ++k) {
+                    const int tok = 8 * k + jr;
+                    const uint32_t addr = abase + (uint32_t)(tok * 128 + (((cj & 7) ^ (tok & 7)) << 4));
+                    float a0 = __uint_as_float(f0[4 * k]), a1 = __uint_as_float(f0[4 * k + 1]);
+                    float b0 = __uint_as_float(f0[4 * k + 2]), b1 = __uint_as_float(f0[4 * k + 3]);
+                    float c0 = __uint_as_float(f1[4 * k]), c1 = __uint_as_float(f1[4 * k + 1]);
+                    float d0 = __uint_as_float(f1[4 * k + 2]), d1 = __uint_as_float(f1[4 * k + 3]);
+                    if (OGATE) {
+                        uint32_t za, zb, zc, zd;
+                        ldmatrix_x4_trans(addr, za, zb, zc, zd);
+                        a0 = gate(a0, bf_lo(za)); a1 = gate(a1, bf_hi(za));
+                        b0 = gate(b0, bf_lo(zb)); b1 = gate(b1, bf_hi(zb));
+                        c0 = gate(c0, bf_lo(zc)); c1 = gate(c1, bf_hi(zc));
+                        d0 = gate(d0, bf_lo(zd)); d1 = gate(d1, bf_hi(zd));
                     }
-                };
-#pragma unroll
-                for (int r8 = 0; r8 < 32; r8 += 8) put8(o0, r8, 0);
-#pragma unroll
-                for (int r8 = 0; r8 < 32; r8 += 8) put8(o1, r8, 32);
+                    stmatrix_x4_trans(addr, pack_bf16(a0, a1), pack_bf16(b0, b1), pack_bf16(c0, c1), pack_bf16(d0, d1));
+                }
                 fence_async_smem();
                 state_sync();
                 if (v == 0) {
                     tma_store_3d(&maps.o, sm + SM_KQ, 0, h, (int)r0);
                     tma_store_3d(&maps.o, sm + SM_KQ + 8192, 64, h, (int)r0);
                     bulk_commit();
+                    bulk_wait_read_all();
                 }
-            } else {
-                store_o(o0, o1, r0, ln);
+                return;
             }
-        };
-
-        // O of chunk cc (its TMEM slot) out through the staging tile; then the [K+ ; Q+] region is
-        // released to the prep warps (KQFREE) once the store has read it.
-        auto flush_o = [&](int cc, long long r0, int ln) {
             float o0[32], o1[32];
             tmem_ld32(tmem + tq + o_slot(cc), o0);
             tmem_ld32(tmem + tq + o_slot(cc) + 32, o1);
             tmem_ld_wait();
-            write_o(o0, o1, r0, ln);
-            if (v == 0) bulk_wait_read_all();
+            store_o(o0, o1, r0, ln);
         };
         long long prev_row0 = 0;
         int prev_len = 0;
