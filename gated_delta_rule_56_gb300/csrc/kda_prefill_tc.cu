@@ -302,11 +302,14 @@ __device__ __forceinline__ void group_sync() {
     asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
 }
 
-// Every thread of a warp group waits on `bar`; true only if all of them saw the phase complete,
-// so the group leaves its loop together when a wait runs out.
+// Every thread of a warp group waits on `bar` (and then on `bar2`, if given: two waits share one
+// group barrier); true only if all of them saw the phases complete, so the group leaves its loop
+// together when a wait runs out.
 template <int ID, int N>
-__device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity) {
-    const uint32_t bad = mbar_wait(bar, parity, kWaitNs) ? 0u : 1u;
+__device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, uint64_t *bar2 = nullptr,
+                                           uint32_t parity2 = 0) {
+    uint32_t bad = mbar_wait(bar, parity, kWaitNs) ? 0u : 1u;
+    if (!bad && bar2) bad = mbar_wait(bar2, parity2, kWaitNs) ? 0u : 1u;
     uint32_t any;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
@@ -320,7 +323,10 @@ __device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity) {
 }
 
 __device__ __forceinline__ void prep_sync() { group_sync<1, NP>(); }
-__device__ __forceinline__ bool prep_wait(uint64_t *bar, uint32_t parity) { return group_wait<1, NP>(bar, parity); }
+__device__ __forceinline__ bool prep_wait(uint64_t *bar, uint32_t parity, uint64_t *bar2 = nullptr,
+                                          uint32_t parity2 = 0) {
+    return group_wait<1, NP>(bar, parity, bar2, parity2);
+}
 __device__ __forceinline__ bool state_wait(uint64_t *bar, uint32_t parity) { return group_wait<2, NS>(bar, parity); }
 __device__ __forceinline__ void state_sync() { group_sync<2, NS>(); }
 
@@ -1255,8 +1261,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int len = (int)min((long long)C, eos - row0);
 
             // ---- 2. decay-scaled operands (once MMA1 of the previous chunk has read [K+ ; Q+]) --
-            if (!(ok = prep_wait(&bars[BAR_QK], par))) break;
-            if (c > 0 && !(ok = prep_wait(&bars[BAR_KQFREE], par ^ 1u))) break;
+            if (!(ok = prep_wait(&bars[BAR_QK], par, c > 0 ? &bars[BAR_KQFREE] : nullptr, par ^ 1u))) break;
             if (mh)
                 build_operands<1, NORM>(sm, gm, cst, tr0, j, len, SM_KH + 16384u * par, nrmb + 128 * (c % 3));
             else
