@@ -30,8 +30,9 @@
 //   state warps 8..11  thread = TMEM lane = value column: the bf16 state copy fused with the
 //                      decay S <- S Diag(gam_last), A and P out of TMEM and the 16 x 16 diagonal
 //                      blocks of the inverse, -(K+ S)^T and U^T as bf16 A operands in TMEM, and O
-//                      of chunk c - 1 out (staged in shared memory, one TMA tensor store) while the
-//                      prep warps merge the inverse of chunk c.
+//                      of chunk c - 1 out while the prep warps merge the inverse of chunk c (read
+//                      from TMEM in the MMA-fragment layout, stored transposed by stmatrix into the
+//                      TMA tile layout in shared memory, one TMA tensor store per 64 channels).
 //   issuer warp 12     the whole warp walks the chunks and one elected lane issues every MMA and
 //                      TMA copy, in the order the work becomes ready; mbarriers carry each
 //                      hand-off between the three groups.
