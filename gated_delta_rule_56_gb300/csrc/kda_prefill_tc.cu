@@ -412,9 +412,9 @@ __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4]
     lds8(fo_c, cst + (MH ? CST_C1 : CST_C0) * 128 + 8 * j);
     lds8(pe, cst + (MH ? CST_EG31 : CST_EM0) * 128 + 8 * j);
     lds8(khe, cst + (MH ? CST_E63M1 : CST_E63G31) * 128 + 8 * j);
-    // One row per iteration (the loop is kept rolled: the unrolled body is large, and the fetch of
-    // its instructions cost more than the loop).
-#pragma unroll 1
+    // Two rows per iteration (fully unrolled, the body's instructions cost more to fetch than the
+    // loop saves; one row per iteration pays a 4-way select of Gam per element).
+#pragma unroll 2
     for (int m = 0; m < 4; ++m) {
         const int r = r0 + m;
         const bool live = r < len;
