@@ -76,7 +76,7 @@ def parse(argv=None):
                          "backward = all gradients of the headline shape (kda_backward); "
                          "fp32 = the small fp32 configuration B=1 T=256 H=2 d=64 (tf32 tensor-core kernel); "
                          "d64 = the headline shape with heads of 64 channels (bf16)")
-    ap.add_argument("--ncu-case", choices=("prefill", "decode", "decode256", "backward", "long", "varlen"),
+    ap.add_argument("--ncu-case", choices=("prefill", "decode", "decode256", "backward", "long", "varlen", "fp32"),
                     help="run two launches of the small profiling case (for ncu) and exit")
     args = ap.parse_args(argv)
     if args.steps < 1:
@@ -674,7 +674,8 @@ def ncu_case(kind):
     decode256: the decode workload's own step, N=256 H=32 d=128 (a 537 MB state, past L2);
     backward: B=2 T=1024 H=32 d=128 (512 CTAs); long: B=1 T=65,536 H=32 d=128, split along the
     sequence like the long-context workload (its first prefill launch is the local pass); varlen:
-    the first 8 sequences of the varlen workload's lengths, H=32."""
+    the first 8 sequences of the varlen workload's lengths, H=32; fp32: fp32 inputs, B=4 T=2048
+    H=32 d=64 (the tf32 tensor-core kernel, 128 CTAs of 32 chunks)."""
     import gated_delta_rule_56_gb300 as kda
     import kda_inputs as ki
     from gated_delta_rule_56_gb300.build import build
@@ -698,6 +699,10 @@ def ncu_case(kind):
         st = x["state"].clone()
         for t in range(2):
             o = kda.decode_step(*(x[n][t] for n in NAMES), st)
+    elif kind == "fp32":
+        x = ki.prefill_inputs(4, 2048, 32, 64, 64, dtype=torch.float32, device=dev, seed=0)
+        for _ in range(2):
+            o, _s = kda.prefill(*(x[n] for n in NAMES))
     elif kind == "backward":
         x = ki.prefill_inputs(2, 1024, 32, 128, 128, device=dev, seed=0)
         do = ki.gate_logits_like(x["v"], seed=4)

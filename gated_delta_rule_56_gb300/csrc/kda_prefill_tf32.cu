@@ -55,11 +55,12 @@ constexpr uint32_t SM_KHT = SM_KQ + 32768;        // Khat^T: row = key channel, 
 constexpr uint32_t SM_VT = SM_KHT + 16384;        // V^T: row = value column (rows 64..127 zero), K = token
 constexpr uint32_t SM_T = SM_VT + 32768;          // T: row r, K = s
 constexpr uint32_t SM_P = SM_T + 16384;           // P: row r, K = s
-constexpr uint32_t SM_GAM = SM_P + 16384;         // Gam, fp32 [64 rows][64 channels]
+constexpr uint32_t SG = 68;                       // row stride (floats) of Gam: bank-free for the build's lanes
+constexpr uint32_t SM_GAM = SM_P + 16384;         // Gam, fp32 [64 rows][SG]
 constexpr uint32_t SA = 68;                       // row stride (floats) of A and X
 constexpr uint32_t SM_AS = SM_APA;                //   A (fp32 [64][SA], beta-scaled rows) once the A/P MMAs are done
 constexpr uint32_t SM_X = SM_APA + 64 * SA * 4;   //   X = (I + A)^{-1}, the same time
-constexpr uint32_t SM_CST = SM_GAM + 16384;       // per-channel factors [CST_N][64]
+constexpr uint32_t SM_CST = SM_GAM + 64 * SG * 4;  // per-channel factors [CST_N][64]
 constexpr uint32_t SM_WS = SM_CST + 2048;         // block sums of g [4][64]
 constexpr uint32_t SM_BETA = SM_WS + 1024;        // beta [64]
 constexpr uint32_t SM_BAR = SM_BETA + 256;        // mbarrier
@@ -258,11 +259,11 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tf32_kernel(const RunParams
             float add = 0.f;
             for (int gq = 0; gq < grp; ++gq) add += wsum[gq * 64 + ch];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) gam[(16 * grp + i) * 64 + ch] = loc[i] + add;
+            for (int i = 0; i < 16; ++i) gam[(16 * grp + i) * SG + ch] = loc[i] + add;
             __syncthreads();
             if (tid < 64) {
-                const float G15 = gam[15 * 64 + tid], G31 = gam[31 * 64 + tid];
-                const float G47 = gam[47 * 64 + tid], G63 = gam[63 * 64 + tid];
+                const float G15 = gam[15 * SG + tid], G31 = gam[31 * SG + tid];
+                const float G47 = gam[47 * SG + tid], G63 = gam[63 * SG + tid];
                 cst[CST_M0 * 64 + tid] = G15 * kLog2e;
                 cst[CST_M1 * 64 + tid] = G47 * kLog2e;
                 cst[CST_C0 * 64 + tid] = ex2f((G31 - G15) * kLog2e);  // exp(Gam_31 - Gam_15)
@@ -273,29 +274,21 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tf32_kernel(const RunParams
             __syncthreads();
         }
 
-        // ---- 2. decay-scaled operands (thread = row r, 16 channels) ------------------------------
+        // ---- 2. decay-scaled operands. Warp w owns rows 8w..8w+7: lane = row 8w + lane / 4 and
+        // channels lane % 4 + 4i, so that the lanes of one store cover one 128-byte line of the
+        // K-major core-matrix layout (and the rows' Gam entries fall in distinct banks).
         {
-            const int r = tid >> 2, c0 = 16 * (tid & 3);
-            const bool live = r < len && c0 < d;  // d is 32 or 64: a thread's 16 channels are all in or all out
+            const int r = 8 * warp + (lane >> 2), cq = lane & 3;
+            const bool rlive = r < len;
             const int mh = r >> 5;
-            float kr[16], qr[16], vr[16];
-            {
-                const size_t e = (size_t)(r0 + r) * rs + (size_t)h * d + c0;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 a = live ? *reinterpret_cast<const float4 *>(kg + e + 4 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float4 b = live ? *reinterpret_cast<const float4 *>(qg + e + 4 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float4 w = live ? *reinterpret_cast<const float4 *>(vg + e + 4 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    kr[4 * u] = a.x; kr[4 * u + 1] = a.y; kr[4 * u + 2] = a.z; kr[4 * u + 3] = a.w;
-                    qr[4 * u] = b.x; qr[4 * u + 1] = b.y; qr[4 * u + 2] = b.z; qr[4 * u + 3] = b.w;
-                    vr[4 * u] = w.x; vr[4 * u + 1] = w.y; vr[4 * u + 2] = w.z; vr[4 * u + 3] = w.w;
-                }
-            }
-#pragma unroll
+            const size_t e = (size_t)(r0 + r) * rs + (size_t)h * d;
+#pragma unroll 4
             for (int i = 0; i < 16; ++i) {
-                const int ch = c0 + i;
-                const float kv = kr[i], qv = qr[i], vv = vr[i];
-                const float G = gam[r * 64 + ch] * kLog2e;
+                const int ch = 4 * i + cq;
+                const bool live = rlive && ch < d;  // d is 32 or 64
+                const float kv = live ? kg[e + ch] : 0.f, qv = live ? qg[e + ch] : 0.f;
+                const float vv = live ? vg[e + ch] : 0.f;
+                const float G = gam[r * SG + ch] * kLog2e;
                 // |Gam_r - ref| <= 80 for g in [-5, 0]; the clamps only keep factors finite
                 const float ef = fminf(fmaxf(G - cst[(mh ? CST_M1 : CST_M0) * 64 + ch], -126.f), 126.f);
                 const float f = ex2f(ef), fi = ex2f(-ef);
@@ -341,21 +334,29 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tf32_kernel(const RunParams
             const int j0 = (warp & 1) ? 32 : 0;  // the diagonal half of row i
             tmem_ld32(tmem + tq + TM_AP + j0, vals);
             tmem_ld_wait();
+            // 16-byte stores: a lane writes 4 consecutive entries of its row (A rows 272 bytes apart,
+            // P rows in the core-matrix layout), 4 wavefronts per warp store.
             if (L < 64) {  // A row i (strictly lower, beta-scaled); the non-causal half is dropped by selection
                 const float b = sbeta[i];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) As[i * SA + j0 + k] = (j0 + k < i) ? vals[k] * b : 0.f;
-                if (j0 == 32)
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4 *>(As + i * SA + j0 + k) =
+                        make_float4((j0 + k < i) ? vals[k] * b : 0.f, (j0 + k + 1 < i) ? vals[k + 1] * b : 0.f,
+                                    (j0 + k + 2 < i) ? vals[k + 2] * b : 0.f, (j0 + k + 3 < i) ? vals[k + 3] * b : 0.f);
+                // rows 32..63, columns 0..31 come from the off tile below; rows 0..31, columns 32..63 are zero
+                const int z0 = j0 == 32 ? 0 : 32;
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) As[i * SA + k] = 0.f;  // rows 32..63, columns 0..31: off tile below
-                else
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) As[i * SA + 32 + k] = 0.f;
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4 *>(As + i * SA + z0 + k) = make_float4(0.f, 0.f, 0.f, 0.f);
             } else {       // P row i (lower)
 #pragma unroll
-                for (int k = 0; k < 32; ++k) st_op(sm, SM_P, i, j0 + k, (j0 + k <= i) ? vals[k] : 0.f);
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4 *>(sm + SM_P + tk_off(i, j0 + k)) =
+                        make_float4(tf32r((j0 + k <= i) ? vals[k] : 0.f), tf32r((j0 + k + 1 <= i) ? vals[k + 1] : 0.f),
+                                    tf32r((j0 + k + 2 <= i) ? vals[k + 2] : 0.f), tf32r((j0 + k + 3 <= i) ? vals[k + 3] : 0.f));
 #pragma unroll
-                for (int k = 0; k < 32; ++k) st_op(sm, SM_P, i, (32 - j0) + k, 0.f);
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4 *>(sm + SM_P + tk_off(i, (32 - j0) + k)) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
         __syncthreads();  // the off tile overwrites part of the zeros above
@@ -368,10 +369,14 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tf32_kernel(const RunParams
                 if (warp < 2) {
                     const float b = sbeta[i];
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) As[i * SA + k] = vals[k] * b;
+                    for (int k = 0; k < 32; k += 4)
+                        *reinterpret_cast<float4 *>(As + i * SA + k) =
+                            make_float4(vals[k] * b, vals[k + 1] * b, vals[k + 2] * b, vals[k + 3] * b);
                 } else {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) st_op(sm, SM_P, i, k, vals[k]);
+                    for (int k = 0; k < 32; k += 4)
+                        *reinterpret_cast<float4 *>(sm + SM_P + tk_off(i, k)) =
+                            make_float4(tf32r(vals[k]), tf32r(vals[k + 1]), tf32r(vals[k + 2]), tf32r(vals[k + 3]));
                 }
             }
         }
@@ -433,9 +438,15 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tf32_kernel(const RunParams
                 Xs[(32 + r) * SA + cc] = -acc;
             }
             __syncthreads();
-            for (int e = tid; e < 64 * 64; e += NT) {
-                const int i = e >> 6, jc = e & 63;
-                st_op(sm, SM_T, i, jc, Xs[i * SA + jc] * sbeta[jc]);
+            // T = X Diag(beta), 16 bytes per lane: rows 8 w + lane % 8 (one 128-byte line of the
+            // core-matrix layout per 8 lanes), columns 16 q + 4 (lane / 8) .. + 3.
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int i = 8 * warp + (lane & 7), jc = 16 * q + 4 * (lane >> 3);
+                const float4 x = *reinterpret_cast<const float4 *>(Xs + i * SA + jc);
+                const float4 b = *reinterpret_cast<const float4 *>(sbeta + jc);
+                *reinterpret_cast<float4 *>(sm + SM_T + tk_off(i, jc)) =
+                    make_float4(tf32r(x.x * b.x), tf32r(x.y * b.y), tf32r(x.z * b.z), tf32r(x.w * b.w));
             }
         }
         fence_async_smem();
