@@ -237,6 +237,15 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tf32_kernel(const RunParams
     for (int c = 0; c < nchunks && ok; ++c) {
         const long long r0 = bos + (long long)c * C;
         const int len = (int)min((long long)C, eos - r0);
+        if (c + 1 < nchunks) {  // the next chunk's rows of q, k, v and g into L2 (thread = row, tensor)
+            const long long rr = r0 + C + (tid & 63);
+            if (rr < eos) {
+                const int pt = tid >> 6;
+                const float *a = (pt == 0 ? qg : pt == 1 ? kg : pt == 2 ? vg : gg) + (size_t)rr * rs + (size_t)h * d;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+                if (d > 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(a + 32));
+            }
+        }
 
         // ---- 1. Gam = cumsum of g per channel; beta -----------------------------------------
         {
@@ -282,12 +291,19 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tf32_kernel(const RunParams
             const bool rlive = r < len;
             const int mh = r >> 5;
             const size_t e = (size_t)(r0 + r) * rs + (size_t)h * d;
-#pragma unroll 4
+            float kr[16], qr[16], vr[16];  // all of the thread's loads in flight at once
+#pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int ch = 4 * i + cq;
                 const bool live = rlive && ch < d;  // d is 32 or 64
-                const float kv = live ? kg[e + ch] : 0.f, qv = live ? qg[e + ch] : 0.f;
-                const float vv = live ? vg[e + ch] : 0.f;
+                kr[i] = live ? kg[e + ch] : 0.f;
+                qr[i] = live ? qg[e + ch] : 0.f;
+                vr[i] = live ? vg[e + ch] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int ch = 4 * i + cq;
+                const float kv = kr[i], qv = qr[i], vv = vr[i];
                 const float G = gam[r * SG + ch] * kLog2e;
                 // |Gam_r - ref| <= 80 for g in [-5, 0]; the clamps only keep factors finite
                 const float ef = fminf(fmaxf(G - cst[(mh ? CST_M1 : CST_M0) * 64 + ch], -126.f), 126.f);
@@ -390,52 +406,63 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tf32_kernel(const RunParams
             float *Ys = gam;
             for (int e = tid; e < 64 * 64; e += NT) Xs[(e >> 6) * SA + (e & 63)] = 0.f;
             __syncthreads();
-            if (tid < 64) {
+            if (tid < 64) {  // column jj of diagonal block B0, held in registers (entries above jj are 0)
                 const int B0 = 16 * (tid >> 4), jj = tid & 15;
-#pragma unroll 1
-                for (int i = jj; i < 16; ++i) {
-                    float acc = 0.f;
-                    for (int k = jj; k < i; ++k) acc = fmaf(As[(B0 + i) * SA + B0 + k], Xs[(B0 + k) * SA + B0 + jj], acc);
-                    Xs[(B0 + i) * SA + B0 + jj] = (i == jj) ? 1.f : -acc;
+                float x[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float acc = 0.f;  // the terms k < jj are A x 0 and leave acc at +0
+#pragma unroll
+                    for (int k = 0; k < i; ++k) acc = fmaf(As[(B0 + i) * SA + B0 + k], x[k], acc);
+                    x[i] = i < jj ? 0.f : (i == jj ? 1.f : -acc);
                 }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) Xs[(B0 + i) * SA + B0 + jj] = x[i];
             }
             __syncthreads();
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {  // 16 -> 32, blocks (1, 0) and (3, 2): Y = A_IJ X_JJ
-                const int e = tid + NT * q2, pp = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            // Each thread: one row x 4 consecutive columns of a product (one left entry and one
+            // 16-byte right vector per K step), every entry summed in K order.
+            auto fma4 = [](float (&acc)[4], float a, float4 x) {
+                acc[0] = fmaf(a, x.x, acc[0]); acc[1] = fmaf(a, x.y, acc[1]);
+                acc[2] = fmaf(a, x.z, acc[2]); acc[3] = fmaf(a, x.w, acc[3]);
+            };
+            if (tid < 128) {  // 16 -> 32, blocks (1, 0) and (3, 2): Y = A_IJ X_JJ
+                const int pp = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
                 const int I = 2 * pp + 1, J = 2 * pp;
-                float acc = 0.f;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int k = 0; k < 16; ++k) acc = fmaf(As[(16 * I + r) * SA + 16 * J + k], Xs[(16 * J + k) * SA + 16 * J + cc], acc);
-                Ys[e] = acc;
+                for (int k = 0; k < 16; ++k)
+                    fma4(acc, As[(16 * I + r) * SA + 16 * J + k],
+                         *reinterpret_cast<const float4 *>(Xs + (16 * J + k) * SA + 16 * J + c4));
+                *reinterpret_cast<float4 *>(Ys + pp * 256 + r * 16 + c4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
             }
             __syncthreads();
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {  // X_IJ = -X_II Y
-                const int e = tid + NT * q2, pp = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            if (tid < 128) {  // X_IJ = -X_II Y
+                const int pp = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
                 const int I = 2 * pp + 1, J = 2 * pp;
-                float acc = 0.f;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int k = 0; k < 16; ++k) acc = fmaf(Xs[(16 * I + r) * SA + 16 * I + k], Ys[pp * 256 + k * 16 + cc], acc);
-                Xs[(16 * I + r) * SA + 16 * J + cc] = -acc;
+                for (int k = 0; k < 16; ++k)
+                    fma4(acc, Xs[(16 * I + r) * SA + 16 * I + k], *reinterpret_cast<const float4 *>(Ys + pp * 256 + k * 16 + c4));
+                *reinterpret_cast<float4 *>(Xs + (16 * I + r) * SA + 16 * J + c4) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
             }
             __syncthreads();
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {  // 32 -> 64: Y = A_BA X_AA
-                const int e = tid + NT * q4, r = e >> 5, cc = e & 31;
-                float acc = 0.f;
+            {  // 32 -> 64: Y = A_BA X_AA
+                const int r = tid >> 3, c4 = 4 * (tid & 7);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-                for (int k = 0; k < 32; ++k) acc = fmaf(As[(32 + r) * SA + k], Xs[k * SA + cc], acc);
-                Ys[e] = acc;
+                for (int k = 0; k < 32; ++k)
+                    fma4(acc, As[(32 + r) * SA + k], *reinterpret_cast<const float4 *>(Xs + k * SA + c4));
+                *reinterpret_cast<float4 *>(Ys + r * 32 + c4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
             }
             __syncthreads();
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {  // X_BA = -X_BB Y
-                const int e = tid + NT * q4, r = e >> 5, cc = e & 31;
-                float acc = 0.f;
+            {  // X_BA = -X_BB Y
+                const int r = tid >> 3, c4 = 4 * (tid & 7);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-                for (int k = 0; k < 32; ++k) acc = fmaf(Xs[(32 + r) * SA + 32 + k], Ys[k * 32 + cc], acc);
-                Xs[(32 + r) * SA + cc] = -acc;
+                for (int k = 0; k < 32; ++k)
+                    fma4(acc, Xs[(32 + r) * SA + 32 + k], *reinterpret_cast<const float4 *>(Ys + k * 32 + c4));
+                *reinterpret_cast<float4 *>(Xs + (32 + r) * SA + c4) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
             }
             __syncthreads();
             // T = X Diag(beta), 16 bytes per lane: rows 8 w + lane % 8 (one 128-byte line of the
@@ -525,19 +552,26 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tf32_kernel(const RunParams
         }
         if (!(ok = mma_done())) break;
 
-        // ---- 11. O out (lane v < d: value column v, 64 tokens) -----------------------------------
-        if (warp < 2) {
-            const int v = 32 * warp + lane;
+        // ---- 11. O out: O^T (lane = value column) into a [token][value] staging tile in the A/P
+        // operand region (free until the next chunk's build), then every thread stores rows of it.
+        {
+            float *Ost = reinterpret_cast<float *>(sm + SM_APA);  // [64 tokens][SA]
+            if (warp < 2) {
+                const int v = 32 * warp + lane;
 #pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-                float x[32];
-                tmem_ld32(tmem + tq + TM_O + 32 * cb, x);
-                tmem_ld_wait();
-                if (v < d)
+                for (int cb = 0; cb < 2; ++cb) {
+                    float x[32];
+                    tmem_ld32(tmem + tq + TM_O + 32 * cb, x);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (32 * cb + i < len) og[(size_t)(r0 + 32 * cb + i) * rs + (size_t)h * d + v] = x[i];
+                    for (int i = 0; i < 32; ++i) Ost[(32 * cb + i) * SA + v] = x[i];
+                }
             }
+            __syncthreads();
+            const int v = tid & 63;
+#pragma unroll 4
+            for (int t = tid >> 6; t < 64; t += 4)
+                if (t < len && v < d) og[(size_t)(r0 + t) * rs + (size_t)h * d + v] = Ost[t * SA + v];
         }
         tc_fence_before();
         __syncthreads();  // the next chunk's operands overwrite what these MMAs read
