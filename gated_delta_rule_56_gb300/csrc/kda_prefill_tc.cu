@@ -1253,7 +1253,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 cst[CST_E63G31 * 128 + ch] = ex2((G63 - G31) * kLog2e);
                 gcs[128 * (cc % 3) + ch] = ex2(G63 * kLog2e);
             }
-            prep_sync();
+            // No group barrier here: every prep thread arrives after its own writes, so the phase
+            // completes only when all of them are visible; the operand build of chunk cc reads
+            // the factors after the group barriers of the waits and merges in between.
             mbar_arrive(&bars[(cc & 1) ? BAR_S1D1 : BAR_S1D0]);  // gam_last and beta of chunk cc are in place
             return true;
         };
