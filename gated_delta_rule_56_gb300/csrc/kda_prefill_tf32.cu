@@ -20,8 +20,10 @@
 // plain fp32 forward substitution. Everything else is fp32 on the CUDA cores.
 //
 // Layout of the work: one CTA of 256 threads per (sequence, head), chunks in order, the steps of a
-// chunk one after another between block barriers (no overlap between chunks: the path is meant
-// for the small fp32 configurations, where a chunk's latency, not throughput, is what counts).
+// chunk one after another between block barriers (the path is meant for the small fp32
+// configurations, where a chunk's latency, not throughput, is what counts); the only overlap
+// between chunks is step 1 of the next chunk (Gam, its factors, beta), which runs while MMA1 of the
+// current one is in flight.
 // Heads of 32 channels run with the missing channels zero (zero key and query channels add
 // nothing; the padded state rows and columns stay zero and are not stored). The state lives in
 // TMEM lanes 0..63 (value columns); lanes 64..127 hold zeros so that the M = 128 MMAs stay in
