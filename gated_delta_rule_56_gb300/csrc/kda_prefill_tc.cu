@@ -122,7 +122,7 @@ static_assert(SM_KH % 1024 == 0 && SM_KQ % 1024 == 0 && SM_AP % 1024 == 0 && SM_
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // Per-channel factor rows in SM_CST.
-enum { CST_M0 = 0, CST_M1, CST_C0, CST_C1, CST_EM0, CST_EG31, CST_E63M1, CST_E63G31, CST_N };
+enum { CST_C0 = 0, CST_C1, CST_EM0, CST_EG31, CST_E63M1, CST_E63G31, CST_N };
 static_assert(CST_N * 512 <= 4096, "factor rows overflow SM_CST");
 
 // TMEM column offsets.
@@ -165,17 +165,6 @@ __device__ __forceinline__ void mul2(float &a, float &b, float x, float y) {
         : "=l"(r)
         : "l"(((uint64_t)__float_as_uint(b) << 32) | __float_as_uint(a)),
           "l"(((uint64_t)__float_as_uint(y) << 32) | __float_as_uint(x)));
-    a = __uint_as_float((uint32_t)r);
-    b = __uint_as_float((uint32_t)(r >> 32));
-}
-// Two fused multiply-adds in one instruction: a = a * x + u, b = b * y + v (each rounded once).
-__device__ __forceinline__ void fma2(float &a, float &b, float x, float y, float u, float v) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;"
-        : "=l"(r)
-        : "l"(((uint64_t)__float_as_uint(b) << 32) | __float_as_uint(a)),
-          "l"(((uint64_t)__float_as_uint(y) << 32) | __float_as_uint(x)),
-          "l"(((uint64_t)__float_as_uint(v) << 32) | __float_as_uint(u)));
     a = __uint_as_float((uint32_t)r);
     b = __uint_as_float((uint32_t)(r >> 32));
 }
@@ -332,7 +321,9 @@ __device__ __forceinline__ bool state_wait(uint64_t *bar, uint32_t parity) { ret
 __device__ __forceinline__ void state_sync() { group_sync<2, NS>(); }
 
 // Decay-scaled bf16 operands of one row half (MH = 0: rows 0..31, MH = 1: rows 32..63) for a
-// thread's 4 rows r0..r0+3 x 8 channels 8j..8j+7; gm holds Gam of those entries. With the L2
+// thread's 4 rows r0..r0+3 x 8 channels 8j..8j+7; gm holds Gam_r - Gam_ref of those entries
+// (ref = row 15 for MH = 0, row 47 for MH = 1; summed within the 16-row blocks, so no large
+// cumulative values cancel). With the L2
 // normalisation (NORM) the operands of the A/P tiles are built from the raw q/k rows, which are
 // exact bf16 values, and the A/P read-out applies the inverse norms to the fp32 products: a
 // normalised row rounded to bf16 before the product would put an absolute error of about
@@ -407,8 +398,7 @@ __device__ __forceinline__ float row_inv_norm(const float *nrm, int kq, int r) {
 template <int MH, bool NORM, int ROWS>
 __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4][8], const float *cst, int r0,
                                                int j, int len, uint32_t khb, const float *nrm) {
-    float ref[8], fo_c[8], pe[8], khe[8];
-    lds8(ref, cst + (MH ? CST_M1 : CST_M0) * 128 + 8 * j);  // the reference Gam, times log2(e)
+    float fo_c[8], pe[8], khe[8];
     lds8(fo_c, cst + (MH ? CST_C1 : CST_C0) * 128 + 8 * j);
     lds8(pe, cst + (MH ? CST_EG31 : CST_EM0) * 128 + 8 * j);
     lds8(khe, cst + (MH ? CST_E63M1 : CST_E63G31) * 128 + 8 * j);
@@ -434,8 +424,8 @@ __device__ __forceinline__ void build_operands(uint8_t *sm, const float (&gm)[4]
             const float q0 = bf_lo(qq[i >> 1]), q1 = bf_hi(qq[i >> 1]);
             // |Gam_r - ref| <= 80 for g in [-5, 0]; the clamp only keeps factors finite (no 0 * inf)
             // for gates outside that range.
-            float e0 = gr[i], e1 = gr[i + 1];
-            fma2(e0, e1, kLog2e, kLog2e, -ref[i], -ref[i + 1]);
+            float e0 = gr[i], e1 = gr[i + 1];  // Gam_r - Gam_ref
+            mul2(e0, e1, kLog2e, kLog2e);
             e0 = fminf(fmaxf(e0, -126.f), 126.f);
             e1 = fminf(fmaxf(e1, -126.f), 126.f);
             const float f0 = ex2(e0), f1 = ex2(e1), fi0 = ex2(-e0), fi1 = ex2(-e1);
@@ -1138,7 +1128,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int rb = warp & 3;  // 16-row block
         const int tr0 = 16 * rb + 4 * rq;
         const int mh = rb >> 1;
-        float gm[4][8];  // Gam of the thread's 4 rows x 8 channels (current chunk)
+        float gm[4][8];  // Gam_r - Gam_ref of the thread's 4 rows x 8 channels (current chunk; ref = row 15 or 47)
         int g_inflight = -1;  // chunk of a g-tile copy issued here and not yet waited for
         // beta of token tid of a chunk, loaded one step ahead (raw bf16 bits, converted when used)
         auto load_beta = [&](int cc) -> uint32_t {
@@ -1204,6 +1194,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     *reinterpret_cast<float4 *>(wts + 128 * rb + 8 * j) = make_float4(incl[0], incl[1], incl[2], incl[3]);
                     *reinterpret_cast<float4 *>(wts + 128 * rb + 8 * j + 4) = make_float4(incl[4], incl[5], incl[6], incl[7]);
                 }
+                // gm now holds Gam relative to the start of the thread's 16-row block. The operand
+                // build needs Gam_r - Gam_ref with the reference row at the end of block 0 or 2
+                // (rows 15, 47): for blocks 1 and 3 that is the block-relative value itself, for
+                // blocks 0 and 2 the block-relative value minus the block's total (held by the
+                // lanes of row group 3).
+                if ((rb & 1) == 0) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float tot = __shfl_sync(0xffffffffu, incl[i], (lane & 7) | 24);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) gm[m][i] -= tot;
+                    }
+                }
             }
             if (tid < C) sbeta[64 * (cc & 1) + tid] = bet;
             if (NORM) add_row_square_sums(nrmb + 128 * (cc % 3), qk, tr0, lane);
@@ -1215,25 +1218,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tma_load_3d(sm + SM_G + 8192, &maps.g, &bars[BAR_G], 64, h, r);
                 g_inflight = cc + 1;
             }
-#pragma unroll
-            for (int pb = 0; pb < 3; ++pb) {  // add the sums of the earlier 16-row blocks
-                if (pb < rb) {
-                    const float4 a0 = *reinterpret_cast<const float4 *>(wts + 128 * pb + 8 * j);
-                    const float4 a1 = *reinterpret_cast<const float4 *>(wts + 128 * pb + 8 * j + 4);
-                    const float add[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) gm[m][i] += add[i];
-                    }
-                }
-            }
             if (DUMP && blockIdx.x == 0 && cc < p.dump_chunks) {  // Gam, [token][d_k]
 #pragma unroll
                 for (int m = 0; m < 4; ++m)
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        p.dump[(size_t)cc * kDumpFloatsPerChunk + kDumpGam + (tr0 + m) * D + 8 * j + i] = gm[m][i];
+                        p.dump[(size_t)cc * kDumpFloatsPerChunk + kDumpGam + (tr0 + m) * D + 8 * j + i] =
+                            gm[m][i] + (mh ? wts[8 * j + i] + wts[128 + 8 * j + i] + wts[256 + 8 * j + i] : wts[8 * j + i]);
             }
             if (NORM && tid < 128) {  // the row sums of squares are complete: inverse norms in place
                 float *nb = nrmb + 128 * (cc % 3) + tid;
@@ -1243,8 +1234,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int ch = tid;
                 const float G15 = wts[ch], G31 = G15 + wts[128 + ch];
                 const float G47 = G31 + wts[256 + ch], G63 = G47 + wts[384 + ch];
-                cst[CST_M0 * 128 + ch] = G15 * kLog2e;
-                cst[CST_M1 * 128 + ch] = G47 * kLog2e;
                 cst[CST_C0 * 128 + ch] = ex2((G31 - G15) * kLog2e);
                 cst[CST_C1 * 128 + ch] = ex2((G47 - G31) * kLog2e);
                 cst[CST_EM0 * 128 + ch] = ex2(G15 * kLog2e);
