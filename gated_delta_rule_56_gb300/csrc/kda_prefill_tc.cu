@@ -115,7 +115,8 @@ constexpr uint32_t SM_NRM = SM_TPTR + 16;                 // fp32 [3 chunks][k, 
 constexpr uint32_t SM_USED = SM_NRM + 1536;
 constexpr uint32_t SMEM_BYTES = SM_USED + 1024;           // + alignment slack
 static_assert(SM_X + 64 * SA * 4 <= SM_OFF, "solve buffers overflow their region");
-static_assert(SM_Y + 4352 + 32 * SA * 4 <= SM_VT, "solve scratch overflows its region");
+constexpr uint32_t SM_YC = SM_Y + 4352 + 32 * SA * 4;  //   and the 32 -> 64 merge's product A_BA X_AA
+static_assert(SM_YC + 32 * SA * 4 <= SM_VT, "solve scratch overflows its region");
 static_assert(SM_KH % 1024 == 0 && SM_KQ % 1024 == 0 && SM_AP % 1024 == 0 && SM_APB % 1024 == 0 &&
                   SM_OFF % 1024 == 0 && SM_OFFB % 1024 == 0 && SM_VT % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
@@ -250,11 +251,11 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
 // strides `ls` and `rs` (floats), tf32 inputs and fp32 accumulation (mma.sync m16n8k8).
 // acc layout: acc[0] = (g, 2t), acc[1] = (g, 2t+1), acc[2] = (g+8, 2t), acc[3] = (g+8, 2t+1)
 // with g = lane / 4, t = lane % 4.
-template <int K>
+template <int K, bool INIT = true>
 __device__ __forceinline__ void warp_mma_16x8(float (&acc)[4], const float *L, int ls, const float *R, int rs,
                                               int lane) {
     const int g = lane >> 2, t = lane & 3;
-    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    if (INIT) acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
 #pragma unroll
     for (int k0 = 0; k0 < K; k0 += 8) {
         const uint32_t a0 = to_tf32(L[g * ls + k0 + t]), a1 = to_tf32(L[(g + 8) * ls + k0 + t]);
@@ -604,14 +605,9 @@ __device__ __forceinline__ void solve_diag_block(uint8_t *sm, const float *As, f
     }
 }
 
-// Zero fills of the inverse (thread z of 128): the two upper X blocks the 32 -> 64 merge reads
-// (rows 0..15 x cols 16..31, rows 32..47 x cols 48..63) and the six strictly-upper 16 x 16 blocks
-// of T.
-__device__ __forceinline__ void solve_zero_fill(uint8_t *sm, float *Xs, int z) {
-    // X rows 0..15 cols 16..31 and rows 32..47 cols 48..63 (read by the 32 -> 64 merge)
-    const int blk = z >> 6, rr = (z & 63) >> 2, cq = (z & 3) * 4;
-    *reinterpret_cast<float4 *>(Xs + (32 * blk + rr) * SA + 32 * blk + 16 + cq) =
-        make_float4(0.f, 0.f, 0.f, 0.f);
+// Zero fills of the inverse (thread z of 128): the six strictly-upper 16 x 16 blocks of T. (The
+// merges never read the upper blocks of X: they skip the K steps those blocks would contribute.)
+__device__ __forceinline__ void solve_zero_fill(uint8_t *sm, int z) {
     // T: the six strictly-upper 16 x 16 blocks (192 chunks of 16 bytes)
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
@@ -1041,7 +1037,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         p.dump[(size_t)c * kDumpFloatsPerChunk + kDumpA + e] = s2 < r ? As[r * SA + s2] : 0.f;
                     }
                 solve_diag_block(sm, As, Xs, warp & 3, lane, sbc);
-                solve_zero_fill(sm, Xs, v);
+                solve_zero_fill(sm, v);
             }
             fence_async_smem();  // T and P are read by MMAs
             mbar_arrive(&bars[BAR_EPIDONE]);
@@ -1273,7 +1269,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // The state warps have read A and P out of TMEM and inverted the 16 x 16 diagonal
             // blocks (with the zero fills); the block merges run here.
             if (!(ok = prep_wait(&bars[BAR_EPIDONE], par))) break;
-            // (b) 16 -> 32: warp (p, nt) < 4 computes column tile nt of X_{2p+1,2p} (tf32 mma)
+            // (b) 16 -> 32: warp (p, nt) < 4 computes column tile nt of X_{2p+1,2p} (tf32 mma).
+            // Meanwhile warps 4..7 start (c)'s first product Y = A_BA X_AA with what the 16 x 16
+            // blocks already give: its columns 16..31 whole (X_AA is zero above X_11 there) and the
+            // first half (X_00) of its columns 0..15, finished with X_10 once (b) is done.
+            float *Yc = reinterpret_cast<float *>(sm + SM_YC);
+            float accp[4];
+            const int w4 = warp - 4, cmt = w4 >> 1, cnt = w4 & 1;  // (c) tiles of warps 4..7
             if (warp < 4) {
                 const int pp = warp >> 1, nt = warp & 1;
                 const int I = 2 * pp + 1, J = 2 * pp;
@@ -1285,17 +1287,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 warp_mma_16x8<16>(acc, Xs + 16 * I * SA + 16 * I, SA, Yb + 8 * nt, SA, lane);
                 warp_store_16x8(Xs + 16 * I * SA + 16 * J + 8 * nt, SA, acc, -1.f, lane);
                 store_t_16x8(sm + SM_T, 16 * I, 16 * J + 8 * nt, acc, sbc, lane);
+            } else {
+                float acc[4];
+                const float *Ab = As + (32 + 16 * cmt) * SA;
+                warp_mma_16x8<16>(acc, Ab + 16, SA, Xs + 16 * SA + 8 * (2 + cnt), SA, lane);
+                warp_store_16x8(Yc + 16 * cmt * SA + 8 * (2 + cnt), SA, acc, 1.f, lane);
+                warp_mma_16x8<16>(accp, Ab, SA, Xs + 8 * cnt, SA, lane);
             }
             prep_sync();
-            // (c) 32 -> 64: X_BA = -X_BB A_BA X_AA with 32 x 32 blocks; warp w owns one 16 x 8 tile.
+            if (warp >= 4) {  // the rest of (c)'s columns 0..15: + A_BA[:, 16..31] X_10
+                warp_mma_16x8<16, false>(accp, As + (32 + 16 * cmt) * SA + 16, SA, Xs + 16 * SA + 8 * cnt, SA, lane);
+                warp_store_16x8(Yc + 16 * cmt * SA + 8 * cnt, SA, accp, 1.f, lane);
+            }
+            prep_sync();
+            // (c) 32 -> 64: X_BA = -X_BB Y with 32 x 32 blocks; warp w owns one 16 x 8 tile. X_BB is
+            // zero above X_33, so its first 16 rows take K = 16.
             {
                 const int mt = warp >> 2, nt = warp & 3;
-                float *Y = reinterpret_cast<float *>(sm + SM_Y + 4352);
                 float acc[4];
-                warp_mma_16x8<32>(acc, As + (32 + 16 * mt) * SA, SA, Xs + 8 * nt, SA, lane);
-                warp_store_16x8(Y + 16 * mt * SA + 8 * nt, SA, acc, 1.f, lane);
-                prep_sync();
-                warp_mma_16x8<32>(acc, Xs + (32 + 16 * mt) * SA + 32, SA, Y + 8 * nt, SA, lane);
+                if (mt == 0)
+                    warp_mma_16x8<16>(acc, Xs + 32 * SA + 32, SA, Yc + 8 * nt, SA, lane);
+                else
+                    warp_mma_16x8<32>(acc, Xs + 48 * SA + 32, SA, Yc + 8 * nt, SA, lane);
                 store_t_16x8(sm + SM_T, 32 + 16 * mt, 8 * nt, acc, sbc, lane);
             }
             fence_async_smem();  // the T stores
