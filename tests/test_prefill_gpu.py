@@ -248,6 +248,32 @@ def test_varlen_longest_first_order_changes_nothing():
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_more_ctas_than_sms(d):
+    """A launch with more (sequence, head) CTAs than the GPU has SMs takes the instance whose
+    operand build runs one row per loop iteration: 50 packed sequences (lengths 0..300, ragged
+    chunks, one empty) x 4 heads = 200 CTAs, initial states; every output and final state against
+    the oracle, and bit for bit against the same sequences run in two launches of fewer CTAs."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H = 4
+    lengths = ki.varlen_lengths(50, 0, 300, seed=23)
+    lengths[7] = 0
+    assert 50 * H > sms
+    x = ki.varlen_inputs(lengths, H, d, d, device=DEV, seed=24)
+    o, s = run(x)
+    ro, rs = ref(x)
+    assert_close(o, ro, "o")
+    assert_close(s, rs, "final_state")
+    # The first 25 sequences alone (100 CTAs): the two-row instance; same bits.
+    cut = int(lengths[:25].sum())
+    x1 = {n: x[n][:, :cut] for n in NAMES}
+    x1["cu_seqlens"] = x["cu_seqlens"][:26].clone()
+    x1["initial_state"] = x["initial_state"][:25]
+    assert 25 * H <= sms
+    o1, s1 = run(x1)
+    assert torch.equal(o1, o[:, :cut]) and torch.equal(s1, s[:25])
+
+
 @pytest.mark.parametrize("d", [64, 32])
 @pytest.mark.parametrize("lengths", [[200], [70, 1, 130, 0, 64, 2000]])
 def test_small_heads_bf16_tensor_core_path(d, lengths):
